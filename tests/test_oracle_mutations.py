@@ -1,0 +1,131 @@
+"""Plant plausible mistakes in the CPU reference (on the CPU, one at a time)
+and check that at least one pin catches each: the pins must be sharp enough
+that a dropped term, a wrong sign or index, or a swapped operand fails."""
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import moe_oracle as M
+from tests import test_oracle_pins as pins
+
+_orig = {n: getattr(M, n) for n in ("topk_renorm", "permutation_maps", "silu", "swiglu_expert",
+                                      "decode_e4m3", "decode_bf16", "moe_forward_grouped",
+                                      "moe_forward_per_token", "shared_expert", "router_logits")}
+
+
+def _no_renorm(logits, k):
+    idx, _ = _orig["topk_renorm"](logits, k)
+    p = M.softmax(logits)
+    return idx, np.take_along_axis(p, idx.astype(np.int64), axis=1)
+
+
+def _lowest_k(logits, k):
+    return _orig["topk_renorm"](-np.asarray(logits), k)
+
+
+def _ties_high(logits, k):
+    logits = np.asarray(logits, float)
+    E = logits.shape[1]
+    idx, w = _orig["topk_renorm"](logits[:, ::-1], k)
+    return (E - 1 - idx).astype(np.int32), w
+
+
+def _perm_descending(idx, E):
+    counts, offsets, perm_token, inv_row = _orig["permutation_maps"](idx, E)
+    pt = perm_token.copy()
+    inv = inv_row.copy()
+    for e in range(E):
+        a, b = offsets[e], offsets[e + 1]
+        pt[a:b] = perm_token[a:b][::-1]
+        for r in range(a, b):
+            t = perm_token[r]
+            j = list(idx[t]).index(e)
+            inv[t, j] = a + b - 1 - r
+    return counts, offsets, pt, inv
+
+
+def _silu_sign(z):
+    return _orig["silu"](-np.asarray(z, float))
+
+
+def _swiglu_swapped(x, wg, wu, wd):
+    return _orig["swiglu_expert"](x, wu, wg, wd)
+
+
+def _swiglu_no_gate(x, wg, wu, wd):
+    x = np.asarray(x, float)
+    return ((x @ np.asarray(wg).T) * (x @ np.asarray(wu).T)) @ np.asarray(wd).T
+
+
+def _e4m3_bias8(bits):
+    return _orig["decode_e4m3"](bits) / 2.0
+
+
+def _bf16_sub_as_normal(bits):
+    b = np.asarray(bits).astype(np.int64)
+    out = _orig["decode_bf16"](bits)
+    sub = ((b >> 7) & 0xFF) == 0
+    out = np.where(sub & ((b & 0x7F) != 0), out * 2.0, out)
+    return out
+
+
+def _router_transposed_bias(x, w, bias=None):
+    lg = _orig["router_logits"](x, w, None)
+    return lg if bias is None else lg - np.asarray(bias)[None, :]
+
+
+def _shared_dropped(x, wg, wu, wd):
+    return np.zeros((np.asarray(x).shape[0], np.asarray(wd).shape[0]))
+
+
+MUTATIONS = {
+    "no_renormalisation": ("topk_renorm", _no_renorm),
+    "lowest_k_selected": ("topk_renorm", _lowest_k),
+    "ties_to_higher_index": ("topk_renorm", _ties_high),
+    "rows_descending_token": ("permutation_maps", _perm_descending),
+    "silu_sign_flip": ("silu", _silu_sign),
+    "gate_up_swapped": ("swiglu_expert", _swiglu_swapped),
+    "activation_dropped": ("swiglu_expert", _swiglu_no_gate),
+    "e4m3_wrong_bias": ("decode_e4m3", _e4m3_bias8),
+    "bf16_subnormal_as_normal": ("decode_bf16", _bf16_sub_as_normal),
+    "router_bias_sign": ("router_logits", _router_transposed_bias),
+    "shared_expert_dropped": ("shared_expert", _shared_dropped),
+}
+
+PIN_CHECKS = [
+    pins.test_decode_bf16_fixed_values,
+    pins.test_decode_bf16_all_patterns_match_binary32_upper_half,
+    pins.test_decode_e4m3_fixed_values,
+    pins.test_decode_e4m3_all_codes_match_torch,
+    pins.test_worked_example_groups_and_rows,
+    pins.test_worked_example_router_reproduces_weights,
+    pins.test_worked_example_combine_of_T1,
+    pins.test_router_logits_match_library_linear,
+    lambda: pins.test_topk_brute_force_over_subsets(6, 3),
+    pins.test_topk_ties_go_to_lower_index,
+    pins.test_silu_closed_form_values,
+    pins.test_swiglu_expert_matches_library_ffn,
+    pins.test_single_expert_is_dense_swiglu,
+    pins.test_shared_expert_is_added_with_weight_one,
+    lambda: pins.test_permutation_invariants(37, 8, 2),
+]
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_some_pin_catches_the_mutation(name, monkeypatch):
+    attr, fn = MUTATIONS[name]
+    monkeypatch.setattr(M, attr, fn)
+    monkeypatch.setattr(oracle, attr, fn)
+    caught = []
+    for check in PIN_CHECKS:
+        try:
+            check()
+        except Exception:  # an assertion, or a shape error, both count
+            caught.append(getattr(check, "__name__", "lambda"))
+    assert caught, f"mutation {name} passed every pin"
+
+
+def test_unmutated_oracle_passes_every_check():
+    for check in PIN_CHECKS:
+        check()

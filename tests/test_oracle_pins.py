@@ -1,0 +1,337 @@
+"""Pins of the CPU reference to facts outside itself: the page's worked
+example, the storage-format definitions, closed forms, library routines,
+brute force over tiny inputs, and the invariants the page states.
+
+Run on CPU (no GPU marker).
+"""
+
+import math
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+import torch.nn.functional as F
+
+import oracle
+from oracle import moe_oracle
+from routed_expert_ffn_gemm_gb300 import inputs
+from tests import helpers
+
+
+# ---------------------------------------------------------------------------
+# storage formats
+# ---------------------------------------------------------------------------
+
+def test_decode_bf16_fixed_values():
+    cases = {0x3F80: 1.0, 0xBF80: -1.0, 0x4049: 3.140625, 0x0000: 0.0, 0x4000: 2.0,
+             0x3F00: 0.5, 0x0080: 2.0 ** -126, 0x0001: 2.0 ** -133,
+             0x7F7F: (2 - 2 ** -7) * 2.0 ** 127, 0x7F80: math.inf, 0xFF80: -math.inf}
+    got = oracle.decode_bf16(np.array(list(cases), dtype=np.uint16))
+    assert np.array_equal(got, np.array(list(cases.values())))
+    assert np.isnan(oracle.decode_bf16(np.array([0x7FC0], np.uint16)))[0]
+    assert np.signbit(oracle.decode_bf16(np.array([0x8000], np.uint16)))[0]
+
+
+def test_decode_bf16_all_patterns_match_binary32_upper_half():
+    # bf16 is the upper 16 bits of an IEEE binary32: reinterpret via numpy
+    bits = np.arange(1 << 16, dtype=np.uint32)
+    with np.errstate(invalid="ignore"):
+        ref = (bits << 16).view(np.float32).astype(np.float64)
+    got = oracle.decode_bf16(bits.astype(np.uint16))
+    both_nan = np.isnan(ref) & np.isnan(got)
+    assert np.all(both_nan | (ref == got))
+
+
+def test_decode_e4m3_fixed_values():
+    # OCP 8-bit floating point spec, E4M3: bias 7, max normal 448, min
+    # subnormal 2^-9, S.1111.111 is NaN, no infinities
+    cases = {0x00: 0.0, 0x38: 1.0, 0x40: 2.0, 0x7E: 448.0, 0xFE: -448.0, 0x01: 2.0 ** -9,
+             0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x3C: 1.5, 0x77: 240.0, 0x78: 256.0}
+    got = oracle.decode_e4m3(np.array(list(cases), dtype=np.uint8))
+    assert np.array_equal(got, np.array(list(cases.values())))
+    assert np.isnan(oracle.decode_e4m3(np.array([0x7F, 0xFF], np.uint8))).all()
+
+
+def test_decode_e4m3_all_codes_match_torch():
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = oracle.decode_e4m3(codes.numpy())
+    both_nan = np.isnan(ref) & np.isnan(got)
+    assert np.all(both_nan | (ref == got))
+
+
+# ---------------------------------------------------------------------------
+# the worked example (page section 二)
+# ---------------------------------------------------------------------------
+
+def test_worked_example_groups_and_rows():
+    g, idx, w, groups = helpers.worked_example()
+    counts, offsets, perm_token, inv_row = oracle.permutation_maps(idx, g["E"])
+    assert counts.tolist() == g["rows_per_expert"] == [3, 2, 2, 1]
+    assert int(counts.sum()) == g["assignments"] == 8
+    assert offsets.tolist() == [0, 3, 5, 7, 8]
+    for e in range(g["E"]):
+        assert perm_token[offsets[e]:offsets[e + 1]].tolist() == groups[e]
+    # the inverse map sends each assignment to a row of its own token and expert
+    for t in range(g["T"]):
+        for j in range(g["k"]):
+            r = inv_row[t, j]
+            assert perm_token[r] == t
+            assert offsets[idx[t, j]] <= r < offsets[idx[t, j] + 1]
+    assert perm_token.tolist() == [0, 1, 2, 2, 3, 0, 1, 3]
+    assert inv_row.tolist() == [[0, 5], [6, 1], [2, 3], [4, 7]]
+
+
+def test_worked_example_router_reproduces_weights():
+    g, idx, w, _ = helpers.worked_example()
+    logits = helpers.worked_example_logits(idx, w, g["E"])
+    got_idx, got_w = oracle.topk_renorm(logits, g["k"])
+    assert got_idx.tolist() == idx.tolist()
+    np.testing.assert_allclose(got_w, w, rtol=0, atol=1e-12)
+    for t in range(g["T"]):
+        printed = {int(e[1:]) - 1: v for e, v in g["routing"][f"T{t + 1}"].items()}
+        assert {int(e): float(v) for e, v in zip(got_idx[t], got_w[t])} == pytest.approx(printed, abs=1e-12)
+
+
+def _library_ffn(x, wg, wu, wd):
+    x, wg, wu, wd = (torch.from_numpy(np.asarray(a, np.float64)) for a in (x, wg, wu, wd))
+    return F.linear(F.silu(F.linear(x, wg)) * F.linear(x, wu), wd).numpy()
+
+
+def test_worked_example_combine_of_T1():
+    # the page: T1's output is 0.7 * E1(T1) + 0.3 * E3(T1)
+    g, idx, w, _ = helpers.worked_example()
+    rng = np.random.default_rng(7)
+    d, f, E = 6, 10, g["E"]
+    Wg, Wu, Wd = rng.normal(size=(E, f, d)), rng.normal(size=(E, f, d)), rng.normal(size=(E, d, f))
+    x = rng.normal(size=(g["T"], d))
+    ew = oracle.ExpertWeights("f64", Wg, Wu, Wd)
+    wr = np.zeros((E, d))
+    out_i, _, _ = oracle.moe_forward_per_token(x, wr, ew, g["k"], routing=(idx, w))
+    out_ii, _, _ = oracle.moe_forward_grouped(x, wr, ew, g["k"], routing=(idx, w))
+    c = g["combine"]["T1"]
+    t1 = c["E1"] * _library_ffn(x[:1], Wg[0], Wu[0], Wd[0]) + c["E3"] * _library_ffn(x[:1], Wg[2], Wu[2], Wd[2])
+    np.testing.assert_allclose(out_i[0], t1[0], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(out_ii[0], t1[0], rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# router: library matmul, brute force, closed form
+# ---------------------------------------------------------------------------
+
+def test_router_logits_match_library_linear():
+    rng = np.random.default_rng(1)
+    x, w, b = rng.normal(size=(9, 13)), rng.normal(size=(5, 13)), rng.normal(size=5)
+    ref = F.linear(torch.from_numpy(x), torch.from_numpy(w), torch.from_numpy(b)).numpy()
+    np.testing.assert_allclose(oracle.router_logits(x, w, b), ref, rtol=1e-13, atol=1e-13)
+
+
+@pytest.mark.parametrize("E,k", [(4, 1), (5, 2), (6, 3), (6, 6), (3, 2)])
+def test_topk_brute_force_over_subsets(E, k):
+    rng = np.random.default_rng(E * 10 + k)
+    logits = rng.normal(size=(40, E)) * 2
+    idx, w = oracle.topk_renorm(logits, k)
+    best = moe_oracle.brute_force_topk_sets(logits, k)
+    for t in range(logits.shape[0]):
+        assert set(idx[t].tolist()) == best[t]
+        # closed form: renormalised weights = softmax over the chosen logits only
+        sub = scipy.special.softmax(logits[t, idx[t]])
+        np.testing.assert_allclose(w[t], sub, rtol=1e-13, atol=1e-15)
+        # slots in descending weight
+        assert np.all(np.diff(w[t]) <= 0)
+
+
+def test_topk_weights_ignore_unchosen_logits():
+    rng = np.random.default_rng(3)
+    logits = rng.normal(size=(20, 8))
+    idx, w = oracle.topk_renorm(logits, 2)
+    moved = logits.copy()
+    for t in range(20):
+        rest = [e for e in range(8) if e not in idx[t]]
+        moved[t, rest] -= rng.uniform(0, 5, size=len(rest))  # stay below the k-th
+    idx2, w2 = oracle.topk_renorm(moved, 2)
+    assert np.array_equal(idx, idx2)
+    np.testing.assert_allclose(w, w2, rtol=1e-13)
+
+
+def test_topk_ties_go_to_lower_index():
+    logits = np.array([[1.0, 3.0, 3.0, 0.0, 3.0]])
+    idx, w = oracle.topk_renorm(logits, 2)
+    assert idx.tolist() == [[1, 2]]
+    np.testing.assert_allclose(w, [[0.5, 0.5]])
+
+
+def test_topk_gap():
+    logits = np.array([[0.0, 5.0, 4.0, 1.0]])
+    assert oracle.topk_gap(logits, 2)[0] == pytest.approx(3.0)
+    assert np.isinf(oracle.topk_gap(logits, 4)[0])
+
+
+# ---------------------------------------------------------------------------
+# expert FFN: closed-form SiLU values and the library FFN
+# ---------------------------------------------------------------------------
+
+def test_silu_closed_form_values():
+    z = np.array([0.0, 1.0, -1.0, 2.0, -40.0, 40.0, -800.0])
+    want = np.array([0.0, 1 / (1 + math.exp(-1)), -1 / (1 + math.e), 2 / (1 + math.exp(-2)),
+                     -40 * math.exp(-40) / (1 + math.exp(-40)), 40 / (1 + math.exp(-40)), 0.0])
+    np.testing.assert_allclose(oracle.silu(z), want, rtol=1e-15, atol=1e-300)
+    np.testing.assert_allclose(oracle.silu(1.0 * np.array([1.0]))[0], 0.7310585786300049, rtol=1e-15)
+
+
+def test_silu_matches_library():
+    z = np.random.default_rng(0).normal(size=1000) * 10
+    np.testing.assert_allclose(oracle.silu(z), F.silu(torch.from_numpy(z)).numpy(), rtol=1e-14, atol=1e-300)
+
+
+def test_swiglu_expert_matches_library_ffn():
+    rng = np.random.default_rng(2)
+    x, wg, wu, wd = rng.normal(size=(7, 12)), rng.normal(size=(20, 12)), rng.normal(size=(20, 12)), rng.normal(size=(12, 20))
+    np.testing.assert_allclose(oracle.swiglu_expert(x, wg, wu, wd), _library_ffn(x, wg, wu, wd), rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# special cases of the layer
+# ---------------------------------------------------------------------------
+
+def _rand_layer(rng, T=12, d=8, f=16, E=5):
+    x = rng.normal(size=(T, d))
+    wr = rng.normal(size=(E, d)) / np.sqrt(d)
+    Wg, Wu = rng.normal(size=(E, f, d)) / np.sqrt(d), rng.normal(size=(E, f, d)) / np.sqrt(d)
+    Wd = rng.normal(size=(E, d, f)) / np.sqrt(d)
+    return x, wr, Wg, Wu, Wd
+
+
+def test_single_expert_is_dense_swiglu():
+    rng = np.random.default_rng(11)
+    x, wr, Wg, Wu, Wd = _rand_layer(rng, E=1)
+    ew = oracle.ExpertWeights("f64", Wg, Wu, Wd)
+    for fn in (oracle.moe_forward_per_token, oracle.moe_forward_grouped):
+        out, idx, w = fn(x, wr, ew, 1)
+        np.testing.assert_allclose(out, _library_ffn(x, Wg[0], Wu[0], Wd[0]), rtol=1e-12, atol=1e-12)
+        assert np.all(idx == 0) and np.allclose(w, 1.0)
+
+
+def test_k_equal_E_is_full_softmax_mixture():
+    rng = np.random.default_rng(12)
+    x, wr, Wg, Wu, Wd = _rand_layer(rng, E=4)
+    ew = oracle.ExpertWeights("f64", Wg, Wu, Wd)
+    p = scipy.special.softmax(x @ wr.T, axis=1)
+    want = sum(p[:, e:e + 1] * _library_ffn(x, Wg[e], Wu[e], Wd[e]) for e in range(4))
+    for fn in (oracle.moe_forward_per_token, oracle.moe_forward_grouped):
+        out, _, _ = fn(x, wr, ew, 4)
+        np.testing.assert_allclose(out, want, rtol=1e-12, atol=1e-12)
+
+
+def test_identical_experts_give_the_dense_ffn():
+    rng = np.random.default_rng(13)
+    x, wr, Wg, Wu, Wd = _rand_layer(rng, E=6)
+    Wg[:], Wu[:], Wd[:] = Wg[0], Wu[0], Wd[0]
+    ew = oracle.ExpertWeights("f64", Wg, Wu, Wd)
+    out, _, _ = oracle.moe_forward_grouped(x, wr, ew, 3)
+    np.testing.assert_allclose(out, _library_ffn(x, Wg[0], Wu[0], Wd[0]), rtol=1e-12, atol=1e-12)
+
+
+def test_zero_tokens_give_zero_output():
+    rng = np.random.default_rng(14)
+    x, wr, Wg, Wu, Wd = _rand_layer(rng)
+    ew = oracle.ExpertWeights("f64", Wg, Wu, Wd)
+    out, _, _ = oracle.moe_forward_per_token(np.zeros_like(x), wr, ew, 2)
+    assert np.all(out == 0)
+
+
+def test_shared_expert_is_added_with_weight_one():
+    rng = np.random.default_rng(15)
+    x, wr, Wg, Wu, Wd = _rand_layer(rng)
+    sh = (rng.normal(size=(9, 8)), rng.normal(size=(9, 8)), rng.normal(size=(8, 9)))
+    ew = oracle.ExpertWeights("f64", Wg, Wu, Wd)
+    base, _, _ = oracle.moe_forward_grouped(x, wr, ew, 2)
+    withs, _, _ = oracle.moe_forward_grouped(x, wr, ew, 2, shared=sh)
+    np.testing.assert_allclose(withs - base, _library_ffn(x, *sh), rtol=1e-11, atol=1e-11)
+
+
+# ---------------------------------------------------------------------------
+# invariants the page states, and the two formulations
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("T,E,k", [(1, 8, 2), (37, 8, 2), (64, 16, 4), (200, 32, 8), (5, 3, 3)])
+def test_permutation_invariants(T, E, k):
+    rng = np.random.default_rng(T + E + k)
+    idx, w = oracle.topk_renorm(rng.normal(size=(T, E)), k)
+    counts, offsets, perm_token, inv_row = oracle.permutation_maps(idx, E)
+    assert counts.sum() == T * k and offsets[-1] == T * k
+    assert np.array_equal(np.bincount(perm_token, minlength=T), np.full(T, k))  # k rows per token
+    for t in range(T):
+        assert len(set(idx[t].tolist())) == k  # distinct experts per token
+    np.testing.assert_allclose(w.sum(axis=1), 1.0, rtol=1e-14)
+    assert np.array_equal(perm_token[inv_row], np.repeat(np.arange(T), k).reshape(T, k))
+    assert sorted(inv_row.ravel().tolist()) == list(range(T * k))
+    for e in range(E):
+        rows = perm_token[offsets[e]:offsets[e + 1]]
+        assert np.all(np.diff(rows) > 0)  # ascending token order inside an expert
+    # permute then unpermute with weights summing to 1 is the identity
+    x = rng.normal(size=(T, 3))
+    x_perm = x[perm_token]
+    back = (w[:, :, None] * x_perm[inv_row]).sum(axis=1)
+    np.testing.assert_allclose(back, x, rtol=1e-13, atol=1e-13)
+
+
+def test_two_formulations_agree_random_layers():
+    rng = np.random.default_rng(21)
+    for (T, d, f, E, k) in [(30, 8, 16, 6, 2), (17, 16, 8, 9, 4), (3, 4, 4, 3, 3)]:
+        x, wr, Wg, Wu, Wd = _rand_layer(rng, T, d, f, E)
+        b = rng.normal(size=E)
+        sh = (rng.normal(size=(5, d)), rng.normal(size=(5, d)), rng.normal(size=(d, 5)))
+        ew = oracle.ExpertWeights("f64", Wg, Wu, Wd)
+        a, ia, wa = oracle.moe_forward_per_token(x, wr, ew, k, bias=b, shared=sh)
+        c, ic, wc = oracle.moe_forward_grouped(x, wr, ew, k, bias=b, shared=sh)
+        assert np.array_equal(ia, ic)
+        np.testing.assert_allclose(a, c, rtol=0, atol=1e-12 * np.abs(a).max())
+
+
+def test_two_formulations_agree_on_generated_fp8_and_bf16_cases():
+    for name, T in [("toy_f32", 64)]:
+        shape = inputs.WORKLOADS[name].with_T(T)
+        case = inputs.make_case(shape, 0)
+        x, wr, b, ew, sh = helpers.oracle_inputs(case, shape)
+        a, _, _ = oracle.moe_forward_per_token(x, wr, ew, shape.k, bias=b, shared=sh)
+        c, _, _ = oracle.moe_forward_grouped(x, wr, ew, shape.k, bias=b, shared=sh)
+        np.testing.assert_allclose(a, c, rtol=0, atol=1e-12 * np.abs(a).max())
+    # a small fp8 + shared layer built with the same generator
+    small = inputs.MoEShape("small_fp8", T=9, d=32, ffn=16, E=6, k=3, ffn_shared=16, wfmt="fp8")
+    case = inputs.make_case(small, 3)
+    x, wr, b, ew, sh = helpers.oracle_inputs(case, small)
+    a, _, _ = oracle.moe_forward_per_token(x, wr, ew, small.k, shared=sh)
+    c, _, _ = oracle.moe_forward_grouped(x, wr, ew, small.k, shared=sh)
+    np.testing.assert_allclose(a, c, rtol=0, atol=1e-12 * np.abs(a).max())
+
+
+def test_fp8_weights_are_code_times_per_channel_scale():
+    small = inputs.MoEShape("small_fp8", T=2, d=16, ffn=8, E=2, k=1, wfmt="fp8")
+    case = inputs.make_case(small, 5)
+    x, wr, b, ew, sh = helpers.oracle_inputs(case, small)
+    wg, wu, wd = ew.get(1)
+    codes = case["w_gate"][1].view(torch.float8_e4m3fn).to(torch.float64)
+    ref = codes * case["s_gate"][1].to(torch.float64)[:, None]
+    np.testing.assert_allclose(wg, ref.numpy(), rtol=0, atol=0)
+    # per-channel amax of the decoded codes is 448 (scale = amax / 448)
+    assert np.allclose(np.abs(codes.numpy()).max(axis=1), 448.0)
+
+
+# ---------------------------------------------------------------------------
+# the skewed prefill recipe
+# ---------------------------------------------------------------------------
+
+def test_zipf_bias_scale_matches_calibration():
+    cal = helpers.load_golden("zipf_bias_alpha.json")["qwen3_30b_a3b_prefill"]
+    assert inputs.ZIPF_ALPHA["qwen3_30b_a3b_prefill"] == cal["alpha"]
+    shape = inputs.WORKLOADS["qwen3_30b_a3b_prefill"]
+    wr = inputs._normal((shape.E, shape.d), 1.0 / np.sqrt(shape.d), 0, "w_router", "cpu", torch.bfloat16)
+    x = inputs.make_tokens(shape, 0)
+    lg = oracle.router_logits(helpers.decode_act(x, "bf16"), helpers.decode_act(wr, "bf16"),
+                              inputs.zipf_bias(shape, 0).double().numpy())
+    idx, _ = oracle.topk_renorm(lg, shape.k)
+    counts, _, _, _ = oracle.permutation_maps(idx, shape.E)
+    r = counts.max() / counts.mean()
+    assert 7.5 <= r <= 8.5
