@@ -1,0 +1,469 @@
+#!/usr/bin/env python
+"""Benchmark: forward of one Mixture-of-Experts FFN layer on GB300.
+
+One step = one pass of the whole layer (router top-k, permutation, grouped
+SwiGLU experts, shared expert if any, combine) over one batch of synthetic
+tokens whose inputs are already resident in HBM.  Default workload: the
+Mixtral-8x7B-shaped layer (d=4096, ffn=14336, E=8, top-2, bf16) at a decode
+batch of T=64 tokens.  Metric: MoE-layer tokens/s (whole job, all ranks).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--T T]
+  python bench.py --impl reference ...   # the fp64 CPU reference, timed on host cores
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs an independent
+replica of the layer on its own batch (the path shards by tokens with no
+exchange step); timings are bracketed by a barrier and the maximum over
+ranks is taken.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from routed_expert_ffn_gemm_gb300 import inputs  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+DEFAULT_HBM_GBS = 6800.0      # fallback peaks when no measured file exists
+DEFAULT_BF16_TFLOPS = 1900.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mixtral_8x7b", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--T", type=int, default=None, help="tokens per step (default: the workload's)")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--weight-sets", type=int, default=0,
+                    help="independent weight sets rotated per step (0: enough to exceed L2)")
+    ap.add_argument("--stage-steps", type=int, default=200)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# shared helpers
+# ---------------------------------------------------------------------------
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), float(pk["bf16_tflops"]), float(pk["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return DEFAULT_HBM_GBS, DEFAULT_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def wbytes(shape):
+    return {"f32": 4, "bf16": 2, "fp8": 1}[shape.wfmt]
+
+
+def abytes(shape):
+    return 4 if shape.act == "f32" else 2
+
+
+def expected_touched(shape):
+    """Expected experts with at least one row under uniform routing."""
+    R = shape.T * shape.k
+    return shape.E * (1.0 - (1.0 - shape.k / shape.E) ** shape.T) if R else 0.0
+
+
+def stage_work(shape, touched, splits):
+    """Algorithmic bytes and flops per launch of the two expert GEMM kernels
+    (and per layer), counting only what the method must read and write."""
+    R, d, f, E, T = shape.T * shape.k, shape.d, shape.ffn, shape.E, shape.T
+    wb, ab = wbytes(shape), abytes(shape)
+    scale = 4 if shape.wfmt == "fp8" else 0
+    gu_bytes = touched * (2 * f * d * wb + 2 * f * scale) + R * d * ab + R * f * ab
+    gu_flops = 4.0 * R * f * d
+    y_bytes = splits * R * d * 4 if splits > 1 else R * d * ab
+    dn_bytes = touched * (d * f * wb + d * scale) + R * f * ab + y_bytes
+    dn_flops = 2.0 * R * f * d
+    fs = shape.ffn_shared
+    layer_bytes = (E * d * ab + touched * 3 * f * d * wb + 3 * fs * d * ab + 2 * T * d * ab)
+    layer_flops = 2.0 * T * d * E + 6.0 * d * f * R + 6.0 * d * fs * T
+    return {"gate_up": (gu_bytes, gu_flops), "down": (dn_bytes, dn_flops),
+            "layer": (layer_bytes, layer_flops)}
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.lines = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, ws, device):
+    if ws == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU reference (fp64 oracle), timed on the host cores
+# ---------------------------------------------------------------------------
+
+def _oracle_session(shape, seed):
+    """Generate the case on the CPU and decode every expert to float64 once
+    (format conversion is excluded from timing)."""
+    import oracle
+    case = inputs.make_case(shape, seed, "cpu")
+
+    def f64(t):
+        return None if t is None else t.to(torch.float64).numpy()
+
+    x = f64(case["x"])
+    wr = f64(case["w_router"])
+    b = f64(case["router_bias"])
+    decoded = {}
+    for e in range(shape.E):
+        if shape.wfmt == "fp8":
+            def dq(w, s):
+                return (w[e].view(torch.float8_e4m3fn).to(torch.float64) * s[e].to(torch.float64)[:, None]).numpy()
+            decoded[e] = (dq(case["w_gate"], case["s_gate"]), dq(case["w_up"], case["s_up"]),
+                          dq(case["w_down"], case["s_down"]))
+        else:
+            decoded[e] = (f64(case["w_gate"][e]), f64(case["w_up"][e]), f64(case["w_down"][e]))
+    shared = None
+    if shape.ffn_shared:
+        shared = tuple(f64(case[n]) for n in ("w_shared_gate", "w_shared_up", "w_shared_down"))
+    ew = oracle.ExpertWeights("f64", *(np.zeros((shape.E, 1, 1)),) * 3)
+    return oracle, x, wr, b, ew, decoded, shared
+
+
+def oracle_tokens_per_s(shape, seed, budget_s, min_tokens=1):
+    """Time the grouped fp64 oracle on a bounded sample of the workload:
+    the first n tokens of one batch, n chosen so the timing takes about
+    budget_s seconds.  Returns (tokens/s, sample description, cores)."""
+    oracle, x, wr, b, ew, decoded, shared = _oracle_session(shape, seed)
+    cores = len(os.sched_getaffinity(0))
+
+    def run(n):
+        t0 = time.perf_counter()
+        oracle.moe_forward_grouped(x[:n], wr, ew, shape.k, bias=b, shared=shared,
+                                   expert_hook=decoded.__getitem__)
+        return time.perf_counter() - t0
+
+    n = min(shape.T, max(min_tokens, 1))
+    dt = run(n)
+    while n < shape.T and dt < budget_s / 4:
+        n = min(shape.T, n * 2)
+        dt = run(n)
+    reps, total = 0, 0.0
+    while total < budget_s and reps < 50:
+        total += run(n)
+        reps += 1
+    sample = (f"{reps} runs of the grouped fp64 oracle over the first {n} of {shape.T} tokens "
+              f"(expert weights decoded to fp64 beforehand, excluded)")
+    return reps * n / total, sample, cores
+
+
+def run_reference(args, shape, ws, rank):
+    if rank != 0:
+        return 0
+    import oracle  # noqa: F401  (the reference arm times the oracle as it stands)
+    oracle_mod, x, wr, b, ew, decoded, shared = _oracle_session(shape, args.seed)
+    cores = len(os.sched_getaffinity(0))
+
+    def step(n):
+        oracle_mod.moe_forward_grouped(x[:n], wr, ew, shape.k, bias=b, shared=shared,
+                                       expert_hook=decoded.__getitem__)
+
+    # size each step so the whole run takes about two minutes
+    t0 = time.perf_counter()
+    step(1)
+    one = max(time.perf_counter() - t0, 1e-4)
+    per_step_budget = 120.0 / max(1, args.steps + args.warmup)
+    n = int(max(1, min(shape.T, per_step_budget / one)))
+    for _ in range(args.warmup):
+        step(n)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step(n)
+    dt = time.perf_counter() - t0
+    value = args.steps * n / dt
+    sample = f"each step: the grouped fp64 oracle over the first {n} of {shape.T} tokens"
+    line = {
+        "impl": "reference", "metric": "moe_layer_tokens_per_s", "value": value, "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(shape),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(shape, extra=None):
+    c = {"workload": f"{shape.name}_moe_layer", "T": shape.T, "d": shape.d, "ffn": shape.ffn,
+         "E": shape.E, "k": shape.k, "ffn_shared": shape.ffn_shared, "act": shape.act,
+         "weights": shape.wfmt, "router_bias": shape.router_bias, "parallelism": "replicas"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, shape, ws, rank, local):
+    from routed_expert_ffn_gemm_gb300 import api, build
+    build.build()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    hbm_gbs, bf16_tf, bf16_tf_sus, peak_src = load_peaks()
+
+    touched_est = expected_touched(shape)
+    touched_bytes = touched_est * 3 * shape.ffn * shape.d * wbytes(shape)
+    n_sets = args.weight_sets or max(1, math.ceil(2 * L2_BYTES / max(touched_bytes, 1)))
+    full_bytes = shape.E * 3 * shape.ffn * shape.d * wbytes(shape)
+    n_sets = min(n_sets, max(1, int(100e9 // max(full_bytes, 1))))
+    seed = args.seed + 1000 * rank
+    sets = [inputs.make_weights(shape, seed + i, device) for i in range(n_sets)]
+    n_x = 4
+    xs = [inputs.make_tokens(shape, seed, device, step=j) for j in range(n_x)]
+    p = api.problem_of(shape)
+    wsp = api.workspace_for(p, device)
+    out = torch.empty((shape.T, shape.d), dtype=xs[0].dtype, device=device)
+    launches = api.moe_layer_launch_count(p)
+    counts = torch.empty(shape.E, dtype=torch.int32, device=device)
+
+    def case(i):
+        c = dict(sets[i % n_sets])
+        c["x"] = xs[i % n_x]
+        return c
+
+    def fwd(i, timer=None, x=None, want_counts=False):
+        c = case(i)
+        if x is not None:
+            c["x"] = x
+        args_ = (p, c["x"], c["w_router"], c["router_bias"], c["w_gate"], c["w_up"], c["w_down"],
+                 c["s_gate"], c["s_up"], c["s_down"], c["w_shared_gate"], c["w_shared_up"],
+                 c["w_shared_down"], out, None, None, counts if want_counts else None, wsp)
+        if timer is None:
+            api.moe_layer_forward(*args_)
+        else:
+            api.moe_layer_forward_timed(*args_, timer)
+
+    for i in range(args.warmup):
+        fwd(i)
+    torch.cuda.synchronize()
+    assert api.moe_read_device_status() == 0
+
+    # ---- timed region: K back-to-back steps, inputs resident in HBM
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(args.steps):
+        fwd(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    ms = e0.elapsed_time(e1)
+    sampler.stop()
+    ms = max_over_ranks(ms, ws, device)
+    value = ws * args.steps * shape.T / (ms / 1e3)
+
+    # ---- per-stage device times (events on the launching stream)
+    ks = min(args.stage_steps, args.steps)
+    timers = [api.StageTimer() for _ in range(ks)]
+    counts_seen = []
+    for i in range(ks):
+        fwd(i, timer=timers[i], want_counts=True)
+        if i < 16:
+            counts_seen.append(counts.clone())
+    torch.cuda.synchronize()
+    stage = {s: [] for s in api.STAGES}
+    for t in timers:
+        for s, v in t.read().items():
+            stage[s].append(v)
+    for t in timers:
+        t.close()
+    stage_ms = {s: statistics.mean(v) for s, v in stage.items()}
+    touched = statistics.mean(float((c > 0).sum()) for c in counts_seen)
+    max_over_mean = statistics.mean(float(c.max()) / max(float(c.float().mean()), 1e-9) for c in counts_seen)
+    plan = api.moe_plan_info(p)
+    splits = max(1, plan["splits_down"])
+    work = stage_work(shape, touched, splits)
+    dominant = max(("gate_up", "down"), key=lambda s: stage_ms[s])
+    b_, f_ = work[dominant]
+    t_s = stage_ms[dominant] / 1e3
+    ridge = bf16_tf * 1e12 / (hbm_gbs * 1e9)
+    if f_ / b_ > ridge:
+        roof = {"bound": "tensor", "achieved": f_ / t_s / 1e12, "peak": bf16_tf, "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": b_ / t_s / 1e9, "peak": hbm_gbs, "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["kernel"] = f"tc_grouped_kernel ({dominant})"
+    roof["peak_source"] = peak_src
+    roof["algorithmic_bytes_per_launch"] = b_
+    roof["algorithmic_flops_per_launch"] = f_
+    lb, lf = work["layer"]
+    layer_s = ms / 1e3 / args.steps
+
+    # ---- end to end: pinned host inputs in, result out, every step
+    e2e = None
+    if not args.no_e2e:
+        xh = [x.cpu().pin_memory() for x in xs]
+        xd = torch.empty_like(xs[0])
+        oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        for i in range(min(args.warmup, 5)):
+            xd.copy_(xh[i % n_x], non_blocking=True)
+            fwd(i, x=xd)
+            oh.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        barrier(ws)
+        e0.record(stream)
+        for i in range(args.steps):
+            xd.copy_(xh[i % n_x], non_blocking=True)
+            fwd(i, x=xd)
+            oh.copy_(out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        ems = max_over_ranks(e0.elapsed_time(e1), ws, device)
+        nb = shape.T * shape.d * abytes(shape)
+        e2e = {"value": ws * args.steps * shape.T / (ems / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": nb, "d2h_bytes_per_step": nb}
+    assert api.moe_read_device_status() == 0
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        v, sample, cores = oracle_tokens_per_s(shape, args.seed, budget_s=15.0)
+        cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        line = {
+            "metric": "moe_layer_tokens_per_s", "value": value, "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if shape.act == "bf16" else "f32", "data": "synthetic",
+            "config": workload_config(shape, {
+                "l2": (f"inputs larger than L2: {touched * 3 * shape.ffn * shape.d * wbytes(shape) / 1e9:.2f} GB "
+                       f"of touched expert weights per step, {n_sets} weight set(s) rotated")}),
+            "roofline": roof,
+            "layer": {"GB_per_s_touched_bytes": lb / layer_s / 1e9, "frac_hbm": lb / layer_s / 1e9 / hbm_gbs,
+                      "TFLOP_per_s": lf / layer_s / 1e12, "touched_experts": touched,
+                      "max_over_mean_rows": max_over_mean},
+            "stages_us": {s: 1e3 * v for s, v in stage_ms.items()},
+            "plan": plan,
+            "gpu_launches": launches * args.steps,
+            "clocks": sampler.summary(),
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse_args()
+    shape = inputs.WORKLOADS[args.workload]
+    if args.T is not None:
+        shape = shape.with_T(args.T)
+    elif args.workload == "mixtral_8x7b":
+        shape = shape.with_T(64)
+    ws, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        return run_reference(args, shape, ws, rank)
+    return run_ours(args, shape, ws, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,297 @@
+/*
+ * moe.h -- C ABI of libmoe_gb300.so: the single-GPU forward of one
+ * Mixture-of-Experts FFN layer on GB300 (sm_103a).
+ *
+ * The layer, as the page "MOE推理流程解析" (ffner.com) lays it out:
+ *   section 三: the router scores every eligible expert; top-k keeps the
+ *     chosen experts' indices and weights; a permutation reads the token
+ *     vectors, writes them in expert order and records an inverse map; a
+ *     grouped GEMM runs all expert matrices (of different row counts) in
+ *     one launch; each expert applies its activation and output projection;
+ *     the inverse map restores token order, the routing weight is applied
+ *     and the contributions of the same token are summed.
+ *   section 二: assignments (token vector, expert, weight) are grouped by
+ *     expert into contiguous matrices, each row keeping its source token id;
+ *     an expert batch counts assignments, not unique tokens (top-2 gives two
+ *     rows per token).
+ *   section 一: shared experts process every token whatever the router
+ *     scores.
+ * Precision ("MoE 推理部署", zzmblog.top, section 专家量化): quantisation
+ * scales are per expert; the router and shared experts stay at higher
+ * precision than quantised routed experts.
+ *
+ * Conventions (all entry points)
+ *   - Every pointer named as a tensor is a DEVICE pointer of the current CUDA
+ *     device, row-major, densely packed, 16-byte aligned.  The caller owns
+ *     every buffer and the stream; the library allocates no device memory.
+ *   - Weights are [out, in] (the reduction index is contiguous):
+ *       w_router [E, d]; w_gate, w_up [E, ffn, d]; w_down [E, d, ffn];
+ *       shared expert: w_shared_gate, w_shared_up [ffn_shared, d],
+ *       w_shared_down [d, ffn_shared].
+ *   - Experts are numbered from 0.  R = T * k assignment rows.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).
+ *     Argument errors are detected on the host and returned before anything
+ *     is enqueued; launch failures return MOE_ERR_CUDA.  Errors found by a
+ *     kernel (an expired bounded wait, an out-of-range index) are recorded in
+ *     a per-device status word read by moe_read_device_status().
+ *   - Unsupported combinations of sizes or dtypes return MOE_ERR_UNSUPPORTED;
+ *     there is no fallback path.
+ *   - T == 0 is valid: nothing is enqueued and MOE_OK is returned.
+ *
+ * Supported storage:  act_dtype / w_dtype
+ *   MOE_F32  / MOE_F32          fp32 CUDA-core path (fp32 accumulation)
+ *   MOE_BF16 / MOE_BF16         tcgen05 tensor-core path (fp32 accumulation)
+ *   MOE_BF16 / MOE_FP8_E4M3     as above, FP8 weights (OCP E4M3) with fp32
+ *                               per-expert, per-output-channel scales;
+ *                               the router and shared expert stay bf16.
+ * Size limits: 1 <= k <= min(E, 32), E <= 1024, d % 8 == 0, ffn % 8 == 0;
+ * the tensor-core path further needs d % 128 == 0, ffn % 128 == 0 and
+ * ffn_shared % 128 == 0.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+/* A cudaStream_t. */
+typedef struct CUstream_st *moe_stream_t;
+
+typedef enum moe_dtype {
+  MOE_F32 = 0,
+  MOE_BF16 = 1,
+  MOE_FP8_E4M3 = 2
+} moe_dtype;
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,    /* null pointer, bad size, k > E, ...        */
+  MOE_ERR_UNSUPPORTED = -2,    /* valid but not implemented combination     */
+  MOE_ERR_WORKSPACE = -3,      /* workspace missing or too small            */
+  MOE_ERR_CUDA = -4,           /* a CUDA runtime / driver call failed       */
+  MOE_ERR_DEVICE_TIMEOUT = -5, /* a kernel's bounded wait expired           */
+  MOE_ERR_DEVICE_BOUNDS = -6   /* a kernel met an out-of-range index/offset */
+} moe_status;
+
+/* The problem statement shared by every entry point. */
+typedef struct moe_problem {
+  int32_t T;          /* tokens in the batch                                */
+  int32_t d;          /* hidden size                                        */
+  int32_t ffn;        /* routed expert intermediate size                    */
+  int32_t E;          /* routed experts                                     */
+  int32_t k;          /* experts chosen per token                           */
+  int32_t ffn_shared; /* shared expert intermediate size; 0 = none          */
+  int32_t act_dtype;  /* moe_dtype of x, w_router, shared expert, outputs   */
+  int32_t w_dtype;    /* moe_dtype of the routed expert weights             */
+} moe_problem;
+
+/*
+ * moe_router_topk -- router scores, softmax, top-k, renormalised weights.
+ * Page "MOE推理流程解析", section 三 (the router scores each eligible expert;
+ * top-k keeps the chosen indices and weights) and section 九 (the kept
+ * weights are re-normalised).
+ *
+ *   l[t,e]   = sum_i x[t,i] * w_router[e,i] (+ router_bias[e]), fp32 accumulate
+ *   p        = softmax(l[t,:]) over all E experts
+ *   S_t      = the k experts with the largest l (ties: lower expert index)
+ *   w[t,j]   = p[S_t,j] / sum_{e in S_t} p[e]   (== softmax over S_t only)
+ * Slots j are in descending weight.
+ *
+ *   x            [T, d] act_dtype
+ *   w_router     [E, d] act_dtype
+ *   router_bias  [E] fp32 or NULL
+ *   logits_in    [T, E] fp32 or NULL: when given, used as l directly (no
+ *                matmul; router_bias must then be NULL; x, w_router unused)
+ *   logits_out   [T, E] fp32 or NULL: receives l (including the bias)
+ *   topk_idx     [T, k] int32 out      topk_w  [T, k] fp32 out
+ */
+MOE_API moe_status moe_router_topk(const moe_problem *p, const void *x, const void *w_router,
+                           const float *router_bias, const float *logits_in,
+                           float *logits_out, int32_t *topk_idx, float *topk_w,
+                           moe_stream_t stream);
+
+/*
+ * moe_permute -- group the T*k assignments by expert and move token rows.
+ * Page "MOE推理流程解析", section 二 (grouping by expert into contiguous
+ * matrices, the source token id kept beside each row) and section 三 (the
+ * permutation writes token vectors in expert order and records an inverse
+ * map for the combine).
+ *
+ *   counts[e]       = #{(t,j) : topk_idx[t,j] == e}                [E] int32 out
+ *   offsets[e]      = sum_{e'<e} counts[e'], offsets[E] = T*k     [E+1] int32 out
+ *   perm_token[r]   = source token of row r                       [T*k] int32 out
+ *   inv_row[t*k+j]  = row holding assignment (t, j)               [T*k] int32 out
+ *   x_perm[r, :]    = x[perm_token[r], :]      [T*k, d] act_dtype out, or NULL
+ * Rows inside an expert's range are in ascending token order (deterministic,
+ * bit-exact).  x may be NULL only when x_perm is NULL.  topk_idx entries
+ * outside [0, E) are skipped and flag MOE_ERR_DEVICE_BOUNDS.
+ * workspace: at least moe_workspace_size() bytes, device memory.
+ */
+MOE_API moe_status moe_permute(const moe_problem *p, const int32_t *topk_idx, const void *x,
+                       int32_t *counts, int32_t *offsets, int32_t *perm_token,
+                       int32_t *inv_row, void *x_perm, void *workspace,
+                       size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * moe_grouped_swiglu -- all expert matrices in one grouped computation.
+ * Page "MOE推理流程解析", section 三 (a grouped GEMM runs several expert
+ * matrices with different row counts in one launch; each expert applies its
+ * activation and output projection) and section 二 (variable-row expert
+ * matrices, no padding in the result).
+ *
+ * For every expert e and every row r in [offsets[e], offsets[e+1]):
+ *   h[r,:]      = SiLU(x_perm[r,:] W_g[e]^T) * (x_perm[r,:] W_u[e]^T)
+ *   y_perm[r,:] = h[r,:] W_d[e]^T
+ * with FP8 weights W[e][o,:] = code[e][o,:] * scale[e][o] (s_gate, s_up
+ * [E, ffn]; s_down [E, d]; NULL unless w_dtype == MOE_FP8_E4M3).
+ *
+ *   x_perm   [T*k, d] act_dtype      offsets [E+1] int32 (device)
+ *   y_perm   [T*k, d] act_dtype out
+ * h is kept in workspace in act_dtype (bf16 for the tensor-core path).
+ * Offsets must be non-decreasing with offsets[E] <= T*k; rows outside every
+ * expert's range are left untouched.
+ */
+MOE_API moe_status moe_grouped_swiglu(const moe_problem *p, const void *x_perm, const int32_t *offsets,
+                              const void *w_gate, const void *w_up, const void *w_down,
+                              const float *s_gate, const float *s_up, const float *s_down,
+                              void *y_perm, void *workspace, size_t workspace_bytes,
+                              moe_stream_t stream);
+
+/*
+ * moe_combine -- restore token order, apply routing weights, sum.
+ * Page "MOE推理流程解析", section 三 (the inverse map restores token order,
+ * the routing weight is applied, contributions with the same token id are
+ * summed) and section 二 (T1's output is 0.7 * E1(T1) + 0.3 * E3(T1)).
+ *
+ *   out[t,:] = sum_{j<k} topk_w[t,j] * y_perm[inv_row[t*k+j], :] (+ shared_out[t,:])
+ * accumulated in fp32 in slot order j = 0..k-1, rounded once to act_dtype.
+ *   y_perm [T*k, d]  inv_row [T*k] int32  topk_w [T, k] fp32
+ *   shared_out [T, d] act_dtype or NULL      out [T, d] act_dtype
+ */
+MOE_API moe_status moe_combine(const moe_problem *p, const void *y_perm, const int32_t *inv_row,
+                       const float *topk_w, const void *shared_out, void *out,
+                       moe_stream_t stream);
+
+/*
+ * moe_layer_forward -- the whole layer: router top-k, permutation, grouped
+ * SwiGLU experts, optional shared expert, combine (page "MOE推理流程解析",
+ * sections 一, 二, 三; section 十一 lists the step: routing, token
+ * permutation, grouped expert compute, combine, unpermutation).
+ *
+ *   out[t,:] = sum_{e in S_t} w[t,e] * FFN_e(x[t,:]) + FFN_shared(x[t,:])
+ *
+ * Shared expert weights are all NULL when p->ffn_shared == 0, all non-NULL
+ * otherwise.  topk_idx_out [T,k], topk_w_out [T,k] and counts_out [E] are
+ * optional copies of the routing decision (NULL = not wanted).
+ * The whole sequence is enqueued on `stream` without any host
+ * synchronisation, so it can be captured into a CUDA graph by the caller.
+ */
+MOE_API moe_status moe_layer_forward(const moe_problem *p, const void *x, const void *w_router,
+                             const float *router_bias, const void *w_gate, const void *w_up,
+                             const void *w_down, const float *s_gate, const float *s_up,
+                             const float *s_down, const void *w_shared_gate,
+                             const void *w_shared_up, const void *w_shared_down, void *out,
+                             int32_t *topk_idx_out, float *topk_w_out, int32_t *counts_out,
+                             void *workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * Per-stage timing of the layer forward (page "MOE推理流程解析", section 三:
+ * measure routing, permutation, expert GEMM and combine separately; one
+ * merged MoE timer cannot say which stage is slow).
+ *
+ * A stage timer holds CUDA events for one call of moe_layer_forward_timed();
+ * reading it waits for that call's last event.  Stage indices:
+ */
+enum {
+  MOE_STAGE_ROUTER = 0,   /* logits, softmax, top-k                        */
+  MOE_STAGE_PERMUTE = 1,  /* counts, offsets, maps, row moves              */
+  MOE_STAGE_GATE_UP = 2,  /* grouped gate/up GEMM + SiLU*mul               */
+  MOE_STAGE_DOWN = 3,     /* grouped down GEMM                             */
+  MOE_STAGE_SHARED = 4,   /* shared expert (0 when absent)                 */
+  MOE_STAGE_COMBINE = 5,  /* unpermute, weights, sum                       */
+  MOE_NUM_STAGES = 6
+};
+typedef struct moe_stage_timer moe_stage_timer;
+
+/* Create / destroy a timer (host object owning CUDA events; no device memory). */
+MOE_API moe_status moe_stage_timer_create(moe_stage_timer **timer);
+MOE_API moe_status moe_stage_timer_destroy(moe_stage_timer *timer);
+/* Wait for the timed call to finish; ms[MOE_NUM_STAGES] receives each stage's
+ * device time in milliseconds. */
+MOE_API moe_status moe_stage_timer_read(moe_stage_timer *timer, float *ms);
+
+/* moe_layer_forward with CUDA events recorded on `stream` between stages. */
+MOE_API moe_status moe_layer_forward_timed(
+    const moe_problem *p, const void *x, const void *w_router, const float *router_bias,
+    const void *w_gate, const void *w_up, const void *w_down, const float *s_gate,
+    const float *s_up, const float *s_down, const void *w_shared_gate, const void *w_shared_up,
+    const void *w_shared_down, void *out, int32_t *topk_idx_out, float *topk_w_out,
+    int32_t *counts_out, void *workspace, size_t workspace_bytes, moe_stream_t stream,
+    moe_stage_timer *timer);
+
+/* Number of kernels one moe_layer_forward() call launches for problem *p on
+ * the current device (written to *launches). */
+MOE_API moe_status moe_layer_launch_count(const moe_problem *p, int32_t *launches);
+
+/*
+ * moe_plan_info -- the tiling the library chose for problem *p on the
+ * current device (no page counterpart; for benchmarks and tests):
+ * info[0] rows per tile of the gate/up GEMM, info[1] rows per tile of the
+ * down GEMM, info[2] reduction splits of the down GEMM, info[3] persistent
+ * CTAs per GEMM launch.  All zero for the fp32 CUDA-core path.
+ */
+MOE_API moe_status moe_plan_info(const moe_problem *p, int32_t *info);
+
+/*
+ * moe_workspace_size -- device workspace (bytes) sufficient for every entry
+ * point above with problem *p on the current device.  Returns
+ * MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED for problems the library rejects.
+ */
+MOE_API moe_status moe_workspace_size(const moe_problem *p, size_t *bytes);
+
+/*
+ * moe_read_device_status -- synchronise `stream`, then read and clear the
+ * current device's kernel status word.  *status receives MOE_OK or the first
+ * error a kernel recorded since the last read (MOE_ERR_DEVICE_TIMEOUT,
+ * MOE_ERR_DEVICE_BOUNDS).  Returns MOE_ERR_CUDA if synchronisation fails.
+ */
+MOE_API moe_status moe_read_device_status(moe_stream_t stream, int32_t *status);
+
+/* Human-readable name of a status code (static storage). */
+MOE_API const char *moe_status_string(int32_t status);
+
+/* The last CUDA error text recorded by a call that returned MOE_ERR_CUDA on
+ * this host thread (static thread-local storage; "" if none). */
+MOE_API const char *moe_last_cuda_error(void);
+
+/* MOE_ABI_VERSION of the loaded library. */
+MOE_API int32_t moe_abi_version(void);
+
+/*
+ * moe_selftest_bounded_wait -- failure-detection self test (no page
+ * counterpart).  Launches the tensor-core kernel's wait machinery on a
+ * barrier that nothing arrives at, with a wait limit of timeout_ns
+ * nanoseconds.  No copy or MMA is issued, so the wait expiring leaves no
+ * work in flight; the kernel records MOE_ERR_DEVICE_TIMEOUT in the status
+ * word, frees its tensor memory and returns.  Read the outcome with
+ * moe_read_device_status().
+ */
+MOE_API moe_status moe_selftest_bounded_wait(int64_t timeout_ns, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,256 @@
+"""Thin ctypes binding of libmoe_gb300.so (include/moe.h), same names.
+
+Argument marshalling only: tensors become device pointers, the stream
+defaults to torch's current stream, a non-zero status raises ``MoEError``.
+Every step of the layer runs in the library's CUDA kernels; there is no
+other implementation behind these functions.  The library is loaded on the
+first call and a missing library is an error (build it with
+``python -m routed_expert_ffn_gemm_gb300.build``).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe_gb300.so")
+
+DTYPE = {"f32": 0, "bf16": 1, "fp8": 2}
+OK = 0
+ERR_INVALID_ARG = -1
+ERR_UNSUPPORTED = -2
+ERR_WORKSPACE = -3
+ERR_CUDA = -4
+ERR_DEVICE_TIMEOUT = -5
+ERR_DEVICE_BOUNDS = -6
+
+
+class moe_problem(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("T", "d", "ffn", "E", "k", "ffn_shared", "act_dtype", "w_dtype")]
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        msg = f"{fn} failed: {moe_status_string(status)}"
+        if status == ERR_CUDA:
+            msg += f" ({_lib().moe_last_cuda_error().decode()})"
+        super().__init__(msg)
+
+
+_LIB = None
+_VP = ctypes.c_void_p
+_PP = ctypes.POINTER(moe_problem)
+
+_SIGS = {
+    "moe_router_topk": [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP],
+    "moe_permute": [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t, _VP],
+    "moe_grouped_swiglu": [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t, _VP],
+    "moe_combine": [_PP, _VP, _VP, _VP, _VP, _VP, _VP],
+    "moe_layer_forward": [_PP] + [_VP] * 18 + [ctypes.c_size_t, _VP],
+    "moe_workspace_size": [_PP, ctypes.POINTER(ctypes.c_size_t)],
+    "moe_read_device_status": [_VP, ctypes.POINTER(ctypes.c_int32)],
+    "moe_status_string": [ctypes.c_int32],
+    "moe_last_cuda_error": [],
+    "moe_abi_version": [],
+    "moe_selftest_bounded_wait": [ctypes.c_int64, _VP],
+    "moe_stage_timer_create": [ctypes.POINTER(_VP)],
+    "moe_stage_timer_destroy": [_VP],
+    "moe_stage_timer_read": [_VP, ctypes.POINTER(ctypes.c_float)],
+    "moe_layer_forward_timed": [_PP] + [_VP] * 18 + [ctypes.c_size_t, _VP, _VP],
+    "moe_layer_launch_count": [_PP, ctypes.POINTER(ctypes.c_int32)],
+    "moe_plan_info": [_PP, ctypes.POINTER(ctypes.c_int32)],
+}
+STAGES = ("router", "permute", "gate_up", "down", "shared", "combine")
+EXPORTS = tuple(_SIGS)
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m routed_expert_ffn_gemm_gb300.build`")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, args in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int32
+        lib.moe_status_string.restype = ctypes.c_char_p
+        lib.moe_last_cuda_error.restype = ctypes.c_char_p
+        _LIB = lib
+    return _LIB
+
+
+def problem(T, d, ffn, E, k, ffn_shared=0, act="bf16", wfmt="bf16") -> moe_problem:
+    return moe_problem(T, d, ffn, E, k, ffn_shared, DTYPE[act], DTYPE[wfmt])
+
+
+def problem_of(shape) -> moe_problem:
+    """moe_problem of an ``inputs.MoEShape``."""
+    return problem(shape.T, shape.d, shape.ffn, shape.E, shape.k, shape.ffn_shared, shape.act, shape.wfmt)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("the library takes device tensors")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _call(name, *args):
+    st = getattr(_lib(), name)(*args)
+    if st != OK:
+        raise MoEError(name, st)
+
+
+def moe_router_topk(p, x, w_router, router_bias, logits_in, logits_out, topk_idx, topk_w, stream=None):
+    _call("moe_router_topk", ctypes.byref(p), _ptr(x), _ptr(w_router), _ptr(router_bias),
+          _ptr(logits_in), _ptr(logits_out), _ptr(topk_idx), _ptr(topk_w), _stream(stream))
+
+
+def moe_permute(p, topk_idx, x, counts, offsets, perm_token, inv_row, x_perm, workspace, stream=None):
+    _call("moe_permute", ctypes.byref(p), _ptr(topk_idx), _ptr(x), _ptr(counts), _ptr(offsets),
+          _ptr(perm_token), _ptr(inv_row), _ptr(x_perm), _ptr(workspace),
+          0 if workspace is None else workspace.numel() * workspace.element_size(), _stream(stream))
+
+
+def moe_grouped_swiglu(p, x_perm, offsets, w_gate, w_up, w_down, s_gate, s_up, s_down, y_perm,
+                       workspace, stream=None):
+    _call("moe_grouped_swiglu", ctypes.byref(p), _ptr(x_perm), _ptr(offsets), _ptr(w_gate), _ptr(w_up),
+          _ptr(w_down), _ptr(s_gate), _ptr(s_up), _ptr(s_down), _ptr(y_perm), _ptr(workspace),
+          0 if workspace is None else workspace.numel() * workspace.element_size(), _stream(stream))
+
+
+def moe_combine(p, y_perm, inv_row, topk_w, shared_out, out, stream=None):
+    _call("moe_combine", ctypes.byref(p), _ptr(y_perm), _ptr(inv_row), _ptr(topk_w), _ptr(shared_out),
+          _ptr(out), _stream(stream))
+
+
+def moe_layer_forward(p, x, w_router, router_bias, w_gate, w_up, w_down, s_gate, s_up, s_down,
+                      w_shared_gate, w_shared_up, w_shared_down, out, topk_idx_out, topk_w_out,
+                      counts_out, workspace, stream=None):
+    _call("moe_layer_forward", ctypes.byref(p), _ptr(x), _ptr(w_router), _ptr(router_bias), _ptr(w_gate),
+          _ptr(w_up), _ptr(w_down), _ptr(s_gate), _ptr(s_up), _ptr(s_down), _ptr(w_shared_gate),
+          _ptr(w_shared_up), _ptr(w_shared_down), _ptr(out), _ptr(topk_idx_out), _ptr(topk_w_out),
+          _ptr(counts_out), _ptr(workspace),
+          0 if workspace is None else workspace.numel() * workspace.element_size(), _stream(stream))
+
+
+def moe_layer_forward_timed(p, x, w_router, router_bias, w_gate, w_up, w_down, s_gate, s_up, s_down,
+                            w_shared_gate, w_shared_up, w_shared_down, out, topk_idx_out, topk_w_out,
+                            counts_out, workspace, timer, stream=None):
+    _call("moe_layer_forward_timed", ctypes.byref(p), _ptr(x), _ptr(w_router), _ptr(router_bias),
+          _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(s_gate), _ptr(s_up), _ptr(s_down),
+          _ptr(w_shared_gate), _ptr(w_shared_up), _ptr(w_shared_down), _ptr(out), _ptr(topk_idx_out),
+          _ptr(topk_w_out), _ptr(counts_out), _ptr(workspace),
+          0 if workspace is None else workspace.numel() * workspace.element_size(), _stream(stream),
+          timer.handle)
+
+
+class StageTimer:
+    """moe_stage_timer: CUDA events between the stages of one layer call."""
+
+    def __init__(self):
+        h = ctypes.c_void_p(None)
+        _call("moe_stage_timer_create", ctypes.byref(h))
+        self.handle = h
+
+    def read(self):
+        """{stage: milliseconds} of the last timed call (waits for it)."""
+        ms = (ctypes.c_float * len(STAGES))()
+        _call("moe_stage_timer_read", self.handle, ms)
+        return dict(zip(STAGES, (float(v) for v in ms)))
+
+    def close(self):
+        if self.handle is not None:
+            _lib().moe_stage_timer_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def moe_layer_launch_count(p) -> int:
+    n = ctypes.c_int32(0)
+    _call("moe_layer_launch_count", ctypes.byref(p), ctypes.byref(n))
+    return int(n.value)
+
+
+def moe_plan_info(p) -> dict:
+    info = (ctypes.c_int32 * 4)()
+    _call("moe_plan_info", ctypes.byref(p), info)
+    return {"bn_gateup": info[0], "bn_down": info[1], "splits_down": info[2], "grid": info[3]}
+
+
+def moe_workspace_size(p) -> int:
+    n = ctypes.c_size_t(0)
+    _call("moe_workspace_size", ctypes.byref(p), ctypes.byref(n))
+    return int(n.value)
+
+
+def moe_read_device_status(stream=None) -> int:
+    v = ctypes.c_int32(0)
+    _call("moe_read_device_status", _stream(stream), ctypes.byref(v))
+    return int(v.value)
+
+
+def moe_status_string(status: int) -> str:
+    return _lib().moe_status_string(int(status)).decode()
+
+
+def moe_abi_version() -> int:
+    return int(_lib().moe_abi_version())
+
+
+def moe_selftest_bounded_wait(timeout_ns: int, stream=None):
+    _call("moe_selftest_bounded_wait", int(timeout_ns), _stream(stream))
+
+
+# ---------------------------------------------------------------------------
+# conveniences over the C calls (allocation through torch)
+# ---------------------------------------------------------------------------
+
+def workspace_for(p, device="cuda") -> torch.Tensor:
+    """A device workspace of moe_workspace_size(p) bytes (16-byte aligned)."""
+    return torch.empty(max(16, moe_workspace_size(p)), dtype=torch.uint8, device=device)
+
+
+def layer_forward(p, case, out=None, workspace=None, want_routing=False, stream=None, timer=None):
+    """moe_layer_forward (or moe_layer_forward_timed when a StageTimer is
+    given) on a case dict (``inputs.make_case`` keys)."""
+    x = case["x"]
+    if out is None:
+        out = torch.empty_like(x)
+    if workspace is None:
+        workspace = workspace_for(p, x.device)
+    idx = w = counts = None
+    if want_routing:
+        idx = torch.empty((p.T, p.k), dtype=torch.int32, device=x.device)
+        w = torch.empty((p.T, p.k), dtype=torch.float32, device=x.device)
+        counts = torch.empty((p.E,), dtype=torch.int32, device=x.device)
+    args = (p, x, case["w_router"], case["router_bias"], case["w_gate"], case["w_up"],
+            case["w_down"], case["s_gate"], case["s_up"], case["s_down"],
+            case["w_shared_gate"], case["w_shared_up"], case["w_shared_down"], out,
+            idx, w, counts, workspace)
+    if timer is None:
+        moe_layer_forward(*args, stream=stream)
+    else:
+        moe_layer_forward_timed(*args, timer, stream=stream)
+    return (out, idx, w, counts) if want_routing else out

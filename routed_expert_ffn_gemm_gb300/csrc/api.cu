@@ -1,0 +1,409 @@
+// C-ABI entry points: host-side validation, workspace layout, and the
+// launch sequence of the layer forward ("MOE推理流程解析", section 三 and
+// section 十一: routing, token permutation, grouped expert compute, combine,
+// unpermutation; every stage on one GPU, section 二).
+#include <stdlib.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+size_t act_bytes(int dt) { return dt == MOE_F32 ? 4 : 2; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Which compute path a problem takes.
+enum class Path { kSimt, kTensor };
+
+moe_status check_problem(const moe_problem* p, Path* path) {
+  if (p == nullptr) return MOE_ERR_INVALID_ARG;
+  if (p->T < 0 || p->d <= 0 || p->ffn <= 0 || p->E <= 0 || p->k <= 0 || p->ffn_shared < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (p->k > p->E) return MOE_ERR_INVALID_ARG;
+  if (p->k > 32 || p->E > 1024) return MOE_ERR_UNSUPPORTED;
+  if (p->d % 8 != 0 || p->ffn % 8 != 0 || p->ffn_shared % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)p->T * p->k > (1 << 24)) return MOE_ERR_UNSUPPORTED;
+  if (p->act_dtype == MOE_F32 && p->w_dtype == MOE_F32) {
+    *path = Path::kSimt;
+  } else if (p->act_dtype == MOE_BF16 && (p->w_dtype == MOE_BF16 || p->w_dtype == MOE_FP8_E4M3)) {
+    if (p->d % 128 != 0 || p->ffn % 128 != 0 || p->ffn_shared % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    if (p->w_dtype == MOE_FP8_E4M3) return MOE_ERR_UNSUPPORTED;
+    *path = Path::kTensor;
+  } else {
+    return MOE_ERR_UNSUPPORTED;
+  }
+  return router_topk_check(p->d, p->E, p->act_dtype);
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct Layout {
+  size_t idx, w, logits, counts, offsets, perm_token, inv_row, chunk, x_perm, h, y;
+  size_t sh_offsets, sh_h, sh_y, total;
+  TcPlan plan, sh_plan;
+};
+
+// Workspace of moe_layer_forward (a superset of what the other entry points
+// need).  `splits` may be forced to 1 (standalone grouped entry point).
+Layout layout(const moe_problem& p, Path path, int num_sms, bool allow_splits) {
+  Layout L{};
+  const size_t T = p.T, k = p.k, E = p.E, R = T * k, d = p.d, f = p.ffn, ab = act_bytes(p.act_dtype);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align256(off + (bytes ? bytes : 1));
+    return o;
+  };
+  if (path == Path::kTensor) {
+    L.plan = tc_plan(p.T, p.k, p.E, p.d, p.ffn, num_sms, p.w_dtype);
+    if (!allow_splits) L.plan.splits_down = 1;
+    if (p.ffn_shared) {
+      L.sh_plan = tc_plan(p.T, 1, 1, p.d, p.ffn_shared, num_sms, MOE_BF16);
+      L.sh_plan.splits_down = 1;
+    }
+  }
+  L.idx = take(R * 4);
+  L.w = take(R * 4);
+  L.logits = take(T * E * 4);
+  L.counts = take(E * 4);
+  L.offsets = take((E + 1) * 4);
+  L.perm_token = take(R * 4);
+  L.inv_row = take(R * 4);
+  L.chunk = take(permute_scratch_bytes(p.T, p.k, p.E));
+  L.x_perm = take(R * d * ab);
+  L.h = take(R * f * ab);
+  const size_t S = path == Path::kTensor ? (size_t)L.plan.splits_down : 1;
+  L.y = take(S > 1 ? S * R * d * 4 : R * d * ab);
+  L.sh_offsets = take(8);
+  L.sh_h = take(T * (size_t)p.ffn_shared * ab);
+  L.sh_y = take(p.ffn_shared ? T * d * ab : 0);
+  L.total = off;
+  return L;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+__global__ void set_pair_kernel(int32_t* p, int a, int b) {
+  p[0] = a;
+  p[1] = b;
+}
+
+long long wait_limit_ns() {
+  static long long v = [] {
+    const char* s = getenv("MOE_WAIT_LIMIT_NS");
+    const long long x = s ? atoll(s) : 0;
+    return x > 0 ? x : kDefaultWaitNs;
+  }();
+  return v;
+}
+
+// Grouped SwiGLU over `G` groups of rows, dispatched by path.
+moe_status run_grouped(Path path, int R, int d, int ffn, int G, int w_dtype, const void* x_rows,
+                       const int32_t* offsets, const void* wg, const void* wu, const void* wd,
+                       const float* sg, const float* su, const float* sd, void* h, void* y,
+                       const TcPlan& plan, int* status, cudaStream_t s, cudaEvent_t mid) {
+  if (path == Path::kSimt) {
+    SimtGroupedArgs a{R, d, ffn, G, static_cast<const float*>(x_rows), offsets,
+                      static_cast<const float*>(wg), static_cast<const float*>(wu),
+                      static_cast<const float*>(wd), static_cast<float*>(h), static_cast<float*>(y),
+                      status};
+    return simt_grouped_launch(a, s, mid);
+  }
+  TcGroupedArgs a{R, d, ffn, G, w_dtype, x_rows, offsets, wg, wu, wd, sg, su, sd, h, y, status,
+                  wait_limit_ns()};
+  return tc_grouped_launch(a, plan, s, mid);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+moe_status moe_workspace_size(const moe_problem* p, size_t* bytes) {
+  if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+  Path path;
+  MOE_TRY(check_problem(p, &path));
+  DeviceCtx ctx;
+  MOE_TRY(device_ctx(&ctx));
+  *bytes = layout(*p, path, ctx.num_sms, true).total;
+  return MOE_OK;
+}
+
+moe_status moe_router_topk(const moe_problem* p, const void* x, const void* w_router,
+                           const float* router_bias, const float* logits_in, float* logits_out,
+                           int32_t* topk_idx, float* topk_w, moe_stream_t stream) {
+  Path path;
+  MOE_TRY(check_problem(p, &path));
+  if (topk_idx == nullptr || topk_w == nullptr) return MOE_ERR_INVALID_ARG;
+  if (logits_in != nullptr && router_bias != nullptr) return MOE_ERR_INVALID_ARG;
+  if (logits_in == nullptr && (x == nullptr || w_router == nullptr)) return MOE_ERR_INVALID_ARG;
+  if ((x && !aligned16(x)) || (w_router && !aligned16(w_router))) return MOE_ERR_INVALID_ARG;
+  if (p->T == 0) return MOE_OK;
+  RouterArgs a{p->T, p->d, p->E, p->k, p->act_dtype, x, w_router, router_bias, logits_in,
+               logits_out, topk_idx, topk_w};
+  return router_topk_launch(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_permute(const moe_problem* p, const int32_t* topk_idx, const void* x,
+                       int32_t* counts, int32_t* offsets, int32_t* perm_token, int32_t* inv_row,
+                       void* x_perm, void* workspace, size_t workspace_bytes,
+                       moe_stream_t stream) {
+  Path path;
+  MOE_TRY(check_problem(p, &path));
+  if (counts == nullptr || offsets == nullptr || perm_token == nullptr || inv_row == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (p->T > 0 && topk_idx == nullptr) return MOE_ERR_INVALID_ARG;
+  if ((x_perm != nullptr) != (x != nullptr)) return MOE_ERR_INVALID_ARG;
+  if ((x && !aligned16(x)) || (x_perm && !aligned16(x_perm))) return MOE_ERR_INVALID_ARG;
+  const size_t scratch = permute_scratch_bytes(p->T, p->k, p->E);
+  if (scratch > 0 && (workspace == nullptr || workspace_bytes < scratch)) return MOE_ERR_WORKSPACE;
+  DeviceCtx ctx;
+  MOE_TRY(device_ctx(&ctx));
+  PermuteArgs a{p->T, p->k, p->E, p->d, (int)act_bytes(p->act_dtype), topk_idx, x, counts,
+                offsets, perm_token, inv_row, x_perm, static_cast<int32_t*>(workspace),
+                ctx.status};
+  return permute_launch(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_grouped_swiglu(const moe_problem* p, const void* x_perm, const int32_t* offsets,
+                              const void* w_gate, const void* w_up, const void* w_down,
+                              const float* s_gate, const float* s_up, const float* s_down,
+                              void* y_perm, void* workspace, size_t workspace_bytes,
+                              moe_stream_t stream) {
+  Path path;
+  MOE_TRY(check_problem(p, &path));
+  if (p->T == 0) return MOE_OK;
+  if (!x_perm || !offsets || !w_gate || !w_up || !w_down || !y_perm) return MOE_ERR_INVALID_ARG;
+  for (const void* q : {x_perm, w_gate, w_up, w_down, (const void*)y_perm})
+    if (!aligned16(q)) return MOE_ERR_INVALID_ARG;
+  const bool fp8 = p->w_dtype == MOE_FP8_E4M3;
+  if (fp8 != (s_gate != nullptr) || fp8 != (s_up != nullptr) || fp8 != (s_down != nullptr))
+    return MOE_ERR_INVALID_ARG;
+  DeviceCtx ctx;
+  MOE_TRY(device_ctx(&ctx));
+  const Layout L = layout(*p, path, ctx.num_sms, false);
+  const size_t R = (size_t)p->T * p->k;
+  const size_t need = align256(R * p->ffn * act_bytes(p->act_dtype));
+  if (workspace == nullptr || workspace_bytes < need) return MOE_ERR_WORKSPACE;
+  return run_grouped(path, (int)R, p->d, p->ffn, p->E, p->w_dtype, x_perm, offsets, w_gate, w_up,
+                     w_down, s_gate, s_up, s_down, workspace, y_perm, L.plan, ctx.status,
+                     reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+moe_status moe_combine(const moe_problem* p, const void* y_perm, const int32_t* inv_row,
+                       const float* topk_w, const void* shared_out, void* out,
+                       moe_stream_t stream) {
+  Path path;
+  MOE_TRY(check_problem(p, &path));
+  if (p->T == 0) return MOE_OK;
+  if (!y_perm || !inv_row || !topk_w || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y_perm) || !aligned16(out) || (shared_out && !aligned16(shared_out)))
+    return MOE_ERR_INVALID_ARG;
+  CombineArgs a{p->T, p->k, p->d, p->act_dtype, y_perm, 0, inv_row, topk_w, shared_out, out};
+  return combine_launch(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"
+
+struct moe_stage_timer {
+  cudaEvent_t ev[MOE_NUM_STAGES + 1];
+  int recorded;
+};
+
+namespace moe {
+namespace {
+
+moe_status layer_forward_impl(const moe_problem* p, const void* x, const void* w_router,
+                              const float* router_bias, const void* w_gate, const void* w_up,
+                              const void* w_down, const float* s_gate, const float* s_up,
+                              const float* s_down, const void* w_shared_gate,
+                              const void* w_shared_up, const void* w_shared_down, void* out,
+                              int32_t* topk_idx_out, float* topk_w_out, int32_t* counts_out,
+                              void* workspace, size_t workspace_bytes, moe_stream_t stream,
+                              moe_stage_timer* timer) {
+  Path path;
+  MOE_TRY(check_problem(p, &path));
+  if (p->T == 0) return MOE_OK;
+  if (!x || !w_router || !w_gate || !w_up || !w_down || !out) return MOE_ERR_INVALID_ARG;
+  for (const void* q : {x, w_router, w_gate, w_up, w_down, (const void*)out})
+    if (!aligned16(q)) return MOE_ERR_INVALID_ARG;
+  const bool fp8 = p->w_dtype == MOE_FP8_E4M3;
+  if (fp8 != (s_gate != nullptr) || fp8 != (s_up != nullptr) || fp8 != (s_down != nullptr))
+    return MOE_ERR_INVALID_ARG;
+  const bool has_shared = p->ffn_shared > 0;
+  if (has_shared != (w_shared_gate != nullptr) || has_shared != (w_shared_up != nullptr) ||
+      has_shared != (w_shared_down != nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (has_shared && (!aligned16(w_shared_gate) || !aligned16(w_shared_up) || !aligned16(w_shared_down)))
+    return MOE_ERR_INVALID_ARG;
+  DeviceCtx ctx;
+  MOE_TRY(device_ctx(&ctx));
+  const Layout L = layout(*p, path, ctx.num_sms, true);
+  if (workspace == nullptr || workspace_bytes < L.total || !aligned16(workspace))
+    return MOE_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int R = p->T * p->k;
+  auto mark = [&](int i) -> moe_status {
+    if (timer != nullptr) {
+      MOE_TRY_CUDA(cudaEventRecord(timer->ev[i], s));
+      timer->recorded = i + 1;
+    }
+    return MOE_OK;
+  };
+
+  int32_t* idx = topk_idx_out ? topk_idx_out : at<int32_t>(workspace, L.idx);
+  float* w = topk_w_out ? topk_w_out : at<float>(workspace, L.w);
+  int32_t* counts = counts_out ? counts_out : at<int32_t>(workspace, L.counts);
+  int32_t* offsets = at<int32_t>(workspace, L.offsets);
+  int32_t* perm_token = at<int32_t>(workspace, L.perm_token);
+  int32_t* inv_row = at<int32_t>(workspace, L.inv_row);
+  void* x_perm = at<uint8_t>(workspace, L.x_perm);
+  void* h = at<uint8_t>(workspace, L.h);
+  void* y = at<uint8_t>(workspace, L.y);
+
+  MOE_TRY(mark(0));
+  // 1. router: logits, softmax, top-k, renormalised weights
+  RouterArgs ra{p->T, p->d, p->E, p->k, p->act_dtype, x, w_router, router_bias, nullptr,
+                at<float>(workspace, L.logits), idx, w};
+  MOE_TRY(router_topk_launch(ra, s));
+  MOE_TRY(mark(1));
+  // 2. permutation: counts, offsets, row maps, x -> x_perm
+  PermuteArgs pa{p->T, p->k, p->E, p->d, (int)act_bytes(p->act_dtype), idx, x, counts, offsets,
+                 perm_token, inv_row, x_perm, at<int32_t>(workspace, L.chunk), ctx.status};
+  MOE_TRY(permute_launch(pa, s));
+  MOE_TRY(mark(2));
+  // 3. grouped SwiGLU experts (gate/up + SiLU*mul, then down)
+  MOE_TRY(run_grouped(path, R, p->d, p->ffn, p->E, p->w_dtype, x_perm, offsets, w_gate, w_up,
+                      w_down, s_gate, s_up, s_down, h, y, L.plan, ctx.status, s,
+                      timer ? timer->ev[3] : nullptr));
+  MOE_TRY(mark(4));
+  // 4. shared expert: every token, weight 1 (one group holding all T rows)
+  void* sh_y = nullptr;
+  if (has_shared) {
+    int32_t* sh_off = at<int32_t>(workspace, L.sh_offsets);
+    set_pair_kernel<<<1, 1, 0, s>>>(sh_off, 0, p->T);
+    MOE_TRY_CUDA(cudaGetLastError());
+    sh_y = at<uint8_t>(workspace, L.sh_y);
+    MOE_TRY(run_grouped(path, p->T, p->d, p->ffn_shared, 1, p->act_dtype, x, sh_off,
+                        w_shared_gate, w_shared_up, w_shared_down, nullptr, nullptr, nullptr,
+                        at<uint8_t>(workspace, L.sh_h), sh_y, L.sh_plan, ctx.status, s, nullptr));
+  }
+  MOE_TRY(mark(5));
+  // 5. combine: inverse map, routing weights, sum (+ shared expert)
+  const int partials = path == Path::kTensor && L.plan.splits_down > 1 ? L.plan.splits_down : 0;
+  CombineArgs ca{p->T, p->k, p->d, p->act_dtype, y, partials, inv_row, w, sh_y, out};
+  MOE_TRY(combine_launch(ca, s));
+  return mark(6);
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" {
+
+moe_status moe_layer_forward(const moe_problem* p, const void* x, const void* w_router,
+                             const float* router_bias, const void* w_gate, const void* w_up,
+                             const void* w_down, const float* s_gate, const float* s_up,
+                             const float* s_down, const void* w_shared_gate,
+                             const void* w_shared_up, const void* w_shared_down, void* out,
+                             int32_t* topk_idx_out, float* topk_w_out, int32_t* counts_out,
+                             void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  return layer_forward_impl(p, x, w_router, router_bias, w_gate, w_up, w_down, s_gate, s_up,
+                            s_down, w_shared_gate, w_shared_up, w_shared_down, out, topk_idx_out,
+                            topk_w_out, counts_out, workspace, workspace_bytes, stream, nullptr);
+}
+
+moe_status moe_layer_forward_timed(const moe_problem* p, const void* x, const void* w_router,
+                                   const float* router_bias, const void* w_gate, const void* w_up,
+                                   const void* w_down, const float* s_gate, const float* s_up,
+                                   const float* s_down, const void* w_shared_gate,
+                                   const void* w_shared_up, const void* w_shared_down, void* out,
+                                   int32_t* topk_idx_out, float* topk_w_out, int32_t* counts_out,
+                                   void* workspace, size_t workspace_bytes, moe_stream_t stream,
+                                   moe_stage_timer* timer) {
+  if (timer == nullptr) return MOE_ERR_INVALID_ARG;
+  timer->recorded = 0;
+  return layer_forward_impl(p, x, w_router, router_bias, w_gate, w_up, w_down, s_gate, s_up,
+                            s_down, w_shared_gate, w_shared_up, w_shared_down, out, topk_idx_out,
+                            topk_w_out, counts_out, workspace, workspace_bytes, stream, timer);
+}
+
+moe_status moe_stage_timer_create(moe_stage_timer** timer) {
+  if (timer == nullptr) return MOE_ERR_INVALID_ARG;
+  moe_stage_timer* t = new moe_stage_timer();
+  for (int i = 0; i <= MOE_NUM_STAGES; ++i) {
+    cudaError_t e = cudaEventCreate(&t->ev[i]);
+    if (e != cudaSuccess) {
+      for (int j = 0; j < i; ++j) cudaEventDestroy(t->ev[j]);
+      delete t;
+      return cuda_status(e);
+    }
+  }
+  t->recorded = 0;
+  *timer = t;
+  return MOE_OK;
+}
+
+moe_status moe_stage_timer_destroy(moe_stage_timer* timer) {
+  if (timer == nullptr) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i <= MOE_NUM_STAGES; ++i) cudaEventDestroy(timer->ev[i]);
+  delete timer;
+  return MOE_OK;
+}
+
+moe_status moe_stage_timer_read(moe_stage_timer* timer, float* ms) {
+  if (timer == nullptr || ms == nullptr) return MOE_ERR_INVALID_ARG;
+  if (timer->recorded != MOE_NUM_STAGES + 1) return MOE_ERR_INVALID_ARG;
+  MOE_TRY_CUDA(cudaEventSynchronize(timer->ev[MOE_NUM_STAGES]));
+  for (int i = 0; i < MOE_NUM_STAGES; ++i)
+    MOE_TRY_CUDA(cudaEventElapsedTime(&ms[i], timer->ev[i], timer->ev[i + 1]));
+  return MOE_OK;
+}
+
+moe_status moe_plan_info(const moe_problem* p, int32_t* info) {
+  if (info == nullptr) return MOE_ERR_INVALID_ARG;
+  Path path;
+  MOE_TRY(check_problem(p, &path));
+  info[0] = info[1] = info[2] = info[3] = 0;
+  if (path != Path::kTensor) return MOE_OK;
+  DeviceCtx ctx;
+  MOE_TRY(device_ctx(&ctx));
+  const Layout L = layout(*p, path, ctx.num_sms, true);
+  info[0] = L.plan.bn_gateup;
+  info[1] = L.plan.bn_down;
+  info[2] = L.plan.splits_down;
+  info[3] = L.plan.grid;
+  return MOE_OK;
+}
+
+moe_status moe_layer_launch_count(const moe_problem* p, int32_t* launches) {
+  if (launches == nullptr) return MOE_ERR_INVALID_ARG;
+  Path path;
+  MOE_TRY(check_problem(p, &path));
+  if (p->T == 0) {
+    *launches = 0;
+    return MOE_OK;
+  }
+  int n = router_launch_count(p->T, p->E, false, true);
+  n += permute_launch_count(p->T, p->k, true);
+  n += 2;                        // gate/up, down
+  if (p->ffn_shared > 0) n += 3;  // offsets, gate/up, down
+  n += 1;                        // combine
+  *launches = n;
+  return MOE_OK;
+}
+
+moe_status moe_selftest_bounded_wait(int64_t timeout_ns, moe_stream_t stream) {
+  if (timeout_ns <= 0) return MOE_ERR_INVALID_ARG;
+  DeviceCtx ctx;
+  MOE_TRY(device_ctx(&ctx));
+  return tc_selftest_launch(ctx.status, timeout_ns, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,155 @@
+// Internal declarations shared by the translation units of libmoe_gb300.so.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// host-side context
+// ---------------------------------------------------------------------------
+
+struct DeviceCtx {
+  int device = -1;
+  int num_sms = 0;
+  int* status = nullptr;  // device address of this device's status word
+};
+
+// Current device, its SM count and status-word address (cached per device).
+moe_status device_ctx(DeviceCtx* ctx);
+
+// Remember the text of a failed CUDA call for moe_last_cuda_error().
+void record_cuda_error(cudaError_t err);
+void record_cuda_error_text(const char* text);
+
+inline moe_status cuda_status(cudaError_t err) {
+  if (err == cudaSuccess) return MOE_OK;
+  record_cuda_error(err);
+  return MOE_ERR_CUDA;
+}
+
+#define MOE_TRY_CUDA(expr)                                   \
+  do {                                                       \
+    cudaError_t _e = (expr);                                 \
+    if (_e != cudaSuccess) return ::moe::cuda_status(_e);    \
+  } while (0)
+
+#define MOE_TRY(expr)                                        \
+  do {                                                       \
+    moe_status _s = (expr);                                  \
+    if (_s != MOE_OK) return _s;                             \
+  } while (0)
+
+// 2-D row-major tensor map for TMA: `rows` x `cols` elements of
+// `elem_bytes`, row pitch `cols * elem_bytes`, box `box_cols` x `box_rows`,
+// 128-byte swizzle, zero fill out of bounds.
+moe_status make_tmap_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                        int elem_bytes, uint32_t box_rows, uint32_t box_cols);
+
+// ---------------------------------------------------------------------------
+// device-side status word
+// ---------------------------------------------------------------------------
+
+// Record the first error of a kernel (the status word keeps the first one).
+__device__ __forceinline__ void set_device_status(int* status, int code) {
+  if (status != nullptr) atomicCAS(status, 0, code);
+}
+
+// ---------------------------------------------------------------------------
+// kernel launchers (each in its own translation unit)
+// ---------------------------------------------------------------------------
+
+struct RouterArgs {
+  int T, d, E, k, act_dtype;
+  const void* x;
+  const void* w_router;
+  const float* bias;
+  const float* logits_in;
+  float* logits_out;
+  int32_t* idx;
+  float* w;
+};
+moe_status router_topk_launch(const RouterArgs& a, cudaStream_t s);
+moe_status router_topk_check(int d, int E, int act_dtype);
+int router_launch_count(int T, int E, bool logits_in, bool logits_out);
+
+struct PermuteArgs {
+  int T, k, E, d, act_bytes;
+  const int32_t* idx;
+  const void* x;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* perm_token;
+  int32_t* inv_row;
+  void* x_perm;
+  int32_t* chunk_scratch;  // [n_chunks * E] when the chunked path is used
+  int* status;
+};
+size_t permute_scratch_bytes(int T, int k, int E);
+int permute_launch_count(int T, int k, bool move_rows);
+moe_status permute_launch(const PermuteArgs& a, cudaStream_t s);
+
+struct CombineArgs {
+  int T, k, d, act_dtype;
+  const void* y;           // y_perm [R, d] act dtype, or fp32 partials
+  int y_partials;          // 0: y is act dtype [R, d]; S>0: fp32 [S, R, d]
+  const int32_t* inv_row;
+  const float* w;
+  const void* shared;      // [T, d] act dtype or nullptr
+  void* out;
+};
+moe_status combine_launch(const CombineArgs& a, cudaStream_t s);
+
+// fp32 CUDA-core grouped SwiGLU (both GEMMs, fp32 accumulation).
+struct SimtGroupedArgs {
+  int R, d, ffn, E;
+  const float* x_perm;
+  const int32_t* offsets;
+  const float* w_gate;
+  const float* w_up;
+  const float* w_down;
+  float* h;       // [R, ffn] scratch
+  float* y;       // [R, d]
+  int* status;
+};
+// `mid` (nullable): event recorded between the gate/up and the down kernels.
+moe_status simt_grouped_launch(const SimtGroupedArgs& a, cudaStream_t s, cudaEvent_t mid);
+
+// tcgen05 grouped GEMM (bf16 or FP8 weights, bf16 activations).
+struct TcPlan {
+  int bn_gateup;       // max rows per tile in the gate/up GEMM
+  int bn_down;         // max rows per tile in the down GEMM
+  int splits_down;     // K splits of the down GEMM (1 = direct bf16 output)
+  int grid;            // persistent CTAs
+};
+struct TcGroupedArgs {
+  int R, d, ffn, G;    // rows, hidden, intermediate, groups (experts)
+  int w_dtype;         // MOE_BF16 or MOE_FP8_E4M3
+  const void* x_perm;  // [R, d] bf16 (B operand of gate/up)
+  const int32_t* offsets;
+  const void* w_gate;
+  const void* w_up;
+  const void* w_down;
+  const float* s_gate;
+  const float* s_up;
+  const float* s_down;
+  void* h;             // [R, ffn] bf16 scratch
+  void* y;             // [R, d] bf16 when splits_down == 1, else fp32 [S, R, d]
+  int* status;
+  long long timeout_ns;
+};
+TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype);
+moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStream_t s,
+                             cudaEvent_t mid);
+moe_status tc_selftest_launch(int* status, long long timeout_ns, cudaStream_t s);
+
+// Default limit of every bounded wait inside a kernel (nanoseconds).
+constexpr long long kDefaultWaitNs = 2000000000LL;
+
+}  // namespace moe

@@ -1,0 +1,240 @@
+// Router: logits l = x W_r^T (+ b) in fp32, then softmax / top-k /
+// renormalisation per token ("MOE推理流程解析", section 三: the router
+// scores every eligible expert, top-k keeps the chosen indices and weights;
+// section 九: the kept weights are re-normalised).
+//
+// router_kernel: a block owns TT = 8 tokens, whose rows are staged once in
+// shared memory, and a slice of the experts; each warp accumulates EPW
+// experts x 8 tokens with 16-byte loads of W_r rows (fp32 FMA) and a shuffle
+// reduction.  With one expert slice (gridDim.y == 1, "fused") the logits stay
+// in shared memory and the same block selects the top-k; with several slices
+// (few tokens: more blocks stream W_r) the logits go to global memory and
+// topk_kernel follows.
+//
+// Selection: k rounds of a warp arg-max over the E logits (larger logit
+// first, ties to the lower expert index).  Weights: exp(l_j - l_max) / sum
+// over the kept set, which equals p_j / sum_{kept} p with p = softmax over
+// all E (the full-softmax denominator cancels).  Slots are in selection
+// order, i.e. descending weight.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kTT = 8;  // tokens per block
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ void load16(const float* p, float (&v)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+}
+__device__ __forceinline__ void load16(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 a = *reinterpret_cast<const uint4*>(p);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&a);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h[i]);
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
+}
+template <typename T> struct VecN { static constexpr int N = 16 / sizeof(T); };
+
+// (v1, e1) ranks before (v2, e2): larger logit, ties to the lower index.
+__device__ __forceinline__ bool ranks_before(float v1, int e1, float v2, int e2) {
+  return v1 > v2 || (v1 == v2 && e1 < e2);
+}
+
+// One warp: top-k of one token's logits row (shared or global memory).
+__device__ void topk_row(const float* row, int E, int k, int32_t* idx_out, float* w_out) {
+  const int lane = threadIdx.x & 31;
+  const int per_lane = (E + 31) / 32;  // <= 32
+  uint32_t taken = 0;                  // bit i: expert lane + 32*i already chosen
+  float my_v = 0.f;
+  int my_e = 0;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int be = E;  // E = no candidate
+    for (int i = 0; i < per_lane; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u)) {
+        const float v = row[e];
+        if (ranks_before(v, e, bv, be)) { bv = v; be = e; }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (ranks_before(ov, oe, bv, be)) { bv = ov; be = oe; }
+    }
+    if (be >= E) {  // only NaN logits remain: take the lowest unchosen expert
+      int le = E;
+      for (int i = 0; i < per_lane; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !((taken >> i) & 1u)) { le = e; break; }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) le = min(le, __shfl_xor_sync(0xffffffffu, le, o));
+      be = le;
+      bv = row[be];
+    }
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    if (lane == j) { my_v = bv; my_e = be; }
+  }
+  const float vmax = __shfl_sync(0xffffffffu, my_v, 0);
+  const float ex = lane < k ? expf(my_v - vmax) : 0.f;
+  float s = ex;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane < k) {
+    idx_out[lane] = my_e;
+    w_out[lane] = ex / s;
+  }
+}
+
+template <typename ActT, int EPW>
+__global__ void __launch_bounds__(kThreads) router_kernel(
+    int T, int d, int E, int k, const ActT* __restrict__ x, const ActT* __restrict__ wr,
+    const float* __restrict__ bias, const float* __restrict__ logits_in,
+    float* __restrict__ logits_out, int32_t* __restrict__ idx, float* __restrict__ w) {
+  constexpr int VN = VecN<ActT>::N;
+  extern __shared__ __align__(16) uint8_t sm[];
+  const bool fused = gridDim.y == 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = blockIdx.x * kTT;
+  ActT* xs = reinterpret_cast<ActT*>(sm);                                   // [TT][d]
+  float* ls = reinterpret_cast<float*>(sm + (logits_in ? 0 : sizeof(ActT) * kTT * d));  // [TT][E]
+
+  if (logits_in == nullptr) {
+    const int vec_per_row = d / VN;
+    for (int v = threadIdx.x; v < kTT * vec_per_row; v += kThreads) {
+      const int t = v / vec_per_row, c = (v % vec_per_row) * VN;
+      uint4 val = make_uint4(0, 0, 0, 0);
+      if (t0 + t < T) val = *reinterpret_cast<const uint4*>(x + (size_t)(t0 + t) * d + c);
+      *reinterpret_cast<uint4*>(xs + (size_t)t * d + c) = val;
+    }
+    __syncthreads();
+    const int slice = ((E + gridDim.y - 1) / gridDim.y + EPW - 1) / EPW * EPW;
+    const int e_lo = blockIdx.y * slice, e_hi = min(E, e_lo + slice);
+    for (int eb = e_lo + warp * EPW; eb < e_hi; eb += 8 * EPW) {
+      float acc[EPW][kTT];
+#pragma unroll
+      for (int a = 0; a < EPW; ++a)
+#pragma unroll
+        for (int t = 0; t < kTT; ++t) acc[a][t] = 0.f;
+      for (int i = lane * VN; i < d; i += 32 * VN) {
+        float xv[kTT][8];
+#pragma unroll
+        for (int t = 0; t < kTT; ++t) load16(xs + (size_t)t * d + i, xv[t]);
+#pragma unroll
+        for (int a = 0; a < EPW; ++a) {
+          if (eb + a < e_hi) {
+            float wv[8];
+            load16(wr + (size_t)(eb + a) * d + i, wv);
+#pragma unroll
+            for (int t = 0; t < kTT; ++t)
+#pragma unroll
+              for (int q = 0; q < VN; ++q) acc[a][t] = fmaf(wv[q], xv[t][q], acc[a][t]);
+          }
+        }
+      }
+#pragma unroll
+      for (int a = 0; a < EPW; ++a) {
+        const int e = eb + a;
+#pragma unroll
+        for (int t = 0; t < kTT; ++t) {
+          float v = acc[a][t];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          if (lane == 0 && e < e_hi) {
+            v += bias != nullptr ? bias[e] : 0.f;
+            if (fused) ls[t * E + e] = v;
+            if (logits_out != nullptr && t0 + t < T) logits_out[(size_t)(t0 + t) * E + e] = v;
+          }
+        }
+      }
+    }
+  } else {
+    for (int i = threadIdx.x; i < kTT * E; i += kThreads) {
+      const int t = i / E;
+      ls[i] = t0 + t < T ? logits_in[(size_t)t0 * E + i] : 0.f;
+    }
+  }
+  if (!fused) return;
+  __syncthreads();
+  const int t = t0 + warp;  // 8 warps <-> 8 tokens
+  if (t < T) topk_row(ls + warp * E, E, k, idx + (size_t)t * k, w + (size_t)t * k);
+}
+
+__global__ void __launch_bounds__(kThreads) topk_kernel(int T, int E, int k,
+                                                        const float* __restrict__ logits,
+                                                        int32_t* __restrict__ idx,
+                                                        float* __restrict__ w) {
+  const int t = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+  if (t < T) topk_row(logits + (size_t)t * E, E, k, idx + (size_t)t * k, w + (size_t)t * k);
+}
+
+// Few token tiles and a global logits buffer available: split the experts
+// over more blocks (one expert per warp), then a separate top-k pass.
+bool use_split(int T, int E, bool logits_in, bool scratch) {
+  const int tiles = (T + kTT - 1) / kTT;
+  return !logits_in && scratch && tiles <= 16 && E > 8;
+}
+
+template <typename ActT>
+moe_status launch_typed(const RouterArgs& a, float* logits_scratch, cudaStream_t s) {
+  const int tiles = (a.T + kTT - 1) / kTT;
+  const size_t xs_bytes = a.logits_in ? 0 : sizeof(ActT) * kTT * a.d;
+  const bool split = use_split(a.T, a.E, a.logits_in != nullptr, logits_scratch != nullptr);
+  if (split) {
+    auto kern = router_kernel<ActT, 1>;
+    MOE_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)xs_bytes));
+    dim3 grid(tiles, (a.E + 7) / 8);
+    kern<<<grid, kThreads, xs_bytes, s>>>(a.T, a.d, a.E, a.k, static_cast<const ActT*>(a.x),
+                                          static_cast<const ActT*>(a.w_router), a.bias, nullptr,
+                                          logits_scratch, a.idx, a.w);
+    MOE_TRY_CUDA(cudaGetLastError());
+    topk_kernel<<<(a.T + 7) / 8, kThreads, 0, s>>>(a.T, a.E, a.k, logits_scratch, a.idx, a.w);
+    MOE_TRY_CUDA(cudaGetLastError());
+    return MOE_OK;
+  }
+  const size_t smem = xs_bytes + sizeof(float) * kTT * a.E;
+  if (smem > 220 * 1024) return MOE_ERR_UNSUPPORTED;
+  auto kern = router_kernel<ActT, 4>;
+  MOE_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  kern<<<dim3(tiles, 1), kThreads, smem, s>>>(a.T, a.d, a.E, a.k, static_cast<const ActT*>(a.x),
+                                              static_cast<const ActT*>(a.w_router), a.bias,
+                                              a.logits_in, a.logits_out, a.idx, a.w);
+  MOE_TRY_CUDA(cudaGetLastError());
+  if (a.logits_in != nullptr && a.logits_out != nullptr && a.logits_out != a.logits_in)
+    MOE_TRY_CUDA(cudaMemcpyAsync(a.logits_out, a.logits_in, sizeof(float) * a.T * a.E,
+                                 cudaMemcpyDeviceToDevice, s));
+  return MOE_OK;
+}
+
+}  // namespace
+
+int router_launch_count(int T, int E, bool logits_in, bool logits_out) {
+  return use_split(T, E, logits_in, logits_out) ? 2 : 1;
+}
+
+moe_status router_topk_check(int d, int E, int act_dtype) {
+  if (E > 1024) return MOE_ERR_UNSUPPORTED;
+  if (act_dtype != MOE_F32 && act_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (d % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  const size_t act = act_dtype == MOE_F32 ? 4 : 2;
+  if (act * kTT * d + sizeof(float) * kTT * E > 220 * 1024) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status router_topk_launch(const RouterArgs& a, cudaStream_t s) {
+  if (a.T == 0) return MOE_OK;
+  MOE_TRY(router_topk_check(a.d, a.E, a.act_dtype));
+  // a caller-visible logits_out doubles as the split path's global buffer
+  float* scratch = a.logits_out;
+  if (a.act_dtype == MOE_BF16) return launch_typed<__nv_bfloat16>(a, scratch, s);
+  return launch_typed<float>(a, scratch, s);
+}
+
+}  // namespace moe

@@ -1,0 +1,378 @@
+"""GPU parity: every entry point of the C-ABI library against the CPU
+reference, element by element, on seeded inputs.
+
+Bars (written in each test):
+  routing indices, counts, offsets, permutation maps, row moves: bit-exact;
+  routing weights: fp32 rounding (rtol 2e-6 given the same fp32 logits);
+  layer / expert outputs: max|err| <= 2e-2 * max|ref| for bf16 storage,
+  <= 1e-4 * max|ref| for fp32 storage.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from routed_expert_ffn_gemm_gb300 import api, build, inputs
+from tests import helpers
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+BF16_TOL = 2e-2
+F32_TOL = 1e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    build.build()
+    api._lib()
+    yield
+    assert api.moe_read_device_status() == 0, "a kernel recorded an error"
+
+
+def _bf16_rand(shape, std, gen):
+    return (torch.randn(shape, generator=gen, device=DEV) * std).to(torch.bfloat16)
+
+
+def _f64(t):
+    return helpers.decode_act(t, "bf16" if t.dtype == torch.bfloat16 else "f32")
+
+
+# ---------------------------------------------------------------------------
+# router
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("T,E,k", [(64, 8, 2), (300, 128, 8), (257, 256, 8), (33, 4, 4), (5, 1024, 32),
+                                   (1, 8, 1), (16, 8, 8)])
+def test_router_topk_bit_exact_given_oracle_logits(T, E, k):
+    rng = np.random.default_rng(T * 1000 + E + k)
+    for _ in range(50):  # reject near-ties below 1e-6 (several answers would be valid)
+        lg = rng.normal(size=(T, E)).astype(np.float32).astype(np.float64)
+        if helpers.routing_gap_ok(lg, k, 1e-6):
+            break
+    idx_ref, w_ref = oracle.topk_renorm(lg, k)
+    p = api.problem(T, 128, 128, E, k)
+    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    w = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    api.moe_router_topk(p, None, None, None, torch.from_numpy(lg.astype(np.float32)).to(DEV), None, idx, w)
+    torch.cuda.synchronize()
+    assert np.array_equal(idx.cpu().numpy(), idx_ref)
+    np.testing.assert_allclose(w.cpu().numpy(), w_ref, rtol=2e-6, atol=1e-7)
+
+
+def test_router_exact_ties_go_to_lower_index():
+    lg = np.array([[1.0, 3.0, 3.0, 0.0, 3.0, -1.0, 3.0, 2.0]] * 9, dtype=np.float32)
+    p = api.problem(9, 128, 128, 8, 3)
+    idx = torch.empty((9, 3), dtype=torch.int32, device=DEV)
+    w = torch.empty((9, 3), dtype=torch.float32, device=DEV)
+    api.moe_router_topk(p, None, None, None, torch.from_numpy(lg).to(DEV), None, idx, w)
+    idx_ref, w_ref = oracle.topk_renorm(lg.astype(np.float64), 3)
+    assert np.array_equal(idx.cpu().numpy(), idx_ref)
+    assert idx_ref[0].tolist() == [1, 2, 4]
+    np.testing.assert_allclose(w.cpu().numpy(), w_ref, rtol=2e-6)
+
+
+@pytest.mark.parametrize("act,T,d,E,k", [("bf16", 40, 512, 16, 4), ("bf16", 3, 2048, 128, 8), ("f32", 64, 128, 8, 2),
+                                         ("bf16", 200, 7168, 256, 8), ("bf16", 64, 4096, 8, 2)])
+def test_router_logits_and_choice(act, T, d, E, k):
+    g = torch.Generator(device=DEV).manual_seed(T + d + E)
+    dt = torch.bfloat16 if act == "bf16" else torch.float32
+    x = torch.randn((T, d), generator=g, device=DEV).to(dt)
+    wr = (torch.randn((E, d), generator=g, device=DEV) / d ** 0.5).to(dt)
+    bias = torch.randn((E,), generator=g, device=DEV) * 0.1
+    p = api.problem(T, d, 128, E, k, act=act, wfmt=act)
+    logits = torch.empty((T, E), dtype=torch.float32, device=DEV)
+    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    w = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    api.moe_router_topk(p, x, wr, bias, None, logits, idx, w)
+    torch.cuda.synchronize()
+    ref = oracle.router_logits(_f64(x), _f64(wr), bias.double().cpu().numpy())
+    lg = logits.cpu().numpy().astype(np.float64)
+    # fp32 accumulation of d products: |err| <= 1e-5 * max|l|
+    assert np.abs(lg - ref).max() <= 1e-5 * np.abs(ref).max()
+    # the choice is exactly the oracle's top-k of the GPU's own logits
+    idx_g, w_g = oracle.topk_renorm(lg, k)
+    assert np.array_equal(idx.cpu().numpy(), idx_g)
+    np.testing.assert_allclose(w.cpu().numpy(), w_g, rtol=2e-6, atol=1e-7)
+    # and the oracle's choice on its own logits wherever the decision is clear
+    idx_r, _ = oracle.topk_renorm(ref, k)
+    clear = oracle.topk_gap(ref, k) >= 1e-3
+    assert np.array_equal(idx.cpu().numpy()[clear], idx_r[clear])
+
+
+# ---------------------------------------------------------------------------
+# the worked example (page "MOE推理流程解析", section 二)
+# ---------------------------------------------------------------------------
+
+def test_worked_example_through_router_and_permute():
+    g, idx_ref, w_ref, groups = helpers.worked_example()
+    T, E, k = g["T"], g["E"], g["k"]
+    lg = helpers.worked_example_logits(idx_ref, w_ref, E).astype(np.float32)
+    p = api.problem(T, 128, 128, E, k)
+    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    w = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    api.moe_router_topk(p, None, None, None, torch.from_numpy(lg).to(DEV), None, idx, w)
+    counts = torch.empty(E, dtype=torch.int32, device=DEV)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    perm = torch.empty(T * k, dtype=torch.int32, device=DEV)
+    inv = torch.empty(T * k, dtype=torch.int32, device=DEV)
+    api.moe_permute(p, idx, None, counts, offsets, perm, inv, None, None)
+    torch.cuda.synchronize()
+    assert idx.cpu().numpy().tolist() == idx_ref.tolist()
+    np.testing.assert_allclose(w.cpu().numpy(), w_ref, rtol=1e-6)
+    assert counts.cpu().tolist() == g["rows_per_expert"] == [3, 2, 2, 1]
+    assert offsets.cpu().tolist() == [0, 3, 5, 7, 8]
+    pt = perm.cpu().numpy()
+    for e in range(E):
+        assert pt[offsets[e]:offsets[e + 1]].tolist() == groups[e]
+    assert inv.cpu().numpy().reshape(T, k).tolist() == [[0, 5], [6, 1], [2, 3], [4, 7]]
+
+
+# ---------------------------------------------------------------------------
+# permutation
+# ---------------------------------------------------------------------------
+
+def _random_idx(T, E, k, rng, skew=False):
+    if skew:
+        p = 1.0 / np.arange(1, E + 1) ** 1.2
+        p /= p.sum()
+        return np.stack([rng.choice(E, k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+    return np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+
+
+@pytest.mark.parametrize("T,E,k,skew", [(1, 8, 2, False), (64, 8, 2, False), (128, 128, 8, False),
+                                        (256, 8, 8, False), (257, 8, 8, False), (1000, 64, 6, True),
+                                        (8192, 128, 8, True), (4096, 256, 8, False), (3, 1024, 32, False)])
+def test_permute_bit_exact(T, E, k, skew):
+    rng = np.random.default_rng(T + E + k)
+    idx = _random_idx(T, E, k, rng, skew)
+    counts_r, offsets_r, perm_r, inv_r = oracle.permutation_maps(idx, E)
+    d = 128
+    g = torch.Generator(device=DEV).manual_seed(T)
+    x = _bf16_rand((T, d), 1.0, g)
+    p = api.problem(T, d, 128, E, k)
+    ws = api.workspace_for(p)
+    counts = torch.empty(E, dtype=torch.int32, device=DEV)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    perm = torch.empty(T * k, dtype=torch.int32, device=DEV)
+    inv = torch.empty(T * k, dtype=torch.int32, device=DEV)
+    x_perm = torch.empty((T * k, d), dtype=torch.bfloat16, device=DEV)
+    api.moe_permute(p, torch.from_numpy(idx).to(DEV), x, counts, offsets, perm, inv, x_perm, ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(counts.cpu().numpy(), counts_r)
+    assert np.array_equal(offsets.cpu().numpy(), offsets_r)
+    assert np.array_equal(perm.cpu().numpy(), perm_r)
+    assert np.array_equal(inv.cpu().numpy().reshape(T, k), inv_r)
+    assert torch.equal(x_perm.cpu(), x.cpu()[torch.from_numpy(perm_r.astype(np.int64))])
+
+
+def test_permute_flags_out_of_range_expert():
+    T, E, k = 16, 8, 2
+    idx = _random_idx(T, E, k, np.random.default_rng(0))
+    idx[5, 1] = E  # invalid
+    p = api.problem(T, 128, 128, E, k)
+    counts = torch.empty(E, dtype=torch.int32, device=DEV)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    perm = torch.empty(T * k, dtype=torch.int32, device=DEV)
+    inv = torch.empty(T * k, dtype=torch.int32, device=DEV)
+    api.moe_permute(p, torch.from_numpy(idx).to(DEV), None, counts, offsets, perm, inv, None, None)
+    assert api.moe_read_device_status() == api.ERR_DEVICE_BOUNDS
+    assert int(counts.sum()) == T * k - 1
+    assert api.moe_read_device_status() == 0  # reading cleared it
+
+
+# ---------------------------------------------------------------------------
+# combine
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("act", ["bf16", "f32"])
+def test_combine_matches_definition(act):
+    T, k, d = 37, 4, 256
+    R = T * k
+    rng = np.random.default_rng(5)
+    dt = torch.bfloat16 if act == "bf16" else torch.float32
+    g = torch.Generator(device=DEV).manual_seed(5)
+    y = torch.randn((R, d), generator=g, device=DEV).to(dt)
+    sh = torch.randn((T, d), generator=g, device=DEV).to(dt)
+    inv = rng.permutation(R).astype(np.int32)
+    w = rng.uniform(0.1, 1.0, size=(T, k))
+    w = (w / w.sum(1, keepdims=True)).astype(np.float32)
+    out = torch.empty((T, d), dtype=dt, device=DEV)
+    p = api.problem(T, d, 128, 8, k, act=act, wfmt=act)
+    api.moe_combine(p, y, torch.from_numpy(inv).to(DEV), torch.from_numpy(w).to(DEV), sh, out)
+    torch.cuda.synchronize()
+    yf, sf = _f64(y), _f64(sh)
+    ref = (w.astype(np.float64)[:, :, None] * yf[inv.reshape(T, k)]).sum(1) + sf
+    got = _f64(out)
+    bound = (2.0 ** -8 if act == "bf16" else 1e-6) * np.abs(ref) + 1e-6 * np.abs(ref).max()
+    assert np.all(np.abs(got - ref) <= bound)
+
+
+# ---------------------------------------------------------------------------
+# grouped SwiGLU experts
+# ---------------------------------------------------------------------------
+
+GROUP_COUNTS = {
+    "ragged": [0, 1, 15, 16, 17, 31, 32, 33, 100, 127, 128, 129, 0, 300, 2, 5],
+    "decode": [1, 0, 2, 1, 0, 0, 1, 3, 0, 1, 2, 1, 0, 0, 1, 1],
+    "one_hot_expert": [0] * 7 + [517] + [0] * 8,
+}
+
+
+@pytest.mark.parametrize("kind", sorted(GROUP_COUNTS))
+@pytest.mark.parametrize("d,f", [(256, 384), (128, 256)])
+def test_grouped_swiglu_tensor_path(kind, d, f):
+    counts = np.array(GROUP_COUNTS[kind])
+    E = len(counts)
+    R = int(counts.sum())
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    g = torch.Generator(device=DEV).manual_seed(R + d)
+    x = _bf16_rand((R, d), 1.0, g)
+    wg, wu = _bf16_rand((E, f, d), d ** -0.5, g), _bf16_rand((E, f, d), d ** -0.5, g)
+    wd = _bf16_rand((E, d, f), d ** -0.5, g)
+    p = api.problem(R, d, f, E, 1)
+    y = torch.full((R, d), float("nan"), dtype=torch.bfloat16, device=DEV)
+    ws = api.workspace_for(p)
+    api.moe_grouped_swiglu(p, x, torch.from_numpy(offsets).to(DEV), wg, wu, wd, None, None, None, y, ws)
+    torch.cuda.synchronize()
+    got = _f64(y)
+    xf = _f64(x)
+    ref = np.zeros_like(got)
+    for e in range(E):
+        a, b = offsets[e], offsets[e + 1]
+        if b > a:
+            ref[a:b] = oracle.swiglu_expert(xf[a:b], _f64(wg[e]), _f64(wu[e]), _f64(wd[e]))
+    assert np.isfinite(got).all()
+    assert np.abs(got - ref).max() <= BF16_TOL * np.abs(ref).max()
+    # tighter statistical check: bf16 rounding of h and y only
+    assert np.sqrt(((got - ref) ** 2).mean()) <= 1e-2 * np.sqrt((ref ** 2).mean())
+
+
+# ---------------------------------------------------------------------------
+# whole layer
+# ---------------------------------------------------------------------------
+
+def _layer_check(shape, seed, tol, tokens=None, clear_gap=1e-3):
+    case = inputs.make_case(shape, seed, DEV)
+    p = api.problem_of(shape)
+    out, idx, w, counts = api.layer_forward(p, case, want_routing=True)
+    torch.cuda.synchronize()
+    x, wr, b, ew, sh = helpers.oracle_inputs(case, shape)
+    lg = oracle.router_logits(x, wr, b)
+    idx_r, w_r = oracle.topk_renorm(lg, shape.k)
+    idx_g = idx.cpu().numpy()
+    clear = oracle.topk_gap(lg, shape.k) >= clear_gap
+    # routing: bit-exact wherever the decision is not a near-tie
+    assert np.array_equal(idx_g[clear], idx_r[clear])
+    np.testing.assert_allclose(w.cpu().numpy()[clear], w_r[clear], rtol=1e-4, atol=1e-6)
+    cnt_g = counts.cpu().numpy()
+    assert cnt_g.sum() == shape.T * shape.k
+    assert np.array_equal(cnt_g, np.bincount(idx_g.ravel(), minlength=shape.E))
+    # output: the oracle's layer under the GPU's (verified) routing
+    sel = np.arange(shape.T) if tokens is None else np.asarray(tokens)
+    ref, _, _ = oracle.moe_forward_per_token(x, wr, ew, shape.k, bias=b, shared=sh,
+                                             routing=(idx_g, w.cpu().numpy().astype(np.float64)),
+                                             tokens=sel)
+    got = helpers.decode_act(out, shape.act)[sel]
+    assert np.isfinite(got).all()
+    err = np.abs(got - ref).max()
+    assert err <= tol * np.abs(ref).max(), f"max|err| {err:.3g} vs max|ref| {np.abs(ref).max():.3g}"
+    return case
+
+
+def test_layer_toy_f32():
+    shape = inputs.WORKLOADS["toy_f32"]
+    seed = helpers.seed_without_near_ties(shape, 0, min_gap=1e-4)
+    _layer_check(shape, seed, F32_TOL, clear_gap=1e-4)
+
+
+def test_worked_example_combine_on_gpu():
+    # the page: T1 -> 0.7 * E1(T1) + 0.3 * E3(T1); run the layer's grouped
+    # expert and combine entry points on the worked example's routing
+    g, idx_ref, w_ref, groups = helpers.worked_example()
+    T, E, k = g["T"], g["E"], g["k"]
+    d, f = 128, 128
+    gen = torch.Generator(device=DEV).manual_seed(11)
+    x = _bf16_rand((T, d), 1.0, gen)
+    wg, wu, wd = (_bf16_rand((E, f, d), d ** -0.5, gen), _bf16_rand((E, f, d), d ** -0.5, gen),
+                  _bf16_rand((E, d, f), d ** -0.5, gen))
+    p = api.problem(T, d, f, E, k)
+    ws = api.workspace_for(p)
+    idx_t = torch.from_numpy(idx_ref).to(DEV)
+    counts = torch.empty(E, dtype=torch.int32, device=DEV)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    perm = torch.empty(T * k, dtype=torch.int32, device=DEV)
+    inv = torch.empty(T * k, dtype=torch.int32, device=DEV)
+    x_perm = torch.empty((T * k, d), dtype=torch.bfloat16, device=DEV)
+    y = torch.empty((T * k, d), dtype=torch.bfloat16, device=DEV)
+    out = torch.empty((T, d), dtype=torch.bfloat16, device=DEV)
+    api.moe_permute(p, idx_t, x, counts, offsets, perm, inv, x_perm, ws)
+    api.moe_grouped_swiglu(p, x_perm, offsets, wg, wu, wd, None, None, None, y, ws)
+    api.moe_combine(p, y, inv, torch.from_numpy(w_ref.astype(np.float32)).to(DEV), None, out)
+    torch.cuda.synchronize()
+    xf = _f64(x)
+    c = g["combine"]["T1"]
+    e1 = oracle.swiglu_expert(xf[:1], _f64(wg[0]), _f64(wu[0]), _f64(wd[0]))[0]
+    e3 = oracle.swiglu_expert(xf[:1], _f64(wg[2]), _f64(wu[2]), _f64(wd[2]))[0]
+    ref = c["E1"] * e1 + c["E3"] * e3
+    got = _f64(out)[0]
+    assert np.abs(got - ref).max() <= BF16_TOL * np.abs(ref).max()
+
+
+@pytest.mark.parametrize("T,d,f,E,k", [(300, 256, 384, 16, 4), (7, 128, 256, 8, 2), (1, 256, 128, 4, 4),
+                                       (2100, 128, 128, 32, 1)])
+def test_layer_bf16_small_multi_tile(T, d, f, E, k):
+    shape = inputs.MoEShape("small", T=T, d=d, ffn=f, E=E, k=k)
+    _layer_check(shape, 1, BF16_TOL)
+
+
+@pytest.mark.parametrize("T", [1, 8, 32, 64])
+def test_layer_mixtral_shaped(T):
+    _layer_check(inputs.WORKLOADS["mixtral_8x7b"].with_T(T), 0, BF16_TOL)
+
+
+@pytest.mark.parametrize("T", [1, 16, 128])
+def test_layer_qwen3_30b_a3b_shaped_decode(T):
+    _layer_check(inputs.WORKLOADS["qwen3_30b_a3b"].with_T(T), 0, BF16_TOL)
+
+
+def test_layer_qwen3_30b_a3b_shaped_prefill_sampled():
+    shape = inputs.WORKLOADS["qwen3_30b_a3b_prefill"]
+    tokens = np.linspace(0, shape.T - 1, 48).astype(int)
+    case = _layer_check(shape, 0, BF16_TOL, tokens=tokens)
+    # the skewed load reached the device: hottest expert holds several times the mean
+    p = api.problem_of(shape)
+    _, _, _, counts = api.layer_forward(p, case, want_routing=True)
+    c = counts.cpu().numpy()
+    assert c.max() / c.mean() > 4.0
+
+
+def test_layer_empty_batch():
+    shape = inputs.WORKLOADS["qwen3_30b_a3b"].with_T(0)
+    case = inputs.make_weights(shape, 0, DEV)
+    case["x"] = torch.empty((0, shape.d), dtype=torch.bfloat16, device=DEV)
+    out = api.layer_forward(api.problem_of(shape), case, out=torch.empty((0, shape.d), dtype=torch.bfloat16, device=DEV),
+                            workspace=torch.empty(16, dtype=torch.uint8, device=DEV))
+    assert out.shape == (0, shape.d)
+
+
+def test_workspace_too_small_is_rejected():
+    shape = inputs.MoEShape("small", T=8, d=128, ffn=128, E=4, k=2)
+    case = inputs.make_case(shape, 0, DEV)
+    p = api.problem_of(shape)
+    with pytest.raises(api.MoEError) as e:
+        api.layer_forward(p, case, workspace=torch.empty(64, dtype=torch.uint8, device=DEV))
+    assert e.value.status == api.ERR_WORKSPACE
+
+
+# ---------------------------------------------------------------------------
+# failure detection: a bounded wait that expires
+# ---------------------------------------------------------------------------
+
+def test_bounded_wait_expires_cleanly_and_context_survives():
+    api.moe_selftest_bounded_wait(2_000_000)  # 2 ms on a barrier nothing arrives at
+    assert api.moe_read_device_status() == api.ERR_DEVICE_TIMEOUT
+    assert api.moe_read_device_status() == 0
+    # the context is still usable: a normal layer runs and matches
+    shape = inputs.MoEShape("small", T=20, d=128, ffn=256, E=8, k=2)
+    _layer_check(shape, 3, BF16_TOL)

@@ -1,0 +1,92 @@
+"""The C-ABI library loads and exports every entry point include/moe.h
+declares; host-side argument validation answers without a GPU (no compute
+call is made here)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from routed_expert_ffn_gemm_gb300 import api, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return api._lib()
+
+
+def declared_entry_points():
+    with open(os.path.join(ROOT, "include", "moe.h")) as f:
+        text = f.read()
+    return re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", text)
+
+
+def test_header_declares_the_boundary():
+    names = set(declared_entry_points())
+    for n in ("moe_router_topk", "moe_permute", "moe_grouped_swiglu", "moe_combine", "moe_layer_forward",
+              "moe_workspace_size", "moe_read_device_status", "moe_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_entry_points()
+    assert names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/moe.h but not exported"
+    assert set(names) == set(api.EXPORTS), "binding and header disagree"
+
+
+def test_abi_version_and_status_strings(lib):
+    assert api.moe_abi_version() == 1
+    assert api.moe_status_string(0) == "MOE_OK"
+    assert api.moe_status_string(api.ERR_DEVICE_TIMEOUT) == "MOE_ERR_DEVICE_TIMEOUT"
+    assert api.moe_status_string(-99) == "MOE_ERR_UNKNOWN"
+
+
+def _ws_status(lib, p):
+    n = ctypes.c_size_t(0)
+    return lib.moe_workspace_size(ctypes.byref(p), ctypes.byref(n))
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(T=4, d=128, ffn=256, E=4, k=5), api.ERR_INVALID_ARG),          # k > E
+    (dict(T=-1, d=128, ffn=256, E=4, k=2), api.ERR_INVALID_ARG),         # negative T
+    (dict(T=4, d=0, ffn=256, E=4, k=2), api.ERR_INVALID_ARG),            # empty hidden
+    (dict(T=4, d=128, ffn=256, E=2048, k=2), api.ERR_UNSUPPORTED),       # E > 1024
+    (dict(T=4, d=100, ffn=256, E=8, k=2, act="f32", wfmt="f32"), api.ERR_UNSUPPORTED),   # d % 8
+    (dict(T=4, d=192, ffn=256, E=8, k=2), api.ERR_UNSUPPORTED),          # tensor path: d % 128
+    (dict(T=4, d=128, ffn=256, E=8, k=2, act="f32", wfmt="bf16"), api.ERR_UNSUPPORTED),  # mixed
+    (dict(T=4, d=128, ffn=256, E=40, k=33), api.ERR_UNSUPPORTED),        # k > 32
+])
+def test_problem_validation_without_gpu(lib, kw, want):
+    assert _ws_status(lib, api.problem(**kw)) == want
+
+
+def test_null_pointers_rejected_before_any_launch(lib):
+    p = api.problem(T=4, d=128, ffn=256, E=8, k=2, act="f32", wfmt="f32")
+    # topk outputs missing
+    assert lib.moe_router_topk(ctypes.byref(p), None, None, None, None, None, None, None, None) == api.ERR_INVALID_ARG
+    # x_perm requested without x
+    assert lib.moe_permute(ctypes.byref(p), None, None, None, None, None, None, None, None, 0, None) == api.ERR_INVALID_ARG
+    assert lib.moe_combine(ctypes.byref(p), None, None, None, None, None, None) == api.ERR_INVALID_ARG
+    assert lib.moe_layer_forward(ctypes.byref(p), *([None] * 18), 0, None) == api.ERR_INVALID_ARG
+
+
+def test_empty_batch_is_a_no_op(lib):
+    p = api.problem(T=0, d=128, ffn=256, E=8, k=2)
+    ws = ctypes.c_size_t(0)
+    # T == 0 returns OK before any launch, even with null tensors
+    assert lib.moe_grouped_swiglu(ctypes.byref(p), *([None] * 10), 0, None) == 0
+    assert lib.moe_combine(ctypes.byref(p), None, None, None, None, None, None) == 0
+    assert lib.moe_layer_forward(ctypes.byref(p), *([None] * 18), 0, None) == 0
+    del ws
+
+
+def test_misaligned_pointer_rejected(lib):
+    p = api.problem(T=4, d=128, ffn=256, E=8, k=2)
+    fake = ctypes.c_void_p(0x1000 + 8)  # never dereferenced: rejected on the host
+    assert lib.moe_combine(ctypes.byref(p), fake, fake, fake, None, fake, None) == api.ERR_INVALID_ARG
