@@ -162,6 +162,9 @@ class ClockSampler:
 
 
 def dist_setup(args):
+    """One process per GPU (torchrun env).  The ranks are independent
+    replicas; the process group only carries the timing barrier and the
+    max-over-ranks reduction."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -182,9 +185,17 @@ def max_over_ranks(v, ws, device):
     if ws == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dev = device if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_tokens_per_s(ms_this_rank, ws, steps, tokens_per_step, device):
+    """Units all ranks processed / the slowest rank's time (weak scaling:
+    each rank runs `steps` steps of `tokens_per_step` tokens)."""
+    ms = max_over_ranks(ms_this_rank, ws, device)
+    return ws * steps * tokens_per_step / (ms / 1e3), ms
 
 
 # ---------------------------------------------------------------------------
@@ -354,10 +365,8 @@ def run_ours(args, shape, ws, rank, local):
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(ws)
-    ms = e0.elapsed_time(e1)
     sampler.stop()
-    ms = max_over_ranks(ms, ws, device)
-    value = ws * args.steps * shape.T / (ms / 1e3)
+    value, ms = whole_job_tokens_per_s(e0.elapsed_time(e1), ws, args.steps, shape.T, device)
 
     # ---- per-stage device times (events on the launching stream)
     ks = min(args.stage_steps, args.steps)

@@ -49,13 +49,7 @@ F64 = np.float64
 # Storage formats, decoded from their definitions
 # ---------------------------------------------------------------------------
 
-def decode_bf16(bits) -> np.ndarray:
-    """bfloat16 bit patterns (uint16) -> float64.
-
-    bfloat16 is the upper half of an IEEE-754 binary32: 1 sign bit, 8 exponent
-    bits (bias 127), 7 fraction bits.  Exponent 0 encodes zero / subnormals
-    (value = fraction/128 * 2^-126), exponent 255 encodes inf / NaN.
-    """
+def _bf16_formula(bits) -> np.ndarray:
     b = np.asarray(bits).astype(np.int64) & 0xFFFF
     sign = np.where((b >> 15) & 1, -1.0, 1.0)
     exp = (b >> 7) & 0xFF
@@ -67,14 +61,18 @@ def decode_bf16(bits) -> np.ndarray:
     return out.astype(F64)
 
 
-def decode_e4m3(bits) -> np.ndarray:
-    """OCP FP8 E4M3 ("fn" flavour) bit patterns (uint8) -> float64.
+def decode_bf16(bits) -> np.ndarray:
+    """bfloat16 bit patterns (uint16) -> float64.
 
-    1 sign bit, 4 exponent bits (bias 7), 3 fraction bits.  Exponent 0 encodes
-    zero / subnormals (value = fraction/8 * 2^-6).  There are no infinities:
-    exponent 15 with fraction 7 is NaN, every other code is finite, so the
-    largest magnitude is 2^8 * 1.75 = 448.
+    bfloat16 is the upper half of an IEEE-754 binary32: 1 sign bit, 8 exponent
+    bits (bias 127), 7 fraction bits.  Exponent 0 encodes zero / subnormals
+    (value = fraction/128 * 2^-126), exponent 255 encodes inf / NaN.
+    The formula is evaluated once for all 65536 patterns, then looked up.
     """
+    return _BF16_TABLE[np.asarray(bits).astype(np.int64) & 0xFFFF]
+
+
+def _e4m3_formula(bits) -> np.ndarray:
     b = np.asarray(bits).astype(np.int64) & 0xFF
     sign = np.where((b >> 7) & 1, -1.0, 1.0)
     exp = (b >> 3) & 0xF
@@ -84,6 +82,23 @@ def decode_e4m3(bits) -> np.ndarray:
     out = np.where(exp == 0, sub, normal)
     out = np.where((exp == 15) & (frac == 7), np.nan, out)
     return out.astype(F64)
+
+
+def decode_e4m3(bits) -> np.ndarray:
+    """OCP FP8 E4M3 ("fn" flavour) bit patterns (uint8) -> float64.
+
+    1 sign bit, 4 exponent bits (bias 7), 3 fraction bits.  Exponent 0 encodes
+    zero / subnormals (value = fraction/8 * 2^-6).  There are no infinities:
+    exponent 15 with fraction 7 is NaN, every other code is finite, so the
+    largest magnitude is 2^8 * 1.75 = 448.
+    The formula is evaluated once for all 256 codes, then looked up.
+    """
+    return _E4M3_TABLE[np.asarray(bits).astype(np.int64) & 0xFF]
+
+
+with np.errstate(invalid="ignore"):
+    _BF16_TABLE = _bf16_formula(np.arange(1 << 16))
+    _E4M3_TABLE = _e4m3_formula(np.arange(1 << 8))
 
 
 def _to_f64(arr, fmt: str) -> np.ndarray:

@@ -52,7 +52,7 @@ _SIGS = {
     "moe_permute": [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t, _VP],
     "moe_grouped_swiglu": [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t, _VP],
     "moe_combine": [_PP, _VP, _VP, _VP, _VP, _VP, _VP],
-    "moe_layer_forward": [_PP] + [_VP] * 18 + [ctypes.c_size_t, _VP],
+    "moe_layer_forward": [_PP] + [_VP] * 17 + [ctypes.c_size_t, _VP],
     "moe_workspace_size": [_PP, ctypes.POINTER(ctypes.c_size_t)],
     "moe_read_device_status": [_VP, ctypes.POINTER(ctypes.c_int32)],
     "moe_status_string": [ctypes.c_int32],
@@ -62,7 +62,7 @@ _SIGS = {
     "moe_stage_timer_create": [ctypes.POINTER(_VP)],
     "moe_stage_timer_destroy": [_VP],
     "moe_stage_timer_read": [_VP, ctypes.POINTER(ctypes.c_float)],
-    "moe_layer_forward_timed": [_PP] + [_VP] * 18 + [ctypes.c_size_t, _VP, _VP],
+    "moe_layer_forward_timed": [_PP] + [_VP] * 17 + [ctypes.c_size_t, _VP, _VP],
     "moe_layer_launch_count": [_PP, ctypes.POINTER(ctypes.c_int32)],
     "moe_plan_info": [_PP, ctypes.POINTER(ctypes.c_int32)],
 }

@@ -28,7 +28,6 @@ moe_status check_problem(const moe_problem* p, Path* path) {
     *path = Path::kSimt;
   } else if (p->act_dtype == MOE_BF16 && (p->w_dtype == MOE_BF16 || p->w_dtype == MOE_FP8_E4M3)) {
     if (p->d % 128 != 0 || p->ffn % 128 != 0 || p->ffn_shared % 128 != 0) return MOE_ERR_UNSUPPORTED;
-    if (p->w_dtype == MOE_FP8_E4M3) return MOE_ERR_UNSUPPORTED;
     *path = Path::kTensor;
   } else {
     return MOE_ERR_UNSUPPORTED;

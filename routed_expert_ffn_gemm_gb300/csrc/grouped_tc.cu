@@ -24,10 +24,17 @@
 //                   warp 1 also allocates / frees 512 TMEM columns
 //   warps 2..5      epilogue: tcgen05.ld from TMEM, SiLU(g)*u (gate/up) or
 //                   the projection (down), 64/128-byte coalesced stores
+//   warps 6..9      (FP8 weights only) converters: E4M3 tile staged by TMA ->
+//                   bf16 tile in the 128-byte-swizzled layout the MMA reads
 // Accumulators are double-buffered in TMEM (buffer b at column 256*b; gate at
 // +0, up at +128) so the epilogue of one unit overlaps the next unit's loads
 // and MMAs.  Every wait is bounded: on expiry the kernel records
 // MOE_ERR_DEVICE_TIMEOUT, lets issued copies land, frees TMEM and returns.
+//
+// FP8 weights ("MoE 推理部署", section 专家量化: per-expert scales) are
+// dequantised in-kernel: every E4M3 value is exact in bf16, so the MMA runs
+// kind::f16 on the exact weights and the per-output-channel scale (one TMEM
+// lane = one channel) multiplies the fp32 accumulator in the epilogue.
 #include <string.h>
 
 #include "common.cuh"
@@ -39,7 +46,8 @@ namespace {
 constexpr int kBM = 128;          // output channels per tile (MMA M)
 constexpr int kBK = 64;           // reduction elements per stage (128 bytes of bf16)
 constexpr int kBoxN = 16;         // rows per B box
-constexpr int kThreads = 192;
+constexpr int kThreads = 192;          // producer, MMA, 4 epilogue warps
+constexpr int kConvThreads = 128;      // FP8: 4 converter warps
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxGroups = 1024;
 constexpr int kSmemLimit = 232448;  // opt-in maximum dynamic shared memory per block
@@ -58,20 +66,26 @@ struct TcParams {
   int* status;
   long long timeout_ns;
   int selftest;            // 1: issue no copies/MMAs, wait on a barrier nothing arrives at
+  const float* scale0;     // FP8: per-channel scales of A0 / A1 ([G*M])
+  const float* scale1;
 };
 
-template <int MODE, int BN>
+template <int MODE, int BN, bool FP8>
 struct Cfg {
   static constexpr int NA = MODE == kGateUp ? 2 : 1;           // weight operands per stage
-  static constexpr int A_BYTES = kBM * kBK * 2;                // 16 KB
+  static constexpr int A_BYTES = kBM * kBK * 2;                // 16 KB bf16 tile (MMA operand)
   static constexpr int B_BYTES = BN * kBK * 2;
-  static constexpr int STAGE_BYTES = NA * A_BYTES + B_BYTES;   // multiple of 1024
-  static constexpr int TAIL_BYTES = 8 * 24 + 16 + 4 * 2 * (kMaxGroups + 8);
+  static constexpr int STG_BYTES = FP8 ? kBM * kBK : 0;        // 8 KB E4M3 staging tile
+  static constexpr int B_OFF = NA * A_BYTES;
+  static constexpr int STG_OFF = B_OFF + B_BYTES;
+  static constexpr int STAGE_BYTES = STG_OFF + NA * STG_BYTES; // multiple of 1024
+  static constexpr int THREADS = kThreads + (FP8 ? kConvThreads : 0);
+  static constexpr int TAIL_BYTES = 8 * 36 + 16 + 4 * 2 * (kMaxGroups + 8);
   static constexpr int STAGES_FIT = (kSmemLimit - 1024 - TAIL_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 10 ? 10 : STAGES_FIT;
   static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
-  // barriers: full[S], empty[S], acc_full[2], acc_empty[2], drain
-  static constexpr int NBARS = 2 * STAGES + 5;
+  // barriers: full[S], empty[S], conv[S], acc_full[2], acc_empty[2], drain
+  static constexpr int NBARS = 3 * STAGES + 5;
   static constexpr int SLOT_OFF = BAR_OFF + 8 * NBARS;         // TMEM base address
   static constexpr int ABORT_OFF = SLOT_OFF + 8;
   static constexpr int OFFS_OFF = ABORT_OFF + 8;               // int offs[G+1]
@@ -79,6 +93,7 @@ struct Cfg {
   static constexpr int SMEM_BYTES = PREFIX_OFF + 4 * (kMaxGroups + 4) + 1024;
   static_assert(STAGES >= 2, "pipeline too shallow");
   static_assert(SMEM_BYTES <= kSmemLimit, "shared memory budget");
+  static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
   static_assert(BN % kBoxN == 0 && BN <= (MODE == kGateUp ? 128 : 256), "tile rows");
 };
 
@@ -108,12 +123,34 @@ __device__ __forceinline__ Unit decode_unit(int u, const int* offs, const int* p
 
 __device__ __forceinline__ void store_out(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
-template <int MODE, int BN>
-__global__ void __launch_bounds__(kThreads, 1)
+// Two E4M3 values (low byte = first) -> two bf16 (low half = first), exact.
+// The hardware conversion gives f16; every E4M3 value is zero or a normal
+// f16 whose 7 low mantissa bits are zero, so moving the exponent/mantissa
+// fields to bf16 positions and adding the bias difference (127 - 15 = 112)
+// is exact.  Zero halves stay zero.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t v) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(v));
+  const uint32_t mag = (h & 0x7FFF7FFFu) >> 3;
+  const uint32_t nz = __vcmpne2(mag, 0u);
+  return (h & 0x80008000u) | (mag + (0x38003800u & nz));
+}
+
+__device__ __forceinline__ uint4 e4m3x8_to_bf16x8(uint32_t lo, uint32_t hi) {
+  uint4 r;
+  r.x = e4m3x2_to_bf16x2((uint16_t)(lo & 0xFFFFu));
+  r.y = e4m3x2_to_bf16x2((uint16_t)(lo >> 16));
+  r.z = e4m3x2_to_bf16x2((uint16_t)(hi & 0xFFFFu));
+  r.w = e4m3x2_to_bf16x2((uint16_t)(hi >> 16));
+  return r;
+}
+
+template <int MODE, int BN, bool FP8>
+__global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
     tc_grouped_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA0,
                       const __grid_constant__ CUtensorMap tmA1,
                       const __grid_constant__ CUtensorMap tmB) {
-  using C = Cfg<MODE, BN>;
+  using C = Cfg<MODE, BN, FP8>;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = ptx::smem_u32(smem_raw);
@@ -123,9 +160,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bars = sbase + C::BAR_OFF;
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
-  auto accf_bar = [&](int b) { return bars + 8u * (2 * STAGES + b); };
-  auto acce_bar = [&](int b) { return bars + 8u * (2 * STAGES + 2 + b); };
-  const uint32_t drain_bar = bars + 8u * (2 * STAGES + 4);
+  auto conv_bar = [&](int s) { return bars + 8u * (2 * STAGES + s); };
+  auto accf_bar = [&](int b) { return bars + 8u * (3 * STAGES + b); };
+  auto acce_bar = [&](int b) { return bars + 8u * (3 * STAGES + 2 + b); };
+  const uint32_t drain_bar = bars + 8u * (3 * STAGES + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::SLOT_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::ABORT_OFF);
   int* offs = reinterpret_cast<int*>(smem + C::OFFS_OFF);
@@ -138,6 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(full_bar(s), 1);
       ptx::mbar_init(empty_bar(s), 1);
+      ptx::mbar_init(conv_bar(s), kConvThreads / 32);  // one arrival per converter warp
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(accf_bar(b), 1);
@@ -160,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Group row ranges (clamped into [0, R]) and the exclusive prefix of
   // per-group tile counts ceil(rows / BN).
   const int G = p.selftest ? 1 : p.G;
-  for (int g = threadIdx.x; g <= G; g += kThreads) {
+  for (int g = threadIdx.x; g <= G; g += C::THREADS) {
     int o = p.selftest ? 0 : p.offsets[g];
     if (o < 0 || o > p.R) {
       set_device_status(p.status, MOE_ERR_DEVICE_BOUNDS);
@@ -170,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   {
-    const int per = (G + kThreads - 1) / kThreads;
+    const int per = (G + C::THREADS - 1) / C::THREADS;
     const int g0 = min(G, threadIdx.x * per), g1 = min(G, g0 + per);
     int local = 0;
     for (int g = g0; g < g1; ++g) local += (max(0, offs[g + 1] - offs[g]) + BN - 1) / BN;
@@ -180,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += n;
     }
-    __shared__ int warp_sum[kThreads / 32];
+    __shared__ int warp_sum[C::THREADS / 32];
     if (lane == 31) warp_sum[warp] = incl;
     __syncthreads();
     int before = 0;
@@ -190,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefix[g] = run;
       run += (max(0, offs[g + 1] - offs[g]) + BN - 1) / BN;
     }
-    if (threadIdx.x == kThreads - 1) prefix[G] = before + incl;
+    if (threadIdx.x == C::THREADS - 1) prefix[G] = before + incl;
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -218,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Unit x = decode_unit(u, offs, prefix, G, MT, S, BN);
         const int kb0 = x.ks * kb_per_split, kb1 = min(kblocks, kb0 + kb_per_split);
         const int nbox = (x.n_valid + kBoxN - 1) / kBoxN;
-        const uint32_t bytes = C::NA * C::A_BYTES + nbox * kBoxN * kBK * 2;
+        const uint32_t bytes = C::NA * (FP8 ? C::STG_BYTES : C::A_BYTES) + nbox * kBoxN * kBK * 2;
         const int arow = x.g * p.M + x.mt * kBM;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!ptx::mbar_wait_bounded(empty_bar(stage), phase ^ 1u, deadline, abort_flag)) {
@@ -228,9 +267,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
           armed[stage] = (int)phase;
           const uint32_t sa = sbase + stage * C::STAGE_BYTES;
-          ptx::tma_load_2d(sa, &tmA0, full_bar(stage), kb * kBK, arow, pol_w);
-          if (MODE == kGateUp) ptx::tma_load_2d(sa + C::A_BYTES, &tmA1, full_bar(stage), kb * kBK, arow, pol_w);
-          const uint32_t sb = sa + C::NA * C::A_BYTES;
+          // weights: bf16 straight into the MMA tile, or E4M3 into staging
+          const uint32_t wa = FP8 ? sa + C::STG_OFF : sa;
+          const uint32_t wstep = FP8 ? C::STG_BYTES : C::A_BYTES;
+          ptx::tma_load_2d(wa, &tmA0, full_bar(stage), kb * kBK, arow, pol_w);
+          if (MODE == kGateUp) ptx::tma_load_2d(wa + wstep, &tmA1, full_bar(stage), kb * kBK, arow, pol_w);
+          const uint32_t sb = sa + C::B_OFF;
           for (int i = 0; i < nbox; ++i)
             ptx::tma_load_2d(sb + i * kBoxN * kBK * 2, &tmB, full_bar(stage), kb * kBK,
                              x.row0 + i * kBoxN, pol_x);
@@ -278,7 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t d0 = tmem_base + 256u * buf;
           const uint32_t d1 = d0 + 128u;
           for (int kb = kb0; kb < kb1; ++kb) {
-            if (!ptx::mbar_wait_bounded(full_bar(stage), phase, deadline, abort_flag)) {
+            if (!ptx::mbar_wait_bounded(full_bar(stage), phase, deadline, abort_flag) ||
+                (FP8 && !ptx::mbar_wait_bounded(conv_bar(stage), phase, deadline, abort_flag))) {
               ok = false;
               break;
             }
@@ -286,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t sa = sbase + stage * C::STAGE_BYTES;
             const uint64_t da0 = ptx::sdesc_k_sw128(sa);
             const uint64_t da1 = ptx::sdesc_k_sw128(sa + C::A_BYTES);
-            const uint64_t db = ptx::sdesc_k_sw128(sa + C::NA * C::A_BYTES);
+            const uint64_t db = ptx::sdesc_k_sw128(sa + C::B_OFF);
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk) {
               const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
@@ -314,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else {
+  } else if (warp < kThreads / 32) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     const int ch_local = q * 32 + lane;
@@ -337,6 +380,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + 256u * buf;
       const int ch = x.mt * kBM + ch_local;
       const int n_mma = ((x.n_valid + 15) / 16) * 16;
+      const float sc0 = FP8 ? p.scale0[(size_t)x.g * p.M + ch] : 1.f;
+      const float sc1 = FP8 && MODE == kGateUp ? p.scale1[(size_t)x.g * p.M + ch] : 1.f;
       for (int c0 = 0; c0 < n_mma; c0 += 16) {
         uint32_t ra[16];
         ptx::tmem_ld16(taddr + c0, ra);
@@ -348,8 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             if (c0 + j < x.n_valid) {
-              const float g = __uint_as_float(ra[j]);
-              const float v = g / (1.f + __expf(-g)) * __uint_as_float(rb[j]);
+              const float g = __uint_as_float(ra[j]) * sc0;
+              const float v = g / (1.f + __expf(-g)) * (__uint_as_float(rb[j]) * sc1);
               store_out(h + (size_t)(x.row0 + c0 + j) * p.M + ch, v);
             }
           }
@@ -359,18 +404,63 @@ __global__ void __launch_bounds__(kThreads, 1)
             float* y = static_cast<float*>(p.out) + (size_t)x.ks * p.R * p.M;
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-              if (c0 + j < x.n_valid) y[(size_t)(x.row0 + c0 + j) * p.M + ch] = __uint_as_float(ra[j]);
+              if (c0 + j < x.n_valid) y[(size_t)(x.row0 + c0 + j) * p.M + ch] = __uint_as_float(ra[j]) * sc0;
           } else {
             __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.out);
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-              if (c0 + j < x.n_valid) store_out(y + (size_t)(x.row0 + c0 + j) * p.M + ch, __uint_as_float(ra[j]));
+              if (c0 + j < x.n_valid) store_out(y + (size_t)(x.row0 + c0 + j) * p.M + ch, __uint_as_float(ra[j]) * sc0);
           }
         }
       }
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(acce_bar(buf));
+    }
+    if (!ok && lane == 0) set_device_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
+  } else if (FP8 && !p.selftest) {
+    // ------------------------------------------------------------ converters
+    // Same unit / k-block / stage walk as the MMA issuer.  For each stage:
+    // wait for the E4M3 tile, write it as bf16 into the swizzled MMA tile
+    // (16-byte chunk j of row r at chunk position j ^ (r % 8)), make the
+    // writes visible to the tensor core, then arrive on conv_bar.
+    const int ct = threadIdx.x - kThreads;  // 0..127
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+      const Unit x = decode_unit(u, offs, prefix, G, MT, S, BN);
+      const int kb0 = x.ks * kb_per_split, kb1 = min(kblocks, kb0 + kb_per_split);
+      for (int kb = kb0; kb < kb1; ++kb) {
+        int got = 0;
+        if (lane == 0) got = ptx::mbar_wait_bounded(full_bar(stage), phase, deadline, abort_flag) ? 1 : 0;
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = smem + stage * C::STAGE_BYTES;
+#pragma unroll
+        for (int a = 0; a < C::NA; ++a) {
+          const uint8_t* src = st + C::STG_OFF + a * C::STG_BYTES;
+          uint8_t* dst = st + a * C::A_BYTES;
+#pragma unroll
+          for (int i = ct; i < kBM * kBK / 16; i += kConvThreads) {  // 16 E4M3 per chunk
+            const int r = i >> 2, c = i & 3;
+            const uint4 v = *reinterpret_cast<const uint4*>(src + r * kBK + c * 16);
+            const int sw = r & 7;
+            *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * c) ^ sw) << 4)) = e4m3x8_to_bf16x8(v.x, v.y);
+            *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * c + 1) ^ sw) << 4)) = e4m3x8_to_bf16x8(v.z, v.w);
+          }
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(conv_bar(stage));
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
     }
     if (!ok && lane == 0) set_device_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
   }
@@ -383,22 +473,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int MODE, int BN>
+template <int MODE, int BN, bool FP8>
 moe_status launch_one(const TcParams& p, const CUtensorMap& a0, const CUtensorMap& a1,
                       const CUtensorMap& b, int grid, cudaStream_t s) {
-  using C = Cfg<MODE, BN>;
-  auto kern = tc_grouped_kernel<MODE, BN>;
+  using C = Cfg<MODE, BN, FP8>;
+  auto kern = tc_grouped_kernel<MODE, BN, FP8>;
   MOE_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES));
-  kern<<<grid, kThreads, C::SMEM_BYTES, s>>>(p, a0, a1, b);
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(p, a0, a1, b);
   MOE_TRY_CUDA(cudaGetLastError());
   return MOE_OK;
 }
 
 template <int MODE>
-moe_status launch_mode(int bn, const TcParams& p, const CUtensorMap& a0, const CUtensorMap& a1,
-                       const CUtensorMap& b, int grid, cudaStream_t s) {
-  if (bn == 32) return launch_one<MODE, 32>(p, a0, a1, b, grid, s);
-  if (bn == 128) return launch_one<MODE, 128>(p, a0, a1, b, grid, s);
+moe_status launch_mode(int bn, bool fp8, const TcParams& p, const CUtensorMap& a0,
+                       const CUtensorMap& a1, const CUtensorMap& b, int grid, cudaStream_t s) {
+  if (fp8) {
+    if (bn == 32) return launch_one<MODE, 32, true>(p, a0, a1, b, grid, s);
+    if (bn == 128) return launch_one<MODE, 128, true>(p, a0, a1, b, grid, s);
+  } else {
+    if (bn == 32) return launch_one<MODE, 32, false>(p, a0, a1, b, grid, s);
+    if (bn == 128) return launch_one<MODE, 128, false>(p, a0, a1, b, grid, s);
+  }
   return MOE_ERR_UNSUPPORTED;
 }
 
@@ -437,14 +532,20 @@ TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int /*w_dtype*/
 moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStream_t s,
                              cudaEvent_t mid) {
   if (a.R == 0) return MOE_OK;
-  if (a.w_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  const bool fp8 = a.w_dtype == MOE_FP8_E4M3;
+  if (!fp8 && a.w_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (fp8 && (a.s_gate == nullptr || a.s_up == nullptr || a.s_down == nullptr)) return MOE_ERR_INVALID_ARG;
   if (a.d % kBM != 0 || a.ffn % kBM != 0 || a.G > kMaxGroups) return MOE_ERR_UNSUPPORTED;
+  // weights: bf16 tiles [128 x 64] with 128-byte swizzle, or E4M3 tiles
+  // [128 x 64 bytes] staged unswizzled for the converters
+  const int wb = fp8 ? 1 : 2;
+  const bool wsw = !fp8;
   CUtensorMap wg, wu, xb, wd, hb;
-  MOE_TRY(make_tmap_2d(&wg, a.w_gate, (uint64_t)a.G * a.ffn, a.d, 2, kBM, kBK));
-  MOE_TRY(make_tmap_2d(&wu, a.w_up, (uint64_t)a.G * a.ffn, a.d, 2, kBM, kBK));
-  MOE_TRY(make_tmap_2d(&xb, a.x_perm, a.R, a.d, 2, kBoxN, kBK));
-  MOE_TRY(make_tmap_2d(&wd, a.w_down, (uint64_t)a.G * a.d, a.ffn, 2, kBM, kBK));
-  MOE_TRY(make_tmap_2d(&hb, a.h, a.R, a.ffn, 2, kBoxN, kBK));
+  MOE_TRY(make_tmap_2d(&wg, a.w_gate, (uint64_t)a.G * a.ffn, a.d, wb, kBM, kBK, wsw));
+  MOE_TRY(make_tmap_2d(&wu, a.w_up, (uint64_t)a.G * a.ffn, a.d, wb, kBM, kBK, wsw));
+  MOE_TRY(make_tmap_2d(&xb, a.x_perm, a.R, a.d, 2, kBoxN, kBK, true));
+  MOE_TRY(make_tmap_2d(&wd, a.w_down, (uint64_t)a.G * a.d, a.ffn, wb, kBM, kBK, wsw));
+  MOE_TRY(make_tmap_2d(&hb, a.h, a.R, a.ffn, 2, kBoxN, kBK, true));
 
   TcParams p{};
   p.G = a.G;
@@ -459,7 +560,9 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   p.splits = 1;
   p.out = a.h;
   p.out_f32 = 0;
-  MOE_TRY(launch_mode<kGateUp>(plan.bn_gateup, p, wg, wu, xb, plan.grid, s));
+  p.scale0 = a.s_gate;
+  p.scale1 = a.s_up;
+  MOE_TRY(launch_mode<kGateUp>(plan.bn_gateup, fp8, p, wg, wu, xb, plan.grid, s));
   if (mid != nullptr) MOE_TRY_CUDA(cudaEventRecord(mid, s));
 
   p.M = a.d;
@@ -467,7 +570,9 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   p.splits = plan.splits_down;
   p.out = a.y;
   p.out_f32 = plan.splits_down > 1 ? 1 : 0;
-  MOE_TRY(launch_mode<kDown>(plan.bn_down, p, wd, wd, hb, plan.grid, s));
+  p.scale0 = a.s_down;
+  p.scale1 = nullptr;
+  MOE_TRY(launch_mode<kDown>(plan.bn_down, fp8, p, wd, wd, hb, plan.grid, s));
   return MOE_OK;
 }
 
@@ -483,7 +588,7 @@ moe_status tc_selftest_launch(int* status, long long timeout_ns, cudaStream_t s)
   p.status = status;
   p.timeout_ns = timeout_ns;
   p.selftest = 1;
-  return launch_one<kGateUp, 32>(p, dummy, dummy, dummy, 1, s);
+  return launch_one<kGateUp, 32, false>(p, dummy, dummy, dummy, 1, s);
 }
 
 }  // namespace moe

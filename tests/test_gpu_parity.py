@@ -5,7 +5,8 @@ Bars (written in each test):
   routing indices, counts, offsets, permutation maps, row moves: bit-exact;
   routing weights: fp32 rounding (rtol 2e-6 given the same fp32 logits);
   layer / expert outputs: max|err| <= 2e-2 * max|ref| for bf16 storage,
-  <= 1e-4 * max|ref| for fp32 storage.
+  <= 5e-2 * max|ref| for FP8 (E4M3) expert weights, <= 1e-4 * max|ref| for
+  fp32 storage.
 """
 
 import numpy as np
@@ -19,6 +20,7 @@ from tests import helpers
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 BF16_TOL = 2e-2
+FP8_TOL = 5e-2
 F32_TOL = 1e-4
 
 
@@ -248,6 +250,56 @@ def test_grouped_swiglu_tensor_path(kind, d, f):
     assert np.sqrt(((got - ref) ** 2).mean()) <= 1e-2 * np.sqrt((ref ** 2).mean())
 
 
+def _fp8_stack(E, rows, cols, gen, all_codes_expert=None):
+    w = torch.empty((E, rows, cols), dtype=torch.uint8, device=DEV)
+    s = torch.empty((E, rows), dtype=torch.float32, device=DEV)
+    for e in range(E):
+        q, sc = inputs._fp8_quantise(torch.randn((rows, cols), generator=gen, device=DEV) * cols ** -0.5)
+        w[e].copy_(q)
+        s[e].copy_(sc)
+    if all_codes_expert is not None:
+        # every finite E4M3 code (NaN codes 0x7F / 0xFF excluded), cycling
+        codes = torch.tensor([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=torch.uint8, device=DEV)
+        n = rows * cols
+        w[all_codes_expert].copy_(codes.repeat(n // len(codes) + 1)[:n].view(rows, cols))
+        s[all_codes_expert].fill_(1.0 / 448.0)
+    return w, s
+
+
+@pytest.mark.parametrize("kind", ["ragged", "decode"])
+def test_grouped_swiglu_fp8_weights(kind):
+    counts = np.array(GROUP_COUNTS[kind])
+    E, d, f = len(counts), 256, 384
+    R = int(counts.sum())
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    g = torch.Generator(device=DEV).manual_seed(77)
+    x = _bf16_rand((R, d), 1.0, g)
+    busy = int(np.argmax(counts))
+    wg, sg = _fp8_stack(E, f, d, g, all_codes_expert=busy)
+    wu, su = _fp8_stack(E, f, d, g)
+    wd, sd = _fp8_stack(E, d, f, g, all_codes_expert=busy)
+    p = api.problem(R, d, f, E, 1, wfmt="fp8")
+    y = torch.full((R, d), float("nan"), dtype=torch.bfloat16, device=DEV)
+    api.moe_grouped_swiglu(p, x, torch.from_numpy(offsets).to(DEV), wg, wu, wd, sg, su, sd, y, api.workspace_for(p))
+    torch.cuda.synchronize()
+    ew = oracle.ExpertWeights("fp8", wg.cpu().numpy(), wu.cpu().numpy(), wd.cpu().numpy(),
+                              sg.cpu().numpy(), su.cpu().numpy(), sd.cpu().numpy())
+    xf, got = _f64(x), _f64(y)
+    ref = np.zeros_like(got)
+    for e in range(E):
+        a, b = offsets[e], offsets[e + 1]
+        if b > a:
+            ref[a:b] = oracle.swiglu_expert(xf[a:b], *ew.get(e))
+    assert np.isfinite(got).all()
+    assert np.abs(got - ref).max() <= FP8_TOL * np.abs(ref).max()
+    # the dequantisation is exact: only the bf16 roundings of h and y remain
+    for e in range(E):
+        a, b = offsets[e], offsets[e + 1]
+        if b > a:
+            rel = np.sqrt(((got[a:b] - ref[a:b]) ** 2).mean()) / np.sqrt((ref[a:b] ** 2).mean())
+            assert rel <= 1e-2, f"expert {e}: relative rms error {rel:.3g}"
+
+
 # ---------------------------------------------------------------------------
 # whole layer
 # ---------------------------------------------------------------------------
@@ -345,6 +397,13 @@ def test_layer_qwen3_30b_a3b_shaped_prefill_sampled():
     _, _, _, counts = api.layer_forward(p, case, want_routing=True)
     c = counts.cpu().numpy()
     assert c.max() / c.mean() > 4.0
+
+
+@pytest.mark.parametrize("T,sample", [(1, None), (64, 12), (4096, 12)])
+def test_layer_deepseek_v3_shaped_fp8_with_shared_expert(T, sample):
+    shape = inputs.WORKLOADS["deepseek_v3"].with_T(T)
+    tokens = None if sample is None else np.linspace(0, T - 1, sample).astype(int)
+    _layer_check(shape, 0, FP8_TOL, tokens=tokens)
 
 
 def test_layer_empty_batch():

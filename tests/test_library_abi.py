@@ -40,6 +40,23 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(names) == set(api.EXPORTS), "binding and header disagree"
 
 
+def _header_arity():
+    with open(os.path.join(ROOT, "include", "moe.h")) as f:
+        text = f.read()
+    out = {}
+    for m in re.finditer(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(([^;]*?)\)\s*;", text, re.S):
+        params = m.group(2).strip()
+        out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_arity_matches_header():
+    arity = _header_arity()
+    assert set(arity) == set(api.EXPORTS)
+    for name, n in arity.items():
+        assert len(api._SIGS[name]) == n, f"{name}: header has {n} parameters, binding {len(api._SIGS[name])}"
+
+
 def test_abi_version_and_status_strings(lib):
     assert api.moe_abi_version() == 1
     assert api.moe_status_string(0) == "MOE_OK"
@@ -73,7 +90,7 @@ def test_null_pointers_rejected_before_any_launch(lib):
     # x_perm requested without x
     assert lib.moe_permute(ctypes.byref(p), None, None, None, None, None, None, None, None, 0, None) == api.ERR_INVALID_ARG
     assert lib.moe_combine(ctypes.byref(p), None, None, None, None, None, None) == api.ERR_INVALID_ARG
-    assert lib.moe_layer_forward(ctypes.byref(p), *([None] * 18), 0, None) == api.ERR_INVALID_ARG
+    assert lib.moe_layer_forward(ctypes.byref(p), *([None] * 17), 0, None) == api.ERR_INVALID_ARG
 
 
 def test_empty_batch_is_a_no_op(lib):
@@ -82,7 +99,7 @@ def test_empty_batch_is_a_no_op(lib):
     # T == 0 returns OK before any launch, even with null tensors
     assert lib.moe_grouped_swiglu(ctypes.byref(p), *([None] * 10), 0, None) == 0
     assert lib.moe_combine(ctypes.byref(p), None, None, None, None, None, None) == 0
-    assert lib.moe_layer_forward(ctypes.byref(p), *([None] * 18), 0, None) == 0
+    assert lib.moe_layer_forward(ctypes.byref(p), *([None] * 17), 0, None) == 0
     del ws
 
 
