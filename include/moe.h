@@ -145,6 +145,30 @@ MOE_API moe_status moe_permute(const moe_problem *p, const int32_t *topk_idx, co
                        size_t workspace_bytes, moe_stream_t stream);
 
 /*
+ * moe_permute_static_scratch -- moe_permute without a workspace argument.
+ * No counterpart on the pages: it exists for callers that cannot allocate
+ * device memory -- code hosted by another framework whose memory manager
+ * must own every allocation, or latency-critical loops that cannot afford a
+ * cudaMalloc (which may synchronise the device).  Arguments and results are
+ * those of moe_permute; the caller still passes every input and output.
+ *
+ * The scratch moe_permute takes from the workspace (per-chunk expert counts,
+ * ceil(T*k/256) * E int32 values) lives instead in a 1 MiB array compiled
+ * into the library and held by every GPU that loads it until the process
+ * exits.  Problems needing more (ceil(T*k/256) * E > 262144) are rejected
+ * with MOE_ERR_WORKSPACE.  The first call on each device looks up the
+ * array's device address with that device current; make that first call
+ * before any stream capture.  All calls share the array and it keeps the
+ * last call's contents (every entry read is first rewritten, so nothing has
+ * to be cleared); calls that overlap on the GPU race on it.  Allocates
+ * nothing.
+ */
+MOE_API moe_status moe_permute_static_scratch(const moe_problem *p, const int32_t *topk_idx,
+                                              const void *x, int32_t *counts, int32_t *offsets,
+                                              int32_t *perm_token, int32_t *inv_row,
+                                              void *x_perm, moe_stream_t stream);
+
+/*
  * moe_grouped_swiglu -- all expert matrices in one grouped computation.
  * Page "MOE推理流程解析", section 三 (a grouped GEMM runs several expert
  * matrices with different row counts in one launch; each expert applies its

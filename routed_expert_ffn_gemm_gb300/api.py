@@ -65,6 +65,7 @@ _SIGS = {
     "moe_layer_forward_timed": [_PP] + [_VP] * 17 + [ctypes.c_size_t, _VP, _VP],
     "moe_layer_launch_count": [_PP, ctypes.POINTER(ctypes.c_int32)],
     "moe_plan_info": [_PP, ctypes.POINTER(ctypes.c_int32)],
+    "moe_permute_static_scratch": [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP],
 }
 STAGES = ("router", "permute", "gate_up", "down", "shared", "combine")
 EXPORTS = tuple(_SIGS)
@@ -126,6 +127,14 @@ def moe_permute(p, topk_idx, x, counts, offsets, perm_token, inv_row, x_perm, wo
     _call("moe_permute", ctypes.byref(p), _ptr(topk_idx), _ptr(x), _ptr(counts), _ptr(offsets),
           _ptr(perm_token), _ptr(inv_row), _ptr(x_perm), _ptr(workspace),
           0 if workspace is None else workspace.numel() * workspace.element_size(), _stream(stream))
+
+
+def moe_permute_static_scratch(p, topk_idx, x, counts, offsets, perm_token, inv_row, x_perm, stream=None):
+    """moe_permute for callers that cannot allocate device memory: the
+    permutation's scratch comes from a fixed 1 MiB array inside the library
+    instead of a caller workspace (see include/moe.h for its limits)."""
+    _call("moe_permute_static_scratch", ctypes.byref(p), _ptr(topk_idx), _ptr(x), _ptr(counts),
+          _ptr(offsets), _ptr(perm_token), _ptr(inv_row), _ptr(x_perm), _stream(stream))
 
 
 def moe_grouped_swiglu(p, x_perm, offsets, w_gate, w_up, w_down, s_gate, s_up, s_down, y_perm,
