@@ -3,10 +3,11 @@
 // scores every eligible expert, top-k keeps the chosen indices and weights;
 // section 九: the kept weights are re-normalised).
 //
-// router_kernel: a block owns TT = 8 tokens, whose rows are staged once in
-// shared memory, and a slice of the experts; each warp accumulates EPW
-// experts x 8 tokens with 16-byte loads of W_r rows (fp32 FMA) and a shuffle
-// reduction.  With one expert slice (gridDim.y == 1, "fused") the logits stay
+// router_kernel: a block owns TT tokens (8, or 1 for small batches), whose
+// rows are staged once in shared memory, and a slice of the experts; each
+// warp accumulates EPW experts x TT tokens with 16-byte loads of W_r rows
+// (fp32 FMA, the hidden loop unrolled so several loads are in flight) and a
+// shuffle reduction.  With one expert slice (gridDim.y == 1, "fused") the logits stay
 // in shared memory and the same block selects the top-k; with several slices
 // (few tokens: more blocks stream W_r) the logits go to global memory and
 // topk_kernel follows.
@@ -21,7 +22,7 @@
 namespace moe {
 namespace {
 
-constexpr int kTT = 8;  // tokens per block
+constexpr int kTT = 8;  // tokens per block (large batches)
 constexpr int kThreads = 256;
 
 __device__ __forceinline__ void load16(const float* p, float (&v)[8]) {
@@ -93,7 +94,7 @@ __device__ void topk_row(const float* row, int E, int k, int32_t* idx_out, float
   }
 }
 
-template <typename ActT, int EPW>
+template <typename ActT, int EPW, int TT>
 __global__ void __launch_bounds__(kThreads) router_kernel(
     int T, int d, int E, int k, const ActT* __restrict__ x, const ActT* __restrict__ wr,
     const float* __restrict__ bias, const float* __restrict__ logits_in,
@@ -102,13 +103,14 @@ __global__ void __launch_bounds__(kThreads) router_kernel(
   extern __shared__ __align__(16) uint8_t sm[];
   const bool fused = gridDim.y == 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t0 = blockIdx.x * kTT;
+  const int t0 = blockIdx.x * TT;
   ActT* xs = reinterpret_cast<ActT*>(sm);                                   // [TT][d]
-  float* ls = reinterpret_cast<float*>(sm + (logits_in ? 0 : sizeof(ActT) * kTT * d));  // [TT][E]
+  float* ls = reinterpret_cast<float*>(sm + (logits_in ? 0 : sizeof(ActT) * TT * d));  // [TT][E]
 
   if (logits_in == nullptr) {
     const int vec_per_row = d / VN;
-    for (int v = threadIdx.x; v < kTT * vec_per_row; v += kThreads) {
+#pragma unroll 4
+    for (int v = threadIdx.x; v < TT * vec_per_row; v += kThreads) {
       const int t = v / vec_per_row, c = (v % vec_per_row) * VN;
       uint4 val = make_uint4(0, 0, 0, 0);
       if (t0 + t < T) val = *reinterpret_cast<const uint4*>(x + (size_t)(t0 + t) * d + c);
@@ -118,22 +120,23 @@ __global__ void __launch_bounds__(kThreads) router_kernel(
     const int slice = ((E + gridDim.y - 1) / gridDim.y + EPW - 1) / EPW * EPW;
     const int e_lo = blockIdx.y * slice, e_hi = min(E, e_lo + slice);
     for (int eb = e_lo + warp * EPW; eb < e_hi; eb += 8 * EPW) {
-      float acc[EPW][kTT];
+      float acc[EPW][TT];
 #pragma unroll
       for (int a = 0; a < EPW; ++a)
 #pragma unroll
-        for (int t = 0; t < kTT; ++t) acc[a][t] = 0.f;
+        for (int t = 0; t < TT; ++t) acc[a][t] = 0.f;
+#pragma unroll 4
       for (int i = lane * VN; i < d; i += 32 * VN) {
-        float xv[kTT][8];
+        float xv[TT][8];
 #pragma unroll
-        for (int t = 0; t < kTT; ++t) load16(xs + (size_t)t * d + i, xv[t]);
+        for (int t = 0; t < TT; ++t) load16(xs + (size_t)t * d + i, xv[t]);
 #pragma unroll
         for (int a = 0; a < EPW; ++a) {
           if (eb + a < e_hi) {
             float wv[8];
             load16(wr + (size_t)(eb + a) * d + i, wv);
 #pragma unroll
-            for (int t = 0; t < kTT; ++t)
+            for (int t = 0; t < TT; ++t)
 #pragma unroll
               for (int q = 0; q < VN; ++q) acc[a][t] = fmaf(wv[q], xv[t][q], acc[a][t]);
           }
@@ -143,7 +146,7 @@ __global__ void __launch_bounds__(kThreads) router_kernel(
       for (int a = 0; a < EPW; ++a) {
         const int e = eb + a;
 #pragma unroll
-        for (int t = 0; t < kTT; ++t) {
+        for (int t = 0; t < TT; ++t) {
           float v = acc[a][t];
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -156,15 +159,16 @@ __global__ void __launch_bounds__(kThreads) router_kernel(
       }
     }
   } else {
-    for (int i = threadIdx.x; i < kTT * E; i += kThreads) {
+    for (int i = threadIdx.x; i < TT * E; i += kThreads) {
       const int t = i / E;
       ls[i] = t0 + t < T ? logits_in[(size_t)t0 * E + i] : 0.f;
     }
   }
   if (!fused) return;
   __syncthreads();
-  const int t = t0 + warp;  // 8 warps <-> 8 tokens
-  if (t < T) topk_row(ls + warp * E, E, k, idx + (size_t)t * k, w + (size_t)t * k);
+  // one warp per token
+  for (int t = warp; t < TT; t += kThreads / 32)
+    if (t0 + t < T) topk_row(ls + t * E, E, k, idx + (size_t)(t0 + t) * k, w + (size_t)(t0 + t) * k);
 }
 
 __global__ void __launch_bounds__(kThreads) topk_kernel(int T, int E, int k,
@@ -175,33 +179,50 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(int T, int E, int k,
   if (t < T) topk_row(logits + (size_t)t * E, E, k, idx + (size_t)t * k, w + (size_t)t * k);
 }
 
-// Few token tiles and a global logits buffer available: split the experts
-// over more blocks (one expert per warp), then a separate top-k pass.
+// Few tokens and a global logits buffer available: split the experts over
+// more blocks (one expert per warp, one token per block when the batch is
+// tiny), then a separate top-k pass unless one block sees all experts.
 bool use_split(int T, int E, bool logits_in, bool scratch) {
-  const int tiles = (T + kTT - 1) / kTT;
-  return !logits_in && scratch && tiles <= 16 && E > 8;
+  return !logits_in && scratch && T <= 512;
 }
+int split_tt(int T) { return T <= 32 ? 1 : kTT; }
+bool split_needs_topk_pass(int E) { return (E + 7) / 8 > 1; }
 
 template <typename ActT>
 moe_status launch_typed(const RouterArgs& a, float* logits_scratch, cudaStream_t s) {
-  const int tiles = (a.T + kTT - 1) / kTT;
-  const size_t xs_bytes = a.logits_in ? 0 : sizeof(ActT) * kTT * a.d;
   const bool split = use_split(a.T, a.E, a.logits_in != nullptr, logits_scratch != nullptr);
   if (split) {
-    auto kern = router_kernel<ActT, 1>;
-    MOE_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)xs_bytes));
-    dim3 grid(tiles, (a.E + 7) / 8);
-    kern<<<grid, kThreads, xs_bytes, s>>>(a.T, a.d, a.E, a.k, static_cast<const ActT*>(a.x),
-                                          static_cast<const ActT*>(a.w_router), a.bias, nullptr,
-                                          logits_scratch, a.idx, a.w);
+    const int tt = split_tt(a.T);
+    const size_t xs_bytes = sizeof(ActT) * tt * a.d;
+    const int gy = (a.E + 7) / 8;
+    // one block row sees every expert: keep the logits in shared memory
+    const size_t smem = xs_bytes + (gy == 1 ? sizeof(float) * tt * a.E : 0);
+    dim3 grid((a.T + tt - 1) / tt, gy);
+    if (tt == 1) {
+      auto kern = router_kernel<ActT, 1, 1>;
+      MOE_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+      kern<<<grid, kThreads, smem, s>>>(a.T, a.d, a.E, a.k, static_cast<const ActT*>(a.x),
+                                        static_cast<const ActT*>(a.w_router), a.bias, nullptr,
+                                        logits_scratch, a.idx, a.w);
+    } else {
+      auto kern = router_kernel<ActT, 1, kTT>;
+      MOE_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+      kern<<<grid, kThreads, smem, s>>>(a.T, a.d, a.E, a.k, static_cast<const ActT*>(a.x),
+                                        static_cast<const ActT*>(a.w_router), a.bias, nullptr,
+                                        logits_scratch, a.idx, a.w);
+    }
     MOE_TRY_CUDA(cudaGetLastError());
-    topk_kernel<<<(a.T + 7) / 8, kThreads, 0, s>>>(a.T, a.E, a.k, logits_scratch, a.idx, a.w);
-    MOE_TRY_CUDA(cudaGetLastError());
+    if (gy > 1) {
+      topk_kernel<<<(a.T + 7) / 8, kThreads, 0, s>>>(a.T, a.E, a.k, logits_scratch, a.idx, a.w);
+      MOE_TRY_CUDA(cudaGetLastError());
+    }
     return MOE_OK;
   }
+  const int tiles = (a.T + kTT - 1) / kTT;
+  const size_t xs_bytes = a.logits_in ? 0 : sizeof(ActT) * kTT * a.d;
   const size_t smem = xs_bytes + sizeof(float) * kTT * a.E;
   if (smem > 220 * 1024) return MOE_ERR_UNSUPPORTED;
-  auto kern = router_kernel<ActT, 4>;
+  auto kern = router_kernel<ActT, 4, kTT>;
   MOE_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   kern<<<dim3(tiles, 1), kThreads, smem, s>>>(a.T, a.d, a.E, a.k, static_cast<const ActT*>(a.x),
                                               static_cast<const ActT*>(a.w_router), a.bias,
@@ -216,7 +237,7 @@ moe_status launch_typed(const RouterArgs& a, float* logits_scratch, cudaStream_t
 }  // namespace
 
 int router_launch_count(int T, int E, bool logits_in, bool logits_out) {
-  return use_split(T, E, logits_in, logits_out) ? 2 : 1;
+  return use_split(T, E, logits_in, logits_out) && split_needs_topk_pass(E) ? 2 : 1;
 }
 
 moe_status router_topk_check(int d, int E, int act_dtype) {
