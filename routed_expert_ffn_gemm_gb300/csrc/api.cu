@@ -188,11 +188,20 @@ moe_status moe_grouped_swiglu(const moe_problem* p, const void* x_perm, const in
   MOE_TRY(device_ctx(&ctx));
   const Layout L = layout(*p, path, ctx.num_sms, false);
   const size_t R = (size_t)p->T * p->k;
-  const size_t need = align256(R * p->ffn * act_bytes(p->act_dtype));
-  if (workspace == nullptr || workspace_bytes < need) return MOE_ERR_WORKSPACE;
-  return run_grouped(path, (int)R, p->d, p->ffn, p->E, p->w_dtype, x_perm, offsets, w_gate, w_up,
-                     w_down, s_gate, s_up, s_down, workspace, y_perm, L.plan, ctx.status,
-                     reinterpret_cast<cudaStream_t>(stream), nullptr);
+  const size_t h_bytes = align256(R * p->ffn * act_bytes(p->act_dtype));
+  // FP8 experts run on f16 operands: round x_perm to f16 into the workspace
+  const size_t need = h_bytes + (fp8 ? align256(R * p->d * 2) : 0);
+  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const void* rows = x_perm;
+  if (fp8) {
+    void* xf16 = at<uint8_t>(workspace, h_bytes);
+    MOE_TRY(bf16_to_f16_launch(x_perm, xf16, R * p->d, s));
+    rows = xf16;
+  }
+  return run_grouped(path, (int)R, p->d, p->ffn, p->E, p->w_dtype, rows, offsets, w_gate, w_up,
+                     w_down, s_gate, s_up, s_down, workspace, y_perm, L.plan, ctx.status, s,
+                     nullptr);
 }
 
 moe_status moe_combine(const moe_problem* p, const void* y_perm, const int32_t* inv_row,
@@ -273,8 +282,10 @@ moe_status layer_forward_impl(const moe_problem* p, const void* x, const void* w
   MOE_TRY(router_topk_launch(ra, s));
   MOE_TRY(mark(1));
   // 2. permutation: counts, offsets, row maps, x -> x_perm
+  // FP8 experts run on f16 operands: the row move rounds x to f16
   PermuteArgs pa{p->T, p->k, p->E, p->d, (int)act_bytes(p->act_dtype), idx, x, counts, offsets,
-                 perm_token, inv_row, x_perm, at<int32_t>(workspace, L.chunk), ctx.status};
+                 perm_token, inv_row, x_perm, at<int32_t>(workspace, L.chunk), ctx.status,
+                 fp8 ? 1 : 0};
   MOE_TRY(permute_launch(pa, s));
   MOE_TRY(mark(2));
   // 3. grouped SwiGLU experts (gate/up + SiLU*mul, then down)

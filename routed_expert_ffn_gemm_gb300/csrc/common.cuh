@@ -90,10 +90,13 @@ struct PermuteArgs {
   void* x_perm;
   int32_t* chunk_scratch;  // [n_chunks * E] when the chunked path is used
   int* status;
+  int to_f16;              // 1: x is bf16 and x_perm receives it rounded to f16
 };
 size_t permute_scratch_bytes(int T, int k, int E);
 int permute_launch_count(int T, int k, bool move_rows);
 moe_status permute_launch(const PermuteArgs& a, cudaStream_t s);
+// bf16 rows -> f16 rows (saturating), n elements, n % 8 == 0.
+moe_status bf16_to_f16_launch(const void* src, void* dst, size_t n, cudaStream_t s);
 
 struct CombineArgs {
   int T, k, d, act_dtype;
@@ -131,7 +134,7 @@ struct TcPlan {
 struct TcGroupedArgs {
   int R, d, ffn, G;    // rows, hidden, intermediate, groups (experts)
   int w_dtype;         // MOE_BF16 or MOE_FP8_E4M3
-  const void* x_perm;  // [R, d] bf16 (B operand of gate/up)
+  const void* x_perm;  // [R, d] B operand of gate/up: bf16, or f16 with FP8 weights
   const int32_t* offsets;
   const void* w_gate;
   const void* w_up;
@@ -139,7 +142,7 @@ struct TcGroupedArgs {
   const float* s_gate;
   const float* s_up;
   const float* s_down;
-  void* h;             // [R, ffn] bf16 scratch
+  void* h;             // [R, ffn] scratch: bf16, or f16 with FP8 weights
   void* y;             // [R, d] bf16 when splits_down == 1, else fp32 [S, R, d]
   int* status;
   long long timeout_ns;

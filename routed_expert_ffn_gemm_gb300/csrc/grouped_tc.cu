@@ -25,17 +25,22 @@
 //   warps 2..5      epilogue: tcgen05.ld from TMEM, SiLU(g)*u (gate/up) or
 //                   the projection (down), 64/128-byte coalesced stores
 //   warps 6..9      (FP8 weights only) converters: E4M3 tile staged by TMA ->
-//                   bf16 tile in the 128-byte-swizzled layout the MMA reads
+//                   f16 tile in the 128-byte-swizzled layout the MMA reads
 // Accumulators are double-buffered in TMEM (buffer b at column 256*b; gate at
 // +0, up at +128) so the epilogue of one unit overlaps the next unit's loads
 // and MMAs.  Every wait is bounded: on expiry the kernel records
 // MOE_ERR_DEVICE_TIMEOUT, lets issued copies land, frees TMEM and returns.
 //
 // FP8 weights ("MoE 推理部署", section 专家量化: per-expert scales) are
-// dequantised in-kernel: every E4M3 value is exact in bf16, so the MMA runs
-// kind::f16 on the exact weights and the per-output-channel scale (one TMEM
-// lane = one channel) multiplies the fp32 accumulator in the epilogue.
+// dequantised in-kernel: every E4M3 value is exact in f16 and one hardware
+// conversion turns two of them into an f16 pair, so the MMA runs kind::f16
+// with f16 operands (weights exact; activations and h carried in f16, which
+// holds bf16 values exactly inside f16's normal range) and the
+// per-output-channel scale (one TMEM lane = one channel) multiplies the fp32
+// accumulator in the epilogue.
 #include <string.h>
+
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -123,25 +128,20 @@ __device__ __forceinline__ Unit decode_unit(int u, const int* offs, const int* p
 
 __device__ __forceinline__ void store_out(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
-// Two E4M3 values (low byte = first) -> two bf16 (low half = first), exact.
-// The hardware conversion gives f16; every E4M3 value is zero or a normal
-// f16 whose 7 low mantissa bits are zero, so moving the exponent/mantissa
-// fields to bf16 positions and adding the bias difference (127 - 15 = 112)
-// is exact.  Zero halves stay zero.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t v) {
+// Eight E4M3 values (two 32-bit words, lowest byte first) -> eight f16,
+// exactly (every E4M3 value is representable in f16).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v16) {
   uint32_t h;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(v));
-  const uint32_t mag = (h & 0x7FFF7FFFu) >> 3;
-  const uint32_t nz = __vcmpne2(mag, 0u);
-  return (h & 0x80008000u) | (mag + (0x38003800u & nz));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((uint16_t)v16));
+  return h;
 }
 
-__device__ __forceinline__ uint4 e4m3x8_to_bf16x8(uint32_t lo, uint32_t hi) {
+__device__ __forceinline__ uint4 e4m3x8_to_f16x8(uint32_t lo, uint32_t hi) {
   uint4 r;
-  r.x = e4m3x2_to_bf16x2((uint16_t)(lo & 0xFFFFu));
-  r.y = e4m3x2_to_bf16x2((uint16_t)(lo >> 16));
-  r.z = e4m3x2_to_bf16x2((uint16_t)(hi & 0xFFFFu));
-  r.w = e4m3x2_to_bf16x2((uint16_t)(hi >> 16));
+  r.x = e4m3x2_to_f16x2(lo & 0xFFFFu);
+  r.y = e4m3x2_to_f16x2(lo >> 16);
+  r.z = e4m3x2_to_f16x2(hi & 0xFFFFu);
+  r.w = e4m3x2_to_f16x2(hi >> 16);
   return r;
 }
 
@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
           }
           ptx::tc_fence_after();
           const int n_mma = ((x.n_valid + 15) / 16) * 16;
-          const uint32_t idesc = ptx::idesc_bf16_f32(kBM, n_mma);
+          const uint32_t idesc = FP8 ? ptx::idesc_f16_f32(kBM, n_mma) : ptx::idesc_bf16_f32(kBM, n_mma);
           const uint32_t d0 = tmem_base + 256u * buf;
           const uint32_t d1 = d0 + 128u;
           for (int kb = kb0; kb < kb1; ++kb) {
@@ -389,13 +389,16 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
           uint32_t rb[16];
           ptx::tmem_ld16(taddr + 128u + c0, rb);
           ptx::tmem_ld_wait();
-          __nv_bfloat16* h = static_cast<__nv_bfloat16*>(p.out);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             if (c0 + j < x.n_valid) {
               const float g = __uint_as_float(ra[j]) * sc0;
               const float v = g / (1.f + __expf(-g)) * (__uint_as_float(rb[j]) * sc1);
-              store_out(h + (size_t)(x.row0 + c0 + j) * p.M + ch, v);
+              const size_t o = (size_t)(x.row0 + c0 + j) * p.M + ch;
+              if (FP8)
+                static_cast<__half*>(p.out)[o] = __float2half_rn(v);  // h feeds an f16 MMA
+              else
+                store_out(static_cast<__nv_bfloat16*>(p.out) + o, v);
             }
           }
         } else {
@@ -421,7 +424,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
   } else if (FP8 && !p.selftest) {
     // ------------------------------------------------------------ converters
     // Same unit / k-block / stage walk as the MMA issuer.  For each stage:
-    // wait for the E4M3 tile, write it as bf16 into the swizzled MMA tile
+    // wait for the E4M3 tile, write it as f16 into the swizzled MMA tile
     // (16-byte chunk j of row r at chunk position j ^ (r % 8)), make the
     // writes visible to the tensor core, then arrive on conv_bar.
     const int ct = threadIdx.x - kThreads;  // 0..127
@@ -449,8 +452,8 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
             const int r = i >> 2, c = i & 3;
             const uint4 v = *reinterpret_cast<const uint4*>(src + r * kBK + c * 16);
             const int sw = r & 7;
-            *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * c) ^ sw) << 4)) = e4m3x8_to_bf16x8(v.x, v.y);
-            *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * c + 1) ^ sw) << 4)) = e4m3x8_to_bf16x8(v.z, v.w);
+            *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * c) ^ sw) << 4)) = e4m3x8_to_f16x8(v.x, v.y);
+            *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * c + 1) ^ sw) << 4)) = e4m3x8_to_f16x8(v.z, v.w);
           }
         }
         ptx::fence_proxy_async_smem();

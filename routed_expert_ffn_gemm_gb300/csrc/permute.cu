@@ -14,7 +14,11 @@
 //                            grid-wide row gather moves x -> x_perm;
 //   chunked path (any R):    count per 256-assignment chunk, one scan block,
 //                            then per chunk: ranks, maps and row moves.
-// Row moves are 16-byte vector loads/stores, one warp per row.
+// Row moves are 16-byte vector loads/stores, one warp per row.  When the
+// experts run on f16 operands (FP8 weights) the row move also rounds the
+// bf16 token vector to f16 (saturating to the largest finite f16).
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 
 namespace moe {
@@ -23,6 +27,23 @@ namespace {
 constexpr int kChunk = 256;       // assignments per chunk (chunked path)
 constexpr int kSmallMaxR = 2048;  // largest R for the single-block path
 constexpr int kSmallWarps = 16;
+
+// 8 bf16 -> 8 f16 (round to nearest, saturate to +-65504).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
+  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v);
+  uint4 r;
+  uint32_t* o = reinterpret_cast<uint32_t*>(&r);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(b[i]);
+    uint32_t h;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(f.y), "f"(f.x));
+    o[i] = h;
+  }
+  return r;
+}
+
+__device__ __forceinline__ uint4 move16(uint4 v, int to_f16) { return to_f16 ? bf16x8_to_f16x8(v) : v; }
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
   uint32_t m;
@@ -134,13 +155,20 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(int R, int E, int vec_
                                                           const int32_t* __restrict__ offsets,
                                                           const int32_t* __restrict__ perm_token,
                                                           const uint4* __restrict__ x,
-                                                          uint4* __restrict__ x_perm) {
+                                                          uint4* __restrict__ x_perm, int to_f16) {
   const int lane = threadIdx.x & 31;
   const int nrows = min(R, offsets[E]);
   for (int r = blockIdx.x * 8 + (threadIdx.x >> 5); r < nrows; r += gridDim.x * 8) {
     const size_t src = (size_t)perm_token[r] * vec_per_row, dst = (size_t)r * vec_per_row;
-    for (int v = lane; v < vec_per_row; v += 32) x_perm[dst + v] = x[src + v];
+    for (int v = lane; v < vec_per_row; v += 32) x_perm[dst + v] = move16(x[src + v], to_f16);
   }
+}
+
+// n elements of bf16 -> f16, 8 per thread.
+__global__ void __launch_bounds__(256) bf16_to_f16_kernel(const uint4* __restrict__ src,
+                                                          uint4* __restrict__ dst, size_t nvec) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < nvec; i += (size_t)gridDim.x * blockDim.x)
+    dst[i] = bf16x8_to_f16x8(src[i]);
 }
 
 // -------------------------------------------------------------- chunked path
@@ -189,7 +217,7 @@ __global__ void __launch_bounds__(256) permute_scatter_kernel(
     int R, int k, int E, int vec_per_row, const int32_t* __restrict__ idx,
     const int32_t* __restrict__ chunk_base, int32_t* __restrict__ perm_token,
     int32_t* __restrict__ inv_row, const uint4* __restrict__ x, uint4* __restrict__ x_perm,
-    int* status) {
+    int* status, int to_f16) {
   extern __shared__ int sm[];
   int* wcnt = sm;                 // [8][E]
   int* lrank = wcnt + 8 * E;      // [kChunk]
@@ -228,7 +256,7 @@ __global__ void __launch_bounds__(256) permute_scatter_kernel(
       const int r = rows[i];
       if (r < 0) continue;
       const size_t src = (size_t)((c0 + i) / k) * vec_per_row, dst = (size_t)r * vec_per_row;
-      for (int v = lane; v < vec_per_row; v += 32) x_perm[dst + v] = x[src + v];
+      for (int v = lane; v < vec_per_row; v += 32) x_perm[dst + v] = move16(x[src + v], to_f16);
     }
   }
 }
@@ -236,6 +264,16 @@ __global__ void __launch_bounds__(256) permute_scatter_kernel(
 size_t small_smem(int R, int E) { return sizeof(int) * ((size_t)kSmallWarps * E + R + 32 + E); }
 
 }  // namespace
+
+moe_status bf16_to_f16_launch(const void* src, void* dst, size_t n, cudaStream_t s) {
+  if (n == 0) return MOE_OK;
+  if (n % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  const size_t nvec = n / 8;
+  const int blocks = (int)((nvec + 255) / 256 < 4096 ? (nvec + 255) / 256 : 4096);
+  bf16_to_f16_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst), nvec);
+  MOE_TRY_CUDA(cudaGetLastError());
+  return MOE_OK;
+}
 
 size_t permute_scratch_bytes(int T, int k, int E) {
   const size_t R = (size_t)T * k;
@@ -269,7 +307,7 @@ moe_status permute_launch(const PermuteArgs& a, cudaStream_t s) {
       const int blocks = min(1024, (R + 7) / 8);
       gather_rows_kernel<<<blocks, 256, 0, s>>>(R, a.E, vec_per_row, a.offsets, a.perm_token,
                                                 static_cast<const uint4*>(a.x),
-                                                static_cast<uint4*>(a.x_perm));
+                                                static_cast<uint4*>(a.x_perm), a.to_f16);
       MOE_TRY_CUDA(cudaGetLastError());
     }
     return MOE_OK;
@@ -285,7 +323,7 @@ moe_status permute_launch(const PermuteArgs& a, cudaStream_t s) {
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   permute_scatter_kernel<<<n_chunks, 256, smem, s>>>(
       R, a.k, a.E, vec_per_row, a.idx, a.chunk_scratch, a.perm_token, a.inv_row,
-      static_cast<const uint4*>(a.x), static_cast<uint4*>(a.x_perm), a.status);
+      static_cast<const uint4*>(a.x), static_cast<uint4*>(a.x_perm), a.status, a.to_f16);
   MOE_TRY_CUDA(cudaGetLastError());
   return MOE_OK;
 }

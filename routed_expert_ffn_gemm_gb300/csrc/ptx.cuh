@@ -197,5 +197,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          | ((uint32_t)(M >> 4) << 24);       // M >> 4
 }
 
+// Same with A = B = f16.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+  return (1u << 4)                           // D format: f32
+         | ((uint32_t)(N >> 3) << 17)        // N >> 3
+         | ((uint32_t)(M >> 4) << 24);       // M >> 4
+}
+
 }  // namespace ptx
 }  // namespace moe
