@@ -41,6 +41,7 @@ struct Layout {
   size_t idx, w, logits, counts, offsets, perm_token, inv_row, chunk, x_perm, h, y;
   size_t sh_offsets, sh_h, sh_y, total;
   TcPlan plan, sh_plan;
+  int router_splits;  // 0: CUDA-core router; else tensor-core logits with this many K splits
 };
 
 // Workspace of moe_layer_forward (a superset of what the other entry points
@@ -64,7 +65,8 @@ Layout layout(const moe_problem& p, Path path, int num_sms, bool allow_splits) {
   }
   L.idx = take(R * 4);
   L.w = take(R * 4);
-  L.logits = take(T * E * 4);
+  L.router_splits = router_tc_splits(p.T, p.d, p.E, p.act_dtype, num_sms, (size_t)-1);
+  L.logits = take((L.router_splits > 1 ? (size_t)L.router_splits : 1) * T * E * 4);
   L.counts = take(E * 4);
   L.offsets = take((E + 1) * 4);
   L.perm_token = take(R * 4);
@@ -144,8 +146,14 @@ moe_status moe_router_topk(const moe_problem* p, const void* x, const void* w_ro
   if (logits_in == nullptr && (x == nullptr || w_router == nullptr)) return MOE_ERR_INVALID_ARG;
   if ((x && !aligned16(x)) || (w_router && !aligned16(w_router))) return MOE_ERR_INVALID_ARG;
   if (p->T == 0) return MOE_OK;
+  DeviceCtx ctx;
+  MOE_TRY(device_ctx(&ctx));
+  // tensor-core logits need a global buffer: only when the caller gave one
+  const int tcs = logits_out ? router_tc_splits(p->T, p->d, p->E, p->act_dtype, ctx.num_sms,
+                                                (size_t)p->T * p->E)
+                             : 0;
   RouterArgs a{p->T, p->d, p->E, p->k, p->act_dtype, x, w_router, router_bias, logits_in,
-               logits_out, topk_idx, topk_w};
+               logits_out, topk_idx, topk_w, logits_out, tcs, ctx.num_sms, ctx.status};
   return router_topk_launch(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -277,8 +285,12 @@ moe_status layer_forward_impl(const moe_problem* p, const void* x, const void* w
 
   MOE_TRY(mark(0));
   // 1. router: logits, softmax, top-k, renormalised weights
+  // the logits region is the CUDA-core split path's buffer, or the tensor
+  // core's partial-sum scratch (the logits themselves are not an output here)
+  float* lg = at<float>(workspace, L.logits);
   RouterArgs ra{p->T, p->d, p->E, p->k, p->act_dtype, x, w_router, router_bias, nullptr,
-                at<float>(workspace, L.logits), idx, w};
+                L.router_splits > 0 ? nullptr : lg, idx, w, lg, L.router_splits, ctx.num_sms,
+                ctx.status};
   MOE_TRY(router_topk_launch(ra, s));
   MOE_TRY(mark(1));
   // 2. permutation: counts, offsets, row maps, x -> x_perm
@@ -400,7 +412,10 @@ moe_status moe_layer_launch_count(const moe_problem* p, int32_t* launches) {
     *launches = 0;
     return MOE_OK;
   }
-  int n = router_launch_count(p->T, p->E, false, true);
+  DeviceCtx ctx;
+  MOE_TRY(device_ctx(&ctx));
+  const int rs = router_tc_splits(p->T, p->d, p->E, p->act_dtype, ctx.num_sms, (size_t)-1);
+  int n = rs > 0 ? 2 : router_launch_count(p->T, p->E, false, true);
   n += permute_launch_count(p->T, p->k, true);
   n += 2;                        // gate/up, down
   if (p->ffn_shared > 0) n += 3;  // offsets, gate/up, down

@@ -74,7 +74,16 @@ struct RouterArgs {
   float* logits_out;
   int32_t* idx;
   float* w;
+  // tensor-core logits (bf16, E % 128 == 0, large T): scratch of
+  // tc_splits * T * E fp32 (may be logits_out when tc_splits == 1)
+  float* tc_scratch;
+  int tc_splits;
+  int num_sms;
+  int* status;
 };
+// Tensor-core logits apply to this problem (and how many K splits), given a
+// scratch of `scratch_floats` fp32 values; 0 = use the CUDA-core kernels.
+int router_tc_splits(int T, int d, int E, int act_dtype, int num_sms, size_t scratch_floats);
 moe_status router_topk_launch(const RouterArgs& a, cudaStream_t s);
 moe_status router_topk_check(int d, int E, int act_dtype);
 int router_launch_count(int T, int E, bool logits_in, bool logits_out);
@@ -151,6 +160,11 @@ TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype);
 moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStream_t s,
                              cudaEvent_t mid);
 moe_status tc_selftest_launch(int* status, long long timeout_ns, cudaStream_t s);
+// Dense out[s][n][m] = sum over the s-th K slice of a[m, :] . b[n, :] (bf16
+// operands, fp32 results, `splits` K slices), on the tensor cores.
+moe_status tc_dense_f32_launch(const void* a, const void* b, float* out, int M, int N, int K,
+                               int splits, int num_sms, int* status, long long timeout_ns,
+                               cudaStream_t s);
 
 // Default limit of every bounded wait inside a kernel (nanoseconds).
 constexpr long long kDefaultWaitNs = 2000000000LL;

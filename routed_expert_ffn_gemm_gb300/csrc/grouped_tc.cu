@@ -73,6 +73,7 @@ struct TcParams {
   int selftest;            // 1: issue no copies/MMAs, wait on a barrier nothing arrives at
   const float* scale0;     // FP8: per-channel scales of A0 / A1 ([G*M])
   const float* scale1;
+  int dense;               // 1: one group holding rows [0, R) (offsets unused)
 };
 
 template <int MODE, int BN, bool FP8>
@@ -200,7 +201,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
   // per-group tile counts ceil(rows / BN).
   const int G = p.selftest ? 1 : p.G;
   for (int g = threadIdx.x; g <= G; g += C::THREADS) {
-    int o = p.selftest ? 0 : p.offsets[g];
+    int o = p.selftest ? 0 : (p.dense ? (g == 0 ? 0 : p.R) : p.offsets[g]);
     if (o < 0 || o > p.R) {
       set_device_status(p.status, MOE_ERR_DEVICE_BOUNDS);
       o = o < 0 ? 0 : p.R;
@@ -577,6 +578,28 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   p.scale1 = nullptr;
   MOE_TRY(launch_mode<kDown>(plan.bn_down, fp8, p, wd, wd, hb, plan.grid, s));
   return MOE_OK;
+}
+
+moe_status tc_dense_f32_launch(const void* a, const void* b, float* out, int M, int N, int K,
+                               int splits, int num_sms, int* status, long long timeout_ns,
+                               cudaStream_t s) {
+  if (N == 0) return MOE_OK;
+  if (M % kBM != 0 || K % 8 != 0 || splits < 1) return MOE_ERR_UNSUPPORTED;
+  CUtensorMap ta, tb;
+  MOE_TRY(make_tmap_2d(&ta, a, (uint64_t)M, K, 2, kBM, kBK, true));
+  MOE_TRY(make_tmap_2d(&tb, b, (uint64_t)N, K, 2, kBoxN, kBK, true));
+  TcParams p{};
+  p.G = 1;
+  p.dense = 1;
+  p.R = N;
+  p.M = M;
+  p.K = K;
+  p.splits = splits;
+  p.out = out;
+  p.out_f32 = 1;
+  p.status = status;
+  p.timeout_ns = timeout_ns;
+  return launch_mode<kDown>(128, false, p, ta, ta, tb, num_sms, s);
 }
 
 moe_status tc_selftest_launch(int* status, long long timeout_ns, cudaStream_t s) {

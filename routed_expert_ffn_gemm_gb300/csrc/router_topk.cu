@@ -179,6 +179,27 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(int T, int E, int k,
   if (t < T) topk_row(logits + (size_t)t * E, E, k, idx + (size_t)t * k, w + (size_t)t * k);
 }
 
+// Top-k after the tensor-core logits: l[t, :] = sum_s part[s][t][:] (s in
+// order) + bias, staged per warp in shared memory (optionally written out).
+__global__ void __launch_bounds__(kThreads) topk_partials_kernel(
+    int T, int E, int k, int S, const float* __restrict__ part, const float* __restrict__ bias,
+    float* __restrict__ logits_out, int32_t* __restrict__ idx, float* __restrict__ w) {
+  extern __shared__ float rows[];  // [8][E]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (kThreads / 32) + warp;
+  if (t >= T) return;
+  float* row = rows + warp * E;
+  for (int e = lane; e < E; e += 32) {
+    float v = part[(size_t)t * E + e];
+    for (int s = 1; s < S; ++s) v += part[((size_t)s * T + t) * E + e];
+    if (bias != nullptr) v += bias[e];
+    row[e] = v;
+    if (logits_out != nullptr) logits_out[(size_t)t * E + e] = v;
+  }
+  __syncwarp();
+  topk_row(row, E, k, idx + (size_t)t * k, w + (size_t)t * k);
+}
+
 // Few tokens and a global logits buffer available: split the experts over
 // more blocks (one expert per warp, one token per block when the batch is
 // tiny), then a separate top-k pass unless one block sees all experts.
@@ -249,9 +270,35 @@ moe_status router_topk_check(int d, int E, int act_dtype) {
   return MOE_OK;
 }
 
+int router_tc_splits(int T, int d, int E, int act_dtype, int num_sms, size_t scratch_floats) {
+  if (act_dtype != MOE_BF16 || E % 128 != 0 || T < 256 || d % 64 != 0) return 0;
+  if ((size_t)T * E > scratch_floats) return 0;
+  const int tiles = ((T + 127) / 128) * (E / 128);
+  const int kblocks = d / 64;
+  int splits = 1;
+  while (tiles * splits < num_sms && splits < 8 && kblocks / (splits + 1) >= 8) ++splits;
+  while (splits > 1 && (size_t)splits * T * E > scratch_floats) --splits;
+  return splits;
+}
+
 moe_status router_topk_launch(const RouterArgs& a, cudaStream_t s) {
   if (a.T == 0) return MOE_OK;
   MOE_TRY(router_topk_check(a.d, a.E, a.act_dtype));
+  if (a.logits_in == nullptr && a.tc_splits > 0 && a.tc_scratch != nullptr) {
+    // logits on the tensor cores: [splits][T][E] fp32 partials
+    MOE_TRY(tc_dense_f32_launch(a.w_router, a.x, a.tc_scratch, a.E, a.T, a.d, a.tc_splits,
+                                a.num_sms, a.status, kDefaultWaitNs, s));
+    const size_t smem = sizeof(float) * 8 * a.E;
+    MOE_TRY_CUDA(cudaFuncSetAttribute(topk_partials_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    // logits_out may be the scratch itself when there is one split: each
+    // element is read, then rewritten (biased) by the same lane
+    float* lo = a.logits_out;
+    if (lo == a.tc_scratch && a.tc_splits > 1) return MOE_ERR_INVALID_ARG;
+    topk_partials_kernel<<<(a.T + 7) / 8, kThreads, smem, s>>>(a.T, a.E, a.k, a.tc_splits, a.tc_scratch,
+                                                               a.bias, lo, a.idx, a.w);
+    MOE_TRY_CUDA(cudaGetLastError());
+    return MOE_OK;
+  }
   // a caller-visible logits_out doubles as the split path's global buffer
   float* scratch = a.logits_out;
   if (a.act_dtype == MOE_BF16) return launch_typed<__nv_bfloat16>(a, scratch, s);

@@ -75,7 +75,10 @@ def test_router_exact_ties_go_to_lower_index():
 
 
 @pytest.mark.parametrize("act,T,d,E,k", [("bf16", 40, 512, 16, 4), ("bf16", 3, 2048, 128, 8), ("f32", 64, 128, 8, 2),
-                                         ("bf16", 200, 7168, 256, 8), ("bf16", 64, 4096, 8, 2)])
+                                         ("bf16", 200, 7168, 256, 8), ("bf16", 64, 4096, 8, 2),
+                                         # tensor-core logits (bf16, E % 128 == 0, T >= 256), ragged T
+                                         ("bf16", 300, 2048, 128, 8), ("bf16", 1000, 7168, 256, 8),
+                                         ("bf16", 257, 512, 384, 6)])
 def test_router_logits_and_choice(act, T, d, E, k):
     g = torch.Generator(device=DEV).manual_seed(T + d + E)
     dt = torch.bfloat16 if act == "bf16" else torch.float32
