@@ -26,9 +26,11 @@
 //                   the projection (down), 64/128-byte coalesced stores
 //   warps 6..9      (FP8 weights only) converters: E4M3 tile staged by TMA ->
 //                   f16 tile in the 128-byte-swizzled layout the MMA reads
-// Accumulators are double-buffered in TMEM (buffer b at column 256*b; gate at
-// +0, up at +128) so the epilogue of one unit overlaps the next unit's loads
-// and MMAs.  Every wait is bounded: on expiry the kernel records
+// Accumulators live in TMEM (512 columns): a buffer holds the gate and up
+// accumulators (gate at +0, up at +max(BN,128)) or the down accumulator;
+// two buffers when they fit (BN <= 128 for gate/up, <= 256 for down), so the
+// epilogue of one unit overlaps the next unit's loads and MMAs; gate/up with
+// BN = 256 (prefill: half the operand bytes per flop) uses one buffer.  Every wait is bounded: on expiry the kernel records
 // MOE_ERR_DEVICE_TIMEOUT, lets issued copies land, frees TMEM and returns.
 //
 // FP8 weights ("MoE 推理部署", section 专家量化: per-expert scales) are
@@ -38,6 +40,7 @@
 // holds bf16 values exactly inside f16's normal range) and the
 // per-output-channel scale (one TMEM lane = one channel) multiplies the fp32
 // accumulator in the epilogue.
+#include <stdlib.h>
 #include <string.h>
 
 #include <cuda_fp16.h>
@@ -50,7 +53,8 @@ namespace {
 
 constexpr int kBM = 128;          // output channels per tile (MMA M)
 constexpr int kBK = 64;           // reduction elements per stage (128 bytes of bf16)
-constexpr int kBoxN = 16;         // rows per B box
+constexpr int kBoxSmall = 16;     // rows per B box for decode tiles (BN = 32)
+constexpr int kBoxLarge = 64;     // rows per B box for BN >= 128
 constexpr int kThreads = 192;          // producer, MMA, 4 epilogue warps
 constexpr int kConvThreads = 128;      // FP8: 4 converter warps
 constexpr uint32_t kTmemCols = 512;
@@ -74,6 +78,7 @@ struct TcParams {
   const float* scale0;     // FP8: per-channel scales of A0 / A1 ([G*M])
   const float* scale1;
   int dense;               // 1: one group holding rows [0, R) (offsets unused)
+  int boxn;                // rows per B box of tmB (16 or 64)
 };
 
 template <int MODE, int BN, bool FP8>
@@ -86,6 +91,10 @@ struct Cfg {
   static constexpr int STG_OFF = B_OFF + B_BYTES;
   static constexpr int STAGE_BYTES = STG_OFF + NA * STG_BYTES; // multiple of 1024
   static constexpr int THREADS = kThreads + (FP8 ? kConvThreads : 0);
+  // TMEM: one accumulator buffer = NA accumulators of max(BN,128) columns
+  static constexpr int UP_OFF = BN > 128 ? BN : 128;
+  static constexpr int ACC_COLS = NA * UP_OFF;
+  static constexpr int NBUF = 2 * ACC_COLS <= 512 ? 2 : 1;
   static constexpr int TAIL_BYTES = 8 * 36 + 16 + 4 * 2 * (kMaxGroups + 8);
   static constexpr int STAGES_FIT = (kSmemLimit - 1024 - TAIL_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 10 ? 10 : STAGES_FIT;
@@ -100,7 +109,7 @@ struct Cfg {
   static_assert(STAGES >= 2, "pipeline too shallow");
   static_assert(SMEM_BYTES <= kSmemLimit, "shared memory budget");
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
-  static_assert(BN % kBoxN == 0 && BN <= (MODE == kGateUp ? 128 : 256), "tile rows");
+  static_assert(BN % 16 == 0 && BN <= 256 && ACC_COLS <= 512, "tile rows");
 };
 
 struct Unit {
@@ -257,8 +266,8 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
       for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
         const Unit x = decode_unit(u, offs, prefix, G, MT, S, BN);
         const int kb0 = x.ks * kb_per_split, kb1 = min(kblocks, kb0 + kb_per_split);
-        const int nbox = (x.n_valid + kBoxN - 1) / kBoxN;
-        const uint32_t bytes = C::NA * (FP8 ? C::STG_BYTES : C::A_BYTES) + nbox * kBoxN * kBK * 2;
+        const int nbox = (x.n_valid + p.boxn - 1) / p.boxn;
+        const uint32_t bytes = C::NA * (FP8 ? C::STG_BYTES : C::A_BYTES) + nbox * p.boxn * kBK * 2;
         const int arow = x.g * p.M + x.mt * kBM;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!ptx::mbar_wait_bounded(empty_bar(stage), phase ^ 1u, deadline, abort_flag)) {
@@ -275,8 +284,8 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
           if (MODE == kGateUp) ptx::tma_load_2d(wa + wstep, &tmA1, full_bar(stage), kb * kBK, arow, pol_w);
           const uint32_t sb = sa + C::B_OFF;
           for (int i = 0; i < nbox; ++i)
-            ptx::tma_load_2d(sb + i * kBoxN * kBK * 2, &tmB, full_bar(stage), kb * kBK,
-                             x.row0 + i * kBoxN, pol_x);
+            ptx::tma_load_2d(sb + i * p.boxn * kBK * 2, &tmB, full_bar(stage), kb * kBK,
+                             x.row0 + i * p.boxn, pol_x);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -309,8 +318,8 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
         for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++it) {
           const Unit x = decode_unit(u, offs, prefix, G, MT, S, BN);
           const int kb0 = x.ks * kb_per_split, kb1 = min(kblocks, kb0 + kb_per_split);
-          const int buf = it & 1;
-          const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+          const int buf = it % C::NBUF;
+          const uint32_t acc_phase = (uint32_t)(it / C::NBUF) & 1u;
           if (!ptx::mbar_wait_bounded(acce_bar(buf), acc_phase ^ 1u, deadline, abort_flag)) {
             ok = false;
             break;
@@ -318,8 +327,8 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
           ptx::tc_fence_after();
           const int n_mma = ((x.n_valid + 15) / 16) * 16;
           const uint32_t idesc = FP8 ? ptx::idesc_f16_f32(kBM, n_mma) : ptx::idesc_bf16_f32(kBM, n_mma);
-          const uint32_t d0 = tmem_base + 256u * buf;
-          const uint32_t d1 = d0 + 128u;
+          const uint32_t d0 = tmem_base + (uint32_t)(C::ACC_COLS * buf);
+          const uint32_t d1 = d0 + (uint32_t)C::UP_OFF;
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!ptx::mbar_wait_bounded(full_bar(stage), phase, deadline, abort_flag) ||
                 (FP8 && !ptx::mbar_wait_bounded(conv_bar(stage), phase, deadline, abort_flag))) {
@@ -365,8 +374,8 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
     int it = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++it) {
-      const int buf = it & 1;
-      const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+      const int buf = it % C::NBUF;
+      const uint32_t acc_phase = (uint32_t)(it / C::NBUF) & 1u;
       // one lane waits, the warp follows its verdict (tcgen05.ld below is
       // warp-collective, so the warp must agree)
       int got = 0;
@@ -378,7 +387,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
       }
       ptx::tc_fence_after();
       const Unit x = decode_unit(u, offs, prefix, G, MT, S, BN);
-      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + 256u * buf;
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(C::ACC_COLS * buf);
       const int ch = x.mt * kBM + ch_local;
       const int n_mma = ((x.n_valid + 15) / 16) * 16;
       const float sc0 = FP8 ? p.scale0[(size_t)x.g * p.M + ch] : 1.f;
@@ -388,7 +397,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
         ptx::tmem_ld16(taddr + c0, ra);
         if (MODE == kGateUp) {
           uint32_t rb[16];
-          ptx::tmem_ld16(taddr + 128u + c0, rb);
+          ptx::tmem_ld16(taddr + (uint32_t)C::UP_OFF + c0, rb);
           ptx::tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -494,22 +503,36 @@ moe_status launch_mode(int bn, bool fp8, const TcParams& p, const CUtensorMap& a
   if (fp8) {
     if (bn == 32) return launch_one<MODE, 32, true>(p, a0, a1, b, grid, s);
     if (bn == 128) return launch_one<MODE, 128, true>(p, a0, a1, b, grid, s);
+    if (bn == 256) return launch_one<MODE, 256, true>(p, a0, a1, b, grid, s);
   } else {
     if (bn == 32) return launch_one<MODE, 32, false>(p, a0, a1, b, grid, s);
     if (bn == 128) return launch_one<MODE, 128, false>(p, a0, a1, b, grid, s);
+    if (bn == 256) return launch_one<MODE, 256, false>(p, a0, a1, b, grid, s);
   }
   return MOE_ERR_UNSUPPORTED;
 }
 
+int env_int(const char* name) {
+  const char* v = getenv(name);
+  return v ? atoi(v) : 0;
+}
+
+int bn_ok(int bn) { return bn == 32 || bn == 128 || bn == 256 ? bn : 0; }
+int boxn_of(int bn) { return bn >= 128 ? kBoxLarge : kBoxSmall; }
+
 }  // namespace
 
+// Rows per tile from the expected rows per expert: 32 for decode (a few rows
+// each), 128 in between, 256 for prefill (halves operand bytes per flop).
+// MOE_BN_GATEUP / MOE_BN_DOWN override (tuning).
 TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int /*w_dtype*/) {
   TcPlan pl;
   const double R = (double)T * k;
   const double mean = R / E;
   const double est_max = mean + 3.0 * __builtin_sqrt(mean) + 1.0;
-  pl.bn_gateup = est_max <= 32.0 ? 32 : 128;
-  pl.bn_down = pl.bn_gateup;
+  const int bn = est_max <= 32.0 ? 32 : (mean >= 128.0 ? 256 : 128);
+  pl.bn_gateup = bn_ok(env_int("MOE_BN_GATEUP")) ? env_int("MOE_BN_GATEUP") : bn;
+  pl.bn_down = bn_ok(env_int("MOE_BN_DOWN")) ? env_int("MOE_BN_DOWN") : bn;
   const double touched = E < R ? E : R;
   const double tiles_a = R / pl.bn_down;
   const int tiles = (int)(touched > tiles_a ? touched : tiles_a + 0.5);
@@ -547,9 +570,10 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   CUtensorMap wg, wu, xb, wd, hb;
   MOE_TRY(make_tmap_2d(&wg, a.w_gate, (uint64_t)a.G * a.ffn, a.d, wb, kBM, kBK, wsw));
   MOE_TRY(make_tmap_2d(&wu, a.w_up, (uint64_t)a.G * a.ffn, a.d, wb, kBM, kBK, wsw));
-  MOE_TRY(make_tmap_2d(&xb, a.x_perm, a.R, a.d, 2, kBoxN, kBK, true));
+  const int box_gu = boxn_of(plan.bn_gateup), box_dn = boxn_of(plan.bn_down);
+  MOE_TRY(make_tmap_2d(&xb, a.x_perm, a.R, a.d, 2, box_gu, kBK, true));
   MOE_TRY(make_tmap_2d(&wd, a.w_down, (uint64_t)a.G * a.d, a.ffn, wb, kBM, kBK, wsw));
-  MOE_TRY(make_tmap_2d(&hb, a.h, a.R, a.ffn, 2, kBoxN, kBK, true));
+  MOE_TRY(make_tmap_2d(&hb, a.h, a.R, a.ffn, 2, box_dn, kBK, true));
 
   TcParams p{};
   p.G = a.G;
@@ -566,6 +590,7 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   p.out_f32 = 0;
   p.scale0 = a.s_gate;
   p.scale1 = a.s_up;
+  p.boxn = box_gu;
   MOE_TRY(launch_mode<kGateUp>(plan.bn_gateup, fp8, p, wg, wu, xb, plan.grid, s));
   if (mid != nullptr) MOE_TRY_CUDA(cudaEventRecord(mid, s));
 
@@ -576,6 +601,7 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   p.out_f32 = plan.splits_down > 1 ? 1 : 0;
   p.scale0 = a.s_down;
   p.scale1 = nullptr;
+  p.boxn = box_dn;
   MOE_TRY(launch_mode<kDown>(plan.bn_down, fp8, p, wd, wd, hb, plan.grid, s));
   return MOE_OK;
 }
@@ -587,7 +613,7 @@ moe_status tc_dense_f32_launch(const void* a, const void* b, float* out, int M, 
   if (M % kBM != 0 || K % 8 != 0 || splits < 1) return MOE_ERR_UNSUPPORTED;
   CUtensorMap ta, tb;
   MOE_TRY(make_tmap_2d(&ta, a, (uint64_t)M, K, 2, kBM, kBK, true));
-  MOE_TRY(make_tmap_2d(&tb, b, (uint64_t)N, K, 2, kBoxN, kBK, true));
+  MOE_TRY(make_tmap_2d(&tb, b, (uint64_t)N, K, 2, kBoxLarge, kBK, true));
   TcParams p{};
   p.G = 1;
   p.dense = 1;
@@ -599,6 +625,7 @@ moe_status tc_dense_f32_launch(const void* a, const void* b, float* out, int M, 
   p.out_f32 = 1;
   p.status = status;
   p.timeout_ns = timeout_ns;
+  p.boxn = kBoxLarge;
   return launch_mode<kDown>(128, false, p, ta, ta, tb, num_sms, s);
 }
 
@@ -614,6 +641,7 @@ moe_status tc_selftest_launch(int* status, long long timeout_ns, cudaStream_t s)
   p.status = status;
   p.timeout_ns = timeout_ns;
   p.selftest = 1;
+  p.boxn = kBoxSmall;
   return launch_one<kGateUp, 32, false>(p, dummy, dummy, dummy, 1, s);
 }
 

@@ -221,6 +221,7 @@ GROUP_COUNTS = {
     "ragged": [0, 1, 15, 16, 17, 31, 32, 33, 100, 127, 128, 129, 0, 300, 2, 5],
     "decode": [1, 0, 2, 1, 0, 0, 1, 3, 0, 1, 2, 1, 0, 0, 1, 1],
     "one_hot_expert": [0] * 7 + [517] + [0] * 8,
+    "prefill_like": [300, 0, 257, 513, 129, 128, 255, 256, 1, 600, 380, 17, 0, 999, 64, 2],
 }
 
 
@@ -267,6 +268,46 @@ def _fp8_stack(E, rows, cols, gen, all_codes_expert=None):
         w[all_codes_expert].copy_(codes.repeat(n // len(codes) + 1)[:n].view(rows, cols))
         s[all_codes_expert].fill_(1.0 / 448.0)
     return w, s
+
+
+@pytest.mark.parametrize("bn", [32, 128, 256])
+@pytest.mark.parametrize("fp8", [False, True])
+def test_grouped_swiglu_every_tile_size(bn, fp8, monkeypatch):
+    # the same ragged groups through each tile-row count of both GEMMs
+    monkeypatch.setenv("MOE_BN_GATEUP", str(bn))
+    monkeypatch.setenv("MOE_BN_DOWN", str(bn))
+    counts = np.array(GROUP_COUNTS["prefill_like"])
+    E, d, f = len(counts), 256, 256
+    R = int(counts.sum())
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    g = torch.Generator(device=DEV).manual_seed(bn)
+    x = _bf16_rand((R, d), 1.0, g)
+    p = api.problem(R, d, f, E, 1, wfmt="fp8" if fp8 else "bf16")
+    if fp8:
+        wg, sg = _fp8_stack(E, f, d, g)
+        wu, su = _fp8_stack(E, f, d, g)
+        wd, sd = _fp8_stack(E, d, f, g)
+        ew = oracle.ExpertWeights("fp8", wg.cpu().numpy(), wu.cpu().numpy(), wd.cpu().numpy(),
+                                  sg.cpu().numpy(), su.cpu().numpy(), sd.cpu().numpy())
+    else:
+        wg, wu = _bf16_rand((E, f, d), d ** -0.5, g), _bf16_rand((E, f, d), d ** -0.5, g)
+        wd = _bf16_rand((E, d, f), d ** -0.5, g)
+        sg = su = sd = None
+        ew = oracle.ExpertWeights("bf16", inputs.to_numpy_stored(wg), inputs.to_numpy_stored(wu),
+                                  inputs.to_numpy_stored(wd))
+    assert api.moe_plan_info(p)["bn_gateup"] == bn
+    y = torch.full((R, d), float("nan"), dtype=torch.bfloat16, device=DEV)
+    api.moe_grouped_swiglu(p, x, torch.from_numpy(offsets).to(DEV), wg, wu, wd, sg, su, sd, y, api.workspace_for(p))
+    torch.cuda.synchronize()
+    xf, got = _f64(x), _f64(y)
+    ref = np.zeros_like(got)
+    for e in range(E):
+        a, b = offsets[e], offsets[e + 1]
+        if b > a:
+            ref[a:b] = oracle.swiglu_expert(xf[a:b], *ew.get(e))
+    assert np.isfinite(got).all()
+    assert np.abs(got - ref).max() <= (FP8_TOL if fp8 else BF16_TOL) * np.abs(ref).max()
+    assert np.sqrt(((got - ref) ** 2).mean()) <= 1e-2 * np.sqrt((ref ** 2).mean())
 
 
 @pytest.mark.parametrize("kind", ["ragged", "decode"])
