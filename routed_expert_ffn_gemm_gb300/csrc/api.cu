@@ -267,7 +267,7 @@ moe_status layer_forward_impl(const moe_problem* p, const void* x, const void* w
   const int R = p->T * p->k;
   auto mark = [&](int i) -> moe_status {
     if (timer != nullptr) {
-      MOE_TRY_CUDA(cudaEventRecord(timer->ev[i], s));
+      MOE_TRY_CUDA(cudaEventRecordWithFlags(timer->ev[i], s, cudaEventRecordExternal));
       timer->recorded = i + 1;
     }
     return MOE_OK;

@@ -96,7 +96,7 @@ moe_status simt_grouped_launch(const SimtGroupedArgs& a, cudaStream_t s, cudaEve
   simt_gateup_kernel<<<blocks, 256, smem_g, s>>>(a.R, a.d, a.ffn, a.E, a.x_perm, a.offsets,
                                                  a.w_gate, a.w_up, a.h);
   MOE_TRY_CUDA(cudaGetLastError());
-  if (mid != nullptr) MOE_TRY_CUDA(cudaEventRecord(mid, s));
+  if (mid != nullptr) MOE_TRY_CUDA(cudaEventRecordWithFlags(mid, s, cudaEventRecordExternal));
   simt_down_kernel<<<blocks, 256, smem_d, s>>>(a.R, a.d, a.ffn, a.E, a.h, a.offsets, a.w_down,
                                                a.y);
   MOE_TRY_CUDA(cudaGetLastError());

@@ -592,7 +592,7 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   p.scale1 = a.s_up;
   p.boxn = box_gu;
   MOE_TRY(launch_mode<kGateUp>(plan.bn_gateup, fp8, p, wg, wu, xb, plan.grid, s));
-  if (mid != nullptr) MOE_TRY_CUDA(cudaEventRecord(mid, s));
+  if (mid != nullptr) MOE_TRY_CUDA(cudaEventRecordWithFlags(mid, s, cudaEventRecordExternal));
 
   p.M = a.d;
   p.K = a.ffn;

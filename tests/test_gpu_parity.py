@@ -450,6 +450,35 @@ def test_layer_deepseek_v3_shaped_fp8_with_shared_expert(T, sample):
     _layer_check(shape, 0, FP8_TOL, tokens=tokens)
 
 
+def test_layer_forward_captured_in_a_cuda_graph_with_stage_timer():
+    # the whole layer is enqueued without host synchronisation, so it can be
+    # captured; the stage timer's events become timestamp nodes
+    shape = inputs.MoEShape("small", T=40, d=256, ffn=384, E=16, k=4)
+    case = inputs.make_case(shape, 2, DEV)
+    p = api.problem_of(shape)
+    ws = api.workspace_for(p)
+    direct = api.layer_forward(p, case, workspace=ws)
+    out = torch.empty_like(direct)
+    timer = api.StageTimer()
+    api.layer_forward(p, case, out=out, workspace=ws, timer=timer)  # warm (function attributes)
+    torch.cuda.synchronize()
+    out.zero_()
+    g = torch.cuda.CUDAGraph()
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            api.layer_forward(p, case, out=out, workspace=ws, timer=timer)
+    torch.cuda.current_stream().wait_stream(stream)
+    g.replay()
+    torch.cuda.synchronize()
+    ms = timer.read()
+    assert set(ms) == set(api.STAGES) and all(v >= 0.0 for v in ms.values())
+    assert ms["gate_up"] > 0.0 and ms["down"] > 0.0
+    assert torch.equal(out, direct)  # deterministic: same bits as the direct call
+    timer.close()
+
+
 def test_layer_empty_batch():
     shape = inputs.WORKLOADS["qwen3_30b_a3b"].with_T(0)
     case = inputs.make_weights(shape, 0, DEV)
