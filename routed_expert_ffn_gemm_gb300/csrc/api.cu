@@ -89,6 +89,7 @@ T* at(void* ws, size_t off) {
 }
 
 __global__ void set_pair_kernel(int32_t* p, int a, int b) {
+  griddep_begin();
   p[0] = a;
   p[1] = b;
 }
@@ -267,7 +268,7 @@ moe_status layer_forward_impl(const moe_problem* p, const void* x, const void* w
   const int R = p->T * p->k;
   auto mark = [&](int i) -> moe_status {
     if (timer != nullptr) {
-      MOE_TRY_CUDA(cudaEventRecordWithFlags(timer->ev[i], s, cudaEventRecordExternal));
+      MOE_TRY_CUDA(record_event(timer->ev[i], s));
       timer->recorded = i + 1;
     }
     return MOE_OK;
@@ -309,7 +310,7 @@ moe_status layer_forward_impl(const moe_problem* p, const void* x, const void* w
   void* sh_y = nullptr;
   if (has_shared) {
     int32_t* sh_off = at<int32_t>(workspace, L.sh_offsets);
-    set_pair_kernel<<<1, 1, 0, s>>>(sh_off, 0, p->T);
+    MOE_TRY_CUDA(launch_k(set_pair_kernel, dim3(1), dim3(1), 0, s, sh_off, 0, p->T));
     MOE_TRY_CUDA(cudaGetLastError());
     sh_y = at<uint8_t>(workspace, L.sh_y);
     MOE_TRY(run_grouped(path, p->T, p->d, p->ffn_shared, 1, p->act_dtype, x, sh_off,

@@ -52,6 +52,7 @@ __global__ void __launch_bounds__(256) combine_kernel(int T, int k, int d, int R
                                                       const float* __restrict__ w,
                                                       const ActT* __restrict__ shared,
                                                       ActT* __restrict__ out, int* status) {
+  griddep_begin();
   const int groups = d / 8;
   const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (gid >= (long long)T * groups) return;
@@ -100,18 +101,18 @@ moe_status combine_launch(const CombineArgs& a, cudaStream_t s) {
     const __nv_bfloat16* sh = static_cast<const __nv_bfloat16*>(a.shared);
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
     if (a.y_partials > 0)
-      combine_kernel<__nv_bfloat16, float><<<blocks, 256, 0, s>>>(
+      MOE_TRY_CUDA(launch_k(combine_kernel<__nv_bfloat16, float>, dim3(blocks), dim3(256), 0, s, 
           a.T, a.k, a.d, R, a.y_partials, static_cast<const float*>(a.y), a.inv_row, a.w, sh, out,
-          ctx.status);
+          ctx.status));
     else
-      combine_kernel<__nv_bfloat16, __nv_bfloat16><<<blocks, 256, 0, s>>>(
+      MOE_TRY_CUDA(launch_k(combine_kernel<__nv_bfloat16, __nv_bfloat16>, dim3(blocks), dim3(256), 0, s, 
           a.T, a.k, a.d, R, 1, static_cast<const __nv_bfloat16*>(a.y), a.inv_row, a.w, sh, out,
-          ctx.status);
+          ctx.status));
   } else if (a.act_dtype == MOE_F32) {
-    combine_kernel<float, float><<<blocks, 256, 0, s>>>(
+    MOE_TRY_CUDA(launch_k(combine_kernel<float, float>, dim3(blocks), dim3(256), 0, s, 
         a.T, a.k, a.d, R, a.y_partials > 0 ? a.y_partials : 1, static_cast<const float*>(a.y),
         a.inv_row, a.w, static_cast<const float*>(a.shared), static_cast<float*>(a.out),
-        ctx.status);
+        ctx.status));
   } else {
     return MOE_ERR_UNSUPPORTED;
   }

@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/moe.h"
 
 namespace moe {
@@ -51,6 +53,57 @@ inline moe_status cuda_status(cudaError_t err) {
 // `box_cols` x `box_rows`, 128-byte swizzle or none, zero fill out of bounds.
 moe_status make_tmap_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                         int elem_bytes, uint32_t box_rows, uint32_t box_cols, bool swizzle128);
+
+// ---------------------------------------------------------------------------
+// launches: programmatic dependent launch
+// ---------------------------------------------------------------------------
+
+// Every kernel of the library is launched with programmatic stream
+// serialisation: it may be scheduled while the previous kernel on the stream
+// is still finishing, and it calls griddep_wait() before its first access to
+// global memory, which returns once the previous grid has completed and its
+// writes are visible.  This overlaps launch latency and kernel prologues with
+// the previous kernel's tail.  MOE_PDL=0 in the environment launches plainly.
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// Record `ev` on `s`; inside stream capture as an external (timestamp) node,
+// so a captured layer keeps its stage times.
+inline cudaError_t record_event(cudaEvent_t ev, cudaStream_t s) {
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &st);
+  if (e != cudaSuccess) return e;
+  return st == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal)
+                                             : cudaEventRecord(ev, s);
+}
+
+// Wait until the previous grid on the stream has completed (no-op when the
+// kernel was not launched as a programmatic dependent).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next grid on the stream be scheduled (it still waits in
+// griddep_wait() for this grid to complete).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_begin() {
+  griddep_wait();
+  griddep_launch_dependents();
+}
 
 // ---------------------------------------------------------------------------
 // device-side status word

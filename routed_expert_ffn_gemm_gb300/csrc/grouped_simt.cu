@@ -36,6 +36,7 @@ __global__ void __launch_bounds__(256) simt_gateup_kernel(int R, int d, int ffn,
                                                           const float* __restrict__ wg,
                                                           const float* __restrict__ wu,
                                                           float* __restrict__ h) {
+  griddep_begin();
   extern __shared__ float xs[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int r = blockIdx.x; r < R; r += gridDim.x) {
@@ -64,6 +65,7 @@ __global__ void __launch_bounds__(256) simt_down_kernel(int R, int d, int ffn, i
                                                         const int32_t* __restrict__ offsets,
                                                         const float* __restrict__ wd,
                                                         float* __restrict__ y) {
+  griddep_begin();
   extern __shared__ float hs[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int r = blockIdx.x; r < R; r += gridDim.x) {
@@ -93,12 +95,12 @@ moe_status simt_grouped_launch(const SimtGroupedArgs& a, cudaStream_t s, cudaEve
   MOE_TRY_CUDA(cudaFuncSetAttribute(simt_down_kernel,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_d));
   const int blocks = a.R < 65535 ? a.R : 65535;
-  simt_gateup_kernel<<<blocks, 256, smem_g, s>>>(a.R, a.d, a.ffn, a.E, a.x_perm, a.offsets,
-                                                 a.w_gate, a.w_up, a.h);
+  MOE_TRY_CUDA(launch_k(simt_gateup_kernel, dim3(blocks), dim3(256), smem_g, s, a.R, a.d, a.ffn, a.E, a.x_perm, a.offsets,
+                                                 a.w_gate, a.w_up, a.h));
   MOE_TRY_CUDA(cudaGetLastError());
-  if (mid != nullptr) MOE_TRY_CUDA(cudaEventRecordWithFlags(mid, s, cudaEventRecordExternal));
-  simt_down_kernel<<<blocks, 256, smem_d, s>>>(a.R, a.d, a.ffn, a.E, a.h, a.offsets, a.w_down,
-                                               a.y);
+  if (mid != nullptr) MOE_TRY_CUDA(record_event(mid, s));
+  MOE_TRY_CUDA(launch_k(simt_down_kernel, dim3(blocks), dim3(256), smem_d, s, a.R, a.d, a.ffn, a.E, a.h, a.offsets, a.w_down,
+                                               a.y));
   MOE_TRY_CUDA(cudaGetLastError());
   return MOE_OK;
 }

@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
   int* prefix = reinterpret_cast<int*>(smem + C::PREFIX_OFF);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint64_t deadline = ptx::globaltimer_ns() + (uint64_t)p.timeout_ns;
+  griddep_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -205,6 +205,11 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
     ptx::tmem_relinquish();
   }
+
+  // The prologue above touches no global memory; from here on the previous
+  // kernel's results (offsets, operands) must be complete.
+  griddep_wait();
+  const uint64_t deadline = ptx::globaltimer_ns() + (uint64_t)p.timeout_ns;
 
   // Group row ranges (clamped into [0, R]) and the exclusive prefix of
   // per-group tile counts ceil(rows / BN).
@@ -492,7 +497,7 @@ moe_status launch_one(const TcParams& p, const CUtensorMap& a0, const CUtensorMa
   using C = Cfg<MODE, BN, FP8>;
   auto kern = tc_grouped_kernel<MODE, BN, FP8>;
   MOE_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES));
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(p, a0, a1, b);
+  MOE_TRY_CUDA(launch_k(kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, s, p, a0, a1, b));
   MOE_TRY_CUDA(cudaGetLastError());
   return MOE_OK;
 }
@@ -523,16 +528,20 @@ int boxn_of(int bn) { return bn >= 128 ? kBoxLarge : kBoxSmall; }
 }  // namespace
 
 // Rows per tile from the expected rows per expert: 32 for decode (a few rows
-// each), 128 in between, 256 for prefill (halves operand bytes per flop).
+// each), else 128; the bf16 down GEMM takes 256 at prefill (half the operand
+// bytes per flop with its accumulators still double-buffered).  Measured on
+// GB300: gate/up at 256 rows loses its epilogue overlap (one TMEM buffer)
+// and runs slower than at 128; FP8 tiles of 256 leave too few stages.
 // MOE_BN_GATEUP / MOE_BN_DOWN override (tuning).
-TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int /*w_dtype*/) {
+TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype) {
   TcPlan pl;
   const double R = (double)T * k;
   const double mean = R / E;
   const double est_max = mean + 3.0 * __builtin_sqrt(mean) + 1.0;
-  const int bn = est_max <= 32.0 ? 32 : (mean >= 128.0 ? 256 : 128);
+  const int bn = est_max <= 32.0 ? 32 : 128;
+  const int bn_dn = (bn == 128 && mean >= 128.0 && w_dtype != MOE_FP8_E4M3) ? 256 : bn;
   pl.bn_gateup = bn_ok(env_int("MOE_BN_GATEUP")) ? env_int("MOE_BN_GATEUP") : bn;
-  pl.bn_down = bn_ok(env_int("MOE_BN_DOWN")) ? env_int("MOE_BN_DOWN") : bn;
+  pl.bn_down = bn_ok(env_int("MOE_BN_DOWN")) ? env_int("MOE_BN_DOWN") : bn_dn;
   const double touched = E < R ? E : R;
   const double tiles_a = R / pl.bn_down;
   const int tiles = (int)(touched > tiles_a ? touched : tiles_a + 0.5);
@@ -592,7 +601,7 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   p.scale1 = a.s_up;
   p.boxn = box_gu;
   MOE_TRY(launch_mode<kGateUp>(plan.bn_gateup, fp8, p, wg, wu, xb, plan.grid, s));
-  if (mid != nullptr) MOE_TRY_CUDA(cudaEventRecordWithFlags(mid, s, cudaEventRecordExternal));
+  if (mid != nullptr) MOE_TRY_CUDA(record_event(mid, s));
 
   p.M = a.d;
   p.K = a.ffn;

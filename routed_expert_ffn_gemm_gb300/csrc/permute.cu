@@ -10,10 +10,11 @@
 // with warp match_any + popc and prefix sums over warps, chunks and experts;
 // no result depends on the order of atomic operations.
 //
-//   small path  (R <= 2048): one block computes every map, then a
-//                            grid-wide row gather moves x -> x_perm;
+//   small path  (R <= 2048): one block computes every map;
 //   chunked path (any R):    count per 256-assignment chunk, one scan block,
-//                            then per chunk: ranks, maps and row moves.
+//                            then per chunk: ranks and maps;
+// then a grid-wide row gather moves x -> x_perm (one warp per row; the
+// chunked blocks are too few to move rows at full bandwidth themselves).
 // Row moves are 16-byte vector loads/stores, one warp per row.  When the
 // experts run on f16 operands (FP8 weights) the row move also rounds the
 // bf16 token vector to f16 (saturating to the largest finite f16).
@@ -104,6 +105,7 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(
     int R, int k, int E, const int32_t* __restrict__ idx, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ perm_token,
     int32_t* __restrict__ inv_row, int* status) {
+  griddep_begin();
   extern __shared__ int sm[];
   int* wcnt = sm;                        // [kSmallWarps][E]
   int* lrank = wcnt + kSmallWarps * E;   // [R]
@@ -156,10 +158,12 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(int R, int E, int vec_
                                                           const int32_t* __restrict__ perm_token,
                                                           const uint4* __restrict__ x,
                                                           uint4* __restrict__ x_perm, int to_f16) {
+  griddep_begin();
   const int lane = threadIdx.x & 31;
   const int nrows = min(R, offsets[E]);
   for (int r = blockIdx.x * 8 + (threadIdx.x >> 5); r < nrows; r += gridDim.x * 8) {
     const size_t src = (size_t)perm_token[r] * vec_per_row, dst = (size_t)r * vec_per_row;
+#pragma unroll 4
     for (int v = lane; v < vec_per_row; v += 32) x_perm[dst + v] = move16(x[src + v], to_f16);
   }
 }
@@ -167,6 +171,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(int R, int E, int vec_
 // n elements of bf16 -> f16, 8 per thread.
 __global__ void __launch_bounds__(256) bf16_to_f16_kernel(const uint4* __restrict__ src,
                                                           uint4* __restrict__ dst, size_t nvec) {
+  griddep_begin();
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < nvec; i += (size_t)gridDim.x * blockDim.x)
     dst[i] = bf16x8_to_f16x8(src[i]);
 }
@@ -175,6 +180,7 @@ __global__ void __launch_bounds__(256) bf16_to_f16_kernel(const uint4* __restric
 __global__ void __launch_bounds__(256) permute_count_kernel(int R, int E,
                                                             const int32_t* __restrict__ idx,
                                                             int32_t* __restrict__ chunk_cnt) {
+  griddep_begin();
   extern __shared__ int cnt[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
@@ -192,6 +198,7 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int n_chunks, int E,
                                                             int32_t* __restrict__ chunk_cnt,
                                                             int32_t* __restrict__ counts,
                                                             int32_t* __restrict__ offsets) {
+  griddep_begin();
   __shared__ int warp_tot[32];
   const int e = threadIdx.x;
   int tot = 0;
@@ -218,6 +225,7 @@ __global__ void __launch_bounds__(256) permute_scatter_kernel(
     const int32_t* __restrict__ chunk_base, int32_t* __restrict__ perm_token,
     int32_t* __restrict__ inv_row, const uint4* __restrict__ x, uint4* __restrict__ x_perm,
     int* status, int to_f16) {
+  griddep_begin();
   extern __shared__ int sm[];
   int* wcnt = sm;                 // [8][E]
   int* lrank = wcnt + 8 * E;      // [kChunk]
@@ -270,7 +278,7 @@ moe_status bf16_to_f16_launch(const void* src, void* dst, size_t n, cudaStream_t
   if (n % 8 != 0) return MOE_ERR_UNSUPPORTED;
   const size_t nvec = n / 8;
   const int blocks = (int)((nvec + 255) / 256 < 4096 ? (nvec + 255) / 256 : 4096);
-  bf16_to_f16_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst), nvec);
+  MOE_TRY_CUDA(launch_k(bf16_to_f16_kernel, dim3(blocks), dim3(256), 0, s, static_cast<const uint4*>(src), static_cast<uint4*>(dst), nvec));
   MOE_TRY_CUDA(cudaGetLastError());
   return MOE_OK;
 }
@@ -284,7 +292,17 @@ size_t permute_scratch_bytes(int T, int k, int E) {
 int permute_launch_count(int T, int k, bool move_rows) {
   const long long R = (long long)T * k;
   if (R == 0) return 0;
-  return R <= kSmallMaxR ? 1 + (move_rows ? 1 : 0) : 3;
+  return (R <= kSmallMaxR ? 1 : 3) + (move_rows ? 1 : 0);
+}
+
+// x_perm[r] = x[perm_token[r]] over a grid-stride of warps.
+moe_status gather_launch(const PermuteArgs& a, int R, int vec_per_row, cudaStream_t s) {
+  if (a.x_perm == nullptr) return MOE_OK;
+  const int blocks = min(4096, (R + 7) / 8);
+  MOE_TRY_CUDA(launch_k(gather_rows_kernel, dim3(blocks), dim3(256), 0, s, R, a.E, vec_per_row,
+                        a.offsets, a.perm_token, static_cast<const uint4*>(a.x),
+                        static_cast<uint4*>(a.x_perm), a.to_f16));
+  return MOE_OK;
 }
 
 moe_status permute_launch(const PermuteArgs& a, cudaStream_t s) {
@@ -300,32 +318,25 @@ moe_status permute_launch(const PermuteArgs& a, cudaStream_t s) {
     const size_t smem = small_smem(R, a.E);
     MOE_TRY_CUDA(cudaFuncSetAttribute(permute_small_kernel,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    permute_small_kernel<<<1, 1024, smem, s>>>(R, a.k, a.E, a.idx, a.counts, a.offsets,
-                                               a.perm_token, a.inv_row, a.status);
+    MOE_TRY_CUDA(launch_k(permute_small_kernel, dim3(1), dim3(1024), smem, s, R, a.k, a.E, a.idx, a.counts, a.offsets,
+                                               a.perm_token, a.inv_row, a.status));
     MOE_TRY_CUDA(cudaGetLastError());
-    if (a.x_perm != nullptr) {
-      const int blocks = min(1024, (R + 7) / 8);
-      gather_rows_kernel<<<blocks, 256, 0, s>>>(R, a.E, vec_per_row, a.offsets, a.perm_token,
-                                                static_cast<const uint4*>(a.x),
-                                                static_cast<uint4*>(a.x_perm), a.to_f16);
-      MOE_TRY_CUDA(cudaGetLastError());
-    }
-    return MOE_OK;
+    return gather_launch(a, R, vec_per_row, s);
   }
   if (a.chunk_scratch == nullptr) return MOE_ERR_WORKSPACE;
   const int n_chunks = (R + kChunk - 1) / kChunk;
-  permute_count_kernel<<<n_chunks, 256, sizeof(int) * a.E, s>>>(R, a.E, a.idx, a.chunk_scratch);
+  MOE_TRY_CUDA(launch_k(permute_count_kernel, dim3(n_chunks), dim3(256), sizeof(int) * a.E, s, R, a.E, a.idx, a.chunk_scratch));
   MOE_TRY_CUDA(cudaGetLastError());
-  permute_scan_kernel<<<1, 1024, 0, s>>>(n_chunks, a.E, a.chunk_scratch, a.counts, a.offsets);
+  MOE_TRY_CUDA(launch_k(permute_scan_kernel, dim3(1), dim3(1024), 0, s, n_chunks, a.E, a.chunk_scratch, a.counts, a.offsets));
   MOE_TRY_CUDA(cudaGetLastError());
   const size_t smem = sizeof(int) * (8 * (size_t)a.E + 2 * kChunk);
   MOE_TRY_CUDA(cudaFuncSetAttribute(permute_scatter_kernel,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-  permute_scatter_kernel<<<n_chunks, 256, smem, s>>>(
+  MOE_TRY_CUDA(launch_k(permute_scatter_kernel, dim3(n_chunks), dim3(256), smem, s, 
       R, a.k, a.E, vec_per_row, a.idx, a.chunk_scratch, a.perm_token, a.inv_row,
-      static_cast<const uint4*>(a.x), static_cast<uint4*>(a.x_perm), a.status, a.to_f16);
+      static_cast<const uint4*>(a.x), static_cast<uint4*>(nullptr), a.status, a.to_f16));
   MOE_TRY_CUDA(cudaGetLastError());
-  return MOE_OK;
+  return gather_launch(a, R, vec_per_row, s);
 }
 
 }  // namespace moe

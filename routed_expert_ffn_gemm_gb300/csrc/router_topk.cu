@@ -99,6 +99,7 @@ __global__ void __launch_bounds__(kThreads) router_kernel(
     int T, int d, int E, int k, const ActT* __restrict__ x, const ActT* __restrict__ wr,
     const float* __restrict__ bias, const float* __restrict__ logits_in,
     float* __restrict__ logits_out, int32_t* __restrict__ idx, float* __restrict__ w) {
+  griddep_begin();
   constexpr int VN = VecN<ActT>::N;
   extern __shared__ __align__(16) uint8_t sm[];
   const bool fused = gridDim.y == 1;
@@ -175,6 +176,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(int T, int E, int k,
                                                         const float* __restrict__ logits,
                                                         int32_t* __restrict__ idx,
                                                         float* __restrict__ w) {
+  griddep_begin();
   const int t = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
   if (t < T) topk_row(logits + (size_t)t * E, E, k, idx + (size_t)t * k, w + (size_t)t * k);
 }
@@ -184,6 +186,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(int T, int E, int k,
 __global__ void __launch_bounds__(kThreads) topk_partials_kernel(
     int T, int E, int k, int S, const float* __restrict__ part, const float* __restrict__ bias,
     float* __restrict__ logits_out, int32_t* __restrict__ idx, float* __restrict__ w) {
+  griddep_begin();
   extern __shared__ float rows[];  // [8][E]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * (kThreads / 32) + warp;
@@ -222,19 +225,19 @@ moe_status launch_typed(const RouterArgs& a, float* logits_scratch, cudaStream_t
     if (tt == 1) {
       auto kern = router_kernel<ActT, 1, 1>;
       MOE_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-      kern<<<grid, kThreads, smem, s>>>(a.T, a.d, a.E, a.k, static_cast<const ActT*>(a.x),
+      MOE_TRY_CUDA(launch_k(kern, dim3(grid), dim3(kThreads), smem, s, a.T, a.d, a.E, a.k, static_cast<const ActT*>(a.x),
                                         static_cast<const ActT*>(a.w_router), a.bias, nullptr,
-                                        logits_scratch, a.idx, a.w);
+                                        logits_scratch, a.idx, a.w));
     } else {
       auto kern = router_kernel<ActT, 1, kTT>;
       MOE_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-      kern<<<grid, kThreads, smem, s>>>(a.T, a.d, a.E, a.k, static_cast<const ActT*>(a.x),
+      MOE_TRY_CUDA(launch_k(kern, dim3(grid), dim3(kThreads), smem, s, a.T, a.d, a.E, a.k, static_cast<const ActT*>(a.x),
                                         static_cast<const ActT*>(a.w_router), a.bias, nullptr,
-                                        logits_scratch, a.idx, a.w);
+                                        logits_scratch, a.idx, a.w));
     }
     MOE_TRY_CUDA(cudaGetLastError());
     if (gy > 1) {
-      topk_kernel<<<(a.T + 7) / 8, kThreads, 0, s>>>(a.T, a.E, a.k, logits_scratch, a.idx, a.w);
+      MOE_TRY_CUDA(launch_k(topk_kernel, dim3((a.T + 7) / 8), dim3(kThreads), 0, s, a.T, a.E, a.k, logits_scratch, a.idx, a.w));
       MOE_TRY_CUDA(cudaGetLastError());
     }
     return MOE_OK;
@@ -245,9 +248,9 @@ moe_status launch_typed(const RouterArgs& a, float* logits_scratch, cudaStream_t
   if (smem > 220 * 1024) return MOE_ERR_UNSUPPORTED;
   auto kern = router_kernel<ActT, 4, kTT>;
   MOE_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-  kern<<<dim3(tiles, 1), kThreads, smem, s>>>(a.T, a.d, a.E, a.k, static_cast<const ActT*>(a.x),
+  MOE_TRY_CUDA(launch_k(kern, dim3(dim3(tiles, 1)), dim3(kThreads), smem, s, a.T, a.d, a.E, a.k, static_cast<const ActT*>(a.x),
                                               static_cast<const ActT*>(a.w_router), a.bias,
-                                              a.logits_in, a.logits_out, a.idx, a.w);
+                                              a.logits_in, a.logits_out, a.idx, a.w));
   MOE_TRY_CUDA(cudaGetLastError());
   if (a.logits_in != nullptr && a.logits_out != nullptr && a.logits_out != a.logits_in)
     MOE_TRY_CUDA(cudaMemcpyAsync(a.logits_out, a.logits_in, sizeof(float) * a.T * a.E,
@@ -294,8 +297,8 @@ moe_status router_topk_launch(const RouterArgs& a, cudaStream_t s) {
     // element is read, then rewritten (biased) by the same lane
     float* lo = a.logits_out;
     if (lo == a.tc_scratch && a.tc_splits > 1) return MOE_ERR_INVALID_ARG;
-    topk_partials_kernel<<<(a.T + 7) / 8, kThreads, smem, s>>>(a.T, a.E, a.k, a.tc_splits, a.tc_scratch,
-                                                               a.bias, lo, a.idx, a.w);
+    MOE_TRY_CUDA(launch_k(topk_partials_kernel, dim3((a.T + 7) / 8), dim3(kThreads), smem, s, a.T, a.E, a.k, a.tc_splits, a.tc_scratch,
+                                                               a.bias, lo, a.idx, a.w));
     MOE_TRY_CUDA(cudaGetLastError());
     return MOE_OK;
   }

@@ -1,6 +1,7 @@
 // Library runtime: per-device context (SM count, kernel status word),
 // CUDA error text, TMA tensor-map encoding, status strings.
 #include <mutex>
+#include <stdlib.h>
 #include <string.h>
 
 #include "common.cuh"
@@ -35,6 +36,14 @@ void record_cuda_error_text(const char* text) {
 
 void record_cuda_error(cudaError_t err) {
   record_cuda_error_text(cudaGetErrorString(err));
+}
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("MOE_PDL");
+    return !(v != nullptr && v[0] == '0');
+  }();
+  return on;
 }
 
 moe_status device_ctx(DeviceCtx* out) {
