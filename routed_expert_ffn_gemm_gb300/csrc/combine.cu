@@ -14,6 +14,8 @@
 namespace moe {
 namespace {
 
+constexpr int kMaxSplits = 8;  // the down GEMM uses at most 8 K splits
+
 __device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
   const float4 a = *reinterpret_cast<const float4*>(p);
   const float4 b = *reinterpret_cast<const float4*>(p + 4);
@@ -45,7 +47,7 @@ __device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&v)[8]) {
   *reinterpret_cast<uint4*>(p) = a;
 }
 
-template <typename ActT, typename YT>
+template <typename ActT, typename YT, bool SPLIT>
 __global__ void __launch_bounds__(256) combine_kernel(int T, int k, int d, int R, int S,
                                                       const YT* __restrict__ y,
                                                       const int32_t* __restrict__ inv_row,
@@ -60,6 +62,7 @@ __global__ void __launch_bounds__(256) combine_kernel(int T, int k, int d, int R
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll 4
   for (int j = 0; j < k; ++j) {
     const int r = inv_row[(size_t)t * k + j];
     if (r < 0 || r >= R) {
@@ -67,14 +70,28 @@ __global__ void __launch_bounds__(256) combine_kernel(int T, int k, int d, int R
       continue;
     }
     const float wj = w[(size_t)t * k + j];
-    float part[8];
-    load8(y + (size_t)r * d + c, part);
-    for (int s = 1; s < S; ++s) {
-      float q[8];
-      load8(y + ((size_t)s * R + r) * d + c, q);
+    if (!SPLIT) {
+      float part[8];
+      load8(y + (size_t)r * d + c, part);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) part[i] += q[i];
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, part[i], acc[i]);
+      continue;
     }
+    // issue every partial's load before summing (split counts <= 8), so the
+    // loads are in flight together; the sum is still in order s = 0..S-1
+    float q[kMaxSplits][8];
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s)
+      if (s < S) load8(y + ((size_t)s * R + r) * d + c, q[s]);
+    float part[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) part[i] = q[0][i];
+#pragma unroll
+    for (int s = 1; s < kMaxSplits; ++s)
+      if (s < S) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) part[i] += q[s][i];
+      }
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, part[i], acc[i]);
   }
@@ -91,6 +108,7 @@ __global__ void __launch_bounds__(256) combine_kernel(int T, int k, int d, int R
 
 moe_status combine_launch(const CombineArgs& a, cudaStream_t s) {
   if (a.T == 0) return MOE_OK;
+  if (a.y_partials > kMaxSplits) return MOE_ERR_UNSUPPORTED;
   if (a.d % 8 != 0) return MOE_ERR_UNSUPPORTED;
   DeviceCtx ctx;
   MOE_TRY(device_ctx(&ctx));
@@ -101,18 +119,24 @@ moe_status combine_launch(const CombineArgs& a, cudaStream_t s) {
     const __nv_bfloat16* sh = static_cast<const __nv_bfloat16*>(a.shared);
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
     if (a.y_partials > 0)
-      MOE_TRY_CUDA(launch_k(combine_kernel<__nv_bfloat16, float>, dim3(blocks), dim3(256), 0, s, 
+      MOE_TRY_CUDA(launch_k(combine_kernel<__nv_bfloat16, float, true>, dim3(blocks), dim3(256), 0, s, 
           a.T, a.k, a.d, R, a.y_partials, static_cast<const float*>(a.y), a.inv_row, a.w, sh, out,
           ctx.status));
     else
-      MOE_TRY_CUDA(launch_k(combine_kernel<__nv_bfloat16, __nv_bfloat16>, dim3(blocks), dim3(256), 0, s, 
+      MOE_TRY_CUDA(launch_k(combine_kernel<__nv_bfloat16, __nv_bfloat16, false>, dim3(blocks), dim3(256), 0, s, 
           a.T, a.k, a.d, R, 1, static_cast<const __nv_bfloat16*>(a.y), a.inv_row, a.w, sh, out,
           ctx.status));
   } else if (a.act_dtype == MOE_F32) {
-    MOE_TRY_CUDA(launch_k(combine_kernel<float, float>, dim3(blocks), dim3(256), 0, s, 
-        a.T, a.k, a.d, R, a.y_partials > 0 ? a.y_partials : 1, static_cast<const float*>(a.y),
-        a.inv_row, a.w, static_cast<const float*>(a.shared), static_cast<float*>(a.out),
-        ctx.status));
+    if (a.y_partials > 1)
+      MOE_TRY_CUDA(launch_k(combine_kernel<float, float, true>, dim3(blocks), dim3(256), 0, s,
+          a.T, a.k, a.d, R, a.y_partials, static_cast<const float*>(a.y),
+          a.inv_row, a.w, static_cast<const float*>(a.shared), static_cast<float*>(a.out),
+          ctx.status));
+    else
+      MOE_TRY_CUDA(launch_k(combine_kernel<float, float, false>, dim3(blocks), dim3(256), 0, s,
+          a.T, a.k, a.d, R, 1, static_cast<const float*>(a.y),
+          a.inv_row, a.w, static_cast<const float*>(a.shared), static_cast<float*>(a.out),
+          ctx.status));
   } else {
     return MOE_ERR_UNSUPPORTED;
   }

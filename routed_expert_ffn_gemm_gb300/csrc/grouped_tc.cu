@@ -87,20 +87,28 @@ struct Cfg {
   static constexpr int A_BYTES = kBM * kBK * 2;                // 16 KB bf16 tile (MMA operand)
   static constexpr int B_BYTES = BN * kBK * 2;
   static constexpr int STG_BYTES = FP8 ? kBM * kBK : 0;        // 8 KB E4M3 staging tile
-  static constexpr int B_OFF = NA * A_BYTES;
-  static constexpr int STG_OFF = B_OFF + B_BYTES;
-  static constexpr int STAGE_BYTES = STG_OFF + NA * STG_BYTES; // multiple of 1024
+  // bf16: one ring of TMA slots [A0 A1 | B] read by the MMA.  FP8: a deep
+  // ring of TMA slots [E4M3 A0 A1 | B] (cheap bytes: it hides HBM latency)
+  // and a short ring of OSTAGES f16 operand slots [A0 A1] that the
+  // converters fill and the MMA reads.
+  static constexpr int OSTAGES = FP8 ? 2 : 0;
+  static constexpr int OPND_BYTES = NA * A_BYTES;
+  static constexpr int RING_OFF = OSTAGES * OPND_BYTES;
+  static constexpr int W_BYTES = FP8 ? STG_BYTES : A_BYTES;    // weight tile bytes in a TMA slot
+  static constexpr int B_OFF = NA * W_BYTES;
+  static constexpr int STAGE_BYTES = B_OFF + B_BYTES;           // multiple of 1024
   static constexpr int THREADS = kThreads + (FP8 ? kConvThreads : 0);
   // TMEM: one accumulator buffer = NA accumulators of max(BN,128) columns
   static constexpr int UP_OFF = BN > 128 ? BN : 128;
   static constexpr int ACC_COLS = NA * UP_OFF;
   static constexpr int NBUF = 2 * ACC_COLS <= 512 ? 2 : 1;
   static constexpr int TAIL_BYTES = 8 * 36 + 16 + 4 * 2 * (kMaxGroups + 8);
-  static constexpr int STAGES_FIT = (kSmemLimit - 1024 - TAIL_BYTES) / STAGE_BYTES;
+  static constexpr int STAGES_FIT = (kSmemLimit - 1024 - TAIL_BYTES - RING_OFF) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 10 ? 10 : STAGES_FIT;
-  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
-  // barriers: full[S], empty[S], conv[S], acc_full[2], acc_empty[2], drain
-  static constexpr int NBARS = 3 * STAGES + 5;
+  static constexpr int BAR_OFF = RING_OFF + STAGES * STAGE_BYTES;
+  // barriers: full[S], empty[S], opnd_full[2], opnd_empty[2], acc_full[2],
+  // acc_empty[2], drain
+  static constexpr int NBARS = 2 * STAGES + 9;
   static constexpr int SLOT_OFF = BAR_OFF + 8 * NBARS;         // TMEM base address
   static constexpr int ABORT_OFF = SLOT_OFF + 8;
   static constexpr int OFFS_OFF = ABORT_OFF + 8;               // int offs[G+1]
@@ -170,10 +178,11 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
   const uint32_t bars = sbase + C::BAR_OFF;
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
-  auto conv_bar = [&](int s) { return bars + 8u * (2 * STAGES + s); };
-  auto accf_bar = [&](int b) { return bars + 8u * (3 * STAGES + b); };
-  auto acce_bar = [&](int b) { return bars + 8u * (3 * STAGES + 2 + b); };
-  const uint32_t drain_bar = bars + 8u * (3 * STAGES + 4);
+  auto ofull_bar = [&](int c) { return bars + 8u * (2 * STAGES + c); };
+  auto oempty_bar = [&](int c) { return bars + 8u * (2 * STAGES + 2 + c); };
+  auto accf_bar = [&](int b) { return bars + 8u * (2 * STAGES + 4 + b); };
+  auto acce_bar = [&](int b) { return bars + 8u * (2 * STAGES + 6 + b); };
+  const uint32_t drain_bar = bars + 8u * (2 * STAGES + 8);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::SLOT_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::ABORT_OFF);
   int* offs = reinterpret_cast<int*>(smem + C::OFFS_OFF);
@@ -186,7 +195,10 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(full_bar(s), 1);
       ptx::mbar_init(empty_bar(s), 1);
-      ptx::mbar_init(conv_bar(s), kConvThreads / 32);  // one arrival per converter warp
+    }
+    for (int c = 0; c < 2; ++c) {
+      ptx::mbar_init(ofull_bar(c), kConvThreads / 32);  // one arrival per converter warp
+      ptx::mbar_init(oempty_bar(c), 1);                 // the MMA's commit
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(accf_bar(b), 1);
@@ -272,7 +284,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
         const Unit x = decode_unit(u, offs, prefix, G, MT, S, BN);
         const int kb0 = x.ks * kb_per_split, kb1 = min(kblocks, kb0 + kb_per_split);
         const int nbox = (x.n_valid + p.boxn - 1) / p.boxn;
-        const uint32_t bytes = C::NA * (FP8 ? C::STG_BYTES : C::A_BYTES) + nbox * p.boxn * kBK * 2;
+        const uint32_t bytes = C::NA * C::W_BYTES + nbox * p.boxn * kBK * 2;
         const int arow = x.g * p.M + x.mt * kBM;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!ptx::mbar_wait_bounded(empty_bar(stage), phase ^ 1u, deadline, abort_flag)) {
@@ -281,12 +293,10 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
           }
           ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
           armed[stage] = (int)phase;
-          const uint32_t sa = sbase + stage * C::STAGE_BYTES;
           // weights: bf16 straight into the MMA tile, or E4M3 into staging
-          const uint32_t wa = FP8 ? sa + C::STG_OFF : sa;
-          const uint32_t wstep = FP8 ? C::STG_BYTES : C::A_BYTES;
-          ptx::tma_load_2d(wa, &tmA0, full_bar(stage), kb * kBK, arow, pol_w);
-          if (MODE == kGateUp) ptx::tma_load_2d(wa + wstep, &tmA1, full_bar(stage), kb * kBK, arow, pol_w);
+          const uint32_t sa = sbase + C::RING_OFF + stage * C::STAGE_BYTES;
+          ptx::tma_load_2d(sa, &tmA0, full_bar(stage), kb * kBK, arow, pol_w);
+          if (MODE == kGateUp) ptx::tma_load_2d(sa + C::W_BYTES, &tmA1, full_bar(stage), kb * kBK, arow, pol_w);
           const uint32_t sb = sa + C::B_OFF;
           for (int i = 0; i < nbox; ++i)
             ptx::tma_load_2d(sb + i * p.boxn * kBK * 2, &tmB, full_bar(stage), kb * kBK,
@@ -317,8 +327,8 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
         // nothing ever arrives on full_bar(0): the wait must expire
         ok = ptx::mbar_wait_bounded(full_bar(0), 0u, deadline, abort_flag);
       } else {
-        int stage = 0;
-        uint32_t phase = 0;
+        int stage = 0, ostage = 0;
+        uint32_t phase = 0, ophase = 0;
         int it = 0;
         for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++it) {
           const Unit x = decode_unit(u, offs, prefix, G, MT, S, BN);
@@ -336,14 +346,15 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
           const uint32_t d1 = d0 + (uint32_t)C::UP_OFF;
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!ptx::mbar_wait_bounded(full_bar(stage), phase, deadline, abort_flag) ||
-                (FP8 && !ptx::mbar_wait_bounded(conv_bar(stage), phase, deadline, abort_flag))) {
+                (FP8 && !ptx::mbar_wait_bounded(ofull_bar(ostage), ophase, deadline, abort_flag))) {
               ok = false;
               break;
             }
             ptx::tc_fence_after();
-            const uint32_t sa = sbase + stage * C::STAGE_BYTES;
-            const uint64_t da0 = ptx::sdesc_k_sw128(sa);
-            const uint64_t da1 = ptx::sdesc_k_sw128(sa + C::A_BYTES);
+            const uint32_t sa = sbase + C::RING_OFF + stage * C::STAGE_BYTES;
+            const uint32_t aa = FP8 ? sbase + ostage * C::OPND_BYTES : sa;
+            const uint64_t da0 = ptx::sdesc_k_sw128(aa);
+            const uint64_t da1 = ptx::sdesc_k_sw128(aa + C::A_BYTES);
             const uint64_t db = ptx::sdesc_k_sw128(sa + C::B_OFF);
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk) {
@@ -356,6 +367,13 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1u;
+            }
+            if (FP8) {
+              ptx::mma_commit(oempty_bar(ostage));
+              if (++ostage == C::OSTAGES) {
+                ostage = 0;
+                ophase ^= 1u;
+              }
             }
           }
           if (ok) ptx::mma_commit(accf_bar(buf));
@@ -438,30 +456,36 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
     if (!ok && lane == 0) set_device_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
   } else if (FP8 && !p.selftest) {
     // ------------------------------------------------------------ converters
-    // Same unit / k-block / stage walk as the MMA issuer.  For each stage:
-    // wait for the E4M3 tile, write it as f16 into the swizzled MMA tile
-    // (16-byte chunk j of row r at chunk position j ^ (r % 8)), make the
-    // writes visible to the tensor core, then arrive on conv_bar.
+    // Same unit / k-block walk as the MMA issuer.  For each k-block: wait for
+    // the E4M3 tiles in the TMA slot and for a free operand slot, write the
+    // f16 tiles into the swizzled operand slot (16-byte chunk j of row r at
+    // chunk position j ^ (r % 8)), make the writes visible to the tensor
+    // core, then arrive on opnd_full.  The MMA's commit frees both slots.
     const int ct = threadIdx.x - kThreads;  // 0..127
-    int stage = 0;
-    uint32_t phase = 0;
+    int stage = 0, ostage = 0;
+    uint32_t phase = 0, ophase = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
       const Unit x = decode_unit(u, offs, prefix, G, MT, S, BN);
       const int kb0 = x.ks * kb_per_split, kb1 = min(kblocks, kb0 + kb_per_split);
       for (int kb = kb0; kb < kb1; ++kb) {
         int got = 0;
-        if (lane == 0) got = ptx::mbar_wait_bounded(full_bar(stage), phase, deadline, abort_flag) ? 1 : 0;
+        if (lane == 0)
+          got = ptx::mbar_wait_bounded(full_bar(stage), phase, deadline, abort_flag) &&
+                        ptx::mbar_wait_bounded(oempty_bar(ostage), ophase ^ 1u, deadline, abort_flag)
+                    ? 1
+                    : 0;
         got = __shfl_sync(0xffffffffu, got, 0);
         if (!got) {
           ok = false;
           break;
         }
-        uint8_t* st = smem + stage * C::STAGE_BYTES;
+        const uint8_t* st = smem + C::RING_OFF + stage * C::STAGE_BYTES;
+        uint8_t* op = smem + ostage * C::OPND_BYTES;
 #pragma unroll
         for (int a = 0; a < C::NA; ++a) {
-          const uint8_t* src = st + C::STG_OFF + a * C::STG_BYTES;
-          uint8_t* dst = st + a * C::A_BYTES;
+          const uint8_t* src = st + a * C::STG_BYTES;
+          uint8_t* dst = op + a * C::A_BYTES;
 #pragma unroll
           for (int i = ct; i < kBM * kBK / 16; i += kConvThreads) {  // 16 E4M3 per chunk
             const int r = i >> 2, c = i & 3;
@@ -473,10 +497,14 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
         }
         ptx::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(conv_bar(stage));
+        if (lane == 0) ptx::mbar_arrive(ofull_bar(ostage));
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
+        }
+        if (++ostage == C::OSTAGES) {
+          ostage = 0;
+          ophase ^= 1u;
         }
       }
     }

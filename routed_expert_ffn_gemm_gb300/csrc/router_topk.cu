@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(kThreads) router_kernel(
       for (int a = 0; a < EPW; ++a)
 #pragma unroll
         for (int t = 0; t < TT; ++t) acc[a][t] = 0.f;
-#pragma unroll 4
+#pragma unroll 8
       for (int i = lane * VN; i < d; i += 32 * VN) {
         float xv[TT][8];
 #pragma unroll
@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(kThreads) topk_partials_kernel(
 bool use_split(int T, int E, bool logits_in, bool scratch) {
   return !logits_in && scratch && T <= 512;
 }
-int split_tt(int T) { return T <= 32 ? 1 : kTT; }
+int split_tt(int T) { return T <= 128 ? 1 : kTT; }
 bool split_needs_topk_pass(int E) { return (E + 7) / 8 > 1; }
 
 template <typename ActT>
