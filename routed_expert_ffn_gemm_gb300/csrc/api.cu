@@ -72,7 +72,9 @@ Layout layout(const moe_problem& p, Path path, int num_sms, bool allow_splits) {
   L.perm_token = take(R * 4);
   L.inv_row = take(R * 4);
   L.chunk = take(permute_scratch_bytes(p.T, p.k, p.E));
-  L.x_perm = take(R * d * ab);
+  // CUDA-core path: the permuted rows; tensor path: unused for bf16, the
+  // f16 copy of x for FP8 (the gate/up GEMM gathers token rows itself)
+  L.x_perm = take(path == Path::kTensor ? (p.w_dtype == MOE_FP8_E4M3 ? T * d * 2 : 0) : R * d * ab);
   L.h = take(R * f * ab);
   const size_t S = path == Path::kTensor ? (size_t)L.plan.splits_down : 1;
   L.y = take(S > 1 ? S * R * d * 4 : R * d * ab);
@@ -107,7 +109,9 @@ long long wait_limit_ns() {
 moe_status run_grouped(Path path, int R, int d, int ffn, int G, int w_dtype, const void* x_rows,
                        const int32_t* offsets, const void* wg, const void* wu, const void* wd,
                        const float* sg, const float* su, const float* sd, void* h, void* y,
-                       const TcPlan& plan, int* status, cudaStream_t s, cudaEvent_t mid) {
+                       const TcPlan& plan, int* status, cudaStream_t s, cudaEvent_t mid,
+                       const int32_t* gather_rows = nullptr, const void* x_src = nullptr,
+                       int T_src = 0) {
   if (path == Path::kSimt) {
     SimtGroupedArgs a{R, d, ffn, G, static_cast<const float*>(x_rows), offsets,
                       static_cast<const float*>(wg), static_cast<const float*>(wu),
@@ -116,7 +120,7 @@ moe_status run_grouped(Path path, int R, int d, int ffn, int G, int w_dtype, con
     return simt_grouped_launch(a, s, mid);
   }
   TcGroupedArgs a{R, d, ffn, G, w_dtype, x_rows, offsets, wg, wu, wd, sg, su, sd, h, y, status,
-                  wait_limit_ns()};
+                  wait_limit_ns(), gather_rows, x_src, T_src};
   return tc_grouped_launch(a, plan, s, mid);
 }
 
@@ -295,16 +299,24 @@ moe_status layer_forward_impl(const moe_problem* p, const void* x, const void* w
   MOE_TRY(router_topk_launch(ra, s));
   MOE_TRY(mark(1));
   // 2. permutation: counts, offsets, row maps, x -> x_perm
-  // FP8 experts run on f16 operands: the row move rounds x to f16
-  PermuteArgs pa{p->T, p->k, p->E, p->d, (int)act_bytes(p->act_dtype), idx, x, counts, offsets,
-                 perm_token, inv_row, x_perm, at<int32_t>(workspace, L.chunk), ctx.status,
-                 fp8 ? 1 : 0};
+  // On the tensor path the permutation writes only the maps: the gate/up
+  // GEMM gathers token rows by perm_token itself (FP8 experts gather from
+  // an f16 copy of x).
+  const bool tensor = path == Path::kTensor;
+  PermuteArgs pa{p->T, p->k, p->E, p->d, (int)act_bytes(p->act_dtype), idx, tensor ? nullptr : x,
+                 counts, offsets, perm_token, inv_row, tensor ? nullptr : x_perm,
+                 at<int32_t>(workspace, L.chunk), ctx.status, 0};
   MOE_TRY(permute_launch(pa, s));
   MOE_TRY(mark(2));
   // 3. grouped SwiGLU experts (gate/up + SiLU*mul, then down)
+  const void* x_src = x;
+  if (tensor && fp8) {
+    MOE_TRY(bf16_to_f16_launch(x, x_perm, (size_t)p->T * p->d, s));
+    x_src = x_perm;
+  }
   MOE_TRY(run_grouped(path, R, p->d, p->ffn, p->E, p->w_dtype, x_perm, offsets, w_gate, w_up,
                       w_down, s_gate, s_up, s_down, h, y, L.plan, ctx.status, s,
-                      timer ? timer->ev[3] : nullptr));
+                      timer ? timer->ev[3] : nullptr, tensor ? perm_token : nullptr, x_src, p->T));
   MOE_TRY(mark(4));
   // 4. shared expert: every token, weight 1 (one group holding all T rows)
   void* sh_y = nullptr;
@@ -417,7 +429,8 @@ moe_status moe_layer_launch_count(const moe_problem* p, int32_t* launches) {
   MOE_TRY(device_ctx(&ctx));
   const int rs = router_tc_splits(p->T, p->d, p->E, p->act_dtype, ctx.num_sms, (size_t)-1);
   int n = rs > 0 ? 2 : router_launch_count(p->T, p->E, false, true);
-  n += permute_launch_count(p->T, p->k, true);
+  n += permute_launch_count(p->T, p->k, path == Path::kSimt);
+  if (path == Path::kTensor && p->w_dtype == MOE_FP8_E4M3) n += 1;  // x -> f16
   n += 2;                        // gate/up, down
   if (p->ffn_shared > 0) n += 3;  // offsets, gate/up, down
   n += 1;                        // combine

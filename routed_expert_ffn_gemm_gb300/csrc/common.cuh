@@ -208,6 +208,11 @@ struct TcGroupedArgs {
   void* y;             // [R, d] bf16 when splits_down == 1, else fp32 [S, R, d]
   int* status;
   long long timeout_ns;
+  // nullable: gather the gate/up row operand from x_src [T_src, d] (rows
+  // gather_rows[r], e.g. perm_token) instead of reading x_perm
+  const int32_t* gather_rows;
+  const void* x_src;
+  int T_src;
 };
 TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype);
 moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStream_t s,

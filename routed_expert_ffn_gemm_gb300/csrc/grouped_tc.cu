@@ -24,7 +24,7 @@
 //                   warp 1 also allocates / frees 512 TMEM columns
 //   warps 2..5      epilogue: tcgen05.ld from TMEM, SiLU(g)*u (gate/up) or
 //                   the projection (down), 64/128-byte coalesced stores
-//   warps 6..9      (FP8 weights only) converters: E4M3 tile staged by TMA ->
+//   warps 6..13     (FP8 weights only) converters: E4M3 tile staged by TMA ->
 //                   f16 tile in the 128-byte-swizzled layout the MMA reads
 // Accumulators live in TMEM (512 columns): a buffer holds the gate and up
 // accumulators (gate at +0, up at +max(BN,128)) or the down accumulator;
@@ -56,7 +56,7 @@ constexpr int kBK = 64;           // reduction elements per stage (128 bytes of 
 constexpr int kBoxSmall = 16;     // rows per B box for decode tiles (BN = 32)
 constexpr int kBoxLarge = 64;     // rows per B box for BN >= 128
 constexpr int kThreads = 192;          // producer, MMA, 4 epilogue warps
-constexpr int kConvThreads = 128;      // FP8: 4 converter warps
+constexpr int kConvThreads = 256;      // FP8: 8 converter warps (two per scheduler)
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxGroups = 1024;
 constexpr int kSmemLimit = 232448;  // opt-in maximum dynamic shared memory per block
@@ -79,6 +79,10 @@ struct TcParams {
   const float* scale1;
   int dense;               // 1: one group holding rows [0, R) (offsets unused)
   int boxn;                // rows per B box of tmB (16 or 64)
+  // gate/up only, nullable: B row j of a group's tile is row
+  // gather_rows[row0 + j] of tmB (the token rows, gathered by TMA gather4;
+  // tmB's box is then one row high) instead of row row0 + j
+  const int32_t* gather_rows;
 };
 
 template <int MODE, int BN, bool FP8>
@@ -91,8 +95,15 @@ struct Cfg {
   // ring of TMA slots [E4M3 A0 A1 | B] (cheap bytes: it hides HBM latency)
   // and a short ring of OSTAGES f16 operand slots [A0 A1] that the
   // converters fill and the MMA reads.
-  static constexpr int OSTAGES = FP8 ? 2 : 0;
+  // operand slots: enough that converters run ahead of the MMA's commits
+  // (a commit round trip per slot otherwise serialises decode), while the
+  // TMA ring keeps at least 4 slots
   static constexpr int OPND_BYTES = NA * A_BYTES;
+  static constexpr int W_BYTES_ = FP8 ? STG_BYTES : A_BYTES;
+  static constexpr int SLOT_ = NA * W_BYTES_ + B_BYTES;
+  static constexpr int AVAIL_ = kSmemLimit - 1024 - (8 * 40 + 16 + 4 * 2 * (kMaxGroups + 8));
+  static constexpr int OSTAGES = !FP8 ? 0 : (AVAIL_ - 4 * SLOT_) / OPND_BYTES >= 4 ? 4
+                                          : (AVAIL_ - 4 * SLOT_) / OPND_BYTES >= 3 ? 3 : 2;
   static constexpr int RING_OFF = OSTAGES * OPND_BYTES;
   static constexpr int W_BYTES = FP8 ? STG_BYTES : A_BYTES;    // weight tile bytes in a TMA slot
   static constexpr int B_OFF = NA * W_BYTES;
@@ -102,13 +113,13 @@ struct Cfg {
   static constexpr int UP_OFF = BN > 128 ? BN : 128;
   static constexpr int ACC_COLS = NA * UP_OFF;
   static constexpr int NBUF = 2 * ACC_COLS <= 512 ? 2 : 1;
-  static constexpr int TAIL_BYTES = 8 * 36 + 16 + 4 * 2 * (kMaxGroups + 8);
+  static constexpr int TAIL_BYTES = 8 * 40 + 16 + 4 * 2 * (kMaxGroups + 8);
   static constexpr int STAGES_FIT = (kSmemLimit - 1024 - TAIL_BYTES - RING_OFF) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 10 ? 10 : STAGES_FIT;
   static constexpr int BAR_OFF = RING_OFF + STAGES * STAGE_BYTES;
-  // barriers: full[S], empty[S], opnd_full[2], opnd_empty[2], acc_full[2],
+  // barriers: full[S], empty[S], opnd_full[4], opnd_empty[4], acc_full[2],
   // acc_empty[2], drain
-  static constexpr int NBARS = 2 * STAGES + 9;
+  static constexpr int NBARS = 2 * STAGES + 13;
   static constexpr int SLOT_OFF = BAR_OFF + 8 * NBARS;         // TMEM base address
   static constexpr int ABORT_OFF = SLOT_OFF + 8;
   static constexpr int OFFS_OFF = ABORT_OFF + 8;               // int offs[G+1]
@@ -179,10 +190,10 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
   auto ofull_bar = [&](int c) { return bars + 8u * (2 * STAGES + c); };
-  auto oempty_bar = [&](int c) { return bars + 8u * (2 * STAGES + 2 + c); };
-  auto accf_bar = [&](int b) { return bars + 8u * (2 * STAGES + 4 + b); };
-  auto acce_bar = [&](int b) { return bars + 8u * (2 * STAGES + 6 + b); };
-  const uint32_t drain_bar = bars + 8u * (2 * STAGES + 8);
+  auto oempty_bar = [&](int c) { return bars + 8u * (2 * STAGES + 4 + c); };
+  auto accf_bar = [&](int b) { return bars + 8u * (2 * STAGES + 8 + b); };
+  auto acce_bar = [&](int b) { return bars + 8u * (2 * STAGES + 10 + b); };
+  const uint32_t drain_bar = bars + 8u * (2 * STAGES + 12);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::SLOT_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::ABORT_OFF);
   int* offs = reinterpret_cast<int*>(smem + C::OFFS_OFF);
@@ -196,7 +207,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
       ptx::mbar_init(full_bar(s), 1);
       ptx::mbar_init(empty_bar(s), 1);
     }
-    for (int c = 0; c < 2; ++c) {
+    for (int c = 0; c < 4; ++c) {
       ptx::mbar_init(ofull_bar(c), kConvThreads / 32);  // one arrival per converter warp
       ptx::mbar_init(oempty_bar(c), 1);                 // the MMA's commit
     }
@@ -271,9 +282,13 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && !p.selftest) {
+    // The whole warp walks the units; lane 0 waits for free slots and
+    // issues the weight copies and row boxes, and in gather mode every lane
+    // issues up to two gather4 row copies per slot.
+    if (!p.selftest) {
       const uint64_t pol_w = ptx::policy_evict_first();
       const uint64_t pol_x = ptx::policy_evict_last();
+      const bool gather = p.gather_rows != nullptr;
       int stage = 0;
       uint32_t phase = 0;
       int armed[STAGES];
@@ -284,30 +299,58 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
         const Unit x = decode_unit(u, offs, prefix, G, MT, S, BN);
         const int kb0 = x.ks * kb_per_split, kb1 = min(kblocks, kb0 + kb_per_split);
         const int nbox = (x.n_valid + p.boxn - 1) / p.boxn;
-        const uint32_t bytes = C::NA * C::W_BYTES + nbox * p.boxn * kBK * 2;
+        const int nops = (x.n_valid + 3) / 4;  // gather4 copies of this tile
+        // this lane's gather rows: ops lane and lane + 32 (BN <= 256); rows
+        // past the group's end repeat its first row (their columns are unused)
+        int gr[2][4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int i = 4 * (lane + 32 * h) + q;
+            gr[h][q] = (gather && lane + 32 * h < nops) ? p.gather_rows[x.row0 + (i < x.n_valid ? i : 0)] : 0;
+          }
+        const uint32_t bbytes = gather ? (uint32_t)nops * 4 * kBK * 2 : (uint32_t)nbox * p.boxn * kBK * 2;
+        const uint32_t bytes = C::NA * C::W_BYTES + bbytes;
         const int arow = x.g * p.M + x.mt * kBM;
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!ptx::mbar_wait_bounded(empty_bar(stage), phase ^ 1u, deadline, abort_flag)) {
+          int got = 1;
+          if (lane == 0) got = ptx::mbar_wait_bounded(empty_bar(stage), phase ^ 1u, deadline, abort_flag) ? 1 : 0;
+          got = __shfl_sync(0xffffffffu, got, 0);
+          if (!got) {
             ok = false;
             break;
           }
-          ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
-          armed[stage] = (int)phase;
           // weights: bf16 straight into the MMA tile, or E4M3 into staging
           const uint32_t sa = sbase + C::RING_OFF + stage * C::STAGE_BYTES;
-          ptx::tma_load_2d(sa, &tmA0, full_bar(stage), kb * kBK, arow, pol_w);
-          if (MODE == kGateUp) ptx::tma_load_2d(sa + C::W_BYTES, &tmA1, full_bar(stage), kb * kBK, arow, pol_w);
           const uint32_t sb = sa + C::B_OFF;
-          for (int i = 0; i < nbox; ++i)
-            ptx::tma_load_2d(sb + i * p.boxn * kBK * 2, &tmB, full_bar(stage), kb * kBK,
-                             x.row0 + i * p.boxn, pol_x);
+          if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
+            armed[stage] = (int)phase;
+            ptx::tma_load_2d(sa, &tmA0, full_bar(stage), kb * kBK, arow, pol_w);
+            if (MODE == kGateUp) ptx::tma_load_2d(sa + C::W_BYTES, &tmA1, full_bar(stage), kb * kBK, arow, pol_w);
+            if (!gather)
+              for (int i = 0; i < nbox; ++i)
+                ptx::tma_load_2d(sb + i * p.boxn * kBK * 2, &tmB, full_bar(stage), kb * kBK,
+                                 x.row0 + i * p.boxn, pol_x);
+          }
+          __syncwarp();
+          if (gather) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int op = lane + 32 * h;
+              if (op < nops)
+                ptx::tma_gather4_2d(sb + op * 4 * kBK * 2, &tmB, full_bar(stage), kb * kBK, gr[h][0],
+                                    gr[h][1], gr[h][2], gr[h][3], pol_x);
+            }
+          }
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      if (!ok) {
+      if (!ok && lane == 0) {
         set_device_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
         // let every issued copy land before shared memory is released
         const uint64_t grace = ptx::globaltimer_ns() + 100000000ull;
@@ -461,7 +504,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
     // f16 tiles into the swizzled operand slot (16-byte chunk j of row r at
     // chunk position j ^ (r % 8)), make the writes visible to the tensor
     // core, then arrive on opnd_full.  The MMA's commit frees both slots.
-    const int ct = threadIdx.x - kThreads;  // 0..127
+    const int ct = threadIdx.x - kThreads;  // 0 .. kConvThreads-1
     int stage = 0, ostage = 0;
     uint32_t phase = 0, ophase = 0;
     bool ok = true;
@@ -608,7 +651,10 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   MOE_TRY(make_tmap_2d(&wg, a.w_gate, (uint64_t)a.G * a.ffn, a.d, wb, kBM, kBK, wsw));
   MOE_TRY(make_tmap_2d(&wu, a.w_up, (uint64_t)a.G * a.ffn, a.d, wb, kBM, kBK, wsw));
   const int box_gu = boxn_of(plan.bn_gateup), box_dn = boxn_of(plan.bn_down);
-  MOE_TRY(make_tmap_2d(&xb, a.x_perm, a.R, a.d, 2, box_gu, kBK, true));
+  if (a.gather_rows != nullptr)  // token rows by index: one-row boxes for gather4
+    MOE_TRY(make_tmap_2d(&xb, a.x_src, a.T_src, a.d, 2, 1, kBK, true));
+  else
+    MOE_TRY(make_tmap_2d(&xb, a.x_perm, a.R, a.d, 2, box_gu, kBK, true));
   MOE_TRY(make_tmap_2d(&wd, a.w_down, (uint64_t)a.G * a.d, a.ffn, wb, kBM, kBK, wsw));
   MOE_TRY(make_tmap_2d(&hb, a.h, a.R, a.ffn, 2, box_dn, kBK, true));
 
@@ -628,7 +674,9 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   p.scale0 = a.s_gate;
   p.scale1 = a.s_up;
   p.boxn = box_gu;
+  p.gather_rows = a.gather_rows;
   MOE_TRY(launch_mode<kGateUp>(plan.bn_gateup, fp8, p, wg, wu, xb, plan.grid, s));
+  p.gather_rows = nullptr;
   if (mid != nullptr) MOE_TRY_CUDA(record_event(mid, s));
 
   p.M = a.d;

@@ -103,6 +103,20 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Gather of four rows (any row indices) of one 64-element column block: the
+// tensor map's box is one row high; the rows land consecutively (4 x box)
+// at `dst` with the map's swizzle, completing `bar`'s transaction count.
+__device__ __forceinline__ void tma_gather4_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                               int32_t c_inner, int32_t r0, int32_t r1, int32_t r2,
+                                               int32_t r3, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c_inner), "r"(r0), "r"(r1), "r"(r2),
+      "r"(r3), "l"(policy)
+      : "memory");
+}
+
 // Generic-proxy shared-memory writes -> visible to the async proxy.
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
