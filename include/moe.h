@@ -274,7 +274,8 @@ MOE_API moe_status moe_layer_launch_count(const moe_problem *p, int32_t *launche
  * current device (no page counterpart; for benchmarks and tests):
  * info[0] rows per tile of the gate/up GEMM, info[1] rows per tile of the
  * down GEMM, info[2] reduction splits of the down GEMM, info[3] persistent
- * CTAs per GEMM launch.  All zero for the fp32 CUDA-core path.
+ * CTAs per GEMM launch, info[4] reduction splits of the gate/up GEMM.
+ * All zero for the fp32 CUDA-core path.
  */
 MOE_API moe_status moe_plan_info(const moe_problem *p, int32_t *info);
 

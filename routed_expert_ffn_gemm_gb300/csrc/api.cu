@@ -39,9 +39,10 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
   size_t idx, w, logits, counts, offsets, perm_token, inv_row, chunk, x_perm, h, y;
-  size_t sh_offsets, sh_h, sh_y, total;
+  size_t sh_offsets, sh_h, sh_y, gu_part, sh_gu_part, total;
   TcPlan plan, sh_plan;
   int router_splits;  // 0: CUDA-core router; else tensor-core logits with this many K splits
+  bool gather;        // gate/up gathers token rows (decode tiling) instead of x_perm
 };
 
 // Workspace of moe_layer_forward (a superset of what the other entry points
@@ -57,7 +58,7 @@ Layout layout(const moe_problem& p, Path path, int num_sms, bool allow_splits) {
   };
   if (path == Path::kTensor) {
     L.plan = tc_plan(p.T, p.k, p.E, p.d, p.ffn, num_sms, p.w_dtype);
-    if (!allow_splits) L.plan.splits_down = 1;
+    if (!allow_splits) L.plan.splits_down = L.plan.splits_gateup = 1;
     if (p.ffn_shared) {
       L.sh_plan = tc_plan(p.T, 1, 1, p.d, p.ffn_shared, num_sms, MOE_BF16);
       L.sh_plan.splits_down = 1;
@@ -72,15 +73,22 @@ Layout layout(const moe_problem& p, Path path, int num_sms, bool allow_splits) {
   L.perm_token = take(R * 4);
   L.inv_row = take(R * 4);
   L.chunk = take(permute_scratch_bytes(p.T, p.k, p.E));
-  // CUDA-core path: the permuted rows; tensor path: unused for bf16, the
-  // f16 copy of x for FP8 (the gate/up GEMM gathers token rows itself)
-  L.x_perm = take(path == Path::kTensor ? (p.w_dtype == MOE_FP8_E4M3 ? T * d * 2 : 0) : R * d * ab);
+  // The permuted rows, except in the decode tiling of the tensor path
+  // (32-row tiles): there the gate/up GEMM gathers token rows itself and this
+  // region holds only the f16 copy of x for FP8 experts.
+  const bool gather = path == Path::kTensor && L.plan.bn_gateup == 32;
+  L.gather = gather;
+  L.x_perm = take(gather ? (p.w_dtype == MOE_FP8_E4M3 ? T * d * 2 : 0) : R * d * ab);
   L.h = take(R * f * ab);
   const size_t S = path == Path::kTensor ? (size_t)L.plan.splits_down : 1;
   L.y = take(S > 1 ? S * R * d * 4 : R * d * ab);
   L.sh_offsets = take(8);
   L.sh_h = take(T * (size_t)p.ffn_shared * ab);
   L.sh_y = take(p.ffn_shared ? T * d * ab : 0);
+  const size_t sgu = path == Path::kTensor && L.plan.splits_gateup > 1 ? L.plan.splits_gateup : 0;
+  L.gu_part = take(sgu * R * 2 * f * 4);
+  const size_t ssh = path == Path::kTensor && p.ffn_shared && L.sh_plan.splits_gateup > 1 ? L.sh_plan.splits_gateup : 0;
+  L.sh_gu_part = take(ssh * T * 2 * (size_t)p.ffn_shared * 4);
   L.total = off;
   return L;
 }
@@ -111,7 +119,7 @@ moe_status run_grouped(Path path, int R, int d, int ffn, int G, int w_dtype, con
                        const float* sg, const float* su, const float* sd, void* h, void* y,
                        const TcPlan& plan, int* status, cudaStream_t s, cudaEvent_t mid,
                        const int32_t* gather_rows = nullptr, const void* x_src = nullptr,
-                       int T_src = 0) {
+                       int T_src = 0, float* gu_partials = nullptr) {
   if (path == Path::kSimt) {
     SimtGroupedArgs a{R, d, ffn, G, static_cast<const float*>(x_rows), offsets,
                       static_cast<const float*>(wg), static_cast<const float*>(wu),
@@ -120,7 +128,7 @@ moe_status run_grouped(Path path, int R, int d, int ffn, int G, int w_dtype, con
     return simt_grouped_launch(a, s, mid);
   }
   TcGroupedArgs a{R, d, ffn, G, w_dtype, x_rows, offsets, wg, wu, wd, sg, su, sd, h, y, status,
-                  wait_limit_ns(), gather_rows, x_src, T_src};
+                  wait_limit_ns(), gather_rows, x_src, T_src, gu_partials};
   return tc_grouped_launch(a, plan, s, mid);
 }
 
@@ -299,24 +307,26 @@ moe_status layer_forward_impl(const moe_problem* p, const void* x, const void* w
   MOE_TRY(router_topk_launch(ra, s));
   MOE_TRY(mark(1));
   // 2. permutation: counts, offsets, row maps, x -> x_perm
-  // On the tensor path the permutation writes only the maps: the gate/up
-  // GEMM gathers token rows by perm_token itself (FP8 experts gather from
-  // an f16 copy of x).
-  const bool tensor = path == Path::kTensor;
-  PermuteArgs pa{p->T, p->k, p->E, p->d, (int)act_bytes(p->act_dtype), idx, tensor ? nullptr : x,
-                 counts, offsets, perm_token, inv_row, tensor ? nullptr : x_perm,
-                 at<int32_t>(workspace, L.chunk), ctx.status, 0};
+  // In the decode tiling the permutation writes only the maps: the gate/up
+  // GEMM gathers token rows by perm_token itself (FP8 experts gather from an
+  // f16 copy of x).  Otherwise the row move fills x_perm (rounded to f16 for
+  // FP8 experts, which run on f16 operands).
+  const bool gather = L.gather;
+  PermuteArgs pa{p->T, p->k, p->E, p->d, (int)act_bytes(p->act_dtype), idx, gather ? nullptr : x,
+                 counts, offsets, perm_token, inv_row, gather ? nullptr : x_perm,
+                 at<int32_t>(workspace, L.chunk), ctx.status, fp8 && !gather ? 1 : 0};
   MOE_TRY(permute_launch(pa, s));
   MOE_TRY(mark(2));
   // 3. grouped SwiGLU experts (gate/up + SiLU*mul, then down)
   const void* x_src = x;
-  if (tensor && fp8) {
+  if (gather && fp8) {
     MOE_TRY(bf16_to_f16_launch(x, x_perm, (size_t)p->T * p->d, s));
     x_src = x_perm;
   }
   MOE_TRY(run_grouped(path, R, p->d, p->ffn, p->E, p->w_dtype, x_perm, offsets, w_gate, w_up,
                       w_down, s_gate, s_up, s_down, h, y, L.plan, ctx.status, s,
-                      timer ? timer->ev[3] : nullptr, tensor ? perm_token : nullptr, x_src, p->T));
+                      timer ? timer->ev[3] : nullptr, gather ? perm_token : nullptr, x_src, p->T,
+                      at<float>(workspace, L.gu_part)));
   MOE_TRY(mark(4));
   // 4. shared expert: every token, weight 1 (one group holding all T rows)
   void* sh_y = nullptr;
@@ -327,7 +337,8 @@ moe_status layer_forward_impl(const moe_problem* p, const void* x, const void* w
     sh_y = at<uint8_t>(workspace, L.sh_y);
     MOE_TRY(run_grouped(path, p->T, p->d, p->ffn_shared, 1, p->act_dtype, x, sh_off,
                         w_shared_gate, w_shared_up, w_shared_down, nullptr, nullptr, nullptr,
-                        at<uint8_t>(workspace, L.sh_h), sh_y, L.sh_plan, ctx.status, s, nullptr));
+                        at<uint8_t>(workspace, L.sh_h), sh_y, L.sh_plan, ctx.status, s, nullptr,
+                        nullptr, nullptr, 0, at<float>(workspace, L.sh_gu_part)));
   }
   MOE_TRY(mark(5));
   // 5. combine: inverse map, routing weights, sum (+ shared expert)
@@ -405,7 +416,7 @@ moe_status moe_plan_info(const moe_problem* p, int32_t* info) {
   if (info == nullptr) return MOE_ERR_INVALID_ARG;
   Path path;
   MOE_TRY(check_problem(p, &path));
-  info[0] = info[1] = info[2] = info[3] = 0;
+  info[0] = info[1] = info[2] = info[3] = info[4] = 0;
   if (path != Path::kTensor) return MOE_OK;
   DeviceCtx ctx;
   MOE_TRY(device_ctx(&ctx));
@@ -414,6 +425,7 @@ moe_status moe_plan_info(const moe_problem* p, int32_t* info) {
   info[1] = L.plan.bn_down;
   info[2] = L.plan.splits_down;
   info[3] = L.plan.grid;
+  info[4] = L.plan.splits_gateup;
   return MOE_OK;
 }
 
@@ -429,9 +441,13 @@ moe_status moe_layer_launch_count(const moe_problem* p, int32_t* launches) {
   MOE_TRY(device_ctx(&ctx));
   const int rs = router_tc_splits(p->T, p->d, p->E, p->act_dtype, ctx.num_sms, (size_t)-1);
   int n = rs > 0 ? 2 : router_launch_count(p->T, p->E, false, true);
-  n += permute_launch_count(p->T, p->k, path == Path::kSimt);
-  if (path == Path::kTensor && p->w_dtype == MOE_FP8_E4M3) n += 1;  // x -> f16
+  const Layout L0 = layout(*p, path, ctx.num_sms, true);
+  n += permute_launch_count(p->T, p->k, !L0.gather);
+  if (L0.gather && p->w_dtype == MOE_FP8_E4M3) n += 1;  // x -> f16
+  const Layout L = layout(*p, path, ctx.num_sms, true);
   n += 2;                        // gate/up, down
+  if (path == Path::kTensor && L.plan.splits_gateup > 1) n += 1;       // split-K finalize
+  if (path == Path::kTensor && p->ffn_shared > 0 && L.sh_plan.splits_gateup > 1) n += 1;
   if (p->ffn_shared > 0) n += 3;  // offsets, gate/up, down
   n += 1;                        // combine
   *launches = n;

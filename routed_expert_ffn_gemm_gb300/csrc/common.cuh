@@ -191,6 +191,8 @@ struct TcPlan {
   int bn_gateup;       // max rows per tile in the gate/up GEMM
   int bn_down;         // max rows per tile in the down GEMM
   int splits_down;     // K splits of the down GEMM (1 = direct bf16 output)
+  int splits_gateup;   // K splits of the gate/up GEMM (1 = SiLU*mul in its epilogue;
+                       // else fp32 partials, then an in-order sum + SiLU*mul pass)
   int grid;            // persistent CTAs
 };
 struct TcGroupedArgs {
@@ -213,6 +215,7 @@ struct TcGroupedArgs {
   const int32_t* gather_rows;
   const void* x_src;
   int T_src;
+  float* gu_partials;  // [splits_gateup, R, 2*ffn] fp32 when splits_gateup > 1
 };
 TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype);
 moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStream_t s,

@@ -24,7 +24,7 @@
 //                   warp 1 also allocates / frees 512 TMEM columns
 //   warps 2..5      epilogue: tcgen05.ld from TMEM, SiLU(g)*u (gate/up) or
 //                   the projection (down), 64/128-byte coalesced stores
-//   warps 6..13     (FP8 weights only) converters: E4M3 tile staged by TMA ->
+//   warps 6..9      (FP8 weights only) converters (warp w: every 4th stage): E4M3 tile staged by TMA ->
 //                   f16 tile in the 128-byte-swizzled layout the MMA reads
 // Accumulators live in TMEM (512 columns): a buffer holds the gate and up
 // accumulators (gate at +0, up at +max(BN,128)) or the down accumulator;
@@ -43,6 +43,8 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <type_traits>
+
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -56,7 +58,7 @@ constexpr int kBK = 64;           // reduction elements per stage (128 bytes of 
 constexpr int kBoxSmall = 16;     // rows per B box for decode tiles (BN = 32)
 constexpr int kBoxLarge = 64;     // rows per B box for BN >= 128
 constexpr int kThreads = 192;          // producer, MMA, 4 epilogue warps
-constexpr int kConvThreads = 256;      // FP8: 8 converter warps (two per scheduler)
+constexpr int kConvThreads = 128;      // FP8: 4 converter warps, each converting whole stages
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxGroups = 1024;
 constexpr int kSmemLimit = 232448;  // opt-in maximum dynamic shared memory per block
@@ -102,8 +104,8 @@ struct Cfg {
   static constexpr int W_BYTES_ = FP8 ? STG_BYTES : A_BYTES;
   static constexpr int SLOT_ = NA * W_BYTES_ + B_BYTES;
   static constexpr int AVAIL_ = kSmemLimit - 1024 - (8 * 40 + 16 + 4 * 2 * (kMaxGroups + 8));
-  static constexpr int OSTAGES = !FP8 ? 0 : (AVAIL_ - 4 * SLOT_) / OPND_BYTES >= 4 ? 4
-                                          : (AVAIL_ - 4 * SLOT_) / OPND_BYTES >= 3 ? 3 : 2;
+  static constexpr int OSTAGES = !FP8 ? 0 : (AVAIL_ - 6 * SLOT_) / OPND_BYTES >= 4 ? 4
+                                          : (AVAIL_ - 6 * SLOT_) / OPND_BYTES >= 3 ? 3 : 2;
   static constexpr int RING_OFF = OSTAGES * OPND_BYTES;
   static constexpr int W_BYTES = FP8 ? STG_BYTES : A_BYTES;    // weight tile bytes in a TMA slot
   static constexpr int B_OFF = NA * W_BYTES;
@@ -208,7 +210,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
       ptx::mbar_init(empty_bar(s), 1);
     }
     for (int c = 0; c < 4; ++c) {
-      ptx::mbar_init(ofull_bar(c), kConvThreads / 32);  // one arrival per converter warp
+      ptx::mbar_init(ofull_bar(c), 1);                  // the converting warp
       ptx::mbar_init(oempty_bar(c), 1);                 // the MMA's commit
     }
     for (int b = 0; b < 2; ++b) {
@@ -465,6 +467,18 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
           uint32_t rb[16];
           ptx::tmem_ld16(taddr + (uint32_t)C::UP_OFF + c0, rb);
           ptx::tmem_ld_wait();
+          if (p.out_f32) {
+            // K-split: scaled fp32 partials, SiLU*mul after the in-order sum
+            float* part = static_cast<float*>(p.out) + (size_t)x.ks * p.R * 2 * p.M;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (c0 + j < x.n_valid) {
+                float* row = part + (size_t)(x.row0 + c0 + j) * 2 * p.M;
+                row[ch] = __uint_as_float(ra[j]) * sc0;
+                row[p.M + ch] = __uint_as_float(rb[j]) * sc1;
+              }
+            continue;
+          }
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             if (c0 + j < x.n_valid) {
@@ -499,19 +513,25 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
     if (!ok && lane == 0) set_device_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
   } else if (FP8 && !p.selftest) {
     // ------------------------------------------------------------ converters
-    // Same unit / k-block walk as the MMA issuer.  For each k-block: wait for
-    // the E4M3 tiles in the TMA slot and for a free operand slot, write the
-    // f16 tiles into the swizzled operand slot (16-byte chunk j of row r at
-    // chunk position j ^ (r % 8)), make the writes visible to the tensor
-    // core, then arrive on opnd_full.  The MMA's commit frees both slots.
-    const int ct = threadIdx.x - kThreads;  // 0 .. kConvThreads-1
-    int stage = 0, ostage = 0;
-    uint32_t phase = 0, ophase = 0;
+    // The k-blocks of this CTA's units form one sequence (the MMA walks the
+    // same one); converter warp cw converts positions cw, cw + 4, ... whole,
+    // so four stages convert at once and one stage's latency chain (copy
+    // landed -> convert -> proxy fence -> arrive) is hidden behind the
+    // others.  Position n uses TMA slot n % STAGES and operand slot
+    // n % OSTAGES; the phases follow from n.  Each E4M3 tile becomes an f16
+    // tile in the 128-byte-swizzled layout (16-byte chunk j of row r at chunk
+    // position j ^ (r % 8)); the MMA's commit frees both slots.
+    constexpr int NW = kConvThreads / 32;
+    const int cw = warp - kThreads / 32;
     bool ok = true;
+    int n = 0;  // sequence position
     for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
       const Unit x = decode_unit(u, offs, prefix, G, MT, S, BN);
       const int kb0 = x.ks * kb_per_split, kb1 = min(kblocks, kb0 + kb_per_split);
-      for (int kb = kb0; kb < kb1; ++kb) {
+      for (int kb = kb0; kb < kb1; ++kb, ++n) {
+        if (n % NW != cw) continue;
+        const int stage = n % STAGES, ostage = n % C::OSTAGES;
+        const uint32_t phase = (uint32_t)(n / STAGES) & 1u, ophase = (uint32_t)(n / C::OSTAGES) & 1u;
         int got = 0;
         if (lane == 0)
           got = ptx::mbar_wait_bounded(full_bar(stage), phase, deadline, abort_flag) &&
@@ -529,8 +549,8 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
         for (int a = 0; a < C::NA; ++a) {
           const uint8_t* src = st + a * C::STG_BYTES;
           uint8_t* dst = op + a * C::A_BYTES;
-#pragma unroll
-          for (int i = ct; i < kBM * kBK / 16; i += kConvThreads) {  // 16 E4M3 per chunk
+#pragma unroll 4
+          for (int i = lane; i < kBM * kBK / 16; i += 32) {  // 16 E4M3 per chunk
             const int r = i >> 2, c = i & 3;
             const uint4 v = *reinterpret_cast<const uint4*>(src + r * kBK + c * 16);
             const int sw = r & 7;
@@ -541,14 +561,6 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ofull_bar(ostage));
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
-        if (++ostage == C::OSTAGES) {
-          ostage = 0;
-          ophase ^= 1u;
-        }
       }
     }
     if (!ok && lane == 0) set_device_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
@@ -594,6 +606,49 @@ int env_int(const char* name) {
 }
 
 int bn_ok(int bn) { return bn == 32 || bn == 128 || bn == 256 ? bn : 0; }
+
+// K splits (<= 8, each >= 4 k-blocks) so that `units` work units fill whole
+// waves of the SMs when there are fewer than two waves of them.
+int choose_splits(int units, int kblocks, int num_sms) {
+  int best_s = 1;
+  if (units >= 2 * num_sms) return 1;
+  double best = 0.0;
+  for (int s = 1; s <= 8; ++s) {
+    if (kblocks / s < 4) break;
+    const double u = (double)units * s;
+    const double waves = __builtin_ceil(u / num_sms);
+    const double eff = u / (waves * num_sms);
+    if (eff > best + 0.02) {
+      best = eff;
+      best_s = s;
+    }
+  }
+  return best_s;
+}
+
+// h[r, c] = SiLU(sum_s g[s][r][c]) * sum_s u[s][r][c] from the gate/up
+// GEMM's fp32 partials [S][R][2M] (g at column c, u at M + c), s in order.
+template <typename OutT>
+__global__ void __launch_bounds__(256) swiglu_finalize_kernel(int R, int M, int S,
+                                                              const float* __restrict__ part,
+                                                              OutT* __restrict__ h) {
+  griddep_begin();
+  const size_t n = (size_t)R * M;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t r = i / M, c = i % M;
+    float g = 0.f, u = 0.f;
+    for (int s = 0; s < S; ++s) {
+      const float* row = part + ((size_t)s * R + r) * 2 * M;
+      g += row[c];
+      u += row[M + c];
+    }
+    const float v = g / (1.f + __expf(-g)) * u;
+    if constexpr (sizeof(OutT) == 2 && std::is_same<OutT, __half>::value)
+      h[i] = __float2half_rn(v);
+    else
+      h[i] = __float2bfloat16_rn(v);
+  }
+}
 int boxn_of(int bn) { return bn >= 128 ? kBoxLarge : kBoxSmall; }
 
 }  // namespace
@@ -614,24 +669,14 @@ TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype) {
   pl.bn_gateup = bn_ok(env_int("MOE_BN_GATEUP")) ? env_int("MOE_BN_GATEUP") : bn;
   pl.bn_down = bn_ok(env_int("MOE_BN_DOWN")) ? env_int("MOE_BN_DOWN") : bn_dn;
   const double touched = E < R ? E : R;
-  const double tiles_a = R / pl.bn_down;
-  const int tiles = (int)(touched > tiles_a ? touched : tiles_a + 0.5);
-  const int units = tiles * (d / kBM);
-  const int kblocks = (ffn + kBK - 1) / kBK;
-  pl.splits_down = 1;
-  if (units < 2 * num_sms) {
-    double best = 0.0;
-    for (int s = 1; s <= 8; ++s) {
-      if (kblocks / s < 4) break;
-      const double u = (double)units * s;
-      const double waves = __builtin_ceil(u / num_sms);
-      const double eff = u / (waves * num_sms);
-      if (eff > best + 0.02) {
-        best = eff;
-        pl.splits_down = s;
-      }
-    }
-  }
+  auto tiles_of = [&](int bn_) {
+    const double a = R / bn_;
+    return (int)(touched > a ? touched : a + 0.5);
+  };
+  pl.splits_down = choose_splits(tiles_of(pl.bn_down) * (d / kBM), (ffn + kBK - 1) / kBK, num_sms);
+  pl.splits_gateup = choose_splits(tiles_of(pl.bn_gateup) * (ffn / kBM), (d + kBK - 1) / kBK, num_sms);
+  if (env_int("MOE_SPLITS_GATEUP") >= 1 && env_int("MOE_SPLITS_GATEUP") <= 8)
+    pl.splits_gateup = env_int("MOE_SPLITS_GATEUP");
   pl.grid = num_sms;
   return pl;
 }
@@ -668,15 +713,27 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
 
   p.M = a.ffn;
   p.K = a.d;
-  p.splits = 1;
-  p.out = a.h;
-  p.out_f32 = 0;
+  const bool gu_split = plan.splits_gateup > 1 && a.gu_partials != nullptr;
+  p.splits = gu_split ? plan.splits_gateup : 1;
+  p.out = gu_split ? static_cast<void*>(a.gu_partials) : a.h;
+  p.out_f32 = gu_split ? 1 : 0;
   p.scale0 = a.s_gate;
   p.scale1 = a.s_up;
   p.boxn = box_gu;
   p.gather_rows = a.gather_rows;
   MOE_TRY(launch_mode<kGateUp>(plan.bn_gateup, fp8, p, wg, wu, xb, plan.grid, s));
   p.gather_rows = nullptr;
+  if (gu_split) {
+    const size_t n = (size_t)a.R * a.ffn;
+    const int blocks = (int)((n + 255) / 256 < 8192 ? (n + 255) / 256 : 8192);
+    if (fp8)
+      MOE_TRY_CUDA(launch_k(swiglu_finalize_kernel<__half>, dim3(blocks), dim3(256), 0, s, a.R, a.ffn,
+                            plan.splits_gateup, (const float*)a.gu_partials, static_cast<__half*>(a.h)));
+    else
+      MOE_TRY_CUDA(launch_k(swiglu_finalize_kernel<__nv_bfloat16>, dim3(blocks), dim3(256), 0, s, a.R,
+                            a.ffn, plan.splits_gateup, (const float*)a.gu_partials,
+                            static_cast<__nv_bfloat16*>(a.h)));
+  }
   if (mid != nullptr) MOE_TRY_CUDA(record_event(mid, s));
 
   p.M = a.d;

@@ -479,6 +479,18 @@ def test_layer_forward_captured_in_a_cuda_graph_with_stage_timer():
     timer.close()
 
 
+@pytest.mark.parametrize("splits", [1, 3, 8])
+@pytest.mark.parametrize("wfmt", ["bf16", "fp8"])
+def test_layer_gateup_split_k(splits, wfmt, monkeypatch):
+    # the gate/up GEMM split along its reduction: fp32 partials, then an
+    # in-order sum and SiLU*mul pass (chosen automatically at tiny batches)
+    monkeypatch.setenv("MOE_SPLITS_GATEUP", str(splits))
+    shape = inputs.MoEShape("small", T=5, d=512, ffn=256, E=16, k=4, ffn_shared=256 if wfmt == "fp8" else 0,
+                            wfmt=wfmt)
+    assert api.moe_plan_info(api.problem_of(shape))["splits_gateup"] == splits
+    _layer_check(shape, 4, FP8_TOL if wfmt == "fp8" else BF16_TOL)
+
+
 def test_layer_empty_batch():
     shape = inputs.WORKLOADS["qwen3_30b_a3b"].with_T(0)
     case = inputs.make_weights(shape, 0, DEV)
