@@ -24,7 +24,7 @@
 //                   warp 1 also allocates / frees 512 TMEM columns
 //   warps 2..5      epilogue: tcgen05.ld from TMEM, SiLU(g)*u (gate/up) or
 //                   the projection (down), 64/128-byte coalesced stores
-//   warps 6..9      (FP8 weights only) converters (warp w: every 4th stage): E4M3 tile staged by TMA ->
+//   warps 6..9      (FP8 weights only) converters: E4M3 tile staged by TMA ->
 //                   f16 tile in the 128-byte-swizzled layout the MMA reads
 // Accumulators live in TMEM (512 columns): a buffer holds the gate and up
 // accumulators (gate at +0, up at +max(BN,128)) or the down accumulator;
@@ -58,7 +58,7 @@ constexpr int kBK = 64;           // reduction elements per stage (128 bytes of 
 constexpr int kBoxSmall = 16;     // rows per B box for decode tiles (BN = 32)
 constexpr int kBoxLarge = 64;     // rows per B box for BN >= 128
 constexpr int kThreads = 192;          // producer, MMA, 4 epilogue warps
-constexpr int kConvThreads = 128;      // FP8: 4 converter warps, each converting whole stages
+constexpr int kConvThreads = 128;      // FP8: 4 converter warps sharing each stage
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxGroups = 1024;
 constexpr int kSmemLimit = 232448;  // opt-in maximum dynamic shared memory per block
@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
       ptx::mbar_init(empty_bar(s), 1);
     }
     for (int c = 0; c < 4; ++c) {
-      ptx::mbar_init(ofull_bar(c), 1);                  // the converting warp
+      ptx::mbar_init(ofull_bar(c), kConvThreads / 32);  // one arrival per converter warp
       ptx::mbar_init(oempty_bar(c), 1);                 // the MMA's commit
     }
     for (int b = 0; b < 2; ++b) {
@@ -513,25 +513,20 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
     if (!ok && lane == 0) set_device_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
   } else if (FP8 && !p.selftest) {
     // ------------------------------------------------------------ converters
-    // The k-blocks of this CTA's units form one sequence (the MMA walks the
-    // same one); converter warp cw converts positions cw, cw + 4, ... whole,
-    // so four stages convert at once and one stage's latency chain (copy
-    // landed -> convert -> proxy fence -> arrive) is hidden behind the
-    // others.  Position n uses TMA slot n % STAGES and operand slot
-    // n % OSTAGES; the phases follow from n.  Each E4M3 tile becomes an f16
-    // tile in the 128-byte-swizzled layout (16-byte chunk j of row r at chunk
-    // position j ^ (r % 8)); the MMA's commit frees both slots.
-    constexpr int NW = kConvThreads / 32;
-    const int cw = warp - kThreads / 32;
+    // Same unit / k-block walk as the MMA issuer; the four converter warps
+    // share each stage.  Per k-block: wait for the E4M3 tiles in the TMA
+    // slot and for a free operand slot, write the f16 tiles into the
+    // swizzled operand slot (16-byte chunk j of row r at chunk position
+    // j ^ (r % 8)), make the writes visible to the tensor core, then arrive
+    // on opnd_full.  The MMA's commit frees both slots.
+    const int ct = threadIdx.x - kThreads;  // 0 .. kConvThreads-1
+    int stage = 0, ostage = 0;
+    uint32_t phase = 0, ophase = 0;
     bool ok = true;
-    int n = 0;  // sequence position
     for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
       const Unit x = decode_unit(u, offs, prefix, G, MT, S, BN);
       const int kb0 = x.ks * kb_per_split, kb1 = min(kblocks, kb0 + kb_per_split);
-      for (int kb = kb0; kb < kb1; ++kb, ++n) {
-        if (n % NW != cw) continue;
-        const int stage = n % STAGES, ostage = n % C::OSTAGES;
-        const uint32_t phase = (uint32_t)(n / STAGES) & 1u, ophase = (uint32_t)(n / C::OSTAGES) & 1u;
+      for (int kb = kb0; kb < kb1; ++kb) {
         int got = 0;
         if (lane == 0)
           got = ptx::mbar_wait_bounded(full_bar(stage), phase, deadline, abort_flag) &&
@@ -549,8 +544,8 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
         for (int a = 0; a < C::NA; ++a) {
           const uint8_t* src = st + a * C::STG_BYTES;
           uint8_t* dst = op + a * C::A_BYTES;
-#pragma unroll 4
-          for (int i = lane; i < kBM * kBK / 16; i += 32) {  // 16 E4M3 per chunk
+#pragma unroll
+          for (int i = ct; i < kBM * kBK / 16; i += kConvThreads) {  // 16 E4M3 per chunk
             const int r = i >> 2, c = i & 3;
             const uint4 v = *reinterpret_cast<const uint4*>(src + r * kBK + c * 16);
             const int sw = r & 7;
@@ -561,6 +556,14 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ofull_bar(ostage));
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        if (++ostage == C::OSTAGES) {
+          ostage = 0;
+          ophase ^= 1u;
+        }
       }
     }
     if (!ok && lane == 0) set_device_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
