@@ -296,6 +296,28 @@ def run_reference(args, shape, ws, rank):
     return 0
 
 
+def measured_traffic(shape, role):
+    """DRAM bytes per launch of the dominant kernel from a committed ncu
+    capture (profiles/dram_traffic.txt), or None when there is none for this
+    workload or the kernel source changed since it was taken."""
+    import hashlib
+    src = os.path.join(ROOT, "routed_expert_ffn_gemm_gb300", "csrc", "grouped_tc.cu")
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    try:
+        with open(src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        with open(path) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) == 5 and not line.startswith("#"):
+                    w, t, r, h, b = parts
+                    if w == shape.name and int(t) == shape.T and r == role and h == sha:
+                        return float(b)
+    except OSError:
+        pass
+    return None
+
+
 def workload_config(shape, extra=None):
     c = {"workload": f"{shape.name}_moe_layer", "T": shape.T, "d": shape.d, "ffn": shape.ffn,
          "E": shape.E, "k": shape.k, "ffn_shared": shape.ffn_shared, "act": shape.act,
@@ -443,7 +465,7 @@ def run_ours(args, shape, ws, rank, local):
     else:
         roof = {"bound": "hbm", "achieved": b_ / t_s / 1e9, "peak": hbm_gbs, "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"] = measured_traffic(shape, dominant)
     roof["kernel"] = f"tc_grouped_kernel ({dominant})"
     roof["peak_source"] = peak_src
     roof["algorithmic_bytes_per_launch"] = b_
