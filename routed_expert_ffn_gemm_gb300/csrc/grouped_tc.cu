@@ -460,50 +460,71 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
       const int n_mma = ((x.n_valid + 15) / 16) * 16;
       const float sc0 = FP8 ? p.scale0[(size_t)x.g * p.M + ch] : 1.f;
       const float sc1 = FP8 && MODE == kGateUp ? p.scale1[(size_t)x.g * p.M + ch] : 1.f;
-      for (int c0 = 0; c0 < n_mma; c0 += 16) {
-        uint32_t ra[16];
-        ptx::tmem_ld16(taddr + c0, ra);
-        if (MODE == kGateUp) {
-          uint32_t rb[16];
-          ptx::tmem_ld16(taddr + (uint32_t)C::UP_OFF + c0, rb);
-          ptx::tmem_ld_wait();
-          if (p.out_f32) {
-            // K-split: scaled fp32 partials, SiLU*mul after the in-order sum
-            float* part = static_cast<float*>(p.out) + (size_t)x.ks * p.R * 2 * p.M;
+      // CW accumulator columns per TMEM wait: 32 for the projection (its
+      // epilogue is the longer one per MMA cycle), 16 for gate/up (measured
+      // faster there).  BN is a multiple of 32, so columns past n_mma stay
+      // inside this accumulator; they are not stored.
+      constexpr int CW = MODE == kGateUp ? 16 : 32;
+#pragma unroll 1
+      for (int c0 = 0; c0 < n_mma; c0 += CW) {
+        uint32_t ra[CW], rb[CW];
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (c0 + j < x.n_valid) {
-                float* row = part + (size_t)(x.row0 + c0 + j) * 2 * p.M;
-                row[ch] = __uint_as_float(ra[j]) * sc0;
-                row[p.M + ch] = __uint_as_float(rb[j]) * sc1;
+        for (int hlf = 0; hlf < CW / 16; ++hlf) {
+          ptx::tmem_ld16(taddr + c0 + 16 * hlf, *reinterpret_cast<uint32_t(*)[16]>(&ra[16 * hlf]));
+          if (MODE == kGateUp)
+            ptx::tmem_ld16(taddr + (uint32_t)C::UP_OFF + c0 + 16 * hlf,
+                           *reinterpret_cast<uint32_t(*)[16]>(&rb[16 * hlf]));
+        }
+        ptx::tmem_ld_wait();
+        // halves of 16 columns; the empty asm keeps the compiler from
+        // interleaving them (which costs registers, not time)
+#pragma unroll
+        for (int hlf = 0; hlf < CW / 16; ++hlf) {
+          const int cb = c0 + 16 * hlf;
+          const int nj = min(16, x.n_valid - cb);
+          const uint32_t* a = ra + 16 * hlf;
+          const uint32_t* b = rb + 16 * hlf;
+          if (nj > 0) {
+            if (MODE == kGateUp) {
+              if (p.out_f32) {
+                // K-split: scaled fp32 partials, SiLU*mul after the in-order sum
+                float* row = static_cast<float*>(p.out) + ((size_t)x.ks * p.R + x.row0 + cb) * 2 * p.M + ch;
+#pragma unroll
+                for (int j = 0; j < 16; ++j, row += 2 * p.M)
+                  if (j < nj) {
+                    row[0] = __uint_as_float(a[j]) * sc0;
+                    row[p.M] = __uint_as_float(b[j]) * sc1;
+                  }
+              } else if (FP8) {
+                __half* o = static_cast<__half*>(p.out) + (size_t)(x.row0 + cb) * p.M + ch;  // h feeds an f16 MMA
+#pragma unroll
+                for (int j = 0; j < 16; ++j, o += p.M)
+                  if (j < nj) {
+                    const float g = __uint_as_float(a[j]) * sc0;
+                    *o = __float2half_rn(g / (1.f + __expf(-g)) * (__uint_as_float(b[j]) * sc1));
+                  }
+              } else {
+                __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + (size_t)(x.row0 + cb) * p.M + ch;
+#pragma unroll
+                for (int j = 0; j < 16; ++j, o += p.M)
+                  if (j < nj) {
+                    const float g = __uint_as_float(a[j]);
+                    store_out(o, g / (1.f + __expf(-g)) * __uint_as_float(b[j]));
+                  }
               }
-            continue;
-          }
+            } else if (p.out_f32) {
+              float* o = static_cast<float*>(p.out) + ((size_t)x.ks * p.R + x.row0 + cb) * p.M + ch;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            if (c0 + j < x.n_valid) {
-              const float g = __uint_as_float(ra[j]) * sc0;
-              const float v = g / (1.f + __expf(-g)) * (__uint_as_float(rb[j]) * sc1);
-              const size_t o = (size_t)(x.row0 + c0 + j) * p.M + ch;
-              if (FP8)
-                static_cast<__half*>(p.out)[o] = __float2half_rn(v);  // h feeds an f16 MMA
-              else
-                store_out(static_cast<__nv_bfloat16*>(p.out) + o, v);
+              for (int j = 0; j < 16; ++j, o += p.M)
+                if (j < nj) *o = __uint_as_float(a[j]) * sc0;
+            } else {
+              __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + (size_t)(x.row0 + cb) * p.M + ch;
+#pragma unroll
+              for (int j = 0; j < 16; ++j, o += p.M)
+                if (j < nj) store_out(o, __uint_as_float(a[j]) * sc0);
             }
           }
-        } else {
-          ptx::tmem_ld_wait();
-          if (p.out_f32) {
-            float* y = static_cast<float*>(p.out) + (size_t)x.ks * p.R * p.M;
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (c0 + j < x.n_valid) y[(size_t)(x.row0 + c0 + j) * p.M + ch] = __uint_as_float(ra[j]) * sc0;
-          } else {
-            __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.out);
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (c0 + j < x.n_valid) store_out(y + (size_t)(x.row0 + c0 + j) * p.M + ch, __uint_as_float(ra[j]) * sc0);
-          }
+          asm volatile("" ::: "memory");
         }
       }
       ptx::tc_fence_before();
