@@ -58,7 +58,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define MOE_API __attribute__((visibility("default")))
@@ -274,8 +274,10 @@ MOE_API moe_status moe_layer_launch_count(const moe_problem *p, int32_t *launche
  * current device (no page counterpart; for benchmarks and tests):
  * info[0] rows per tile of the gate/up GEMM, info[1] rows per tile of the
  * down GEMM, info[2] reduction splits of the down GEMM, info[3] persistent
- * CTAs per GEMM launch, info[4] reduction splits of the gate/up GEMM.
- * All zero for the fp32 CUDA-core path.
+ * CTAs per GEMM launch, info[4] reduction splits of the gate/up GEMM,
+ * info[5] bit 0 / bit 1: the gate/up / down GEMM runs on CTA pairs
+ * (256 output channels per tile).  `info` holds 6 entries.  All zero for
+ * the fp32 CUDA-core path.
  */
 MOE_API moe_status moe_plan_info(const moe_problem *p, int32_t *info);
 

@@ -203,10 +203,10 @@ def moe_layer_launch_count(p) -> int:
 
 
 def moe_plan_info(p) -> dict:
-    info = (ctypes.c_int32 * 5)()
+    info = (ctypes.c_int32 * 6)()
     _call("moe_plan_info", ctypes.byref(p), info)
     return {"bn_gateup": info[0], "bn_down": info[1], "splits_down": info[2], "grid": info[3],
-            "splits_gateup": info[4]}
+            "splits_gateup": info[4], "pair_gateup": info[5] & 1, "pair_down": (info[5] >> 1) & 1}
 
 
 def moe_workspace_size(p) -> int:

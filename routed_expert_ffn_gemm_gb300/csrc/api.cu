@@ -416,7 +416,7 @@ moe_status moe_plan_info(const moe_problem* p, int32_t* info) {
   if (info == nullptr) return MOE_ERR_INVALID_ARG;
   Path path;
   MOE_TRY(check_problem(p, &path));
-  info[0] = info[1] = info[2] = info[3] = info[4] = 0;
+  info[0] = info[1] = info[2] = info[3] = info[4] = info[5] = 0;
   if (path != Path::kTensor) return MOE_OK;
   DeviceCtx ctx;
   MOE_TRY(device_ctx(&ctx));
@@ -426,6 +426,7 @@ moe_status moe_plan_info(const moe_problem* p, int32_t* info) {
   info[2] = L.plan.splits_down;
   info[3] = L.plan.grid;
   info[4] = L.plan.splits_gateup;
+  info[5] = (L.plan.pair_gateup ? 1 : 0) | (L.plan.pair_down ? 2 : 0);
   return MOE_OK;
 }
 

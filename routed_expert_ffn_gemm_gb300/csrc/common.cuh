@@ -67,19 +67,36 @@ moe_status make_tmap_2d(CUtensorMap* map, const void* base, uint64_t rows, uint6
 bool pdl_enabled();
 
 template <typename... KArgs, typename... Args>
-inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                            cudaStream_t s, Args&&... args) {
+inline cudaError_t launch_kc(int cluster, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t s, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pdl_enabled()) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster > 1) {  // thread-block clusters of `cluster` CTAs along x
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = (unsigned)cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t s, Args&&... args) {
+  return launch_kc(1, kern, grid, block, smem, s, std::forward<Args>(args)...);
 }
 
 // Record `ev` on `s`; inside stream capture as an external (timestamp) node,
@@ -194,6 +211,8 @@ struct TcPlan {
   int splits_gateup;   // K splits of the gate/up GEMM (1 = SiLU*mul in its epilogue;
                        // else fp32 partials, then an in-order sum + SiLU*mul pass)
   int grid;            // persistent CTAs
+  int pair_gateup;     // 1: the gate/up GEMM runs on CTA pairs (cta_group::2, M = 256)
+  int pair_down;       // 1: the down GEMM runs on CTA pairs
 };
 struct TcGroupedArgs {
   int R, d, ffn, G;    // rows, hidden, intermediate, groups (experts)

@@ -14,24 +14,31 @@
 // ceil(n/16)*16 MMA columns: the decode regime (1-2 rows per expert) and the
 // prefill regime (hundreds of rows) run the same kernel.
 //
-// Work unit = (expert g, tile of BN rows, 128-channel tile mt, K split ks).
+// Work unit = (expert g, tile of BN rows, channel tile mt, K split ks).
 // A persistent grid (one CTA per SM) strides over the units; the per-expert
 // tile counts are derived on the device from the offsets (no host sync).
-// CTA roles (192 threads):
-//   warp 0 lane 0   TMA producer: weight tile(s) [128 x 64] + ceil(n/16)
-//                   row boxes [16 x 64] per stage, 128-byte swizzle
+// CTA roles (320 threads):
+//   warp 0 lane 0   TMA producer: weight tile(s) [128 x 64] + the row boxes
+//                   per stage, 128-byte swizzle
 //   warp 1 lane 0   MMA issuer: tcgen05.mma kind::f16, fp32 accumulate;
 //                   warp 1 also allocates / frees 512 TMEM columns
-//   warps 2..5      epilogue: tcgen05.ld from TMEM, SiLU(g)*u (gate/up) or
-//                   the projection (down), 64/128-byte coalesced stores
-//   warps 6..9      (FP8 weights only) converters: E4M3 tile staged by TMA ->
+//   warps 2..9      epilogue: tcgen05.ld from TMEM (two warps per lane
+//                   quadrant, alternate column chunks), SiLU(g)*u (gate/up)
+//                   or the projection (down), 64-byte coalesced stores
+//   warps 10..13    (FP8 weights only) converters: E4M3 tile staged by TMA ->
 //                   f16 tile in the 128-byte-swizzled layout the MMA reads
+// CTA pairs (prefill tiles): a cluster of two CTAs runs each unit with
+// cta_group::2 MMAs, M = 256 channels (128 per CTA, each CTA's TMEM holding
+// its own accumulator rows); each CTA stages its 128 weight rows and half
+// of the unit's B rows, so per SM the B bytes per flop halve.  The even
+// CTA issues the MMAs; the copies of both CTAs complete its barriers and
+// its commits arrive on both CTAs' barriers.
 // Accumulators live in TMEM (512 columns): a buffer holds the gate and up
 // accumulators (gate at +0, up at +max(BN,128)) or the down accumulator;
 // two buffers when they fit (BN <= 128 for gate/up, <= 256 for down), so the
-// epilogue of one unit overlaps the next unit's loads and MMAs; gate/up with
-// BN = 256 (prefill: half the operand bytes per flop) uses one buffer.  Every wait is bounded: on expiry the kernel records
-// MOE_ERR_DEVICE_TIMEOUT, lets issued copies land, frees TMEM and returns.
+// epilogue of one unit overlaps the next unit's loads and MMAs.  Every wait
+// is bounded: on expiry the kernel records MOE_ERR_DEVICE_TIMEOUT, lets
+// issued copies land, frees TMEM and returns.
 //
 // FP8 weights ("MoE 推理部署", section 专家量化: per-expert scales) are
 // dequantised in-kernel: every E4M3 value is exact in f16 and one hardware
@@ -56,8 +63,9 @@ namespace {
 constexpr int kBM = 128;          // output channels per tile (MMA M)
 constexpr int kBK = 64;           // reduction elements per stage (128 bytes of bf16)
 constexpr int kBoxSmall = 16;     // rows per B box for decode tiles (BN = 32)
-constexpr int kBoxLarge = 64;     // rows per B box for BN >= 128
-constexpr int kThreads = 192;          // producer, MMA, 4 epilogue warps
+constexpr int kBoxLarge = 128;    // rows per B box of the dense (router) GEMM
+constexpr int kEpiWarps = 8;           // two per TMEM lane quadrant, alternating column chunks
+constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer, MMA, epilogue warps
 constexpr int kConvThreads = 128;      // FP8: 4 converter warps sharing each stage
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxGroups = 1024;
@@ -87,11 +95,16 @@ struct TcParams {
   const int32_t* gather_rows;
 };
 
-template <int MODE, int BN, bool FP8>
+template <int MODE, int BN, bool FP8, bool PAIR>
 struct Cfg {
+  // PAIR: a CTA pair (cluster of 2) runs one unit with cta_group::2 MMAs:
+  // M = 256 output channels (128 per CTA, each CTA's TMEM holding its own
+  // 128 accumulator rows for all N columns) and each CTA staging half of
+  // the unit's B rows, so a CTA moves half the B bytes per flop
+  static constexpr int CH = PAIR ? 2 * kBM : kBM;               // output channels per unit
   static constexpr int NA = MODE == kGateUp ? 2 : 1;           // weight operands per stage
   static constexpr int A_BYTES = kBM * kBK * 2;                // 16 KB bf16 tile (MMA operand)
-  static constexpr int B_BYTES = BN * kBK * 2;
+  static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * kBK * 2;
   static constexpr int STG_BYTES = FP8 ? kBM * kBK : 0;        // 8 KB E4M3 staging tile
   // bf16: one ring of TMA slots [A0 A1 | B] read by the MMA.  FP8: a deep
   // ring of TMA slots [E4M3 A0 A1 | B] (cheap bytes: it hides HBM latency)
@@ -131,6 +144,7 @@ struct Cfg {
   static_assert(SMEM_BYTES <= kSmemLimit, "shared memory budget");
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
   static_assert(BN % 16 == 0 && BN <= 256 && ACC_COLS <= 512, "tile rows");
+  static_assert(!PAIR || BN >= 64, "pair tiles split B rows in halves");
 };
 
 struct Unit {
@@ -159,6 +173,16 @@ __device__ __forceinline__ Unit decode_unit(int u, const int* offs, const int* p
 
 __device__ __forceinline__ void store_out(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
+// SiLU(g) * u with SiLU(g) = g * sigmoid(g) and sigmoid(g) = (1 + tanh(g/2)) / 2:
+// one hardware tanh (relative error ~2^-11, below the bf16 / f16 rounding
+// of h) instead of an exponential and a division.
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  const float a = 0.5f * g;
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(a));
+  return fmaf(a, t, a) * u;
+}
+
 // Eight E4M3 values (two 32-bit words, lowest byte first) -> eight f16,
 // exactly (every E4M3 value is representable in f16).
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v16) {
@@ -176,13 +200,15 @@ __device__ __forceinline__ uint4 e4m3x8_to_f16x8(uint32_t lo, uint32_t hi) {
   return r;
 }
 
-template <int MODE, int BN, bool FP8>
-__global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
+template <int MODE, int BN, bool FP8, bool PAIR>
+__global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
     tc_grouped_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA0,
                       const __grid_constant__ CUtensorMap tmA1,
                       const __grid_constant__ CUtensorMap tmB) {
-  using C = Cfg<MODE, BN, FP8>;
+  using C = Cfg<MODE, BN, FP8, PAIR>;
   constexpr int STAGES = C::STAGES;
+  // pair barriers with remote arrivers live in the even CTA (rank 0)
+  constexpr uint32_t kRemote = PAIR ? 2u : 1u;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = ptx::smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw_s & 1023u)) & 1023u;
@@ -202,20 +228,30 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
   int* prefix = reinterpret_cast<int*>(smem + C::PREFIX_OFF);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;
+  const bool leader = rank == 0u;
+  // the even CTA's copy of a barrier (shared::cluster address)
+  auto lead = [&](uint32_t bar) { return PAIR ? ptx::mapa_shared(bar, 0u) : bar; };
+  // units: the pair walks one sequence together
+  const int u_first = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int u_step = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
   griddep_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      ptx::mbar_init(full_bar(s), 1);
+      // bf16 pairs: both producers arrive on the even CTA's full barrier
+      // (their copies complete it); FP8: each CTA's converters wait on
+      // their own CTA's copies
+      ptx::mbar_init(full_bar(s), PAIR && !FP8 ? 2 : 1);
       ptx::mbar_init(empty_bar(s), 1);
     }
     for (int c = 0; c < 4; ++c) {
-      ptx::mbar_init(ofull_bar(c), kConvThreads / 32);  // one arrival per converter warp
-      ptx::mbar_init(oempty_bar(c), 1);                 // the MMA's commit
+      ptx::mbar_init(ofull_bar(c), kRemote * kConvThreads / 32);  // one arrival per converter warp
+      ptx::mbar_init(oempty_bar(c), 1);                           // the MMA's commit
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(accf_bar(b), 1);
-      ptx::mbar_init(acce_bar(b), 4);  // one arrival per epilogue warp
+      ptx::mbar_init(acce_bar(b), kRemote * kEpiWarps);  // one arrival per epilogue warp
     }
     ptx::mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -227,8 +263,8 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
     ptx::prefetch_tmap(&tmB);
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
-    ptx::tmem_relinquish();
+    ptx::tmem_alloc<PAIR>(ptx::smem_u32(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish<PAIR>();
   }
 
   // The prologue above touches no global memory; from here on the previous
@@ -272,11 +308,15 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
     if (threadIdx.x == C::THREADS - 1) prefix[G] = before + incl;
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  // pairs: the peer's barriers must be initialised before any remote arrive
+  if constexpr (PAIR)
+    ptx::cluster_sync();
+  else
+    __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int MT = p.M / kBM;
+  const int MT = p.M / C::CH;
   const int S = p.splits;
   const int total_units = p.selftest ? 1 : prefix[G] * MT * S;
   const int kblocks = (p.K + kBK - 1) / kBK;
@@ -297,10 +337,14 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
 #pragma unroll
       for (int s = 0; s < STAGES; ++s) armed[s] = -1;
       bool ok = true;
-      for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+      for (int u = u_first; u < total_units && ok; u += u_step) {
         const Unit x = decode_unit(u, offs, prefix, G, MT, S, BN);
         const int kb0 = x.ks * kb_per_split, kb1 = min(kblocks, kb0 + kb_per_split);
-        const int nbox = (x.n_valid + p.boxn - 1) / p.boxn;
+        // B rows this CTA stages: all of the tile, or (pair) its half of
+        // the tile's MMA width rounded to 32
+        const int bhalf = PAIR ? ((x.n_valid + 31) / 32) * 16 : x.n_valid;
+        const int brow0 = x.row0 + (int)rank * bhalf;
+        const int nbox = (bhalf + p.boxn - 1) / p.boxn;
         const int nops = (x.n_valid + 3) / 4;  // gather4 copies of this tile
         // this lane's gather rows: ops lane and lane + 32 (BN <= 256); rows
         // past the group's end repeat its first row (their columns are unused)
@@ -314,10 +358,11 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
           }
         const uint32_t bbytes = gather ? (uint32_t)nops * 4 * kBK * 2 : (uint32_t)nbox * p.boxn * kBK * 2;
         const uint32_t bytes = C::NA * C::W_BYTES + bbytes;
-        const int arow = x.g * p.M + x.mt * kBM;
+        const int arow = x.g * p.M + x.mt * C::CH + (int)rank * kBM;
         for (int kb = kb0; kb < kb1; ++kb) {
           int got = 1;
-          if (lane == 0) got = ptx::mbar_wait_bounded(empty_bar(stage), phase ^ 1u, deadline, abort_flag) ? 1 : 0;
+          if (lane == 0)
+            got = ptx::mbar_wait_bounded(empty_bar(stage), phase ^ 1u, deadline, abort_flag) ? 1 : 0;
           got = __shfl_sync(0xffffffffu, got, 0);
           if (!got) {
             ok = false;
@@ -327,14 +372,25 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
           const uint32_t sa = sbase + C::RING_OFF + stage * C::STAGE_BYTES;
           const uint32_t sb = sa + C::B_OFF;
           if (lane == 0) {
-            ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
             armed[stage] = (int)phase;
-            ptx::tma_load_2d(sa, &tmA0, full_bar(stage), kb * kBK, arow, pol_w);
-            if (MODE == kGateUp) ptx::tma_load_2d(sa + C::W_BYTES, &tmA1, full_bar(stage), kb * kBK, arow, pol_w);
-            if (!gather)
+            if (PAIR && !FP8) {
+              // both CTAs' copies complete the even CTA's barrier
+              const uint32_t fb = lead(full_bar(stage));
+              ptx::mbar_arrive_expect_tx_cluster(fb, bytes);
+              ptx::tma_load_2d_pair(sa, &tmA0, fb, kb * kBK, arow, pol_w);
+              if (MODE == kGateUp) ptx::tma_load_2d_pair(sa + C::W_BYTES, &tmA1, fb, kb * kBK, arow, pol_w);
               for (int i = 0; i < nbox; ++i)
-                ptx::tma_load_2d(sb + i * p.boxn * kBK * 2, &tmB, full_bar(stage), kb * kBK,
-                                 x.row0 + i * p.boxn, pol_x);
+                ptx::tma_load_2d_pair(sb + i * p.boxn * kBK * 2, &tmB, fb, kb * kBK, brow0 + i * p.boxn, pol_x);
+            } else {
+              ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
+              ptx::tma_load_2d(sa, &tmA0, full_bar(stage), kb * kBK, arow, pol_w);
+              if (MODE == kGateUp)
+                ptx::tma_load_2d(sa + C::W_BYTES, &tmA1, full_bar(stage), kb * kBK, arow, pol_w);
+              if (!gather)
+                for (int i = 0; i < nbox; ++i)
+                  ptx::tma_load_2d(sb + i * p.boxn * kBK * 2, &tmB, full_bar(stage), kb * kBK,
+                                   brow0 + i * p.boxn, pol_x);
+            }
           }
           __syncwarp();
           if (gather) {
@@ -356,18 +412,33 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
         set_device_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
         // let every issued copy land before shared memory is released
         const uint64_t grace = ptx::globaltimer_ns() + 100000000ull;
-        for (int s = 0; s < STAGES; ++s) {
-          if (armed[s] < 0) continue;
-          while (!ptx::mbar_try_wait(full_bar(s), (uint32_t)armed[s]) && ptx::globaltimer_ns() < grace) {
+        if (PAIR && !FP8 && !leader) {
+          // this CTA's copies complete the peer's barriers: wait a while
+          const uint64_t t_end = ptx::globaltimer_ns() + 20000000ull;
+          while (ptx::globaltimer_ns() < t_end) {
+          }
+        } else {
+          for (int s = 0; s < STAGES; ++s) {
+            if (armed[s] < 0) continue;
+            while (!ptx::mbar_try_wait(full_bar(s), (uint32_t)armed[s]) && ptx::globaltimer_ns() < grace) {
+            }
           }
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // (pairs: the even CTA issues for both)
+    if (lane == 0 && leader) {
       bool ok = true;
       bool issued = false;
+      // pairs: the commit arrives on the barrier at the same offset in both CTAs
+      auto commit = [&](uint32_t bar) {
+        if (PAIR)
+          ptx::mma_commit_pair(bar);
+        else
+          ptx::mma_commit(bar);
+      };
       if (p.selftest) {
         // nothing ever arrives on full_bar(0): the wait must expire
         ok = ptx::mbar_wait_bounded(full_bar(0), 0u, deadline, abort_flag);
@@ -375,7 +446,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
         int stage = 0, ostage = 0;
         uint32_t phase = 0, ophase = 0;
         int it = 0;
-        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++it) {
+        for (int u = u_first; u < total_units && ok; u += u_step, ++it) {
           const Unit x = decode_unit(u, offs, prefix, G, MT, S, BN);
           const int kb0 = x.ks * kb_per_split, kb1 = min(kblocks, kb0 + kb_per_split);
           const int buf = it % C::NBUF;
@@ -385,8 +456,8 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
             break;
           }
           ptx::tc_fence_after();
-          const int n_mma = ((x.n_valid + 15) / 16) * 16;
-          const uint32_t idesc = FP8 ? ptx::idesc_f16_f32(kBM, n_mma) : ptx::idesc_bf16_f32(kBM, n_mma);
+          const int n_mma = PAIR ? ((x.n_valid + 31) / 32) * 32 : ((x.n_valid + 15) / 16) * 16;
+          const uint32_t idesc = FP8 ? ptx::idesc_f16_f32(C::CH, n_mma) : ptx::idesc_bf16_f32(C::CH, n_mma);
           const uint32_t d0 = tmem_base + (uint32_t)(C::ACC_COLS * buf);
           const uint32_t d1 = d0 + (uint32_t)C::UP_OFF;
           for (int kb = kb0; kb < kb1; ++kb) {
@@ -404,31 +475,36 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk) {
               const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
-              ptx::mma_f16(d0, da0 + 2 * kk, db + 2 * kk, idesc, acc);
-              if (MODE == kGateUp) ptx::mma_f16(d1, da1 + 2 * kk, db + 2 * kk, idesc, acc);
+              if (PAIR) {
+                ptx::mma_f16_pair(d0, da0 + 2 * kk, db + 2 * kk, idesc, acc);
+                if (MODE == kGateUp) ptx::mma_f16_pair(d1, da1 + 2 * kk, db + 2 * kk, idesc, acc);
+              } else {
+                ptx::mma_f16(d0, da0 + 2 * kk, db + 2 * kk, idesc, acc);
+                if (MODE == kGateUp) ptx::mma_f16(d1, da1 + 2 * kk, db + 2 * kk, idesc, acc);
+              }
             }
             issued = true;
-            ptx::mma_commit(empty_bar(stage));
+            commit(empty_bar(stage));
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1u;
             }
             if (FP8) {
-              ptx::mma_commit(oempty_bar(ostage));
+              commit(oempty_bar(ostage));
               if (++ostage == C::OSTAGES) {
                 ostage = 0;
                 ophase ^= 1u;
               }
             }
           }
-          if (ok) ptx::mma_commit(accf_bar(buf));
+          if (ok) commit(accf_bar(buf));
         }
       }
       if (!ok) {
         set_device_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
         if (issued) {
           // wait for the MMAs already issued before TMEM is freed
-          ptx::mma_commit(drain_bar);
+          commit(drain_bar);
           const uint64_t grace = ptx::globaltimer_ns() + 100000000ull;
           while (!ptx::mbar_try_wait(drain_bar, 0u) && ptx::globaltimer_ns() < grace) {
           }
@@ -439,9 +515,10 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     const int ch_local = q * 32 + lane;
+    const int eg = (warp - 2) >> 2;  // which of the quadrant's two warps: alternate column chunks
     int it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++it) {
+    for (int u = u_first; u < total_units; u += u_step, ++it) {
       const int buf = it % C::NBUF;
       const uint32_t acc_phase = (uint32_t)(it / C::NBUF) & 1u;
       // one lane waits, the warp follows its verdict (tcgen05.ld below is
@@ -456,7 +533,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
       ptx::tc_fence_after();
       const Unit x = decode_unit(u, offs, prefix, G, MT, S, BN);
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(C::ACC_COLS * buf);
-      const int ch = x.mt * kBM + ch_local;
+      const int ch = x.mt * C::CH + (int)rank * kBM + ch_local;
       const int n_mma = ((x.n_valid + 15) / 16) * 16;
       const float sc0 = FP8 ? p.scale0[(size_t)x.g * p.M + ch] : 1.f;
       const float sc1 = FP8 && MODE == kGateUp ? p.scale1[(size_t)x.g * p.M + ch] : 1.f;
@@ -466,7 +543,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
       // inside this accumulator; they are not stored.
       constexpr int CW = MODE == kGateUp ? 16 : 32;
 #pragma unroll 1
-      for (int c0 = 0; c0 < n_mma; c0 += CW) {
+      for (int c0 = eg * CW; c0 < n_mma; c0 += 2 * CW) {
         uint32_t ra[CW], rb[CW];
 #pragma unroll
         for (int hlf = 0; hlf < CW / 16; ++hlf) {
@@ -501,7 +578,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
                 for (int j = 0; j < 16; ++j, o += p.M)
                   if (j < nj) {
                     const float g = __uint_as_float(a[j]) * sc0;
-                    *o = __float2half_rn(g / (1.f + __expf(-g)) * (__uint_as_float(b[j]) * sc1));
+                    *o = __float2half_rn(silu_mul(g, __uint_as_float(b[j]) * sc1));
                   }
               } else {
                 __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + (size_t)(x.row0 + cb) * p.M + ch;
@@ -509,7 +586,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
                 for (int j = 0; j < 16; ++j, o += p.M)
                   if (j < nj) {
                     const float g = __uint_as_float(a[j]);
-                    store_out(o, g / (1.f + __expf(-g)) * __uint_as_float(b[j]));
+                    store_out(o, silu_mul(g, __uint_as_float(b[j])));
                   }
               }
             } else if (p.out_f32) {
@@ -529,7 +606,12 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
       }
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(acce_bar(buf));
+      if (lane == 0) {
+        if (PAIR)
+          ptx::mbar_arrive_cluster(lead(acce_bar(buf)));
+        else
+          ptx::mbar_arrive(acce_bar(buf));
+      }
     }
     if (!ok && lane == 0) set_device_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
   } else if (FP8 && !p.selftest) {
@@ -544,7 +626,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
     int stage = 0, ostage = 0;
     uint32_t phase = 0, ophase = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+    for (int u = u_first; u < total_units && ok; u += u_step) {
       const Unit x = decode_unit(u, offs, prefix, G, MT, S, BN);
       const int kb0 = x.ks * kb_per_split, kb1 = min(kblocks, kb0 + kb_per_split);
       for (int kb = kb0; kb < kb1; ++kb) {
@@ -576,7 +658,12 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
         }
         ptx::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(ofull_bar(ostage));
+        if (lane == 0) {
+          if (PAIR)
+            ptx::mbar_arrive_cluster(lead(ofull_bar(ostage)));
+          else
+            ptx::mbar_arrive(ofull_bar(ostage));
+        }
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
@@ -591,27 +678,70 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8>::THREADS, 1)
   }
 
   ptx::tc_fence_before();
-  __syncthreads();
+  // pairs: neither CTA leaves (or frees TMEM) while its peer may still
+  // write its barriers or the MMA read its shared memory
+  if constexpr (PAIR)
+    ptx::cluster_sync();
+  else
+    __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, kTmemCols);
+    ptx::tmem_dealloc<PAIR>(tmem_base, kTmemCols);
   }
 }
 
-template <int MODE, int BN, bool FP8>
+template <int MODE, int BN, bool FP8, bool PAIR = false>
 moe_status launch_one(const TcParams& p, const CUtensorMap& a0, const CUtensorMap& a1,
                       const CUtensorMap& b, int grid, cudaStream_t s) {
-  using C = Cfg<MODE, BN, FP8>;
-  auto kern = tc_grouped_kernel<MODE, BN, FP8>;
+  using C = Cfg<MODE, BN, FP8, PAIR>;
+  auto kern = tc_grouped_kernel<MODE, BN, FP8, PAIR>;
   MOE_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES));
-  MOE_TRY_CUDA(launch_k(kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, s, p, a0, a1, b));
+  if (PAIR) {
+    // The grid is persistent: every pair must be resident at once, and not
+    // every SM finds a partner (clusters stay inside a GPC), so take the
+    // number of co-resident pairs from the occupancy query (per device).
+    static int resident[64];
+    int dev = 0;
+    MOE_TRY_CUDA(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+    if (resident[dev] == 0) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(grid & ~1);
+      cfg.blockDim = dim3(C::THREADS);
+      cfg.dynamicSmemBytes = C::SMEM_BYTES;
+      cudaLaunchAttribute attr;
+      attr.id = cudaLaunchAttributeClusterDimension;
+      attr.val.clusterDim.x = 2;
+      attr.val.clusterDim.y = 1;
+      attr.val.clusterDim.z = 1;
+      cfg.attrs = &attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      MOE_TRY_CUDA(cudaOccupancyMaxActiveClusters(&n, kern, &cfg));
+      resident[dev] = n > 0 ? n : -1;
+    }
+    if (resident[dev] < 0) return MOE_ERR_UNSUPPORTED;
+    grid = min(grid & ~1, 2 * resident[dev]);
+  }
+  MOE_TRY_CUDA(launch_kc(PAIR ? 2 : 1, kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, s, p, a0, a1, b));
   MOE_TRY_CUDA(cudaGetLastError());
   return MOE_OK;
 }
 
 template <int MODE>
-moe_status launch_mode(int bn, bool fp8, const TcParams& p, const CUtensorMap& a0,
+moe_status launch_mode(int bn, bool fp8, bool pair, const TcParams& p, const CUtensorMap& a0,
                        const CUtensorMap& a1, const CUtensorMap& b, int grid, cudaStream_t s) {
+  if (pair) {
+    if (p.M % (2 * kBM) != 0 || grid < 2) return MOE_ERR_UNSUPPORTED;
+    if (fp8) {
+      if (bn == 128) return launch_one<MODE, 128, true, true>(p, a0, a1, b, grid, s);
+      if (bn == 256) return launch_one<MODE, 256, true, true>(p, a0, a1, b, grid, s);
+    } else {
+      if (bn == 128) return launch_one<MODE, 128, false, true>(p, a0, a1, b, grid, s);
+      if (bn == 256) return launch_one<MODE, 256, false, true>(p, a0, a1, b, grid, s);
+    }
+    return MOE_ERR_UNSUPPORTED;
+  }
   if (fp8) {
     if (bn == 32) return launch_one<MODE, 32, true>(p, a0, a1, b, grid, s);
     if (bn == 128) return launch_one<MODE, 128, true>(p, a0, a1, b, grid, s);
@@ -673,24 +803,36 @@ __global__ void __launch_bounds__(256) swiglu_finalize_kernel(int R, int M, int 
       h[i] = __float2bfloat16_rn(v);
   }
 }
-int boxn_of(int bn) { return bn >= 128 ? kBoxLarge : kBoxSmall; }
+// Rows per B box: 16 for decode tiles; else one box for all of a CTA's B
+// rows (BN, or BN/2 on a CTA pair): every TMA copy costs a fixed overhead
+// on top of its bytes, measured to matter at prefill.  MOE_BOXN = 64/128/256
+// overrides (tuning) where it fits.
+int boxn_of(int bn, bool pair) {
+  if (bn < 128) return kBoxSmall;
+  const int cap = pair ? bn / 2 : bn;
+  const int e = env_int("MOE_BOXN");
+  if ((e == 64 || e == 128 || e == 256) && e <= cap) return e;
+  return cap;
+}
 
 }  // namespace
 
 // Rows per tile from the expected rows per expert: 32 for decode (a few rows
-// each), else 128; the bf16 down GEMM takes 256 at prefill (half the operand
-// bytes per flop with its accumulators still double-buffered).  Measured on
-// GB300: gate/up at 256 rows loses its epilogue overlap (one TMEM buffer)
-// and runs slower than at 128; FP8 tiles of 256 leave too few stages.
-// MOE_BN_GATEUP / MOE_BN_DOWN override (tuning).
+// each), else 128; at prefill (>= 128 rows per expert on average) both GEMMs
+// take 256 (the bf16 down GEMM; FP8 down tiles of 256 leave too few stages).
+// Gate/up at 256 rows has one TMEM buffer (its epilogue is not overlapped
+// with the next unit's MMAs), yet on CTA pairs it moves the fewest operand
+// bytes per flop and measured fastest on GB300 (with the eight-warp
+// epilogue).  MOE_BN_GATEUP / MOE_BN_DOWN override (tuning).
 TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype) {
   TcPlan pl;
   const double R = (double)T * k;
   const double mean = R / E;
   const double est_max = mean + 3.0 * __builtin_sqrt(mean) + 1.0;
   const int bn = est_max <= 32.0 ? 32 : 128;
+  const int bn_gu = (bn == 128 && mean >= 128.0) ? 256 : bn;
   const int bn_dn = (bn == 128 && mean >= 128.0 && w_dtype != MOE_FP8_E4M3) ? 256 : bn;
-  pl.bn_gateup = bn_ok(env_int("MOE_BN_GATEUP")) ? env_int("MOE_BN_GATEUP") : bn;
+  pl.bn_gateup = bn_ok(env_int("MOE_BN_GATEUP")) ? env_int("MOE_BN_GATEUP") : bn_gu;
   pl.bn_down = bn_ok(env_int("MOE_BN_DOWN")) ? env_int("MOE_BN_DOWN") : bn_dn;
   const double touched = E < R ? E : R;
   auto tiles_of = [&](int bn_) {
@@ -702,6 +844,12 @@ TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype) {
   if (env_int("MOE_SPLITS_GATEUP") >= 1 && env_int("MOE_SPLITS_GATEUP") <= 8)
     pl.splits_gateup = env_int("MOE_SPLITS_GATEUP");
   pl.grid = num_sms;
+  // CTA pairs at prefill tiles (>= 128 rows) when the channel count splits
+  // into 256-channel pair tiles; MOE_PAIR=0 keeps single CTAs (tuning)
+  const char* pe = getenv("MOE_PAIR");
+  const bool pairs_ok = !(pe != nullptr && pe[0] == '0') && num_sms >= 2;
+  pl.pair_gateup = pairs_ok && pl.bn_gateup >= 128 && ffn % (2 * kBM) == 0 && pl.splits_gateup == 1 ? 1 : 0;
+  pl.pair_down = pairs_ok && pl.bn_down >= 128 && d % (2 * kBM) == 0 ? 1 : 0;
   return pl;
 }
 
@@ -719,7 +867,9 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   CUtensorMap wg, wu, xb, wd, hb;
   MOE_TRY(make_tmap_2d(&wg, a.w_gate, (uint64_t)a.G * a.ffn, a.d, wb, kBM, kBK, wsw));
   MOE_TRY(make_tmap_2d(&wu, a.w_up, (uint64_t)a.G * a.ffn, a.d, wb, kBM, kBK, wsw));
-  const int box_gu = boxn_of(plan.bn_gateup), box_dn = boxn_of(plan.bn_down);
+  const int box_gu = boxn_of(plan.bn_gateup, plan.pair_gateup != 0);
+  const int box_dn = boxn_of(plan.bn_down, plan.pair_down != 0);
+  if (plan.pair_gateup && a.gather_rows != nullptr) return MOE_ERR_UNSUPPORTED;
   if (a.gather_rows != nullptr)  // token rows by index: one-row boxes for gather4
     MOE_TRY(make_tmap_2d(&xb, a.x_src, a.T_src, a.d, 2, 1, kBK, true));
   else
@@ -745,7 +895,7 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   p.scale1 = a.s_up;
   p.boxn = box_gu;
   p.gather_rows = a.gather_rows;
-  MOE_TRY(launch_mode<kGateUp>(plan.bn_gateup, fp8, p, wg, wu, xb, plan.grid, s));
+  MOE_TRY(launch_mode<kGateUp>(plan.bn_gateup, fp8, plan.pair_gateup != 0, p, wg, wu, xb, plan.grid, s));
   p.gather_rows = nullptr;
   if (gu_split) {
     const size_t n = (size_t)a.R * a.ffn;
@@ -768,7 +918,7 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   p.scale0 = a.s_down;
   p.scale1 = nullptr;
   p.boxn = box_dn;
-  MOE_TRY(launch_mode<kDown>(plan.bn_down, fp8, p, wd, wd, hb, plan.grid, s));
+  MOE_TRY(launch_mode<kDown>(plan.bn_down, fp8, plan.pair_down != 0, p, wd, wd, hb, plan.grid, s));
   return MOE_OK;
 }
 
@@ -792,7 +942,7 @@ moe_status tc_dense_f32_launch(const void* a, const void* b, float* out, int M, 
   p.status = status;
   p.timeout_ns = timeout_ns;
   p.boxn = kBoxLarge;
-  return launch_mode<kDown>(128, false, p, ta, ta, tb, num_sms, s);
+  return launch_mode<kDown>(128, false, false, p, ta, ta, tb, num_sms, s);
 }
 
 moe_status tc_selftest_launch(int* status, long long timeout_ns, cudaStream_t s) {

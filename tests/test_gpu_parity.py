@@ -270,12 +270,14 @@ def _fp8_stack(E, rows, cols, gen, all_codes_expert=None):
     return w, s
 
 
-@pytest.mark.parametrize("bn", [32, 128, 256])
+@pytest.mark.parametrize("bn,pair", [(32, 0), (128, 0), (256, 0), (128, 1), (256, 1)])
 @pytest.mark.parametrize("fp8", [False, True])
-def test_grouped_swiglu_every_tile_size(bn, fp8, monkeypatch):
-    # the same ragged groups through each tile-row count of both GEMMs
+def test_grouped_swiglu_every_tile_size(bn, pair, fp8, monkeypatch):
+    # the same ragged groups through each tile-row count of both GEMMs, on
+    # single CTAs and on CTA pairs (256 output channels per tile)
     monkeypatch.setenv("MOE_BN_GATEUP", str(bn))
     monkeypatch.setenv("MOE_BN_DOWN", str(bn))
+    monkeypatch.setenv("MOE_PAIR", str(pair))
     counts = np.array(GROUP_COUNTS["prefill_like"])
     E, d, f = len(counts), 256, 256
     R = int(counts.sum())
@@ -295,7 +297,9 @@ def test_grouped_swiglu_every_tile_size(bn, fp8, monkeypatch):
         sg = su = sd = None
         ew = oracle.ExpertWeights("bf16", inputs.to_numpy_stored(wg), inputs.to_numpy_stored(wu),
                                   inputs.to_numpy_stored(wd))
-    assert api.moe_plan_info(p)["bn_gateup"] == bn
+    info = api.moe_plan_info(p)
+    assert info["bn_gateup"] == bn
+    assert (info["pair_gateup"], info["pair_down"]) == (pair, pair)
     y = torch.full((R, d), float("nan"), dtype=torch.bfloat16, device=DEV)
     api.moe_grouped_swiglu(p, x, torch.from_numpy(offsets).to(DEV), wg, wu, wd, sg, su, sd, y, api.workspace_for(p))
     torch.cuda.synchronize()
@@ -479,12 +483,15 @@ def test_layer_forward_captured_in_a_cuda_graph_with_stage_timer():
     timer.close()
 
 
-@pytest.mark.parametrize("splits", [1, 3, 8])
+@pytest.mark.parametrize("splits,bn", [(1, 0), (3, 0), (8, 0), (3, 256)])
 @pytest.mark.parametrize("wfmt", ["bf16", "fp8"])
-def test_layer_gateup_split_k(splits, wfmt, monkeypatch):
+def test_layer_gateup_split_k(splits, bn, wfmt, monkeypatch):
     # the gate/up GEMM split along its reduction: fp32 partials, then an
-    # in-order sum and SiLU*mul pass (chosen automatically at tiny batches)
+    # in-order sum and SiLU*mul pass (chosen automatically at tiny batches);
+    # bn=256 forces the interleaved gate/up tile through the same partials
     monkeypatch.setenv("MOE_SPLITS_GATEUP", str(splits))
+    if bn:
+        monkeypatch.setenv("MOE_BN_GATEUP", str(bn))
     shape = inputs.MoEShape("small", T=5, d=512, ffn=256, E=16, k=4, ffn_shared=256 if wfmt == "fp8" else 0,
                             wfmt=wfmt)
     assert api.moe_plan_info(api.problem_of(shape))["splits_gateup"] == splits
