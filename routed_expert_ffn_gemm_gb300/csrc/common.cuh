@@ -50,9 +50,10 @@ inline moe_status cuda_status(cudaError_t err) {
 
 // 2-D row-major tensor map for TMA: `rows` x `cols` elements of
 // `elem_bytes` (2: bf16, 1: bytes), row pitch `cols * elem_bytes`, box
-// `box_cols` x `box_rows`, 128-byte swizzle or none, zero fill out of bounds.
+// `box_cols` x `box_rows`, swizzle of `swizzle_bytes` (128, 64 or 0: none),
+// zero fill out of bounds.
 moe_status make_tmap_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                        int elem_bytes, uint32_t box_rows, uint32_t box_cols, bool swizzle128);
+                        int elem_bytes, uint32_t box_rows, uint32_t box_cols, int swizzle_bytes);
 
 // ---------------------------------------------------------------------------
 // launches: programmatic dependent launch

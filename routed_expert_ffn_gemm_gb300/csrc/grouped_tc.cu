@@ -17,7 +17,7 @@
 // Work unit = (expert g, tile of BN rows, channel tile mt, K split ks).
 // A persistent grid (one CTA per SM) strides over the units; the per-expert
 // tile counts are derived on the device from the offsets (no host sync).
-// CTA roles (320 threads):
+// CTA roles (320 threads; 448 with FP8 weights):
 //   warp 0 lane 0   TMA producer: weight tile(s) [128 x 64] + the row boxes
 //                   per stage, 128-byte swizzle
 //   warp 1 lane 0   MMA issuer: tcgen05.mma kind::f16, fp32 accumulate;
@@ -26,7 +26,9 @@
 //                   quadrant, alternate column chunks), SiLU(g)*u (gate/up)
 //                   or the projection (down), 64-byte coalesced stores
 //   warps 10..13    (FP8 weights only) converters: E4M3 tile staged by TMA ->
-//                   f16 tile in the 128-byte-swizzled layout the MMA reads
+//                   f16 tile, into tensor memory (decode tiles: the MMA
+//                   reads A from TMEM) or into the 128-byte-swizzled
+//                   shared-memory layout the MMA reads
 // CTA pairs (prefill tiles): a cluster of two CTAs runs each unit with
 // cta_group::2 MMAs, M = 256 channels (128 per CTA, each CTA's TMEM holding
 // its own accumulator rows); each CTA stages its 128 weight rows and half
@@ -106,6 +108,10 @@ struct Cfg {
   static constexpr int A_BYTES = kBM * kBK * 2;                // 16 KB bf16 tile (MMA operand)
   static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * kBK * 2;
   static constexpr int STG_BYTES = FP8 ? kBM * kBK : 0;        // 8 KB E4M3 staging tile
+  // FP8 decode tiles: the converters write the f16 weight tile into tensor
+  // memory (tcgen05.st) and the MMA reads A from there, so the f16 operand
+  // never passes through shared memory
+  static constexpr bool TA = FP8 && BN == 32 && !PAIR;
   // bf16: one ring of TMA slots [A0 A1 | B] read by the MMA.  FP8: a deep
   // ring of TMA slots [E4M3 A0 A1 | B] (cheap bytes: it hides HBM latency)
   // and a short ring of OSTAGES f16 operand slots [A0 A1] that the
@@ -113,12 +119,13 @@ struct Cfg {
   // operand slots: enough that converters run ahead of the MMA's commits
   // (a commit round trip per slot otherwise serialises decode), while the
   // TMA ring keeps at least 4 slots
-  static constexpr int OPND_BYTES = NA * A_BYTES;
+  static constexpr int OPND_BYTES = TA ? 0 : NA * A_BYTES;
   static constexpr int W_BYTES_ = FP8 ? STG_BYTES : A_BYTES;
   static constexpr int SLOT_ = NA * W_BYTES_ + B_BYTES;
   static constexpr int AVAIL_ = kSmemLimit - 1024 - (8 * 40 + 16 + 4 * 2 * (kMaxGroups + 8));
-  static constexpr int OSTAGES = !FP8 ? 0 : (AVAIL_ - 6 * SLOT_) / OPND_BYTES >= 4 ? 4
-                                          : (AVAIL_ - 6 * SLOT_) / OPND_BYTES >= 3 ? 3 : 2;
+  static constexpr int OSTAGES = !FP8 ? 0 : TA ? 4
+                                 : (AVAIL_ - 6 * SLOT_) / (NA * A_BYTES) >= 4 ? 4
+                                 : (AVAIL_ - 6 * SLOT_) / (NA * A_BYTES) >= 3 ? 3 : 2;
   static constexpr int RING_OFF = OSTAGES * OPND_BYTES;
   static constexpr int W_BYTES = FP8 ? STG_BYTES : A_BYTES;    // weight tile bytes in a TMA slot
   static constexpr int B_OFF = NA * W_BYTES;
@@ -145,6 +152,14 @@ struct Cfg {
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
   static_assert(BN % 16 == 0 && BN <= 256 && ACC_COLS <= 512, "tile rows");
   static_assert(!PAIR || BN >= 64, "pair tiles split B rows in halves");
+  static_assert(!TA || (UP_OFF == 128 && ACC_COLS * NBUF <= 512), "TMEM operand slots sit between accumulators");
+  // TMEM column of operand slot o, weight matrix a (TA): the 32-column
+  // accumulators of a decode tile sit at multiples of 128, the 96 columns
+  // after each hold three 32-column A tiles (64 f16 of K per lane)
+  static __device__ __forceinline__ uint32_t ta_col(int o, int a) {
+    const int i = o * NA + a;
+    return (uint32_t)((i / 3) * 128 + 32 * (1 + i % 3));
+  }
 };
 
 struct Unit {
@@ -475,7 +490,11 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk) {
               const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
-              if (PAIR) {
+              if (C::TA) {
+                const uint32_t at = tmem_base + 8u * kk;  // 16 f16 of K = 8 columns
+                ptx::mma_f16_ta(d0, at + C::ta_col(ostage, 0), db + 2 * kk, idesc, acc);
+                if (MODE == kGateUp) ptx::mma_f16_ta(d1, at + C::ta_col(ostage, 1), db + 2 * kk, idesc, acc);
+              } else if (PAIR) {
                 ptx::mma_f16_pair(d0, da0 + 2 * kk, db + 2 * kk, idesc, acc);
                 if (MODE == kGateUp) ptx::mma_f16_pair(d1, da1 + 2 * kk, db + 2 * kk, idesc, acc);
               } else {
@@ -618,10 +637,10 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
     // ------------------------------------------------------------ converters
     // Same unit / k-block walk as the MMA issuer; the four converter warps
     // share each stage.  Per k-block: wait for the E4M3 tiles in the TMA
-    // slot and for a free operand slot, write the f16 tiles into the
-    // swizzled operand slot (16-byte chunk j of row r at chunk position
-    // j ^ (r % 8)), make the writes visible to the tensor core, then arrive
-    // on opnd_full.  The MMA's commit frees both slots.
+    // slot and for a free operand slot, write the f16 tiles (tensor memory
+    // or a shared-memory operand slot), make the writes visible to the
+    // tensor core, then arrive on opnd_full.  The MMA's commit frees both
+    // slots.
     const int ct = threadIdx.x - kThreads;  // 0 .. kConvThreads-1
     int stage = 0, ostage = 0;
     uint32_t phase = 0, ophase = 0;
@@ -642,21 +661,54 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
           break;
         }
         const uint8_t* st = smem + C::RING_OFF + stage * C::STAGE_BYTES;
-        uint8_t* op = smem + ostage * C::OPND_BYTES;
+        if constexpr (C::TA) {
+          // one weight row per thread: the row is this warp's TMEM lane
+          // (quadrant warp % 4); the staging tile carries the 64-byte swizzle
+          // (16-byte chunk c of row r at chunk c ^ ((r >> 1) & 3)), so the
+          // warp's 32 rows read conflict-free
+          ptx::tc_fence_after();
+          const int qd = warp & 3;
+          const int r = qd * 32 + lane;
 #pragma unroll
-        for (int a = 0; a < C::NA; ++a) {
-          const uint8_t* src = st + a * C::STG_BYTES;
-          uint8_t* dst = op + a * C::A_BYTES;
+          for (int a = 0; a < C::NA; ++a) {
+            const uint8_t* src = st + a * C::STG_BYTES + r * kBK;
+            uint32_t w[32];
 #pragma unroll
-          for (int i = ct; i < kBM * kBK / 16; i += kConvThreads) {  // 16 E4M3 per chunk
-            const int r = i >> 2, c = i & 3;
-            const uint4 v = *reinterpret_cast<const uint4*>(src + r * kBK + c * 16);
-            const int sw = r & 7;
-            *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * c) ^ sw) << 4)) = e4m3x8_to_f16x8(v.x, v.y);
-            *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * c + 1) ^ sw) << 4)) = e4m3x8_to_f16x8(v.z, v.w);
+            for (int c = 0; c < 4; ++c) {
+              const uint4 v = *reinterpret_cast<const uint4*>(src + ((c ^ ((r >> 1) & 3)) << 4));
+              const uint4 lo = e4m3x8_to_f16x8(v.x, v.y), hi = e4m3x8_to_f16x8(v.z, v.w);
+              w[8 * c + 0] = lo.x;
+              w[8 * c + 1] = lo.y;
+              w[8 * c + 2] = lo.z;
+              w[8 * c + 3] = lo.w;
+              w[8 * c + 4] = hi.x;
+              w[8 * c + 5] = hi.y;
+              w[8 * c + 6] = hi.z;
+              w[8 * c + 7] = hi.w;
+            }
+            ptx::tmem_st32(tmem_base + ((uint32_t)(qd * 32) << 16) + C::ta_col(ostage, a), w);
           }
+          ptx::tmem_st_wait();
+          ptx::tc_fence_before();
+        } else {
+          // the f16 tile goes to the swizzled shared-memory operand slot
+          // (16-byte chunk j of row r at chunk position j ^ (r % 8))
+          uint8_t* op = smem + ostage * C::OPND_BYTES;
+#pragma unroll
+          for (int a = 0; a < C::NA; ++a) {
+            const uint8_t* src = st + a * C::STG_BYTES;
+            uint8_t* dst = op + a * C::A_BYTES;
+#pragma unroll
+            for (int i = ct; i < kBM * kBK / 16; i += kConvThreads) {  // 16 E4M3 per chunk
+              const int r = i >> 2, c = i & 3;
+              const uint4 v = *reinterpret_cast<const uint4*>(src + r * kBK + c * 16);
+              const int sw = r & 7;
+              *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * c) ^ sw) << 4)) = e4m3x8_to_f16x8(v.x, v.y);
+              *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * c + 1) ^ sw) << 4)) = e4m3x8_to_f16x8(v.z, v.w);
+            }
+          }
+          ptx::fence_proxy_async_smem();
         }
-        ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
           if (PAIR)
@@ -819,7 +871,7 @@ int boxn_of(int bn, bool pair) {
 
 // Rows per tile from the expected rows per expert: 32 for decode (a few rows
 // each), else 128; at prefill (>= 128 rows per expert on average) both GEMMs
-// take 256 (the bf16 down GEMM; FP8 down tiles of 256 leave too few stages).
+// take 256.
 // Gate/up at 256 rows has one TMEM buffer (its epilogue is not overlapped
 // with the next unit's MMAs), yet on CTA pairs it moves the fewest operand
 // bytes per flop and measured fastest on GB300 (with the eight-warp
@@ -831,7 +883,7 @@ TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype) {
   const double est_max = mean + 3.0 * __builtin_sqrt(mean) + 1.0;
   const int bn = est_max <= 32.0 ? 32 : 128;
   const int bn_gu = (bn == 128 && mean >= 128.0) ? 256 : bn;
-  const int bn_dn = (bn == 128 && mean >= 128.0 && w_dtype != MOE_FP8_E4M3) ? 256 : bn;
+  const int bn_dn = (bn == 128 && mean >= 128.0) ? 256 : bn;
   pl.bn_gateup = bn_ok(env_int("MOE_BN_GATEUP")) ? env_int("MOE_BN_GATEUP") : bn_gu;
   pl.bn_down = bn_ok(env_int("MOE_BN_DOWN")) ? env_int("MOE_BN_DOWN") : bn_dn;
   const double touched = E < R ? E : R;
@@ -863,19 +915,22 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   // weights: bf16 tiles [128 x 64] with 128-byte swizzle, or E4M3 tiles
   // [128 x 64 bytes] staged unswizzled for the converters
   const int wb = fp8 ? 1 : 2;
-  const bool wsw = !fp8;
+  // E4M3 staging for the tensor-memory operand path (decode tiles) carries
+  // the 64-byte swizzle its converters read conflict-free
+  const int wsw_gu = !fp8 ? 128 : (plan.bn_gateup == 32 && !plan.pair_gateup) ? 64 : 0;
+  const int wsw_dn = !fp8 ? 128 : (plan.bn_down == 32 && !plan.pair_down) ? 64 : 0;
   CUtensorMap wg, wu, xb, wd, hb;
-  MOE_TRY(make_tmap_2d(&wg, a.w_gate, (uint64_t)a.G * a.ffn, a.d, wb, kBM, kBK, wsw));
-  MOE_TRY(make_tmap_2d(&wu, a.w_up, (uint64_t)a.G * a.ffn, a.d, wb, kBM, kBK, wsw));
+  MOE_TRY(make_tmap_2d(&wg, a.w_gate, (uint64_t)a.G * a.ffn, a.d, wb, kBM, kBK, wsw_gu));
+  MOE_TRY(make_tmap_2d(&wu, a.w_up, (uint64_t)a.G * a.ffn, a.d, wb, kBM, kBK, wsw_gu));
   const int box_gu = boxn_of(plan.bn_gateup, plan.pair_gateup != 0);
   const int box_dn = boxn_of(plan.bn_down, plan.pair_down != 0);
   if (plan.pair_gateup && a.gather_rows != nullptr) return MOE_ERR_UNSUPPORTED;
   if (a.gather_rows != nullptr)  // token rows by index: one-row boxes for gather4
-    MOE_TRY(make_tmap_2d(&xb, a.x_src, a.T_src, a.d, 2, 1, kBK, true));
+    MOE_TRY(make_tmap_2d(&xb, a.x_src, a.T_src, a.d, 2, 1, kBK, 128));
   else
-    MOE_TRY(make_tmap_2d(&xb, a.x_perm, a.R, a.d, 2, box_gu, kBK, true));
-  MOE_TRY(make_tmap_2d(&wd, a.w_down, (uint64_t)a.G * a.d, a.ffn, wb, kBM, kBK, wsw));
-  MOE_TRY(make_tmap_2d(&hb, a.h, a.R, a.ffn, 2, box_dn, kBK, true));
+    MOE_TRY(make_tmap_2d(&xb, a.x_perm, a.R, a.d, 2, box_gu, kBK, 128));
+  MOE_TRY(make_tmap_2d(&wd, a.w_down, (uint64_t)a.G * a.d, a.ffn, wb, kBM, kBK, wsw_dn));
+  MOE_TRY(make_tmap_2d(&hb, a.h, a.R, a.ffn, 2, box_dn, kBK, 128));
 
   TcParams p{};
   p.G = a.G;
@@ -928,8 +983,8 @@ moe_status tc_dense_f32_launch(const void* a, const void* b, float* out, int M, 
   if (N == 0) return MOE_OK;
   if (M % kBM != 0 || K % 8 != 0 || splits < 1) return MOE_ERR_UNSUPPORTED;
   CUtensorMap ta, tb;
-  MOE_TRY(make_tmap_2d(&ta, a, (uint64_t)M, K, 2, kBM, kBK, true));
-  MOE_TRY(make_tmap_2d(&tb, b, (uint64_t)N, K, 2, kBoxLarge, kBK, true));
+  MOE_TRY(make_tmap_2d(&ta, a, (uint64_t)M, K, 2, kBM, kBK, 128));
+  MOE_TRY(make_tmap_2d(&tb, b, (uint64_t)N, K, 2, kBoxLarge, kBK, 128));
   TcParams p{};
   p.G = 1;
   p.dense = 1;
