@@ -105,13 +105,18 @@ struct Cfg {
   // the unit's B rows, so a CTA moves half the B bytes per flop
   static constexpr int CH = PAIR ? 2 * kBM : kBM;               // output channels per unit
   static constexpr int NA = MODE == kGateUp ? 2 : 1;           // weight operands per stage
-  static constexpr int A_BYTES = kBM * kBK * 2;                // 16 KB bf16 tile (MMA operand)
-  static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * kBK * 2;
-  static constexpr int STG_BYTES = FP8 ? kBM * kBK : 0;        // 8 KB E4M3 staging tile
   // FP8 decode tiles: the converters write the f16 weight tile into tensor
   // memory (tcgen05.st) and the MMA reads A from there, so the f16 operand
-  // never passes through shared memory
+  // never passes through shared memory.  Their stages span 128 elements of
+  // K: 128-byte E4M3 rows (64-byte rows cost as many copy requests per row
+  // as 128-byte bf16 rows, for half the bytes), B in two 64-element halves.
   static constexpr bool TA = FP8 && BN == 32 && !PAIR;
+  static constexpr int KB = TA ? 2 * kBK : kBK;                // K elements per stage
+  static constexpr int NSUB = KB / kBK;                        // 64-element B sub-tiles per stage
+  static constexpr int A_BYTES = kBM * kBK * 2;                // 16 KB bf16 tile (MMA operand)
+  static constexpr int BSUB_BYTES = (PAIR ? BN / 2 : BN) * kBK * 2;
+  static constexpr int B_BYTES = NSUB * BSUB_BYTES;
+  static constexpr int STG_BYTES = FP8 ? kBM * KB : 0;         // E4M3 staging tile (8 or 16 KB)
   // bf16: one ring of TMA slots [A0 A1 | B] read by the MMA.  FP8: a deep
   // ring of TMA slots [E4M3 A0 A1 | B] (cheap bytes: it hides HBM latency)
   // and a short ring of OSTAGES f16 operand slots [A0 A1] that the
@@ -123,7 +128,7 @@ struct Cfg {
   static constexpr int W_BYTES_ = FP8 ? STG_BYTES : A_BYTES;
   static constexpr int SLOT_ = NA * W_BYTES_ + B_BYTES;
   static constexpr int AVAIL_ = kSmemLimit - 1024 - (8 * 40 + 16 + 4 * 2 * (kMaxGroups + 8));
-  static constexpr int OSTAGES = !FP8 ? 0 : TA ? 4
+  static constexpr int OSTAGES = !FP8 ? 0 : TA ? 4 / NA
                                  : (AVAIL_ - 6 * SLOT_) / (NA * A_BYTES) >= 4 ? 4
                                  : (AVAIL_ - 6 * SLOT_) / (NA * A_BYTES) >= 3 ? 3 : 2;
   static constexpr int RING_OFF = OSTAGES * OPND_BYTES;
@@ -152,13 +157,13 @@ struct Cfg {
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
   static_assert(BN % 16 == 0 && BN <= 256 && ACC_COLS <= 512, "tile rows");
   static_assert(!PAIR || BN >= 64, "pair tiles split B rows in halves");
-  static_assert(!TA || (UP_OFF == 128 && ACC_COLS * NBUF <= 512), "TMEM operand slots sit between accumulators");
+  static_assert(!TA || (UP_OFF == 128 && ACC_COLS * NBUF <= 512 && OSTAGES * NA <= 4),
+                "TMEM operand slots sit between accumulators");
   // TMEM column of operand slot o, weight matrix a (TA): the 32-column
-  // accumulators of a decode tile sit at multiples of 128, the 96 columns
-  // after each hold three 32-column A tiles (64 f16 of K per lane)
+  // accumulators of a decode tile sit at multiples of 128; columns 64..127
+  // after each hold one 64-column A tile (128 f16 of K per lane)
   static __device__ __forceinline__ uint32_t ta_col(int o, int a) {
-    const int i = o * NA + a;
-    return (uint32_t)((i / 3) * 128 + 32 * (1 + i % 3));
+    return (uint32_t)(64 + 128 * (o * NA + a));
   }
 };
 
@@ -334,7 +339,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
   const int MT = p.M / C::CH;
   const int S = p.splits;
   const int total_units = p.selftest ? 1 : prefix[G] * MT * S;
-  const int kblocks = (p.K + kBK - 1) / kBK;
+  const int kblocks = (p.K + C::KB - 1) / C::KB;
   const int kb_per_split = (kblocks + S - 1) / S;
 
   if (warp == 0) {
@@ -371,7 +376,8 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
             const int i = 4 * (lane + 32 * h) + q;
             gr[h][q] = (gather && lane + 32 * h < nops) ? p.gather_rows[x.row0 + (i < x.n_valid ? i : 0)] : 0;
           }
-        const uint32_t bbytes = gather ? (uint32_t)nops * 4 * kBK * 2 : (uint32_t)nbox * p.boxn * kBK * 2;
+        const uint32_t bbytes =
+            C::NSUB * (gather ? (uint32_t)nops * 4 * kBK * 2 : (uint32_t)nbox * p.boxn * kBK * 2);
         const uint32_t bytes = C::NA * C::W_BYTES + bbytes;
         const int arow = x.g * p.M + x.mt * C::CH + (int)rank * kBM;
         for (int kb = kb0; kb < kb1; ++kb) {
@@ -392,19 +398,21 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
               // both CTAs' copies complete the even CTA's barrier
               const uint32_t fb = lead(full_bar(stage));
               ptx::mbar_arrive_expect_tx_cluster(fb, bytes);
-              ptx::tma_load_2d_pair(sa, &tmA0, fb, kb * kBK, arow, pol_w);
-              if (MODE == kGateUp) ptx::tma_load_2d_pair(sa + C::W_BYTES, &tmA1, fb, kb * kBK, arow, pol_w);
+              ptx::tma_load_2d_pair(sa, &tmA0, fb, kb * C::KB, arow, pol_w);
+              if (MODE == kGateUp) ptx::tma_load_2d_pair(sa + C::W_BYTES, &tmA1, fb, kb * C::KB, arow, pol_w);
               for (int i = 0; i < nbox; ++i)
-                ptx::tma_load_2d_pair(sb + i * p.boxn * kBK * 2, &tmB, fb, kb * kBK, brow0 + i * p.boxn, pol_x);
+                ptx::tma_load_2d_pair(sb + i * p.boxn * kBK * 2, &tmB, fb, kb * C::KB, brow0 + i * p.boxn, pol_x);
             } else {
               ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
-              ptx::tma_load_2d(sa, &tmA0, full_bar(stage), kb * kBK, arow, pol_w);
+              ptx::tma_load_2d(sa, &tmA0, full_bar(stage), kb * C::KB, arow, pol_w);
               if (MODE == kGateUp)
-                ptx::tma_load_2d(sa + C::W_BYTES, &tmA1, full_bar(stage), kb * kBK, arow, pol_w);
+                ptx::tma_load_2d(sa + C::W_BYTES, &tmA1, full_bar(stage), kb * C::KB, arow, pol_w);
               if (!gather)
-                for (int i = 0; i < nbox; ++i)
-                  ptx::tma_load_2d(sb + i * p.boxn * kBK * 2, &tmB, full_bar(stage), kb * kBK,
-                                   brow0 + i * p.boxn, pol_x);
+#pragma unroll
+                for (int sub = 0; sub < C::NSUB; ++sub)
+                  for (int i = 0; i < nbox; ++i)
+                    ptx::tma_load_2d(sb + sub * C::BSUB_BYTES + i * p.boxn * kBK * 2, &tmB, full_bar(stage),
+                                     kb * C::KB + sub * kBK, brow0 + i * p.boxn, pol_x);
             }
           }
           __syncwarp();
@@ -413,8 +421,10 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
             for (int h = 0; h < 2; ++h) {
               const int op = lane + 32 * h;
               if (op < nops)
-                ptx::tma_gather4_2d(sb + op * 4 * kBK * 2, &tmB, full_bar(stage), kb * kBK, gr[h][0],
-                                    gr[h][1], gr[h][2], gr[h][3], pol_x);
+#pragma unroll
+                for (int sub = 0; sub < C::NSUB; ++sub)
+                  ptx::tma_gather4_2d(sb + sub * C::BSUB_BYTES + op * 4 * kBK * 2, &tmB, full_bar(stage),
+                                      kb * C::KB + sub * kBK, gr[h][0], gr[h][1], gr[h][2], gr[h][3], pol_x);
             }
           }
           if (++stage == STAGES) {
@@ -486,20 +496,21 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
             const uint32_t aa = FP8 ? sbase + ostage * C::OPND_BYTES : sa;
             const uint64_t da0 = ptx::sdesc_k_sw128(aa);
             const uint64_t da1 = ptx::sdesc_k_sw128(aa + C::A_BYTES);
-            const uint64_t db = ptx::sdesc_k_sw128(sa + C::B_OFF);
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk) {
+            for (int kk = 0; kk < C::KB / 16; ++kk) {
               const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
+              // B: 64-element sub-tile kk / 4, K step kk % 4 inside it
+              const uint64_t db = ptx::sdesc_k_sw128(sa + C::B_OFF + (kk >> 2) * C::BSUB_BYTES) + 2 * (kk & 3);
               if (C::TA) {
                 const uint32_t at = tmem_base + 8u * kk;  // 16 f16 of K = 8 columns
-                ptx::mma_f16_ta(d0, at + C::ta_col(ostage, 0), db + 2 * kk, idesc, acc);
-                if (MODE == kGateUp) ptx::mma_f16_ta(d1, at + C::ta_col(ostage, 1), db + 2 * kk, idesc, acc);
+                ptx::mma_f16_ta(d0, at + C::ta_col(ostage, 0), db, idesc, acc);
+                if (MODE == kGateUp) ptx::mma_f16_ta(d1, at + C::ta_col(ostage, 1), db, idesc, acc);
               } else if (PAIR) {
-                ptx::mma_f16_pair(d0, da0 + 2 * kk, db + 2 * kk, idesc, acc);
-                if (MODE == kGateUp) ptx::mma_f16_pair(d1, da1 + 2 * kk, db + 2 * kk, idesc, acc);
+                ptx::mma_f16_pair(d0, da0 + 2 * kk, db, idesc, acc);
+                if (MODE == kGateUp) ptx::mma_f16_pair(d1, da1 + 2 * kk, db, idesc, acc);
               } else {
-                ptx::mma_f16(d0, da0 + 2 * kk, db + 2 * kk, idesc, acc);
-                if (MODE == kGateUp) ptx::mma_f16(d1, da1 + 2 * kk, db + 2 * kk, idesc, acc);
+                ptx::mma_f16(d0, da0 + 2 * kk, db, idesc, acc);
+                if (MODE == kGateUp) ptx::mma_f16(d1, da1 + 2 * kk, db, idesc, acc);
               }
             }
             issued = true;
@@ -553,6 +564,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
       const Unit x = decode_unit(u, offs, prefix, G, MT, S, BN);
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(C::ACC_COLS * buf);
       const int ch = x.mt * C::CH + (int)rank * kBM + ch_local;
+      const bool empty_k = x.ks * kb_per_split >= kblocks;
       const int n_mma = ((x.n_valid + 15) / 16) * 16;
       const float sc0 = FP8 ? p.scale0[(size_t)x.g * p.M + ch] : 1.f;
       const float sc1 = FP8 && MODE == kGateUp ? p.scale1[(size_t)x.g * p.M + ch] : 1.f;
@@ -572,6 +584,12 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
                            *reinterpret_cast<uint32_t(*)[16]>(&rb[16 * hlf]));
         }
         ptx::tmem_ld_wait();
+        if (empty_k) {
+          // a K split past the end of K (ceil-sized splits): no MMA wrote
+          // this accumulator, its partial sums are zero
+#pragma unroll
+          for (int j = 0; j < CW; ++j) ra[j] = rb[j] = 0u;
+        }
         // halves of 16 columns; the empty asm keeps the compiler from
         // interleaving them (which costs registers, not time)
 #pragma unroll
@@ -663,30 +681,34 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
         const uint8_t* st = smem + C::RING_OFF + stage * C::STAGE_BYTES;
         if constexpr (C::TA) {
           // one weight row per thread: the row is this warp's TMEM lane
-          // (quadrant warp % 4); the staging tile carries the 64-byte swizzle
-          // (16-byte chunk c of row r at chunk c ^ ((r >> 1) & 3)), so the
-          // warp's 32 rows read conflict-free
+          // (quadrant warp % 4); the 128-byte staging rows carry the 128-byte
+          // swizzle (16-byte chunk c of row r at chunk c ^ (r & 7)), so the
+          // warp's 32 rows read conflict-free; each half row (64 E4M3) fills
+          // 32 TMEM columns
           ptx::tc_fence_after();
           const int qd = warp & 3;
           const int r = qd * 32 + lane;
 #pragma unroll
           for (int a = 0; a < C::NA; ++a) {
-            const uint8_t* src = st + a * C::STG_BYTES + r * kBK;
-            uint32_t w[32];
+            const uint8_t* src = st + a * C::STG_BYTES + r * C::KB;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const uint4 v = *reinterpret_cast<const uint4*>(src + ((c ^ ((r >> 1) & 3)) << 4));
-              const uint4 lo = e4m3x8_to_f16x8(v.x, v.y), hi = e4m3x8_to_f16x8(v.z, v.w);
-              w[8 * c + 0] = lo.x;
-              w[8 * c + 1] = lo.y;
-              w[8 * c + 2] = lo.z;
-              w[8 * c + 3] = lo.w;
-              w[8 * c + 4] = hi.x;
-              w[8 * c + 5] = hi.y;
-              w[8 * c + 6] = hi.z;
-              w[8 * c + 7] = hi.w;
+            for (int hf = 0; hf < C::KB / 64; ++hf) {
+              uint32_t w[32];
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                const uint4 v = *reinterpret_cast<const uint4*>(src + (((4 * hf + c) ^ (r & 7)) << 4));
+                const uint4 lo = e4m3x8_to_f16x8(v.x, v.y), hi = e4m3x8_to_f16x8(v.z, v.w);
+                w[8 * c + 0] = lo.x;
+                w[8 * c + 1] = lo.y;
+                w[8 * c + 2] = lo.z;
+                w[8 * c + 3] = lo.w;
+                w[8 * c + 4] = hi.x;
+                w[8 * c + 5] = hi.y;
+                w[8 * c + 6] = hi.z;
+                w[8 * c + 7] = hi.w;
+              }
+              ptx::tmem_st32(tmem_base + ((uint32_t)(qd * 32) << 16) + C::ta_col(ostage, a) + 32 * hf, w);
             }
-            ptx::tmem_st32(tmem_base + ((uint32_t)(qd * 32) << 16) + C::ta_col(ostage, a), w);
           }
           ptx::tmem_st_wait();
           ptx::tc_fence_before();
@@ -891,8 +913,11 @@ TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype) {
     const double a = R / bn_;
     return (int)(touched > a ? touched : a + 0.5);
   };
-  pl.splits_down = choose_splits(tiles_of(pl.bn_down) * (d / kBM), (ffn + kBK - 1) / kBK, num_sms);
-  pl.splits_gateup = choose_splits(tiles_of(pl.bn_gateup) * (ffn / kBM), (d + kBK - 1) / kBK, num_sms);
+  // K per stage: 128 on the FP8 tensor-memory operand path (decode tiles)
+  const int kw_dn = w_dtype == MOE_FP8_E4M3 && pl.bn_down == 32 ? 2 * kBK : kBK;
+  const int kw_gu = w_dtype == MOE_FP8_E4M3 && pl.bn_gateup == 32 ? 2 * kBK : kBK;
+  pl.splits_down = choose_splits(tiles_of(pl.bn_down) * (d / kBM), (ffn + kw_dn - 1) / kw_dn, num_sms);
+  pl.splits_gateup = choose_splits(tiles_of(pl.bn_gateup) * (ffn / kBM), (d + kw_gu - 1) / kw_gu, num_sms);
   if (env_int("MOE_SPLITS_GATEUP") >= 1 && env_int("MOE_SPLITS_GATEUP") <= 8)
     pl.splits_gateup = env_int("MOE_SPLITS_GATEUP");
   pl.grid = num_sms;
@@ -915,13 +940,16 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   // weights: bf16 tiles [128 x 64] with 128-byte swizzle, or E4M3 tiles
   // [128 x 64 bytes] staged unswizzled for the converters
   const int wb = fp8 ? 1 : 2;
-  // E4M3 staging for the tensor-memory operand path (decode tiles) carries
-  // the 64-byte swizzle its converters read conflict-free
-  const int wsw_gu = !fp8 ? 128 : (plan.bn_gateup == 32 && !plan.pair_gateup) ? 64 : 0;
-  const int wsw_dn = !fp8 ? 128 : (plan.bn_down == 32 && !plan.pair_down) ? 64 : 0;
+  // E4M3 staging for the tensor-memory operand path (decode tiles): boxes
+  // 128 bytes wide with the 128-byte swizzle its converters read
+  // conflict-free
+  const bool ta_gu = fp8 && plan.bn_gateup == 32 && !plan.pair_gateup;
+  const bool ta_dn = fp8 && plan.bn_down == 32 && !plan.pair_down;
+  const int wsw_gu = !fp8 || ta_gu ? 128 : 0, wsw_dn = !fp8 || ta_dn ? 128 : 0;
+  const int wk_gu = ta_gu ? 2 * kBK : kBK, wk_dn = ta_dn ? 2 * kBK : kBK;
   CUtensorMap wg, wu, xb, wd, hb;
-  MOE_TRY(make_tmap_2d(&wg, a.w_gate, (uint64_t)a.G * a.ffn, a.d, wb, kBM, kBK, wsw_gu));
-  MOE_TRY(make_tmap_2d(&wu, a.w_up, (uint64_t)a.G * a.ffn, a.d, wb, kBM, kBK, wsw_gu));
+  MOE_TRY(make_tmap_2d(&wg, a.w_gate, (uint64_t)a.G * a.ffn, a.d, wb, kBM, wk_gu, wsw_gu));
+  MOE_TRY(make_tmap_2d(&wu, a.w_up, (uint64_t)a.G * a.ffn, a.d, wb, kBM, wk_gu, wsw_gu));
   const int box_gu = boxn_of(plan.bn_gateup, plan.pair_gateup != 0);
   const int box_dn = boxn_of(plan.bn_down, plan.pair_down != 0);
   if (plan.pair_gateup && a.gather_rows != nullptr) return MOE_ERR_UNSUPPORTED;
@@ -929,7 +957,7 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
     MOE_TRY(make_tmap_2d(&xb, a.x_src, a.T_src, a.d, 2, 1, kBK, 128));
   else
     MOE_TRY(make_tmap_2d(&xb, a.x_perm, a.R, a.d, 2, box_gu, kBK, 128));
-  MOE_TRY(make_tmap_2d(&wd, a.w_down, (uint64_t)a.G * a.d, a.ffn, wb, kBM, kBK, wsw_dn));
+  MOE_TRY(make_tmap_2d(&wd, a.w_down, (uint64_t)a.G * a.d, a.ffn, wb, kBM, wk_dn, wsw_dn));
   MOE_TRY(make_tmap_2d(&hb, a.h, a.R, a.ffn, 2, box_dn, kBK, 128));
 
   TcParams p{};

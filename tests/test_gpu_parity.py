@@ -483,16 +483,18 @@ def test_layer_forward_captured_in_a_cuda_graph_with_stage_timer():
     timer.close()
 
 
-@pytest.mark.parametrize("splits,bn", [(1, 0), (3, 0), (8, 0), (3, 256)])
+@pytest.mark.parametrize("splits,bn,d", [(1, 0, 512), (3, 0, 512), (8, 0, 512), (3, 256, 512), (8, 0, 640)])
 @pytest.mark.parametrize("wfmt", ["bf16", "fp8"])
-def test_layer_gateup_split_k(splits, bn, wfmt, monkeypatch):
+def test_layer_gateup_split_k(splits, bn, d, wfmt, monkeypatch):
     # the gate/up GEMM split along its reduction: fp32 partials, then an
     # in-order sum and SiLU*mul pass (chosen automatically at tiny batches);
-    # bn=256 forces the interleaved gate/up tile through the same partials
+    # bn=256 forces the 256-row tile through the same partials; ceil-sized
+    # splits can leave the last ones without k-blocks (d=640 in 64-element
+    # blocks over 8 splits, d=512 in the 128-element FP8 decode blocks)
     monkeypatch.setenv("MOE_SPLITS_GATEUP", str(splits))
     if bn:
         monkeypatch.setenv("MOE_BN_GATEUP", str(bn))
-    shape = inputs.MoEShape("small", T=5, d=512, ffn=256, E=16, k=4, ffn_shared=256 if wfmt == "fp8" else 0,
+    shape = inputs.MoEShape("small", T=5, d=d, ffn=256, E=16, k=4, ffn_shared=256 if wfmt == "fp8" else 0,
                             wfmt=wfmt)
     assert api.moe_plan_info(api.problem_of(shape))["splits_gateup"] == splits
     _layer_check(shape, 4, FP8_TOL if wfmt == "fp8" else BF16_TOL)
