@@ -194,28 +194,62 @@ __global__ void __launch_bounds__(256) permute_count_kernel(int R, int E,
 }
 
 // chunk_cnt[c][e] -> offsets[e] + sum_{c'<c} chunk_cnt[c'][e] (in place).
+// One block of 1024 threads: 32 experts at a time along the lanes (loads
+// coalesced over experts), the chunks split into 32 slices over the warps;
+// per-slice sums combine through shared memory.  A first pass finds the
+// per-expert totals (-> counts, offsets), a second writes the running sums.
 __global__ void __launch_bounds__(1024) permute_scan_kernel(int n_chunks, int E,
                                                             int32_t* __restrict__ chunk_cnt,
                                                             int32_t* __restrict__ counts,
                                                             int32_t* __restrict__ offsets) {
   griddep_begin();
+  __shared__ int part[32][33];
+  __shared__ int base_e[1024];
   __shared__ int warp_tot[32];
-  const int e = threadIdx.x;
-  int tot = 0;
-  if (e < E) {
-    for (int c = 0; c < n_chunks; ++c) {
-      const int v = chunk_cnt[(size_t)c * E + e];
-      chunk_cnt[(size_t)c * E + e] = tot;
-      tot += v;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int per = (n_chunks + 31) / 32;
+  const int c0 = min(n_chunks, w * per), c1 = min(n_chunks, c0 + per);
+  for (int g = 0; g < E; g += 32) {
+    const int e = g + lane;
+    int sum = 0;
+    if (e < E)
+      for (int c = c0; c < c1; ++c) sum += chunk_cnt[(size_t)c * E + e];
+    part[w][lane] = sum;
+    __syncthreads();
+    if (w == 0 && e < E) {
+      int t = 0;
+      for (int i = 0; i < 32; ++i) t += part[i][lane];
+      base_e[e] = t;
     }
+    __syncthreads();
   }
-  const int incl = block_inclusive_scan(e < E ? tot : 0, warp_tot);
-  const int base = incl - tot;
+  const int e = threadIdx.x;
+  const int tot = e < E ? base_e[e] : 0;
+  const int incl = block_inclusive_scan(tot, warp_tot);
   if (e < E) {
     counts[e] = tot;
-    offsets[e] = base;
+    offsets[e] = incl - tot;
     if (e == E - 1) offsets[E] = incl;
-    for (int c = 0; c < n_chunks; ++c) chunk_cnt[(size_t)c * E + e] += base;
+    base_e[e] = incl - tot;
+  }
+  __syncthreads();
+  for (int g = 0; g < E; g += 32) {
+    const int e2 = g + lane;
+    int sum = 0;
+    if (e2 < E)
+      for (int c = c0; c < c1; ++c) sum += chunk_cnt[(size_t)c * E + e2];
+    part[w][lane] = sum;
+    __syncthreads();
+    if (e2 < E) {
+      int run = base_e[e2];
+      for (int i = 0; i < w; ++i) run += part[i][lane];
+      for (int c = c0; c < c1; ++c) {
+        const int v = chunk_cnt[(size_t)c * E + e2];
+        chunk_cnt[(size_t)c * E + e2] = run;
+        run += v;
+      }
+    }
+    __syncthreads();
   }
 }
 
