@@ -97,6 +97,14 @@ struct TcParams {
   const int32_t* gather_rows;
 };
 
+// Whether FP8 tiles take the tensor-memory operand path (see Cfg::TA): the
+// decode tiles (32 rows) on single CTAs, and pair tiles whose accumulators
+// (one buffer: gate and up of 128 rows, or the projection of up to 256)
+// leave half of the 512 TMEM columns free.
+__host__ __device__ constexpr bool ta_config(int mode, int bn, bool fp8, bool pair) {
+  return fp8 && (pair ? (mode == kGateUp ? bn <= 128 : bn <= 256) : bn == 32);
+}
+
 template <int MODE, int BN, bool FP8, bool PAIR>
 struct Cfg {
   // PAIR: a CTA pair (cluster of 2) runs one unit with cta_group::2 MMAs:
@@ -105,12 +113,14 @@ struct Cfg {
   // the unit's B rows, so a CTA moves half the B bytes per flop
   static constexpr int CH = PAIR ? 2 * kBM : kBM;               // output channels per unit
   static constexpr int NA = MODE == kGateUp ? 2 : 1;           // weight operands per stage
-  // FP8 decode tiles: the converters write the f16 weight tile into tensor
-  // memory (tcgen05.st) and the MMA reads A from there, so the f16 operand
-  // never passes through shared memory.  Their stages span 128 elements of
-  // K: 128-byte E4M3 rows (64-byte rows cost as many copy requests per row
-  // as 128-byte bf16 rows, for half the bytes), B in two 64-element halves.
-  static constexpr bool TA = FP8 && BN == 32 && !PAIR;
+  // FP8 tensor-memory operand path: the converters write the f16 weight
+  // tile into tensor memory (tcgen05.st) and the MMA reads A from there, so
+  // the f16 operand never passes through shared memory (whose bandwidth the
+  // E4M3 tile, the f16 tile and the MMA's reads otherwise share).  Stages
+  // span 128 elements of K: 128-byte E4M3 rows (64-byte rows cost as many
+  // copy requests per row as 128-byte bf16 rows, for half the bytes), B in
+  // two 64-element halves.
+  static constexpr bool TA = ta_config(MODE, BN, FP8, PAIR);
   static constexpr int KB = TA ? 2 * kBK : kBK;                // K elements per stage
   static constexpr int NSUB = KB / kBK;                        // 64-element B sub-tiles per stage
   static constexpr int A_BYTES = kBM * kBK * 2;                // 16 KB bf16 tile (MMA operand)
@@ -128,7 +138,16 @@ struct Cfg {
   static constexpr int W_BYTES_ = FP8 ? STG_BYTES : A_BYTES;
   static constexpr int SLOT_ = NA * W_BYTES_ + B_BYTES;
   static constexpr int AVAIL_ = kSmemLimit - 1024 - (8 * 40 + 16 + 4 * 2 * (kMaxGroups + 8));
-  static constexpr int OSTAGES = !FP8 ? 0 : TA ? 4 / NA
+  // TMEM: one accumulator buffer = NA accumulators of max(BN,128) columns;
+  // two buffers when they fit beside the operand slots of the TA path
+  static constexpr int UP_OFF = BN > 128 ? BN : 128;
+  static constexpr int ACC_COLS = NA * UP_OFF;
+  static constexpr bool TA_DECODE = TA && BN == 32;
+  static constexpr int NBUF = TA && !TA_DECODE ? (2 * ACC_COLS + 2 * 64 * NA <= 512 ? 2 : 1)
+                                               : (2 * ACC_COLS <= 512 ? 2 : 1);
+  // TA operand slots of 64 columns (128 f16 of K per lane) per weight matrix
+  static constexpr int TA_SLOTS = TA_DECODE ? 4 : (512 - NBUF * ACC_COLS) / 64;
+  static constexpr int OSTAGES = !FP8 ? 0 : TA ? (TA_SLOTS / NA > 4 ? 4 : TA_SLOTS / NA)
                                  : (AVAIL_ - 6 * SLOT_) / (NA * A_BYTES) >= 4 ? 4
                                  : (AVAIL_ - 6 * SLOT_) / (NA * A_BYTES) >= 3 ? 3 : 2;
   static constexpr int RING_OFF = OSTAGES * OPND_BYTES;
@@ -136,10 +155,6 @@ struct Cfg {
   static constexpr int B_OFF = NA * W_BYTES;
   static constexpr int STAGE_BYTES = B_OFF + B_BYTES;           // multiple of 1024
   static constexpr int THREADS = kThreads + (FP8 ? kConvThreads : 0);
-  // TMEM: one accumulator buffer = NA accumulators of max(BN,128) columns
-  static constexpr int UP_OFF = BN > 128 ? BN : 128;
-  static constexpr int ACC_COLS = NA * UP_OFF;
-  static constexpr int NBUF = 2 * ACC_COLS <= 512 ? 2 : 1;
   static constexpr int TAIL_BYTES = 8 * 40 + 16 + 4 * 2 * (kMaxGroups + 8);
   static constexpr int STAGES_FIT = (kSmemLimit - 1024 - TAIL_BYTES - RING_OFF) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 10 ? 10 : STAGES_FIT;
@@ -157,13 +172,15 @@ struct Cfg {
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
   static_assert(BN % 16 == 0 && BN <= 256 && ACC_COLS <= 512, "tile rows");
   static_assert(!PAIR || BN >= 64, "pair tiles split B rows in halves");
-  static_assert(!TA || (UP_OFF == 128 && ACC_COLS * NBUF <= 512 && OSTAGES * NA <= 4),
-                "TMEM operand slots sit between accumulators");
-  // TMEM column of operand slot o, weight matrix a (TA): the 32-column
-  // accumulators of a decode tile sit at multiples of 128; columns 64..127
-  // after each hold one 64-column A tile (128 f16 of K per lane)
+  static_assert(!TA || (OSTAGES >= 2 && (TA_DECODE ? UP_OFF == 128 && ACC_COLS * NBUF <= 512 && OSTAGES * NA <= 4
+                                                  : NBUF * ACC_COLS + OSTAGES * NA * 64 <= 512)),
+                "TMEM operand slots");
+  // TMEM column of operand slot o, weight matrix a (TA).  Decode tiles: the
+  // 32-column accumulators sit at multiples of 128 and columns 64..127
+  // after each hold an A tile; otherwise the A tiles follow the
+  // accumulator buffers.
   static __device__ __forceinline__ uint32_t ta_col(int o, int a) {
-    return (uint32_t)(64 + 128 * (o * NA + a));
+    return TA_DECODE ? (uint32_t)(64 + 128 * (o * NA + a)) : (uint32_t)(NBUF * ACC_COLS + 64 * (o * NA + a));
   }
 };
 
@@ -503,8 +520,13 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
               const uint64_t db = ptx::sdesc_k_sw128(sa + C::B_OFF + (kk >> 2) * C::BSUB_BYTES) + 2 * (kk & 3);
               if (C::TA) {
                 const uint32_t at = tmem_base + 8u * kk;  // 16 f16 of K = 8 columns
-                ptx::mma_f16_ta(d0, at + C::ta_col(ostage, 0), db, idesc, acc);
-                if (MODE == kGateUp) ptx::mma_f16_ta(d1, at + C::ta_col(ostage, 1), db, idesc, acc);
+                if (PAIR) {
+                  ptx::mma_f16_ta_pair(d0, at + C::ta_col(ostage, 0), db, idesc, acc);
+                  if (MODE == kGateUp) ptx::mma_f16_ta_pair(d1, at + C::ta_col(ostage, 1), db, idesc, acc);
+                } else {
+                  ptx::mma_f16_ta(d0, at + C::ta_col(ostage, 0), db, idesc, acc);
+                  if (MODE == kGateUp) ptx::mma_f16_ta(d1, at + C::ta_col(ostage, 1), db, idesc, acc);
+                }
               } else if (PAIR) {
                 ptx::mma_f16_pair(d0, da0 + 2 * kk, db, idesc, acc);
                 if (MODE == kGateUp) ptx::mma_f16_pair(d1, da1 + 2 * kk, db, idesc, acc);
@@ -904,7 +926,9 @@ TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype) {
   const double mean = R / E;
   const double est_max = mean + 3.0 * __builtin_sqrt(mean) + 1.0;
   const int bn = est_max <= 32.0 ? 32 : 128;
-  const int bn_gu = (bn == 128 && mean >= 128.0) ? 256 : bn;
+  // FP8 weights keep 128-row gate/up tiles: on CTA pairs their accumulators
+  // leave room in TMEM for the f16 weight operand (the TA path)
+  const int bn_gu = (bn == 128 && mean >= 128.0 && w_dtype != MOE_FP8_E4M3) ? 256 : bn;
   const int bn_dn = (bn == 128 && mean >= 128.0) ? 256 : bn;
   pl.bn_gateup = bn_ok(env_int("MOE_BN_GATEUP")) ? env_int("MOE_BN_GATEUP") : bn_gu;
   pl.bn_down = bn_ok(env_int("MOE_BN_DOWN")) ? env_int("MOE_BN_DOWN") : bn_dn;
@@ -943,8 +967,8 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   // E4M3 staging for the tensor-memory operand path (decode tiles): boxes
   // 128 bytes wide with the 128-byte swizzle its converters read
   // conflict-free
-  const bool ta_gu = fp8 && plan.bn_gateup == 32 && !plan.pair_gateup;
-  const bool ta_dn = fp8 && plan.bn_down == 32 && !plan.pair_down;
+  const bool ta_gu = ta_config(kGateUp, plan.bn_gateup, fp8, plan.pair_gateup != 0);
+  const bool ta_dn = ta_config(kDown, plan.bn_down, fp8, plan.pair_down != 0);
   const int wsw_gu = !fp8 || ta_gu ? 128 : 0, wsw_dn = !fp8 || ta_dn ? 128 : 0;
   const int wk_gu = ta_gu ? 2 * kBK : kBK, wk_dn = ta_dn ? 2 * kBK : kBK;
   CUtensorMap wg, wu, xb, wd, hb;
