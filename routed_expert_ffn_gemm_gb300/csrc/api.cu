@@ -39,7 +39,9 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
   size_t idx, w, logits, counts, offsets, perm_token, inv_row, chunk, x_perm, h, y;
-  size_t sh_offsets, sh_h, sh_y, gu_part, sh_gu_part, total;
+  size_t sh_offsets, sh_h, sh_y, gu_part, sh_gu_part, gu_cnt, sh_gu_cnt, total;
+  size_t cnt_ints;  // gate/up finalize counters (routed, then shared), zeroed by the permutation
+  size_t cnt_routed;
   TcPlan plan, sh_plan;
   int router_splits;  // 0: CUDA-core router; else tensor-core logits with this many K splits
   bool gather;        // gate/up gathers token rows (decode tiling) instead of x_perm
@@ -89,8 +91,22 @@ Layout layout(const moe_problem& p, Path path, int num_sms, bool allow_splits) {
   L.gu_part = take(sgu * R * 2 * f * 4);
   const size_t ssh = path == Path::kTensor && p.ffn_shared && L.sh_plan.splits_gateup > 1 ? L.sh_plan.splits_gateup : 0;
   L.sh_gu_part = take(ssh * T * 2 * (size_t)p.ffn_shared * 4);
+  // arrival counters of the fused gate/up finalize (one region, zeroed by
+  // the permutation of each call)
+  // (decode tiles only: the finalizing warp walks the tile's rows itself)
+  const size_t cr = sgu && L.plan.bn_gateup == 32 ? gu_counters_size(p.T * p.k, p.E, p.ffn, L.plan) : 0;
+  const size_t cs = ssh && L.sh_plan.bn_gateup == 32 ? gu_counters_size(p.T, 1, p.ffn_shared, L.sh_plan) : 0;
+  L.gu_cnt = take((cr + cs) * 4);
+  L.sh_gu_cnt = L.gu_cnt + cr * 4;
+  L.cnt_ints = cr + cs;
+  L.cnt_routed = cr;
   L.total = off;
   return L;
+}
+
+bool fuse_topk_in_permute(int T, int k, int E, int router_splits) {
+  return router_splits == 0 && T <= 16 && router_topk_separate(T, E, false, true) &&
+         (long long)T * k <= permute_small_max();
 }
 
 template <typename T>
@@ -119,7 +135,7 @@ moe_status run_grouped(Path path, int R, int d, int ffn, int G, int w_dtype, con
                        const float* sg, const float* su, const float* sd, void* h, void* y,
                        const TcPlan& plan, int* status, cudaStream_t s, cudaEvent_t mid,
                        const int32_t* gather_rows = nullptr, const void* x_src = nullptr,
-                       int T_src = 0, float* gu_partials = nullptr) {
+                       int T_src = 0, float* gu_partials = nullptr, int* gu_cnt = nullptr) {
   if (path == Path::kSimt) {
     SimtGroupedArgs a{R, d, ffn, G, static_cast<const float*>(x_rows), offsets,
                       static_cast<const float*>(wg), static_cast<const float*>(wu),
@@ -128,7 +144,7 @@ moe_status run_grouped(Path path, int R, int d, int ffn, int G, int w_dtype, con
     return simt_grouped_launch(a, s, mid);
   }
   TcGroupedArgs a{R, d, ffn, G, w_dtype, x_rows, offsets, wg, wu, wd, sg, su, sd, h, y, status,
-                  wait_limit_ns(), gather_rows, x_src, T_src, gu_partials};
+                  wait_limit_ns(), gather_rows, x_src, T_src, gu_partials, gu_cnt};
   return tc_grouped_launch(a, plan, s, mid);
 }
 
@@ -301,9 +317,13 @@ moe_status layer_forward_impl(const moe_problem* p, const void* x, const void* w
   // the logits region is the CUDA-core split path's buffer, or the tensor
   // core's partial-sum scratch (the logits themselves are not an output here)
   float* lg = at<float>(workspace, L.logits);
+  // tiny batches (a token per warp of the one-block permutation): the
+  // permutation kernel selects the top-k from the global logits itself
+  // (one launch fewer on the latency-bound path)
+  const bool fuse_topk = fuse_topk_in_permute(p->T, p->k, p->E, L.router_splits);
   RouterArgs ra{p->T, p->d, p->E, p->k, p->act_dtype, x, w_router, router_bias, nullptr,
                 L.router_splits > 0 ? nullptr : lg, idx, w, lg, L.router_splits, ctx.num_sms,
-                ctx.status};
+                ctx.status, fuse_topk ? 1 : 0};
   MOE_TRY(router_topk_launch(ra, s));
   MOE_TRY(mark(1));
   // 2. permutation: counts, offsets, row maps, x -> x_perm
@@ -314,7 +334,9 @@ moe_status layer_forward_impl(const moe_problem* p, const void* x, const void* w
   const bool gather = L.gather;
   PermuteArgs pa{p->T, p->k, p->E, p->d, (int)act_bytes(p->act_dtype), idx, gather ? nullptr : x,
                  counts, offsets, perm_token, inv_row, gather ? nullptr : x_perm,
-                 at<int32_t>(workspace, L.chunk), ctx.status, fp8 && !gather ? 1 : 0};
+                 at<int32_t>(workspace, L.chunk), ctx.status, fp8 && !gather ? 1 : 0,
+                 fuse_topk ? lg : nullptr, fuse_topk ? idx : nullptr, fuse_topk ? w : nullptr,
+                 L.cnt_ints ? at<int32_t>(workspace, L.gu_cnt) : nullptr, L.cnt_ints};
   MOE_TRY(permute_launch(pa, s));
   MOE_TRY(mark(2));
   // 3. grouped SwiGLU experts (gate/up + SiLU*mul, then down)
@@ -326,19 +348,24 @@ moe_status layer_forward_impl(const moe_problem* p, const void* x, const void* w
   MOE_TRY(run_grouped(path, R, p->d, p->ffn, p->E, p->w_dtype, x_perm, offsets, w_gate, w_up,
                       w_down, s_gate, s_up, s_down, h, y, L.plan, ctx.status, s,
                       timer ? timer->ev[3] : nullptr, gather ? perm_token : nullptr, x_src, p->T,
-                      at<float>(workspace, L.gu_part)));
+                      at<float>(workspace, L.gu_part), L.cnt_routed ? at<int>(workspace, L.gu_cnt) : nullptr));
   MOE_TRY(mark(4));
   // 4. shared expert: every token, weight 1 (one group holding all T rows)
   void* sh_y = nullptr;
   if (has_shared) {
-    int32_t* sh_off = at<int32_t>(workspace, L.sh_offsets);
-    MOE_TRY_CUDA(launch_k(set_pair_kernel, dim3(1), dim3(1), 0, s, sh_off, 0, p->T));
-    MOE_TRY_CUDA(cudaGetLastError());
+    // tensor path: a dense single group (no offsets array); CUDA cores: {0, T}
+    int32_t* sh_off = nullptr;
+    if (path != Path::kTensor) {
+      sh_off = at<int32_t>(workspace, L.sh_offsets);
+      MOE_TRY_CUDA(launch_k(set_pair_kernel, dim3(1), dim3(1), 0, s, sh_off, 0, p->T));
+      MOE_TRY_CUDA(cudaGetLastError());
+    }
     sh_y = at<uint8_t>(workspace, L.sh_y);
     MOE_TRY(run_grouped(path, p->T, p->d, p->ffn_shared, 1, p->act_dtype, x, sh_off,
                         w_shared_gate, w_shared_up, w_shared_down, nullptr, nullptr, nullptr,
                         at<uint8_t>(workspace, L.sh_h), sh_y, L.sh_plan, ctx.status, s, nullptr,
-                        nullptr, nullptr, 0, at<float>(workspace, L.sh_gu_part)));
+                        nullptr, nullptr, 0, at<float>(workspace, L.sh_gu_part),
+                        L.cnt_ints > L.cnt_routed ? at<int>(workspace, L.sh_gu_cnt) : nullptr));
   }
   MOE_TRY(mark(5));
   // 5. combine: inverse map, routing weights, sum (+ shared expert)
@@ -442,14 +469,18 @@ moe_status moe_layer_launch_count(const moe_problem* p, int32_t* launches) {
   MOE_TRY(device_ctx(&ctx));
   const int rs = router_tc_splits(p->T, p->d, p->E, p->act_dtype, ctx.num_sms, (size_t)-1);
   int n = rs > 0 ? 2 : router_launch_count(p->T, p->E, false, true);
+  // the tiny-batch permutation selects the top-k in place of the separate pass
+  if (fuse_topk_in_permute(p->T, p->k, p->E, rs)) n -= 1;
   const Layout L0 = layout(*p, path, ctx.num_sms, true);
   n += permute_launch_count(p->T, p->k, !L0.gather);
   if (L0.gather && p->w_dtype == MOE_FP8_E4M3) n += 1;  // x -> f16
   const Layout L = layout(*p, path, ctx.num_sms, true);
   n += 2;                        // gate/up, down
-  if (path == Path::kTensor && L.plan.splits_gateup > 1) n += 1;       // split-K finalize
-  if (path == Path::kTensor && p->ffn_shared > 0 && L.sh_plan.splits_gateup > 1) n += 1;
-  if (p->ffn_shared > 0) n += 3;  // offsets, gate/up, down
+  // split-K gate/up: a finalize pass unless the GEMM finalizes itself
+  // (decode tiles)
+  if (path == Path::kTensor && L.plan.splits_gateup > 1 && L.plan.bn_gateup != 32) n += 1;
+  if (path == Path::kTensor && p->ffn_shared > 0 && L.sh_plan.splits_gateup > 1 && L.sh_plan.bn_gateup != 32) n += 1;
+  if (p->ffn_shared > 0) n += path == Path::kTensor ? 2 : 3;  // (offsets), gate/up, down
   n += 1;                        // combine
   *launches = n;
   return MOE_OK;

@@ -151,6 +151,9 @@ struct RouterArgs {
   int tc_splits;
   int num_sms;
   int* status;
+  // 1: when the top-k would be a separate pass over global logits, skip it
+  // (the caller's permutation selects the top-k from logits_out itself)
+  int defer_topk;
 };
 // Tensor-core logits apply to this problem (and how many K splits), given a
 // scratch of `scratch_floats` fp32 values; 0 = use the CUDA-core kernels.
@@ -158,6 +161,9 @@ int router_tc_splits(int T, int d, int E, int act_dtype, int num_sms, size_t scr
 moe_status router_topk_launch(const RouterArgs& a, cudaStream_t s);
 moe_status router_topk_check(int d, int E, int act_dtype);
 int router_launch_count(int T, int E, bool logits_in, bool logits_out);
+// The CUDA-core router writes global logits and selects the top-k in a
+// separate pass (the pass `defer_topk` skips).
+bool router_topk_separate(int T, int E, bool logits_in, bool logits_out);
 
 struct PermuteArgs {
   int T, k, E, d, act_bytes;
@@ -171,7 +177,17 @@ struct PermuteArgs {
   int32_t* chunk_scratch;  // [n_chunks * E] when the chunked path is used
   int* status;
   int to_f16;              // 1: x is bf16 and x_perm receives it rounded to f16
+  // nullable: router logits [T, E]; the small path then selects the top-k
+  // itself into idx_out / w_out (and reads idx from there)
+  const float* topk_logits;
+  int32_t* idx_out;
+  float* w_out;
+  // nullable: zero_n int32 the first permutation kernel sets to zero
+  int32_t* zero;
+  size_t zero_n;
 };
+// Largest T*k the single-block path (which can also select the top-k) takes.
+int permute_small_max();
 size_t permute_scratch_bytes(int T, int k, int E);
 int permute_launch_count(int T, int k, bool move_rows);
 moe_status permute_launch(const PermuteArgs& a, cudaStream_t s);
@@ -236,7 +252,12 @@ struct TcGroupedArgs {
   const void* x_src;
   int T_src;
   float* gu_partials;  // [splits_gateup, R, 2*ffn] fp32 when splits_gateup > 1
+  // nullable with gu_partials: zeroed arrival counters (gu_counters_size
+  // ints); the GEMM then finalizes h itself instead of a separate pass
+  int* gu_cnt;
 };
+// Arrival counters the fused gate/up finalize needs for R rows in G groups.
+size_t gu_counters_size(int R, int G, int ffn, const TcPlan& plan);
 TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype);
 moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStream_t s,
                              cudaEvent_t mid);

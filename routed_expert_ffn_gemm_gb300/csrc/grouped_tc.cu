@@ -71,6 +71,7 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer, MMA, epilogue warps
 constexpr int kConvThreads = 128;      // FP8: 4 converter warps sharing each stage
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxGroups = 1024;
+constexpr int kMaxGuSplits = 8;   // gate/up K splits (choose_splits and the override cap)
 constexpr int kSmemLimit = 232448;  // opt-in maximum dynamic shared memory per block
 
 enum { kGateUp = 0, kDown = 1 };
@@ -95,6 +96,12 @@ struct TcParams {
   // gather_rows[row0 + j] of tmB (the token rows, gathered by TMA gather4;
   // tmB's box is then one row high) instead of row row0 + j
   const int32_t* gather_rows;
+  // gate/up K split with fused finalize (nullable): per (row tile, channel
+  // tile) arrival counters, zero on entry and left zero; the CTA that
+  // completes a tile's last split sums its partials in split order and
+  // writes SiLU*mul to fin_out (bf16, or f16 with FP8 weights)
+  int* tile_cnt;
+  void* fin_out;
 };
 
 // Whether FP8 tiles take the tensor-memory operand path (see Cfg::TA): the
@@ -671,6 +678,47 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
         else
           ptx::mbar_arrive(acce_bar(buf));
       }
+      if (MODE == kGateUp && p.out_f32 && p.tile_cnt != nullptr) {
+        // fused finalize, per (tile, lane quadrant): the two warps of the
+        // quadrant in each of the S splits arrive once their partials are
+        // written; the warp whose arrival completes the 2*S sums the 32
+        // channels' partials in split order (as the separate finalize
+        // would), applies SiLU*mul, and sets the counter back to zero.  No
+        // warp waits for another, so no barrier can hang.
+        __threadfence();
+        __syncwarp();
+        int* cnt = p.tile_cnt + (u / S) * 4 + q;
+        int last = 0;
+        if (lane == 0) last = atomicAdd(cnt, 1) == 2 * S - 1 ? 1 : 0;
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+          __threadfence();
+          const int c = x.mt * C::CH + ch_local;
+          const float* part = static_cast<const float*>(p.out);
+          for (int r = x.row0; r < x.row0 + x.n_valid; ++r) {
+            // all of a row's partials in flight at once, then summed in order
+            float gs[kMaxGuSplits], us[kMaxGuSplits];
+#pragma unroll
+            for (int sp = 0; sp < kMaxGuSplits; ++sp) {
+              const float* row = part + ((size_t)min(sp, S - 1) * p.R + r) * 2 * p.M;
+              gs[sp] = sp < S ? __ldcg(row + c) : 0.f;
+              us[sp] = sp < S ? __ldcg(row + p.M + c) : 0.f;
+            }
+            float g = 0.f, uv = 0.f;
+#pragma unroll
+            for (int sp = 0; sp < kMaxGuSplits; ++sp) {
+              g += gs[sp];
+              uv += us[sp];
+            }
+            const float hv = silu_mul(g, uv);
+            if (FP8)
+              static_cast<__half*>(p.fin_out)[(size_t)r * p.M + c] = __float2half_rn(hv);
+            else
+              store_out(static_cast<__nv_bfloat16*>(p.fin_out) + (size_t)r * p.M + c, hv);
+          }
+          if (lane == 0) *cnt = 0;
+        }
+      }
     }
     if (!ok && lane == 0) set_device_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
   } else if (FP8 && !p.selftest) {
@@ -994,7 +1042,11 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
 
   p.M = a.ffn;
   p.K = a.d;
+  p.dense = a.offsets == nullptr ? 1 : 0;  // one group holding rows [0, R)
   const bool gu_split = plan.splits_gateup > 1 && a.gu_partials != nullptr;
+  const bool gu_fused = gu_split && a.gu_cnt != nullptr;
+  p.tile_cnt = gu_fused ? a.gu_cnt : nullptr;
+  p.fin_out = gu_fused ? a.h : nullptr;
   p.splits = gu_split ? plan.splits_gateup : 1;
   p.out = gu_split ? static_cast<void*>(a.gu_partials) : a.h;
   p.out_f32 = gu_split ? 1 : 0;
@@ -1004,7 +1056,9 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   p.gather_rows = a.gather_rows;
   MOE_TRY(launch_mode<kGateUp>(plan.bn_gateup, fp8, plan.pair_gateup != 0, p, wg, wu, xb, plan.grid, s));
   p.gather_rows = nullptr;
-  if (gu_split) {
+  p.tile_cnt = nullptr;
+  p.fin_out = nullptr;
+  if (gu_split && !gu_fused) {
     const size_t n = (size_t)a.R * a.ffn;
     const int blocks = (int)((n + 255) / 256 < 8192 ? (n + 255) / 256 : 8192);
     if (fp8)
@@ -1027,6 +1081,13 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   p.boxn = box_dn;
   MOE_TRY(launch_mode<kDown>(plan.bn_down, fp8, plan.pair_down != 0, p, wd, wd, hb, plan.grid, s));
   return MOE_OK;
+}
+
+size_t gu_counters_size(int R, int G, int ffn, const TcPlan& plan) {
+  if (plan.splits_gateup <= 1) return 0;
+  const size_t tiles = (size_t)R / plan.bn_gateup + (size_t)G;  // sum of ceil(n_g / BN)
+  const int ch = plan.pair_gateup ? 2 * kBM : kBM;
+  return tiles * (size_t)(ffn / ch) * 4;  // per (tile, channel tile, lane quadrant)
 }
 
 moe_status tc_dense_f32_launch(const void* a, const void* b, float* out, int M, int N, int K,

@@ -21,6 +21,7 @@
 #include <cuda_fp16.h>
 
 #include "common.cuh"
+#include "topk.cuh"
 
 namespace moe {
 namespace {
@@ -100,18 +101,40 @@ __device__ __forceinline__ void warp_walk(const int32_t* __restrict__ idx, int a
 }
 
 // ---------------------------------------------------------------- small path
-// smem: wcnt[kSmallWarps][E], lrank[R], warp_tot[32], base[E]
+// smem: wcnt[kSmallWarps][E], lrank[R], warp_tot[32], base[E], and with
+// top-k selection rows[kSmallWarps][E] floats.
+// With `logits` the block first selects each token's top-k (one warp per
+// token, its logits row staged in shared memory) into idx_out / w_out, and
+// the permutation then reads those indices: one launch instead of two at
+// small batches.
 __global__ void __launch_bounds__(1024) permute_small_kernel(
-    int R, int k, int E, const int32_t* __restrict__ idx, int32_t* __restrict__ counts,
+    int R, int k, int E, const int32_t* idx, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ perm_token,
-    int32_t* __restrict__ inv_row, int* status) {
+    int32_t* __restrict__ inv_row, int* status, const float* __restrict__ logits,
+    int32_t* idx_out, float* __restrict__ w_out, int32_t* __restrict__ zero, size_t zero_n) {
   griddep_begin();
+  for (size_t i = threadIdx.x; i < zero_n; i += blockDim.x) zero[i] = 0;
   extern __shared__ int sm[];
   int* wcnt = sm;                        // [kSmallWarps][E]
   int* lrank = wcnt + kSmallWarps * E;   // [R]
   int* warp_tot = lrank + R;             // [32]
   int* base = warp_tot + 32;             // [E]
   const int warp = threadIdx.x >> 5;
+  if (logits != nullptr) {
+    float* rows = reinterpret_cast<float*>(base + E);  // [kSmallWarps][E]
+    const int lane = threadIdx.x & 31, T = R / k;
+    if (warp < kSmallWarps) {
+      float* row = rows + warp * E;
+      for (int t = warp; t < T; t += kSmallWarps) {
+        for (int e = lane; e < E; e += 32) row[e] = logits[(size_t)t * E + e];
+        __syncwarp();
+        topk_row(row, E, k, idx_out + (size_t)t * k, w_out + (size_t)t * k);
+        __syncwarp();
+      }
+    }
+    __syncthreads();  // the indices written above are read below
+    idx = idx_out;
+  }
   for (int i = threadIdx.x; i < kSmallWarps * E; i += blockDim.x) wcnt[i] = 0;
   __syncthreads();
   const int seg = (R + kSmallWarps - 1) / kSmallWarps;
@@ -179,8 +202,11 @@ __global__ void __launch_bounds__(256) bf16_to_f16_kernel(const uint4* __restric
 // -------------------------------------------------------------- chunked path
 __global__ void __launch_bounds__(256) permute_count_kernel(int R, int E,
                                                             const int32_t* __restrict__ idx,
-                                                            int32_t* __restrict__ chunk_cnt) {
+                                                            int32_t* __restrict__ chunk_cnt,
+                                                            int32_t* __restrict__ zero, size_t zero_n) {
   griddep_begin();
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < zero_n; i += (size_t)gridDim.x * blockDim.x)
+    zero[i] = 0;
   extern __shared__ int cnt[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
@@ -303,7 +329,9 @@ __global__ void __launch_bounds__(256) permute_scatter_kernel(
   }
 }
 
-size_t small_smem(int R, int E) { return sizeof(int) * ((size_t)kSmallWarps * E + R + 32 + E); }
+size_t small_smem(int R, int E, bool topk) {
+  return sizeof(int) * ((size_t)kSmallWarps * E + R + 32 + E) + (topk ? sizeof(float) * kSmallWarps * E : 0);
+}
 
 }  // namespace
 
@@ -322,6 +350,8 @@ size_t permute_scratch_bytes(int T, int k, int E) {
   if (R <= (size_t)kSmallMaxR) return 0;
   return ((R + kChunk - 1) / kChunk) * (size_t)E * sizeof(int32_t);
 }
+
+int permute_small_max() { return kSmallMaxR; }
 
 int permute_launch_count(int T, int k, bool move_rows) {
   const long long R = (long long)T * k;
@@ -348,18 +378,22 @@ moe_status permute_launch(const PermuteArgs& a, cudaStream_t s) {
   }
   if (a.E > 1024) return MOE_ERR_UNSUPPORTED;
   const int vec_per_row = (a.d * a.act_bytes) / 16;
+  const bool topk = a.topk_logits != nullptr;
+  if (topk && (R > kSmallMaxR || a.idx_out == nullptr || a.w_out == nullptr)) return MOE_ERR_INVALID_ARG;
   if (R <= kSmallMaxR) {
-    const size_t smem = small_smem(R, a.E);
+    const size_t smem = small_smem(R, a.E, topk);
     MOE_TRY_CUDA(cudaFuncSetAttribute(permute_small_kernel,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     MOE_TRY_CUDA(launch_k(permute_small_kernel, dim3(1), dim3(1024), smem, s, R, a.k, a.E, a.idx, a.counts, a.offsets,
-                                               a.perm_token, a.inv_row, a.status));
+                          a.perm_token, a.inv_row, a.status, a.topk_logits, a.idx_out, a.w_out, a.zero,
+                          a.zero != nullptr ? a.zero_n : 0));
     MOE_TRY_CUDA(cudaGetLastError());
     return gather_launch(a, R, vec_per_row, s);
   }
   if (a.chunk_scratch == nullptr) return MOE_ERR_WORKSPACE;
   const int n_chunks = (R + kChunk - 1) / kChunk;
-  MOE_TRY_CUDA(launch_k(permute_count_kernel, dim3(n_chunks), dim3(256), sizeof(int) * a.E, s, R, a.E, a.idx, a.chunk_scratch));
+  MOE_TRY_CUDA(launch_k(permute_count_kernel, dim3(n_chunks), dim3(256), sizeof(int) * a.E, s, R, a.E, a.idx,
+                        a.chunk_scratch, a.zero, a.zero != nullptr ? a.zero_n : 0));
   MOE_TRY_CUDA(cudaGetLastError());
   MOE_TRY_CUDA(launch_k(permute_scan_kernel, dim3(1), dim3(1024), 0, s, n_chunks, a.E, a.chunk_scratch, a.counts, a.offsets));
   MOE_TRY_CUDA(cudaGetLastError());

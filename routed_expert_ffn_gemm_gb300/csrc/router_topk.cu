@@ -10,14 +10,11 @@
 // shuffle reduction.  With one expert slice (gridDim.y == 1, "fused") the logits stay
 // in shared memory and the same block selects the top-k; with several slices
 // (few tokens: more blocks stream W_r) the logits go to global memory and
-// topk_kernel follows.
-//
-// Selection: k rounds of a warp arg-max over the E logits (larger logit
-// first, ties to the lower expert index).  Weights: exp(l_j - l_max) / sum
-// over the kept set, which equals p_j / sum_{kept} p with p = softmax over
-// all E (the full-softmax denominator cancels).  Slots are in selection
-// order, i.e. descending weight.
+// topk_kernel follows (or, at small batches inside the layer, the
+// permutation kernel selects the top-k itself).  Selection and weights:
+// topk_row (topk.cuh).
 #include "common.cuh"
+#include "topk.cuh"
 
 namespace moe {
 namespace {
@@ -40,59 +37,6 @@ __device__ __forceinline__ void load16(const __nv_bfloat16* p, float (&v)[8]) {
   }
 }
 template <typename T> struct VecN { static constexpr int N = 16 / sizeof(T); };
-
-// (v1, e1) ranks before (v2, e2): larger logit, ties to the lower index.
-__device__ __forceinline__ bool ranks_before(float v1, int e1, float v2, int e2) {
-  return v1 > v2 || (v1 == v2 && e1 < e2);
-}
-
-// One warp: top-k of one token's logits row (shared or global memory).
-__device__ void topk_row(const float* row, int E, int k, int32_t* idx_out, float* w_out) {
-  const int lane = threadIdx.x & 31;
-  const int per_lane = (E + 31) / 32;  // <= 32
-  uint32_t taken = 0;                  // bit i: expert lane + 32*i already chosen
-  float my_v = 0.f;
-  int my_e = 0;
-  for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int be = E;  // E = no candidate
-    for (int i = 0; i < per_lane; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u)) {
-        const float v = row[e];
-        if (ranks_before(v, e, bv, be)) { bv = v; be = e; }
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (ranks_before(ov, oe, bv, be)) { bv = ov; be = oe; }
-    }
-    if (be >= E) {  // only NaN logits remain: take the lowest unchosen expert
-      int le = E;
-      for (int i = 0; i < per_lane; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && !((taken >> i) & 1u)) { le = e; break; }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) le = min(le, __shfl_xor_sync(0xffffffffu, le, o));
-      be = le;
-      bv = row[be];
-    }
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
-    if (lane == j) { my_v = bv; my_e = be; }
-  }
-  const float vmax = __shfl_sync(0xffffffffu, my_v, 0);
-  const float ex = lane < k ? expf(my_v - vmax) : 0.f;
-  float s = ex;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  if (lane < k) {
-    idx_out[lane] = my_e;
-    w_out[lane] = ex / s;
-  }
-}
 
 template <typename ActT, int EPW, int TT>
 __global__ void __launch_bounds__(kThreads) router_kernel(
@@ -172,13 +116,21 @@ __global__ void __launch_bounds__(kThreads) router_kernel(
     if (t0 + t < T) topk_row(ls + t * E, E, k, idx + (size_t)(t0 + t) * k, w + (size_t)(t0 + t) * k);
 }
 
+// One warp per token; the row is staged in shared memory once (the k
+// selection rounds read it k times).
 __global__ void __launch_bounds__(kThreads) topk_kernel(int T, int E, int k,
                                                         const float* __restrict__ logits,
                                                         int32_t* __restrict__ idx,
                                                         float* __restrict__ w) {
   griddep_begin();
-  const int t = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
-  if (t < T) topk_row(logits + (size_t)t * E, E, k, idx + (size_t)t * k, w + (size_t)t * k);
+  extern __shared__ float rows[];  // [8][E]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (kThreads / 32) + warp;
+  if (t >= T) return;
+  float* row = rows + warp * E;
+  for (int e = lane; e < E; e += 32) row[e] = logits[(size_t)t * E + e];
+  __syncwarp();
+  topk_row(row, E, k, idx + (size_t)t * k, w + (size_t)t * k);
 }
 
 // Top-k after the tensor-core logits: l[t, :] = sum_s part[s][t][:] (s in
@@ -236,8 +188,11 @@ moe_status launch_typed(const RouterArgs& a, float* logits_scratch, cudaStream_t
                                         logits_scratch, a.idx, a.w));
     }
     MOE_TRY_CUDA(cudaGetLastError());
-    if (gy > 1) {
-      MOE_TRY_CUDA(launch_k(topk_kernel, dim3((a.T + 7) / 8), dim3(kThreads), 0, s, a.T, a.E, a.k, logits_scratch, a.idx, a.w));
+    if (gy > 1 && !a.defer_topk) {
+      const size_t tsmem = sizeof(float) * 8 * a.E;
+      MOE_TRY_CUDA(cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tsmem));
+      MOE_TRY_CUDA(launch_k(topk_kernel, dim3((a.T + 7) / 8), dim3(kThreads), tsmem, s, a.T, a.E, a.k, logits_scratch,
+                            a.idx, a.w));
       MOE_TRY_CUDA(cudaGetLastError());
     }
     return MOE_OK;
@@ -262,6 +217,10 @@ moe_status launch_typed(const RouterArgs& a, float* logits_scratch, cudaStream_t
 
 int router_launch_count(int T, int E, bool logits_in, bool logits_out) {
   return use_split(T, E, logits_in, logits_out) && split_needs_topk_pass(E) ? 2 : 1;
+}
+
+bool router_topk_separate(int T, int E, bool logits_in, bool logits_out) {
+  return use_split(T, E, logits_in, logits_out) && split_needs_topk_pass(E);
 }
 
 moe_status router_topk_check(int d, int E, int act_dtype) {

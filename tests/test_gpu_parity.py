@@ -529,3 +529,40 @@ def test_bounded_wait_expires_cleanly_and_context_survives():
     # the context is still usable: a normal layer runs and matches
     shape = inputs.MoEShape("small", T=20, d=128, ffn=256, E=8, k=2)
     _layer_check(shape, 3, BF16_TOL)
+
+
+@pytest.mark.parametrize("shape", [
+    inputs.WORKLOADS["toy_f32"],                                    # CUDA-core path
+    inputs.WORKLOADS["qwen3_30b_a3b"].with_T(1),                    # fused top-k, split-K gate/up
+    inputs.MoEShape("ds_small", T=2, d=1024, ffn=512, E=64, k=8, ffn_shared=512, wfmt="fp8"),
+    inputs.MoEShape("chunked", T=400, d=256, ffn=256, E=32, k=8),   # chunked permutation
+], ids=lambda s: s.name)
+def test_layer_launch_count_matches_the_kernels_launched(shape):
+    # moe_layer_launch_count (the bench's gpu_launches) against the kernel
+    # nodes of one layer call captured into a CUDA graph (driver API)
+    import ctypes
+    cu = ctypes.CDLL("libcuda.so.1")
+    case = inputs.make_case(shape, 0, DEV)
+    p = api.problem_of(shape)
+    ws = api.workspace_for(p)
+    out = api.layer_forward(p, case, workspace=ws)  # warm (function attributes)
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    h = ctypes.c_void_p(stream.cuda_stream)
+    assert cu.cuStreamBeginCapture_v2(h, ctypes.c_int(2)) == 0  # relaxed capture mode
+    try:
+        api.layer_forward(p, case, out=out, workspace=ws, stream=stream)
+    finally:
+        graph = ctypes.c_void_p()
+        assert cu.cuStreamEndCapture(h, ctypes.byref(graph)) == 0
+    n = ctypes.c_size_t(0)
+    assert cu.cuGraphGetNodes(graph, None, ctypes.byref(n)) == 0
+    nodes = (ctypes.c_void_p * n.value)()
+    assert cu.cuGraphGetNodes(graph, nodes, ctypes.byref(n)) == 0
+    kinds = []
+    for nd in nodes:
+        t = ctypes.c_int(-1)
+        assert cu.cuGraphNodeGetType(ctypes.c_void_p(nd), ctypes.byref(t)) == 0
+        kinds.append(t.value)
+    cu.cuGraphDestroy(graph)
+    assert kinds.count(0) == api.moe_layer_launch_count(p), kinds  # 0: kernel node
