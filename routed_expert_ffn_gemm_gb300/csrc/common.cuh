@@ -54,6 +54,11 @@ inline moe_status cuda_status(cudaError_t err) {
 // zero fill out of bounds.
 moe_status make_tmap_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                         int elem_bytes, uint32_t box_rows, uint32_t box_cols, int swizzle_bytes);
+// 3-D view of the same row-major matrix (16-bit elements, cols % 128 == 0)
+// whose box {64, box_rows, 2} copies two consecutive 64-element column
+// blocks at once, as two 128-byte-swizzled tiles one after the other.
+moe_status make_tmap_kpair(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                           int elem_bytes, uint32_t box_rows);
 
 // ---------------------------------------------------------------------------
 // launches: programmatic dependent launch

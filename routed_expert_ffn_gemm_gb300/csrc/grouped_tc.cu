@@ -128,7 +128,11 @@ struct Cfg {
   // copy requests per row as 128-byte bf16 rows, for half the bytes), B in
   // two 64-element halves.
   static constexpr bool TA = ta_config(MODE, BN, FP8, PAIR);
-  static constexpr int KB = TA ? 2 * kBK : kBK;                // K elements per stage
+  // bf16 down GEMM on pairs: 128 elements of K per stage as well, A and B
+  // each in ONE copy (3-D boxes of two 64-element column blocks): half the
+  // copies and half the barrier round trips per byte of a 64-element stage
+  static constexpr bool K2 = MODE == kDown && PAIR && !FP8;
+  static constexpr int KB = TA || K2 ? 2 * kBK : kBK;          // K elements per stage
   static constexpr int NSUB = KB / kBK;                        // 64-element B sub-tiles per stage
   static constexpr int A_BYTES = kBM * kBK * 2;                // 16 KB bf16 tile (MMA operand)
   static constexpr int BSUB_BYTES = (PAIR ? BN / 2 : BN) * kBK * 2;
@@ -142,7 +146,7 @@ struct Cfg {
   // (a commit round trip per slot otherwise serialises decode), while the
   // TMA ring keeps at least 4 slots
   static constexpr int OPND_BYTES = TA ? 0 : NA * A_BYTES;
-  static constexpr int W_BYTES_ = FP8 ? STG_BYTES : A_BYTES;
+  static constexpr int W_BYTES_ = FP8 ? STG_BYTES : NSUB * A_BYTES;
   static constexpr int SLOT_ = NA * W_BYTES_ + B_BYTES;
   static constexpr int AVAIL_ = kSmemLimit - 1024 - (8 * 40 + 16 + 4 * 2 * (kMaxGroups + 8));
   // TMEM: one accumulator buffer = NA accumulators of max(BN,128) columns;
@@ -158,7 +162,10 @@ struct Cfg {
                                  : (AVAIL_ - 6 * SLOT_) / (NA * A_BYTES) >= 4 ? 4
                                  : (AVAIL_ - 6 * SLOT_) / (NA * A_BYTES) >= 3 ? 3 : 2;
   static constexpr int RING_OFF = OSTAGES * OPND_BYTES;
-  static constexpr int W_BYTES = FP8 ? STG_BYTES : A_BYTES;    // weight tile bytes in a TMA slot
+  static constexpr int W_BYTES = FP8 ? STG_BYTES : NSUB * A_BYTES;  // weight tile bytes in a TMA slot
+  // distance between the A matrices where the MMA reads them (TMA slot, or
+  // FP8 operand slot)
+  static constexpr int A_STRIDE = FP8 ? A_BYTES : W_BYTES;
   static constexpr int B_OFF = NA * W_BYTES;
   static constexpr int STAGE_BYTES = B_OFF + B_BYTES;           // multiple of 1024
   static constexpr int THREADS = kThreads + (FP8 ? kConvThreads : 0);
@@ -368,18 +375,18 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // The whole warp walks the units; lane 0 waits for free slots and
-    // issues the weight copies and row boxes, and in gather mode every lane
-    // issues up to two gather4 row copies per slot.
-    if (!p.selftest) {
+    // Lane 0 waits for free slots and issues the weight copies and row
+    // boxes; in gather mode the whole warp walks the units and every lane
+    // issues up to two gather4 row copies per slot (otherwise lanes 1-31
+    // leave at once: no warp-wide step per slot).
+    const bool gather = p.gather_rows != nullptr;
+    if (!p.selftest && (gather || lane == 0)) {
       const uint64_t pol_w = ptx::policy_evict_first();
       const uint64_t pol_x = ptx::policy_evict_last();
-      const bool gather = p.gather_rows != nullptr;
+      const uint32_t wmask = gather ? 0xffffffffu : 1u;
       int stage = 0;
       uint32_t phase = 0;
-      int armed[STAGES];
-#pragma unroll
-      for (int s = 0; s < STAGES; ++s) armed[s] = -1;
+      long long issued = 0;  // slots armed so far (the abort path derives their phases)
       bool ok = true;
       for (int u = u_first; u < total_units && ok; u += u_step) {
         const Unit x = decode_unit(u, offs, prefix, G, MT, S, BN);
@@ -408,7 +415,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
           int got = 1;
           if (lane == 0)
             got = ptx::mbar_wait_bounded(empty_bar(stage), phase ^ 1u, deadline, abort_flag) ? 1 : 0;
-          got = __shfl_sync(0xffffffffu, got, 0);
+          if (gather) got = __shfl_sync(0xffffffffu, got, 0);
           if (!got) {
             ok = false;
             break;
@@ -417,8 +424,14 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
           const uint32_t sa = sbase + C::RING_OFF + stage * C::STAGE_BYTES;
           const uint32_t sb = sa + C::B_OFF;
           if (lane == 0) {
-            armed[stage] = (int)phase;
-            if (PAIR && !FP8) {
+            ++issued;
+            if (C::K2) {
+              // one 3-D copy each for A and the B rows (two column blocks)
+              const uint32_t fb = lead(full_bar(stage));
+              ptx::mbar_arrive_expect_tx_cluster(fb, bytes);
+              ptx::tma_load_3d_pair(sa, &tmA0, fb, arow, kb * 2, pol_w);
+              ptx::tma_load_3d_pair(sb, &tmB, fb, brow0, kb * 2, pol_x);
+            } else if (PAIR && !FP8) {
               // both CTAs' copies complete the even CTA's barrier
               const uint32_t fb = lead(full_bar(stage));
               ptx::mbar_arrive_expect_tx_cluster(fb, bytes);
@@ -439,7 +452,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
                                      kb * C::KB + sub * kBK, brow0 + i * p.boxn, pol_x);
             }
           }
-          __syncwarp();
+          __syncwarp(wmask);
           if (gather) {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -467,9 +480,11 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
           while (ptx::globaltimer_ns() < t_end) {
           }
         } else {
-          for (int s = 0; s < STAGES; ++s) {
-            if (armed[s] < 0) continue;
-            while (!ptx::mbar_try_wait(full_bar(s), (uint32_t)armed[s]) && ptx::globaltimer_ns() < grace) {
+          // the last min(issued, STAGES) slots may still have copies in flight
+          for (long long j = issued > STAGES ? issued - STAGES : 0; j < issued; ++j) {
+            const int s = (int)(j % STAGES);
+            const uint32_t par = (uint32_t)((j / STAGES) & 1);
+            while (!ptx::mbar_try_wait(full_bar(s), par) && ptx::globaltimer_ns() < grace) {
             }
           }
         }
@@ -519,12 +534,14 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
             const uint32_t sa = sbase + C::RING_OFF + stage * C::STAGE_BYTES;
             const uint32_t aa = FP8 ? sbase + ostage * C::OPND_BYTES : sa;
             const uint64_t da0 = ptx::sdesc_k_sw128(aa);
-            const uint64_t da1 = ptx::sdesc_k_sw128(aa + C::A_BYTES);
+            const uint64_t da1 = ptx::sdesc_k_sw128(aa + C::A_STRIDE);
 #pragma unroll
             for (int kk = 0; kk < C::KB / 16; ++kk) {
               const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
               // B: 64-element sub-tile kk / 4, K step kk % 4 inside it
               const uint64_t db = ptx::sdesc_k_sw128(sa + C::B_OFF + (kk >> 2) * C::BSUB_BYTES) + 2 * (kk & 3);
+              // A (TMA or operand slot): sub-tile kk / 4 as well (64 K each)
+              const uint64_t ka = (uint64_t)((kk >> 2) * (C::A_BYTES >> 4)) + 2 * (kk & 3);
               if (C::TA) {
                 const uint32_t at = tmem_base + 8u * kk;  // 16 f16 of K = 8 columns
                 if (PAIR) {
@@ -535,11 +552,11 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
                   if (MODE == kGateUp) ptx::mma_f16_ta(d1, at + C::ta_col(ostage, 1), db, idesc, acc);
                 }
               } else if (PAIR) {
-                ptx::mma_f16_pair(d0, da0 + 2 * kk, db, idesc, acc);
-                if (MODE == kGateUp) ptx::mma_f16_pair(d1, da1 + 2 * kk, db, idesc, acc);
+                ptx::mma_f16_pair(d0, da0 + ka, db, idesc, acc);
+                if (MODE == kGateUp) ptx::mma_f16_pair(d1, da1 + ka, db, idesc, acc);
               } else {
-                ptx::mma_f16(d0, da0 + 2 * kk, db, idesc, acc);
-                if (MODE == kGateUp) ptx::mma_f16(d1, da1 + 2 * kk, db, idesc, acc);
+                ptx::mma_f16(d0, da0 + ka, db, idesc, acc);
+                if (MODE == kGateUp) ptx::mma_f16(d1, da1 + ka, db, idesc, acc);
               }
             }
             issued = true;
@@ -1029,8 +1046,16 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
     MOE_TRY(make_tmap_2d(&xb, a.x_src, a.T_src, a.d, 2, 1, kBK, 128));
   else
     MOE_TRY(make_tmap_2d(&xb, a.x_perm, a.R, a.d, 2, box_gu, kBK, 128));
-  MOE_TRY(make_tmap_2d(&wd, a.w_down, (uint64_t)a.G * a.d, a.ffn, wb, kBM, wk_dn, wsw_dn));
-  MOE_TRY(make_tmap_2d(&hb, a.h, a.R, a.ffn, 2, box_dn, kBK, 128));
+  // bf16 down GEMM on pairs: 3-D maps, one copy per operand and stage (its
+  // B rows in one box: all BN/2 rows of the CTA)
+  const bool k2_dn = !fp8 && plan.pair_down;
+  if (k2_dn) {
+    MOE_TRY(make_tmap_kpair(&wd, a.w_down, (uint64_t)a.G * a.d, a.ffn, 2, kBM));
+    MOE_TRY(make_tmap_kpair(&hb, a.h, a.R, a.ffn, 2, plan.bn_down / 2));
+  } else {
+    MOE_TRY(make_tmap_2d(&wd, a.w_down, (uint64_t)a.G * a.d, a.ffn, wb, kBM, wk_dn, wsw_dn));
+    MOE_TRY(make_tmap_2d(&hb, a.h, a.R, a.ffn, 2, box_dn, kBK, 128));
+  }
 
   TcParams p{};
   p.G = a.G;
@@ -1078,7 +1103,7 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   p.out_f32 = plan.splits_down > 1 ? 1 : 0;
   p.scale0 = a.s_down;
   p.scale1 = nullptr;
-  p.boxn = box_dn;
+  p.boxn = k2_dn ? plan.bn_down / 2 : box_dn;
   MOE_TRY(launch_mode<kDown>(plan.bn_down, fp8, plan.pair_down != 0, p, wd, wd, hb, plan.grid, s));
   return MOE_OK;
 }

@@ -152,6 +152,27 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// 3-D box {64 elements, rows, 2}: two consecutive 64-element column blocks
+// of `rows` rows in one copy (coordinates: 0, row, first block), landing as
+// two 128-byte-swizzled tiles one after the other.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t c_row,
+                                            int32_t c_kb, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(0), "r"(c_row), "r"(c_kb), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
+                                                 int32_t c_row, int32_t c_kb, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(0), "r"(c_row), "r"(c_kb), "l"(policy)
+      : "memory");
+}
+
 // Gather of four rows (any row indices) of one 64-element column block: the
 // tensor map's box is one row high; the rows land consecutively (4 x box)
 // at `dst` with the map's swizzle, completing `bar`'s transaction count.

@@ -65,6 +65,37 @@ moe_status device_ctx(DeviceCtx* out) {
   return MOE_OK;
 }
 
+moe_status make_tmap_kpair(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                           int elem_bytes, uint32_t box_rows) {
+  if (elem_bytes != 2 || cols % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  if (g_encode == nullptr) {
+    record_cuda_error_text("cuTensorMapEncodeTiled is unavailable");
+    return MOE_ERR_CUDA;
+  }
+  if ((reinterpret_cast<uintptr_t>(base) & 15u) != 0) return MOE_ERR_INVALID_ARG;
+  // dims (innermost first): 64 elements of a column block, rows, column blocks
+  cuuint64_t dims[3] = {64, rows, cols / 64};
+  cuuint64_t strides[2] = {cols * (cuuint64_t)elem_bytes, 64 * (cuuint64_t)elem_bytes};
+  cuuint32_t box[3] = {64, box_rows, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    record_cuda_error_text("cuTensorMapEncodeTiled (3-d) failed");
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
 moe_status make_tmap_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                         int elem_bytes, uint32_t box_rows, uint32_t box_cols, int swizzle_bytes) {
   std::call_once(g_encode_once, [] {
