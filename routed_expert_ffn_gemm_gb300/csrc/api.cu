@@ -75,10 +75,11 @@ Layout layout(const moe_problem& p, Path path, int num_sms, bool allow_splits) {
   L.perm_token = take(R * 4);
   L.inv_row = take(R * 4);
   L.chunk = take(permute_scratch_bytes(p.T, p.k, p.E));
-  // The permuted rows, except in the decode tiling of the tensor path
-  // (32-row tiles): there the gate/up GEMM gathers token rows itself and this
-  // region holds only the f16 copy of x for FP8 experts.
-  const bool gather = path == Path::kTensor && L.plan.bn_gateup == 32;
+  // The permuted rows, except on the tensor path: there the gate/up GEMM
+  // gathers the token rows itself (TMA gather4 for 32-row tiles, cp.async
+  // for larger ones) and this region holds only the f16 copy of x for FP8
+  // experts.
+  const bool gather = path == Path::kTensor;
   L.gather = gather;
   L.x_perm = take(gather ? (p.w_dtype == MOE_FP8_E4M3 ? T * d * 2 : 0) : R * d * ab);
   L.h = take(R * f * ab);
@@ -327,10 +328,9 @@ moe_status layer_forward_impl(const moe_problem* p, const void* x, const void* w
   MOE_TRY(router_topk_launch(ra, s));
   MOE_TRY(mark(1));
   // 2. permutation: counts, offsets, row maps, x -> x_perm
-  // In the decode tiling the permutation writes only the maps: the gate/up
+  // On the tensor path the permutation writes only the maps: the gate/up
   // GEMM gathers token rows by perm_token itself (FP8 experts gather from an
-  // f16 copy of x).  Otherwise the row move fills x_perm (rounded to f16 for
-  // FP8 experts, which run on f16 operands).
+  // f16 copy of x).  On the CUDA-core path the row move fills x_perm.
   const bool gather = L.gather;
   PermuteArgs pa{p->T, p->k, p->E, p->d, (int)act_bytes(p->act_dtype), idx, gather ? nullptr : x,
                  counts, offsets, perm_token, inv_row, gather ? nullptr : x_perm,

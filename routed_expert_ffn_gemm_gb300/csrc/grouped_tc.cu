@@ -102,6 +102,13 @@ struct TcParams {
   // writes SiLU*mul to fin_out (bf16, or f16 with FP8 weights)
   int* tile_cnt;
   void* fin_out;
+  // gate/up at prefill tiles (BN >= 128), with gather_rows: the producer
+  // warp gathers the token rows from x_src itself with 16-byte cp.async
+  // (row by row, 128-byte swizzle applied by hand) instead of reading a
+  // materialised x_perm; the weights still come by TMA
+  int lsu_gather;
+  const void* x_src;
+  int d_src;  // row length of x_src (elements)
 };
 
 // Whether FP8 tiles take the tensor-memory operand path (see Cfg::TA): the
@@ -174,8 +181,8 @@ struct Cfg {
   static constexpr int STAGES = STAGES_FIT > 10 ? 10 : STAGES_FIT;
   static constexpr int BAR_OFF = RING_OFF + STAGES * STAGE_BYTES;
   // barriers: full[S], empty[S], opnd_full[4], opnd_empty[4], acc_full[2],
-  // acc_empty[2], drain
-  static constexpr int NBARS = 2 * STAGES + 13;
+  // acc_empty[2], drain, rows_full[S] (gathered B rows of a pair CTA)
+  static constexpr int NBARS = 3 * STAGES + 13;
   static constexpr int SLOT_OFF = BAR_OFF + 8 * NBARS;         // TMEM base address
   static constexpr int ABORT_OFF = SLOT_OFF + 8;
   static constexpr int OFFS_OFF = ABORT_OFF + 8;               // int offs[G+1]
@@ -273,6 +280,11 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
   auto accf_bar = [&](int b) { return bars + 8u * (2 * STAGES + 8 + b); };
   auto acce_bar = [&](int b) { return bars + 8u * (2 * STAGES + 10 + b); };
   const uint32_t drain_bar = bars + 8u * (2 * STAGES + 12);
+  auto bfull_bar = [&](int s) { return bars + 8u * (2 * STAGES + 13 + s); };
+  const bool lsu = MODE == kGateUp && p.lsu_gather != 0;
+  // bf16 pairs gathering rows: each CTA's row copies complete its own
+  // rows_full barrier; the odd CTA's MMA warp relays it to the even CTA
+  const bool relay = PAIR && !FP8 && lsu;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::SLOT_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::ABORT_OFF);
   int* offs = reinterpret_cast<int*>(smem + C::OFFS_OFF);
@@ -293,8 +305,11 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
       // bf16 pairs: both producers arrive on the even CTA's full barrier
       // (their copies complete it); FP8: each CTA's converters wait on
       // their own CTA's copies
-      ptx::mbar_init(full_bar(s), PAIR && !FP8 ? 2 : 1);
+      // (+ 32 per-lane arrivals of the gathered rows, or the relayed
+      // arrival of the odd CTA's rows)
+      ptx::mbar_init(full_bar(s), PAIR && !FP8 ? 2 + (relay ? 1 : 0) : 1 + (lsu ? 32 : 0));
       ptx::mbar_init(empty_bar(s), 1);
+      ptx::mbar_init(bfull_bar(s), 32);
     }
     for (int c = 0; c < 4; ++c) {
       ptx::mbar_init(ofull_bar(c), kRemote * kConvThreads / 32);  // one arrival per converter warp
@@ -379,11 +394,12 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
     // boxes; in gather mode the whole warp walks the units and every lane
     // issues up to two gather4 row copies per slot (otherwise lanes 1-31
     // leave at once: no warp-wide step per slot).
-    const bool gather = p.gather_rows != nullptr;
-    if (!p.selftest && (gather || lane == 0)) {
+    const bool gather = p.gather_rows != nullptr && !lsu;
+    if (!p.selftest && (gather || lsu || lane == 0)) {
       const uint64_t pol_w = ptx::policy_evict_first();
       const uint64_t pol_x = ptx::policy_evict_last();
-      const uint32_t wmask = gather ? 0xffffffffu : 1u;
+      const uint32_t wmask = gather || lsu ? 0xffffffffu : 1u;
+      const __nv_bfloat16* xs = static_cast<const __nv_bfloat16*>(p.x_src);  // 16-bit rows (bf16 or f16)
       int stage = 0;
       uint32_t phase = 0;
       long long issued = 0;  // slots armed so far (the abort path derives their phases)
@@ -407,15 +423,24 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
             const int i = 4 * (lane + 32 * h) + q;
             gr[h][q] = (gather && lane + 32 * h < nops) ? p.gather_rows[x.row0 + (i < x.n_valid ? i : 0)] : 0;
           }
+        // gathered rows (lsu): this lane's rows lane + 32 i of the CTA's
+        // B rows, their token ids (-1: past the group's end, not copied)
+        constexpr int RPL = (PAIR ? BN / 2 : BN) / 32 > 0 ? (PAIR ? BN / 2 : BN) / 32 : 1;
+        int tok[RPL];
+#pragma unroll
+        for (int i = 0; i < RPL; ++i) {
+          const int r = brow0 + lane + 32 * i;
+          tok[i] = (lsu && lane + 32 * i < bhalf && r < x.row0 + x.n_valid) ? p.gather_rows[r] : -1;
+        }
         const uint32_t bbytes =
-            C::NSUB * (gather ? (uint32_t)nops * 4 * kBK * 2 : (uint32_t)nbox * p.boxn * kBK * 2);
+            lsu ? 0u : C::NSUB * (gather ? (uint32_t)nops * 4 * kBK * 2 : (uint32_t)nbox * p.boxn * kBK * 2);
         const uint32_t bytes = C::NA * C::W_BYTES + bbytes;
         const int arow = x.g * p.M + x.mt * C::CH + (int)rank * kBM;
         for (int kb = kb0; kb < kb1; ++kb) {
           int got = 1;
           if (lane == 0)
             got = ptx::mbar_wait_bounded(empty_bar(stage), phase ^ 1u, deadline, abort_flag) ? 1 : 0;
-          if (gather) got = __shfl_sync(0xffffffffu, got, 0);
+          if (gather || lsu) got = __shfl_sync(0xffffffffu, got, 0);
           if (!got) {
             ok = false;
             break;
@@ -437,20 +462,39 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
               ptx::mbar_arrive_expect_tx_cluster(fb, bytes);
               ptx::tma_load_2d_pair(sa, &tmA0, fb, kb * C::KB, arow, pol_w);
               if (MODE == kGateUp) ptx::tma_load_2d_pair(sa + C::W_BYTES, &tmA1, fb, kb * C::KB, arow, pol_w);
-              for (int i = 0; i < nbox; ++i)
-                ptx::tma_load_2d_pair(sb + i * p.boxn * kBK * 2, &tmB, fb, kb * C::KB, brow0 + i * p.boxn, pol_x);
+              if (!lsu)
+                for (int i = 0; i < nbox; ++i)
+                  ptx::tma_load_2d_pair(sb + i * p.boxn * kBK * 2, &tmB, fb, kb * C::KB, brow0 + i * p.boxn, pol_x);
             } else {
               ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
               ptx::tma_load_2d(sa, &tmA0, full_bar(stage), kb * C::KB, arow, pol_w);
               if (MODE == kGateUp)
                 ptx::tma_load_2d(sa + C::W_BYTES, &tmA1, full_bar(stage), kb * C::KB, arow, pol_w);
-              if (!gather)
+              if (!gather && !lsu)
 #pragma unroll
                 for (int sub = 0; sub < C::NSUB; ++sub)
                   for (int i = 0; i < nbox; ++i)
                     ptx::tma_load_2d(sb + sub * C::BSUB_BYTES + i * p.boxn * kBK * 2, &tmB, full_bar(stage),
                                      kb * C::KB + sub * kBK, brow0 + i * p.boxn, pol_x);
             }
+          }
+          if (lsu) {
+            // every lane: its rows' 128-byte K slices (per 64-element
+            // sub-tile), chunk c of row r at chunk c ^ (r % 8); then one
+            // arrival per lane once its copies have landed
+#pragma unroll
+            for (int i = 0; i < RPL; ++i) {
+              if (tok[i] < 0) continue;
+              const int r = lane + 32 * i;
+#pragma unroll
+              for (int sub = 0; sub < C::NSUB; ++sub) {
+                const __nv_bfloat16* src = xs + (size_t)tok[i] * p.d_src + kb * C::KB + sub * kBK;
+                const uint32_t dst = sb + sub * C::BSUB_BYTES + r * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) ptx::cp_async16(dst + ((c ^ (r & 7)) << 4), src + 8 * c);
+              }
+            }
+            ptx::cp_async_arrive_noinc(relay ? bfull_bar(stage) : full_bar(stage));
           }
           __syncwarp(wmask);
           if (gather) {
@@ -470,6 +514,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
           }
         }
       }
+      if (!ok && lsu) asm volatile("cp.async.wait_all;" ::: "memory");  // this lane's row copies
       if (!ok && lane == 0) {
         set_device_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
         // let every issued copy land before shared memory is released
@@ -526,10 +571,14 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
           const uint32_t d1 = d0 + (uint32_t)C::UP_OFF;
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!ptx::mbar_wait_bounded(full_bar(stage), phase, deadline, abort_flag) ||
+                (relay && !ptx::mbar_wait_bounded(bfull_bar(stage), phase, deadline, abort_flag)) ||
                 (FP8 && !ptx::mbar_wait_bounded(ofull_bar(ostage), ophase, deadline, abort_flag))) {
               ok = false;
               break;
             }
+            // rows gathered by cp.async are generic-proxy writes: order them
+            // before the tensor core's reads
+            if (lsu && !FP8) ptx::fence_proxy_async_smem();
             ptx::tc_fence_after();
             const uint32_t sa = sbase + C::RING_OFF + stage * C::STAGE_BYTES;
             const uint32_t aa = FP8 ? sbase + ostage * C::OPND_BYTES : sa;
@@ -586,6 +635,31 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
           }
         }
       }
+    }
+    if (lane == 0 && !leader && relay && !p.selftest) {
+      // odd CTA of a pair gathering rows: once this CTA's rows of a slot
+      // have landed, make them visible to the tensor core and tell the
+      // even CTA (its full barrier counts this arrival)
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int u = u_first; u < total_units && ok; u += u_step) {
+        const Unit x = decode_unit(u, offs, prefix, G, MT, S, BN);
+        const int kb0 = x.ks * kb_per_split, kb1 = min(kblocks, kb0 + kb_per_split);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!ptx::mbar_wait_bounded(bfull_bar(stage), phase, deadline, abort_flag)) {
+            ok = false;
+            break;
+          }
+          ptx::fence_proxy_async_smem();
+          ptx::mbar_arrive_cluster(lead(full_bar(stage)));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) set_device_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
     }
   } else if (warp < kThreads / 32) {
     // ------------------------------------------------------------ epilogue
@@ -766,6 +840,9 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
           break;
         }
         const uint8_t* st = smem + C::RING_OFF + stage * C::STAGE_BYTES;
+        // rows gathered by cp.async (generic proxy) sit in this slot: make
+        // them visible to the tensor core before the operand arrival
+        if (lsu) ptx::fence_proxy_async_smem();
         if constexpr (C::TA) {
           // one weight row per thread: the row is this warp's TMEM lane
           // (quadrant warp % 4); the 128-byte staging rows carry the 128-byte
@@ -1041,7 +1118,10 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   MOE_TRY(make_tmap_2d(&wu, a.w_up, (uint64_t)a.G * a.ffn, a.d, wb, kBM, wk_gu, wsw_gu));
   const int box_gu = boxn_of(plan.bn_gateup, plan.pair_gateup != 0);
   const int box_dn = boxn_of(plan.bn_down, plan.pair_down != 0);
-  if (plan.pair_gateup && a.gather_rows != nullptr) return MOE_ERR_UNSUPPORTED;
+  // gathered token rows: TMA gather4 for decode tiles, cp.async by the
+  // producer warp for prefill tiles (gather4 costs a copy per 4 rows)
+  const bool lsu = a.gather_rows != nullptr && plan.bn_gateup >= 128;
+  if (plan.pair_gateup && a.gather_rows != nullptr && !lsu) return MOE_ERR_UNSUPPORTED;
   if (a.gather_rows != nullptr)  // token rows by index: one-row boxes for gather4
     MOE_TRY(make_tmap_2d(&xb, a.x_src, a.T_src, a.d, 2, 1, kBK, 128));
   else
@@ -1079,8 +1159,12 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   p.scale1 = a.s_up;
   p.boxn = box_gu;
   p.gather_rows = a.gather_rows;
+  p.lsu_gather = lsu ? 1 : 0;
+  p.x_src = a.x_src;
+  p.d_src = a.d;
   MOE_TRY(launch_mode<kGateUp>(plan.bn_gateup, fp8, plan.pair_gateup != 0, p, wg, wu, xb, plan.grid, s));
   p.gather_rows = nullptr;
+  p.lsu_gather = 0;
   p.tile_cnt = nullptr;
   p.fin_out = nullptr;
   if (gu_split && !gu_fused) {

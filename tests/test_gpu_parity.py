@@ -500,6 +500,23 @@ def test_layer_gateup_split_k(splits, bn, d, wfmt, monkeypatch):
     _layer_check(shape, 4, FP8_TOL if wfmt == "fp8" else BF16_TOL)
 
 
+@pytest.mark.parametrize("bn,pair", [(128, 0), (128, 1), (256, 0), (256, 1)])
+@pytest.mark.parametrize("wfmt", ["bf16", "fp8"])
+def test_layer_gathered_rows_every_tile(bn, pair, wfmt, monkeypatch):
+    # the gate/up GEMM gathers its token rows (cp.async by the producer warp
+    # for tiles of >= 128 rows), on single CTAs and on CTA pairs, with groups
+    # spanning several tiles and ragged tails
+    monkeypatch.setenv("MOE_BN_GATEUP", str(bn))
+    monkeypatch.setenv("MOE_BN_DOWN", str(bn))
+    monkeypatch.setenv("MOE_PAIR", str(pair))
+    monkeypatch.setenv("MOE_SPLITS_GATEUP", "1")  # (pairs take unsplit gate/up GEMMs)
+    shape = inputs.MoEShape("gathered", T=300, d=512, ffn=512, E=8, k=2, wfmt=wfmt,
+                            ffn_shared=256 if wfmt == "fp8" else 0)
+    info = api.moe_plan_info(api.problem_of(shape))
+    assert (info["bn_gateup"], info["pair_gateup"]) == (bn, pair)
+    _layer_check(shape, 3, FP8_TOL if wfmt == "fp8" else BF16_TOL)
+
+
 def test_layer_empty_batch():
     shape = inputs.WORKLOADS["qwen3_30b_a3b"].with_T(0)
     case = inputs.make_weights(shape, 0, DEV)
