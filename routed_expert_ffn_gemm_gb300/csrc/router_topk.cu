@@ -20,6 +20,12 @@ namespace moe {
 namespace {
 
 constexpr int kTT = 8;  // tokens per block (large batches)
+// Batches from 256 tokens take the tensor-core logits (E % 128 == 0, bf16),
+// and from 32 when W_r is large (d*E >= 2^20): the W_r tiles stream through
+// TMA into tcgen05 with the K range split over the SMs, where the CUDA-core
+// kernel re-reads W_r per 8-token tile.  Below that the CUDA-core kernels'
+// two short launches measured faster on GB300.
+bool tc_router_size(int T, int d, int E) { return T >= 256 || (T >= 32 && (long long)d * E >= (1LL << 20)); }
 constexpr int kThreads = 256;
 
 __device__ __forceinline__ void load16(const float* p, float (&v)[8]) {
@@ -233,12 +239,12 @@ moe_status router_topk_check(int d, int E, int act_dtype) {
 }
 
 int router_tc_splits(int T, int d, int E, int act_dtype, int num_sms, size_t scratch_floats) {
-  if (act_dtype != MOE_BF16 || E % 128 != 0 || T < 256 || d % 64 != 0) return 0;
+  if (act_dtype != MOE_BF16 || E % 128 != 0 || !tc_router_size(T, d, E) || d % 64 != 0) return 0;
   if ((size_t)T * E > scratch_floats) return 0;
   const int tiles = ((T + 127) / 128) * (E / 128);
   const int kblocks = d / 64;
   int splits = 1;
-  while (tiles * splits < num_sms && splits < 8 && kblocks / (splits + 1) >= 8) ++splits;
+  while (tiles * splits < num_sms && splits < 16 && kblocks / (splits + 1) >= 8) ++splits;
   while (splits > 1 && (size_t)splits * T * E > scratch_floats) --splits;
   return splits;
 }
