@@ -96,7 +96,7 @@ Layout layout(const moe_problem& p, Path path, int num_sms, bool allow_splits) {
   // the permutation of each call)
   // (decode tiles only: the finalizing warp walks the tile's rows itself)
   const size_t cr = sgu && L.plan.bn_gateup == 32 ? gu_counters_size(p.T * p.k, p.E, p.ffn, L.plan) : 0;
-  const size_t cs = ssh && L.sh_plan.bn_gateup == 32 ? gu_counters_size(p.T, 1, p.ffn_shared, L.sh_plan) : 0;
+  const size_t cs = 0;  // (the shared expert's gate/up finalizes in its own pass)
   L.gu_cnt = take((cr + cs) * 4);
   L.sh_gu_cnt = L.gu_cnt + cr * 4;
   L.cnt_ints = cr + cs;
@@ -314,6 +314,22 @@ moe_status layer_forward_impl(const moe_problem* p, const void* x, const void* w
   void* y = at<uint8_t>(workspace, L.y);
 
   MOE_TRY(mark(0));
+  // 4. (first) shared expert: every token, weight 1.  On the tensor path it
+  // needs only x, so it runs on the side stream, concurrently with routing
+  // and permutation (whose small kernels share the SMs with it); the
+  // combine joins it.  Its split-K gate/up finalizes in a separate pass.
+  void* sh_y = nullptr;
+  const bool side = has_shared && path == Path::kTensor;
+  if (side) {
+    sh_y = at<uint8_t>(workspace, L.sh_y);
+    MOE_TRY_CUDA(cudaEventRecord(ctx.fork, s));
+    MOE_TRY_CUDA(cudaStreamWaitEvent(ctx.side, ctx.fork, 0));
+    MOE_TRY(run_grouped(path, p->T, p->d, p->ffn_shared, 1, p->act_dtype, x, nullptr, w_shared_gate,
+                        w_shared_up, w_shared_down, nullptr, nullptr, nullptr, at<uint8_t>(workspace, L.sh_h),
+                        sh_y, L.sh_plan, ctx.status, ctx.side, nullptr, nullptr, nullptr, 0,
+                        at<float>(workspace, L.sh_gu_part), nullptr));
+    MOE_TRY_CUDA(cudaEventRecord(ctx.join, ctx.side));
+  }
   // 1. router: logits, softmax, top-k, renormalised weights
   // the logits region is the CUDA-core split path's buffer, or the tensor
   // core's partial-sum scratch (the logits themselves are not an output here)
@@ -350,22 +366,19 @@ moe_status layer_forward_impl(const moe_problem* p, const void* x, const void* w
                       timer ? timer->ev[3] : nullptr, gather ? perm_token : nullptr, x_src, p->T,
                       at<float>(workspace, L.gu_part), L.cnt_routed ? at<int>(workspace, L.gu_cnt) : nullptr));
   MOE_TRY(mark(4));
-  // 4. shared expert: every token, weight 1 (one group holding all T rows)
-  void* sh_y = nullptr;
-  if (has_shared) {
-    // tensor path: a dense single group (no offsets array); CUDA cores: {0, T}
-    int32_t* sh_off = nullptr;
-    if (path != Path::kTensor) {
-      sh_off = at<int32_t>(workspace, L.sh_offsets);
-      MOE_TRY_CUDA(launch_k(set_pair_kernel, dim3(1), dim3(1), 0, s, sh_off, 0, p->T));
-      MOE_TRY_CUDA(cudaGetLastError());
-    }
+  // 4. shared expert (CUDA-core path: here, one group {0, T}); on the
+  // tensor path, join the side stream
+  if (side) {
+    MOE_TRY_CUDA(cudaStreamWaitEvent(s, ctx.join, 0));
+  } else if (has_shared) {
+    int32_t* sh_off = at<int32_t>(workspace, L.sh_offsets);
+    MOE_TRY_CUDA(launch_k(set_pair_kernel, dim3(1), dim3(1), 0, s, sh_off, 0, p->T));
+    MOE_TRY_CUDA(cudaGetLastError());
     sh_y = at<uint8_t>(workspace, L.sh_y);
     MOE_TRY(run_grouped(path, p->T, p->d, p->ffn_shared, 1, p->act_dtype, x, sh_off,
                         w_shared_gate, w_shared_up, w_shared_down, nullptr, nullptr, nullptr,
                         at<uint8_t>(workspace, L.sh_h), sh_y, L.sh_plan, ctx.status, s, nullptr,
-                        nullptr, nullptr, 0, at<float>(workspace, L.sh_gu_part),
-                        L.cnt_ints > L.cnt_routed ? at<int>(workspace, L.sh_gu_cnt) : nullptr));
+                        nullptr, nullptr, 0, at<float>(workspace, L.sh_gu_part), nullptr));
   }
   MOE_TRY(mark(5));
   // 5. combine: inverse map, routing weights, sum (+ shared expert)
@@ -479,7 +492,7 @@ moe_status moe_layer_launch_count(const moe_problem* p, int32_t* launches) {
   // split-K gate/up: a finalize pass unless the GEMM finalizes itself
   // (decode tiles)
   if (path == Path::kTensor && L.plan.splits_gateup > 1 && L.plan.bn_gateup != 32) n += 1;
-  if (path == Path::kTensor && p->ffn_shared > 0 && L.sh_plan.splits_gateup > 1 && L.sh_plan.bn_gateup != 32) n += 1;
+  if (path == Path::kTensor && p->ffn_shared > 0 && L.sh_plan.splits_gateup > 1) n += 1;
   if (p->ffn_shared > 0) n += path == Path::kTensor ? 2 : 3;  // (offsets), gate/up, down
   n += 1;                        // combine
   *launches = n;

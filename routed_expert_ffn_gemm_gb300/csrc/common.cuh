@@ -21,6 +21,10 @@ struct DeviceCtx {
   int device = -1;
   int num_sms = 0;
   int* status = nullptr;  // device address of this device's status word
+  // side stream + fork/join events (created on first use): the layer runs
+  // the shared expert there, concurrently with routing and permutation
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
 };
 
 // Current device, its SM count and status-word address (cached per device).

@@ -59,6 +59,9 @@ moe_status device_ctx(DeviceCtx* out) {
     MOE_TRY_CUDA(cudaGetSymbolAddress(&p, g_kernel_status));
     c.num_sms = sms;
     c.status = static_cast<int*>(p);
+    MOE_TRY_CUDA(cudaStreamCreateWithFlags(&c.side, cudaStreamNonBlocking));
+    MOE_TRY_CUDA(cudaEventCreateWithFlags(&c.fork, cudaEventDisableTiming));
+    MOE_TRY_CUDA(cudaEventCreateWithFlags(&c.join, cudaEventDisableTiming));
     c.device = dev;
   }
   *out = c;
