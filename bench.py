@@ -19,6 +19,7 @@ ranks is taken.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -49,6 +50,9 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mixtral_8x7b", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--T", type=int, default=None, help="tokens per step (default: the workload's)")
+    ap.add_argument("--E", type=int, default=None,
+                    help="number of routed experts (default: the workload's; fewer experts make a "
+                         "small case of the same expert shapes, e.g. for profiler captures)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--weight-sets", type=int, default=0,
                     help="independent weight sets rotated per step (0: enough to exceed L2)")
@@ -536,6 +540,10 @@ def main():
         shape = shape.with_T(args.T)
     elif args.workload == "mixtral_8x7b":
         shape = shape.with_T(64)
+    if args.E is not None:
+        if not shape.k <= args.E:
+            raise SystemExit("--E must be at least the workload's top-k")
+        shape = dataclasses.replace(shape, E=args.E)
     ws, rank, local = dist_setup(args)
     if args.impl == "reference":
         return run_reference(args, shape, ws, rank)
