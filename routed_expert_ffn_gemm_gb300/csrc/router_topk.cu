@@ -243,8 +243,10 @@ int router_tc_splits(int T, int d, int E, int act_dtype, int num_sms, size_t scr
   if ((size_t)T * E > scratch_floats) return 0;
   const int tiles = ((T + 127) / 128) * (E / 128);
   const int kblocks = d / 64;
+  // as many K splits as keep every unit in one wave of the SMs (a partial
+  // second wave costs a whole unit's time), each split >= 8 k-blocks
   int splits = 1;
-  while (tiles * splits < num_sms && splits < 16 && kblocks / (splits + 1) >= 8) ++splits;
+  while ((splits + 1) * tiles <= num_sms && splits < 16 && kblocks / (splits + 1) >= 8) ++splits;
   while (splits > 1 && (size_t)splits * T * E > scratch_floats) --splits;
   return splits;
 }
