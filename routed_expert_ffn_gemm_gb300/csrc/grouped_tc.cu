@@ -192,7 +192,7 @@ struct Cfg {
   static_assert(SMEM_BYTES <= kSmemLimit, "shared memory budget");
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
   static_assert(BN % 16 == 0 && BN <= 256 && ACC_COLS <= 512, "tile rows");
-  static_assert(!PAIR || BN >= 64, "pair tiles split B rows in halves");
+  static_assert(!PAIR || BN >= 32, "pair tiles split B rows in halves");
   static_assert(!TA || (OSTAGES >= 2 && (TA_DECODE ? UP_OFF == 128 && ACC_COLS * NBUF <= 512 && OSTAGES * NA <= 4
                                                   : NBUF * ACC_COLS + OSTAGES * NA * 64 <= 512)),
                 "TMEM operand slots");
@@ -778,13 +778,13 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
         // warp waits for another, so no barrier can hang.
         __threadfence();
         __syncwarp();
-        int* cnt = p.tile_cnt + (u / S) * 4 + q;
+        int* cnt = p.tile_cnt + (u / S) * (PAIR ? 8 : 4) + (int)rank * 4 + q;
         int last = 0;
         if (lane == 0) last = atomicAdd(cnt, 1) == 2 * S - 1 ? 1 : 0;
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
           __threadfence();
-          const int c = x.mt * C::CH + ch_local;
+          const int c = x.mt * C::CH + (int)rank * kBM + ch_local;
           const float* part = static_cast<const float*>(p.out);
           for (int r = x.row0; r < x.row0 + x.n_valid; ++r) {
             // all of a row's partials in flight at once, then summed in order
@@ -972,6 +972,7 @@ moe_status launch_mode(int bn, bool fp8, bool pair, const TcParams& p, const CUt
   if (pair) {
     if (p.M % (2 * kBM) != 0 || grid < 2) return MOE_ERR_UNSUPPORTED;
     if (fp8) {
+      if (bn == 32) return launch_one<MODE, 32, true, true>(p, a0, a1, b, grid, s);
       if (bn == 128) return launch_one<MODE, 128, true, true>(p, a0, a1, b, grid, s);
       if (bn == 256) return launch_one<MODE, 256, true, true>(p, a0, a1, b, grid, s);
     } else {
@@ -1079,20 +1080,30 @@ TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype) {
     const double a = R / bn_;
     return (int)(touched > a ? touched : a + 0.5);
   };
+  // CTA pairs.  MOE_PAIR=0 keeps single CTAs; MOE_PAIR=2 also runs the
+  // FP8 decode tiles on pairs (supported and tested, but measured no faster
+  // on GB300: each CTA's tensor core still consumes its own f16 weight
+  // tile, whose bytes per stage bound the FP8 decode tiles either way).
+  const char* pe = getenv("MOE_PAIR");
+  const bool pairs_ok = !(pe != nullptr && pe[0] == '0') && num_sms >= 2;
+  const bool fp8 = w_dtype == MOE_FP8_E4M3;
+  const bool dec_pairs = pairs_ok && pe != nullptr && pe[0] == '2';
+  const bool dec_pair_gu = dec_pairs && fp8 && pl.bn_gateup == 32 && ffn % (2 * kBM) == 0;
+  const bool dec_pair_dn = dec_pairs && fp8 && pl.bn_down == 32 && d % (2 * kBM) == 0;
   // K per stage: 128 on the FP8 tensor-memory operand path (decode tiles)
-  const int kw_dn = w_dtype == MOE_FP8_E4M3 && pl.bn_down == 32 ? 2 * kBK : kBK;
-  const int kw_gu = w_dtype == MOE_FP8_E4M3 && pl.bn_gateup == 32 ? 2 * kBK : kBK;
-  pl.splits_down = choose_splits(tiles_of(pl.bn_down) * (d / kBM), (ffn + kw_dn - 1) / kw_dn, num_sms);
-  pl.splits_gateup = choose_splits(tiles_of(pl.bn_gateup) * (ffn / kBM), (d + kw_gu - 1) / kw_gu, num_sms);
+  const int kw_dn = fp8 && pl.bn_down == 32 ? 2 * kBK : kBK;
+  const int kw_gu = fp8 && pl.bn_gateup == 32 ? 2 * kBK : kBK;
+  const int ch_dn = dec_pair_dn ? 2 * kBM : kBM, ch_gu = dec_pair_gu ? 2 * kBM : kBM;
+  pl.splits_down = choose_splits(tiles_of(pl.bn_down) * (d / ch_dn), (ffn + kw_dn - 1) / kw_dn, num_sms);
+  pl.splits_gateup = choose_splits(tiles_of(pl.bn_gateup) * (ffn / ch_gu), (d + kw_gu - 1) / kw_gu, num_sms);
   if (env_int("MOE_SPLITS_GATEUP") >= 1 && env_int("MOE_SPLITS_GATEUP") <= 8)
     pl.splits_gateup = env_int("MOE_SPLITS_GATEUP");
   pl.grid = num_sms;
-  // CTA pairs at prefill tiles (>= 128 rows) when the channel count splits
-  // into 256-channel pair tiles; MOE_PAIR=0 keeps single CTAs (tuning)
-  const char* pe = getenv("MOE_PAIR");
-  const bool pairs_ok = !(pe != nullptr && pe[0] == '0') && num_sms >= 2;
-  pl.pair_gateup = pairs_ok && pl.bn_gateup >= 128 && ffn % (2 * kBM) == 0 && pl.splits_gateup == 1 ? 1 : 0;
-  pl.pair_down = pairs_ok && pl.bn_down >= 128 && d % (2 * kBM) == 0 ? 1 : 0;
+  // and pairs at prefill tiles (>= 128 rows) when the channel count splits
+  // into 256-channel pair tiles
+  pl.pair_gateup =
+      dec_pair_gu || (pairs_ok && pl.bn_gateup >= 128 && ffn % (2 * kBM) == 0 && pl.splits_gateup == 1) ? 1 : 0;
+  pl.pair_down = dec_pair_dn || (pairs_ok && pl.bn_down >= 128 && d % (2 * kBM) == 0) ? 1 : 0;
   return pl;
 }
 
@@ -1120,7 +1131,7 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   const int box_dn = boxn_of(plan.bn_down, plan.pair_down != 0);
   // gathered token rows: TMA gather4 for decode tiles, cp.async by the
   // producer warp for prefill tiles (gather4 costs a copy per 4 rows)
-  const bool lsu = a.gather_rows != nullptr && plan.bn_gateup >= 128;
+  const bool lsu = a.gather_rows != nullptr && (plan.bn_gateup >= 128 || plan.pair_gateup);
   if (plan.pair_gateup && a.gather_rows != nullptr && !lsu) return MOE_ERR_UNSUPPORTED;
   if (a.gather_rows != nullptr)  // token rows by index: one-row boxes for gather4
     MOE_TRY(make_tmap_2d(&xb, a.x_src, a.T_src, a.d, 2, 1, kBK, 128));
@@ -1196,7 +1207,7 @@ size_t gu_counters_size(int R, int G, int ffn, const TcPlan& plan) {
   if (plan.splits_gateup <= 1) return 0;
   const size_t tiles = (size_t)R / plan.bn_gateup + (size_t)G;  // sum of ceil(n_g / BN)
   const int ch = plan.pair_gateup ? 2 * kBM : kBM;
-  return tiles * (size_t)(ffn / ch) * 4;  // per (tile, channel tile, lane quadrant)
+  return tiles * (size_t)(ffn / ch) * (plan.pair_gateup ? 8 : 4);  // per (tile, channel tile, CTA, quadrant)
 }
 
 moe_status tc_dense_f32_launch(const void* a, const void* b, float* out, int M, int N, int K,

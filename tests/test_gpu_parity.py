@@ -270,14 +270,17 @@ def _fp8_stack(E, rows, cols, gen, all_codes_expert=None):
     return w, s
 
 
-@pytest.mark.parametrize("bn,pair", [(32, 0), (128, 0), (256, 0), (128, 1), (256, 1)])
+@pytest.mark.parametrize("bn,pair", [(32, 0), (128, 0), (256, 0), (32, 1), (128, 1), (256, 1)])
 @pytest.mark.parametrize("fp8", [False, True])
 def test_grouped_swiglu_every_tile_size(bn, pair, fp8, monkeypatch):
     # the same ragged groups through each tile-row count of both GEMMs, on
-    # single CTAs and on CTA pairs (256 output channels per tile)
+    # single CTAs and on CTA pairs (256 output channels per tile; 32-row
+    # tiles run on pairs with FP8 weights only)
+    if bn == 32 and pair and not fp8:
+        pytest.skip("32-row tiles take CTA pairs with FP8 weights only")
     monkeypatch.setenv("MOE_BN_GATEUP", str(bn))
     monkeypatch.setenv("MOE_BN_DOWN", str(bn))
-    monkeypatch.setenv("MOE_PAIR", str(pair))
+    monkeypatch.setenv("MOE_PAIR", str(2 if pair and bn == 32 else pair))  # 2: pairs at decode tiles too
     counts = np.array(GROUP_COUNTS["prefill_like"])
     E, d, f = len(counts), 256, 256
     R = int(counts.sum())
@@ -483,20 +486,26 @@ def test_layer_forward_captured_in_a_cuda_graph_with_stage_timer():
     timer.close()
 
 
-@pytest.mark.parametrize("splits,bn,d", [(1, 0, 512), (3, 0, 512), (8, 0, 512), (3, 256, 512), (8, 0, 640)])
+@pytest.mark.parametrize("splits,bn,d,pair", [(1, 0, 512, 0), (3, 0, 512, 0), (8, 0, 512, 0), (3, 256, 512, 0),
+                                               (8, 0, 640, 0), (3, 0, 512, 1), (8, 0, 512, 1)])
 @pytest.mark.parametrize("wfmt", ["bf16", "fp8"])
-def test_layer_gateup_split_k(splits, bn, d, wfmt, monkeypatch):
+def test_layer_gateup_split_k(splits, bn, d, pair, wfmt, monkeypatch):
     # the gate/up GEMM split along its reduction: fp32 partials, then an
     # in-order sum and SiLU*mul pass (chosen automatically at tiny batches);
     # bn=256 forces the 256-row tile through the same partials; ceil-sized
     # splits can leave the last ones without k-blocks (d=640 in 64-element
     # blocks over 8 splits, d=512 in the 128-element FP8 decode blocks)
     monkeypatch.setenv("MOE_SPLITS_GATEUP", str(splits))
+    monkeypatch.setenv("MOE_PAIR", str(2 * pair))  # 2: FP8 decode tiles on CTA pairs
     if bn:
         monkeypatch.setenv("MOE_BN_GATEUP", str(bn))
     shape = inputs.MoEShape("small", T=5, d=d, ffn=256, E=16, k=4, ffn_shared=256 if wfmt == "fp8" else 0,
                             wfmt=wfmt)
-    assert api.moe_plan_info(api.problem_of(shape))["splits_gateup"] == splits
+    info = api.moe_plan_info(api.problem_of(shape))
+    assert info["splits_gateup"] == splits
+    # FP8 decode tiles run on CTA pairs (split-K partials and the fused
+    # finalize per CTA of the pair); bf16 decode tiles stay on single CTAs
+    assert info["pair_gateup"] == (pair if wfmt == "fp8" and not bn else 0)
     _layer_check(shape, 4, FP8_TOL if wfmt == "fp8" else BF16_TOL)
 
 
