@@ -21,6 +21,12 @@ Parity status per function (what pins each one is listed in the tests):
                                     cases, formulation (ii))
   moe_forward_grouped               pinned (formulation (i), special cases)
   shared_expert                     pinned (library FFN)
+  round_to_e4m3                     pinned (library float8 cast on every
+                                    in-range midpoint and a dense sweep;
+                                    saturation; ties to even)
+  quantize_rows_e4m3 /              pinned (scale = row max / 448 hits code
+  dequantize_rows_e4m3              0x7E; lossless on E4M3-representable
+                                    rows; zero rows)
 """
 
 from .moe_oracle import (  # noqa: F401
@@ -37,4 +43,7 @@ from .moe_oracle import (  # noqa: F401
     moe_forward_per_token,
     moe_forward_grouped,
     shared_expert,
+    round_to_e4m3,
+    quantize_rows_e4m3,
+    dequantize_rows_e4m3,
 )

@@ -140,6 +140,50 @@ class ExpertWeights:
 
 
 # ---------------------------------------------------------------------------
+# FP8 activations for the routed experts' gate/up matrices (optional mode)
+# ---------------------------------------------------------------------------
+
+# Finite non-negative E4M3 magnitudes, indexed by code 0x00..0x7E (0x7F is
+# NaN).  They increase with the code, so the nearest code is found by search.
+_E4M3_POS = _E4M3_TABLE[:0x7F]
+
+
+def round_to_e4m3(v) -> np.ndarray:
+    """float32 values -> E4M3 codes (uint8): round to the nearest E4M3 value,
+    ties to the code with an even mantissa (round-half-to-even, the IEEE
+    default carried to the 8-bit grid), magnitudes beyond 448 clamped to 448
+    ("saturate to finite").  Zero keeps its sign bit."""
+    v = np.asarray(v, dtype=np.float32).astype(F64)
+    a = np.minimum(np.abs(v), 448.0)
+    hi = np.clip(np.searchsorted(_E4M3_POS, a, side="left"), 0, 0x7E)
+    lo = np.maximum(hi - 1, 0)
+    d_lo = a - _E4M3_POS[lo]
+    d_hi = _E4M3_POS[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.int64)
+    code = np.where(np.signbit(v), code | 0x80, code)
+    return code.astype(np.uint8)
+
+
+def quantize_rows_e4m3(x) -> Tuple[np.ndarray, np.ndarray]:
+    """Per-row FP8 quantisation of activations (float32 arithmetic, the
+    values the device computes): scale s_t = max_i |x[t, i]| / 448 (1 for an
+    all-zero row), codes q[t, i] = round_to_e4m3(x[t, i] / s_t).
+    Returns (codes uint8 [T, d], scales float32 [T]).  ``x`` holds exact
+    stored values (bf16 values are exact in float32)."""
+    x32 = np.asarray(x, dtype=np.float32)
+    amax = np.max(np.abs(x32), axis=1)
+    s = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    q = (x32 / s[:, None]).astype(np.float32)
+    return round_to_e4m3(q), s
+
+
+def dequantize_rows_e4m3(codes, scales) -> np.ndarray:
+    """codes [T, d] uint8, scales [T] float32 -> float64 values code * scale."""
+    return decode_e4m3(codes) * np.asarray(scales, F64)[:, None]
+
+
+# ---------------------------------------------------------------------------
 # Router: scores, softmax, top-k, renormalisation (section 三; section 九)
 # ---------------------------------------------------------------------------
 
@@ -257,9 +301,14 @@ def silu(z: np.ndarray) -> np.ndarray:
     return out
 
 
-def swiglu_expert(x_rows: np.ndarray, wg: np.ndarray, wu: np.ndarray, wd: np.ndarray) -> np.ndarray:
-    """One expert on a matrix of rows: (SiLU(X W_gᵀ) ⊙ (X W_uᵀ)) W_dᵀ."""
+def swiglu_expert(x_rows: np.ndarray, wg: np.ndarray, wu: np.ndarray, wd: np.ndarray,
+                  act8: bool = False) -> np.ndarray:
+    """One expert on a matrix of rows: (SiLU(X W_gᵀ) ⊙ (X W_uᵀ)) W_dᵀ.
+    ``act8``: the rows enter the gate and up products quantised per row to
+    E4M3 (quantize_rows_e4m3), the FP8-activation mode; h stays exact."""
     x_rows = np.asarray(x_rows, F64)
+    if act8:
+        x_rows = dequantize_rows_e4m3(*quantize_rows_e4m3(x_rows))
     g = x_rows @ np.asarray(wg, F64).T
     u = x_rows @ np.asarray(wu, F64).T
     return (silu(g) * u) @ np.asarray(wd, F64).T
@@ -277,14 +326,16 @@ def shared_expert(x: np.ndarray, wg: np.ndarray, wu: np.ndarray, wd: np.ndarray)
 
 def moe_forward_per_token(x, w_router, experts: ExpertWeights, k: int, bias=None,
                           shared: Optional[Tuple] = None, routing=None,
-                          tokens=None):
+                          tokens=None, act8: bool = False):
     """Formulation (i), the plain definition (section 一): for each token,
     out_t = sum over its chosen experts e of w_{t,e} * FFN_e(x_t)
             (+ shared FFN(x_t)).
 
     ``routing`` = (idx, w) overrides the router (used to evaluate the layer
     under a given expert choice); ``tokens`` restricts the computation to a
-    subset of token ids (rows of the result follow that subset).
+    subset of token ids (rows of the result follow that subset).  ``act8``:
+    the routed experts' gate/up products take the token row quantised per
+    row to E4M3 (the router and the shared expert see x itself).
     Returns (out [n, d], idx, w) in float64.
     """
     x = np.asarray(x, F64)
@@ -307,7 +358,7 @@ def moe_forward_per_token(x, w_router, experts: ExpertWeights, k: int, bias=None
             if e not in cache:
                 cache[e] = experts.get(e)
             wg, wu, wd = cache[e]
-            out[n] += w[n, j] * swiglu_expert(x[t:t + 1], wg, wu, wd)[0]
+            out[n] += w[n, j] * swiglu_expert(x[t:t + 1], wg, wu, wd, act8=act8)[0]
         if shared is not None:
             out[n] += shared_expert(x[t:t + 1], *shared)[0]
     return out, idx, w
@@ -315,7 +366,7 @@ def moe_forward_per_token(x, w_router, experts: ExpertWeights, k: int, bias=None
 
 def moe_forward_grouped(x, w_router, experts: ExpertWeights, k: int, bias=None,
                         shared: Optional[Tuple] = None, routing=None,
-                        expert_hook: Optional[Callable] = None):
+                        expert_hook: Optional[Callable] = None, act8: bool = False):
     """Formulation (ii), the grouped execution of section 二/三: sort the
     assignments by expert (a stable sort keeps ascending token order inside
     each expert), run one matrix per expert, then scatter each result back to
@@ -346,7 +397,7 @@ def moe_forward_grouped(x, w_router, experts: ExpertWeights, k: int, bias=None,
             wg, wu, wd = expert_hook(e)
         else:
             wg, wu, wd = experts.get(e)
-        y = swiglu_expert(x[flat_t[rows]], wg, wu, wd)
+        y = swiglu_expert(x[flat_t[rows]], wg, wu, wd, act8=act8)
         np.add.at(out, flat_t[rows], flat_w[rows, None] * y)
     if shared is not None:
         out += shared_expert(x, *shared)

@@ -11,7 +11,8 @@ from tests import test_oracle_pins as pins
 
 _orig = {n: getattr(M, n) for n in ("topk_renorm", "permutation_maps", "silu", "swiglu_expert",
                                       "decode_e4m3", "decode_bf16", "moe_forward_grouped",
-                                      "moe_forward_per_token", "shared_expert", "router_logits")}
+                                      "moe_forward_per_token", "shared_expert", "router_logits",
+                                      "round_to_e4m3", "quantize_rows_e4m3")}
 
 
 def _no_renorm(logits, k):
@@ -49,11 +50,11 @@ def _silu_sign(z):
     return _orig["silu"](-np.asarray(z, float))
 
 
-def _swiglu_swapped(x, wg, wu, wd):
-    return _orig["swiglu_expert"](x, wu, wg, wd)
+def _swiglu_swapped(x, wg, wu, wd, act8=False):
+    return _orig["swiglu_expert"](x, wu, wg, wd, act8=act8)
 
 
-def _swiglu_no_gate(x, wg, wu, wd):
+def _swiglu_no_gate(x, wg, wu, wd, act8=False):
     x = np.asarray(x, float)
     return ((x @ np.asarray(wg).T) * (x @ np.asarray(wu).T)) @ np.asarray(wd).T
 
@@ -79,6 +80,31 @@ def _shared_dropped(x, wg, wu, wd):
     return np.zeros((np.asarray(x).shape[0], np.asarray(wd).shape[0]))
 
 
+def _e4m3_ties_away(v):
+    # round half away from zero instead of half to even
+    v32 = np.asarray(v, np.float32)
+    c = _orig["round_to_e4m3"](v32)
+    nudged = _orig["round_to_e4m3"](np.nextafter(v32, np.copysign(np.float32(1e9), v32)))
+    mags = M._E4M3_POS
+    a = np.abs(v32).astype(float)
+    hi = np.clip(np.searchsorted(mags, a), 0, 0x7E)
+    tie = (hi > 0) & (mags[hi] - a == a - mags[np.maximum(hi - 1, 0)])
+    return np.where(tie, nudged, c).astype(np.uint8)
+
+
+def _e4m3_no_saturation(v):
+    v32 = np.asarray(v, np.float32)
+    c = _orig["round_to_e4m3"](v32)
+    return np.where(np.abs(v32) > 464.0, c | 0x7F, c).astype(np.uint8)
+
+
+def _row_scale_480(x):
+    x32 = np.asarray(x, np.float32)
+    amax = np.max(np.abs(x32), axis=1)
+    s = np.where(amax > 0, amax / np.float32(480.0), np.float32(1.0)).astype(np.float32)
+    return M.round_to_e4m3((x32 / s[:, None]).astype(np.float32)), s
+
+
 MUTATIONS = {
     "no_renormalisation": ("topk_renorm", _no_renorm),
     "lowest_k_selected": ("topk_renorm", _lowest_k),
@@ -91,6 +117,9 @@ MUTATIONS = {
     "bf16_subnormal_as_normal": ("decode_bf16", _bf16_sub_as_normal),
     "router_bias_sign": ("router_logits", _router_transposed_bias),
     "shared_expert_dropped": ("shared_expert", _shared_dropped),
+    "e4m3_ties_away_from_zero": ("round_to_e4m3", _e4m3_ties_away),
+    "e4m3_overflow_not_saturated": ("round_to_e4m3", _e4m3_no_saturation),
+    "activation_scale_off": ("quantize_rows_e4m3", _row_scale_480),
 }
 
 PIN_CHECKS = [
@@ -109,6 +138,10 @@ PIN_CHECKS = [
     pins.test_single_expert_is_dense_swiglu,
     pins.test_shared_expert_is_added_with_weight_one,
     lambda: pins.test_permutation_invariants(37, 8, 2),
+    pins.test_round_to_e4m3_matches_library_cast_in_range,
+    pins.test_round_to_e4m3_ties_go_to_even_and_saturates,
+    pins.test_quantize_rows_scale_and_extremes,
+    pins.test_quantize_rows_lossless_on_representable_rows,
 ]
 
 

@@ -335,3 +335,71 @@ def test_zipf_bias_scale_matches_calibration():
     counts, _, _, _ = oracle.permutation_maps(idx, shape.E)
     r = counts.max() / counts.mean()
     assert 7.5 <= r <= 8.5
+
+
+# ---------------------------------------------------------------------------
+# FP8 activations (per-row E4M3 quantisation of the gate/up input)
+# ---------------------------------------------------------------------------
+
+def _torch_e4m3_codes(v):
+    import torch
+    return torch.tensor(np.asarray(v, np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def test_round_to_e4m3_matches_library_cast_in_range():
+    # every midpoint between adjacent finite E4M3 magnitudes (the ties), the
+    # values just beside them, and a dense sweep, both signs: the library's
+    # float8 cast rounds to nearest, ties to even
+    mags = oracle.decode_e4m3(np.arange(0x7F))
+    mids = (mags[:-1] + mags[1:]) / 2
+    v = np.concatenate([mids, np.nextafter(mids.astype(np.float32), np.float32(0)),
+                        np.nextafter(mids.astype(np.float32), np.float32(1e9)),
+                        np.linspace(0, 448, 20001)]).astype(np.float32)
+    v = np.concatenate([v, -v])
+    assert np.array_equal(oracle.round_to_e4m3(v), _torch_e4m3_codes(v))
+
+
+def test_round_to_e4m3_ties_go_to_even_and_saturates():
+    assert oracle.round_to_e4m3(np.float32(1.0625)) == 0x38       # between 1 (0x38) and 1.125 (0x39)
+    assert oracle.round_to_e4m3(np.float32(1.1875)) == 0x3A       # between 1.125 (0x39) and 1.25 (0x3A)
+    assert oracle.round_to_e4m3(np.float32(3 * 2.0 ** -10)) == 0x02  # between subnormals 1 and 2
+    assert oracle.round_to_e4m3(np.float32(2.0 ** -10)) == 0x00   # half the smallest subnormal
+    for big in (449.0, 464.0, 1000.0, 3.0e38):
+        assert oracle.round_to_e4m3(np.float32(big)) == 0x7E      # 448, never NaN
+        assert oracle.round_to_e4m3(np.float32(-big)) == 0xFE
+
+
+def test_quantize_rows_scale_and_extremes():
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((6, 300)).astype(np.float32)
+    x[3] = 0.0
+    codes, s = oracle.quantize_rows_e4m3(x)
+    amax = np.abs(x).max(axis=1)
+    nz = amax > 0
+    assert np.array_equal(s[nz], (amax[nz] / np.float32(448)).astype(np.float32))
+    assert s[3] == 1.0 and not codes[3].any()
+    # each nonzero row's largest magnitude lands on the largest code
+    for t in np.flatnonzero(nz):
+        assert (codes[t] & 0x7F).max() == 0x7E
+    # the round trip stays within half an E4M3 step (relative 2^-4) of x
+    back = oracle.dequantize_rows_e4m3(codes, s)
+    tol = np.maximum(np.abs(x) * 2.0 ** -4, s[:, None] * 2.0 ** -10)
+    assert np.all(np.abs(back - x) <= tol + 1e-30)
+
+
+def test_quantize_rows_lossless_on_representable_rows():
+    # rows that are E4M3 values times a power-of-two scale, with one element
+    # at 448 * scale, come back exactly; the FP8-activation expert then
+    # equals the plain one
+    rng = np.random.default_rng(6)
+    codes = rng.integers(0, 0x7E, size=(4, 64)).astype(np.uint8) | (rng.integers(0, 2, size=(4, 64)) * 0x80).astype(np.uint8)
+    codes[:, 0] = 0x7E
+    scale = np.float32(2.0 ** -9)
+    x = (oracle.decode_e4m3(codes) * scale).astype(np.float32)
+    c2, s2 = oracle.quantize_rows_e4m3(x)
+    assert np.all(s2 == scale) and np.array_equal(oracle.decode_e4m3(c2), oracle.decode_e4m3(codes))
+    w = rng.standard_normal((3, 32, 64)) / 8.0
+    wd = rng.standard_normal((64, 32)) / 8.0
+    a = oracle.swiglu_expert(x, w[0], w[1], wd, act8=True)
+    b = oracle.swiglu_expert(x, w[0], w[1], wd)
+    assert np.array_equal(a, b)
