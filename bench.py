@@ -53,6 +53,9 @@ def parse_args():
     ap.add_argument("--E", type=int, default=None,
                     help="number of routed experts (default: the workload's; fewer experts make a "
                          "small case of the same expert shapes, e.g. for profiler captures)")
+    ap.add_argument("--act8", action="store_true",
+                    help="FP8-weight workloads: the routed gate/up GEMM takes the token rows "
+                         "quantised per row to E4M3 (FP8 x FP8 tensor-core instructions)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--weight-sets", type=int, default=0,
                     help="independent weight sets rotated per step (0: enough to exceed L2)")
@@ -79,7 +82,7 @@ def load_peaks():
 
 
 def wbytes(shape):
-    return {"f32": 4, "bf16": 2, "fp8": 1}[shape.wfmt]
+    return {"f32": 4, "bf16": 2, "fp8": 1, "fp8a8": 1}[shape.wfmt]
 
 
 def abytes(shape):
@@ -97,8 +100,10 @@ def stage_work(shape, touched, splits):
     (and per layer), counting only what the method must read and write."""
     R, d, f, E, T = shape.T * shape.k, shape.d, shape.ffn, shape.E, shape.T
     wb, ab = wbytes(shape), abytes(shape)
-    scale = 4 if shape.wfmt == "fp8" else 0
-    gu_bytes = touched * (2 * f * d * wb + 2 * f * scale) + R * d * ab + R * f * ab
+    scale = 4 if shape.wfmt in ("fp8", "fp8a8") else 0
+    # gate/up row operand: the activation dtype, or E4M3 codes + a row scale
+    rows = R * (d + 4) if shape.wfmt == "fp8a8" else R * d * ab
+    gu_bytes = touched * (2 * f * d * wb + 2 * f * scale) + rows + R * f * ab
     gu_flops = 4.0 * R * f * d
     y_bytes = splits * R * d * 4 if splits > 1 else R * d * ab
     dn_bytes = touched * (d * f * wb + d * scale) + R * f * ab + y_bytes
@@ -222,7 +227,7 @@ def _oracle_session(shape, seed):
     b = f64(case["router_bias"])
     decoded = {}
     for e in range(shape.E):
-        if shape.wfmt == "fp8":
+        if shape.wfmt in ("fp8", "fp8a8"):
             def dq(w, s):
                 return (w[e].view(torch.float8_e4m3fn).to(torch.float64) * s[e].to(torch.float64)[:, None]).numpy()
             decoded[e] = (dq(case["w_gate"], case["s_gate"]), dq(case["w_up"], case["s_up"]),
@@ -246,7 +251,7 @@ def oracle_tokens_per_s(shape, seed, budget_s, min_tokens=1):
     def run(n):
         t0 = time.perf_counter()
         oracle.moe_forward_grouped(x[:n], wr, ew, shape.k, bias=b, shared=shared,
-                                   expert_hook=decoded.__getitem__)
+                                   expert_hook=decoded.__getitem__, act8=shape.wfmt == "fp8a8")
         return time.perf_counter() - t0
 
     n = min(shape.T, max(min_tokens, 1))
@@ -272,7 +277,7 @@ def run_reference(args, shape, ws, rank):
 
     def step(n):
         oracle_mod.moe_forward_grouped(x[:n], wr, ew, shape.k, bias=b, shared=shared,
-                                       expert_hook=decoded.__getitem__)
+                                       expert_hook=decoded.__getitem__, act8=shape.wfmt == "fp8a8")
 
     # size each step so the whole run takes about two minutes
     t0 = time.perf_counter()
@@ -463,9 +468,15 @@ def run_ours(args, shape, ws, rank, local):
     dominant = max(("gate_up", "down"), key=lambda s: stage_ms[s])
     b_, f_ = work[dominant]
     t_s = stage_ms[dominant] / 1e3
-    ridge = bf16_tf * 1e12 / (hbm_gbs * 1e9)
+    # FP8 x FP8 gate/up: the contraction's own peak, the measured bf16 rate
+    # times the nominal fp8 / bf16 ratio (4.5 / 2.25)
+    fp8_mma = shape.wfmt == "fp8a8" and dominant == "gate_up"
+    tensor_peak = 2.0 * bf16_tf if fp8_mma else bf16_tf
+    ridge = tensor_peak * 1e12 / (hbm_gbs * 1e9)
     if f_ / b_ > ridge:
-        roof = {"bound": "tensor", "achieved": f_ / t_s / 1e12, "peak": bf16_tf, "unit": "TFLOP/s"}
+        roof = {"bound": "tensor", "achieved": f_ / t_s / 1e12, "peak": tensor_peak, "unit": "TFLOP/s"}
+        if fp8_mma:
+            peak_src += " bf16 x 2 (nominal fp8/bf16 ratio)"
     else:
         roof = {"bound": "hbm", "achieved": b_ / t_s / 1e9, "peak": hbm_gbs, "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
@@ -513,7 +524,8 @@ def run_ours(args, shape, ws, rank, local):
             "metric": "moe_layer_tokens_per_s", "value": value, "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if shape.act == "bf16" else "f32", "data": "synthetic",
+            "dtype": ("fp8" if shape.wfmt == "fp8a8" else "bf16") if shape.act == "bf16" else "f32",
+            "data": "synthetic",
             "config": workload_config(shape, {
                 "l2": (f"inputs larger than L2: {touched * 3 * shape.ffn * shape.d * wbytes(shape) / 1e9:.2f} GB "
                        f"of touched expert weights per step, {n_sets} weight set(s) rotated")}),
@@ -544,6 +556,10 @@ def main():
         if not shape.k <= args.E:
             raise SystemExit("--E must be at least the workload's top-k")
         shape = dataclasses.replace(shape, E=args.E)
+    if args.act8:
+        if shape.wfmt != "fp8":
+            raise SystemExit("--act8 needs a workload with FP8 expert weights")
+        shape = dataclasses.replace(shape, name=shape.name + "_act8", wfmt="fp8a8")
     ws, rank, local = dist_setup(args)
     if args.impl == "reference":
         return run_reference(args, shape, ws, rank)

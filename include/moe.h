@@ -44,6 +44,15 @@
  *   MOE_BF16 / MOE_FP8_E4M3     as above, FP8 weights (OCP E4M3) with fp32
  *                               per-expert, per-output-channel scales;
  *                               the router and shared expert stay bf16.
+ *   MOE_BF16 / MOE_FP8_E4M3_ACT8
+ *                               FP8 weights as above; the routed gate/up
+ *                               GEMM multiplies them with E4M3 token rows
+ *                               (per-row scales, moe_quantize_rows_e4m3):
+ *                               h = SiLU(g) * u with
+ *                               g[r,o] = s_row[r] * s_gate[e,o] *
+ *                                        sum_i q[r,i] * code_gate[e][o,i]
+ *                               (likewise u).  The down GEMM, router and
+ *                               shared expert are as for MOE_FP8_E4M3.
  * Size limits: 1 <= k <= min(E, 32), E <= 1024, d % 8 == 0, ffn % 8 == 0;
  * the tensor-core path further needs d % 128 == 0, ffn % 128 == 0 and
  * ffn_shared % 128 == 0.
@@ -58,7 +67,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 2
+#define MOE_ABI_VERSION 3
 
 #if defined(__GNUC__)
 #define MOE_API __attribute__((visibility("default")))
@@ -72,7 +81,11 @@ typedef struct CUstream_st *moe_stream_t;
 typedef enum moe_dtype {
   MOE_F32 = 0,
   MOE_BF16 = 1,
-  MOE_FP8_E4M3 = 2
+  MOE_FP8_E4M3 = 2,
+  /* w_dtype only: FP8 weights as MOE_FP8_E4M3, and the routed experts'
+   * gate/up products take the token rows quantised per row to E4M3
+   * (moe_quantize_rows_e4m3) on FP8 x FP8 tensor-core instructions */
+  MOE_FP8_E4M3_ACT8 = 3
 } moe_dtype;
 
 typedef enum moe_status {
@@ -179,7 +192,10 @@ MOE_API moe_status moe_permute_static_scratch(const moe_problem *p, const int32_
  *   h[r,:]      = SiLU(x_perm[r,:] W_g[e]^T) * (x_perm[r,:] W_u[e]^T)
  *   y_perm[r,:] = h[r,:] W_d[e]^T
  * with FP8 weights W[e][o,:] = code[e][o,:] * scale[e][o] (s_gate, s_up
- * [E, ffn]; s_down [E, d]; NULL unless w_dtype == MOE_FP8_E4M3).
+ * [E, ffn]; s_down [E, d]; NULL unless w_dtype is MOE_FP8_E4M3 or
+ * MOE_FP8_E4M3_ACT8).  With MOE_FP8_E4M3_ACT8 the rows of x_perm enter the
+ * gate/up products quantised per row (moe_quantize_rows_e4m3, into the
+ * workspace).
  *
  *   x_perm   [T*k, d] act_dtype      offsets [E+1] int32 (device)
  *   y_perm   [T*k, d] act_dtype out
@@ -192,6 +208,31 @@ MOE_API moe_status moe_grouped_swiglu(const moe_problem *p, const void *x_perm, 
                               const float *s_gate, const float *s_up, const float *s_down,
                               void *y_perm, void *workspace, size_t workspace_bytes,
                               moe_stream_t stream);
+
+/*
+ * moe_quantize_rows_e4m3 -- per-row FP8 quantisation of activation rows.
+ * Page "MOE推理流程解析", section 三 (activations may be quantised before
+ * dispatch, so that the permuted rows move fewer bytes, or dispatched at
+ * higher precision and quantised just before the experts) and page
+ * "MoE 推理部署", section 专家量化 (FP8 inference).  The layer forward with
+ * w_dtype MOE_FP8_E4M3_ACT8 quantises x before dispatch with this
+ * operation; moe_grouped_swiglu quantises x_perm (after dispatch).
+ *
+ *   s[r]      = max_i |x[r,i]| / 448, or 1 when row r is all zero
+ *   code[r,i] = E4M3(x[r,i] / s[r]): nearest E4M3 value, ties to the even
+ *               code, magnitudes above 448 saturated to 448, sign kept
+ *               (-0 -> 0x80)
+ * Both divisions are correctly rounded fp32 operations, so the codes and
+ * scales are exact functions of the inputs (bit-reproducible).
+ *
+ *   x       [rows, cols] bf16, device, 16-byte aligned
+ *   codes   [rows, cols] uint8 out (OCP E4M3 bit patterns), 16-byte aligned
+ *   scales  [rows] fp32 out
+ * rows >= 0 (0: nothing is enqueued); cols > 0 and cols % 8 == 0, else
+ * MOE_ERR_UNSUPPORTED.  Null pointers with rows > 0: MOE_ERR_INVALID_ARG.
+ */
+MOE_API moe_status moe_quantize_rows_e4m3(int32_t rows, int32_t cols, const void *x, uint8_t *codes,
+                                          float *scales, moe_stream_t stream);
 
 /*
  * moe_combine -- restore token order, apply routing weights, sum.

@@ -19,7 +19,8 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmoe_gb300.so")
 
-DTYPE = {"f32": 0, "bf16": 1, "fp8": 2}
+# "fp8a8": FP8 weights with FP8 (per-row E4M3) gate/up activations
+DTYPE = {"f32": 0, "bf16": 1, "fp8": 2, "fp8a8": 3}
 OK = 0
 ERR_INVALID_ARG = -1
 ERR_UNSUPPORTED = -2
@@ -66,6 +67,7 @@ _SIGS = {
     "moe_layer_launch_count": [_PP, ctypes.POINTER(ctypes.c_int32)],
     "moe_plan_info": [_PP, ctypes.POINTER(ctypes.c_int32)],
     "moe_permute_static_scratch": [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP],
+    "moe_quantize_rows_e4m3": [ctypes.c_int32, ctypes.c_int32, _VP, _VP, _VP, _VP],
 }
 STAGES = ("router", "permute", "gate_up", "down", "shared", "combine")
 EXPORTS = tuple(_SIGS)
@@ -142,6 +144,13 @@ def moe_grouped_swiglu(p, x_perm, offsets, w_gate, w_up, w_down, s_gate, s_up, s
     _call("moe_grouped_swiglu", ctypes.byref(p), _ptr(x_perm), _ptr(offsets), _ptr(w_gate), _ptr(w_up),
           _ptr(w_down), _ptr(s_gate), _ptr(s_up), _ptr(s_down), _ptr(y_perm), _ptr(workspace),
           0 if workspace is None else workspace.numel() * workspace.element_size(), _stream(stream))
+
+
+def moe_quantize_rows_e4m3(x, codes, scales, stream=None):
+    """Per-row E4M3 codes (uint8 [rows, cols]) and fp32 scales ([rows]) of
+    bf16 rows x [rows, cols]."""
+    rows, cols = (int(v) for v in x.shape)
+    _call("moe_quantize_rows_e4m3", rows, cols, _ptr(x), _ptr(codes), _ptr(scales), _stream(stream))
 
 
 def moe_combine(p, y_perm, inv_row, topk_w, shared_out, out, stream=None):

@@ -26,7 +26,8 @@ moe_status check_problem(const moe_problem* p, Path* path) {
   if ((int64_t)p->T * p->k > (1 << 24)) return MOE_ERR_UNSUPPORTED;
   if (p->act_dtype == MOE_F32 && p->w_dtype == MOE_F32) {
     *path = Path::kSimt;
-  } else if (p->act_dtype == MOE_BF16 && (p->w_dtype == MOE_BF16 || p->w_dtype == MOE_FP8_E4M3)) {
+  } else if (p->act_dtype == MOE_BF16 && (p->w_dtype == MOE_BF16 || p->w_dtype == MOE_FP8_E4M3 ||
+                                          p->w_dtype == MOE_FP8_E4M3_ACT8)) {
     if (p->d % 128 != 0 || p->ffn % 128 != 0 || p->ffn_shared % 128 != 0) return MOE_ERR_UNSUPPORTED;
     *path = Path::kTensor;
   } else {
@@ -37,8 +38,10 @@ moe_status check_problem(const moe_problem* p, Path* path) {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+bool fp8_weights(int w_dtype) { return w_dtype == MOE_FP8_E4M3 || w_dtype == MOE_FP8_E4M3_ACT8; }
+
 struct Layout {
-  size_t idx, w, logits, counts, offsets, perm_token, inv_row, chunk, x_perm, h, y;
+  size_t idx, w, logits, counts, offsets, perm_token, inv_row, chunk, x_perm, x_scale, h, y;
   size_t sh_offsets, sh_h, sh_y, gu_part, sh_gu_part, gu_cnt, sh_gu_cnt, total;
   size_t cnt_ints;  // gate/up finalize counters (routed, then shared), zeroed by the permutation
   size_t cnt_routed;
@@ -78,10 +81,13 @@ Layout layout(const moe_problem& p, Path path, int num_sms, bool allow_splits) {
   // The permuted rows, except on the tensor path: there the gate/up GEMM
   // gathers the token rows itself (TMA gather4 for 32-row tiles, cp.async
   // for larger ones) and this region holds only the f16 copy of x for FP8
-  // experts.
+  // experts, or x's E4M3 codes (and x_scale their row scales) with FP8
+  // activations.
   const bool gather = path == Path::kTensor;
+  const bool act8 = p.w_dtype == MOE_FP8_E4M3_ACT8;
   L.gather = gather;
-  L.x_perm = take(gather ? (p.w_dtype == MOE_FP8_E4M3 ? T * d * 2 : 0) : R * d * ab);
+  L.x_perm = take(gather ? (p.w_dtype == MOE_FP8_E4M3 ? T * d * 2 : act8 ? T * d : 0) : R * d * ab);
+  L.x_scale = take(act8 ? T * 4 : 0);
   L.h = take(R * f * ab);
   const size_t S = path == Path::kTensor ? (size_t)L.plan.splits_down : 1;
   L.y = take(S > 1 ? S * R * d * 4 : R * d * ab);
@@ -136,7 +142,8 @@ moe_status run_grouped(Path path, int R, int d, int ffn, int G, int w_dtype, con
                        const float* sg, const float* su, const float* sd, void* h, void* y,
                        const TcPlan& plan, int* status, cudaStream_t s, cudaEvent_t mid,
                        const int32_t* gather_rows = nullptr, const void* x_src = nullptr,
-                       int T_src = 0, float* gu_partials = nullptr, int* gu_cnt = nullptr) {
+                       int T_src = 0, float* gu_partials = nullptr, int* gu_cnt = nullptr,
+                       const float* row_scale = nullptr) {
   if (path == Path::kSimt) {
     SimtGroupedArgs a{R, d, ffn, G, static_cast<const float*>(x_rows), offsets,
                       static_cast<const float*>(wg), static_cast<const float*>(wu),
@@ -145,7 +152,7 @@ moe_status run_grouped(Path path, int R, int d, int ffn, int G, int w_dtype, con
     return simt_grouped_launch(a, s, mid);
   }
   TcGroupedArgs a{R, d, ffn, G, w_dtype, x_rows, offsets, wg, wu, wd, sg, su, sd, h, y, status,
-                  wait_limit_ns(), gather_rows, x_src, T_src, gu_partials, gu_cnt};
+                  wait_limit_ns(), gather_rows, x_src, T_src, gu_partials, gu_cnt, row_scale};
   return tc_grouped_launch(a, plan, s, mid);
 }
 
@@ -219,7 +226,7 @@ moe_status moe_grouped_swiglu(const moe_problem* p, const void* x_perm, const in
   if (!x_perm || !offsets || !w_gate || !w_up || !w_down || !y_perm) return MOE_ERR_INVALID_ARG;
   for (const void* q : {x_perm, w_gate, w_up, w_down, (const void*)y_perm})
     if (!aligned16(q)) return MOE_ERR_INVALID_ARG;
-  const bool fp8 = p->w_dtype == MOE_FP8_E4M3;
+  const bool fp8 = fp8_weights(p->w_dtype), act8 = p->w_dtype == MOE_FP8_E4M3_ACT8;
   if (fp8 != (s_gate != nullptr) || fp8 != (s_up != nullptr) || fp8 != (s_down != nullptr))
     return MOE_ERR_INVALID_ARG;
   DeviceCtx ctx;
@@ -227,19 +234,41 @@ moe_status moe_grouped_swiglu(const moe_problem* p, const void* x_perm, const in
   const Layout L = layout(*p, path, ctx.num_sms, false);
   const size_t R = (size_t)p->T * p->k;
   const size_t h_bytes = align256(R * p->ffn * act_bytes(p->act_dtype));
-  // FP8 experts run on f16 operands: round x_perm to f16 into the workspace
-  const size_t need = h_bytes + (fp8 ? align256(R * p->d * 2) : 0);
+  // FP8 experts run on f16 operands: round x_perm to f16 into the
+  // workspace; with FP8 activations, its E4M3 codes and row scales
+  const size_t rows_bytes = act8 ? align256(R * p->d) : fp8 ? align256(R * p->d * 2) : 0;
+  const size_t need = h_bytes + rows_bytes + (act8 ? align256(R * 4) : 0);
   if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const void* rows = x_perm;
-  if (fp8) {
+  float* row_scale = nullptr;
+  if (act8) {
+    row_scale = at<float>(workspace, h_bytes + rows_bytes);
+    MOE_TRY(quantize_rows_e4m3_launch(x_perm, (int)R, p->d, at<uint8_t>(workspace, h_bytes), row_scale,
+                                      ctx.num_sms, s));
+    rows = at<uint8_t>(workspace, h_bytes);
+  } else if (fp8) {
     void* xf16 = at<uint8_t>(workspace, h_bytes);
     MOE_TRY(bf16_to_f16_launch(x_perm, xf16, R * p->d, s));
     rows = xf16;
   }
   return run_grouped(path, (int)R, p->d, p->ffn, p->E, p->w_dtype, rows, offsets, w_gate, w_up,
                      w_down, s_gate, s_up, s_down, workspace, y_perm, L.plan, ctx.status, s,
-                     nullptr);
+                     nullptr, nullptr, nullptr, 0, nullptr, nullptr, row_scale);
+}
+
+moe_status moe_quantize_rows_e4m3(int32_t rows, int32_t cols, const void* x, uint8_t* codes,
+                                  float* scales, moe_stream_t stream) {
+  if (rows < 0) return MOE_ERR_INVALID_ARG;
+  if (cols <= 0 || cols % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (rows == 0) return MOE_OK;
+  if (x == nullptr || codes == nullptr || scales == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(codes) || (reinterpret_cast<uintptr_t>(scales) & 3u) != 0)
+    return MOE_ERR_INVALID_ARG;
+  DeviceCtx ctx;
+  MOE_TRY(device_ctx(&ctx));
+  return quantize_rows_e4m3_launch(x, rows, cols, codes, scales, ctx.num_sms,
+                                   reinterpret_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_combine(const moe_problem* p, const void* y_perm, const int32_t* inv_row,
@@ -279,7 +308,7 @@ moe_status layer_forward_impl(const moe_problem* p, const void* x, const void* w
   if (!x || !w_router || !w_gate || !w_up || !w_down || !out) return MOE_ERR_INVALID_ARG;
   for (const void* q : {x, w_router, w_gate, w_up, w_down, (const void*)out})
     if (!aligned16(q)) return MOE_ERR_INVALID_ARG;
-  const bool fp8 = p->w_dtype == MOE_FP8_E4M3;
+  const bool fp8 = fp8_weights(p->w_dtype), act8 = p->w_dtype == MOE_FP8_E4M3_ACT8;
   if (fp8 != (s_gate != nullptr) || fp8 != (s_up != nullptr) || fp8 != (s_down != nullptr))
     return MOE_ERR_INVALID_ARG;
   const bool has_shared = p->ffn_shared > 0;
@@ -356,15 +385,23 @@ moe_status layer_forward_impl(const moe_problem* p, const void* x, const void* w
   MOE_TRY(permute_launch(pa, s));
   MOE_TRY(mark(2));
   // 3. grouped SwiGLU experts (gate/up + SiLU*mul, then down)
+  // FP8 experts gather from an f16 copy of x; with FP8 activations, from
+  // x's per-row E4M3 codes (quantised before dispatch: T rows, not T*k)
   const void* x_src = x;
-  if (gather && fp8) {
+  float* x_scale = nullptr;
+  if (gather && act8) {
+    x_scale = at<float>(workspace, L.x_scale);
+    MOE_TRY(quantize_rows_e4m3_launch(x, p->T, p->d, x_perm, x_scale, ctx.num_sms, s));
+    x_src = x_perm;
+  } else if (gather && fp8) {
     MOE_TRY(bf16_to_f16_launch(x, x_perm, (size_t)p->T * p->d, s));
     x_src = x_perm;
   }
   MOE_TRY(run_grouped(path, R, p->d, p->ffn, p->E, p->w_dtype, x_perm, offsets, w_gate, w_up,
                       w_down, s_gate, s_up, s_down, h, y, L.plan, ctx.status, s,
                       timer ? timer->ev[3] : nullptr, gather ? perm_token : nullptr, x_src, p->T,
-                      at<float>(workspace, L.gu_part), L.cnt_routed ? at<int>(workspace, L.gu_cnt) : nullptr));
+                      at<float>(workspace, L.gu_part), L.cnt_routed ? at<int>(workspace, L.gu_cnt) : nullptr,
+                      x_scale));
   MOE_TRY(mark(4));
   // 4. shared expert (CUDA-core path: here, one group {0, T}); on the
   // tensor path, join the side stream
@@ -486,7 +523,7 @@ moe_status moe_layer_launch_count(const moe_problem* p, int32_t* launches) {
   if (fuse_topk_in_permute(p->T, p->k, p->E, rs)) n -= 1;
   const Layout L0 = layout(*p, path, ctx.num_sms, true);
   n += permute_launch_count(p->T, p->k, !L0.gather);
-  if (L0.gather && p->w_dtype == MOE_FP8_E4M3) n += 1;  // x -> f16
+  if (L0.gather && fp8_weights(p->w_dtype)) n += 1;  // x -> f16, or x -> E4M3 codes
   const Layout L = layout(*p, path, ctx.num_sms, true);
   n += 2;                        // gate/up, down
   // split-K gate/up: a finalize pass unless the GEMM finalizes itself

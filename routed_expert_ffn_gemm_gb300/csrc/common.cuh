@@ -202,6 +202,10 @@ int permute_launch_count(int T, int k, bool move_rows);
 moe_status permute_launch(const PermuteArgs& a, cudaStream_t s);
 // bf16 rows -> f16 rows (saturating), n elements, n % 8 == 0.
 moe_status bf16_to_f16_launch(const void* src, void* dst, size_t n, cudaStream_t s);
+// Per-row E4M3 codes [rows, d] and fp32 scales [rows] of bf16 rows x
+// (scale = row absmax / 448; FP8-activation mode of the gate/up GEMM).
+moe_status quantize_rows_e4m3_launch(const void* x, int rows, int d, void* codes, float* scales,
+                                     int num_sms, cudaStream_t s);
 
 struct CombineArgs {
   int T, k, d, act_dtype;
@@ -242,7 +246,7 @@ struct TcPlan {
 };
 struct TcGroupedArgs {
   int R, d, ffn, G;    // rows, hidden, intermediate, groups (experts)
-  int w_dtype;         // MOE_BF16 or MOE_FP8_E4M3
+  int w_dtype;         // MOE_BF16, MOE_FP8_E4M3 or MOE_FP8_E4M3_ACT8
   const void* x_perm;  // [R, d] B operand of gate/up: bf16, or f16 with FP8 weights
   const int32_t* offsets;
   const void* w_gate;
@@ -264,6 +268,10 @@ struct TcGroupedArgs {
   // nullable with gu_partials: zeroed arrival counters (gu_counters_size
   // ints); the GEMM then finalizes h itself instead of a separate pass
   int* gu_cnt;
+  // FP8 activations (w_dtype MOE_FP8_E4M3_ACT8): x_perm / x_src hold E4M3
+  // codes and row_scale their per-row scales ([T_src] with gather_rows,
+  // else [R])
+  const float* row_scale;
 };
 // Arrival counters the fused gate/up finalize needs for R rows in G groups.
 size_t gu_counters_size(int R, int G, int ffn, const TcPlan& plan);

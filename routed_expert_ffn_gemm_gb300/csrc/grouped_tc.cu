@@ -17,7 +17,7 @@
 // Work unit = (expert g, tile of BN rows, channel tile mt, K split ks).
 // A persistent grid (one CTA per SM) strides over the units; the per-expert
 // tile counts are derived on the device from the offsets (no host sync).
-// CTA roles (320 threads; 448 with FP8 weights):
+// CTA roles (320 threads; 448 with converter warps):
 //   warp 0 lane 0   TMA producer: weight tile(s) [128 x 64] + the row boxes
 //                   per stage, 128-byte swizzle
 //   warp 1 lane 0   MMA issuer: tcgen05.mma kind::f16, fp32 accumulate;
@@ -25,7 +25,7 @@
 //   warps 2..9      epilogue: tcgen05.ld from TMEM (two warps per lane
 //                   quadrant, alternate column chunks), SiLU(g)*u (gate/up)
 //                   or the projection (down), 64-byte coalesced stores
-//   warps 10..13    (FP8 weights only) converters: E4M3 tile staged by TMA ->
+//   warps 10..13    (FP8 weights, f16 MMA) converters: E4M3 tile staged by TMA ->
 //                   f16 tile, into tensor memory (decode tiles: the MMA
 //                   reads A from TMEM) or into the 128-byte-swizzled
 //                   shared-memory layout the MMA reads
@@ -49,6 +49,13 @@
 // holds bf16 values exactly inside f16's normal range) and the
 // per-output-channel scale (one TMEM lane = one channel) multiplies the fp32
 // accumulator in the epilogue.
+//
+// FP8 activations ("MOE推理流程解析", section 三: activations quantised
+// before dispatch; gate/up only): the B rows arrive as E4M3 codes with one
+// fp32 scale per token row, both operands go straight from the TMA ring to
+// tcgen05.mma kind::f8f6f4 (K = 32 per instruction, 128-byte rows = 128
+// elements of K per stage, no converter warps), and the epilogue multiplies
+// each accumulator by its channel's weight scale and its column's row scale.
 #include <stdlib.h>
 #include <string.h>
 
@@ -109,6 +116,9 @@ struct TcParams {
   int lsu_gather;
   const void* x_src;
   int d_src;  // row length of x_src (elements)
+  // FP8 activations (gate/up): per-row quantisation scales of the B rows,
+  // indexed by token (gather_rows) or by row
+  const float* row_scale;
 };
 
 // Whether FP8 tiles take the tensor-memory operand path (see Cfg::TA): the
@@ -119,8 +129,16 @@ __host__ __device__ constexpr bool ta_config(int mode, int bn, bool fp8, bool pa
   return fp8 && (pair ? (mode == kGateUp ? bn <= 128 : bn <= 256) : bn == 32);
 }
 
-template <int MODE, int BN, bool FP8, bool PAIR>
+// Weight formats of the kernel: bf16; FP8 weights converted to f16 for a
+// kind::f16 MMA ("w8a16"); FP8 weights multiplied by FP8 token rows with a
+// kind::f8f6f4 MMA (gate/up only: the FP8-activation mode).
+enum { kWBf16 = 0, kWFp8 = 1, kWFp8Act8 = 2 };
+
+template <int MODE, int BN, int WF, bool PAIR>
 struct Cfg {
+  static constexpr bool FP8 = WF != kWBf16;     // E4M3 weights, per-channel scales
+  static constexpr bool A8 = WF == kWFp8Act8;   // ... times E4M3 token rows (kind::f8f6f4)
+  static constexpr bool CONV = WF == kWFp8;     // converter warps turn E4M3 into f16
   // PAIR: a CTA pair (cluster of 2) runs one unit with cta_group::2 MMAs:
   // M = 256 output channels (128 per CTA, each CTA's TMEM holding its own
   // 128 accumulator rows for all N columns) and each CTA staging half of
@@ -134,13 +152,17 @@ struct Cfg {
   // span 128 elements of K: 128-byte E4M3 rows (64-byte rows cost as many
   // copy requests per row as 128-byte bf16 rows, for half the bytes), B in
   // two 64-element halves.
-  static constexpr bool TA = ta_config(MODE, BN, FP8, PAIR);
+  static constexpr bool TA = ta_config(MODE, BN, CONV, PAIR);
   // bf16 down GEMM on pairs: 128 elements of K per stage as well, A and B
   // each in ONE copy (3-D boxes of two 64-element column blocks): half the
   // copies and half the barrier round trips per byte of a 64-element stage
   static constexpr bool K2 = MODE == kDown && PAIR && !FP8;
-  static constexpr int KB = TA || K2 ? 2 * kBK : kBK;          // K elements per stage
-  static constexpr int NSUB = KB / kBK;                        // 64-element B sub-tiles per stage
+  // FP8 activations: 128 elements of K per stage too, in single 128-byte
+  // rows for both operands (one sub-tile); kind::f8f6f4 takes K = 32 per
+  // instruction
+  static constexpr int KB = TA || K2 || A8 ? 2 * kBK : kBK;     // K elements per stage
+  static constexpr int NSUB = A8 ? 1 : KB / kBK;               // 128-byte B sub-tiles per stage
+  static constexpr int KSTEP = A8 ? 32 : 16;                   // K per MMA instruction
   static constexpr int A_BYTES = kBM * kBK * 2;                // 16 KB bf16 tile (MMA operand)
   static constexpr int BSUB_BYTES = (PAIR ? BN / 2 : BN) * kBK * 2;
   static constexpr int B_BYTES = NSUB * BSUB_BYTES;
@@ -152,7 +174,7 @@ struct Cfg {
   // operand slots: enough that converters run ahead of the MMA's commits
   // (a commit round trip per slot otherwise serialises decode), while the
   // TMA ring keeps at least 4 slots
-  static constexpr int OPND_BYTES = TA ? 0 : NA * A_BYTES;
+  static constexpr int OPND_BYTES = TA || !CONV ? 0 : NA * A_BYTES;
   static constexpr int W_BYTES_ = FP8 ? STG_BYTES : NSUB * A_BYTES;
   static constexpr int SLOT_ = NA * W_BYTES_ + B_BYTES;
   static constexpr int AVAIL_ = kSmemLimit - 1024 - (8 * 40 + 16 + 4 * 2 * (kMaxGroups + 8));
@@ -165,17 +187,17 @@ struct Cfg {
                                                : (2 * ACC_COLS <= 512 ? 2 : 1);
   // TA operand slots of 64 columns (128 f16 of K per lane) per weight matrix
   static constexpr int TA_SLOTS = TA_DECODE ? 4 : (512 - NBUF * ACC_COLS) / 64;
-  static constexpr int OSTAGES = !FP8 ? 0 : TA ? (TA_SLOTS / NA > 4 ? 4 : TA_SLOTS / NA)
+  static constexpr int OSTAGES = !CONV ? 0 : TA ? (TA_SLOTS / NA > 4 ? 4 : TA_SLOTS / NA)
                                  : (AVAIL_ - 6 * SLOT_) / (NA * A_BYTES) >= 4 ? 4
                                  : (AVAIL_ - 6 * SLOT_) / (NA * A_BYTES) >= 3 ? 3 : 2;
   static constexpr int RING_OFF = OSTAGES * OPND_BYTES;
   static constexpr int W_BYTES = FP8 ? STG_BYTES : NSUB * A_BYTES;  // weight tile bytes in a TMA slot
   // distance between the A matrices where the MMA reads them (TMA slot, or
   // FP8 operand slot)
-  static constexpr int A_STRIDE = FP8 ? A_BYTES : W_BYTES;
+  static constexpr int A_STRIDE = CONV ? A_BYTES : W_BYTES;
   static constexpr int B_OFF = NA * W_BYTES;
   static constexpr int STAGE_BYTES = B_OFF + B_BYTES;           // multiple of 1024
-  static constexpr int THREADS = kThreads + (FP8 ? kConvThreads : 0);
+  static constexpr int THREADS = kThreads + (CONV ? kConvThreads : 0);
   static constexpr int TAIL_BYTES = 8 * 40 + 16 + 4 * 2 * (kMaxGroups + 8);
   static constexpr int STAGES_FIT = (kSmemLimit - 1024 - TAIL_BYTES - RING_OFF) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 10 ? 10 : STAGES_FIT;
@@ -258,12 +280,13 @@ __device__ __forceinline__ uint4 e4m3x8_to_f16x8(uint32_t lo, uint32_t hi) {
   return r;
 }
 
-template <int MODE, int BN, bool FP8, bool PAIR>
-__global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
+template <int MODE, int BN, int WF, bool PAIR>
+__global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
     tc_grouped_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA0,
                       const __grid_constant__ CUtensorMap tmA1,
                       const __grid_constant__ CUtensorMap tmB) {
-  using C = Cfg<MODE, BN, FP8, PAIR>;
+  using C = Cfg<MODE, BN, WF, PAIR>;
+  constexpr bool FP8 = C::FP8, A8 = C::A8, CONV = C::CONV;
   constexpr int STAGES = C::STAGES;
   // pair barriers with remote arrivers live in the even CTA (rank 0)
   constexpr uint32_t kRemote = PAIR ? 2u : 1u;
@@ -284,7 +307,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
   const bool lsu = MODE == kGateUp && p.lsu_gather != 0;
   // bf16 pairs gathering rows: each CTA's row copies complete its own
   // rows_full barrier; the odd CTA's MMA warp relays it to the even CTA
-  const bool relay = PAIR && !FP8 && lsu;
+  const bool relay = PAIR && !CONV && lsu;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::SLOT_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::ABORT_OFF);
   int* offs = reinterpret_cast<int*>(smem + C::OFFS_OFF);
@@ -307,7 +330,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
       // their own CTA's copies
       // (+ 32 per-lane arrivals of the gathered rows, or the relayed
       // arrival of the odd CTA's rows)
-      ptx::mbar_init(full_bar(s), PAIR && !FP8 ? 2 + (relay ? 1 : 0) : 1 + (lsu ? 32 : 0));
+      ptx::mbar_init(full_bar(s), PAIR && !CONV ? 2 + (relay ? 1 : 0) : 1 + (lsu ? 32 : 0));
       ptx::mbar_init(empty_bar(s), 1);
       ptx::mbar_init(bfull_bar(s), 32);
     }
@@ -399,7 +422,9 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
       const uint64_t pol_w = ptx::policy_evict_first();
       const uint64_t pol_x = ptx::policy_evict_last();
       const uint32_t wmask = gather || lsu ? 0xffffffffu : 1u;
-      const __nv_bfloat16* xs = static_cast<const __nv_bfloat16*>(p.x_src);  // 16-bit rows (bf16 or f16)
+      // gathered rows: 16-bit elements (bf16 / f16), or E4M3 bytes (FP8 activations)
+      const uint8_t* xs = static_cast<const uint8_t*>(p.x_src);
+      constexpr int kEsz = A8 ? 1 : 2;
       int stage = 0;
       uint32_t phase = 0;
       long long issued = 0;  // slots armed so far (the abort path derives their phases)
@@ -456,7 +481,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
               ptx::mbar_arrive_expect_tx_cluster(fb, bytes);
               ptx::tma_load_3d_pair(sa, &tmA0, fb, arow, kb * 2, pol_w);
               ptx::tma_load_3d_pair(sb, &tmB, fb, brow0, kb * 2, pol_x);
-            } else if (PAIR && !FP8) {
+            } else if (PAIR && !CONV) {
               // both CTAs' copies complete the even CTA's barrier
               const uint32_t fb = lead(full_bar(stage));
               ptx::mbar_arrive_expect_tx_cluster(fb, bytes);
@@ -488,10 +513,10 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
               const int r = lane + 32 * i;
 #pragma unroll
               for (int sub = 0; sub < C::NSUB; ++sub) {
-                const __nv_bfloat16* src = xs + (size_t)tok[i] * p.d_src + kb * C::KB + sub * kBK;
+                const uint8_t* src = xs + ((size_t)tok[i] * p.d_src + (size_t)kb * C::KB + sub * kBK) * kEsz;
                 const uint32_t dst = sb + sub * C::BSUB_BYTES + r * 128;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) ptx::cp_async16(dst + ((c ^ (r & 7)) << 4), src + 8 * c);
+                for (int c = 0; c < 8; ++c) ptx::cp_async16(dst + ((c ^ (r & 7)) << 4), src + 16 * c);
               }
             }
             ptx::cp_async_arrive_noinc(relay ? bfull_bar(stage) : full_bar(stage));
@@ -519,7 +544,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
         set_device_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
         // let every issued copy land before shared memory is released
         const uint64_t grace = ptx::globaltimer_ns() + 100000000ull;
-        if (PAIR && !FP8 && !leader) {
+        if (PAIR && !CONV && !leader) {
           // this CTA's copies complete the peer's barriers: wait a while
           const uint64_t t_end = ptx::globaltimer_ns() + 20000000ull;
           while (ptx::globaltimer_ns() < t_end) {
@@ -566,26 +591,27 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
           }
           ptx::tc_fence_after();
           const int n_mma = PAIR ? ((x.n_valid + 31) / 32) * 32 : ((x.n_valid + 15) / 16) * 16;
+          // (kind::f8f6f4 takes the same descriptor bits: E4M3 is format 0)
           const uint32_t idesc = FP8 ? ptx::idesc_f16_f32(C::CH, n_mma) : ptx::idesc_bf16_f32(C::CH, n_mma);
           const uint32_t d0 = tmem_base + (uint32_t)(C::ACC_COLS * buf);
           const uint32_t d1 = d0 + (uint32_t)C::UP_OFF;
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!ptx::mbar_wait_bounded(full_bar(stage), phase, deadline, abort_flag) ||
                 (relay && !ptx::mbar_wait_bounded(bfull_bar(stage), phase, deadline, abort_flag)) ||
-                (FP8 && !ptx::mbar_wait_bounded(ofull_bar(ostage), ophase, deadline, abort_flag))) {
+                (CONV && !ptx::mbar_wait_bounded(ofull_bar(ostage), ophase, deadline, abort_flag))) {
               ok = false;
               break;
             }
             // rows gathered by cp.async are generic-proxy writes: order them
             // before the tensor core's reads
-            if (lsu && !FP8) ptx::fence_proxy_async_smem();
+            if (lsu && !CONV) ptx::fence_proxy_async_smem();
             ptx::tc_fence_after();
             const uint32_t sa = sbase + C::RING_OFF + stage * C::STAGE_BYTES;
-            const uint32_t aa = FP8 ? sbase + ostage * C::OPND_BYTES : sa;
+            const uint32_t aa = CONV ? sbase + ostage * C::OPND_BYTES : sa;
             const uint64_t da0 = ptx::sdesc_k_sw128(aa);
             const uint64_t da1 = ptx::sdesc_k_sw128(aa + C::A_STRIDE);
 #pragma unroll
-            for (int kk = 0; kk < C::KB / 16; ++kk) {
+            for (int kk = 0; kk < C::KB / C::KSTEP; ++kk) {
               const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
               // B: 64-element sub-tile kk / 4, K step kk % 4 inside it
               const uint64_t db = ptx::sdesc_k_sw128(sa + C::B_OFF + (kk >> 2) * C::BSUB_BYTES) + 2 * (kk & 3);
@@ -599,6 +625,15 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
                 } else {
                   ptx::mma_f16_ta(d0, at + C::ta_col(ostage, 0), db, idesc, acc);
                   if (MODE == kGateUp) ptx::mma_f16_ta(d1, at + C::ta_col(ostage, 1), db, idesc, acc);
+                }
+              } else if (A8) {
+                // E4M3 x E4M3: K = 32 per instruction, 32 bytes per step
+                if (PAIR) {
+                  ptx::mma_f8_pair(d0, da0 + ka, db, idesc, acc);
+                  ptx::mma_f8_pair(d1, da1 + ka, db, idesc, acc);
+                } else {
+                  ptx::mma_f8(d0, da0 + ka, db, idesc, acc);
+                  ptx::mma_f8(d1, da1 + ka, db, idesc, acc);
                 }
               } else if (PAIR) {
                 ptx::mma_f16_pair(d0, da0 + ka, db, idesc, acc);
@@ -614,7 +649,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
               stage = 0;
               phase ^= 1u;
             }
-            if (FP8) {
+            if (CONV) {
               commit(oempty_bar(ostage));
               if (++ostage == C::OSTAGES) {
                 ostage = 0;
@@ -720,22 +755,33 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
           const uint32_t* b = rb + 16 * hlf;
           if (nj > 0) {
             if (MODE == kGateUp) {
+              // FP8 activations: each column (token row) carries its row's
+              // quantisation scale (rows gathered by token: the token's)
+              float rsc[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                rsc[j] = 1.f;
+                if (A8 && j < nj) {
+                  const int r = x.row0 + cb + j;
+                  rsc[j] = p.row_scale[p.gather_rows != nullptr ? p.gather_rows[r] : r];
+                }
+              }
               if (p.out_f32) {
                 // K-split: scaled fp32 partials, SiLU*mul after the in-order sum
                 float* row = static_cast<float*>(p.out) + ((size_t)x.ks * p.R + x.row0 + cb) * 2 * p.M + ch;
 #pragma unroll
                 for (int j = 0; j < 16; ++j, row += 2 * p.M)
                   if (j < nj) {
-                    row[0] = __uint_as_float(a[j]) * sc0;
-                    row[p.M] = __uint_as_float(b[j]) * sc1;
+                    row[0] = __uint_as_float(a[j]) * sc0 * rsc[j];
+                    row[p.M] = __uint_as_float(b[j]) * sc1 * rsc[j];
                   }
               } else if (FP8) {
                 __half* o = static_cast<__half*>(p.out) + (size_t)(x.row0 + cb) * p.M + ch;  // h feeds an f16 MMA
 #pragma unroll
                 for (int j = 0; j < 16; ++j, o += p.M)
                   if (j < nj) {
-                    const float g = __uint_as_float(a[j]) * sc0;
-                    *o = __float2half_rn(silu_mul(g, __uint_as_float(b[j]) * sc1));
+                    const float g = __uint_as_float(a[j]) * sc0 * rsc[j];
+                    *o = __float2half_rn(silu_mul(g, __uint_as_float(b[j]) * sc1 * rsc[j]));
                   }
               } else {
                 __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + (size_t)(x.row0 + cb) * p.M + ch;
@@ -812,7 +858,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
       }
     }
     if (!ok && lane == 0) set_device_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
-  } else if (FP8 && !p.selftest) {
+  } else if (CONV && !p.selftest) {
     // ------------------------------------------------------------ converters
     // Same unit / k-block walk as the MMA issuer; the four converter warps
     // share each stage.  Per k-block: wait for the E4M3 tiles in the TMA
@@ -928,11 +974,11 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, FP8, PAIR>::THREADS, 1)
   }
 }
 
-template <int MODE, int BN, bool FP8, bool PAIR = false>
+template <int MODE, int BN, int WF, bool PAIR = false>
 moe_status launch_one(const TcParams& p, const CUtensorMap& a0, const CUtensorMap& a1,
                       const CUtensorMap& b, int grid, cudaStream_t s) {
-  using C = Cfg<MODE, BN, FP8, PAIR>;
-  auto kern = tc_grouped_kernel<MODE, BN, FP8, PAIR>;
+  using C = Cfg<MODE, BN, WF, PAIR>;
+  auto kern = tc_grouped_kernel<MODE, BN, WF, PAIR>;
   MOE_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES));
   if (PAIR) {
     // The grid is persistent: every pair must be resident at once, and not
@@ -967,28 +1013,35 @@ moe_status launch_one(const TcParams& p, const CUtensorMap& a0, const CUtensorMa
 }
 
 template <int MODE>
-moe_status launch_mode(int bn, bool fp8, bool pair, const TcParams& p, const CUtensorMap& a0,
+moe_status launch_mode(int bn, int wf, bool pair, const TcParams& p, const CUtensorMap& a0,
                        const CUtensorMap& a1, const CUtensorMap& b, int grid, cudaStream_t s) {
   if (pair) {
     if (p.M % (2 * kBM) != 0 || grid < 2) return MOE_ERR_UNSUPPORTED;
-    if (fp8) {
-      if (bn == 32) return launch_one<MODE, 32, true, true>(p, a0, a1, b, grid, s);
-      if (bn == 128) return launch_one<MODE, 128, true, true>(p, a0, a1, b, grid, s);
-      if (bn == 256) return launch_one<MODE, 256, true, true>(p, a0, a1, b, grid, s);
-    } else {
-      if (bn == 128) return launch_one<MODE, 128, false, true>(p, a0, a1, b, grid, s);
-      if (bn == 256) return launch_one<MODE, 256, false, true>(p, a0, a1, b, grid, s);
+    if (wf == kWFp8) {
+      if (bn == 32) return launch_one<MODE, 32, kWFp8, true>(p, a0, a1, b, grid, s);
+      if (bn == 128) return launch_one<MODE, 128, kWFp8, true>(p, a0, a1, b, grid, s);
+      if (bn == 256) return launch_one<MODE, 256, kWFp8, true>(p, a0, a1, b, grid, s);
+    } else if (wf == kWBf16) {
+      if (bn == 128) return launch_one<MODE, 128, kWBf16, true>(p, a0, a1, b, grid, s);
+      if (bn == 256) return launch_one<MODE, 256, kWBf16, true>(p, a0, a1, b, grid, s);
+    } else if (MODE == kGateUp) {
+      if (bn == 128) return launch_one<MODE, 128, kWFp8Act8, true>(p, a0, a1, b, grid, s);
+      if (bn == 256) return launch_one<MODE, 256, kWFp8Act8, true>(p, a0, a1, b, grid, s);
     }
     return MOE_ERR_UNSUPPORTED;
   }
-  if (fp8) {
-    if (bn == 32) return launch_one<MODE, 32, true>(p, a0, a1, b, grid, s);
-    if (bn == 128) return launch_one<MODE, 128, true>(p, a0, a1, b, grid, s);
-    if (bn == 256) return launch_one<MODE, 256, true>(p, a0, a1, b, grid, s);
-  } else {
-    if (bn == 32) return launch_one<MODE, 32, false>(p, a0, a1, b, grid, s);
-    if (bn == 128) return launch_one<MODE, 128, false>(p, a0, a1, b, grid, s);
-    if (bn == 256) return launch_one<MODE, 256, false>(p, a0, a1, b, grid, s);
+  if (wf == kWFp8) {
+    if (bn == 32) return launch_one<MODE, 32, kWFp8>(p, a0, a1, b, grid, s);
+    if (bn == 128) return launch_one<MODE, 128, kWFp8>(p, a0, a1, b, grid, s);
+    if (bn == 256) return launch_one<MODE, 256, kWFp8>(p, a0, a1, b, grid, s);
+  } else if (wf == kWBf16) {
+    if (bn == 32) return launch_one<MODE, 32, kWBf16>(p, a0, a1, b, grid, s);
+    if (bn == 128) return launch_one<MODE, 128, kWBf16>(p, a0, a1, b, grid, s);
+    if (bn == 256) return launch_one<MODE, 256, kWBf16>(p, a0, a1, b, grid, s);
+  } else if (MODE == kGateUp) {
+    if (bn == 32) return launch_one<MODE, 32, kWFp8Act8>(p, a0, a1, b, grid, s);
+    if (bn == 128) return launch_one<MODE, 128, kWFp8Act8>(p, a0, a1, b, grid, s);
+    if (bn == 256) return launch_one<MODE, 256, kWFp8Act8>(p, a0, a1, b, grid, s);
   }
   return MOE_ERR_UNSUPPORTED;
 }
@@ -1086,13 +1139,15 @@ TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype) {
   // tile, whose bytes per stage bound the FP8 decode tiles either way).
   const char* pe = getenv("MOE_PAIR");
   const bool pairs_ok = !(pe != nullptr && pe[0] == '0') && num_sms >= 2;
-  const bool fp8 = w_dtype == MOE_FP8_E4M3;
+  const bool act8 = w_dtype == MOE_FP8_E4M3_ACT8;
+  const bool fp8 = w_dtype == MOE_FP8_E4M3 || act8;
   const bool dec_pairs = pairs_ok && pe != nullptr && pe[0] == '2';
-  const bool dec_pair_gu = dec_pairs && fp8 && pl.bn_gateup == 32 && ffn % (2 * kBM) == 0;
+  const bool dec_pair_gu = dec_pairs && fp8 && !act8 && pl.bn_gateup == 32 && ffn % (2 * kBM) == 0;
   const bool dec_pair_dn = dec_pairs && fp8 && pl.bn_down == 32 && d % (2 * kBM) == 0;
   // K per stage: 128 on the FP8 tensor-memory operand path (decode tiles)
+  // and with FP8 activations (128-byte rows of both operands)
   const int kw_dn = fp8 && pl.bn_down == 32 ? 2 * kBK : kBK;
-  const int kw_gu = fp8 && pl.bn_gateup == 32 ? 2 * kBK : kBK;
+  const int kw_gu = act8 || (fp8 && pl.bn_gateup == 32) ? 2 * kBK : kBK;
   const int ch_dn = dec_pair_dn ? 2 * kBM : kBM, ch_gu = dec_pair_gu ? 2 * kBM : kBM;
   pl.splits_down = choose_splits(tiles_of(pl.bn_down) * (d / ch_dn), (ffn + kw_dn - 1) / kw_dn, num_sms);
   pl.splits_gateup = choose_splits(tiles_of(pl.bn_gateup) * (ffn / ch_gu), (d + kw_gu - 1) / kw_gu, num_sms);
@@ -1110,9 +1165,12 @@ TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype) {
 moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStream_t s,
                              cudaEvent_t mid) {
   if (a.R == 0) return MOE_OK;
-  const bool fp8 = a.w_dtype == MOE_FP8_E4M3;
+  const bool act8 = a.w_dtype == MOE_FP8_E4M3_ACT8;
+  const bool fp8 = a.w_dtype == MOE_FP8_E4M3 || act8;
   if (!fp8 && a.w_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   if (fp8 && (a.s_gate == nullptr || a.s_up == nullptr || a.s_down == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (act8 && a.row_scale == nullptr) return MOE_ERR_INVALID_ARG;
+  const int wf_gu = act8 ? kWFp8Act8 : fp8 ? kWFp8 : kWBf16;
   if (a.d % kBM != 0 || a.ffn % kBM != 0 || a.G > kMaxGroups) return MOE_ERR_UNSUPPORTED;
   // weights: bf16 tiles [128 x 64] with 128-byte swizzle, or E4M3 tiles
   // [128 x 64 bytes] staged unswizzled for the converters
@@ -1120,10 +1178,12 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   // E4M3 staging for the tensor-memory operand path (decode tiles): boxes
   // 128 bytes wide with the 128-byte swizzle its converters read
   // conflict-free
-  const bool ta_gu = ta_config(kGateUp, plan.bn_gateup, fp8, plan.pair_gateup != 0);
+  // FP8 activations: E4M3 weight and row tiles straight into the MMA's
+  // 128-byte-swizzled operands, 128 elements of K per row
+  const bool ta_gu = ta_config(kGateUp, plan.bn_gateup, fp8 && !act8, plan.pair_gateup != 0);
   const bool ta_dn = ta_config(kDown, plan.bn_down, fp8, plan.pair_down != 0);
-  const int wsw_gu = !fp8 || ta_gu ? 128 : 0, wsw_dn = !fp8 || ta_dn ? 128 : 0;
-  const int wk_gu = ta_gu ? 2 * kBK : kBK, wk_dn = ta_dn ? 2 * kBK : kBK;
+  const int wsw_gu = !fp8 || ta_gu || act8 ? 128 : 0, wsw_dn = !fp8 || ta_dn ? 128 : 0;
+  const int wk_gu = ta_gu || act8 ? 2 * kBK : kBK, wk_dn = ta_dn ? 2 * kBK : kBK;
   CUtensorMap wg, wu, xb, wd, hb;
   MOE_TRY(make_tmap_2d(&wg, a.w_gate, (uint64_t)a.G * a.ffn, a.d, wb, kBM, wk_gu, wsw_gu));
   MOE_TRY(make_tmap_2d(&wu, a.w_up, (uint64_t)a.G * a.ffn, a.d, wb, kBM, wk_gu, wsw_gu));
@@ -1133,10 +1193,12 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   // producer warp for prefill tiles (gather4 costs a copy per 4 rows)
   const bool lsu = a.gather_rows != nullptr && (plan.bn_gateup >= 128 || plan.pair_gateup);
   if (plan.pair_gateup && a.gather_rows != nullptr && !lsu) return MOE_ERR_UNSUPPORTED;
+  // row operand: 128-byte rows, 64 16-bit elements or 128 E4M3 codes
+  const int xe = act8 ? 1 : 2, xk = act8 ? 2 * kBK : kBK;
   if (a.gather_rows != nullptr)  // token rows by index: one-row boxes for gather4
-    MOE_TRY(make_tmap_2d(&xb, a.x_src, a.T_src, a.d, 2, 1, kBK, 128));
+    MOE_TRY(make_tmap_2d(&xb, a.x_src, a.T_src, a.d, xe, 1, xk, 128));
   else
-    MOE_TRY(make_tmap_2d(&xb, a.x_perm, a.R, a.d, 2, box_gu, kBK, 128));
+    MOE_TRY(make_tmap_2d(&xb, a.x_perm, a.R, a.d, xe, box_gu, xk, 128));
   // bf16 down GEMM on pairs: 3-D maps, one copy per operand and stage (its
   // B rows in one box: all BN/2 rows of the CTA)
   const bool k2_dn = !fp8 && plan.pair_down;
@@ -1173,9 +1235,11 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   p.lsu_gather = lsu ? 1 : 0;
   p.x_src = a.x_src;
   p.d_src = a.d;
-  MOE_TRY(launch_mode<kGateUp>(plan.bn_gateup, fp8, plan.pair_gateup != 0, p, wg, wu, xb, plan.grid, s));
+  p.row_scale = act8 ? a.row_scale : nullptr;
+  MOE_TRY(launch_mode<kGateUp>(plan.bn_gateup, wf_gu, plan.pair_gateup != 0, p, wg, wu, xb, plan.grid, s));
   p.gather_rows = nullptr;
   p.lsu_gather = 0;
+  p.row_scale = nullptr;
   p.tile_cnt = nullptr;
   p.fin_out = nullptr;
   if (gu_split && !gu_fused) {
@@ -1199,7 +1263,7 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   p.scale0 = a.s_down;
   p.scale1 = nullptr;
   p.boxn = k2_dn ? plan.bn_down / 2 : box_dn;
-  MOE_TRY(launch_mode<kDown>(plan.bn_down, fp8, plan.pair_down != 0, p, wd, wd, hb, plan.grid, s));
+  MOE_TRY(launch_mode<kDown>(plan.bn_down, fp8 ? kWFp8 : kWBf16, plan.pair_down != 0, p, wd, wd, hb, plan.grid, s));
   return MOE_OK;
 }
 
@@ -1230,7 +1294,7 @@ moe_status tc_dense_f32_launch(const void* a, const void* b, float* out, int M, 
   p.status = status;
   p.timeout_ns = timeout_ns;
   p.boxn = kBoxLarge;
-  return launch_mode<kDown>(128, false, false, p, ta, ta, tb, num_sms, s);
+  return launch_mode<kDown>(128, kWBf16, false, p, ta, ta, tb, num_sms, s);
 }
 
 moe_status tc_selftest_launch(int* status, long long timeout_ns, cudaStream_t s) {
@@ -1246,7 +1310,7 @@ moe_status tc_selftest_launch(int* status, long long timeout_ns, cudaStream_t s)
   p.timeout_ns = timeout_ns;
   p.selftest = 1;
   p.boxn = kBoxSmall;
-  return launch_one<kGateUp, 32, false>(p, dummy, dummy, dummy, 1, s);
+  return launch_one<kGateUp, 32, kWBf16>(p, dummy, dummy, dummy, 1, s);
 }
 
 }  // namespace moe

@@ -1,0 +1,81 @@
+// Per-row E4M3 quantisation of token rows for the FP8-activation mode of
+// the routed experts' gate/up GEMM ("MOE推理流程解析", section 三: the
+// activations may be quantised before dispatch, so the permuted rows carry
+// fewer bytes; "MoE 推理部署", section 专家量化: FP8 inference).
+//
+// Row t of x [rows, d] (bf16) becomes
+//   s_t     = max_i |x[t,i]| / 448     (1 for an all-zero row)
+//   q[t,i]  = E4M3(x[t,i] / s_t)       round to nearest, ties to even,
+//                                      magnitudes past 448 saturate to 448
+// with both divisions correctly rounded in fp32, so that the codes are a
+// function of the stored inputs alone.
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kQThreads = 128;
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+}
+
+// One CTA per row (grid-stride over rows); each thread takes 8 elements
+// (16 bytes) at a time.  Pass 1 finds the row's absolute maximum, pass 2
+// re-reads the row (L1/L2-resident: at most a few tens of KB) and writes the
+// codes, 8 bytes per thread.
+__global__ void __launch_bounds__(kQThreads) quantize_rows_e4m3_kernel(const uint4* __restrict__ x, int rows,
+                                                                       int vpr, uint2* __restrict__ codes,
+                                                                       float* __restrict__ scales) {
+  griddep_begin();
+  __shared__ float red[kQThreads / 32];
+  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+    const uint4* xr = x + (size_t)r * vpr;
+    float m = 0.f;
+    for (int v = threadIdx.x; v < vpr; v += kQThreads) {
+      const uint4 q = xr[v];
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    float amax = red[0];
+#pragma unroll
+    for (int i = 1; i < kQThreads / 32; ++i) amax = fmaxf(amax, red[i]);
+    const float s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+    if (threadIdx.x == 0) scales[r] = s;
+    uint2* cr = codes + (size_t)r * vpr;
+    for (int v = threadIdx.x; v < vpr; v += kQThreads) {
+      const uint4 q = xr[v];
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+      uint32_t c[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) c[i] = e4m3x2(__fdiv_rn(bf16_lo(w[i]), s), __fdiv_rn(bf16_hi(w[i]), s));
+      cr[v] = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+    }
+    __syncthreads();  // red[] is rewritten by the next row
+  }
+}
+
+}  // namespace
+
+moe_status quantize_rows_e4m3_launch(const void* x, int rows, int d, void* codes, float* scales,
+                                     int num_sms, cudaStream_t s) {
+  if (rows == 0) return MOE_OK;
+  if (rows < 0 || d <= 0 || d % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  const int blocks = rows < 16 * num_sms ? rows : 16 * num_sms;
+  MOE_TRY_CUDA(launch_k(quantize_rows_e4m3_kernel, dim3(blocks), dim3(kQThreads), 0, s,
+                        static_cast<const uint4*>(x), rows, d / 8, static_cast<uint2*>(codes), scales));
+  MOE_TRY_CUDA(cudaGetLastError());
+  return MOE_OK;
+}
+
+}  // namespace moe

@@ -41,7 +41,8 @@ class MoEShape:
     k: int
     ffn_shared: int = 0
     act: str = "bf16"          # "f32" | "bf16"
-    wfmt: str = "bf16"         # "f32" | "bf16" | "fp8"
+    # "f32" | "bf16" | "fp8" | "fp8a8" (FP8 weights, FP8 gate/up activations)
+    wfmt: str = "bf16"
     router_bias: str = "none"  # "none" | "zipf"
     zipf_s: float = 1.2
 
@@ -129,7 +130,7 @@ def _expert_stack(shape: MoEShape, rows: int, cols: int, seed: int, name: str, d
     that large layers never hold an fp32 copy of the whole stack."""
     std = 1.0 / math.sqrt(shape.d)
     E = shape.E
-    if shape.wfmt == "fp8":
+    if shape.wfmt in ("fp8", "fp8a8"):
         w = torch.empty((E, rows, cols), dtype=torch.uint8, device=device)
         s = torch.empty((E, rows), dtype=torch.float32, device=device)
         for e in range(E):

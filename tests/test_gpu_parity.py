@@ -375,7 +375,7 @@ def _layer_check(shape, seed, tol, tokens=None, clear_gap=1e-3):
     sel = np.arange(shape.T) if tokens is None else np.asarray(tokens)
     ref, _, _ = oracle.moe_forward_per_token(x, wr, ew, shape.k, bias=b, shared=sh,
                                              routing=(idx_g, w.cpu().numpy().astype(np.float64)),
-                                             tokens=sel)
+                                             tokens=sel, act8=shape.wfmt == "fp8a8")
     got = helpers.decode_act(out, shape.act)[sel]
     assert np.isfinite(got).all()
     err = np.abs(got - ref).max()
@@ -488,29 +488,31 @@ def test_layer_forward_captured_in_a_cuda_graph_with_stage_timer():
 
 @pytest.mark.parametrize("splits,bn,d,pair", [(1, 0, 512, 0), (3, 0, 512, 0), (8, 0, 512, 0), (3, 256, 512, 0),
                                                (8, 0, 640, 0), (3, 0, 512, 1), (8, 0, 512, 1)])
-@pytest.mark.parametrize("wfmt", ["bf16", "fp8"])
+@pytest.mark.parametrize("wfmt", ["bf16", "fp8", "fp8a8"])
 def test_layer_gateup_split_k(splits, bn, d, pair, wfmt, monkeypatch):
     # the gate/up GEMM split along its reduction: fp32 partials, then an
     # in-order sum and SiLU*mul pass (chosen automatically at tiny batches);
     # bn=256 forces the 256-row tile through the same partials; ceil-sized
     # splits can leave the last ones without k-blocks (d=640 in 64-element
     # blocks over 8 splits, d=512 in the 128-element FP8 decode blocks)
+    if pair and wfmt != "fp8":
+        pytest.skip("decode tiles run on CTA pairs with FP8 weights and f16 activations only")
     monkeypatch.setenv("MOE_SPLITS_GATEUP", str(splits))
     monkeypatch.setenv("MOE_PAIR", str(2 * pair))  # 2: FP8 decode tiles on CTA pairs
     if bn:
         monkeypatch.setenv("MOE_BN_GATEUP", str(bn))
-    shape = inputs.MoEShape("small", T=5, d=d, ffn=256, E=16, k=4, ffn_shared=256 if wfmt == "fp8" else 0,
+    shape = inputs.MoEShape("small", T=5, d=d, ffn=256, E=16, k=4, ffn_shared=256 if wfmt != "bf16" else 0,
                             wfmt=wfmt)
     info = api.moe_plan_info(api.problem_of(shape))
     assert info["splits_gateup"] == splits
     # FP8 decode tiles run on CTA pairs (split-K partials and the fused
     # finalize per CTA of the pair); bf16 decode tiles stay on single CTAs
     assert info["pair_gateup"] == (pair if wfmt == "fp8" and not bn else 0)
-    _layer_check(shape, 4, FP8_TOL if wfmt == "fp8" else BF16_TOL)
+    _layer_check(shape, 4, FP8_TOL if wfmt != "bf16" else BF16_TOL)
 
 
 @pytest.mark.parametrize("bn,pair", [(128, 0), (128, 1), (256, 0), (256, 1)])
-@pytest.mark.parametrize("wfmt", ["bf16", "fp8"])
+@pytest.mark.parametrize("wfmt", ["bf16", "fp8", "fp8a8"])
 def test_layer_gathered_rows_every_tile(bn, pair, wfmt, monkeypatch):
     # the gate/up GEMM gathers its token rows (cp.async by the producer warp
     # for tiles of >= 128 rows), on single CTAs and on CTA pairs, with groups
@@ -520,10 +522,10 @@ def test_layer_gathered_rows_every_tile(bn, pair, wfmt, monkeypatch):
     monkeypatch.setenv("MOE_PAIR", str(pair))
     monkeypatch.setenv("MOE_SPLITS_GATEUP", "1")  # (pairs take unsplit gate/up GEMMs)
     shape = inputs.MoEShape("gathered", T=300, d=512, ffn=512, E=8, k=2, wfmt=wfmt,
-                            ffn_shared=256 if wfmt == "fp8" else 0)
+                            ffn_shared=256 if wfmt != "bf16" else 0)
     info = api.moe_plan_info(api.problem_of(shape))
     assert (info["bn_gateup"], info["pair_gateup"]) == (bn, pair)
-    _layer_check(shape, 3, FP8_TOL if wfmt == "fp8" else BF16_TOL)
+    _layer_check(shape, 3, FP8_TOL if wfmt != "bf16" else BF16_TOL)
 
 
 def test_layer_empty_batch():
@@ -561,6 +563,7 @@ def test_bounded_wait_expires_cleanly_and_context_survives():
     inputs.WORKLOADS["toy_f32"],                                    # CUDA-core path
     inputs.WORKLOADS["qwen3_30b_a3b"].with_T(1),                    # fused top-k, split-K gate/up
     inputs.MoEShape("ds_small", T=2, d=1024, ffn=512, E=64, k=8, ffn_shared=512, wfmt="fp8"),
+    inputs.MoEShape("ds_small_act8", T=2, d=1024, ffn=512, E=64, k=8, ffn_shared=512, wfmt="fp8a8"),
     inputs.MoEShape("chunked", T=400, d=256, ffn=256, E=32, k=8),   # chunked permutation
 ], ids=lambda s: s.name)
 def test_layer_launch_count_matches_the_kernels_launched(shape):
