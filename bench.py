@@ -56,6 +56,9 @@ def parse_args():
     ap.add_argument("--act8", action="store_true",
                     help="FP8-weight workloads: the routed gate/up GEMM takes the token rows "
                          "quantised per row to E4M3 (FP8 x FP8 tensor-core instructions)")
+    ap.add_argument("--mxfp4", action="store_true",
+                    help="FP8-weight workloads: the routed experts in OCP MXFP4 instead (E2M1 codes, "
+                         "one UE8M0 scale per 32 weights)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--weight-sets", type=int, default=0,
                     help="independent weight sets rotated per step (0: enough to exceed L2)")
@@ -82,7 +85,8 @@ def load_peaks():
 
 
 def wbytes(shape):
-    return {"f32": 4, "bf16": 2, "fp8": 1, "fp8a8": 1}[shape.wfmt]
+    # (MXFP4: half a byte of code and 1/32 byte of scale per weight)
+    return {"f32": 4, "bf16": 2, "fp8": 1, "fp8a8": 1, "mxfp4": 17 / 32}[shape.wfmt]
 
 
 def abytes(shape):
@@ -227,7 +231,10 @@ def _oracle_session(shape, seed):
     b = f64(case["router_bias"])
     decoded = {}
     for e in range(shape.E):
-        if shape.wfmt in ("fp8", "fp8a8"):
+        if shape.wfmt == "mxfp4":
+            decoded[e] = tuple(oracle.decode_mxfp4(case[w][e].numpy(), case[s][e].numpy())
+                               for w, s in (("w_gate", "s_gate"), ("w_up", "s_up"), ("w_down", "s_down")))
+        elif shape.wfmt in ("fp8", "fp8a8"):
             def dq(w, s):
                 return (w[e].view(torch.float8_e4m3fn).to(torch.float64) * s[e].to(torch.float64)[:, None]).numpy()
             decoded[e] = (dq(case["w_gate"], case["s_gate"]), dq(case["w_up"], case["s_up"]),
@@ -524,7 +531,8 @@ def run_ours(args, shape, ws, rank, local):
             "metric": "moe_layer_tokens_per_s", "value": value, "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": ("fp8" if shape.wfmt == "fp8a8" else "bf16") if shape.act == "bf16" else "f32",
+            "dtype": {"fp8a8": "fp8", "fp8": "f16", "mxfp4": "f16"}.get(shape.wfmt, "bf16")
+                     if shape.act == "bf16" else "f32",
             "data": "synthetic",
             "config": workload_config(shape, {
                 "l2": (f"inputs larger than L2: {touched * 3 * shape.ffn * shape.d * wbytes(shape) / 1e9:.2f} GB "
@@ -556,10 +564,13 @@ def main():
         if not shape.k <= args.E:
             raise SystemExit("--E must be at least the workload's top-k")
         shape = dataclasses.replace(shape, E=args.E)
-    if args.act8:
+    if args.act8 and args.mxfp4:
+        raise SystemExit("--act8 and --mxfp4 are separate weight modes")
+    if args.act8 or args.mxfp4:
         if shape.wfmt != "fp8":
-            raise SystemExit("--act8 needs a workload with FP8 expert weights")
-        shape = dataclasses.replace(shape, name=shape.name + "_act8", wfmt="fp8a8")
+            raise SystemExit("--act8 / --mxfp4 need a workload with FP8 expert weights")
+        shape = (dataclasses.replace(shape, name=shape.name + "_act8", wfmt="fp8a8") if args.act8 else
+                 dataclasses.replace(shape, name=shape.name + "_mxfp4", wfmt="mxfp4"))
     ws, rank, local = dist_setup(args)
     if args.impl == "reference":
         return run_reference(args, shape, ws, rank)

@@ -53,6 +53,21 @@
  *                                        sum_i q[r,i] * code_gate[e][o,i]
  *                               (likewise u).  The down GEMM, router and
  *                               shared expert are as for MOE_FP8_E4M3.
+ *   MOE_BF16 / MOE_MXFP4        OCP Microscaling FP4 weights ("MoE 推理部署",
+ *                               section 专家量化: MXFP4 block-scaled 4-bit
+ *                               experts): W[o,i] = E2M1(code[o,i]) *
+ *                               2^(s[i/32,o] - 127).  w_gate / w_up
+ *                               [E, ffn, d/2] and w_down [E, d, ffn/2] bytes,
+ *                               two codes per byte (element 2i in the low
+ *                               nibble of byte i); s_gate / s_up [E, d/32,
+ *                               ffn] and s_down [E, ffn/32, d] UE8M0 bytes,
+ *                               reduction-block-major (a k-block's scales of
+ *                               all output channels contiguous), passed
+ *                               through the float* scale parameters.  The
+ *                               kernels convert to f16 operands, exactly for
+ *                               block scales 2^-23 .. 2^13 (UE8M0 104..140);
+ *                               larger scales overflow f16 and are not
+ *                               supported.  Router and shared expert bf16.
  * Size limits: 1 <= k <= min(E, 32), E <= 1024, d % 8 == 0, ffn % 8 == 0;
  * the tensor-core path further needs d % 128 == 0, ffn % 128 == 0 and
  * ffn_shared % 128 == 0.
@@ -85,7 +100,9 @@ typedef enum moe_dtype {
   /* w_dtype only: FP8 weights as MOE_FP8_E4M3, and the routed experts'
    * gate/up products take the token rows quantised per row to E4M3
    * (moe_quantize_rows_e4m3) on FP8 x FP8 tensor-core instructions */
-  MOE_FP8_E4M3_ACT8 = 3
+  MOE_FP8_E4M3_ACT8 = 3,
+  /* w_dtype only: OCP MXFP4 routed expert weights (see "Supported storage") */
+  MOE_MXFP4 = 4
 } moe_dtype;
 
 typedef enum moe_status {

@@ -27,6 +27,11 @@ Parity status per function (what pins each one is listed in the tests):
   quantize_rows_e4m3 /              pinned (scale = row max / 448 hits code
   dequantize_rows_e4m3              0x7E; lossless on E4M3-representable
                                     rows; zero rows)
+  decode_e2m1, decode_ue8m0,        pinned (the OCP MX element and scale
+  unpack_fp4, decode_mxfp4          definitions at fixed codes, the page's
+                                    storage figure for a 117B-parameter model,
+                                    a hand-decoded block, nibble order and
+                                    scale layout by construction)
 """
 
 from .moe_oracle import (  # noqa: F401
@@ -46,4 +51,8 @@ from .moe_oracle import (  # noqa: F401
     round_to_e4m3,
     quantize_rows_e4m3,
     dequantize_rows_e4m3,
+    decode_e2m1,
+    decode_ue8m0,
+    unpack_fp4,
+    decode_mxfp4,
 )

@@ -31,6 +31,11 @@ design notes of the repository):
 * FP8 weights are OCP E4M3 ("fn": max 448, no infinities) times a per-expert,
   per-output-channel fp32 scale ("MoE 推理部署", section 专家量化: scales are
   per expert).
+* MXFP4 weights follow the OCP Microscaling (MX) format that the same
+  section names: blocks of 32 consecutive weights along the reduction index
+  share one UE8M0 scale 2^(s-127), each weight an FP4 E2M1 code; two codes
+  per byte, the even element in the low nibble; the scales of an expert
+  matrix stored reduction-block-major, [K/32, rows].
 
 Everything is computed in float64 from the exact stored input values.
 """
@@ -101,6 +106,57 @@ with np.errstate(invalid="ignore"):
     _E4M3_TABLE = _e4m3_formula(np.arange(1 << 8))
 
 
+def _e2m1_formula(code) -> np.ndarray:
+    c = np.asarray(code).astype(np.int64) & 0xF
+    sign = np.where((c >> 3) & 1, -1.0, 1.0)
+    exp = (c >> 1) & 0x3
+    frac = (c & 0x1).astype(F64)
+    normal = sign * np.ldexp(1.0 + frac / 2.0, (exp - 1).astype(np.int64))
+    sub = sign * (frac / 2.0)
+    return np.where(exp == 0, sub, normal).astype(F64)
+
+
+_E2M1_TABLE = _e2m1_formula(np.arange(16))
+
+
+def decode_e2m1(codes) -> np.ndarray:
+    """OCP FP4 E2M1 codes (0..15) -> float64.
+
+    1 sign bit, 2 exponent bits (bias 1), 1 fraction bit; exponent 0 encodes
+    zero and the subnormal 0.5.  No infinities or NaN: the magnitudes are
+    0, 0.5, 1, 1.5, 2, 3, 4, 6.  Evaluated once for the 16 codes."""
+    return _E2M1_TABLE[np.asarray(codes).astype(np.int64) & 0xF]
+
+
+def decode_ue8m0(s) -> np.ndarray:
+    """OCP UE8M0 scale bytes -> float64: 2^(s - 127); 0xFF is NaN."""
+    b = np.asarray(s).astype(np.int64) & 0xFF
+    with np.errstate(invalid="ignore"):
+        return np.where(b == 0xFF, np.nan, np.ldexp(1.0, b - 127)).astype(F64)
+
+
+def unpack_fp4(packed) -> np.ndarray:
+    """[..., n/2] bytes -> [..., n] FP4 codes: byte i holds element 2i in its
+    low nibble and element 2i+1 in its high nibble."""
+    b = np.asarray(packed).astype(np.uint8)
+    out = np.empty(b.shape[:-1] + (2 * b.shape[-1],), dtype=np.uint8)
+    out[..., 0::2] = b & 0xF
+    out[..., 1::2] = b >> 4
+    return out
+
+
+def decode_mxfp4(packed, scales) -> np.ndarray:
+    """One MXFP4 matrix -> float64 [rows, K]: packed codes [rows, K/2],
+    scales [K/32, rows] (one UE8M0 byte per 32 consecutive weights of a row):
+    w[o, i] = decode_e2m1(code[o, i]) * decode_ue8m0(scale[i // 32, o])."""
+    codes = unpack_fp4(packed)
+    K = codes.shape[-1]
+    if K % 32:
+        raise ValueError("MXFP4 rows hold whole 32-element blocks")
+    per_elem = np.repeat(decode_ue8m0(scales), 32, axis=0)  # [K, rows]
+    return decode_e2m1(codes) * per_elem.T
+
+
 def _to_f64(arr, fmt: str) -> np.ndarray:
     if fmt == "f32":
         return np.asarray(arr, dtype=np.float32).astype(F64)
@@ -116,9 +172,12 @@ class ExpertWeights:
 
     Layout (output-major, the reduction index contiguous):
       w_gate, w_up : [E, ffn, d]      w_down : [E, d, ffn]
-    ``fmt`` is "f32" (float32 arrays), "bf16" (uint16 bit patterns) or
+    ``fmt`` is "f32" (float32 arrays), "bf16" (uint16 bit patterns),
     "fp8" (uint8 E4M3 codes with fp32 scales s_gate, s_up [E, ffn] and
-    s_down [E, d]: weight = decode_e4m3(code) * scale[e, output_channel]).
+    s_down [E, d]: weight = decode_e4m3(code) * scale[e, output_channel]) or
+    "mxfp4" (packed FP4 codes w_gate, w_up [E, ffn, d/2], w_down [E, d,
+    ffn/2] with UE8M0 block scales s_gate, s_up [E, d/32, ffn], s_down
+    [E, ffn/32, d]: decode_mxfp4 per expert matrix).
     """
 
     def __init__(self, fmt, w_gate, w_up, w_down, s_gate=None, s_up=None, s_down=None):
@@ -126,8 +185,8 @@ class ExpertWeights:
         self.w_gate, self.w_up, self.w_down = w_gate, w_up, w_down
         self.s_gate, self.s_up, self.s_down = s_gate, s_up, s_down
         self.E = int(np.shape(w_gate)[0])
-        if fmt == "fp8" and (s_gate is None or s_up is None or s_down is None):
-            raise ValueError("fp8 expert weights need per-output-channel scales")
+        if fmt in ("fp8", "mxfp4") and (s_gate is None or s_up is None or s_down is None):
+            raise ValueError(f"{fmt} expert weights need their scales")
 
     def get(self, e: int) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
         if self.fmt == "fp8":
@@ -135,6 +194,9 @@ class ExpertWeights:
             wu = decode_e4m3(self.w_up[e]) * np.asarray(self.s_up[e], F64)[:, None]
             wd = decode_e4m3(self.w_down[e]) * np.asarray(self.s_down[e], F64)[:, None]
             return wg, wu, wd
+        if self.fmt == "mxfp4":
+            return (decode_mxfp4(self.w_gate[e], self.s_gate[e]), decode_mxfp4(self.w_up[e], self.s_up[e]),
+                    decode_mxfp4(self.w_down[e], self.s_down[e]))
         return (_to_f64(self.w_gate[e], self.fmt), _to_f64(self.w_up[e], self.fmt),
                 _to_f64(self.w_down[e], self.fmt))
 

@@ -19,8 +19,9 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmoe_gb300.so")
 
-# "fp8a8": FP8 weights with FP8 (per-row E4M3) gate/up activations
-DTYPE = {"f32": 0, "bf16": 1, "fp8": 2, "fp8a8": 3}
+# "fp8a8": FP8 weights with FP8 (per-row E4M3) gate/up activations;
+# "mxfp4": OCP MX 4-bit block-scaled weights
+DTYPE = {"f32": 0, "bf16": 1, "fp8": 2, "fp8a8": 3, "mxfp4": 4}
 OK = 0
 ERR_INVALID_ARG = -1
 ERR_UNSUPPORTED = -2

@@ -27,7 +27,7 @@ moe_status check_problem(const moe_problem* p, Path* path) {
   if (p->act_dtype == MOE_F32 && p->w_dtype == MOE_F32) {
     *path = Path::kSimt;
   } else if (p->act_dtype == MOE_BF16 && (p->w_dtype == MOE_BF16 || p->w_dtype == MOE_FP8_E4M3 ||
-                                          p->w_dtype == MOE_FP8_E4M3_ACT8)) {
+                                          p->w_dtype == MOE_FP8_E4M3_ACT8 || p->w_dtype == MOE_MXFP4)) {
     if (p->d % 128 != 0 || p->ffn % 128 != 0 || p->ffn_shared % 128 != 0) return MOE_ERR_UNSUPPORTED;
     *path = Path::kTensor;
   } else {
@@ -38,7 +38,10 @@ moe_status check_problem(const moe_problem* p, Path* path) {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-bool fp8_weights(int w_dtype) { return w_dtype == MOE_FP8_E4M3 || w_dtype == MOE_FP8_E4M3_ACT8; }
+// Quantised routed weights (FP8 or MXFP4): scale arrays required, f16 operands.
+bool fp8_weights(int w_dtype) {
+  return w_dtype == MOE_FP8_E4M3 || w_dtype == MOE_FP8_E4M3_ACT8 || w_dtype == MOE_MXFP4;
+}
 
 struct Layout {
   size_t idx, w, logits, counts, offsets, perm_token, inv_row, chunk, x_perm, x_scale, h, y;
@@ -86,7 +89,8 @@ Layout layout(const moe_problem& p, Path path, int num_sms, bool allow_splits) {
   const bool gather = path == Path::kTensor;
   const bool act8 = p.w_dtype == MOE_FP8_E4M3_ACT8;
   L.gather = gather;
-  L.x_perm = take(gather ? (p.w_dtype == MOE_FP8_E4M3 ? T * d * 2 : act8 ? T * d : 0) : R * d * ab);
+  const bool f16x = p.w_dtype == MOE_FP8_E4M3 || p.w_dtype == MOE_MXFP4;
+  L.x_perm = take(gather ? (f16x ? T * d * 2 : act8 ? T * d : 0) : R * d * ab);
   L.x_scale = take(act8 ? T * 4 : 0);
   L.h = take(R * f * ab);
   const size_t S = path == Path::kTensor ? (size_t)L.plan.splits_down : 1;

@@ -131,14 +131,18 @@ __host__ __device__ constexpr bool ta_config(int mode, int bn, bool fp8, bool pa
 
 // Weight formats of the kernel: bf16; FP8 weights converted to f16 for a
 // kind::f16 MMA ("w8a16"); FP8 weights multiplied by FP8 token rows with a
-// kind::f8f6f4 MMA (gate/up only: the FP8-activation mode).
-enum { kWBf16 = 0, kWFp8 = 1, kWFp8Act8 = 2 };
+// kind::f8f6f4 MMA (gate/up only: the FP8-activation mode); MXFP4 weights
+// (E2M1 codes with a UE8M0 scale per 32 along K) converted to f16 for a
+// kind::f16 MMA.
+enum { kWBf16 = 0, kWFp8 = 1, kWFp8Act8 = 2, kWMx4 = 3 };
 
 template <int MODE, int BN, int WF, bool PAIR>
 struct Cfg {
-  static constexpr bool FP8 = WF != kWBf16;     // E4M3 weights, per-channel scales
-  static constexpr bool A8 = WF == kWFp8Act8;   // ... times E4M3 token rows (kind::f8f6f4)
-  static constexpr bool CONV = WF == kWFp8;     // converter warps turn E4M3 into f16
+  static constexpr bool FP8 = WF != kWBf16;     // quantised weights: staged, f16 h (or E4M3 rows)
+  static constexpr bool A8 = WF == kWFp8Act8;   // E4M3 weights times E4M3 token rows (kind::f8f6f4)
+  static constexpr bool MX4 = WF == kWMx4;      // MXFP4 weights (block scales applied by the converters)
+  static constexpr bool CHS = FP8 && !MX4;      // per-output-channel weight scales in the epilogue
+  static constexpr bool CONV = WF == kWFp8 || MX4;  // converter warps write f16 weight operands
   // PAIR: a CTA pair (cluster of 2) runs one unit with cta_group::2 MMAs:
   // M = 256 output channels (128 per CTA, each CTA's TMEM holding its own
   // 128 accumulator rows for all N columns) and each CTA staging half of
@@ -156,7 +160,7 @@ struct Cfg {
   // bf16 down GEMM on pairs: 128 elements of K per stage as well, A and B
   // each in ONE copy (3-D boxes of two 64-element column blocks): half the
   // copies and half the barrier round trips per byte of a 64-element stage
-  static constexpr bool K2 = MODE == kDown && PAIR && !FP8;
+  static constexpr bool K2 = MODE == kDown && PAIR && !FP8;     // (bf16 weights only)
   // FP8 activations: 128 elements of K per stage too, in single 128-byte
   // rows for both operands (one sub-tile); kind::f8f6f4 takes K = 32 per
   // instruction
@@ -166,7 +170,10 @@ struct Cfg {
   static constexpr int A_BYTES = kBM * kBK * 2;                // 16 KB bf16 tile (MMA operand)
   static constexpr int BSUB_BYTES = (PAIR ? BN / 2 : BN) * kBK * 2;
   static constexpr int B_BYTES = NSUB * BSUB_BYTES;
-  static constexpr int STG_BYTES = FP8 ? kBM * KB : 0;         // E4M3 staging tile (8 or 16 KB)
+  // staged weight codes: E4M3 (8 or 16 KB), or packed E2M1 (half that)
+  // followed by the UE8M0 block scales, KB/32 runs of 128 bytes
+  static constexpr int STG_BYTES = FP8 ? (MX4 ? kBM * KB / 2 : kBM * KB) : 0;
+  static constexpr int SCL_BYTES = MX4 ? KB / 32 * kBM : 0;
   // bf16: one ring of TMA slots [A0 A1 | B] read by the MMA.  FP8: a deep
   // ring of TMA slots [E4M3 A0 A1 | B] (cheap bytes: it hides HBM latency)
   // and a short ring of OSTAGES f16 operand slots [A0 A1] that the
@@ -175,7 +182,7 @@ struct Cfg {
   // (a commit round trip per slot otherwise serialises decode), while the
   // TMA ring keeps at least 4 slots
   static constexpr int OPND_BYTES = TA || !CONV ? 0 : NA * A_BYTES;
-  static constexpr int W_BYTES_ = FP8 ? STG_BYTES : NSUB * A_BYTES;
+  static constexpr int W_BYTES_ = FP8 ? STG_BYTES + SCL_BYTES : NSUB * A_BYTES;
   static constexpr int SLOT_ = NA * W_BYTES_ + B_BYTES;
   static constexpr int AVAIL_ = kSmemLimit - 1024 - (8 * 40 + 16 + 4 * 2 * (kMaxGroups + 8));
   // TMEM: one accumulator buffer = NA accumulators of max(BN,128) columns;
@@ -191,11 +198,11 @@ struct Cfg {
                                  : (AVAIL_ - 6 * SLOT_) / (NA * A_BYTES) >= 4 ? 4
                                  : (AVAIL_ - 6 * SLOT_) / (NA * A_BYTES) >= 3 ? 3 : 2;
   static constexpr int RING_OFF = OSTAGES * OPND_BYTES;
-  static constexpr int W_BYTES = FP8 ? STG_BYTES : NSUB * A_BYTES;  // weight tile bytes in a TMA slot
+  static constexpr int W_BYTES = W_BYTES_;                      // weight tile bytes in a TMA slot
   // distance between the A matrices where the MMA reads them (TMA slot, or
   // FP8 operand slot)
   static constexpr int A_STRIDE = CONV ? A_BYTES : W_BYTES;
-  static constexpr int B_OFF = NA * W_BYTES;
+  static constexpr int B_OFF = (NA * W_BYTES + 1023) / 1024 * 1024;  // B keeps the 128-byte swizzle's alignment
   static constexpr int STAGE_BYTES = B_OFF + B_BYTES;           // multiple of 1024
   static constexpr int THREADS = kThreads + (CONV ? kConvThreads : 0);
   static constexpr int TAIL_BYTES = 8 * 40 + 16 + 4 * 2 * (kMaxGroups + 8);
@@ -280,11 +287,48 @@ __device__ __forceinline__ uint4 e4m3x8_to_f16x8(uint32_t lo, uint32_t hi) {
   return r;
 }
 
+// MXFP4: the f16 pair multiplier 2^(s - 127) of a UE8M0 block scale s
+// (exact f16 for s in [103, 142]: subnormal below 2^-14; the products
+// code * 2^(s-127) are exact f16 values for s in [104, 140]).
+__device__ __forceinline__ uint32_t ue8m0_to_f16x2(uint32_t s) {
+  const int e = (int)s - 127;
+  const uint32_t h = e >= -14 ? (e <= 15 ? (uint32_t)(e + 15) << 10 : 0x7C00u)
+                              : (e >= -24 ? 1u << (e + 24) : 0u);
+  return h | (h << 16);
+}
+
+// Eight E2M1 codes (one 32-bit word, element 2i in the low nibble of byte
+// i) -> eight f16 (four pairs, the lower element in the low half), each
+// times the block's multiplier m2: one hardware conversion per code pair
+// (exact: every E2M1 value is an f16 value) and one f16x2 multiply by a
+// power of two.
+__device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t v, uint32_t m2, uint32_t* w) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t.reg .b32 h0, h1, h2, h3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 h0, b0;\n\tcvt.rn.f16x2.e2m1x2 h1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 h2, b2;\n\tcvt.rn.f16x2.e2m1x2 h3, b3;\n\t"
+      "mul.rn.f16x2 %0, h0, %5;\n\tmul.rn.f16x2 %1, h1, %5;\n\t"
+      "mul.rn.f16x2 %2, h2, %5;\n\tmul.rn.f16x2 %3, h3, %5;\n\t}"
+      : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+      : "r"(v), "r"(m2));
+}
+
+// One 32-element MXFP4 block (16 bytes of codes) -> 32 f16 in w[0..15].
+__device__ __forceinline__ void e2m1x32_to_f16(const uint4& v, uint32_t m2, uint32_t* w) {
+  e2m1x8_to_f16x8(v.x, m2, w);
+  e2m1x8_to_f16x8(v.y, m2, w + 4);
+  e2m1x8_to_f16x8(v.z, m2, w + 8);
+  e2m1x8_to_f16x8(v.w, m2, w + 12);
+}
+
 template <int MODE, int BN, int WF, bool PAIR>
 __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
     tc_grouped_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmA0,
                       const __grid_constant__ CUtensorMap tmA1,
-                      const __grid_constant__ CUtensorMap tmB) {
+                      const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmS0,
+                      const __grid_constant__ CUtensorMap tmS1) {
+  // (tmS0 / tmS1: the MXFP4 block scales of A0 / A1; unused otherwise)
   using C = Cfg<MODE, BN, WF, PAIR>;
   constexpr bool FP8 = C::FP8, A8 = C::A8, CONV = C::CONV;
   constexpr int STAGES = C::STAGES;
@@ -350,6 +394,10 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
     ptx::prefetch_tmap(&tmA0);
     if (MODE == kGateUp) ptx::prefetch_tmap(&tmA1);
     ptx::prefetch_tmap(&tmB);
+    if (C::MX4) {
+      ptx::prefetch_tmap(&tmS0);
+      if (MODE == kGateUp) ptx::prefetch_tmap(&tmS1);
+    }
   }
   if (warp == 1) {
     ptx::tmem_alloc<PAIR>(ptx::smem_u32(tmem_slot), kTmemCols);
@@ -492,9 +540,18 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
                   ptx::tma_load_2d_pair(sb + i * p.boxn * kBK * 2, &tmB, fb, kb * C::KB, brow0 + i * p.boxn, pol_x);
             } else {
               ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
-              ptx::tma_load_2d(sa, &tmA0, full_bar(stage), kb * C::KB, arow, pol_w);
+              // weight codes (MXFP4: two per byte), then (MXFP4) the
+              // k-block's scales of the tile's 128 rows
+              const int wx = C::MX4 ? kb * (C::KB / 2) : kb * C::KB;
+              ptx::tma_load_2d(sa, &tmA0, full_bar(stage), wx, arow, pol_w);
               if (MODE == kGateUp)
-                ptx::tma_load_2d(sa + C::W_BYTES, &tmA1, full_bar(stage), kb * C::KB, arow, pol_w);
+                ptx::tma_load_2d(sa + C::W_BYTES, &tmA1, full_bar(stage), wx, arow, pol_w);
+              if constexpr (C::MX4) {
+                const int sx = x.mt * C::CH + (int)rank * kBM, sy = x.g * (p.K / 32) + kb * (C::KB / 32);
+                ptx::tma_load_2d(sa + C::STG_BYTES, &tmS0, full_bar(stage), sx, sy, pol_w);
+                if (MODE == kGateUp)
+                  ptx::tma_load_2d(sa + C::W_BYTES + C::STG_BYTES, &tmS1, full_bar(stage), sx, sy, pol_w);
+              }
               if (!gather && !lsu)
 #pragma unroll
                 for (int sub = 0; sub < C::NSUB; ++sub)
@@ -721,8 +778,8 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
       const int ch = x.mt * C::CH + (int)rank * kBM + ch_local;
       const bool empty_k = x.ks * kb_per_split >= kblocks;
       const int n_mma = ((x.n_valid + 15) / 16) * 16;
-      const float sc0 = FP8 ? p.scale0[(size_t)x.g * p.M + ch] : 1.f;
-      const float sc1 = FP8 && MODE == kGateUp ? p.scale1[(size_t)x.g * p.M + ch] : 1.f;
+      const float sc0 = C::CHS ? p.scale0[(size_t)x.g * p.M + ch] : 1.f;
+      const float sc1 = C::CHS && MODE == kGateUp ? p.scale1[(size_t)x.g * p.M + ch] : 1.f;
       // CW accumulator columns per TMEM wait: 32 for the projection (its
       // epilogue is the longer one per MMA cycle), 16 for gate/up (measured
       // faster there).  BN is a multiple of 32, so columns past n_mma stay
@@ -898,26 +955,49 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
           ptx::tc_fence_after();
           const int qd = warp & 3;
           const int r = qd * 32 + lane;
+          if constexpr (C::MX4) {
+            // MXFP4: 64-byte rows of packed codes under the 64-byte swizzle
+            // (16-byte chunk c of row r at chunk c ^ ((r / 2) % 4): the
+            // warp's rows read conflict-free); chunk c is the c-th
+            // 32-element block, its scale at byte c * 128 + r after the codes
 #pragma unroll
-          for (int a = 0; a < C::NA; ++a) {
-            const uint8_t* src = st + a * C::STG_BYTES + r * C::KB;
+            for (int a = 0; a < C::NA; ++a) {
+              const uint8_t* src = st + a * C::W_BYTES + r * (C::KB / 2);
+              const uint8_t* scl = st + a * C::W_BYTES + C::STG_BYTES + r;
 #pragma unroll
-            for (int hf = 0; hf < C::KB / 64; ++hf) {
-              uint32_t w[32];
+              for (int hf = 0; hf < C::KB / 64; ++hf) {
+                uint32_t w[32];
 #pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                const uint4 v = *reinterpret_cast<const uint4*>(src + (((4 * hf + c) ^ (r & 7)) << 4));
-                const uint4 lo = e4m3x8_to_f16x8(v.x, v.y), hi = e4m3x8_to_f16x8(v.z, v.w);
-                w[8 * c + 0] = lo.x;
-                w[8 * c + 1] = lo.y;
-                w[8 * c + 2] = lo.z;
-                w[8 * c + 3] = lo.w;
-                w[8 * c + 4] = hi.x;
-                w[8 * c + 5] = hi.y;
-                w[8 * c + 6] = hi.z;
-                w[8 * c + 7] = hi.w;
+                for (int c = 0; c < 2; ++c) {
+                  const int blk = 2 * hf + c;
+                  const uint4 v = *reinterpret_cast<const uint4*>(src + ((blk ^ ((r >> 1) & 3)) << 4));
+                  e2m1x32_to_f16(v, ue8m0_to_f16x2(scl[blk * kBM]), w + 16 * c);
+                }
+                ptx::tmem_st32(tmem_base + ((uint32_t)(qd * 32) << 16) + C::ta_col(ostage, a) + 32 * hf, w);
               }
-              ptx::tmem_st32(tmem_base + ((uint32_t)(qd * 32) << 16) + C::ta_col(ostage, a) + 32 * hf, w);
+            }
+          } else {
+#pragma unroll
+            for (int a = 0; a < C::NA; ++a) {
+              const uint8_t* src = st + a * C::STG_BYTES + r * C::KB;
+#pragma unroll
+              for (int hf = 0; hf < C::KB / 64; ++hf) {
+                uint32_t w[32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                  const uint4 v = *reinterpret_cast<const uint4*>(src + (((4 * hf + c) ^ (r & 7)) << 4));
+                  const uint4 lo = e4m3x8_to_f16x8(v.x, v.y), hi = e4m3x8_to_f16x8(v.z, v.w);
+                  w[8 * c + 0] = lo.x;
+                  w[8 * c + 1] = lo.y;
+                  w[8 * c + 2] = lo.z;
+                  w[8 * c + 3] = lo.w;
+                  w[8 * c + 4] = hi.x;
+                  w[8 * c + 5] = hi.y;
+                  w[8 * c + 6] = hi.z;
+                  w[8 * c + 7] = hi.w;
+                }
+                ptx::tmem_st32(tmem_base + ((uint32_t)(qd * 32) << 16) + C::ta_col(ostage, a) + 32 * hf, w);
+              }
             }
           }
           ptx::tmem_st_wait();
@@ -926,17 +1006,39 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
           // the f16 tile goes to the swizzled shared-memory operand slot
           // (16-byte chunk j of row r at chunk position j ^ (r % 8))
           uint8_t* op = smem + ostage * C::OPND_BYTES;
+          if constexpr (C::MX4) {
+            // MXFP4: 32-byte rows of packed codes (unswizzled), one
+            // 32-element block per step -> four 16-byte f16 chunks
 #pragma unroll
-          for (int a = 0; a < C::NA; ++a) {
-            const uint8_t* src = st + a * C::STG_BYTES;
-            uint8_t* dst = op + a * C::A_BYTES;
+            for (int a = 0; a < C::NA; ++a) {
+              const uint8_t* src = st + a * C::W_BYTES;
+              uint8_t* dst = op + a * C::A_BYTES;
+#pragma unroll 2
+              for (int i = ct; i < kBM * (kBK / 32); i += kConvThreads) {
+                const int r = i >> 1, c = i & 1;
+                const uint4 v = *reinterpret_cast<const uint4*>(src + r * (kBK / 2) + c * 16);
+                uint32_t w[16];
+                e2m1x32_to_f16(v, ue8m0_to_f16x2(src[C::STG_BYTES + c * kBM + r]), w);
+                const int sw = r & 7;
 #pragma unroll
-            for (int i = ct; i < kBM * kBK / 16; i += kConvThreads) {  // 16 E4M3 per chunk
-              const int r = i >> 2, c = i & 3;
-              const uint4 v = *reinterpret_cast<const uint4*>(src + r * kBK + c * 16);
-              const int sw = r & 7;
-              *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * c) ^ sw) << 4)) = e4m3x8_to_f16x8(v.x, v.y);
-              *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * c + 1) ^ sw) << 4)) = e4m3x8_to_f16x8(v.z, v.w);
+                for (int j = 0; j < 4; ++j)
+                  *reinterpret_cast<uint4*>(dst + r * 128 + (((4 * c + j) ^ sw) << 4)) =
+                      make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int a = 0; a < C::NA; ++a) {
+              const uint8_t* src = st + a * C::STG_BYTES;
+              uint8_t* dst = op + a * C::A_BYTES;
+#pragma unroll
+              for (int i = ct; i < kBM * kBK / 16; i += kConvThreads) {  // 16 E4M3 per chunk
+                const int r = i >> 2, c = i & 3;
+                const uint4 v = *reinterpret_cast<const uint4*>(src + r * kBK + c * 16);
+                const int sw = r & 7;
+                *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * c) ^ sw) << 4)) = e4m3x8_to_f16x8(v.x, v.y);
+                *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * c + 1) ^ sw) << 4)) = e4m3x8_to_f16x8(v.z, v.w);
+              }
             }
           }
           ptx::fence_proxy_async_smem();
@@ -976,7 +1078,8 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
 
 template <int MODE, int BN, int WF, bool PAIR = false>
 moe_status launch_one(const TcParams& p, const CUtensorMap& a0, const CUtensorMap& a1,
-                      const CUtensorMap& b, int grid, cudaStream_t s) {
+                      const CUtensorMap& b, const CUtensorMap& s0, const CUtensorMap& s1, int grid,
+                      cudaStream_t s) {
   using C = Cfg<MODE, BN, WF, PAIR>;
   auto kern = tc_grouped_kernel<MODE, BN, WF, PAIR>;
   MOE_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES));
@@ -1007,42 +1110,50 @@ moe_status launch_one(const TcParams& p, const CUtensorMap& a0, const CUtensorMa
     if (resident[dev] < 0) return MOE_ERR_UNSUPPORTED;
     grid = min(grid & ~1, 2 * resident[dev]);
   }
-  MOE_TRY_CUDA(launch_kc(PAIR ? 2 : 1, kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, s, p, a0, a1, b));
+  MOE_TRY_CUDA(launch_kc(PAIR ? 2 : 1, kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, s, p, a0, a1, b, s0, s1));
   MOE_TRY_CUDA(cudaGetLastError());
   return MOE_OK;
 }
 
+// The kernel instantiations: (rows per tile, weight format, CTA pair).
+// s0 / s1: the MXFP4 block-scale maps of A0 / A1 (any map otherwise).
 template <int MODE>
 moe_status launch_mode(int bn, int wf, bool pair, const TcParams& p, const CUtensorMap& a0,
-                       const CUtensorMap& a1, const CUtensorMap& b, int grid, cudaStream_t s) {
+                       const CUtensorMap& a1, const CUtensorMap& b, const CUtensorMap& s0,
+                       const CUtensorMap& s1, int grid, cudaStream_t s) {
+#define MOE_LAUNCH(BN_, WF_, PAIR_) \
+  if (bn == BN_ && wf == WF_) return launch_one<MODE, BN_, WF_, PAIR_>(p, a0, a1, b, s0, s1, grid, s)
   if (pair) {
     if (p.M % (2 * kBM) != 0 || grid < 2) return MOE_ERR_UNSUPPORTED;
-    if (wf == kWFp8) {
-      if (bn == 32) return launch_one<MODE, 32, kWFp8, true>(p, a0, a1, b, grid, s);
-      if (bn == 128) return launch_one<MODE, 128, kWFp8, true>(p, a0, a1, b, grid, s);
-      if (bn == 256) return launch_one<MODE, 256, kWFp8, true>(p, a0, a1, b, grid, s);
-    } else if (wf == kWBf16) {
-      if (bn == 128) return launch_one<MODE, 128, kWBf16, true>(p, a0, a1, b, grid, s);
-      if (bn == 256) return launch_one<MODE, 256, kWBf16, true>(p, a0, a1, b, grid, s);
-    } else if (MODE == kGateUp) {
-      if (bn == 128) return launch_one<MODE, 128, kWFp8Act8, true>(p, a0, a1, b, grid, s);
-      if (bn == 256) return launch_one<MODE, 256, kWFp8Act8, true>(p, a0, a1, b, grid, s);
+    MOE_LAUNCH(32, kWFp8, true);
+    MOE_LAUNCH(128, kWFp8, true);
+    MOE_LAUNCH(256, kWFp8, true);
+    MOE_LAUNCH(32, kWMx4, true);
+    MOE_LAUNCH(128, kWMx4, true);
+    MOE_LAUNCH(256, kWMx4, true);
+    MOE_LAUNCH(128, kWBf16, true);
+    MOE_LAUNCH(256, kWBf16, true);
+    if constexpr (MODE == kGateUp) {
+      MOE_LAUNCH(128, kWFp8Act8, true);
+      MOE_LAUNCH(256, kWFp8Act8, true);
     }
     return MOE_ERR_UNSUPPORTED;
   }
-  if (wf == kWFp8) {
-    if (bn == 32) return launch_one<MODE, 32, kWFp8>(p, a0, a1, b, grid, s);
-    if (bn == 128) return launch_one<MODE, 128, kWFp8>(p, a0, a1, b, grid, s);
-    if (bn == 256) return launch_one<MODE, 256, kWFp8>(p, a0, a1, b, grid, s);
-  } else if (wf == kWBf16) {
-    if (bn == 32) return launch_one<MODE, 32, kWBf16>(p, a0, a1, b, grid, s);
-    if (bn == 128) return launch_one<MODE, 128, kWBf16>(p, a0, a1, b, grid, s);
-    if (bn == 256) return launch_one<MODE, 256, kWBf16>(p, a0, a1, b, grid, s);
-  } else if (MODE == kGateUp) {
-    if (bn == 32) return launch_one<MODE, 32, kWFp8Act8>(p, a0, a1, b, grid, s);
-    if (bn == 128) return launch_one<MODE, 128, kWFp8Act8>(p, a0, a1, b, grid, s);
-    if (bn == 256) return launch_one<MODE, 256, kWFp8Act8>(p, a0, a1, b, grid, s);
+  MOE_LAUNCH(32, kWFp8, false);
+  MOE_LAUNCH(128, kWFp8, false);
+  MOE_LAUNCH(256, kWFp8, false);
+  MOE_LAUNCH(32, kWMx4, false);
+  MOE_LAUNCH(128, kWMx4, false);
+  MOE_LAUNCH(256, kWMx4, false);
+  MOE_LAUNCH(32, kWBf16, false);
+  MOE_LAUNCH(128, kWBf16, false);
+  MOE_LAUNCH(256, kWBf16, false);
+  if constexpr (MODE == kGateUp) {
+    MOE_LAUNCH(32, kWFp8Act8, false);
+    MOE_LAUNCH(128, kWFp8Act8, false);
+    MOE_LAUNCH(256, kWFp8Act8, false);
   }
+#undef MOE_LAUNCH
   return MOE_ERR_UNSUPPORTED;
 }
 
@@ -1124,7 +1235,7 @@ TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype) {
   const int bn = est_max <= 32.0 ? 32 : 128;
   // FP8 weights keep 128-row gate/up tiles: on CTA pairs their accumulators
   // leave room in TMEM for the f16 weight operand (the TA path)
-  const int bn_gu = (bn == 128 && mean >= 128.0 && w_dtype != MOE_FP8_E4M3) ? 256 : bn;
+  const int bn_gu = (bn == 128 && mean >= 128.0 && w_dtype != MOE_FP8_E4M3 && w_dtype != MOE_MXFP4) ? 256 : bn;
   const int bn_dn = (bn == 128 && mean >= 128.0) ? 256 : bn;
   pl.bn_gateup = bn_ok(env_int("MOE_BN_GATEUP")) ? env_int("MOE_BN_GATEUP") : bn_gu;
   pl.bn_down = bn_ok(env_int("MOE_BN_DOWN")) ? env_int("MOE_BN_DOWN") : bn_dn;
@@ -1140,7 +1251,7 @@ TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype) {
   const char* pe = getenv("MOE_PAIR");
   const bool pairs_ok = !(pe != nullptr && pe[0] == '0') && num_sms >= 2;
   const bool act8 = w_dtype == MOE_FP8_E4M3_ACT8;
-  const bool fp8 = w_dtype == MOE_FP8_E4M3 || act8;
+  const bool fp8 = w_dtype == MOE_FP8_E4M3 || act8 || w_dtype == MOE_MXFP4;
   const bool dec_pairs = pairs_ok && pe != nullptr && pe[0] == '2';
   const bool dec_pair_gu = dec_pairs && fp8 && !act8 && pl.bn_gateup == 32 && ffn % (2 * kBM) == 0;
   const bool dec_pair_dn = dec_pairs && fp8 && pl.bn_down == 32 && d % (2 * kBM) == 0;
@@ -1166,11 +1277,13 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
                              cudaEvent_t mid) {
   if (a.R == 0) return MOE_OK;
   const bool act8 = a.w_dtype == MOE_FP8_E4M3_ACT8;
-  const bool fp8 = a.w_dtype == MOE_FP8_E4M3 || act8;
+  const bool mx4 = a.w_dtype == MOE_MXFP4;
+  const bool fp8 = a.w_dtype == MOE_FP8_E4M3 || act8 || mx4;  // quantised weights: f16 operands, f16 h
   if (!fp8 && a.w_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   if (fp8 && (a.s_gate == nullptr || a.s_up == nullptr || a.s_down == nullptr)) return MOE_ERR_INVALID_ARG;
   if (act8 && a.row_scale == nullptr) return MOE_ERR_INVALID_ARG;
-  const int wf_gu = act8 ? kWFp8Act8 : fp8 ? kWFp8 : kWBf16;
+  const int wf_gu = act8 ? kWFp8Act8 : mx4 ? kWMx4 : fp8 ? kWFp8 : kWBf16;
+  const int wf_dn = mx4 ? kWMx4 : fp8 ? kWFp8 : kWBf16;
   if (a.d % kBM != 0 || a.ffn % kBM != 0 || a.G > kMaxGroups) return MOE_ERR_UNSUPPORTED;
   // weights: bf16 tiles [128 x 64] with 128-byte swizzle, or E4M3 tiles
   // [128 x 64 bytes] staged unswizzled for the converters
@@ -1180,13 +1293,27 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   // conflict-free
   // FP8 activations: E4M3 weight and row tiles straight into the MMA's
   // 128-byte-swizzled operands, 128 elements of K per row
+  // MXFP4: packed codes, half as many bytes per K: 64-byte rows under the
+  // 64-byte swizzle (tensor-memory path, 128 of K) or 32-byte rows
+  // unswizzled (64 of K); the block scales [G, K/32, M] as a 2-D byte
+  // array [G*K/32, M], one box of (K per stage / 32) x 128 per tile
   const bool ta_gu = ta_config(kGateUp, plan.bn_gateup, fp8 && !act8, plan.pair_gateup != 0);
   const bool ta_dn = ta_config(kDown, plan.bn_down, fp8, plan.pair_down != 0);
-  const int wsw_gu = !fp8 || ta_gu || act8 ? 128 : 0, wsw_dn = !fp8 || ta_dn ? 128 : 0;
-  const int wk_gu = ta_gu || act8 ? 2 * kBK : kBK, wk_dn = ta_dn ? 2 * kBK : kBK;
-  CUtensorMap wg, wu, xb, wd, hb;
-  MOE_TRY(make_tmap_2d(&wg, a.w_gate, (uint64_t)a.G * a.ffn, a.d, wb, kBM, wk_gu, wsw_gu));
-  MOE_TRY(make_tmap_2d(&wu, a.w_up, (uint64_t)a.G * a.ffn, a.d, wb, kBM, wk_gu, wsw_gu));
+  const int wsw_gu = mx4 ? (ta_gu ? 64 : 0) : !fp8 || ta_gu || act8 ? 128 : 0;
+  const int wsw_dn = mx4 ? (ta_dn ? 64 : 0) : !fp8 || ta_dn ? 128 : 0;
+  const int kw_gu = ta_gu || act8 ? 2 * kBK : kBK, kw_dn = ta_dn ? 2 * kBK : kBK;  // K per stage
+  const int wk_gu = mx4 ? kw_gu / 2 : kw_gu, wk_dn = mx4 ? kw_dn / 2 : kw_dn;    // box columns
+  const uint64_t wcols_gu = mx4 ? a.d / 2 : a.d, wcols_dn = mx4 ? a.ffn / 2 : a.ffn;
+  CUtensorMap wg, wu, xb, wd, hb, sg, su, sd;
+  MOE_TRY(make_tmap_2d(&wg, a.w_gate, (uint64_t)a.G * a.ffn, wcols_gu, wb, kBM, wk_gu, wsw_gu));
+  MOE_TRY(make_tmap_2d(&wu, a.w_up, (uint64_t)a.G * a.ffn, wcols_gu, wb, kBM, wk_gu, wsw_gu));
+  if (mx4) {
+    MOE_TRY(make_tmap_2d(&sg, a.s_gate, (uint64_t)a.G * (a.d / 32), a.ffn, 1, kw_gu / 32, kBM, 0));
+    MOE_TRY(make_tmap_2d(&su, a.s_up, (uint64_t)a.G * (a.d / 32), a.ffn, 1, kw_gu / 32, kBM, 0));
+    MOE_TRY(make_tmap_2d(&sd, a.s_down, (uint64_t)a.G * (a.ffn / 32), a.d, 1, kw_dn / 32, kBM, 0));
+  } else {
+    sg = su = sd = wg;
+  }
   const int box_gu = boxn_of(plan.bn_gateup, plan.pair_gateup != 0);
   const int box_dn = boxn_of(plan.bn_down, plan.pair_down != 0);
   // gathered token rows: TMA gather4 for decode tiles, cp.async by the
@@ -1206,7 +1333,7 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
     MOE_TRY(make_tmap_kpair(&wd, a.w_down, (uint64_t)a.G * a.d, a.ffn, 2, kBM));
     MOE_TRY(make_tmap_kpair(&hb, a.h, a.R, a.ffn, 2, plan.bn_down / 2));
   } else {
-    MOE_TRY(make_tmap_2d(&wd, a.w_down, (uint64_t)a.G * a.d, a.ffn, wb, kBM, wk_dn, wsw_dn));
+    MOE_TRY(make_tmap_2d(&wd, a.w_down, (uint64_t)a.G * a.d, wcols_dn, wb, kBM, wk_dn, wsw_dn));
     MOE_TRY(make_tmap_2d(&hb, a.h, a.R, a.ffn, 2, box_dn, kBK, 128));
   }
 
@@ -1236,7 +1363,7 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   p.x_src = a.x_src;
   p.d_src = a.d;
   p.row_scale = act8 ? a.row_scale : nullptr;
-  MOE_TRY(launch_mode<kGateUp>(plan.bn_gateup, wf_gu, plan.pair_gateup != 0, p, wg, wu, xb, plan.grid, s));
+  MOE_TRY(launch_mode<kGateUp>(plan.bn_gateup, wf_gu, plan.pair_gateup != 0, p, wg, wu, xb, sg, su, plan.grid, s));
   p.gather_rows = nullptr;
   p.lsu_gather = 0;
   p.row_scale = nullptr;
@@ -1263,7 +1390,7 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   p.scale0 = a.s_down;
   p.scale1 = nullptr;
   p.boxn = k2_dn ? plan.bn_down / 2 : box_dn;
-  MOE_TRY(launch_mode<kDown>(plan.bn_down, fp8 ? kWFp8 : kWBf16, plan.pair_down != 0, p, wd, wd, hb, plan.grid, s));
+  MOE_TRY(launch_mode<kDown>(plan.bn_down, wf_dn, plan.pair_down != 0, p, wd, wd, hb, sd, sd, plan.grid, s));
   return MOE_OK;
 }
 
@@ -1294,7 +1421,7 @@ moe_status tc_dense_f32_launch(const void* a, const void* b, float* out, int M, 
   p.status = status;
   p.timeout_ns = timeout_ns;
   p.boxn = kBoxLarge;
-  return launch_mode<kDown>(128, kWBf16, false, p, ta, ta, tb, num_sms, s);
+  return launch_mode<kDown>(128, kWBf16, false, p, ta, ta, tb, ta, ta, num_sms, s);
 }
 
 moe_status tc_selftest_launch(int* status, long long timeout_ns, cudaStream_t s) {
@@ -1310,7 +1437,7 @@ moe_status tc_selftest_launch(int* status, long long timeout_ns, cudaStream_t s)
   p.timeout_ns = timeout_ns;
   p.selftest = 1;
   p.boxn = kBoxSmall;
-  return launch_one<kGateUp, 32, kWBf16>(p, dummy, dummy, dummy, 1, s);
+  return launch_one<kGateUp, 32, kWBf16>(p, dummy, dummy, dummy, dummy, dummy, 1, s);
 }
 
 }  // namespace moe

@@ -42,6 +42,7 @@ class MoEShape:
     ffn_shared: int = 0
     act: str = "bf16"          # "f32" | "bf16"
     # "f32" | "bf16" | "fp8" | "fp8a8" (FP8 weights, FP8 gate/up activations)
+    # | "mxfp4" (OCP MX 4-bit block-scaled weights)
     wfmt: str = "bf16"
     router_bias: str = "none"  # "none" | "zipf"
     zipf_s: float = 1.2
@@ -125,11 +126,41 @@ def _fp8_quantise(w: torch.Tensor):
     return q.view(torch.uint8), scale
 
 
+_E2M1_MAGS = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)
+
+
+def _mxfp4_quantise(w: torch.Tensor):
+    """MXFP4 codes of a [rows, cols] fp32 block: per 32 consecutive values of
+    a row, the scale 2^e with e = floor(log2(block max)) - 2 (the block's
+    largest magnitude lands in [4, 8), saturating at 6), codes the nearest
+    E2M1 magnitude (ties up) with the sign bit.  Returns packed codes
+    [rows, cols/2] (element 2i in the low nibble) and UE8M0 scales
+    [cols/32, rows]."""
+    rows, cols = w.shape
+    blk = w.reshape(rows, cols // 32, 32)
+    amax = blk.abs().amax(dim=2).clamp_min(2.0 ** -100)
+    e = (torch.floor(torch.log2(amax)) - 2).clamp(-127, 127)
+    q = blk / torch.exp2(e)[..., None]
+    mags = torch.tensor(_E2M1_MAGS, device=w.device)
+    code = torch.bucketize(q.abs().clamp(max=6.0), (mags[1:] + mags[:-1]) / 2)
+    code = (code | ((q < 0).to(code.dtype) << 3)).reshape(rows, cols).to(torch.uint8)
+    packed = code[:, 0::2] | (code[:, 1::2] << 4)
+    return packed.contiguous(), (e + 127).to(torch.uint8).t().contiguous()
+
+
 def _expert_stack(shape: MoEShape, rows: int, cols: int, seed: int, name: str, device):
     """[E, rows, cols] expert matrices ~ N(0, 1/d), generated per expert so
     that large layers never hold an fp32 copy of the whole stack."""
     std = 1.0 / math.sqrt(shape.d)
     E = shape.E
+    if shape.wfmt == "mxfp4":
+        w = torch.empty((E, rows, cols // 2), dtype=torch.uint8, device=device)
+        s = torch.empty((E, cols // 32, rows), dtype=torch.uint8, device=device)
+        for e in range(E):
+            q, sc = _mxfp4_quantise(_normal((rows, cols), std, seed, f"{name}[{e}]", device, torch.float32))
+            w[e].copy_(q)
+            s[e].copy_(sc)
+        return w, s
     if shape.wfmt in ("fp8", "fp8a8"):
         w = torch.empty((E, rows, cols), dtype=torch.uint8, device=device)
         s = torch.empty((E, rows), dtype=torch.float32, device=device)

@@ -59,7 +59,10 @@ def oracle_inputs(case, shape):
     x = decode_act(case["x"], shape.act)
     wr = decode_act(case["w_router"], shape.act)
     bias = None if case["router_bias"] is None else inputs.to_numpy_stored(case["router_bias"]).astype(np.float64)
-    if shape.wfmt in ("fp8", "fp8a8"):
+    if shape.wfmt == "mxfp4":
+        ew = oracle.ExpertWeights("mxfp4", _Lazy(case["w_gate"]), _Lazy(case["w_up"]), _Lazy(case["w_down"]),
+                                  _Lazy(case["s_gate"]), _Lazy(case["s_up"]), _Lazy(case["s_down"]))
+    elif shape.wfmt in ("fp8", "fp8a8"):
         ew = oracle.ExpertWeights("fp8", _Lazy(case["w_gate"]), _Lazy(case["w_up"]), _Lazy(case["w_down"]),
                                   _Lazy(case["s_gate"]), _Lazy(case["s_up"]), _Lazy(case["s_down"]))
     else:

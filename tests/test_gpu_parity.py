@@ -564,6 +564,7 @@ def test_bounded_wait_expires_cleanly_and_context_survives():
     inputs.WORKLOADS["qwen3_30b_a3b"].with_T(1),                    # fused top-k, split-K gate/up
     inputs.MoEShape("ds_small", T=2, d=1024, ffn=512, E=64, k=8, ffn_shared=512, wfmt="fp8"),
     inputs.MoEShape("ds_small_act8", T=2, d=1024, ffn=512, E=64, k=8, ffn_shared=512, wfmt="fp8a8"),
+    inputs.MoEShape("ds_small_mx", T=2, d=1024, ffn=512, E=64, k=8, ffn_shared=512, wfmt="mxfp4"),
     inputs.MoEShape("chunked", T=400, d=256, ffn=256, E=32, k=8),   # chunked permutation
 ], ids=lambda s: s.name)
 def test_layer_launch_count_matches_the_kernels_launched(shape):

@@ -12,7 +12,8 @@ from tests import test_oracle_pins as pins
 _orig = {n: getattr(M, n) for n in ("topk_renorm", "permutation_maps", "silu", "swiglu_expert",
                                       "decode_e4m3", "decode_bf16", "moe_forward_grouped",
                                       "moe_forward_per_token", "shared_expert", "router_logits",
-                                      "round_to_e4m3", "quantize_rows_e4m3")}
+                                      "round_to_e4m3", "quantize_rows_e4m3", "decode_e2m1",
+                                      "decode_ue8m0", "unpack_fp4", "decode_mxfp4")}
 
 
 def _no_renorm(logits, k):
@@ -105,6 +106,25 @@ def _row_scale_480(x):
     return M.round_to_e4m3((x32 / s[:, None]).astype(np.float32)), s
 
 
+def _e2m1_subnormal_quarter(codes):
+    v = _orig["decode_e2m1"](codes)
+    return np.where(np.abs(v) == 0.5, v / 2.0, v)
+
+
+def _ue8m0_bias_126(s):
+    return _orig["decode_ue8m0"](s) * 2.0
+
+
+def _fp4_nibbles_swapped(packed):
+    b = np.asarray(packed).astype(np.uint8)
+    return _orig["unpack_fp4"](((b & 0xF) << 4) | (b >> 4))
+
+
+def _mxfp4_scales_transposed(packed, scales):
+    sc = np.asarray(scales)
+    return _orig["decode_mxfp4"](packed, sc.T.reshape(sc.shape))
+
+
 MUTATIONS = {
     "no_renormalisation": ("topk_renorm", _no_renorm),
     "lowest_k_selected": ("topk_renorm", _lowest_k),
@@ -120,6 +140,10 @@ MUTATIONS = {
     "e4m3_ties_away_from_zero": ("round_to_e4m3", _e4m3_ties_away),
     "e4m3_overflow_not_saturated": ("round_to_e4m3", _e4m3_no_saturation),
     "activation_scale_off": ("quantize_rows_e4m3", _row_scale_480),
+    "e2m1_subnormal_quarter": ("decode_e2m1", _e2m1_subnormal_quarter),
+    "ue8m0_bias_126": ("decode_ue8m0", _ue8m0_bias_126),
+    "fp4_nibbles_swapped": ("unpack_fp4", _fp4_nibbles_swapped),
+    "mxfp4_scales_transposed": ("decode_mxfp4", _mxfp4_scales_transposed),
 }
 
 PIN_CHECKS = [
@@ -142,6 +166,13 @@ PIN_CHECKS = [
     pins.test_round_to_e4m3_ties_go_to_even_and_saturates,
     pins.test_quantize_rows_scale_and_extremes,
     pins.test_quantize_rows_lossless_on_representable_rows,
+    pins.test_decode_e2m1_fixed_values,
+    pins.test_decode_e2m1_agrees_with_e4m3_at_the_same_value,
+    pins.test_decode_ue8m0_fixed_values,
+    pins.test_unpack_fp4_nibble_order,
+    pins.test_decode_mxfp4_hand_block,
+    pins.test_mxfp4_storage_matches_the_page,
+    pins.test_mxfp4_expert_weights_decode_per_matrix,
 ]
 
 

@@ -403,3 +403,93 @@ def test_quantize_rows_lossless_on_representable_rows():
     a = oracle.swiglu_expert(x, w[0], w[1], wd, act8=True)
     b = oracle.swiglu_expert(x, w[0], w[1], wd)
     assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------------------
+# MXFP4 expert weights (OCP Microscaling: E2M1 elements, UE8M0 block scales)
+# ---------------------------------------------------------------------------
+
+def test_decode_e2m1_fixed_values():
+    # the OCP MX element format FP4 E2M1: magnitudes 0, 0.5 (the one
+    # subnormal), 1, 1.5, 2, 3, 4, 6; the high bit is the sign
+    v = oracle.decode_e2m1(np.arange(16))
+    assert v[:8].tolist() == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert v[8:].tolist() == [-0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+    assert np.signbit(v[8]) and not np.signbit(v[0])
+
+
+def test_decode_e2m1_agrees_with_e4m3_at_the_same_value():
+    # every E2M1 value is an E4M3 value: map the fields (exponent e, bias 1
+    # -> bias 7; the fraction bit becomes the top of three) and decode with
+    # the (separately pinned) E4M3 decoder
+    for c in range(16):
+        s, e, m = c >> 3, (c >> 1) & 3, c & 1
+        if e == 0:
+            f8 = 0 if m == 0 else (6 << 3)          # 0.5 = 2^-1
+        else:
+            f8 = ((e - 1 + 7) << 3) | (m << 2)
+        assert oracle.decode_e2m1(c) == oracle.decode_e4m3((s << 7) | f8)
+
+
+def test_decode_ue8m0_fixed_values():
+    v = oracle.decode_ue8m0(np.array([0, 1, 126, 127, 128, 134, 254, 255]))
+    assert v[1:7].tolist() == [2.0 ** -126, 0.5, 1.0, 2.0, 128.0, 2.0 ** 127]
+    assert v[0] == 2.0 ** -127 and np.isnan(v[7])
+
+
+def test_unpack_fp4_nibble_order():
+    codes = oracle.unpack_fp4(np.array([[0x21, 0xF0, 0x7A]], np.uint8))
+    assert codes.tolist() == [[1, 2, 0, 15, 10, 7]]
+
+
+def test_decode_mxfp4_hand_block():
+    # two rows of 64 weights (two 32-element blocks each); scales [K/32, rows]
+    codes = np.zeros((2, 64), np.uint8)
+    codes[0, 0], codes[0, 1], codes[0, 33] = 0x7, 0x9, 0x3      # 6, -0.5 | 1.5
+    codes[1, 2], codes[1, 40], codes[1, 63] = 0x5, 0xC, 0x1     # 3 | -2, 0.5
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    scales = np.array([[127, 126],      # block 0: row 0 x 1, row 1 x 0.5
+                       [128, 130]],     # block 1: row 0 x 2, row 1 x 8
+                      np.uint8)
+    w = oracle.decode_mxfp4(packed, scales)
+    expect = np.zeros((2, 64))
+    expect[0, 0], expect[0, 1], expect[0, 33] = 6.0, -0.5, 3.0
+    expect[1, 2], expect[1, 40], expect[1, 63] = 1.5, -16.0, 4.0
+    assert w.shape == (2, 64) and np.array_equal(w, expect)
+
+
+def test_mxfp4_storage_matches_the_page():
+    # "MoE 推理部署", section 专家量化: the OCP MX 4-bit block format puts a
+    # 117B-parameter model in about 60 GB, inside one 80 GB GPU.  The format
+    # the oracle decodes spends K/2 code bytes and K/32 scale bytes per row of
+    # K weights: 4.25 bits per weight.
+    K, rows = 4096, 3
+    packed = np.zeros((rows, K // 2), np.uint8)
+    scales = np.full((K // 32, rows), 127, np.uint8)
+    assert oracle.decode_mxfp4(packed, scales).shape == (rows, K)
+    bits_per_weight = 8.0 * (packed.size + scales.size) / (rows * K)
+    assert bits_per_weight == 4.25
+    gb = 117e9 * bits_per_weight / 8 / 1e9
+    assert 55.0 <= gb <= 65.0 and gb < 80.0
+
+
+def test_mxfp4_expert_weights_decode_per_matrix():
+    # ExpertWeights("mxfp4") hands each expert's three matrices through
+    # decode_mxfp4 with their own scales; the FFN then sees plain values
+    rng = np.random.default_rng(8)
+    E, d, f = 2, 64, 32
+    wg = rng.integers(0, 256, (E, f, d // 2)).astype(np.uint8)
+    wu = rng.integers(0, 256, (E, f, d // 2)).astype(np.uint8)
+    wd = rng.integers(0, 256, (E, d, f // 2)).astype(np.uint8)
+    sg = rng.integers(120, 130, (E, d // 32, f)).astype(np.uint8)
+    su = rng.integers(120, 130, (E, d // 32, f)).astype(np.uint8)
+    sd = rng.integers(120, 130, (E, f // 32, d)).astype(np.uint8)
+    ew = oracle.ExpertWeights("mxfp4", wg, wu, wd, sg, su, sd)
+    g1, u1, d1 = ew.get(1)
+    assert np.array_equal(g1, oracle.decode_mxfp4(wg[1], sg[1]))
+    assert np.array_equal(u1, oracle.decode_mxfp4(wu[1], su[1]))
+    assert np.array_equal(d1, oracle.decode_mxfp4(wd[1], sd[1]))
+    assert g1.shape == (f, d) and d1.shape == (d, f)
+    # each weight divided by its block's scale is an E2M1 value
+    blk = np.repeat(oracle.decode_ue8m0(sg[1]), 32, axis=0).T
+    assert np.isin(np.abs(g1 / blk), oracle.decode_e2m1(np.arange(8))).all()
