@@ -366,14 +366,19 @@ def silu(z: np.ndarray) -> np.ndarray:
 def swiglu_expert(x_rows: np.ndarray, wg: np.ndarray, wu: np.ndarray, wd: np.ndarray,
                   act8: bool = False) -> np.ndarray:
     """One expert on a matrix of rows: (SiLU(X W_gᵀ) ⊙ (X W_uᵀ)) W_dᵀ.
-    ``act8``: the rows enter the gate and up products quantised per row to
-    E4M3 (quantize_rows_e4m3), the FP8-activation mode; h stays exact."""
+    ``act8``, the FP8-activation mode: both products take E4M3 activations
+    quantised per row (quantize_rows_e4m3): the rows X before the gate and up
+    products, and the rows of h = SiLU(g) ⊙ u (rounded to float32, the
+    quantiser's input precision) before the down product."""
     x_rows = np.asarray(x_rows, F64)
     if act8:
         x_rows = dequantize_rows_e4m3(*quantize_rows_e4m3(x_rows))
     g = x_rows @ np.asarray(wg, F64).T
     u = x_rows @ np.asarray(wu, F64).T
-    return (silu(g) * u) @ np.asarray(wd, F64).T
+    h = silu(g) * u
+    if act8:
+        h = dequantize_rows_e4m3(*quantize_rows_e4m3(h.astype(np.float32)))
+    return h @ np.asarray(wd, F64).T
 
 
 def shared_expert(x: np.ndarray, wg: np.ndarray, wu: np.ndarray, wd: np.ndarray) -> np.ndarray:
@@ -396,8 +401,8 @@ def moe_forward_per_token(x, w_router, experts: ExpertWeights, k: int, bias=None
     ``routing`` = (idx, w) overrides the router (used to evaluate the layer
     under a given expert choice); ``tokens`` restricts the computation to a
     subset of token ids (rows of the result follow that subset).  ``act8``:
-    the routed experts' gate/up products take the token row quantised per
-    row to E4M3 (the router and the shared expert see x itself).
+    the routed experts run in the FP8-activation mode of swiglu_expert (the
+    router and the shared expert see x itself).
     Returns (out [n, d], idx, w) in float64.
     """
     x = np.asarray(x, F64)

@@ -55,6 +55,13 @@ def _swiglu_swapped(x, wg, wu, wd, act8=False):
     return _orig["swiglu_expert"](x, wu, wg, wd, act8=act8)
 
 
+def _swiglu_h_unquantised(x, wg, wu, wd, act8=False):
+    if not act8:
+        return _orig["swiglu_expert"](x, wg, wu, wd)
+    xq = M.dequantize_rows_e4m3(*M.quantize_rows_e4m3(np.asarray(x, float)))
+    return _orig["swiglu_expert"](xq, wg, wu, wd)
+
+
 def _swiglu_no_gate(x, wg, wu, wd, act8=False):
     x = np.asarray(x, float)
     return ((x @ np.asarray(wg).T) * (x @ np.asarray(wu).T)) @ np.asarray(wd).T
@@ -133,6 +140,7 @@ MUTATIONS = {
     "silu_sign_flip": ("silu", _silu_sign),
     "gate_up_swapped": ("swiglu_expert", _swiglu_swapped),
     "activation_dropped": ("swiglu_expert", _swiglu_no_gate),
+    "act8_h_not_quantised": ("swiglu_expert", _swiglu_h_unquantised),
     "e4m3_wrong_bias": ("decode_e4m3", _e4m3_bias8),
     "bf16_subnormal_as_normal": ("decode_bf16", _bf16_sub_as_normal),
     "router_bias_sign": ("router_logits", _router_transposed_bias),
@@ -166,6 +174,7 @@ PIN_CHECKS = [
     pins.test_round_to_e4m3_ties_go_to_even_and_saturates,
     pins.test_quantize_rows_scale_and_extremes,
     pins.test_quantize_rows_lossless_on_representable_rows,
+    pins.test_act8_expert_quantises_both_activations,
     pins.test_decode_e2m1_fixed_values,
     pins.test_decode_e2m1_agrees_with_e4m3_at_the_same_value,
     pins.test_decode_ue8m0_fixed_values,

@@ -389,8 +389,7 @@ def test_quantize_rows_scale_and_extremes():
 
 def test_quantize_rows_lossless_on_representable_rows():
     # rows that are E4M3 values times a power-of-two scale, with one element
-    # at 448 * scale, come back exactly; the FP8-activation expert then
-    # equals the plain one
+    # at 448 * scale, come back exactly
     rng = np.random.default_rng(6)
     codes = rng.integers(0, 0x7E, size=(4, 64)).astype(np.uint8) | (rng.integers(0, 2, size=(4, 64)) * 0x80).astype(np.uint8)
     codes[:, 0] = 0x7E
@@ -398,11 +397,30 @@ def test_quantize_rows_lossless_on_representable_rows():
     x = (oracle.decode_e4m3(codes) * scale).astype(np.float32)
     c2, s2 = oracle.quantize_rows_e4m3(x)
     assert np.all(s2 == scale) and np.array_equal(oracle.decode_e4m3(c2), oracle.decode_e4m3(codes))
-    w = rng.standard_normal((3, 32, 64)) / 8.0
-    wd = rng.standard_normal((64, 32)) / 8.0
-    a = oracle.swiglu_expert(x, w[0], w[1], wd, act8=True)
-    b = oracle.swiglu_expert(x, w[0], w[1], wd)
-    assert np.array_equal(a, b)
+
+
+def test_act8_expert_quantises_both_activations():
+    # On E4M3-representable rows the input quantisation is lossless, so with
+    # an identity down projection the FP8-activation expert returns the rows
+    # of h as quantised per row: each row divided by (its max / 448) lies on
+    # the E4M3 grid, within half a grid step of the plain h, its maximum kept
+    rng = np.random.default_rng(6)
+    codes = rng.integers(0, 0x7E, size=(5, 64)).astype(np.uint8)
+    codes[:, 0] = 0x7E
+    x = (oracle.decode_e4m3(codes) * 2.0 ** -9).astype(np.float32)
+    wg, wu = rng.standard_normal((2, 48, 64)) / 8.0
+    eye = np.eye(48)
+    h8 = oracle.swiglu_expert(x, wg, wu, eye, act8=True)
+    h = oracle.swiglu_expert(x, wg, wu, eye)
+    grid = np.abs(oracle.decode_e4m3(np.arange(0x7F)))
+    for t in range(5):
+        s = np.abs(h8[t]).max() / 448.0
+        assert np.isin(np.abs(h8[t] / s), grid).all()
+        assert np.abs(h8[t] - h[t]).max() <= np.abs(h[t]).max() * 2.0 ** -4
+        np.testing.assert_allclose(np.abs(h8[t]).max(), np.abs(h[t]).max(), rtol=1e-6)
+    # and with a general down projection: the product of those rows
+    wd = rng.standard_normal((64, 48)) / 8.0
+    np.testing.assert_allclose(oracle.swiglu_expert(x, wg, wu, wd, act8=True), h8 @ wd.T, rtol=1e-12, atol=1e-12)
 
 
 # ---------------------------------------------------------------------------
