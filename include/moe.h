@@ -45,14 +45,16 @@
  *                               per-expert, per-output-channel scales;
  *                               the router and shared expert stay bf16.
  *   MOE_BF16 / MOE_FP8_E4M3_ACT8
- *                               FP8 weights as above; the routed gate/up
- *                               GEMM multiplies them with E4M3 token rows
+ *                               FP8 weights as above; both routed GEMMs
+ *                               multiply them with E4M3 activation rows
  *                               (per-row scales, moe_quantize_rows_e4m3):
- *                               h = SiLU(g) * u with
- *                               g[r,o] = s_row[r] * s_gate[e,o] *
- *                                        sum_i q[r,i] * code_gate[e][o,i]
- *                               (likewise u).  The down GEMM, router and
- *                               shared expert are as for MOE_FP8_E4M3.
+ *                               g[r,o] = s_x[r] * s_gate[e,o] *
+ *                                        sum_i q_x[r,i] * code_gate[e][o,i]
+ *                               (likewise u), h = SiLU(g) * u held in f16
+ *                               and quantised per row the same way, then
+ *                               y[r,o] = s_h[r] * s_down[e,o] *
+ *                                        sum_j q_h[r,j] * code_down[e][o,j].
+ *                               Router and shared expert stay bf16.
  *   MOE_BF16 / MOE_MXFP4        OCP Microscaling FP4 weights ("MoE 推理部署",
  *                               section 专家量化: MXFP4 block-scaled 4-bit
  *                               experts): W[o,i] = E2M1(code[o,i]) *
@@ -97,8 +99,8 @@ typedef enum moe_dtype {
   MOE_F32 = 0,
   MOE_BF16 = 1,
   MOE_FP8_E4M3 = 2,
-  /* w_dtype only: FP8 weights as MOE_FP8_E4M3, and the routed experts'
-   * gate/up products take the token rows quantised per row to E4M3
+  /* w_dtype only: FP8 weights as MOE_FP8_E4M3, and both routed expert
+   * products take activations quantised per row to E4M3
    * (moe_quantize_rows_e4m3) on FP8 x FP8 tensor-core instructions */
   MOE_FP8_E4M3_ACT8 = 3,
   /* w_dtype only: OCP MXFP4 routed expert weights (see "Supported storage") */
@@ -209,10 +211,10 @@ MOE_API moe_status moe_permute_static_scratch(const moe_problem *p, const int32_
  *   h[r,:]      = SiLU(x_perm[r,:] W_g[e]^T) * (x_perm[r,:] W_u[e]^T)
  *   y_perm[r,:] = h[r,:] W_d[e]^T
  * with FP8 weights W[e][o,:] = code[e][o,:] * scale[e][o] (s_gate, s_up
- * [E, ffn]; s_down [E, d]; NULL unless w_dtype is MOE_FP8_E4M3 or
- * MOE_FP8_E4M3_ACT8).  With MOE_FP8_E4M3_ACT8 the rows of x_perm enter the
- * gate/up products quantised per row (moe_quantize_rows_e4m3, into the
- * workspace).
+ * [E, ffn]; s_down [E, d]; NULL unless the weights are quantised: FP8, or
+ * MXFP4 with the block-scale arrays described above).  With
+ * MOE_FP8_E4M3_ACT8 the rows of x_perm and of h enter their products
+ * quantised per row (moe_quantize_rows_e4m3, into the workspace).
  *
  *   x_perm   [T*k, d] act_dtype      offsets [E+1] int32 (device)
  *   y_perm   [T*k, d] act_dtype out
@@ -233,7 +235,8 @@ MOE_API moe_status moe_grouped_swiglu(const moe_problem *p, const void *x_perm, 
  * higher precision and quantised just before the experts) and page
  * "MoE 推理部署", section 专家量化 (FP8 inference).  The layer forward with
  * w_dtype MOE_FP8_E4M3_ACT8 quantises x before dispatch with this
- * operation; moe_grouped_swiglu quantises x_perm (after dispatch).
+ * operation, moe_grouped_swiglu quantises x_perm (after dispatch), and both
+ * quantise the rows of h (held in f16) before the down product.
  *
  *   s[r]      = max_i |x[r,i]| / 448, or 1 when row r is all zero
  *   code[r,i] = E4M3(x[r,i] / s[r]): nearest E4M3 value, ties to the even

@@ -45,7 +45,7 @@ bool fp8_weights(int w_dtype) {
 
 struct Layout {
   size_t idx, w, logits, counts, offsets, perm_token, inv_row, chunk, x_perm, x_scale, h, y;
-  size_t sh_offsets, sh_h, sh_y, gu_part, sh_gu_part, gu_cnt, sh_gu_cnt, total;
+  size_t sh_offsets, sh_h, sh_y, gu_part, sh_gu_part, gu_cnt, sh_gu_cnt, h_q, h_scale, total;
   size_t cnt_ints;  // gate/up finalize counters (routed, then shared), zeroed by the permutation
   size_t cnt_routed;
   TcPlan plan, sh_plan;
@@ -93,6 +93,9 @@ Layout layout(const moe_problem& p, Path path, int num_sms, bool allow_splits) {
   L.x_perm = take(gather ? (f16x ? T * d * 2 : act8 ? T * d : 0) : R * d * ab);
   L.x_scale = take(act8 ? T * 4 : 0);
   L.h = take(R * f * ab);
+  // FP8 activations: h's E4M3 codes and row scales for the down GEMM
+  L.h_q = take(act8 ? R * f : 0);
+  L.h_scale = take(act8 ? R * 4 : 0);
   const size_t S = path == Path::kTensor ? (size_t)L.plan.splits_down : 1;
   L.y = take(S > 1 ? S * R * d * 4 : R * d * ab);
   L.sh_offsets = take(8);
@@ -147,7 +150,7 @@ moe_status run_grouped(Path path, int R, int d, int ffn, int G, int w_dtype, con
                        const TcPlan& plan, int* status, cudaStream_t s, cudaEvent_t mid,
                        const int32_t* gather_rows = nullptr, const void* x_src = nullptr,
                        int T_src = 0, float* gu_partials = nullptr, int* gu_cnt = nullptr,
-                       const float* row_scale = nullptr) {
+                       const float* row_scale = nullptr, void* h_q = nullptr, float* h_scale = nullptr) {
   if (path == Path::kSimt) {
     SimtGroupedArgs a{R, d, ffn, G, static_cast<const float*>(x_rows), offsets,
                       static_cast<const float*>(wg), static_cast<const float*>(wu),
@@ -156,7 +159,7 @@ moe_status run_grouped(Path path, int R, int d, int ffn, int G, int w_dtype, con
     return simt_grouped_launch(a, s, mid);
   }
   TcGroupedArgs a{R, d, ffn, G, w_dtype, x_rows, offsets, wg, wu, wd, sg, su, sd, h, y, status,
-                  wait_limit_ns(), gather_rows, x_src, T_src, gu_partials, gu_cnt, row_scale};
+                  wait_limit_ns(), gather_rows, x_src, T_src, gu_partials, gu_cnt, row_scale, h_q, h_scale};
   return tc_grouped_launch(a, plan, s, mid);
 }
 
@@ -241,7 +244,9 @@ moe_status moe_grouped_swiglu(const moe_problem* p, const void* x_perm, const in
   // FP8 experts run on f16 operands: round x_perm to f16 into the
   // workspace; with FP8 activations, its E4M3 codes and row scales
   const size_t rows_bytes = act8 ? align256(R * p->d) : fp8 ? align256(R * p->d * 2) : 0;
-  const size_t need = h_bytes + rows_bytes + (act8 ? align256(R * 4) : 0);
+  // (FP8 activations: x_perm's codes, their scales, then h's codes and scales)
+  const size_t hq_off = h_bytes + rows_bytes + (act8 ? align256(R * 4) : 0);
+  const size_t need = hq_off + (act8 ? align256(R * p->ffn) + align256(R * 4) : 0);
   if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const void* rows = x_perm;
@@ -258,7 +263,9 @@ moe_status moe_grouped_swiglu(const moe_problem* p, const void* x_perm, const in
   }
   return run_grouped(path, (int)R, p->d, p->ffn, p->E, p->w_dtype, rows, offsets, w_gate, w_up,
                      w_down, s_gate, s_up, s_down, workspace, y_perm, L.plan, ctx.status, s,
-                     nullptr, nullptr, nullptr, 0, nullptr, nullptr, row_scale);
+                     nullptr, nullptr, nullptr, 0, nullptr, nullptr, row_scale,
+                     act8 ? at<uint8_t>(workspace, hq_off) : nullptr,
+                     act8 ? at<float>(workspace, hq_off + align256(R * p->ffn)) : nullptr);
 }
 
 moe_status moe_quantize_rows_e4m3(int32_t rows, int32_t cols, const void* x, uint8_t* codes,
@@ -405,7 +412,8 @@ moe_status layer_forward_impl(const moe_problem* p, const void* x, const void* w
                       w_down, s_gate, s_up, s_down, h, y, L.plan, ctx.status, s,
                       timer ? timer->ev[3] : nullptr, gather ? perm_token : nullptr, x_src, p->T,
                       at<float>(workspace, L.gu_part), L.cnt_routed ? at<int>(workspace, L.gu_cnt) : nullptr,
-                      x_scale));
+                      x_scale, act8 ? at<uint8_t>(workspace, L.h_q) : nullptr,
+                      act8 ? at<float>(workspace, L.h_scale) : nullptr));
   MOE_TRY(mark(4));
   // 4. shared expert (CUDA-core path: here, one group {0, T}); on the
   // tensor path, join the side stream
@@ -528,6 +536,7 @@ moe_status moe_layer_launch_count(const moe_problem* p, int32_t* launches) {
   const Layout L0 = layout(*p, path, ctx.num_sms, true);
   n += permute_launch_count(p->T, p->k, !L0.gather);
   if (L0.gather && fp8_weights(p->w_dtype)) n += 1;  // x -> f16, or x -> E4M3 codes
+  if (p->w_dtype == MOE_FP8_E4M3_ACT8) n += 1;        // h -> E4M3 codes
   const Layout L = layout(*p, path, ctx.num_sms, true);
   n += 2;                        // gate/up, down
   // split-K gate/up: a finalize pass unless the GEMM finalizes itself

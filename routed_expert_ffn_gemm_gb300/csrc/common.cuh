@@ -202,10 +202,11 @@ int permute_launch_count(int T, int k, bool move_rows);
 moe_status permute_launch(const PermuteArgs& a, cudaStream_t s);
 // bf16 rows -> f16 rows (saturating), n elements, n % 8 == 0.
 moe_status bf16_to_f16_launch(const void* src, void* dst, size_t n, cudaStream_t s);
-// Per-row E4M3 codes [rows, d] and fp32 scales [rows] of bf16 rows x
-// (scale = row absmax / 448; FP8-activation mode of the gate/up GEMM).
+// Per-row E4M3 codes [rows, d] and fp32 scales [rows] of 16-bit rows x
+// (bf16, or f16 with f16_in; scale = row absmax / 448): the FP8-activation
+// mode's operands of both expert GEMMs.
 moe_status quantize_rows_e4m3_launch(const void* x, int rows, int d, void* codes, float* scales,
-                                     int num_sms, cudaStream_t s);
+                                     int num_sms, cudaStream_t s, bool f16_in = false);
 
 struct CombineArgs {
   int T, k, d, act_dtype;
@@ -270,8 +271,11 @@ struct TcGroupedArgs {
   int* gu_cnt;
   // FP8 activations (w_dtype MOE_FP8_E4M3_ACT8): x_perm / x_src hold E4M3
   // codes and row_scale their per-row scales ([T_src] with gather_rows,
-  // else [R])
+  // else [R]); h_q [R, ffn] / h_scale [R] receive h's codes and row scales
+  // for the down GEMM
   const float* row_scale;
+  void* h_q;
+  float* h_scale;
 };
 // Arrival counters the fused gate/up finalize needs for R rows in G groups.
 size_t gu_counters_size(int R, int G, int ffn, const TcPlan& plan);

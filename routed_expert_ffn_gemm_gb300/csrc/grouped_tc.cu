@@ -687,10 +687,10 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
                 // E4M3 x E4M3: K = 32 per instruction, 32 bytes per step
                 if (PAIR) {
                   ptx::mma_f8_pair(d0, da0 + ka, db, idesc, acc);
-                  ptx::mma_f8_pair(d1, da1 + ka, db, idesc, acc);
+                  if (MODE == kGateUp) ptx::mma_f8_pair(d1, da1 + ka, db, idesc, acc);
                 } else {
                   ptx::mma_f8(d0, da0 + ka, db, idesc, acc);
-                  ptx::mma_f8(d1, da1 + ka, db, idesc, acc);
+                  if (MODE == kGateUp) ptx::mma_f8(d1, da1 + ka, db, idesc, acc);
                 }
               } else if (PAIR) {
                 ptx::mma_f16_pair(d0, da0 + ka, db, idesc, acc);
@@ -811,18 +811,19 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
           const uint32_t* a = ra + 16 * hlf;
           const uint32_t* b = rb + 16 * hlf;
           if (nj > 0) {
-            if (MODE == kGateUp) {
-              // FP8 activations: each column (token row) carries its row's
-              // quantisation scale (rows gathered by token: the token's)
-              float rsc[16];
+            // FP8 activations: each column (token row, or row of h) carries
+            // its row's quantisation scale (rows gathered by token: the
+            // token's)
+            float rsc[16];
 #pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                rsc[j] = 1.f;
-                if (A8 && j < nj) {
-                  const int r = x.row0 + cb + j;
-                  rsc[j] = p.row_scale[p.gather_rows != nullptr ? p.gather_rows[r] : r];
-                }
+            for (int j = 0; j < 16; ++j) {
+              rsc[j] = 1.f;
+              if (A8 && j < nj) {
+                const int r = x.row0 + cb + j;
+                rsc[j] = p.row_scale[p.gather_rows != nullptr ? p.gather_rows[r] : r];
               }
+            }
+            if (MODE == kGateUp) {
               if (p.out_f32) {
                 // K-split: scaled fp32 partials, SiLU*mul after the in-order sum
                 float* row = static_cast<float*>(p.out) + ((size_t)x.ks * p.R + x.row0 + cb) * 2 * p.M + ch;
@@ -853,12 +854,12 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
               float* o = static_cast<float*>(p.out) + ((size_t)x.ks * p.R + x.row0 + cb) * p.M + ch;
 #pragma unroll
               for (int j = 0; j < 16; ++j, o += p.M)
-                if (j < nj) *o = __uint_as_float(a[j]) * sc0;
+                if (j < nj) *o = __uint_as_float(a[j]) * sc0 * rsc[j];
             } else {
               __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + (size_t)(x.row0 + cb) * p.M + ch;
 #pragma unroll
               for (int j = 0; j < 16; ++j, o += p.M)
-                if (j < nj) store_out(o, __uint_as_float(a[j]) * sc0);
+                if (j < nj) store_out(o, __uint_as_float(a[j]) * sc0 * rsc[j]);
             }
           }
           asm volatile("" ::: "memory");
@@ -1133,10 +1134,8 @@ moe_status launch_mode(int bn, int wf, bool pair, const TcParams& p, const CUten
     MOE_LAUNCH(256, kWMx4, true);
     MOE_LAUNCH(128, kWBf16, true);
     MOE_LAUNCH(256, kWBf16, true);
-    if constexpr (MODE == kGateUp) {
-      MOE_LAUNCH(128, kWFp8Act8, true);
-      MOE_LAUNCH(256, kWFp8Act8, true);
-    }
+    MOE_LAUNCH(128, kWFp8Act8, true);
+    MOE_LAUNCH(256, kWFp8Act8, true);
     return MOE_ERR_UNSUPPORTED;
   }
   MOE_LAUNCH(32, kWFp8, false);
@@ -1148,11 +1147,9 @@ moe_status launch_mode(int bn, int wf, bool pair, const TcParams& p, const CUten
   MOE_LAUNCH(32, kWBf16, false);
   MOE_LAUNCH(128, kWBf16, false);
   MOE_LAUNCH(256, kWBf16, false);
-  if constexpr (MODE == kGateUp) {
-    MOE_LAUNCH(32, kWFp8Act8, false);
-    MOE_LAUNCH(128, kWFp8Act8, false);
-    MOE_LAUNCH(256, kWFp8Act8, false);
-  }
+  MOE_LAUNCH(32, kWFp8Act8, false);
+  MOE_LAUNCH(128, kWFp8Act8, false);
+  MOE_LAUNCH(256, kWFp8Act8, false);
 #undef MOE_LAUNCH
   return MOE_ERR_UNSUPPORTED;
 }
@@ -1254,10 +1251,10 @@ TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype) {
   const bool fp8 = w_dtype == MOE_FP8_E4M3 || act8 || w_dtype == MOE_MXFP4;
   const bool dec_pairs = pairs_ok && pe != nullptr && pe[0] == '2';
   const bool dec_pair_gu = dec_pairs && fp8 && !act8 && pl.bn_gateup == 32 && ffn % (2 * kBM) == 0;
-  const bool dec_pair_dn = dec_pairs && fp8 && pl.bn_down == 32 && d % (2 * kBM) == 0;
+  const bool dec_pair_dn = dec_pairs && fp8 && !act8 && pl.bn_down == 32 && d % (2 * kBM) == 0;
   // K per stage: 128 on the FP8 tensor-memory operand path (decode tiles)
   // and with FP8 activations (128-byte rows of both operands)
-  const int kw_dn = fp8 && pl.bn_down == 32 ? 2 * kBK : kBK;
+  const int kw_dn = act8 || (fp8 && pl.bn_down == 32) ? 2 * kBK : kBK;
   const int kw_gu = act8 || (fp8 && pl.bn_gateup == 32) ? 2 * kBK : kBK;
   const int ch_dn = dec_pair_dn ? 2 * kBM : kBM, ch_gu = dec_pair_gu ? 2 * kBM : kBM;
   pl.splits_down = choose_splits(tiles_of(pl.bn_down) * (d / ch_dn), (ffn + kw_dn - 1) / kw_dn, num_sms);
@@ -1281,9 +1278,9 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   const bool fp8 = a.w_dtype == MOE_FP8_E4M3 || act8 || mx4;  // quantised weights: f16 operands, f16 h
   if (!fp8 && a.w_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   if (fp8 && (a.s_gate == nullptr || a.s_up == nullptr || a.s_down == nullptr)) return MOE_ERR_INVALID_ARG;
-  if (act8 && a.row_scale == nullptr) return MOE_ERR_INVALID_ARG;
+  if (act8 && (a.row_scale == nullptr || a.h_q == nullptr || a.h_scale == nullptr)) return MOE_ERR_INVALID_ARG;
   const int wf_gu = act8 ? kWFp8Act8 : mx4 ? kWMx4 : fp8 ? kWFp8 : kWBf16;
-  const int wf_dn = mx4 ? kWMx4 : fp8 ? kWFp8 : kWBf16;
+  const int wf_dn = act8 ? kWFp8Act8 : mx4 ? kWMx4 : fp8 ? kWFp8 : kWBf16;
   if (a.d % kBM != 0 || a.ffn % kBM != 0 || a.G > kMaxGroups) return MOE_ERR_UNSUPPORTED;
   // weights: bf16 tiles [128 x 64] with 128-byte swizzle, or E4M3 tiles
   // [128 x 64 bytes] staged unswizzled for the converters
@@ -1298,10 +1295,10 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   // unswizzled (64 of K); the block scales [G, K/32, M] as a 2-D byte
   // array [G*K/32, M], one box of (K per stage / 32) x 128 per tile
   const bool ta_gu = ta_config(kGateUp, plan.bn_gateup, fp8 && !act8, plan.pair_gateup != 0);
-  const bool ta_dn = ta_config(kDown, plan.bn_down, fp8, plan.pair_down != 0);
+  const bool ta_dn = ta_config(kDown, plan.bn_down, fp8 && !act8, plan.pair_down != 0);
   const int wsw_gu = mx4 ? (ta_gu ? 64 : 0) : !fp8 || ta_gu || act8 ? 128 : 0;
-  const int wsw_dn = mx4 ? (ta_dn ? 64 : 0) : !fp8 || ta_dn ? 128 : 0;
-  const int kw_gu = ta_gu || act8 ? 2 * kBK : kBK, kw_dn = ta_dn ? 2 * kBK : kBK;  // K per stage
+  const int wsw_dn = mx4 ? (ta_dn ? 64 : 0) : !fp8 || ta_dn || act8 ? 128 : 0;
+  const int kw_gu = ta_gu || act8 ? 2 * kBK : kBK, kw_dn = ta_dn || act8 ? 2 * kBK : kBK;  // K per stage
   const int wk_gu = mx4 ? kw_gu / 2 : kw_gu, wk_dn = mx4 ? kw_dn / 2 : kw_dn;    // box columns
   const uint64_t wcols_gu = mx4 ? a.d / 2 : a.d, wcols_dn = mx4 ? a.ffn / 2 : a.ffn;
   CUtensorMap wg, wu, xb, wd, hb, sg, su, sd;
@@ -1334,7 +1331,11 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
     MOE_TRY(make_tmap_kpair(&hb, a.h, a.R, a.ffn, 2, plan.bn_down / 2));
   } else {
     MOE_TRY(make_tmap_2d(&wd, a.w_down, (uint64_t)a.G * a.d, wcols_dn, wb, kBM, wk_dn, wsw_dn));
-    MOE_TRY(make_tmap_2d(&hb, a.h, a.R, a.ffn, 2, box_dn, kBK, 128));
+    // h rows: 16-bit, or (FP8 activations) their E4M3 codes, 128-byte rows
+    if (act8)
+      MOE_TRY(make_tmap_2d(&hb, a.h_q, a.R, a.ffn, 1, box_dn, 2 * kBK, 128));
+    else
+      MOE_TRY(make_tmap_2d(&hb, a.h, a.R, a.ffn, 2, box_dn, kBK, 128));
   }
 
   TcParams p{};
@@ -1381,6 +1382,8 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
                             static_cast<__nv_bfloat16*>(a.h)));
   }
   if (mid != nullptr) MOE_TRY_CUDA(record_event(mid, s));
+  // FP8 activations: h's rows quantised per row for the down GEMM
+  if (act8) MOE_TRY(quantize_rows_e4m3_launch(a.h, a.R, a.ffn, a.h_q, a.h_scale, plan.grid, s, true));
 
   p.M = a.d;
   p.K = a.ffn;
@@ -1389,6 +1392,7 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   p.out_f32 = plan.splits_down > 1 ? 1 : 0;
   p.scale0 = a.s_down;
   p.scale1 = nullptr;
+  p.row_scale = act8 ? a.h_scale : nullptr;
   p.boxn = k2_dn ? plan.bn_down / 2 : box_dn;
   MOE_TRY(launch_mode<kDown>(plan.bn_down, wf_dn, plan.pair_down != 0, p, wd, wd, hb, sd, sd, plan.grid, s));
   return MOE_OK;

@@ -1,14 +1,16 @@
-// Per-row E4M3 quantisation of token rows for the FP8-activation mode of
-// the routed experts' gate/up GEMM ("MOE推理流程解析", section 三: the
-// activations may be quantised before dispatch, so the permuted rows carry
-// fewer bytes; "MoE 推理部署", section 专家量化: FP8 inference).
+// Per-row E4M3 quantisation of activation rows for the FP8-activation mode
+// of the routed experts ("MOE推理流程解析", section 三: the activations may
+// be quantised before dispatch, so the permuted rows carry fewer bytes;
+// "MoE 推理部署", section 专家量化: FP8 inference): the token rows before
+// the gate/up GEMM, the rows of h before the down GEMM.
 //
-// Row t of x [rows, d] (bf16) becomes
+// Row t of x [rows, d] (bf16, or f16: the rows of h) becomes
 //   s_t     = max_i |x[t,i]| / 448     (1 for an all-zero row)
 //   q[t,i]  = E4M3(x[t,i] / s_t)       round to nearest, ties to even,
 //                                      magnitudes past 448 saturate to 448
 // with both divisions correctly rounded in fp32, so that the codes are a
 // function of the stored inputs alone.
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -18,8 +20,17 @@ namespace {
 
 constexpr int kQThreads = 128;
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+// The two 16-bit values of a word as fp32 (exact): bf16, or f16.
+template <bool F16>
+__device__ __forceinline__ float lo16(uint32_t w) {
+  if constexpr (F16) return __half2float(__ushort_as_half((unsigned short)(w & 0xffffu)));
+  return __uint_as_float(w << 16);
+}
+template <bool F16>
+__device__ __forceinline__ float hi16(uint32_t w) {
+  if constexpr (F16) return __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+  return __uint_as_float(w & 0xffff0000u);
+}
 
 __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
@@ -29,6 +40,7 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
 // (16 bytes) at a time.  Pass 1 finds the row's absolute maximum, pass 2
 // re-reads the row (L1/L2-resident: at most a few tens of KB) and writes the
 // codes, 8 bytes per thread.
+template <bool F16>
 __global__ void __launch_bounds__(kQThreads) quantize_rows_e4m3_kernel(const uint4* __restrict__ x, int rows,
                                                                        int vpr, uint2* __restrict__ codes,
                                                                        float* __restrict__ scales) {
@@ -41,7 +53,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_rows_e4m3_kernel(const uin
       const uint4 q = xr[v];
       const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+      for (int i = 0; i < 4; ++i) m = fmaxf(m, fmaxf(fabsf(lo16<F16>(w[i])), fabsf(hi16<F16>(w[i]))));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -58,7 +70,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_rows_e4m3_kernel(const uin
       const uint32_t w[4] = {q.x, q.y, q.z, q.w};
       uint32_t c[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) c[i] = e4m3x2(__fdiv_rn(bf16_lo(w[i]), s), __fdiv_rn(bf16_hi(w[i]), s));
+      for (int i = 0; i < 4; ++i) c[i] = e4m3x2(__fdiv_rn(lo16<F16>(w[i]), s), __fdiv_rn(hi16<F16>(w[i]), s));
       cr[v] = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
     }
     __syncthreads();  // red[] is rewritten by the next row
@@ -68,12 +80,16 @@ __global__ void __launch_bounds__(kQThreads) quantize_rows_e4m3_kernel(const uin
 }  // namespace
 
 moe_status quantize_rows_e4m3_launch(const void* x, int rows, int d, void* codes, float* scales,
-                                     int num_sms, cudaStream_t s) {
+                                     int num_sms, cudaStream_t s, bool f16_in) {
   if (rows == 0) return MOE_OK;
   if (rows < 0 || d <= 0 || d % 8 != 0) return MOE_ERR_UNSUPPORTED;
   const int blocks = rows < 16 * num_sms ? rows : 16 * num_sms;
-  MOE_TRY_CUDA(launch_k(quantize_rows_e4m3_kernel, dim3(blocks), dim3(kQThreads), 0, s,
-                        static_cast<const uint4*>(x), rows, d / 8, static_cast<uint2*>(codes), scales));
+  if (f16_in)
+    MOE_TRY_CUDA(launch_k(quantize_rows_e4m3_kernel<true>, dim3(blocks), dim3(kQThreads), 0, s,
+                          static_cast<const uint4*>(x), rows, d / 8, static_cast<uint2*>(codes), scales));
+  else
+    MOE_TRY_CUDA(launch_k(quantize_rows_e4m3_kernel<false>, dim3(blocks), dim3(kQThreads), 0, s,
+                          static_cast<const uint4*>(x), rows, d / 8, static_cast<uint2*>(codes), scales));
   MOE_TRY_CUDA(cudaGetLastError());
   return MOE_OK;
 }
