@@ -147,7 +147,9 @@ def _random_idx(T, E, k, rng, skew=False):
 
 @pytest.mark.parametrize("T,E,k,skew", [(1, 8, 2, False), (64, 8, 2, False), (128, 128, 8, False),
                                         (256, 8, 8, False), (257, 8, 8, False), (1000, 64, 6, True),
-                                        (8192, 128, 8, True), (4096, 256, 8, False), (3, 1024, 32, False)])
+                                        (8192, 128, 8, True), (4096, 256, 8, False), (3, 1024, 32, False),
+                                        # half a million rows through the chunked path
+                                        (65536, 128, 8, False)])
 def test_permute_bit_exact(T, E, k, skew):
     rng = np.random.default_rng(T + E + k)
     idx = _random_idx(T, E, k, rng, skew)
@@ -423,7 +425,9 @@ def test_worked_example_combine_on_gpu():
 
 
 @pytest.mark.parametrize("T,d,f,E,k", [(300, 256, 384, 16, 4), (7, 128, 256, 8, 2), (1, 256, 128, 4, 4),
-                                       (2100, 128, 128, 32, 1)])
+                                       (2100, 128, 128, 32, 1),
+                                       # the largest expert count and top-k the library takes
+                                       (64, 128, 128, 1024, 32), (3, 256, 128, 1024, 32)])
 def test_layer_bf16_small_multi_tile(T, d, f, E, k):
     shape = inputs.MoEShape("small", T=T, d=d, ffn=f, E=E, k=k)
     _layer_check(shape, 1, BF16_TOL)
