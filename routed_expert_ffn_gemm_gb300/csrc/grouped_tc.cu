@@ -1132,6 +1132,7 @@ moe_status launch_mode(int bn, int wf, bool pair, const TcParams& p, const CUten
     MOE_LAUNCH(32, kWMx4, true);
     MOE_LAUNCH(128, kWMx4, true);
     MOE_LAUNCH(256, kWMx4, true);
+    MOE_LAUNCH(32, kWBf16, true);
     MOE_LAUNCH(128, kWBf16, true);
     MOE_LAUNCH(256, kWBf16, true);
     MOE_LAUNCH(128, kWFp8Act8, true);
@@ -1241,24 +1242,35 @@ TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype) {
     const double a = R / bn_;
     return (int)(touched > a ? touched : a + 0.5);
   };
-  // CTA pairs.  MOE_PAIR=0 keeps single CTAs; MOE_PAIR=2 also runs the
-  // FP8 decode tiles on pairs (supported and tested, but measured no faster
-  // on GB300: each CTA's tensor core still consumes its own f16 weight
-  // tile, whose bytes per stage bound the FP8 decode tiles either way).
+  // CTA pairs.  MOE_PAIR=0 keeps single CTAs; MOE_PAIR=2 also runs every
+  // decode tile on pairs.  By default the decode (32-row) tiles of the bf16
+  // down GEMM take pairs when that needs no more K splits: measured 5-11 %
+  // faster on the down GEMM (fewer, larger units); FP8 decode tiles and the
+  // gate/up GEMM's decode tiles measured no faster on pairs (each CTA's
+  // tensor core still consumes its own weight tile).
   const char* pe = getenv("MOE_PAIR");
   const bool pairs_ok = !(pe != nullptr && pe[0] == '0') && num_sms >= 2;
   const bool act8 = w_dtype == MOE_FP8_E4M3_ACT8;
   const bool fp8 = w_dtype == MOE_FP8_E4M3 || act8 || w_dtype == MOE_MXFP4;
   const bool dec_pairs = pairs_ok && pe != nullptr && pe[0] == '2';
-  const bool dec_pair_gu = dec_pairs && fp8 && !act8 && pl.bn_gateup == 32 && ffn % (2 * kBM) == 0;
-  const bool dec_pair_dn = dec_pairs && fp8 && !act8 && pl.bn_down == 32 && d % (2 * kBM) == 0;
-  // K per stage: 128 on the FP8 tensor-memory operand path (decode tiles)
-  // and with FP8 activations (128-byte rows of both operands)
+  // K per stage: 128 on the FP8 tensor-memory operand path (decode tiles),
+  // with FP8 activations (128-byte rows of both operands), and for the bf16
+  // down GEMM on pairs (two column blocks per copy)
   const int kw_dn = act8 || (fp8 && pl.bn_down == 32) ? 2 * kBK : kBK;
   const int kw_gu = act8 || (fp8 && pl.bn_gateup == 32) ? 2 * kBK : kBK;
-  const int ch_dn = dec_pair_dn ? 2 * kBM : kBM, ch_gu = dec_pair_gu ? 2 * kBM : kBM;
-  pl.splits_down = choose_splits(tiles_of(pl.bn_down) * (d / ch_dn), (ffn + kw_dn - 1) / kw_dn, num_sms);
-  pl.splits_gateup = choose_splits(tiles_of(pl.bn_gateup) * (ffn / ch_gu), (d + kw_gu - 1) / kw_gu, num_sms);
+  // K splits of single-CTA units, and of pair units (2 SMs each, 256
+  // channels, 128 of K per stage)
+  const int kb_dn = (ffn + kw_dn - 1) / kw_dn, kb_dn_pair = (ffn + 2 * kBK - 1) / (2 * kBK);
+  const int s_dn = choose_splits(tiles_of(pl.bn_down) * (d / kBM), kb_dn, num_sms);
+  const int s_dn_pair = choose_splits(tiles_of(pl.bn_down) * (d / (2 * kBM)), kb_dn_pair, num_sms / 2);
+  const bool dn_pair_fits = !act8 && pl.bn_down == 32 && d % (2 * kBM) == 0;
+  const bool dec_pair_dn = dn_pair_fits && (dec_pairs || (pairs_ok && w_dtype == MOE_BF16 && s_dn_pair <= s_dn));
+  const bool dec_pair_gu = dec_pairs && !act8 && pl.bn_gateup == 32 && ffn % (2 * kBM) == 0;
+  pl.splits_down = dec_pair_dn ? s_dn_pair : s_dn;
+  pl.splits_gateup = dec_pair_gu
+                         ? choose_splits(tiles_of(pl.bn_gateup) * (ffn / (2 * kBM)), (d + 2 * kBK - 1) / (2 * kBK),
+                                         num_sms / 2)
+                         : choose_splits(tiles_of(pl.bn_gateup) * (ffn / kBM), (d + kw_gu - 1) / kw_gu, num_sms);
   if (env_int("MOE_SPLITS_GATEUP") >= 1 && env_int("MOE_SPLITS_GATEUP") <= 8)
     pl.splits_gateup = env_int("MOE_SPLITS_GATEUP");
   pl.grid = num_sms;

@@ -277,9 +277,7 @@ def _fp8_stack(E, rows, cols, gen, all_codes_expert=None):
 def test_grouped_swiglu_every_tile_size(bn, pair, fp8, monkeypatch):
     # the same ragged groups through each tile-row count of both GEMMs, on
     # single CTAs and on CTA pairs (256 output channels per tile; 32-row
-    # tiles run on pairs with FP8 weights only)
-    if bn == 32 and pair and not fp8:
-        pytest.skip("32-row tiles take CTA pairs with FP8 weights only")
+    # tiles on pairs with MOE_PAIR=2)
     monkeypatch.setenv("MOE_BN_GATEUP", str(bn))
     monkeypatch.setenv("MOE_BN_DOWN", str(bn))
     monkeypatch.setenv("MOE_PAIR", str(2 if pair and bn == 32 else pair))  # 2: pairs at decode tiles too
@@ -499,8 +497,8 @@ def test_layer_gateup_split_k(splits, bn, d, pair, wfmt, monkeypatch):
     # bn=256 forces the 256-row tile through the same partials; ceil-sized
     # splits can leave the last ones without k-blocks (d=640 in 64-element
     # blocks over 8 splits, d=512 in the 128-element FP8 decode blocks)
-    if pair and wfmt != "fp8":
-        pytest.skip("decode tiles run on CTA pairs with FP8 weights and f16 activations only")
+    if pair and wfmt == "fp8a8":
+        pytest.skip("decode tiles of the FP8-activation mode run on single CTAs")
     monkeypatch.setenv("MOE_SPLITS_GATEUP", str(splits))
     monkeypatch.setenv("MOE_PAIR", str(2 * pair))  # 2: FP8 decode tiles on CTA pairs
     if bn:
@@ -509,9 +507,9 @@ def test_layer_gateup_split_k(splits, bn, d, pair, wfmt, monkeypatch):
                             wfmt=wfmt)
     info = api.moe_plan_info(api.problem_of(shape))
     assert info["splits_gateup"] == splits
-    # FP8 decode tiles run on CTA pairs (split-K partials and the fused
-    # finalize per CTA of the pair); bf16 decode tiles stay on single CTAs
-    assert info["pair_gateup"] == (pair if wfmt == "fp8" and not bn else 0)
+    # decode tiles on CTA pairs (MOE_PAIR=2): split-K partials and the fused
+    # finalize per CTA of the pair
+    assert info["pair_gateup"] == (pair if not bn else 0)
     _layer_check(shape, 4, FP8_TOL if wfmt != "bf16" else BF16_TOL)
 
 
