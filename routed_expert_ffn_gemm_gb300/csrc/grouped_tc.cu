@@ -1135,6 +1135,7 @@ moe_status launch_mode(int bn, int wf, bool pair, const TcParams& p, const CUten
     MOE_LAUNCH(32, kWBf16, true);
     MOE_LAUNCH(128, kWBf16, true);
     MOE_LAUNCH(256, kWBf16, true);
+    MOE_LAUNCH(32, kWFp8Act8, true);
     MOE_LAUNCH(128, kWFp8Act8, true);
     MOE_LAUNCH(256, kWFp8Act8, true);
     return MOE_ERR_UNSUPPORTED;
@@ -1245,9 +1246,9 @@ TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype) {
   // CTA pairs.  MOE_PAIR=0 keeps single CTAs; MOE_PAIR=2 also runs every
   // decode tile on pairs.  By default the decode (32-row) tiles of the bf16
   // down GEMM take pairs when that needs no more K splits: measured 5-11 %
-  // faster on the down GEMM (fewer, larger units); FP8 decode tiles and the
-  // gate/up GEMM's decode tiles measured no faster on pairs (each CTA's
-  // tensor core still consumes its own weight tile).
+  // faster on the down GEMM (fewer, larger units).  The FP8 and
+  // FP8-activation decode tiles and the gate/up GEMM's decode tiles
+  // measured no faster on pairs (within 1-2 %).
   const char* pe = getenv("MOE_PAIR");
   const bool pairs_ok = !(pe != nullptr && pe[0] == '0') && num_sms >= 2;
   const bool act8 = w_dtype == MOE_FP8_E4M3_ACT8;
@@ -1263,9 +1264,9 @@ TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype) {
   const int kb_dn = (ffn + kw_dn - 1) / kw_dn, kb_dn_pair = (ffn + 2 * kBK - 1) / (2 * kBK);
   const int s_dn = choose_splits(tiles_of(pl.bn_down) * (d / kBM), kb_dn, num_sms);
   const int s_dn_pair = choose_splits(tiles_of(pl.bn_down) * (d / (2 * kBM)), kb_dn_pair, num_sms / 2);
-  const bool dn_pair_fits = !act8 && pl.bn_down == 32 && d % (2 * kBM) == 0;
+  const bool dn_pair_fits = pl.bn_down == 32 && d % (2 * kBM) == 0;
   const bool dec_pair_dn = dn_pair_fits && (dec_pairs || (pairs_ok && w_dtype == MOE_BF16 && s_dn_pair <= s_dn));
-  const bool dec_pair_gu = dec_pairs && !act8 && pl.bn_gateup == 32 && ffn % (2 * kBM) == 0;
+  const bool dec_pair_gu = dec_pairs && pl.bn_gateup == 32 && ffn % (2 * kBM) == 0;
   pl.splits_down = dec_pair_dn ? s_dn_pair : s_dn;
   pl.splits_gateup = dec_pair_gu
                          ? choose_splits(tiles_of(pl.bn_gateup) * (ffn / (2 * kBM)), (d + 2 * kBK - 1) / (2 * kBK),

@@ -497,8 +497,6 @@ def test_layer_gateup_split_k(splits, bn, d, pair, wfmt, monkeypatch):
     # bn=256 forces the 256-row tile through the same partials; ceil-sized
     # splits can leave the last ones without k-blocks (d=640 in 64-element
     # blocks over 8 splits, d=512 in the 128-element FP8 decode blocks)
-    if pair and wfmt == "fp8a8":
-        pytest.skip("decode tiles of the FP8-activation mode run on single CTAs")
     monkeypatch.setenv("MOE_SPLITS_GATEUP", str(splits))
     monkeypatch.setenv("MOE_PAIR", str(2 * pair))  # 2: FP8 decode tiles on CTA pairs
     if bn:
