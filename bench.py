@@ -374,14 +374,13 @@ def run_ours(args, shape, ws, rank, local):
         c["x"] = xs[i % n_x]
         return c
 
-    def fwd(i, timer=None, x=None, want_counts=False, out_=None):
+    def fwd(i, timer=None, x=None, want_counts=False):
         c = case(i)
         if x is not None:
             c["x"] = x
         args_ = (p, c["x"], c["w_router"], c["router_bias"], c["w_gate"], c["w_up"], c["w_down"],
                  c["s_gate"], c["s_up"], c["s_down"], c["w_shared_gate"], c["w_shared_up"],
-                 c["w_shared_down"], out if out_ is None else out_, None, None,
-                 counts if want_counts else None, wsp)
+                 c["w_shared_down"], out, None, None, counts if want_counts else None, wsp)
         if timer is None:
             api.moe_layer_forward(*args_)
         else:
@@ -496,78 +495,30 @@ def run_ours(args, shape, ws, rank, local):
     lb, lf = work["layer"]
     layer_s = ms / 1e3 / args.steps
 
-    # ---- end to end: pinned host inputs in, result out, every step.  For
-    # steps of 0.1 ms or more the copies run on their own streams,
-    # double-buffered, so the H2D copy of step i+1 and the D2H read of step
-    # i-1 overlap step i's layer (as a serving loop would); shorter steps are
-    # bound by the host issuing them, and run the three calls in sequence.
-    # Either way every byte crosses inside the timed region.
+    # ---- end to end: pinned host inputs in, result out, every step
     e2e = None
-    pipelined = ms / args.steps >= 0.1
-    if not args.no_e2e and not pipelined:
+    if not args.no_e2e:
         xh = [x.cpu().pin_memory() for x in xs]
-        xd1 = torch.empty_like(xs[0])
-        oh1 = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        xd = torch.empty_like(xs[0])
+        oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         for i in range(min(args.warmup, 5)):
-            xd1.copy_(xh[i % n_x], non_blocking=True)
-            fwd(i, x=xd1)
-            oh1.copy_(out, non_blocking=True)
+            xd.copy_(xh[i % n_x], non_blocking=True)
+            fwd(i, x=xd)
+            oh.copy_(out, non_blocking=True)
         torch.cuda.synchronize()
         barrier(ws)
         e0.record(stream)
         for i in range(args.steps):
-            xd1.copy_(xh[i % n_x], non_blocking=True)
-            fwd(i, x=xd1)
-            oh1.copy_(out, non_blocking=True)
+            xd.copy_(xh[i % n_x], non_blocking=True)
+            fwd(i, x=xd)
+            oh.copy_(out, non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize()
         barrier(ws)
-    elif not args.no_e2e:
-        xh = [x.cpu().pin_memory() for x in xs]
-        xd = [torch.empty_like(xs[0]) for _ in range(2)]
-        od = [torch.empty_like(out) for _ in range(2)]
-        oh = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
-        h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
-        ev_in = [torch.cuda.Event() for _ in range(2)]
-        ev_done = [torch.cuda.Event() for _ in range(2)]
-        ev_out = [torch.cuda.Event() for _ in range(2)]
-        ev_go = torch.cuda.Event()
-
-        def e2e_steps(n):
-            ev_go.record(stream)
-            h2d.wait_event(ev_go)
-            for i in range(n):
-                b = i % 2
-                with torch.cuda.stream(h2d):
-                    if i >= 2:
-                        h2d.wait_event(ev_done[b])  # step i-2 has read xd[b]
-                    xd[b].copy_(xh[i % n_x], non_blocking=True)
-                    ev_in[b].record(h2d)
-                stream.wait_event(ev_in[b])
-                if i >= 2:
-                    stream.wait_event(ev_out[b])  # od[b] of step i-2 is on the host
-                fwd(i, x=xd[b], out_=od[b])
-                ev_done[b].record(stream)
-                with torch.cuda.stream(d2h):
-                    d2h.wait_event(ev_done[b])
-                    oh[b].copy_(od[b], non_blocking=True)
-                    ev_out[b].record(d2h)
-            stream.wait_event(ev_out[(n - 1) % 2])  # the last result is on the host
-
-        e2e_steps(min(args.warmup, 5))
-        torch.cuda.synchronize()
-        barrier(ws)
-        e0.record(stream)
-        e2e_steps(args.steps)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        barrier(ws)
-    if not args.no_e2e:
         ems = max_over_ranks(e0.elapsed_time(e1), ws, device)
         nb = shape.T * shape.d * abytes(shape)
         e2e = {"value": ws * args.steps * shape.T / (ems / 1e3), "unit": "tokens/s",
-               "h2d_bytes_per_step": nb, "d2h_bytes_per_step": nb,
-               "copies": "overlapped (copy streams, double-buffered)" if pipelined else "in sequence"}
+               "h2d_bytes_per_step": nb, "d2h_bytes_per_step": nb}
     assert api.moe_read_device_status() == 0
 
     cpu = None
