@@ -1,0 +1,77 @@
+"""Host-side logic of bench.py (no GPU): the algorithmic bytes and flops the
+roofline divides by, the storage sizes per weight format, the expected
+touched-expert count, and the DRAM-traffic lookup keyed by kernel source."""
+
+import hashlib
+import os
+
+import pytest
+
+import bench
+from routed_expert_ffn_gemm_gb300 import inputs
+
+
+def test_gate_up_algorithmic_bytes_of_the_headline_layer():
+    # Mixtral-shaped, T=64, top-2 over 8 experts, all 8 touched: two bf16
+    # weight matrices [14336, 4096] per expert, the 128 gathered rows in,
+    # h [128, 14336] out
+    shape = inputs.WORKLOADS["mixtral_8x7b"].with_T(64)
+    work = bench.stage_work(shape, touched=8, splits=7)
+    gu_bytes, gu_flops = work["gate_up"]
+    assert gu_bytes == 8 * 2 * 14336 * 4096 * 2 + 128 * 4096 * 2 + 128 * 14336 * 2
+    assert gu_flops == 4.0 * 128 * 14336 * 4096
+    dn_bytes, dn_flops = work["down"]
+    # down: one matrix per expert, h in, 7 fp32 split partials out
+    assert dn_bytes == 8 * 4096 * 14336 * 2 + 128 * 14336 * 2 + 7 * 128 * 4096 * 4
+    assert dn_flops == 2.0 * 128 * 14336 * 4096
+
+
+@pytest.mark.parametrize("wfmt,bytes_per_weight", [("f32", 4), ("bf16", 2), ("fp8", 1), ("fp8a8", 1),
+                                                   ("mxfp4", 17 / 32)])
+def test_bytes_per_weight(wfmt, bytes_per_weight):
+    shape = inputs.MoEShape("s", T=1, d=128, ffn=128, E=2, k=1, wfmt=wfmt,
+                            act="f32" if wfmt == "f32" else "bf16")
+    assert bench.wbytes(shape) == bytes_per_weight
+
+
+def test_fp8_scales_and_fp8_rows_enter_the_bytes():
+    base = inputs.MoEShape("s", T=4, d=256, ffn=128, E=4, k=2, wfmt="fp8")
+    a8 = inputs.MoEShape("s", T=4, d=256, ffn=128, E=4, k=2, wfmt="fp8a8")
+    b_fp8, _ = bench.stage_work(base, touched=4, splits=1)["gate_up"]
+    b_a8, _ = bench.stage_work(a8, touched=4, splits=1)["gate_up"]
+    # same weights and per-channel scales; the rows are E4M3 codes + one
+    # fp32 scale each instead of bf16
+    R, d = 8, 256
+    assert b_fp8 - b_a8 == R * d * 2 - R * (d + 4)
+
+
+def test_expected_touched_closed_form():
+    shape = inputs.WORKLOADS["deepseek_v3"].with_T(1)
+    assert bench.expected_touched(shape) == pytest.approx(8.0)          # k distinct experts
+    shape = inputs.WORKLOADS["mixtral_8x7b"].with_T(64)
+    assert bench.expected_touched(shape) == pytest.approx(8 * (1 - (6 / 8) ** 64))
+    assert bench.expected_touched(shape.with_T(0)) == 0.0
+
+
+def test_traffic_lookup_follows_the_kernel_source(tmp_path, monkeypatch):
+    (tmp_path / "profiles").mkdir()
+    src_dir = tmp_path / "routed_expert_ffn_gemm_gb300" / "csrc"
+    src_dir.mkdir(parents=True)
+    (src_dir / "grouped_tc.cu").write_bytes(b"kernel v1")
+    sha = hashlib.sha256(b"kernel v1").hexdigest()[:16]
+    (tmp_path / "profiles" / "dram_traffic.txt").write_text(
+        "# comment line\nmixtral_8x7b 64 gate_up %s 1884260104\n" % sha)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    shape = inputs.WORKLOADS["mixtral_8x7b"].with_T(64)
+    assert bench.measured_traffic(shape, "gate_up") == 1884260104.0
+    assert bench.measured_traffic(shape, "down") is None
+    assert bench.measured_traffic(shape.with_T(8), "gate_up") is None
+    # the source changes: the old counters no longer describe the kernel
+    (src_dir / "grouped_tc.cu").write_bytes(b"kernel v2")
+    assert bench.measured_traffic(shape, "gate_up") is None
+
+
+def test_committed_traffic_file_parses():
+    path = os.path.join(bench.ROOT, "profiles", "dram_traffic.txt")
+    rows = [ln.split() for ln in open(path) if ln.strip() and not ln.startswith("#")]
+    assert rows and all(len(r) == 5 and len(r[3]) == 16 and float(r[4]) > 0 for r in rows)

@@ -78,6 +78,13 @@ def _ws_status(lib, p):
     (dict(T=4, d=192, ffn=256, E=8, k=2), api.ERR_UNSUPPORTED),          # tensor path: d % 128
     (dict(T=4, d=128, ffn=256, E=8, k=2, act="f32", wfmt="bf16"), api.ERR_UNSUPPORTED),  # mixed
     (dict(T=4, d=128, ffn=256, E=40, k=33), api.ERR_UNSUPPORTED),        # k > 32
+    # the quantised weight modes take the tensor path only (bf16 activations,
+    # d and ffn multiples of 128)
+    (dict(T=4, d=128, ffn=256, E=8, k=2, act="f32", wfmt="fp8"), api.ERR_UNSUPPORTED),
+    (dict(T=4, d=128, ffn=256, E=8, k=2, act="f32", wfmt="fp8a8"), api.ERR_UNSUPPORTED),
+    (dict(T=4, d=128, ffn=256, E=8, k=2, act="f32", wfmt="mxfp4"), api.ERR_UNSUPPORTED),
+    (dict(T=4, d=192, ffn=256, E=8, k=2, wfmt="fp8a8"), api.ERR_UNSUPPORTED),
+    (dict(T=4, d=128, ffn=320, E=8, k=2, wfmt="mxfp4"), api.ERR_UNSUPPORTED),
 ])
 def test_problem_validation_without_gpu(lib, kw, want):
     assert _ws_status(lib, api.problem(**kw)) == want
@@ -107,3 +114,26 @@ def test_misaligned_pointer_rejected(lib):
     p = api.problem(T=4, d=128, ffn=256, E=8, k=2)
     fake = ctypes.c_void_p(0x1000 + 8)  # never dereferenced: rejected on the host
     assert lib.moe_combine(ctypes.byref(p), fake, fake, fake, None, fake, None) == api.ERR_INVALID_ARG
+
+
+def test_quantize_rows_arguments_checked_before_any_launch(lib):
+    fake = ctypes.c_void_p(0x1000)  # never dereferenced: rejected on the host
+    q = lib.moe_quantize_rows_e4m3
+    assert q(-1, 128, fake, fake, fake, None) == api.ERR_INVALID_ARG        # negative rows
+    assert q(4, 12, fake, fake, fake, None) == api.ERR_UNSUPPORTED          # cols % 8
+    assert q(4, 0, fake, fake, fake, None) == api.ERR_UNSUPPORTED           # no columns
+    assert q(4, 128, None, fake, fake, None) == api.ERR_INVALID_ARG         # null input
+    assert q(4, 128, fake, None, fake, None) == api.ERR_INVALID_ARG         # null codes
+    assert q(4, 128, fake, fake, None, None) == api.ERR_INVALID_ARG         # null scales
+    assert q(4, 128, ctypes.c_void_p(0x1008), fake, fake, None) == api.ERR_INVALID_ARG  # misaligned
+    assert q(0, 128, None, None, None, None) == 0                            # empty: no launch
+
+
+def test_quantised_modes_need_their_scales(lib):
+    # FP8 / MXFP4 weights without scale arrays are rejected on the host
+    fake = ctypes.c_void_p(0x1000)
+    for wfmt in ("fp8", "fp8a8", "mxfp4"):
+        p = api.problem(T=4, d=128, ffn=256, E=8, k=2, wfmt=wfmt)
+        args = [fake, fake, None, fake, fake, fake, None, None, None, None, None, None, fake,
+                None, None, None, fake]
+        assert lib.moe_layer_forward(ctypes.byref(p), *args, 1 << 20, None) == api.ERR_INVALID_ARG
