@@ -39,7 +39,7 @@ moe_status check_problem(const moe_problem* p, Path* path) {
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Quantised routed weights (FP8 or MXFP4): scale arrays required, f16 operands.
-bool fp8_weights(int w_dtype) {
+bool quantised_weights(int w_dtype) {
   return w_dtype == MOE_FP8_E4M3 || w_dtype == MOE_FP8_E4M3_ACT8 || w_dtype == MOE_MXFP4;
 }
 
@@ -233,7 +233,7 @@ moe_status moe_grouped_swiglu(const moe_problem* p, const void* x_perm, const in
   if (!x_perm || !offsets || !w_gate || !w_up || !w_down || !y_perm) return MOE_ERR_INVALID_ARG;
   for (const void* q : {x_perm, w_gate, w_up, w_down, (const void*)y_perm})
     if (!aligned16(q)) return MOE_ERR_INVALID_ARG;
-  const bool fp8 = fp8_weights(p->w_dtype), act8 = p->w_dtype == MOE_FP8_E4M3_ACT8;
+  const bool fp8 = quantised_weights(p->w_dtype), act8 = p->w_dtype == MOE_FP8_E4M3_ACT8;
   if (fp8 != (s_gate != nullptr) || fp8 != (s_up != nullptr) || fp8 != (s_down != nullptr))
     return MOE_ERR_INVALID_ARG;
   DeviceCtx ctx;
@@ -319,7 +319,7 @@ moe_status layer_forward_impl(const moe_problem* p, const void* x, const void* w
   if (!x || !w_router || !w_gate || !w_up || !w_down || !out) return MOE_ERR_INVALID_ARG;
   for (const void* q : {x, w_router, w_gate, w_up, w_down, (const void*)out})
     if (!aligned16(q)) return MOE_ERR_INVALID_ARG;
-  const bool fp8 = fp8_weights(p->w_dtype), act8 = p->w_dtype == MOE_FP8_E4M3_ACT8;
+  const bool fp8 = quantised_weights(p->w_dtype), act8 = p->w_dtype == MOE_FP8_E4M3_ACT8;
   if (fp8 != (s_gate != nullptr) || fp8 != (s_up != nullptr) || fp8 != (s_down != nullptr))
     return MOE_ERR_INVALID_ARG;
   const bool has_shared = p->ffn_shared > 0;
@@ -535,7 +535,7 @@ moe_status moe_layer_launch_count(const moe_problem* p, int32_t* launches) {
   if (fuse_topk_in_permute(p->T, p->k, p->E, rs)) n -= 1;
   const Layout L0 = layout(*p, path, ctx.num_sms, true);
   n += permute_launch_count(p->T, p->k, !L0.gather);
-  if (L0.gather && fp8_weights(p->w_dtype)) n += 1;  // x -> f16, or x -> E4M3 codes
+  if (L0.gather && quantised_weights(p->w_dtype)) n += 1;  // x -> f16, or x -> E4M3 codes
   if (p->w_dtype == MOE_FP8_E4M3_ACT8) n += 1;        // h -> E4M3 codes
   const Layout L = layout(*p, path, ctx.num_sms, true);
   n += 2;                        // gate/up, down
