@@ -386,10 +386,18 @@ def run_ours(args, shape, ws, rank, local):
         else:
             api.moe_layer_forward_timed(*args_, timer)
 
+    def check_status(phase):
+        # a kernel that gave up on a bounded wait (or found an index out of
+        # range) records it in the device status word: stop at the phase
+        # that saw it rather than time hundreds more launches
+        st = api.moe_read_device_status()
+        if st != 0:
+            raise RuntimeError(f"device status {st} ({api.moe_status_string(st)}) after {phase}")
+
     for i in range(args.warmup):
         fwd(i)
     torch.cuda.synchronize()
-    assert api.moe_read_device_status() == 0
+    check_status("warm-up")
 
     # The device-resident legs replay CUDA graphs of the public call (one per
     # weight-set / token-batch combination), so host launch cost does not
@@ -410,6 +418,7 @@ def run_ours(args, shape, ws, rank, local):
         for c in range(combos):
             graphs[c].replay()
         torch.cuda.synchronize()
+        check_status("graph capture and first replay")
 
     def step(i):
         if graphs is None:
@@ -432,6 +441,7 @@ def run_ours(args, shape, ws, rank, local):
     torch.cuda.synchronize()
     barrier(ws)
     sampler.stop()
+    check_status("timed steps")
     value, ms = whole_job_tokens_per_s(e0.elapsed_time(e1), ws, args.steps, shape.T, device)
 
     # ---- per-stage device times (events on the launching stream)
@@ -460,6 +470,7 @@ def run_ours(args, shape, ws, rank, local):
             if i < 16:
                 counts_seen.append(counts.clone())
     torch.cuda.synchronize()
+    check_status("stage timing")
     stage = {s: [] for s in api.STAGES}
     for t in timers:
         for s, v in t.read().items():
@@ -519,7 +530,7 @@ def run_ours(args, shape, ws, rank, local):
         nb = shape.T * shape.d * abytes(shape)
         e2e = {"value": ws * args.steps * shape.T / (ems / 1e3), "unit": "tokens/s",
                "h2d_bytes_per_step": nb, "d2h_bytes_per_step": nb}
-    assert api.moe_read_device_status() == 0
+        check_status("end-to-end steps")
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:

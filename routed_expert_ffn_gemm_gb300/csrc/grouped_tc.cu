@@ -219,6 +219,14 @@ struct Cfg {
   static constexpr int SMEM_BYTES = PREFIX_OFF + 4 * (kMaxGroups + 4) + 1024;
   static_assert(STAGES >= 2, "pipeline too shallow");
   static_assert(SMEM_BYTES <= kSmemLimit, "shared memory budget");
+  // At most one CTA of this kernel (of any instantiation) per SM: every CTA
+  // takes all 512 TMEM columns before griddepcontrol.wait, and a second
+  // co-resident CTA (a launch overlapped by programmatic dependence, or the
+  // shared expert's kernel on the side stream) would block in tcgen05.alloc;
+  // with CTA pairs, two clusters that each hold one SM of a TPC would wait
+  // on each other for good.  Shared memory keeps them apart: two CTAs with
+  // their 1 KB reservations overflow the SM's 228 KB.
+  static_assert(2 * (SMEM_BYTES + 1024) > kSmemLimit + 1024, "one TMEM-holding CTA per SM");
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
   static_assert(BN % 16 == 0 && BN <= 256 && ACC_COLS <= 512, "tile rows");
   static_assert(!PAIR || BN >= 32, "pair tiles split B rows in halves");
