@@ -444,6 +444,24 @@ def run_ours(args, shape, ws, rank, local):
     check_status("timed steps")
     value, ms = whole_job_tokens_per_s(e0.elapsed_time(e1), ws, args.steps, shape.T, device)
 
+    # ---- the same steps as plain launches of the public call (no graph):
+    # what a caller that does not capture graphs sees, host launch cost
+    # included wherever it exceeds the device time
+    plain = None
+    if graphs is not None:
+        n_plain = min(args.steps, 200)
+        barrier(ws)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(n_plain):
+            fwd(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        check_status("plain-launch steps")
+        pv, pms = whole_job_tokens_per_s(e0.elapsed_time(e1), ws, n_plain, shape.T, device)
+        plain = {"value": pv, "unit": "tokens/s", "steps": n_plain, "ms_per_step": pms / n_plain}
+
     # ---- per-stage device times (events on the launching stream)
     ks = min(args.stage_steps, args.steps)
     timers = [api.StageTimer() for _ in range(ks)]
@@ -555,6 +573,7 @@ def run_ours(args, shape, ws, rank, local):
             "stages_us": {s: 1e3 * v for s, v in stage_ms.items()},
             "plan": plan,
             "cuda_graphs": graphs is not None,
+            "plain_launches": plain,
             "gpu_launches": launches * args.steps,
             "clocks": sampler.summary(),
             "e2e": e2e,
