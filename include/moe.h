@@ -84,7 +84,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 3
+#define MOE_ABI_VERSION 4
 
 #if defined(__GNUC__)
 #define MOE_API __attribute__((visibility("default")))
@@ -341,6 +341,21 @@ MOE_API moe_status moe_layer_launch_count(const moe_problem *p, int32_t *launche
  * the fp32 CUDA-core path.
  */
 MOE_API moe_status moe_plan_info(const moe_problem *p, int32_t *info);
+
+/*
+ * moe_plan_info_for, moe_layer_launch_count_for, moe_workspace_size_for --
+ * the same answers as moe_plan_info, moe_layer_launch_count and
+ * moe_workspace_size for a device with `num_sms` multiprocessors, computed
+ * on the host alone: they touch no device and need none (planning ahead of
+ * time, and tests of the tiling rules on machines without a GPU).  The
+ * device entry points are these with the current device's SM count.
+ * Returns MOE_ERR_INVALID_ARG for a null output or num_sms outside
+ * [1, 4096], and MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED for problems the
+ * library rejects.
+ */
+MOE_API moe_status moe_plan_info_for(const moe_problem *p, int32_t num_sms, int32_t *info);
+MOE_API moe_status moe_layer_launch_count_for(const moe_problem *p, int32_t num_sms, int32_t *launches);
+MOE_API moe_status moe_workspace_size_for(const moe_problem *p, int32_t num_sms, size_t *bytes);
 
 /*
  * moe_workspace_size -- device workspace (bytes) sufficient for every entry

@@ -67,6 +67,9 @@ _SIGS = {
     "moe_layer_forward_timed": [_PP] + [_VP] * 17 + [ctypes.c_size_t, _VP, _VP],
     "moe_layer_launch_count": [_PP, ctypes.POINTER(ctypes.c_int32)],
     "moe_plan_info": [_PP, ctypes.POINTER(ctypes.c_int32)],
+    "moe_plan_info_for": [_PP, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)],
+    "moe_layer_launch_count_for": [_PP, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)],
+    "moe_workspace_size_for": [_PP, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t)],
     "moe_permute_static_scratch": [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP],
     "moe_quantize_rows_e4m3": [ctypes.c_int32, ctypes.c_int32, _VP, _VP, _VP, _VP],
 }
@@ -212,16 +215,41 @@ def moe_layer_launch_count(p) -> int:
     return int(n.value)
 
 
+def _plan_dict(info) -> dict:
+    return {"bn_gateup": info[0], "bn_down": info[1], "splits_down": info[2], "grid": info[3],
+            "splits_gateup": info[4], "pair_gateup": info[5] & 1, "pair_down": (info[5] >> 1) & 1}
+
+
 def moe_plan_info(p) -> dict:
     info = (ctypes.c_int32 * 6)()
     _call("moe_plan_info", ctypes.byref(p), info)
-    return {"bn_gateup": info[0], "bn_down": info[1], "splits_down": info[2], "grid": info[3],
-            "splits_gateup": info[4], "pair_gateup": info[5] & 1, "pair_down": (info[5] >> 1) & 1}
+    return _plan_dict(info)
 
 
 def moe_workspace_size(p) -> int:
     n = ctypes.c_size_t(0)
     _call("moe_workspace_size", ctypes.byref(p), ctypes.byref(n))
+    return int(n.value)
+
+
+# The planning answers for a device with `num_sms` SMs, computed on the host
+# (no device needed).
+
+def moe_plan_info_for(p, num_sms: int) -> dict:
+    info = (ctypes.c_int32 * 6)()
+    _call("moe_plan_info_for", ctypes.byref(p), int(num_sms), info)
+    return _plan_dict(info)
+
+
+def moe_layer_launch_count_for(p, num_sms: int) -> int:
+    n = ctypes.c_int32(0)
+    _call("moe_layer_launch_count_for", ctypes.byref(p), int(num_sms), ctypes.byref(n))
+    return int(n.value)
+
+
+def moe_workspace_size_for(p, num_sms: int) -> int:
+    n = ctypes.c_size_t(0)
+    _call("moe_workspace_size_for", ctypes.byref(p), int(num_sms), ctypes.byref(n))
     return int(n.value)
 
 

@@ -38,6 +38,9 @@ moe_status check_problem(const moe_problem* p, Path* path) {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Largest SM count the device-free planning entry points accept.
+constexpr int kMaxPlanSms = 4096;
+
 // Quantised routed weights (FP8 or MXFP4): scale arrays required, f16 operands.
 bool quantised_weights(int w_dtype) {
   return w_dtype == MOE_FP8_E4M3 || w_dtype == MOE_FP8_E4M3_ACT8 || w_dtype == MOE_MXFP4;
@@ -170,14 +173,21 @@ using namespace moe;
 
 extern "C" {
 
+moe_status moe_workspace_size_for(const moe_problem* p, int32_t num_sms, size_t* bytes) {
+  if (bytes == nullptr || num_sms < 1 || num_sms > kMaxPlanSms) return MOE_ERR_INVALID_ARG;
+  Path path;
+  MOE_TRY(check_problem(p, &path));
+  *bytes = layout(*p, path, num_sms, true).total;
+  return MOE_OK;
+}
+
 moe_status moe_workspace_size(const moe_problem* p, size_t* bytes) {
   if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
   Path path;
   MOE_TRY(check_problem(p, &path));
   DeviceCtx ctx;
   MOE_TRY(device_ctx(&ctx));
-  *bytes = layout(*p, path, ctx.num_sms, true).total;
-  return MOE_OK;
+  return moe_workspace_size_for(p, ctx.num_sms, bytes);
 }
 
 moe_status moe_router_topk(const moe_problem* p, const void* x, const void* w_router,
@@ -505,11 +515,22 @@ moe_status moe_plan_info(const moe_problem* p, int32_t* info) {
   if (info == nullptr) return MOE_ERR_INVALID_ARG;
   Path path;
   MOE_TRY(check_problem(p, &path));
-  info[0] = info[1] = info[2] = info[3] = info[4] = info[5] = 0;
-  if (path != Path::kTensor) return MOE_OK;
+  if (path != Path::kTensor) {  // the CUDA-core path has no tiling to report
+    info[0] = info[1] = info[2] = info[3] = info[4] = info[5] = 0;
+    return MOE_OK;
+  }
   DeviceCtx ctx;
   MOE_TRY(device_ctx(&ctx));
-  const Layout L = layout(*p, path, ctx.num_sms, true);
+  return moe_plan_info_for(p, ctx.num_sms, info);
+}
+
+moe_status moe_plan_info_for(const moe_problem* p, int32_t num_sms, int32_t* info) {
+  if (info == nullptr || num_sms < 1 || num_sms > kMaxPlanSms) return MOE_ERR_INVALID_ARG;
+  Path path;
+  MOE_TRY(check_problem(p, &path));
+  info[0] = info[1] = info[2] = info[3] = info[4] = info[5] = 0;
+  if (path != Path::kTensor) return MOE_OK;
+  const Layout L = layout(*p, path, num_sms, true);
   info[0] = L.plan.bn_gateup;
   info[1] = L.plan.bn_down;
   info[2] = L.plan.splits_down;
@@ -529,15 +550,25 @@ moe_status moe_layer_launch_count(const moe_problem* p, int32_t* launches) {
   }
   DeviceCtx ctx;
   MOE_TRY(device_ctx(&ctx));
-  const int rs = router_tc_splits(p->T, p->d, p->E, p->act_dtype, ctx.num_sms, (size_t)-1);
+  return moe_layer_launch_count_for(p, ctx.num_sms, launches);
+}
+
+moe_status moe_layer_launch_count_for(const moe_problem* p, int32_t num_sms, int32_t* launches) {
+  if (launches == nullptr || num_sms < 1 || num_sms > kMaxPlanSms) return MOE_ERR_INVALID_ARG;
+  Path path;
+  MOE_TRY(check_problem(p, &path));
+  if (p->T == 0) {
+    *launches = 0;
+    return MOE_OK;
+  }
+  const int rs = router_tc_splits(p->T, p->d, p->E, p->act_dtype, num_sms, (size_t)-1);
   int n = rs > 0 ? 2 : router_launch_count(p->T, p->E, false, true);
   // the tiny-batch permutation selects the top-k in place of the separate pass
   if (fuse_topk_in_permute(p->T, p->k, p->E, rs)) n -= 1;
-  const Layout L0 = layout(*p, path, ctx.num_sms, true);
-  n += permute_launch_count(p->T, p->k, !L0.gather);
-  if (L0.gather && quantised_weights(p->w_dtype)) n += 1;  // x -> f16, or x -> E4M3 codes
+  const Layout L = layout(*p, path, num_sms, true);
+  n += permute_launch_count(p->T, p->k, !L.gather);
+  if (L.gather && quantised_weights(p->w_dtype)) n += 1;  // x -> f16, or x -> E4M3 codes
   if (p->w_dtype == MOE_FP8_E4M3_ACT8) n += 1;        // h -> E4M3 codes
-  const Layout L = layout(*p, path, ctx.num_sms, true);
   n += 2;                        // gate/up, down
   // split-K gate/up: a finalize pass unless the GEMM finalizes itself
   // (decode tiles)

@@ -596,3 +596,19 @@ def test_layer_launch_count_matches_the_kernels_launched(shape):
         kinds.append(t.value)
     cu.cuGraphDestroy(graph)
     assert kinds.count(0) == api.moe_layer_launch_count(p), kinds  # 0: kernel node
+
+
+@pytest.mark.parametrize("shape", [
+    inputs.WORKLOADS["mixtral_8x7b"].with_T(64),
+    inputs.WORKLOADS["qwen3_30b_a3b"].with_T(1),
+    inputs.WORKLOADS["deepseek_v3"].with_T(4096),
+    inputs.WORKLOADS["toy_f32"],
+], ids=lambda s: f"{s.name}_T{s.T}")
+def test_device_planning_is_the_host_planning_at_the_device_sm_count(shape):
+    # the device entry points answer what the device-free ones answer for
+    # this device's multiprocessor count
+    p = api.problem_of(shape)
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    assert api.moe_plan_info(p) == api.moe_plan_info_for(p, sms)
+    assert api.moe_layer_launch_count(p) == api.moe_layer_launch_count_for(p, sms)
+    assert api.moe_workspace_size(p) == api.moe_workspace_size_for(p, sms)

@@ -58,7 +58,7 @@ def test_binding_arity_matches_header():
 
 
 def test_abi_version_and_status_strings(lib):
-    assert api.moe_abi_version() == 3
+    assert api.moe_abi_version() == 4
     assert api.moe_status_string(0) == "MOE_OK"
     assert api.moe_status_string(api.ERR_DEVICE_TIMEOUT) == "MOE_ERR_DEVICE_TIMEOUT"
     assert api.moe_status_string(-99) == "MOE_ERR_UNKNOWN"
