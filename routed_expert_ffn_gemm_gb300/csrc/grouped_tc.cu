@@ -59,6 +59,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
 #include <type_traits>
 
 #include <cuda_fp16.h>
@@ -1096,11 +1097,13 @@ moe_status launch_one(const TcParams& p, const CUtensorMap& a0, const CUtensorMa
     // The grid is persistent: every pair must be resident at once, and not
     // every SM finds a partner (clusters stay inside a GPC), so take the
     // number of co-resident pairs from the occupancy query (per device).
-    static int resident[64];
+    // (host threads may launch concurrently: each entry is written once,
+    // with the same value by whichever thread gets there)
+    static std::atomic<int> resident[64];
     int dev = 0;
     MOE_TRY_CUDA(cudaGetDevice(&dev));
     if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
-    if (resident[dev] == 0) {
+    if (resident[dev].load(std::memory_order_relaxed) == 0) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(grid & ~1);
       cfg.blockDim = dim3(C::THREADS);
@@ -1114,10 +1117,11 @@ moe_status launch_one(const TcParams& p, const CUtensorMap& a0, const CUtensorMa
       cfg.numAttrs = 1;
       int n = 0;
       MOE_TRY_CUDA(cudaOccupancyMaxActiveClusters(&n, kern, &cfg));
-      resident[dev] = n > 0 ? n : -1;
+      resident[dev].store(n > 0 ? n : -1, std::memory_order_relaxed);
     }
-    if (resident[dev] < 0) return MOE_ERR_UNSUPPORTED;
-    grid = min(grid & ~1, 2 * resident[dev]);
+    const int r = resident[dev].load(std::memory_order_relaxed);
+    if (r < 0) return MOE_ERR_UNSUPPORTED;
+    grid = min(grid & ~1, 2 * r);
   }
   MOE_TRY_CUDA(launch_kc(PAIR ? 2 : 1, kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, s, p, a0, a1, b, s0, s1));
   MOE_TRY_CUDA(cudaGetLastError());
