@@ -11,6 +11,7 @@ first call and a missing library is an error (build it with
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 from typing import Optional
 
@@ -113,6 +114,76 @@ def _ptr(t: Optional[torch.Tensor]):
     return t.data_ptr()
 
 
+# Sizes checked before each call.  The C entry points take bare pointers,
+# so a tensor smaller than the problem says, or of another element size,
+# would be read or written out of bounds on the device; here it is a
+# ValueError instead.  Null pointers, alignment and workspace sizes are the
+# library's own checks.
+
+def _check(t: Optional[torch.Tensor], name: str, elems: int, esize: int, dtype=None):
+    if t is None:
+        return
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name}: dtype {t.dtype}, the call takes {dtype}")
+    if t.element_size() != esize:
+        raise ValueError(f"{name}: {t.element_size()}-byte elements, the problem needs {esize}-byte ones")
+    if t.numel() < elems:
+        raise ValueError(f"{name}: {t.numel()} elements, the problem needs {elems}")
+
+
+def _act_size(p) -> int:
+    return 4 if p.act_dtype == DTYPE["f32"] else 2
+
+
+def _key(p) -> tuple:
+    return (p.T, p.d, p.ffn, p.E, p.k, p.ffn_shared, p.act_dtype, p.w_dtype)
+
+
+@functools.lru_cache(maxsize=256)
+def _expert_reqs(key) -> tuple:
+    """(name, elements, element size, dtype) of the routed expert weights
+    and scales, per weight mode: gate/up [E, ffn, d], down [E, d, ffn]; FP8
+    codes with fp32 scales [E, ffn] / [E, d]; MXFP4 codes two per byte with
+    UE8M0 block scales [E, d/32, ffn] / [E, ffn/32, d]."""
+    _, d, f, E, _, _, _, wdt = key
+    if wdt == DTYPE["mxfp4"]:
+        w, ws, gs, ds, ss = E * f * d // 2, 1, E * (d // 32) * f, E * (f // 32) * d, 1
+    elif wdt in (DTYPE["fp8"], DTYPE["fp8a8"]):
+        w, ws, gs, ds, ss = E * f * d, 1, E * f, E * d, 4
+    else:
+        w, ws, gs, ds, ss = E * f * d, 4 if wdt == DTYPE["f32"] else 2, 0, 0, 4
+    return (("w_gate", w, ws, None), ("w_up", w, ws, None), ("w_down", w, ws, None),
+            ("s_gate", gs, ss, None), ("s_up", gs, ss, None), ("s_down", ds, ss, None))
+
+
+@functools.lru_cache(maxsize=256)
+def _layer_reqs(key) -> tuple:
+    T, d, _, E, k, fs, adt, _ = key
+    a = 4 if adt == DTYPE["f32"] else 2
+    return ((("x", T * d, a, None), ("w_router", E * d, a, None), ("router_bias", E, 4, torch.float32))
+            + _expert_reqs(key)
+            + (("w_shared_gate", fs * d, a, None), ("w_shared_up", fs * d, a, None),
+               ("w_shared_down", fs * d, a, None), ("out", T * d, a, None),
+               ("topk_idx_out", T * k, 4, torch.int32), ("topk_w_out", T * k, 4, torch.float32),
+               ("counts_out", E, 4, torch.int32)))
+
+
+def _verify(reqs, tensors):
+    for t, (name, elems, esize, dtype) in zip(tensors, reqs):
+        if t is not None and (t.numel() < elems or t.element_size() != esize
+                              or (dtype is not None and t.dtype != dtype)):
+            _check(t, name, elems, esize, dtype)
+
+
+def _check_experts(p, w_gate, w_up, w_down, s_gate, s_up, s_down):
+    _verify(_expert_reqs(_key(p)), (w_gate, w_up, w_down, s_gate, s_up, s_down))
+
+
+def _check_layer(p, *tensors):
+    """The 16 tensors of moe_layer_forward, x .. counts_out, in order."""
+    _verify(_layer_reqs(_key(p)), tensors)
+
+
 def _stream(stream):
     s = torch.cuda.current_stream() if stream is None else stream
     return s.cuda_stream
@@ -125,11 +196,31 @@ def _call(name, *args):
 
 
 def moe_router_topk(p, x, w_router, router_bias, logits_in, logits_out, topk_idx, topk_w, stream=None):
+    a = _act_size(p)
+    _check(x, "x", p.T * p.d, a)
+    _check(w_router, "w_router", p.E * p.d, a)
+    _check(router_bias, "router_bias", p.E, 4, torch.float32)
+    _check(logits_in, "logits_in", p.T * p.E, 4, torch.float32)
+    _check(logits_out, "logits_out", p.T * p.E, 4, torch.float32)
+    _check(topk_idx, "topk_idx", p.T * p.k, 4, torch.int32)
+    _check(topk_w, "topk_w", p.T * p.k, 4, torch.float32)
     _call("moe_router_topk", ctypes.byref(p), _ptr(x), _ptr(w_router), _ptr(router_bias),
           _ptr(logits_in), _ptr(logits_out), _ptr(topk_idx), _ptr(topk_w), _stream(stream))
 
 
+def _check_permute(p, topk_idx, x, counts, offsets, perm_token, inv_row, x_perm):
+    R, a = p.T * p.k, _act_size(p)
+    _check(topk_idx, "topk_idx", R, 4, torch.int32)
+    _check(x, "x", p.T * p.d, a)
+    _check(counts, "counts", p.E, 4, torch.int32)
+    _check(offsets, "offsets", p.E + 1, 4, torch.int32)
+    _check(perm_token, "perm_token", R, 4, torch.int32)
+    _check(inv_row, "inv_row", R, 4, torch.int32)
+    _check(x_perm, "x_perm", R * p.d, a)
+
+
 def moe_permute(p, topk_idx, x, counts, offsets, perm_token, inv_row, x_perm, workspace, stream=None):
+    _check_permute(p, topk_idx, x, counts, offsets, perm_token, inv_row, x_perm)
     _call("moe_permute", ctypes.byref(p), _ptr(topk_idx), _ptr(x), _ptr(counts), _ptr(offsets),
           _ptr(perm_token), _ptr(inv_row), _ptr(x_perm), _ptr(workspace),
           0 if workspace is None else workspace.numel() * workspace.element_size(), _stream(stream))
@@ -139,12 +230,18 @@ def moe_permute_static_scratch(p, topk_idx, x, counts, offsets, perm_token, inv_
     """moe_permute for callers that cannot allocate device memory: the
     permutation's scratch comes from a fixed 1 MiB array inside the library
     instead of a caller workspace (see include/moe.h for its limits)."""
+    _check_permute(p, topk_idx, x, counts, offsets, perm_token, inv_row, x_perm)
     _call("moe_permute_static_scratch", ctypes.byref(p), _ptr(topk_idx), _ptr(x), _ptr(counts),
           _ptr(offsets), _ptr(perm_token), _ptr(inv_row), _ptr(x_perm), _stream(stream))
 
 
 def moe_grouped_swiglu(p, x_perm, offsets, w_gate, w_up, w_down, s_gate, s_up, s_down, y_perm,
                        workspace, stream=None):
+    R, a = p.T * p.k, _act_size(p)
+    _check(x_perm, "x_perm", R * p.d, a)
+    _check(offsets, "offsets", p.E + 1, 4, torch.int32)
+    _check_experts(p, w_gate, w_up, w_down, s_gate, s_up, s_down)
+    _check(y_perm, "y_perm", R * p.d, a)
     _call("moe_grouped_swiglu", ctypes.byref(p), _ptr(x_perm), _ptr(offsets), _ptr(w_gate), _ptr(w_up),
           _ptr(w_down), _ptr(s_gate), _ptr(s_up), _ptr(s_down), _ptr(y_perm), _ptr(workspace),
           0 if workspace is None else workspace.numel() * workspace.element_size(), _stream(stream))
@@ -154,10 +251,19 @@ def moe_quantize_rows_e4m3(x, codes, scales, stream=None):
     """Per-row E4M3 codes (uint8 [rows, cols]) and fp32 scales ([rows]) of
     bf16 rows x [rows, cols]."""
     rows, cols = (int(v) for v in x.shape)
+    _check(x, "x", rows * cols, 2)
+    _check(codes, "codes", rows * cols, 1)
+    _check(scales, "scales", rows, 4, torch.float32)
     _call("moe_quantize_rows_e4m3", rows, cols, _ptr(x), _ptr(codes), _ptr(scales), _stream(stream))
 
 
 def moe_combine(p, y_perm, inv_row, topk_w, shared_out, out, stream=None):
+    R, a = p.T * p.k, _act_size(p)
+    _check(y_perm, "y_perm", R * p.d, a)
+    _check(inv_row, "inv_row", R, 4, torch.int32)
+    _check(topk_w, "topk_w", R, 4, torch.float32)
+    _check(shared_out, "shared_out", p.T * p.d, a)
+    _check(out, "out", p.T * p.d, a)
     _call("moe_combine", ctypes.byref(p), _ptr(y_perm), _ptr(inv_row), _ptr(topk_w), _ptr(shared_out),
           _ptr(out), _stream(stream))
 
@@ -165,6 +271,8 @@ def moe_combine(p, y_perm, inv_row, topk_w, shared_out, out, stream=None):
 def moe_layer_forward(p, x, w_router, router_bias, w_gate, w_up, w_down, s_gate, s_up, s_down,
                       w_shared_gate, w_shared_up, w_shared_down, out, topk_idx_out, topk_w_out,
                       counts_out, workspace, stream=None):
+    _check_layer(p, x, w_router, router_bias, w_gate, w_up, w_down, s_gate, s_up, s_down, w_shared_gate,
+                 w_shared_up, w_shared_down, out, topk_idx_out, topk_w_out, counts_out)
     _call("moe_layer_forward", ctypes.byref(p), _ptr(x), _ptr(w_router), _ptr(router_bias), _ptr(w_gate),
           _ptr(w_up), _ptr(w_down), _ptr(s_gate), _ptr(s_up), _ptr(s_down), _ptr(w_shared_gate),
           _ptr(w_shared_up), _ptr(w_shared_down), _ptr(out), _ptr(topk_idx_out), _ptr(topk_w_out),
@@ -175,6 +283,8 @@ def moe_layer_forward(p, x, w_router, router_bias, w_gate, w_up, w_down, s_gate,
 def moe_layer_forward_timed(p, x, w_router, router_bias, w_gate, w_up, w_down, s_gate, s_up, s_down,
                             w_shared_gate, w_shared_up, w_shared_down, out, topk_idx_out, topk_w_out,
                             counts_out, workspace, timer, stream=None):
+    _check_layer(p, x, w_router, router_bias, w_gate, w_up, w_down, s_gate, s_up, s_down, w_shared_gate,
+                 w_shared_up, w_shared_down, out, topk_idx_out, topk_w_out, counts_out)
     _call("moe_layer_forward_timed", ctypes.byref(p), _ptr(x), _ptr(w_router), _ptr(router_bias),
           _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(s_gate), _ptr(s_up), _ptr(s_down),
           _ptr(w_shared_gate), _ptr(w_shared_up), _ptr(w_shared_down), _ptr(out), _ptr(topk_idx_out),
