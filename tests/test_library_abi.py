@@ -137,3 +137,20 @@ def test_quantised_modes_need_their_scales(lib):
         args = [fake, fake, None, fake, fake, fake, None, None, None, None, None, None, fake,
                 None, None, None, fake]
         assert lib.moe_layer_forward(ctypes.byref(p), *args, 1 << 20, None) == api.ERR_INVALID_ARG
+
+
+def test_shared_expert_pointers_follow_the_problem(lib):
+    # the shared expert's three matrices are all given when ffn_shared > 0
+    # and all NULL otherwise; bf16 weights take no scale arrays
+    fake = ctypes.c_void_p(0x1000)  # never dereferenced: rejected on the host
+    base = [fake, fake, None, fake, fake, fake, None, None, None]
+    tail = [fake, None, None, None, fake]
+    p = api.problem(T=4, d=128, ffn=256, E=8, k=2, ffn_shared=128)
+    for shared in ([fake, fake, None], [None, None, None], [fake, None, fake]):
+        assert lib.moe_layer_forward(ctypes.byref(p), *base, *shared, *tail, 1 << 20, None) == api.ERR_INVALID_ARG
+    p0 = api.problem(T=4, d=128, ffn=256, E=8, k=2)
+    assert lib.moe_layer_forward(ctypes.byref(p0), *base, fake, fake, fake, *tail, 1 << 20, None) \
+        == api.ERR_INVALID_ARG
+    scaled = [fake, fake, None, fake, fake, fake, fake, fake, fake]
+    assert lib.moe_layer_forward(ctypes.byref(p0), *scaled, None, None, None, *tail, 1 << 20, None) \
+        == api.ERR_INVALID_ARG
