@@ -248,6 +248,23 @@ def _oracle_session(shape, seed):
     return oracle, x, wr, b, ew, decoded, shared
 
 
+def blas_threads():
+    """Threads numpy's BLAS runs the oracle's matmuls on, where it can be
+    read (threadpoolctl), else the environment's setting or the library
+    default (one per core)."""
+    try:
+        import threadpoolctl
+        n = [i["num_threads"] for i in threadpoolctl.threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return "library default (one per core)"
+
+
 def oracle_tokens_per_s(shape, seed, budget_s, min_tokens=1):
     """Time the grouped fp64 oracle on a bounded sample of the workload:
     the first n tokens of one batch, n chosen so the timing takes about
@@ -305,7 +322,8 @@ def run_reference(args, shape, ws, rank):
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": workload_config(shape),
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "blas_threads": blas_threads(),
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -553,7 +571,8 @@ def run_ours(args, shape, ws, rank, local):
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         v, sample, cores = oracle_tokens_per_s(shape, args.seed, budget_s=15.0)
-        cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample}
+        cpu = {"value": v, "unit": "tokens/s", "cores": cores, "blas_threads": blas_threads(), "kind": "oracle",
+               "sample": sample}
 
     if rank == 0:
         line = {
