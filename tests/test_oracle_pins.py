@@ -307,6 +307,23 @@ def test_two_formulations_agree_on_generated_fp8_and_bf16_cases():
     np.testing.assert_allclose(a, c, rtol=0, atol=1e-12 * np.abs(a).max())
 
 
+@pytest.mark.parametrize("wfmt", ["fp8a8", "mxfp4"])
+def test_two_formulations_agree_on_quantised_modes(wfmt):
+    # per token over its chosen set, and grouped per expert: the same layer
+    # with FP8 activations (x and h rows quantised per row) or MXFP4 weights
+    small = inputs.MoEShape("small_q", T=11, d=64, ffn=32, E=6, k=3, ffn_shared=32, wfmt=wfmt)
+    case = inputs.make_case(small, 5)
+    x, wr, b, ew, sh = helpers.oracle_inputs(case, small)
+    act8 = wfmt == "fp8a8"
+    a, ia, _ = oracle.moe_forward_per_token(x, wr, ew, small.k, shared=sh, act8=act8)
+    c, ic, _ = oracle.moe_forward_grouped(x, wr, ew, small.k, shared=sh, act8=act8)
+    assert np.array_equal(ia, ic)
+    np.testing.assert_allclose(a, c, rtol=0, atol=1e-12 * np.abs(a).max())
+    if act8:  # and the quantisation is really applied: unquantised rows give another answer
+        u, _, _ = oracle.moe_forward_grouped(x, wr, ew, small.k, shared=sh)
+        assert np.abs(u - a).max() > 1e-6 * np.abs(a).max()
+
+
 def test_fp8_weights_are_code_times_per_channel_scale():
     small = inputs.MoEShape("small_fp8", T=2, d=16, ffn=8, E=2, k=1, wfmt="fp8")
     case = inputs.make_case(small, 5)
