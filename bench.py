@@ -110,7 +110,9 @@ def stage_work(shape, touched, splits):
     gu_bytes = touched * (2 * f * d * wb + 2 * f * scale) + rows + R * f * ab
     gu_flops = 4.0 * R * f * d
     y_bytes = splits * R * d * 4 if splits > 1 else R * d * ab
-    dn_bytes = touched * (d * f * wb + d * scale) + R * f * ab + y_bytes
+    # down row operand: h in the activation dtype, or h's E4M3 codes + a row scale
+    h_rows = R * (f + 4) if shape.wfmt == "fp8a8" else R * f * ab
+    dn_bytes = touched * (d * f * wb + d * scale) + h_rows + y_bytes
     dn_flops = 2.0 * R * f * d
     fs = shape.ffn_shared
     layer_bytes = (E * d * ab + touched * 3 * f * d * wb + 3 * fs * d * ab + 2 * T * d * ab)

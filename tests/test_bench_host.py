@@ -43,6 +43,11 @@ def test_fp8_scales_and_fp8_rows_enter_the_bytes():
     # fp32 scale each instead of bf16
     R, d = 8, 256
     assert b_fp8 - b_a8 == R * d * 2 - R * (d + 4)
+    # and the down GEMM reads h's E4M3 codes and row scales instead of f16 h
+    d_fp8, _ = bench.stage_work(base, touched=4, splits=1)["down"]
+    d_a8, _ = bench.stage_work(a8, touched=4, splits=1)["down"]
+    f = 128
+    assert d_fp8 - d_a8 == R * f * 2 - R * (f + 4)
 
 
 def test_expected_touched_closed_form():
