@@ -70,9 +70,9 @@
  *                               block scales 2^-23 .. 2^13 (UE8M0 104..140);
  *                               larger scales overflow f16 and are not
  *                               supported.  Router and shared expert bf16.
- * Size limits: 1 <= k <= min(E, 32), E <= 1024, d % 8 == 0, ffn % 8 == 0;
- * the tensor-core path further needs d % 128 == 0, ffn % 128 == 0 and
- * ffn_shared % 128 == 0.
+ * Size limits: 1 <= k <= min(E, 32), E <= 1024, T * k <= 2^24,
+ * d % 8 == 0, ffn % 8 == 0; the tensor-core path further needs
+ * d % 128 == 0, ffn % 128 == 0 and ffn_shared % 128 == 0.
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H

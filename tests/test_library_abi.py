@@ -154,3 +154,9 @@ def test_shared_expert_pointers_follow_the_problem(lib):
     scaled = [fake, fake, None, fake, fake, fake, fake, fake, fake]
     assert lib.moe_layer_forward(ctypes.byref(p0), *scaled, None, None, None, *tail, 1 << 20, None) \
         == api.ERR_INVALID_ARG
+
+
+def test_assignment_rows_limit(lib):
+    # T * k <= 2^24 assignment rows
+    assert _ws_status(lib, api.problem(T=(1 << 21) + 1, d=128, ffn=128, E=8, k=8)) == api.ERR_UNSUPPORTED
+    assert api.moe_workspace_size_for(api.problem(T=1 << 21, d=128, ffn=128, E=8, k=8), 152) > 0
