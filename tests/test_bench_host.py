@@ -80,3 +80,15 @@ def test_committed_traffic_file_parses():
     path = os.path.join(bench.ROOT, "profiles", "dram_traffic.txt")
     rows = [ln.split() for ln in open(path) if ln.strip() and not ln.startswith("#")]
     assert rows and all(len(r) == 5 and len(r[3]) == 16 and float(r[4]) > 0 for r in rows)
+
+
+def test_peaks_measured_else_the_recipe_fallback(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    # no measured file: the earlier GB300 measurement (6.8 TB/s, 1.9 / 1.7 PFLOP/s)
+    assert bench.load_peaks() == (6800.0, 1900.0, 1700.0, "fallback")
+    (tmp_path / "MEASURED_PEAKS.json").write_text(
+        '{"hbm_gbs": 6691.5, "bf16_tflops": 1930.8, "bf16_tflops_sustained": 1723.5}')
+    assert bench.load_peaks() == (6691.5, 1930.8, 1723.5, "measured")
+    # a file without the figures is not a measurement
+    (tmp_path / "MEASURED_PEAKS.json").write_text('{"hbm_gbs": 6691.5}')
+    assert bench.load_peaks()[3] == "fallback"
