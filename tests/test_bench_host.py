@@ -92,3 +92,20 @@ def test_peaks_measured_else_the_recipe_fallback(tmp_path, monkeypatch):
     # a file without the figures is not a measurement
     (tmp_path / "MEASURED_PEAKS.json").write_text('{"hbm_gbs": 6691.5}')
     assert bench.load_peaks()[3] == "fallback"
+
+
+def test_clock_summary_reads_nvidia_smi_lines():
+    s = bench.ClockSampler(0)
+    s.lines = [(0.0, ln) for ln in (
+        "0, 2070, 2070, 900.1, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "0, 1995, 2070, 1390.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "0, 2070, 2070, 1200.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "garbage line",
+        "0, [N/A], 2070, 1.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+    )]
+    out = s.summary()
+    assert out == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+    s.lines = [(0.0, "0, 1500, 2070, 1.0, 0x8, Active, Not Active, Not Active, Not Active")]
+    assert s.summary()["reasons"] == ["hw_slowdown"]
+    s.lines = []
+    assert s.summary()["samples"] == 0
