@@ -190,7 +190,10 @@ MOE_API moe_status moe_permute(const moe_problem *p, const int32_t *topk_idx, co
  * exits.  Problems needing more (ceil(T*k/256) * E > 262144) are rejected
  * with MOE_ERR_WORKSPACE.  The first call on each device looks up the
  * array's device address with that device current; make that first call
- * before any stream capture.  All calls share the array and it keeps the
+ * before any stream capture.  That cached address (like the library's other
+ * per-device state) does not survive a device reset (cudaDeviceReset) in
+ * the same process.  The problem is checked exactly as moe_permute checks
+ * it, then against the array's size.  All calls share the array and it keeps the
  * last call's contents (every entry read is first rewritten, so nothing has
  * to be cleared); calls that overlap on the GPU race on it.  Allocates
  * nothing.

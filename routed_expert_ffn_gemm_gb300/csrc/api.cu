@@ -36,6 +36,15 @@ moe_status check_problem(const moe_problem* p, Path* path) {
   return router_topk_check(p->d, p->E, p->act_dtype);
 }
 
+}  // namespace
+
+moe_status problem_check(const moe_problem* p) {
+  Path path;
+  return check_problem(p, &path);
+}
+
+namespace {
+
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Largest SM count the device-free planning entry points accept.

@@ -28,7 +28,14 @@ struct DeviceCtx {
 };
 
 // Current device, its SM count and status-word address (cached per device).
+// The cache outlives a device reset (cudaDeviceReset) in the same process,
+// so the library is not usable after one.
 moe_status device_ctx(DeviceCtx* ctx);
+
+// The checks every entry point that takes a moe_problem applies (sizes,
+// dtype combination, divisibility, router limits): MOE_OK, or the status
+// the entry point returns before launching anything.
+moe_status problem_check(const moe_problem* p);
 
 // Remember the text of a failed CUDA call for moe_last_cuda_error().
 void record_cuda_error(cudaError_t err);

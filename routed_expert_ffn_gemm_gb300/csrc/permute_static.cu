@@ -14,7 +14,9 @@
 // exits.  Host code cannot use the array's name as a device address, so the
 // first call on each device looks the address up with cudaGetSymbolAddress
 // (with that device current) and caches it; that first call should therefore
-// come before any stream capture.  All calls share the one array and it keeps
+// come before any stream capture.  The cached address does not survive a
+// device reset (cudaDeviceReset) in the same process; neither does the rest
+// of the library's per-device state.  All calls share the one array and it keeps
 // the last call's contents; the count kernel overwrites every entry it later
 // reads, so nothing has to be cleared between calls.  Calls whose work
 // overlaps on the GPU (other streams, other threads) race on the array.
@@ -56,11 +58,8 @@ extern "C" moe_status moe_permute_static_scratch(const moe_problem* p, const int
                                                  int32_t* perm_token, int32_t* inv_row,
                                                  void* x_perm, moe_stream_t stream) {
   using namespace moe;
-  if (p == nullptr) return MOE_ERR_INVALID_ARG;
-  if (p->T < 0 || p->E <= 0 || p->k <= 0 || p->k > p->E || p->d <= 0) return MOE_ERR_INVALID_ARG;
-  if (p->E > 1024 || p->k > 32 || (int64_t)p->T * p->k > (1 << 24)) return MOE_ERR_UNSUPPORTED;
-  if (p->act_dtype != MOE_F32 && p->act_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
-  if (p->d % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  // the same problem checks as moe_permute, so both accept and refuse alike
+  MOE_TRY(problem_check(p));
   if (counts == nullptr || offsets == nullptr || perm_token == nullptr || inv_row == nullptr)
     return MOE_ERR_INVALID_ARG;
   if (p->T > 0 && topk_idx == nullptr) return MOE_ERR_INVALID_ARG;
