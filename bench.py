@@ -4,8 +4,10 @@
 One step = one pass of the whole layer (router top-k, permutation, grouped
 SwiGLU experts, shared expert if any, combine) over one batch of synthetic
 tokens whose inputs are already resident in HBM.  Default workload: the
-Mixtral-8x7B-shaped layer (d=4096, ffn=14336, E=8, top-2, bf16) at a decode
-batch of T=64 tokens.  Metric: MoE-layer tokens/s (whole job, all ranks).
+DeepSeek-V3-shaped layer (d=7168, routed ffn=2048, E=256, top-8, FP8 E4M3
+routed experts with per-output-channel scales, bf16 activations, one bf16
+shared expert of ffn=2048) at a prefill batch of T=4096 tokens, the largest
+configuration of the set.  Metric: MoE-layer tokens/s (whole job, all ranks).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--T T]
   python bench.py --impl reference ...   # the fp64 CPU reference, timed on host cores
@@ -38,6 +40,12 @@ sys.path.insert(0, ROOT)
 from routed_expert_ffn_gemm_gb300 import inputs  # noqa: E402
 
 L2_BYTES = 129 * 1024 * 1024
+# tokens per step when --T is not given: the batch each workload is measured
+# at by default (the DeepSeek-V3-shaped layer at its prefill batch)
+DEFAULT_T = {"deepseek_v3": 4096, "mixtral_8x7b": 64}
+# decoded (float64) expert weights the CPU oracle legs keep at once; past
+# it the oldest decoded expert is dropped and decoded again when needed
+ORACLE_CACHE_BYTES = 12e9
 DEFAULT_HBM_GBS = 6800.0      # fallback peaks when no measured file exists
 DEFAULT_BF16_TFLOPS = 1900.0
 
@@ -48,7 +56,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="mixtral_8x7b", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--workload", default="deepseek_v3", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--T", type=int, default=None, help="tokens per step (default: the workload's)")
     ap.add_argument("--E", type=int, default=None,
                     help="number of routed experts (default: the workload's; fewer experts make a "
@@ -119,6 +127,19 @@ def stage_work(shape, touched, splits):
     layer_flops = 2.0 * T * d * E + 6.0 * d * f * R + 6.0 * d * fs * T
     return {"gate_up": (gu_bytes, gu_flops), "down": (dn_bytes, dn_flops),
             "layer": (layer_bytes, layer_flops)}
+
+
+def layer_roofline(lb, lf, layer_s, hbm_gbs, bf16_tf, touched, max_over_mean):
+    """The whole layer against both roofs: touched-byte bandwidth over the
+    HBM peak, flops over the bf16 tensor peak, and the binding bound (the
+    larger of the two minimum times) with the fraction of it reached."""
+    t_bytes, t_flops = lb / (hbm_gbs * 1e9), lf / (bf16_tf * 1e12)
+    return {"GB_per_s_touched_bytes": lb / layer_s / 1e9, "frac_hbm": lb / layer_s / 1e9 / hbm_gbs,
+            "TFLOP_per_s": lf / layer_s / 1e12, "frac_tensor": lf / layer_s / 1e12 / bf16_tf,
+            "t_bytes_us": t_bytes * 1e6, "t_flops_us": t_flops * 1e6,
+            "bound": "hbm" if t_bytes >= t_flops else "tensor",
+            "frac_binding": max(t_bytes, t_flops) / layer_s,
+            "touched_experts": touched, "max_over_mean_rows": max_over_mean}
 
 
 class ClockSampler:
@@ -219,9 +240,49 @@ def whole_job_tokens_per_s(ms_this_rank, ws, steps, tokens_per_step, device):
 # CPU reference (fp64 oracle), timed on the host cores
 # ---------------------------------------------------------------------------
 
+class _DecodedExperts:
+    """``expert_hook`` for the oracle's grouped formulation: decodes expert e
+    to float64 when the oracle reaches it (FP8 codes times channel scales,
+    MXFP4 blocks, or bf16 values) and keeps at most ORACLE_CACHE_BYTES of
+    decoded experts, dropping the oldest first.  ``decode_s`` accumulates
+    the time spent decoding, which the timed legs subtract: format
+    conversion is not the layer's arithmetic."""
+
+    def __init__(self, case, shape, cap_bytes=ORACLE_CACHE_BYTES):
+        import oracle
+        self.oracle, self.case, self.shape, self.cap = oracle, case, shape, cap_bytes
+        self.cache = {}
+        self.decode_s = 0.0
+
+    def _decode(self, e):
+        c, fmt = self.case, self.shape.wfmt
+        if fmt == "mxfp4":
+            return tuple(self.oracle.decode_mxfp4(c[w][e].numpy(), c[s][e].numpy())
+                         for w, s in (("w_gate", "s_gate"), ("w_up", "s_up"), ("w_down", "s_down")))
+        if fmt in ("fp8", "fp8a8"):
+            def dq(w, s):
+                return (c[w][e].view(torch.float8_e4m3fn).to(torch.float64)
+                        * c[s][e].to(torch.float64)[:, None]).numpy()
+            return dq("w_gate", "s_gate"), dq("w_up", "s_up"), dq("w_down", "s_down")
+        return tuple(c[n][e].to(torch.float64).numpy() for n in ("w_gate", "w_up", "w_down"))
+
+    def __call__(self, e):
+        if e in self.cache:
+            return self.cache[e]
+        t0 = time.perf_counter()
+        w = self._decode(e)
+        self.decode_s += time.perf_counter() - t0
+        per = sum(a.nbytes for a in w)
+        while self.cache and (len(self.cache) + 1) * per > self.cap:
+            self.cache.pop(next(iter(self.cache)))
+        if per <= self.cap:
+            self.cache[e] = w
+        return w
+
+
 def _oracle_session(shape, seed):
-    """Generate the case on the CPU and decode every expert to float64 once
-    (format conversion is excluded from timing)."""
+    """Generate the case on the CPU; expert weights are decoded to float64
+    one expert at a time by the hook (never the whole stack at once)."""
     import oracle
     case = inputs.make_case(shape, seed, "cpu")
 
@@ -231,23 +292,32 @@ def _oracle_session(shape, seed):
     x = f64(case["x"])
     wr = f64(case["w_router"])
     b = f64(case["router_bias"])
-    decoded = {}
-    for e in range(shape.E):
-        if shape.wfmt == "mxfp4":
-            decoded[e] = tuple(oracle.decode_mxfp4(case[w][e].numpy(), case[s][e].numpy())
-                               for w, s in (("w_gate", "s_gate"), ("w_up", "s_up"), ("w_down", "s_down")))
-        elif shape.wfmt in ("fp8", "fp8a8"):
-            def dq(w, s):
-                return (w[e].view(torch.float8_e4m3fn).to(torch.float64) * s[e].to(torch.float64)[:, None]).numpy()
-            decoded[e] = (dq(case["w_gate"], case["s_gate"]), dq(case["w_up"], case["s_up"]),
-                          dq(case["w_down"], case["s_down"]))
-        else:
-            decoded[e] = (f64(case["w_gate"][e]), f64(case["w_up"][e]), f64(case["w_down"][e]))
     shared = None
     if shape.ffn_shared:
         shared = tuple(f64(case[n]) for n in ("w_shared_gate", "w_shared_up", "w_shared_down"))
     ew = oracle.ExpertWeights("f64", *(np.zeros((shape.E, 1, 1)),) * 3)
-    return oracle, x, wr, b, ew, decoded, shared
+    return oracle, x, wr, b, ew, _DecodedExperts(case, shape), shared
+
+
+def _oracle_step(session, shape, n):
+    """One grouped-oracle layer over the first n tokens; returns its time with
+    the expert decoding inside it subtracted."""
+    oracle_mod, x, wr, b, ew, hook, shared = session
+    d0 = hook.decode_s
+    t0 = time.perf_counter()
+    oracle_mod.moe_forward_grouped(x[:n], wr, ew, shape.k, bias=b, shared=shared,
+                                   expert_hook=hook, act8=shape.wfmt == "fp8a8")
+    return time.perf_counter() - t0 - (hook.decode_s - d0)
+
+
+def layer_flops(shape, T):
+    """Algorithmic flops of the layer at T tokens (router, routed experts,
+    shared expert)."""
+    return 2.0 * T * shape.d * shape.E + 6.0 * shape.d * shape.ffn * T * shape.k + 6.0 * shape.d * shape.ffn_shared * T
+
+
+def expected_touched_at(shape, T):
+    return shape.E * (1.0 - (1.0 - shape.k / shape.E) ** T) if T else 0.0
 
 
 def blas_threads():
@@ -267,30 +337,23 @@ def blas_threads():
     return "library default (one per core)"
 
 
-def oracle_tokens_per_s(shape, seed, budget_s, min_tokens=1):
-    """Time the grouped fp64 oracle on a bounded sample of the workload:
-    the first n tokens of one batch, n chosen so the timing takes about
-    budget_s seconds.  Returns (tokens/s, sample description, cores)."""
-    oracle, x, wr, b, ew, decoded, shared = _oracle_session(shape, seed)
+def oracle_tokens_per_s(shape, seed, budget_s, max_flops=4e12):
+    """Time the grouped fp64 oracle on a bounded sample of the workload: the
+    first n tokens of one batch, n = T unless the layer's flops at T exceed
+    max_flops (about 10-30 s of host work), repeated until about budget_s
+    seconds are timed.  Expert weights are decoded one expert at a time,
+    outside the timed time.  Returns (tokens/s, sample description, cores)."""
+    session = _oracle_session(shape, seed)
     cores = len(os.sched_getaffinity(0))
-
-    def run(n):
-        t0 = time.perf_counter()
-        oracle.moe_forward_grouped(x[:n], wr, ew, shape.k, bias=b, shared=shared,
-                                   expert_hook=decoded.__getitem__, act8=shape.wfmt == "fp8a8")
-        return time.perf_counter() - t0
-
-    n = min(shape.T, max(min_tokens, 1))
-    dt = run(n)
-    while n < shape.T and dt < budget_s / 4:
-        n = min(shape.T, n * 2)
-        dt = run(n)
+    n = shape.T
+    while n > 1 and layer_flops(shape, n) > max_flops:
+        n //= 2
     reps, total = 0, 0.0
-    while total < budget_s and reps < 50:
-        total += run(n)
+    while (total < budget_s and reps < 50) or reps == 0:
+        total += _oracle_step(session, shape, n)
         reps += 1
-    sample = (f"{reps} runs of the grouped fp64 oracle over the first {n} of {shape.T} tokens "
-              f"(expert weights decoded to fp64 beforehand, excluded)")
+    sample = (f"{reps} run(s) of the grouped fp64 oracle over the first {n} of {shape.T} tokens "
+              f"(expert weights decoded to fp64 one expert at a time, decoding excluded from the time)")
     return reps * n / total, sample, cores
 
 
@@ -298,27 +361,30 @@ def run_reference(args, shape, ws, rank):
     if rank != 0:
         return 0
     import oracle  # noqa: F401  (the reference arm times the oracle as it stands)
-    oracle_mod, x, wr, b, ew, decoded, shared = _oracle_session(shape, args.seed)
+    session = _oracle_session(shape, args.seed)
+    hook = session[5]
     cores = len(os.sched_getaffinity(0))
 
-    def step(n):
-        oracle_mod.moe_forward_grouped(x[:n], wr, ew, shape.k, bias=b, shared=shared,
-                                       expert_hook=decoded.__getitem__, act8=shape.wfmt == "fp8a8")
-
-    # size each step so the whole run takes about two minutes
-    t0 = time.perf_counter()
-    step(1)
-    one = max(time.perf_counter() - t0, 1e-4)
+    # Each step is the same first n tokens, sized so the whole run takes about
+    # two minutes and every expert those tokens touch stays decoded in the
+    # hook's cache (decoded once, in the first step, outside the timed time).
+    per_expert = 3 * shape.ffn * shape.d * 8
+    n = 1
+    while n < shape.T and expected_touched_at(shape, 2 * n) * per_expert <= ORACLE_CACHE_BYTES:
+        n *= 2
+    one = max(_oracle_step(session, shape, n), 1e-4)
     per_step_budget = 120.0 / max(1, args.steps + args.warmup)
-    n = int(max(1, min(shape.T, per_step_budget / one)))
+    while n > 1 and one > per_step_budget:
+        n //= 2
+        one = max(_oracle_step(session, shape, n), 1e-4)
     for _ in range(args.warmup):
-        step(n)
-    t0 = time.perf_counter()
+        _oracle_step(session, shape, n)
+    dt = 0.0
     for _ in range(args.steps):
-        step(n)
-    dt = time.perf_counter() - t0
+        dt += _oracle_step(session, shape, n)
     value = args.steps * n / dt
-    sample = f"each step: the grouped fp64 oracle over the first {n} of {shape.T} tokens"
+    sample = (f"each step: the grouped fp64 oracle over the first {n} of {shape.T} tokens "
+              f"(the experts they touch decoded to fp64 once, decoding excluded from the time)")
     line = {
         "impl": "reference", "metric": "moe_layer_tokens_per_s", "value": value, "unit": "tokens/s",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
@@ -536,6 +602,10 @@ def run_ours(args, shape, ws, rank, local):
     else:
         roof = {"bound": "hbm", "achieved": b_ / t_s / 1e9, "peak": hbm_gbs, "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
+    # both bounds of the kernel, at the peaks used: the larger one binds
+    roof["t_bytes_us"] = b_ / (hbm_gbs * 1e9) * 1e6
+    roof["t_flops_us"] = f_ / (tensor_peak * 1e12) * 1e6
+    roof["t_measured_us"] = t_s * 1e6
     roof["traffic"] = measured_traffic(shape, dominant)
     roof["kernel"] = f"tc_grouped_kernel ({dominant})"
     roof["peak_source"] = peak_src
@@ -584,13 +654,11 @@ def run_ours(args, shape, ws, rank, local):
             "dtype": {"fp8a8": "fp8", "fp8": "f16", "mxfp4": "f16"}.get(shape.wfmt, "bf16")
                      if shape.act == "bf16" else "f32",
             "data": "synthetic",
-            "config": workload_config(shape, {
-                "l2": (f"inputs larger than L2: {touched * 3 * shape.ffn * shape.d * wbytes(shape) / 1e9:.2f} GB "
-                       f"of touched expert weights per step, {n_sets} weight set(s) rotated")}),
+            "config": workload_config(shape),
+            "l2": (f"inputs larger than L2: {touched * 3 * shape.ffn * shape.d * wbytes(shape) / 1e9:.2f} GB "
+                   f"of touched expert weights per step, {n_sets} weight set(s) rotated"),
             "roofline": roof,
-            "layer": {"GB_per_s_touched_bytes": lb / layer_s / 1e9, "frac_hbm": lb / layer_s / 1e9 / hbm_gbs,
-                      "TFLOP_per_s": lf / layer_s / 1e12, "touched_experts": touched,
-                      "max_over_mean_rows": max_over_mean},
+            "layer": layer_roofline(lb, lf, layer_s, hbm_gbs, bf16_tf, touched, max_over_mean),
             "stages_us": {s: 1e3 * v for s, v in stage_ms.items()},
             "plan": plan,
             "cuda_graphs": graphs is not None,
@@ -609,8 +677,8 @@ def main():
     shape = inputs.WORKLOADS[args.workload]
     if args.T is not None:
         shape = shape.with_T(args.T)
-    elif args.workload == "mixtral_8x7b":
-        shape = shape.with_T(64)
+    elif args.workload in DEFAULT_T:
+        shape = shape.with_T(DEFAULT_T[args.workload])
     if args.E is not None:
         if not shape.k <= args.E:
             raise SystemExit("--E must be at least the workload's top-k")

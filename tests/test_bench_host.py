@@ -109,3 +109,50 @@ def test_clock_summary_reads_nvidia_smi_lines():
     assert s.summary()["reasons"] == ["hw_slowdown"]
     s.lines = []
     assert s.summary()["samples"] == 0
+
+
+def test_default_workload_is_the_largest_configuration():
+    # no flags: the DeepSeek-V3-shaped layer (FP8 experts, bf16 activations,
+    # shared expert) at its prefill batch of 4096 tokens
+    import sys
+    argv, sys.argv = sys.argv, ["bench.py"]
+    try:
+        args = bench.parse_args()
+    finally:
+        sys.argv = argv
+    assert args.workload == "deepseek_v3" and args.T is None
+    shape = inputs.WORKLOADS[args.workload].with_T(bench.DEFAULT_T[args.workload])
+    assert (shape.T, shape.d, shape.ffn, shape.E, shape.k, shape.ffn_shared, shape.wfmt, shape.act) == \
+        (4096, 7168, 2048, 256, 8, 2048, "fp8", "bf16")
+
+
+def test_oracle_hook_decodes_each_expert_as_the_oracle_does_and_bounds_its_cache():
+    import numpy as np
+    import oracle
+    shape = inputs.MoEShape("s", T=4, d=128, ffn=64, E=5, k=2, wfmt="fp8")
+    case = inputs.make_case(shape, 3, "cpu")
+    per = 3 * 64 * 128 * 8
+    hook = bench._DecodedExperts(case, shape, cap_bytes=2 * per)
+    ew = oracle.ExpertWeights("fp8", *(inputs.to_numpy_stored(case[n]) for n in
+                                       ("w_gate", "w_up", "w_down", "s_gate", "s_up", "s_down")))
+    for e in range(shape.E):
+        for a, b in zip(hook(e), ew.get(e)):
+            assert np.array_equal(a, b)
+    # at most two decoded experts kept, the oldest dropped first
+    assert sorted(hook.cache) == [3, 4]
+    t = hook.decode_s
+    hook(4)
+    assert hook.decode_s == t          # a hit decodes nothing
+    hook(0)
+    assert hook.decode_s > t and sorted(hook.cache) == [0, 4]
+
+
+def test_layer_roofline_names_the_binding_bound():
+    # 10 GB and 1 TFLOP against 5 TB/s and 2 PFLOP/s: bytes take 2 ms, flops
+    # 0.5 ms, so HBM binds; at 4 ms the layer reaches half of it
+    r = bench.layer_roofline(10e9, 1e12, 4e-3, 5000.0, 2000.0, 8, 1.0)
+    assert r["bound"] == "hbm"
+    assert r["t_bytes_us"] == pytest.approx(2000.0) and r["t_flops_us"] == pytest.approx(500.0)
+    assert r["frac_binding"] == pytest.approx(0.5)
+    r = bench.layer_roofline(1e9, 4e12, 4e-3, 5000.0, 2000.0, 8, 1.0)
+    assert r["bound"] == "tensor" and r["frac_binding"] == pytest.approx(0.5)
