@@ -113,13 +113,15 @@ def stage_work(shape, touched, splits):
     R, d, f, E, T = shape.T * shape.k, shape.d, shape.ffn, shape.E, shape.T
     wb, ab = wbytes(shape), abytes(shape)
     scale = 4 if shape.wfmt in ("fp8", "fp8a8") else 0
-    # gate/up row operand: the activation dtype, or E4M3 codes + a row scale
-    rows = R * (d + 4) if shape.wfmt == "fp8a8" else R * d * ab
+    # gate/up row operand: the activation dtype; E4M3 codes + a row scale
+    # (FP8 activations); or, FP8 weights on bf16 rows, each row's two E4M3
+    # rows + a row scale
+    rows = {"fp8a8": R * (d + 4), "fp8": R * (2 * d + 4)}.get(shape.wfmt, R * d * ab)
     gu_bytes = touched * (2 * f * d * wb + 2 * f * scale) + rows + R * f * ab
     gu_flops = 4.0 * R * f * d
     y_bytes = splits * R * d * 4 if splits > 1 else R * d * ab
-    # down row operand: h in the activation dtype, or h's E4M3 codes + a row scale
-    h_rows = R * (f + 4) if shape.wfmt == "fp8a8" else R * f * ab
+    # down row operand: h in the activation dtype, or h's E4M3 rows + a row scale
+    h_rows = {"fp8a8": R * (f + 4), "fp8": R * (2 * f + 4)}.get(shape.wfmt, R * f * ab)
     dn_bytes = touched * (d * f * wb + d * scale) + h_rows + y_bytes
     dn_flops = 2.0 * R * f * d
     fs = shape.ffn_shared
@@ -651,8 +653,8 @@ def run_ours(args, shape, ws, rank, local):
             "metric": "moe_layer_tokens_per_s", "value": value, "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": {"fp8a8": "fp8", "fp8": "f16", "mxfp4": "f16"}.get(shape.wfmt, "bf16")
-                     if shape.act == "bf16" else "f32",
+            # (FP8 weights: bf16 rows carried exactly as two E4M3 terms)
+            "dtype": {"fp8a8": "fp8", "mxfp4": "f16"}.get(shape.wfmt, "bf16") if shape.act == "bf16" else "f32",
             "data": "synthetic",
             "config": workload_config(shape),
             "l2": (f"inputs larger than L2: {touched * 3 * shape.ffn * shape.d * wbytes(shape) / 1e9:.2f} GB "

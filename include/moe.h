@@ -44,6 +44,15 @@
  *   MOE_BF16 / MOE_FP8_E4M3     as above, FP8 weights (OCP E4M3) with fp32
  *                               per-expert, per-output-channel scales;
  *                               the router and shared expert stay bf16.
+ *                               The bf16 rows (tokens, then h) enter the
+ *                               FP8 x FP8 tensor-core instructions as two
+ *                               E4M3 rows each (moe_split_rows_e4m3x2),
+ *                               an exact re-encoding of the bf16 values:
+ *                               g[r,o] = s_gate[e,o] * s_x[r] *
+ *                                 sum_i (hi[r,i] + lo[r,i]/16) code_gate[e][o,i]
+ *                               (likewise u); h = SiLU(g) * u held in bf16,
+ *                               split the same way before the down product.
+ *                               Any finite bf16 magnitude is accepted.
  *   MOE_BF16 / MOE_FP8_E4M3_ACT8
  *                               FP8 weights as above; both routed GEMMs
  *                               multiply them with E4M3 activation rows
@@ -84,7 +93,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 4
+#define MOE_ABI_VERSION 5
 
 #if defined(__GNUC__)
 #define MOE_API __attribute__((visibility("default")))
@@ -256,6 +265,34 @@ MOE_API moe_status moe_grouped_swiglu(const moe_problem *p, const void *x_perm, 
  */
 MOE_API moe_status moe_quantize_rows_e4m3(int32_t rows, int32_t cols, const void *x, uint8_t *codes,
                                           float *scales, moe_stream_t stream);
+
+/*
+ * moe_split_rows_e4m3x2 -- bf16 rows as two E4M3 rows each, exactly.
+ * Page "MoE 推理部署", section 专家量化 (FP8 expert weights, the
+ * activations kept at higher precision): the FP8-weight mode
+ * (MOE_FP8_E4M3) multiplies its E4M3 weights with bf16 activation rows on
+ * FP8 x FP8 tensor-core instructions by handing them each row in this
+ * form; the layer forward applies it to x (before dispatch) and to h.
+ *
+ *   s[r]         = 2^p, p the integer with max_i |x[r,i]| / 2^p in
+ *                  (224, 448]; 1 when row r is all zero
+ *   hi[r,i]      = E4M3(x[r,i] / s[r])
+ *   lo[r,i]      = E4M3(16 * (x[r,i] / s[r] - hi[r,i]))
+ * (nearest E4M3 value, ties to the even code).  Then
+ *   x[r,i] = s[r] * (hi[r,i] + lo[r,i] / 16)
+ * exactly for every element with |x[r,i]| >= max_i |x[r,i]| * 2^-13, and
+ * within s[r] * 2^-14 for smaller ones: a bf16 value has 8 significant
+ * bits, hi holds the top four (rounded) and lo the signed remainder.
+ *
+ *   x       [rows, cols] bf16, device, 16-byte aligned
+ *   codes   [rows, 2, cols] uint8 out: row r's hi codes, then its lo codes
+ *           (rows 2r and 2r+1 of a [2*rows, cols] matrix), 16-byte aligned
+ *   scales  [rows] fp32 out (powers of two)
+ * rows >= 0 (0: nothing is enqueued); cols > 0 and cols % 8 == 0, else
+ * MOE_ERR_UNSUPPORTED.  Null pointers with rows > 0: MOE_ERR_INVALID_ARG.
+ */
+MOE_API moe_status moe_split_rows_e4m3x2(int32_t rows, int32_t cols, const void *x, uint8_t *codes,
+                                         float *scales, moe_stream_t stream);
 
 /*
  * moe_combine -- restore token order, apply routing weights, sum.

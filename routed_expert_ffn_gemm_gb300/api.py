@@ -73,6 +73,7 @@ _SIGS = {
     "moe_workspace_size_for": [_PP, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t)],
     "moe_permute_static_scratch": [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP],
     "moe_quantize_rows_e4m3": [ctypes.c_int32, ctypes.c_int32, _VP, _VP, _VP, _VP],
+    "moe_split_rows_e4m3x2": [ctypes.c_int32, ctypes.c_int32, _VP, _VP, _VP, _VP],
 }
 STAGES = ("router", "permute", "gate_up", "down", "shared", "combine")
 EXPORTS = tuple(_SIGS)
@@ -255,6 +256,17 @@ def moe_quantize_rows_e4m3(x, codes, scales, stream=None):
     _check(codes, "codes", rows * cols, 1)
     _check(scales, "scales", rows, 4, torch.float32)
     _call("moe_quantize_rows_e4m3", rows, cols, _ptr(x), _ptr(codes), _ptr(scales), _stream(stream))
+
+
+def moe_split_rows_e4m3x2(x, codes, scales, stream=None):
+    """bf16 rows x [rows, cols] as two E4M3 rows each: codes uint8
+    [rows, 2, cols] (hi, then lo) and power-of-two fp32 scales [rows], with
+    x = s * (hi + lo / 16)."""
+    rows, cols = (int(v) for v in x.shape)
+    _check(x, "x", rows * cols, 2)
+    _check(codes, "codes", 2 * rows * cols, 1)
+    _check(scales, "scales", rows, 4, torch.float32)
+    _call("moe_split_rows_e4m3x2", rows, cols, _ptr(x), _ptr(codes), _ptr(scales), _stream(stream))
 
 
 def moe_combine(p, y_perm, inv_row, topk_w, shared_out, out, stream=None):

@@ -95,19 +95,22 @@ Layout layout(const moe_problem& p, Path path, int num_sms, bool allow_splits) {
   L.chunk = take(permute_scratch_bytes(p.T, p.k, p.E));
   // The permuted rows, except on the tensor path: there the gate/up GEMM
   // gathers the token rows itself (TMA gather4 for 32-row tiles, cp.async
-  // for larger ones) and this region holds only the f16 copy of x for FP8
-  // experts, or x's E4M3 codes (and x_scale their row scales) with FP8
-  // activations.
+  // for larger ones) and this region holds only x's two-term E4M3 rows
+  // (FP8 weights), the f16 copy of x (MXFP4 weights, or FP8 weights on the
+  // converters), or x's E4M3 codes with FP8 activations; x_scale holds the
+  // row scales of the E4M3 rows.
   const bool gather = path == Path::kTensor;
   const bool act8 = p.w_dtype == MOE_FP8_E4M3_ACT8;
+  const bool x2 = fp8_two_term(p.w_dtype);
   L.gather = gather;
-  const bool f16x = p.w_dtype == MOE_FP8_E4M3 || p.w_dtype == MOE_MXFP4;
-  L.x_perm = take(gather ? (f16x ? T * d * 2 : act8 ? T * d : 0) : R * d * ab);
-  L.x_scale = take(act8 ? T * 4 : 0);
+  const bool f16x = (p.w_dtype == MOE_FP8_E4M3 && !x2) || p.w_dtype == MOE_MXFP4;
+  L.x_perm = take(gather ? (f16x ? T * d * 2 : act8 ? T * d : x2 ? 2 * T * d : 0) : R * d * ab);
+  L.x_scale = take(act8 || x2 ? T * 4 : 0);
   L.h = take(R * f * ab);
-  // FP8 activations: h's E4M3 codes and row scales for the down GEMM
-  L.h_q = take(act8 ? R * f : 0);
-  L.h_scale = take(act8 ? R * 4 : 0);
+  // E4M3 rows of h (one per row with FP8 activations, two with two-term
+  // rows) and their row scales, for the down GEMM
+  L.h_q = take(act8 ? R * f : x2 ? 2 * R * f : 0);
+  L.h_scale = take(act8 || x2 ? R * 4 : 0);
   const size_t S = path == Path::kTensor ? (size_t)L.plan.splits_down : 1;
   L.y = take(S > 1 ? S * R * d * 4 : R * d * ab);
   L.sh_offsets = take(8);
@@ -253,6 +256,7 @@ moe_status moe_grouped_swiglu(const moe_problem* p, const void* x_perm, const in
   for (const void* q : {x_perm, w_gate, w_up, w_down, (const void*)y_perm})
     if (!aligned16(q)) return MOE_ERR_INVALID_ARG;
   const bool fp8 = quantised_weights(p->w_dtype), act8 = p->w_dtype == MOE_FP8_E4M3_ACT8;
+  const bool x2 = fp8_two_term(p->w_dtype);
   if (fp8 != (s_gate != nullptr) || fp8 != (s_up != nullptr) || fp8 != (s_down != nullptr))
     return MOE_ERR_INVALID_ARG;
   DeviceCtx ctx;
@@ -260,20 +264,28 @@ moe_status moe_grouped_swiglu(const moe_problem* p, const void* x_perm, const in
   const Layout L = layout(*p, path, ctx.num_sms, false);
   const size_t R = (size_t)p->T * p->k;
   const size_t h_bytes = align256(R * p->ffn * act_bytes(p->act_dtype));
-  // FP8 experts run on f16 operands: round x_perm to f16 into the
-  // workspace; with FP8 activations, its E4M3 codes and row scales
-  const size_t rows_bytes = act8 ? align256(R * p->d) : fp8 ? align256(R * p->d * 2) : 0;
-  // (FP8 activations: x_perm's codes, their scales, then h's codes and scales)
-  const size_t hq_off = h_bytes + rows_bytes + (act8 ? align256(R * 4) : 0);
-  const size_t need = hq_off + (act8 ? align256(R * p->ffn) + align256(R * 4) : 0);
+  // FP8 weights: x_perm's rows split into two E4M3 rows each (or, on the
+  // converters, rounded to f16); with FP8 activations, their E4M3 codes;
+  // E4M3 rows come with row scales
+  const size_t rows_bytes = act8 ? align256(R * p->d) : x2 ? align256(2 * R * p->d)
+                                                       : fp8 ? align256(R * p->d * 2) : 0;
+  const bool e4m3_rows = act8 || x2;
+  // (E4M3 rows: x_perm's codes, their scales, then h's codes and scales)
+  const size_t hq_off = h_bytes + rows_bytes + (e4m3_rows ? align256(R * 4) : 0);
+  const size_t hq_bytes = act8 ? align256(R * p->ffn) : x2 ? align256(2 * R * p->ffn) : 0;
+  const size_t need = hq_off + (e4m3_rows ? hq_bytes + align256(R * 4) : 0);
   if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const void* rows = x_perm;
   float* row_scale = nullptr;
-  if (act8) {
+  if (e4m3_rows) {
     row_scale = at<float>(workspace, h_bytes + rows_bytes);
-    MOE_TRY(quantize_rows_e4m3_launch(x_perm, (int)R, p->d, at<uint8_t>(workspace, h_bytes), row_scale,
-                                      ctx.num_sms, s));
+    if (x2)
+      MOE_TRY(split_rows_e4m3x2_launch(x_perm, (int)R, p->d, at<uint8_t>(workspace, h_bytes), row_scale,
+                                       ctx.num_sms, s));
+    else
+      MOE_TRY(quantize_rows_e4m3_launch(x_perm, (int)R, p->d, at<uint8_t>(workspace, h_bytes), row_scale,
+                                        ctx.num_sms, s));
     rows = at<uint8_t>(workspace, h_bytes);
   } else if (fp8) {
     void* xf16 = at<uint8_t>(workspace, h_bytes);
@@ -283,8 +295,8 @@ moe_status moe_grouped_swiglu(const moe_problem* p, const void* x_perm, const in
   return run_grouped(path, (int)R, p->d, p->ffn, p->E, p->w_dtype, rows, offsets, w_gate, w_up,
                      w_down, s_gate, s_up, s_down, workspace, y_perm, L.plan, ctx.status, s,
                      nullptr, nullptr, nullptr, 0, nullptr, nullptr, row_scale,
-                     act8 ? at<uint8_t>(workspace, hq_off) : nullptr,
-                     act8 ? at<float>(workspace, hq_off + align256(R * p->ffn)) : nullptr);
+                     e4m3_rows ? at<uint8_t>(workspace, hq_off) : nullptr,
+                     e4m3_rows ? at<float>(workspace, hq_off + hq_bytes) : nullptr);
 }
 
 moe_status moe_quantize_rows_e4m3(int32_t rows, int32_t cols, const void* x, uint8_t* codes,
@@ -299,6 +311,20 @@ moe_status moe_quantize_rows_e4m3(int32_t rows, int32_t cols, const void* x, uin
   MOE_TRY(device_ctx(&ctx));
   return quantize_rows_e4m3_launch(x, rows, cols, codes, scales, ctx.num_sms,
                                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_split_rows_e4m3x2(int32_t rows, int32_t cols, const void* x, uint8_t* codes, float* scales,
+                                 moe_stream_t stream) {
+  if (rows < 0) return MOE_ERR_INVALID_ARG;
+  if (cols <= 0 || cols % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (rows == 0) return MOE_OK;
+  if (x == nullptr || codes == nullptr || scales == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(codes) || (reinterpret_cast<uintptr_t>(scales) & 3u) != 0)
+    return MOE_ERR_INVALID_ARG;
+  DeviceCtx ctx;
+  MOE_TRY(device_ctx(&ctx));
+  return split_rows_e4m3x2_launch(x, rows, cols, codes, scales, ctx.num_sms,
+                                  reinterpret_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_combine(const moe_problem* p, const void* y_perm, const int32_t* inv_row,
@@ -417,11 +443,18 @@ moe_status layer_forward_impl(const moe_problem* p, const void* x, const void* w
   // 3. grouped SwiGLU experts (gate/up + SiLU*mul, then down)
   // FP8 experts gather from an f16 copy of x; with FP8 activations, from
   // x's per-row E4M3 codes (quantised before dispatch: T rows, not T*k)
+  // FP8 weights gather x's two-term E4M3 rows (split once per token, before
+  // dispatch)
   const void* x_src = x;
   float* x_scale = nullptr;
+  const bool x2 = fp8_two_term(p->w_dtype);
   if (gather && act8) {
     x_scale = at<float>(workspace, L.x_scale);
     MOE_TRY(quantize_rows_e4m3_launch(x, p->T, p->d, x_perm, x_scale, ctx.num_sms, s));
+    x_src = x_perm;
+  } else if (gather && x2) {
+    x_scale = at<float>(workspace, L.x_scale);
+    MOE_TRY(split_rows_e4m3x2_launch(x, p->T, p->d, x_perm, x_scale, ctx.num_sms, s));
     x_src = x_perm;
   } else if (gather && fp8) {
     MOE_TRY(bf16_to_f16_launch(x, x_perm, (size_t)p->T * p->d, s));
@@ -431,8 +464,8 @@ moe_status layer_forward_impl(const moe_problem* p, const void* x, const void* w
                       w_down, s_gate, s_up, s_down, h, y, L.plan, ctx.status, s,
                       timer ? timer->ev[3] : nullptr, gather ? perm_token : nullptr, x_src, p->T,
                       at<float>(workspace, L.gu_part), L.cnt_routed ? at<int>(workspace, L.gu_cnt) : nullptr,
-                      x_scale, act8 ? at<uint8_t>(workspace, L.h_q) : nullptr,
-                      act8 ? at<float>(workspace, L.h_scale) : nullptr));
+                      x_scale, act8 || x2 ? at<uint8_t>(workspace, L.h_q) : nullptr,
+                      act8 || x2 ? at<float>(workspace, L.h_scale) : nullptr));
   MOE_TRY(mark(4));
   // 4. shared expert (CUDA-core path: here, one group {0, T}); on the
   // tensor path, join the side stream
@@ -576,8 +609,9 @@ moe_status moe_layer_launch_count_for(const moe_problem* p, int32_t num_sms, int
   if (fuse_topk_in_permute(p->T, p->k, p->E, rs)) n -= 1;
   const Layout L = layout(*p, path, num_sms, true);
   n += permute_launch_count(p->T, p->k, !L.gather);
-  if (L.gather && quantised_weights(p->w_dtype)) n += 1;  // x -> f16, or x -> E4M3 codes
-  if (p->w_dtype == MOE_FP8_E4M3_ACT8) n += 1;        // h -> E4M3 codes
+  if (L.gather && quantised_weights(p->w_dtype)) n += 1;  // x -> f16, or x -> E4M3 rows
+  // h -> E4M3 codes, or h -> two-term E4M3 rows
+  if (p->w_dtype == MOE_FP8_E4M3_ACT8 || (path == Path::kTensor && fp8_two_term(p->w_dtype))) n += 1;
   n += 2;                        // gate/up, down
   // split-K gate/up: a finalize pass unless the GEMM finalizes itself
   // (decode tiles)

@@ -214,6 +214,12 @@ moe_status bf16_to_f16_launch(const void* src, void* dst, size_t n, cudaStream_t
 // mode's operands of both expert GEMMs.
 moe_status quantize_rows_e4m3_launch(const void* x, int rows, int d, void* codes, float* scales,
                                      int num_sms, cudaStream_t s, bool f16_in = false);
+// Two-term E4M3 encoding of 16-bit rows (bf16, or f16 with f16_in): codes
+// [rows, 2, d] (hi row, then lo row) and power-of-two scales [rows] with
+// x = s * (hi + lo / 16), exact for elements within 2^13 of the row's
+// largest magnitude: the operands of FP8-weight GEMMs on bf16 activations.
+moe_status split_rows_e4m3x2_launch(const void* x, int rows, int d, void* codes, float* scales, int num_sms,
+                                    cudaStream_t s, bool f16_in = false);
 
 struct CombineArgs {
   int T, k, d, act_dtype;
@@ -284,6 +290,9 @@ struct TcGroupedArgs {
   void* h_q;
   float* h_scale;
 };
+// FP8 weights with bf16 activations run on two-term E4M3 rows (the default;
+// MOE_FP8_CONVERT=1 selects the E4M3 -> f16 weight converters instead).
+bool fp8_two_term(int w_dtype);
 // Arrival counters the fused gate/up finalize needs for R rows in G groups.
 size_t gu_counters_size(int R, int G, int ffn, const TcPlan& plan);
 TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype);

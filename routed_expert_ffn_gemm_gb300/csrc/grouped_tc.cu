@@ -42,13 +42,18 @@
 // is bounded: on expiry the kernel records MOE_ERR_DEVICE_TIMEOUT, lets
 // issued copies land, frees TMEM and returns.
 //
-// FP8 weights ("MoE 推理部署", section 专家量化: per-expert scales) are
-// dequantised in-kernel: every E4M3 value is exact in f16 and one hardware
-// conversion turns two of them into an f16 pair, so the MMA runs kind::f16
-// with f16 operands (weights exact; activations and h carried in f16, which
-// holds bf16 values exactly inside f16's normal range) and the
-// per-output-channel scale (one TMEM lane = one channel) multiplies the fp32
-// accumulator in the epilogue.
+// FP8 weights with bf16 activations ("MoE 推理部署", section 专家量化:
+// per-expert scales): every bf16 row (token rows, rows of h) arrives as two
+// E4M3 rows, hi and lo, with one power-of-two scale s per row and
+// x = s * (hi + lo / 16) -- an exact re-encoding of the bf16 values (see
+// the row split in quantize.cu).  Both operands then go straight from the
+// TMA ring to tcgen05.mma kind::f8f6f4; a tile of n rows is an MMA of 2n
+// columns (hi and lo of row j in columns 2j and 2j+1), and the epilogue
+// forms s * (acc[2j] + acc[2j+1] / 16) times the output channel's scale.
+// The products of E4M3 weights and E4M3 terms are exact, so this computes
+// what a 16-bit MMA on the bf16 rows would, with no weight conversion.
+// (The E4M3 -> f16 converter path below remains for MXFP4 weights, and for
+// FP8 weights when MOE_FP8_CONVERT=1 selects it.)
 //
 // FP8 activations ("MOE推理流程解析", section 三: activations quantised
 // before dispatch; gate/up only): the B rows arrive as E4M3 codes with one
@@ -135,12 +140,19 @@ __host__ __device__ constexpr bool ta_config(int mode, int bn, bool fp8, bool pa
 // kind::f8f6f4 MMA (gate/up only: the FP8-activation mode); MXFP4 weights
 // (E2M1 codes with a UE8M0 scale per 32 along K) converted to f16 for a
 // kind::f16 MMA.
-enum { kWBf16 = 0, kWFp8 = 1, kWFp8Act8 = 2, kWMx4 = 3 };
+// FP8 weights times bf16 rows carried as two E4M3 terms (kind::f8f6f4,
+// two B rows per row: the default for FP8 weights with bf16 activations).
+enum { kWBf16 = 0, kWFp8 = 1, kWFp8Act8 = 2, kWMx4 = 3, kWFp8X2 = 4 };
 
 template <int MODE, int BN, int WF, bool PAIR>
 struct Cfg {
   static constexpr bool FP8 = WF != kWBf16;     // quantised weights: staged, f16 h (or E4M3 rows)
-  static constexpr bool A8 = WF == kWFp8Act8;   // E4M3 weights times E4M3 token rows (kind::f8f6f4)
+  static constexpr bool X2 = WF == kWFp8X2;     // bf16 rows as two E4M3 rows each
+  // E4M3 weights times E4M3 rows (kind::f8f6f4): FP8 activations, or the
+  // two-term rows
+  static constexpr bool A8 = WF == kWFp8Act8 || X2;
+  static constexpr int RM = X2 ? 2 : 1;         // B rows (accumulator columns) per row of the tile
+  static constexpr bool H16 = FP8 && !X2;       // h stored in f16 (else bf16)
   static constexpr bool MX4 = WF == kWMx4;      // MXFP4 weights (block scales applied by the converters)
   static constexpr bool CHS = FP8 && !MX4;      // per-output-channel weight scales in the epilogue
   static constexpr bool CONV = WF == kWFp8 || MX4;  // converter warps write f16 weight operands
@@ -169,7 +181,7 @@ struct Cfg {
   static constexpr int NSUB = A8 ? 1 : KB / kBK;               // 128-byte B sub-tiles per stage
   static constexpr int KSTEP = A8 ? 32 : 16;                   // K per MMA instruction
   static constexpr int A_BYTES = kBM * kBK * 2;                // 16 KB bf16 tile (MMA operand)
-  static constexpr int BSUB_BYTES = (PAIR ? BN / 2 : BN) * kBK * 2;
+  static constexpr int BSUB_BYTES = RM * (PAIR ? BN / 2 : BN) * kBK * 2;
   static constexpr int B_BYTES = NSUB * BSUB_BYTES;
   // staged weight codes: E4M3 (8 or 16 KB), or packed E2M1 (half that)
   // followed by the UE8M0 block scales, KB/32 runs of 128 bytes
@@ -188,7 +200,7 @@ struct Cfg {
   static constexpr int AVAIL_ = kSmemLimit - 1024 - (8 * 40 + 16 + 4 * 2 * (kMaxGroups + 8));
   // TMEM: one accumulator buffer = NA accumulators of max(BN,128) columns;
   // two buffers when they fit beside the operand slots of the TA path
-  static constexpr int UP_OFF = BN > 128 ? BN : 128;
+  static constexpr int UP_OFF = RM * BN > 128 ? RM * BN : 128;
   static constexpr int ACC_COLS = NA * UP_OFF;
   static constexpr bool TA_DECODE = TA && BN == 32;
   static constexpr int NBUF = TA && !TA_DECODE ? (2 * ACC_COLS + 2 * 64 * NA <= 512 ? 2 : 1)
@@ -229,7 +241,7 @@ struct Cfg {
   // their 1 KB reservations overflow the SM's 228 KB.
   static_assert(2 * (SMEM_BYTES + 1024) > kSmemLimit + 1024, "one TMEM-holding CTA per SM");
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
-  static_assert(BN % 16 == 0 && BN <= 256 && ACC_COLS <= 512, "tile rows");
+  static_assert(BN % 16 == 0 && RM * BN <= 256 && ACC_COLS <= 512, "tile rows");
   static_assert(!PAIR || BN >= 32, "pair tiles split B rows in halves");
   static_assert(!TA || (OSTAGES >= 2 && (TA_DECODE ? UP_OFF == 128 && ACC_COLS * NBUF <= 512 && OSTAGES * NA <= 4
                                                   : NBUF * ACC_COLS + OSTAGES * NA * 64 <= 512)),
@@ -493,26 +505,33 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
         // the tile's MMA width rounded to 32
         const int bhalf = PAIR ? ((x.n_valid + 31) / 32) * 16 : x.n_valid;
         const int brow0 = x.row0 + (int)rank * bhalf;
-        const int nbox = (bhalf + p.boxn - 1) / p.boxn;
-        const int nops = (x.n_valid + 3) / 4;  // gather4 copies of this tile
-        // this lane's gather rows: ops lane and lane + 32 (BN <= 256); rows
-        // past the group's end repeat its first row (their columns are unused)
+        // (B rows of the operand: RM per row of the tile, the row's RM
+        // consecutive rows RM * row .. RM * row + RM - 1 of the B matrix)
+        const int nbox = (C::RM * bhalf + p.boxn - 1) / p.boxn;
+        const int nops = (C::RM * x.n_valid + 3) / 4;  // gather4 copies of this tile
+        // this lane's gather rows: ops lane and lane + 32 (RM * BN <= 256);
+        // rows past the group's end repeat its first row (their columns are
+        // unused)
         int gr[2][4];
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const int i = 4 * (lane + 32 * h) + q;
-            gr[h][q] = (gather && lane + 32 * h < nops) ? p.gather_rows[x.row0 + (i < x.n_valid ? i : 0)] : 0;
+            const int i = 4 * (lane + 32 * h) + q, li = i / C::RM;
+            gr[h][q] = (gather && lane + 32 * h < nops)
+                           ? C::RM * p.gather_rows[x.row0 + (li < x.n_valid ? li : 0)] + i % C::RM
+                           : 0;
           }
-        // gathered rows (lsu): this lane's rows lane + 32 i of the CTA's
-        // B rows, their token ids (-1: past the group's end, not copied)
-        constexpr int RPL = (PAIR ? BN / 2 : BN) / 32 > 0 ? (PAIR ? BN / 2 : BN) / 32 : 1;
+        // gathered rows (lsu): this lane's B rows lane + 32 i of the CTA,
+        // their source rows in x_src (-1: past the group's end, not copied)
+        constexpr int CROWS = C::RM * (PAIR ? BN / 2 : BN);
+        constexpr int RPL = CROWS / 32 > 0 ? CROWS / 32 : 1;
         int tok[RPL];
 #pragma unroll
         for (int i = 0; i < RPL; ++i) {
-          const int r = brow0 + lane + 32 * i;
-          tok[i] = (lsu && lane + 32 * i < bhalf && r < x.row0 + x.n_valid) ? p.gather_rows[r] : -1;
+          const int rr = lane + 32 * i, r = brow0 + rr / C::RM;
+          tok[i] = (lsu && rr < C::RM * bhalf && r < x.row0 + x.n_valid) ? C::RM * p.gather_rows[r] + rr % C::RM
+                                                                           : -1;
         }
         const uint32_t bbytes =
             lsu ? 0u : C::NSUB * (gather ? (uint32_t)nops * 4 * kBK * 2 : (uint32_t)nbox * p.boxn * kBK * 2);
@@ -537,7 +556,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
               const uint32_t fb = lead(full_bar(stage));
               ptx::mbar_arrive_expect_tx_cluster(fb, bytes);
               ptx::tma_load_3d_pair(sa, &tmA0, fb, arow, kb * 2, pol_w);
-              ptx::tma_load_3d_pair(sb, &tmB, fb, brow0, kb * 2, pol_x);
+              ptx::tma_load_3d_pair(sb, &tmB, fb, C::RM * brow0, kb * 2, pol_x);
             } else if (PAIR && !CONV) {
               // both CTAs' copies complete the even CTA's barrier
               const uint32_t fb = lead(full_bar(stage));
@@ -546,7 +565,8 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
               if (MODE == kGateUp) ptx::tma_load_2d_pair(sa + C::W_BYTES, &tmA1, fb, kb * C::KB, arow, pol_w);
               if (!lsu)
                 for (int i = 0; i < nbox; ++i)
-                  ptx::tma_load_2d_pair(sb + i * p.boxn * kBK * 2, &tmB, fb, kb * C::KB, brow0 + i * p.boxn, pol_x);
+                  ptx::tma_load_2d_pair(sb + i * p.boxn * kBK * 2, &tmB, fb, kb * C::KB,
+                                        C::RM * brow0 + i * p.boxn, pol_x);
             } else {
               ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
               // weight codes (MXFP4: two per byte), then (MXFP4) the
@@ -566,23 +586,28 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
                 for (int sub = 0; sub < C::NSUB; ++sub)
                   for (int i = 0; i < nbox; ++i)
                     ptx::tma_load_2d(sb + sub * C::BSUB_BYTES + i * p.boxn * kBK * 2, &tmB, full_bar(stage),
-                                     kb * C::KB + sub * kBK, brow0 + i * p.boxn, pol_x);
+                                     kb * C::KB + sub * kBK, C::RM * brow0 + i * p.boxn, pol_x);
             }
           }
           if (lsu) {
-            // every lane: its rows' 128-byte K slices (per 64-element
-            // sub-tile), chunk c of row r at chunk c ^ (r % 8); then one
-            // arrival per lane once its copies have landed
+            // eight lanes per row, one 16-byte chunk each: a warp-wide copy
+            // moves four rows' whole 128-byte K slices (per 64-element
+            // sub-tile), so every 32-byte sector is fetched once; chunk c of
+            // row r lands at chunk c ^ (r % 8).  Row 32 i + j's source is
+            // lane j's tok[i].  Then one arrival per lane once its copies
+            // have landed.
+            const int q = lane >> 3, c = lane & 7;
 #pragma unroll
             for (int i = 0; i < RPL; ++i) {
-              if (tok[i] < 0) continue;
-              const int r = lane + 32 * i;
 #pragma unroll
-              for (int sub = 0; sub < C::NSUB; ++sub) {
-                const uint8_t* src = xs + ((size_t)tok[i] * p.d_src + (size_t)kb * C::KB + sub * kBK) * kEsz;
-                const uint32_t dst = sb + sub * C::BSUB_BYTES + r * 128;
+              for (int g = 0; g < 8; ++g) {
+                const int t = __shfl_sync(0xffffffffu, tok[i], 4 * g + q);
+                if (t < 0) continue;
+                const int r = 32 * i + 4 * g + q;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) ptx::cp_async16(dst + ((c ^ (r & 7)) << 4), src + 16 * c);
+                for (int sub = 0; sub < C::NSUB; ++sub)
+                  ptx::cp_async16(sb + sub * C::BSUB_BYTES + r * 128 + ((c ^ (r & 7)) << 4),
+                                  xs + ((size_t)t * p.d_src + (size_t)kb * C::KB + sub * kBK) * kEsz + 16 * c);
               }
             }
             ptx::cp_async_arrive_noinc(relay ? bfull_bar(stage) : full_bar(stage));
@@ -656,7 +681,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
             break;
           }
           ptx::tc_fence_after();
-          const int n_mma = PAIR ? ((x.n_valid + 31) / 32) * 32 : ((x.n_valid + 15) / 16) * 16;
+          const int n_mma = C::RM * (PAIR ? ((x.n_valid + 31) / 32) * 32 : ((x.n_valid + 15) / 16) * 16);
           // (kind::f8f6f4 takes the same descriptor bits: E4M3 is format 0)
           const uint32_t idesc = FP8 ? ptx::idesc_f16_f32(C::CH, n_mma) : ptx::idesc_bf16_f32(C::CH, n_mma);
           const uint32_t d0 = tmem_base + (uint32_t)(C::ACC_COLS * buf);
@@ -786,7 +811,8 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(C::ACC_COLS * buf);
       const int ch = x.mt * C::CH + (int)rank * kBM + ch_local;
       const bool empty_k = x.ks * kb_per_split >= kblocks;
-      const int n_mma = ((x.n_valid + 15) / 16) * 16;
+      // accumulator columns holding the tile's rows (RM per row)
+      const int n_mma = C::RM * (((x.n_valid + 15) / 16) * 16);
       const float sc0 = C::CHS ? p.scale0[(size_t)x.g * p.M + ch] : 1.f;
       const float sc1 = C::CHS && MODE == kGateUp ? p.scale1[(size_t)x.g * p.M + ch] : 1.f;
       // CW accumulator columns per TMEM wait: 32 for the projection (its
@@ -796,79 +822,87 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
       constexpr int CW = MODE == kGateUp ? 16 : 32;
 #pragma unroll 1
       for (int c0 = eg * CW; c0 < n_mma; c0 += 2 * CW) {
-        uint32_t ra[CW], rb[CW];
+        uint32_t ra[CW], rb_[CW];
 #pragma unroll
         for (int hlf = 0; hlf < CW / 16; ++hlf) {
           ptx::tmem_ld16(taddr + c0 + 16 * hlf, *reinterpret_cast<uint32_t(*)[16]>(&ra[16 * hlf]));
           if (MODE == kGateUp)
             ptx::tmem_ld16(taddr + (uint32_t)C::UP_OFF + c0 + 16 * hlf,
-                           *reinterpret_cast<uint32_t(*)[16]>(&rb[16 * hlf]));
+                           *reinterpret_cast<uint32_t(*)[16]>(&rb_[16 * hlf]));
         }
         ptx::tmem_ld_wait();
         if (empty_k) {
           // a K split past the end of K (ceil-sized splits): no MMA wrote
           // this accumulator, its partial sums are zero
 #pragma unroll
-          for (int j = 0; j < CW; ++j) ra[j] = rb[j] = 0u;
+          for (int j = 0; j < CW; ++j) ra[j] = rb_[j] = 0u;
         }
         // halves of 16 columns; the empty asm keeps the compiler from
         // interleaving them (which costs registers, not time)
 #pragma unroll
         for (int hlf = 0; hlf < CW / 16; ++hlf) {
-          const int cb = c0 + 16 * hlf;
-          const int nj = min(16, x.n_valid - cb);
+          // 16 accumulator columns: rows rb .. rb + NJ - 1 of the tile
+          constexpr int NJ = 16 / C::RM;
+          const int rb = (c0 + 16 * hlf) / C::RM;
+          const int nj = min(NJ, x.n_valid - rb);
           const uint32_t* a = ra + 16 * hlf;
-          const uint32_t* b = rb + 16 * hlf;
+          const uint32_t* b = rb_ + 16 * hlf;
+          // a row's value: its column, or (two-term rows) hi + lo / 16
+          auto val = [&](const uint32_t* acc, int j) {
+            if constexpr (C::RM == 2)
+              return fmaf(__uint_as_float(acc[2 * j + 1]), 0.0625f, __uint_as_float(acc[2 * j]));
+            else
+              return __uint_as_float(acc[j]);
+          };
           if (nj > 0) {
-            // FP8 activations: each column (token row, or row of h) carries
-            // its row's quantisation scale (rows gathered by token: the
-            // token's)
-            float rsc[16];
+            // E4M3 rows: each column (token row, or row of h) carries its
+            // row's scale (rows gathered by token: the token's)
+            float rsc[NJ];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
+            for (int j = 0; j < NJ; ++j) {
               rsc[j] = 1.f;
               if (A8 && j < nj) {
-                const int r = x.row0 + cb + j;
+                const int r = x.row0 + rb + j;
                 rsc[j] = p.row_scale[p.gather_rows != nullptr ? p.gather_rows[r] : r];
               }
             }
             if (MODE == kGateUp) {
               if (p.out_f32) {
                 // K-split: scaled fp32 partials, SiLU*mul after the in-order sum
-                float* row = static_cast<float*>(p.out) + ((size_t)x.ks * p.R + x.row0 + cb) * 2 * p.M + ch;
+                float* row = static_cast<float*>(p.out) + ((size_t)x.ks * p.R + x.row0 + rb) * 2 * p.M + ch;
 #pragma unroll
-                for (int j = 0; j < 16; ++j, row += 2 * p.M)
+                for (int j = 0; j < NJ; ++j, row += 2 * p.M)
                   if (j < nj) {
-                    row[0] = __uint_as_float(a[j]) * sc0 * rsc[j];
-                    row[p.M] = __uint_as_float(b[j]) * sc1 * rsc[j];
+                    row[0] = val(a, j) * sc0 * rsc[j];
+                    row[p.M] = val(b, j) * sc1 * rsc[j];
                   }
-              } else if (FP8) {
-                __half* o = static_cast<__half*>(p.out) + (size_t)(x.row0 + cb) * p.M + ch;  // h feeds an f16 MMA
+              } else if (C::H16) {
+                __half* o = static_cast<__half*>(p.out) + (size_t)(x.row0 + rb) * p.M + ch;  // h feeds an f16 MMA
 #pragma unroll
-                for (int j = 0; j < 16; ++j, o += p.M)
+                for (int j = 0; j < NJ; ++j, o += p.M)
                   if (j < nj) {
-                    const float g = __uint_as_float(a[j]) * sc0 * rsc[j];
-                    *o = __float2half_rn(silu_mul(g, __uint_as_float(b[j]) * sc1 * rsc[j]));
+                    const float g = val(a, j) * sc0 * rsc[j];
+                    *o = __float2half_rn(silu_mul(g, val(b, j) * sc1 * rsc[j]));
                   }
               } else {
-                __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + (size_t)(x.row0 + cb) * p.M + ch;
+                __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + (size_t)(x.row0 + rb) * p.M + ch;
 #pragma unroll
-                for (int j = 0; j < 16; ++j, o += p.M)
+                for (int j = 0; j < NJ; ++j, o += p.M)
                   if (j < nj) {
-                    const float g = __uint_as_float(a[j]);
-                    store_out(o, silu_mul(g, __uint_as_float(b[j])));
+                    const float g = val(a, j) * sc0 * rsc[j];
+                    store_out(o, silu_mul(g, val(b, j) * sc1 * rsc[j]));
                   }
               }
             } else if (p.out_f32) {
-              float* o = static_cast<float*>(p.out) + ((size_t)x.ks * p.R + x.row0 + cb) * p.M + ch;
+              float* o = static_cast<float*>(p.out) + ((size_t)x.ks * p.R + x.row0 + rb) * p.M + ch;
 #pragma unroll
-              for (int j = 0; j < 16; ++j, o += p.M)
-                if (j < nj) *o = __uint_as_float(a[j]) * sc0 * rsc[j];
+              for (int j = 0; j < NJ; ++j, o += p.M)
+                if (j < nj) *o = val(a, j) * sc0 * rsc[j];
             } else {
-              __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + (size_t)(x.row0 + cb) * p.M + ch;
+              __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + (size_t)(x.row0 + rb) * p.M + ch;
 #pragma unroll
-              for (int j = 0; j < 16; ++j, o += p.M)
-                if (j < nj) store_out(o, __uint_as_float(a[j]) * sc0 * rsc[j]);
+              for (int j = 0; j < NJ; ++j, o += p.M)
+                if (j < nj) store_out(o, val(a, j) * sc0 * rsc[j]);
             }
           }
           asm volatile("" ::: "memory");
@@ -915,7 +949,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
               uv += us[sp];
             }
             const float hv = silu_mul(g, uv);
-            if (FP8)
+            if (C::H16)
               static_cast<__half*>(p.fin_out)[(size_t)r * p.M + c] = __float2half_rn(hv);
             else
               store_out(static_cast<__nv_bfloat16*>(p.fin_out) + (size_t)r * p.M + c, hv);
@@ -1150,6 +1184,8 @@ moe_status launch_mode(int bn, int wf, bool pair, const TcParams& p, const CUten
     MOE_LAUNCH(32, kWFp8Act8, true);
     MOE_LAUNCH(128, kWFp8Act8, true);
     MOE_LAUNCH(256, kWFp8Act8, true);
+    MOE_LAUNCH(32, kWFp8X2, true);
+    MOE_LAUNCH(128, kWFp8X2, true);
     return MOE_ERR_UNSUPPORTED;
   }
   MOE_LAUNCH(32, kWFp8, false);
@@ -1164,6 +1200,8 @@ moe_status launch_mode(int bn, int wf, bool pair, const TcParams& p, const CUten
   MOE_LAUNCH(32, kWFp8Act8, false);
   MOE_LAUNCH(128, kWFp8Act8, false);
   MOE_LAUNCH(256, kWFp8Act8, false);
+  MOE_LAUNCH(32, kWFp8X2, false);
+  MOE_LAUNCH(128, kWFp8X2, false);
 #undef MOE_LAUNCH
   return MOE_ERR_UNSUPPORTED;
 }
@@ -1174,6 +1212,16 @@ int env_int(const char* name) {
 }
 
 int bn_ok(int bn) { return bn == 32 || bn == 128 || bn == 256 ? bn : 0; }
+
+}  // namespace
+
+bool fp8_two_term(int w_dtype) {
+  // (read on every call, like the other tuning switches: the workspace
+  // size and the launches must see the same setting)
+  return w_dtype == MOE_FP8_E4M3 && env_int("MOE_FP8_CONVERT") != 1;
+}
+
+namespace {
 
 // K splits (<= 8, each >= 4 k-blocks) so that `units` work units fill whole
 // waves of the SMs when there are fewer than two waves of them.
@@ -1244,12 +1292,16 @@ TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype) {
   const double mean = R / E;
   const double est_max = mean + 3.0 * __builtin_sqrt(mean) + 1.0;
   const int bn = est_max <= 32.0 ? 32 : 128;
-  // FP8 weights keep 128-row gate/up tiles: on CTA pairs their accumulators
-  // leave room in TMEM for the f16 weight operand (the TA path)
+  // Two-term rows (FP8 weights, bf16 activations) take two accumulator
+  // columns per row, so their tiles stop at 128 rows (256 columns).
+  // Converted FP8 weights keep 128-row gate/up tiles: on CTA pairs their
+  // accumulators leave room in TMEM for the f16 weight operand (the TA path)
+  const bool x2 = fp8_two_term(w_dtype);
   const int bn_gu = (bn == 128 && mean >= 128.0 && w_dtype != MOE_FP8_E4M3 && w_dtype != MOE_MXFP4) ? 256 : bn;
-  const int bn_dn = (bn == 128 && mean >= 128.0) ? 256 : bn;
-  pl.bn_gateup = bn_ok(env_int("MOE_BN_GATEUP")) ? env_int("MOE_BN_GATEUP") : bn_gu;
-  pl.bn_down = bn_ok(env_int("MOE_BN_DOWN")) ? env_int("MOE_BN_DOWN") : bn_dn;
+  const int bn_dn = (bn == 128 && mean >= 128.0 && !x2) ? 256 : bn;
+  auto bn_env = [&](const char* name) { return x2 && env_int(name) == 256 ? 0 : bn_ok(env_int(name)); };
+  pl.bn_gateup = bn_env("MOE_BN_GATEUP") ? env_int("MOE_BN_GATEUP") : bn_gu;
+  pl.bn_down = bn_env("MOE_BN_DOWN") ? env_int("MOE_BN_DOWN") : bn_dn;
   const double touched = E < R ? E : R;
   auto tiles_of = [&](int bn_) {
     const double a = R / bn_;
@@ -1263,11 +1315,11 @@ TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype) {
   // measured no faster on pairs (within 1-2 %).
   const char* pe = getenv("MOE_PAIR");
   const bool pairs_ok = !(pe != nullptr && pe[0] == '0') && num_sms >= 2;
-  const bool act8 = w_dtype == MOE_FP8_E4M3_ACT8;
+  const bool act8 = w_dtype == MOE_FP8_E4M3_ACT8 || x2;  // (E4M3 rows: kind::f8f6f4)
   const bool fp8 = w_dtype == MOE_FP8_E4M3 || act8 || w_dtype == MOE_MXFP4;
   const bool dec_pairs = pairs_ok && pe != nullptr && pe[0] == '2';
   // K per stage: 128 on the FP8 tensor-memory operand path (decode tiles),
-  // with FP8 activations (128-byte rows of both operands), and for the bf16
+  // with E4M3 rows (128-byte rows of both operands), and for the bf16
   // down GEMM on pairs (two column blocks per copy)
   const int kw_dn = act8 || (fp8 && pl.bn_down == 32) ? 2 * kBK : kBK;
   const int kw_gu = act8 || (fp8 && pl.bn_gateup == 32) ? 2 * kBK : kBK;
@@ -1298,14 +1350,19 @@ TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype) {
 moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStream_t s,
                              cudaEvent_t mid) {
   if (a.R == 0) return MOE_OK;
-  const bool act8 = a.w_dtype == MOE_FP8_E4M3_ACT8;
+  const bool x2 = fp8_two_term(a.w_dtype);                     // bf16 rows as two E4M3 rows
+  const int rm = x2 ? 2 : 1;                                   // B rows per row
+  const bool fa8 = a.w_dtype == MOE_FP8_E4M3_ACT8;             // FP8 activations
+  const bool act8 = fa8 || x2;                                 // E4M3 rows, kind::f8f6f4
   const bool mx4 = a.w_dtype == MOE_MXFP4;
-  const bool fp8 = a.w_dtype == MOE_FP8_E4M3 || act8 || mx4;  // quantised weights: f16 operands, f16 h
+  const bool fp8 = a.w_dtype == MOE_FP8_E4M3 || act8 || mx4;  // quantised weights
+  const bool h16 = fp8 && !x2;                                 // h in f16 (converted weights, FP8 activations)
   if (!fp8 && a.w_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   if (fp8 && (a.s_gate == nullptr || a.s_up == nullptr || a.s_down == nullptr)) return MOE_ERR_INVALID_ARG;
   if (act8 && (a.row_scale == nullptr || a.h_q == nullptr || a.h_scale == nullptr)) return MOE_ERR_INVALID_ARG;
-  const int wf_gu = act8 ? kWFp8Act8 : mx4 ? kWMx4 : fp8 ? kWFp8 : kWBf16;
-  const int wf_dn = act8 ? kWFp8Act8 : mx4 ? kWMx4 : fp8 ? kWFp8 : kWBf16;
+  if (x2 && (plan.bn_gateup > 128 || plan.bn_down > 128)) return MOE_ERR_UNSUPPORTED;
+  const int wf_gu = x2 ? kWFp8X2 : fa8 ? kWFp8Act8 : mx4 ? kWMx4 : fp8 ? kWFp8 : kWBf16;
+  const int wf_dn = wf_gu;
   if (a.d % kBM != 0 || a.ffn % kBM != 0 || a.G > kMaxGroups) return MOE_ERR_UNSUPPORTED;
   // weights: bf16 tiles [128 x 64] with 128-byte swizzle, or E4M3 tiles
   // [128 x 64 bytes] staged unswizzled for the converters
@@ -1336,18 +1393,20 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   } else {
     sg = su = sd = wg;
   }
-  const int box_gu = boxn_of(plan.bn_gateup, plan.pair_gateup != 0);
-  const int box_dn = boxn_of(plan.bn_down, plan.pair_down != 0);
+  // (B rows per box: rm per row of the tile)
+  const int box_gu = rm * boxn_of(plan.bn_gateup, plan.pair_gateup != 0);
+  const int box_dn = rm * boxn_of(plan.bn_down, plan.pair_down != 0);
   // gathered token rows: TMA gather4 for decode tiles, cp.async by the
   // producer warp for prefill tiles (gather4 costs a copy per 4 rows)
   const bool lsu = a.gather_rows != nullptr && (plan.bn_gateup >= 128 || plan.pair_gateup);
   if (plan.pair_gateup && a.gather_rows != nullptr && !lsu) return MOE_ERR_UNSUPPORTED;
   // row operand: 128-byte rows, 64 16-bit elements or 128 E4M3 codes
+  // (two-term rows: rm = 2 code rows per row)
   const int xe = act8 ? 1 : 2, xk = act8 ? 2 * kBK : kBK;
   if (a.gather_rows != nullptr)  // token rows by index: one-row boxes for gather4
-    MOE_TRY(make_tmap_2d(&xb, a.x_src, a.T_src, a.d, xe, 1, xk, 128));
+    MOE_TRY(make_tmap_2d(&xb, a.x_src, (uint64_t)rm * a.T_src, a.d, xe, 1, xk, 128));
   else
-    MOE_TRY(make_tmap_2d(&xb, a.x_perm, a.R, a.d, xe, box_gu, xk, 128));
+    MOE_TRY(make_tmap_2d(&xb, a.x_perm, (uint64_t)rm * a.R, a.d, xe, box_gu, xk, 128));
   // bf16 down GEMM on pairs: 3-D maps, one copy per operand and stage (its
   // B rows in one box: all BN/2 rows of the CTA)
   const bool k2_dn = !fp8 && plan.pair_down;
@@ -1356,9 +1415,9 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
     MOE_TRY(make_tmap_kpair(&hb, a.h, a.R, a.ffn, 2, plan.bn_down / 2));
   } else {
     MOE_TRY(make_tmap_2d(&wd, a.w_down, (uint64_t)a.G * a.d, wcols_dn, wb, kBM, wk_dn, wsw_dn));
-    // h rows: 16-bit, or (FP8 activations) their E4M3 codes, 128-byte rows
+    // h rows: 16-bit, or their E4M3 codes (rm code rows per row), 128-byte rows
     if (act8)
-      MOE_TRY(make_tmap_2d(&hb, a.h_q, a.R, a.ffn, 1, box_dn, 2 * kBK, 128));
+      MOE_TRY(make_tmap_2d(&hb, a.h_q, (uint64_t)rm * a.R, a.ffn, 1, box_dn, 2 * kBK, 128));
     else
       MOE_TRY(make_tmap_2d(&hb, a.h, a.R, a.ffn, 2, box_dn, kBK, 128));
   }
@@ -1398,7 +1457,7 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   if (gu_split && !gu_fused) {
     const size_t n = (size_t)a.R * a.ffn;
     const int blocks = (int)((n + 255) / 256 < 8192 ? (n + 255) / 256 : 8192);
-    if (fp8)
+    if (h16)
       MOE_TRY_CUDA(launch_k(swiglu_finalize_kernel<__half>, dim3(blocks), dim3(256), 0, s, a.R, a.ffn,
                             plan.splits_gateup, (const float*)a.gu_partials, static_cast<__half*>(a.h)));
     else
@@ -1407,8 +1466,10 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
                             static_cast<__nv_bfloat16*>(a.h)));
   }
   if (mid != nullptr) MOE_TRY_CUDA(record_event(mid, s));
-  // FP8 activations: h's rows quantised per row for the down GEMM
-  if (act8) MOE_TRY(quantize_rows_e4m3_launch(a.h, a.R, a.ffn, a.h_q, a.h_scale, plan.grid, s, true));
+  // FP8 activations: h's rows quantised per row for the down GEMM; two-term
+  // rows: h's bf16 rows split exactly into their two E4M3 rows
+  if (fa8) MOE_TRY(quantize_rows_e4m3_launch(a.h, a.R, a.ffn, a.h_q, a.h_scale, plan.grid, s, true));
+  if (x2) MOE_TRY(split_rows_e4m3x2_launch(a.h, a.R, a.ffn, a.h_q, a.h_scale, plan.grid, s));
 
   p.M = a.d;
   p.K = a.ffn;

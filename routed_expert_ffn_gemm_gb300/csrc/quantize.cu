@@ -77,7 +77,90 @@ __global__ void __launch_bounds__(kQThreads) quantize_rows_e4m3_kernel(const uin
   }
 }
 
+// Two-term E4M3 encoding of bf16 rows, exact for every element within 2^13
+// of its row's largest magnitude (and within s * 2^-14 below that):
+//   s_t      = 2^p, p the integer with max_i |x[t,i]| / 2^p in (224, 448]
+//              (1 for an all-zero row)
+//   hi[t,i]  = E4M3(x[t,i] / s_t)                        round to nearest even
+//   lo[t,i]  = E4M3(16 * (x[t,i] / s_t - hi[t,i]))       round to nearest even
+//   x[t,i]   = s_t * (hi[t,i] + lo[t,i] / 16)
+// A bf16 value has 8 significant bits: hi keeps the top four (rounded) and
+// the remainder, at most half an E4M3 step, is a signed 4-bit multiple of
+// x's own last bit, which lo holds exactly while hi is a normal E4M3 value.
+// Dividing by a power of two is exact, and so are the subtraction and the
+// scaling by 16 in fp32.  Codes [rows, 2, d]: row t's hi codes then its lo
+// codes, so the pair is rows 2t and 2t+1 of a [2*rows, d] byte matrix.
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+  const __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)code, __NV_E4M3);
+  return __half2float(__half(h));
+}
+
+template <bool F16>
+__global__ void __launch_bounds__(kQThreads) split_rows_e4m3x2_kernel(const uint4* __restrict__ x, int rows,
+                                                                      int vpr, uint2* __restrict__ codes,
+                                                                      float* __restrict__ scales) {
+  griddep_begin();
+  __shared__ float red[kQThreads / 32];
+  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+    const uint4* xr = x + (size_t)r * vpr;
+    float m = 0.f;
+    for (int v = threadIdx.x; v < vpr; v += kQThreads) {
+      const uint4 q = xr[v];
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) m = fmaxf(m, fmaxf(fabsf(lo16<F16>(w[i])), fabsf(hi16<F16>(w[i]))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    float amax = red[0];
+#pragma unroll
+    for (int i = 1; i < kQThreads / 32; ++i) amax = fmaxf(amax, red[i]);
+    // amax = f * 2^e with f in [0.5, 1): p = e - 9 puts amax / 2^p in
+    // [256, 448] when f <= 0.875, else p = e - 8 puts it in (224, 256)
+    int e = 0;
+    const float f = frexpf(amax, &e);
+    const int p = amax > 0.f ? (f <= 0.875f ? e - 9 : e - 8) : 0;
+    // x / 2^p as two exact power-of-two factors (each within fp32's range)
+    const float inv_a = ldexpf(1.f, -(p / 2)), inv_b = ldexpf(1.f, -(p - p / 2));
+    if (threadIdx.x == 0) scales[r] = ldexpf(1.f, p);
+    uint2* hr = codes + (size_t)(2 * r) * vpr;
+    uint2* lr = hr + vpr;
+    for (int v = threadIdx.x; v < vpr; v += kQThreads) {
+      const uint4 q = xr[v];
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+      uint32_t ch[4], cl[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float a = lo16<F16>(w[i]) * inv_a * inv_b, b = hi16<F16>(w[i]) * inv_a * inv_b;
+        ch[i] = e4m3x2(a, b);
+        const float ra = 16.f * (a - e4m3_value(ch[i] & 0xffu)), rb = 16.f * (b - e4m3_value(ch[i] >> 8));
+        cl[i] = e4m3x2(ra, rb);
+      }
+      hr[v] = make_uint2(ch[0] | (ch[1] << 16), ch[2] | (ch[3] << 16));
+      lr[v] = make_uint2(cl[0] | (cl[1] << 16), cl[2] | (cl[3] << 16));
+    }
+    __syncthreads();  // red[] is rewritten by the next row
+  }
+}
+
 }  // namespace
+
+moe_status split_rows_e4m3x2_launch(const void* x, int rows, int d, void* codes, float* scales, int num_sms,
+                                    cudaStream_t s, bool f16_in) {
+  if (rows == 0) return MOE_OK;
+  if (rows < 0 || d <= 0 || d % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  const int blocks = rows < 16 * num_sms ? rows : 16 * num_sms;
+  if (f16_in)
+    MOE_TRY_CUDA(launch_k(split_rows_e4m3x2_kernel<true>, dim3(blocks), dim3(kQThreads), 0, s,
+                          static_cast<const uint4*>(x), rows, d / 8, static_cast<uint2*>(codes), scales));
+  else
+    MOE_TRY_CUDA(launch_k(split_rows_e4m3x2_kernel<false>, dim3(blocks), dim3(kQThreads), 0, s,
+                          static_cast<const uint4*>(x), rows, d / 8, static_cast<uint2*>(codes), scales));
+  MOE_TRY_CUDA(cudaGetLastError());
+  return MOE_OK;
+}
 
 moe_status quantize_rows_e4m3_launch(const void* x, int rows, int d, void* codes, float* scales,
                                      int num_sms, cudaStream_t s, bool f16_in) {

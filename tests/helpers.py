@@ -88,6 +88,70 @@ class _Lazy:
         return self.shape[0]
 
 
+class PrefetchedExperts:
+    """``expert_hook`` for the oracle's grouped formulation: decodes, in worker
+    threads and ahead of the grouped loop, the experts that loop will visit
+    (``experts``: ascending ids of the experts holding rows), each through the
+    oracle's own ``ExpertWeights.get``; at most ``ahead`` decoded experts are
+    held at once.  Decoding is most of the oracle's time on the large
+    FP8 / MXFP4 layers, and numpy runs it outside the interpreter lock."""
+
+    def __init__(self, ew, experts, workers=8, ahead=12):
+        from concurrent.futures import ThreadPoolExecutor
+        self.ew = ew
+        self.order = [int(e) for e in experts]
+        self.pool = ThreadPoolExecutor(max_workers=workers)
+        self.futures = {e: self.pool.submit(ew.get, e) for e in self.order[:ahead]}
+        self.next = min(ahead, len(self.order))
+
+    def __call__(self, e):
+        f = self.futures.pop(int(e), None)
+        w = f.result() if f is not None else self.ew.get(int(e))
+        if self.next < len(self.order):
+            n = self.order[self.next]
+            self.next += 1
+            self.futures[n] = self.pool.submit(self.ew.get, n)
+        return w
+
+    def close(self):
+        self.pool.shutdown(wait=True, cancel_futures=True)
+
+
+def check_routing_within_tie_band(logits, k, idx, w, band):
+    """Routing check for every token, given the oracle's float64 logits and a
+    device whose logits may differ from them by up to band / 2 each:
+      * the device's k experts are distinct;
+      * every expert whose logit exceeds the (k+1)-th largest by more than
+        band is among them (no device rounding can drop it);
+      * every expert among them is within band of the k-th largest logit
+        (no device rounding can raise anything lower into the top k);
+      * the weights are the softmax of the oracle's logits over the device's
+        set, renormalised (rtol 1e-4: the logit differences enter the
+        exponent), slots in non-increasing weight.
+    Tokens whose k-th and (k+1)-th logits are further apart than band get
+    exactly the oracle's set this way; near-tie tokens get one of the sets
+    that are valid under the logit error."""
+    logits = np.asarray(logits, np.float64)
+    idx = np.asarray(idx)
+    w = np.asarray(w, np.float64)
+    T, E = logits.shape
+    srt = -np.sort(-logits, axis=1)
+    kth = srt[:, k - 1]
+    k1 = srt[:, k] if k < E else np.full(T, -np.inf)
+    for t in range(T):
+        chosen = idx[t]
+        assert len(set(chosen.tolist())) == k, f"token {t}: repeated experts {chosen}"
+        assert np.all((chosen >= 0) & (chosen < E)), f"token {t}: expert out of range"
+        must = np.nonzero(logits[t] > k1[t] + band)[0]
+        missing = set(must.tolist()) - set(chosen.tolist())
+        assert not missing, f"token {t}: experts {sorted(missing)} clearly in the top {k} are missing"
+        assert np.all(logits[t, chosen] >= kth[t] - band), f"token {t}: an expert below the top-{k} band"
+        z = logits[t, chosen] - logits[t, chosen].max()
+        ref = np.exp(z) / np.exp(z).sum()
+        np.testing.assert_allclose(w[t], ref, rtol=1e-4, atol=1e-6, err_msg=f"token {t}: weights")
+        assert np.all(np.diff(w[t]) <= 1e-6), f"token {t}: slots not in descending weight"
+
+
 def routing_gap_ok(logits, k, min_gap):
     return bool(np.all(oracle.topk_gap(logits, k) >= min_gap))
 

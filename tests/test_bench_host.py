@@ -40,14 +40,15 @@ def test_fp8_scales_and_fp8_rows_enter_the_bytes():
     b_fp8, _ = bench.stage_work(base, touched=4, splits=1)["gate_up"]
     b_a8, _ = bench.stage_work(a8, touched=4, splits=1)["gate_up"]
     # same weights and per-channel scales; the rows are E4M3 codes + one
-    # fp32 scale each instead of bf16
+    # fp32 scale each (FP8 activations) instead of two E4M3 rows + a scale
+    # (FP8 weights on bf16 rows)
     R, d = 8, 256
-    assert b_fp8 - b_a8 == R * d * 2 - R * (d + 4)
-    # and the down GEMM reads h's E4M3 codes and row scales instead of f16 h
+    assert b_fp8 - b_a8 == R * (2 * d + 4) - R * (d + 4)
+    # and the down GEMM reads h's E4M3 codes, one row or two, and row scales
     d_fp8, _ = bench.stage_work(base, touched=4, splits=1)["down"]
     d_a8, _ = bench.stage_work(a8, touched=4, splits=1)["down"]
     f = 128
-    assert d_fp8 - d_a8 == R * f * 2 - R * (f + 4)
+    assert d_fp8 - d_a8 == R * (2 * f + 4) - R * (f + 4)
 
 
 def test_expected_touched_closed_form():

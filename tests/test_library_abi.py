@@ -58,7 +58,7 @@ def test_binding_arity_matches_header():
 
 
 def test_abi_version_and_status_strings(lib):
-    assert api.moe_abi_version() == 4
+    assert api.moe_abi_version() == 5
     assert api.moe_status_string(0) == "MOE_OK"
     assert api.moe_status_string(api.ERR_DEVICE_TIMEOUT) == "MOE_ERR_DEVICE_TIMEOUT"
     assert api.moe_status_string(-99) == "MOE_ERR_UNKNOWN"
@@ -126,6 +126,19 @@ def test_quantize_rows_arguments_checked_before_any_launch(lib):
     assert q(4, 128, fake, None, fake, None) == api.ERR_INVALID_ARG         # null codes
     assert q(4, 128, fake, fake, None, None) == api.ERR_INVALID_ARG         # null scales
     assert q(4, 128, ctypes.c_void_p(0x1008), fake, fake, None) == api.ERR_INVALID_ARG  # misaligned
+    assert q(0, 128, None, None, None, None) == 0                            # empty: no launch
+
+
+def test_split_rows_arguments_checked_before_any_launch(lib):
+    fake = ctypes.c_void_p(0x1000)  # never dereferenced: rejected on the host
+    q = lib.moe_split_rows_e4m3x2
+    assert q(-1, 128, fake, fake, fake, None) == api.ERR_INVALID_ARG        # negative rows
+    assert q(4, 12, fake, fake, fake, None) == api.ERR_UNSUPPORTED          # cols % 8
+    assert q(4, 0, fake, fake, fake, None) == api.ERR_UNSUPPORTED           # no columns
+    assert q(4, 128, None, fake, fake, None) == api.ERR_INVALID_ARG         # null input
+    assert q(4, 128, fake, None, fake, None) == api.ERR_INVALID_ARG         # null codes
+    assert q(4, 128, fake, fake, None, None) == api.ERR_INVALID_ARG         # null scales
+    assert q(4, 128, fake, ctypes.c_void_p(0x1008), fake, None) == api.ERR_INVALID_ARG  # misaligned codes
     assert q(0, 128, None, None, None, None) == 0                            # empty: no launch
 
 

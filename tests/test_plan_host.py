@@ -75,7 +75,9 @@ def test_tile_rows_follow_the_rows_per_expert(name, T, wfmt):
         assert pl["pair_gateup"] == 0
         assert pl["pair_down"] == (1 if wfmt == "bf16" and s.d % 256 == 0 else 0)
     if mean >= 128:  # prefill: whole 256-row tiles, K unsplit, CTA pairs
-        assert pl["bn_down"] == 256
+        # FP8 weights on two-term rows take two accumulator columns per row:
+        # 128-row tiles (256 columns) in both GEMMs
+        assert pl["bn_down"] == (128 if wfmt == "fp8" else 256)
         # weights converted to f16 in tensor memory keep 128-row gate/up tiles
         assert pl["bn_gateup"] == (128 if wfmt in ("fp8", "mxfp4") else 256)
         assert pl["splits_gateup"] == pl["splits_down"] == 1
@@ -107,9 +109,10 @@ def test_splits_only_when_the_units_leave_the_sms_idle():
 @pytest.mark.parametrize("T", [1, 64, 4096])
 def test_launch_count_per_weight_mode(T):
     n = {w: api.moe_layer_launch_count_for(api.problem_of(_shape("deepseek_v3", T, w)), SMS) for w in FORMATS}
-    # FP8 and MXFP4 weights: one more pass (x to f16 for the converted
-    # operands); FP8 activations: two (x's and h's per-row E4M3 codes)
-    assert n["fp8"] == n["bf16"] + 1
+    # MXFP4 weights: one more pass (x to f16 for the converted operands);
+    # FP8 weights: two (x's and h's two-term E4M3 rows); FP8 activations:
+    # two (x's and h's per-row E4M3 codes)
+    assert n["fp8"] == n["bf16"] + 2
     assert n["mxfp4"] == n["bf16"] + 1
     assert n["fp8a8"] == n["bf16"] + 2
 
