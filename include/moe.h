@@ -47,9 +47,10 @@
  *                               The bf16 rows (tokens, then h) enter the
  *                               FP8 x FP8 tensor-core instructions as two
  *                               E4M3 rows each (moe_split_rows_e4m3x2),
- *                               an exact re-encoding of the bf16 values:
+ *                               the bf16 values themselves for elements
+ *                               within 2^9 of their row's maximum:
  *                               g[r,o] = s_gate[e,o] * s_x[r] *
- *                                 sum_i (hi[r,i] + lo[r,i]/16) code_gate[e][o,i]
+ *                                 sum_i (hi[r,i] + lo[r,i]) code_gate[e][o,i]
  *                               (likewise u); h = SiLU(g) * u held in bf16,
  *                               split the same way before the down product.
  *                               Any finite bf16 magnitude is accepted.
@@ -277,16 +278,19 @@ MOE_API moe_status moe_quantize_rows_e4m3(int32_t rows, int32_t cols, const void
  *   s[r]         = 2^p, p the integer with max_i |x[r,i]| / 2^p in
  *                  (224, 448]; 1 when row r is all zero
  *   hi[r,i]      = E4M3(x[r,i] / s[r])
- *   lo[r,i]      = E4M3(16 * (x[r,i] / s[r] - hi[r,i]))
+ *   lo[r,i]      = E4M3(x[r,i] / s[r] - hi[r,i])
  * (nearest E4M3 value, ties to the even code).  Then
- *   x[r,i] = s[r] * (hi[r,i] + lo[r,i] / 16)
- * exactly for every element with |x[r,i]| >= max_i |x[r,i]| * 2^-13, and
- * within s[r] * 2^-14 for smaller ones: a bf16 value has 8 significant
- * bits, hi holds the top four (rounded) and lo the signed remainder.
+ *   x[r,i] = s[r] * (hi[r,i] + lo[r,i])
+ * exactly for every element with |x[r,i]| >= max_i |x[r,i]| * 2^-9, and
+ * within s[r] * 2^-10 for smaller ones: a bf16 value has 8 significant
+ * bits, hi holds the top four (rounded) and lo the signed remainder, which
+ * E4M3 holds exactly down to its smallest step.  An FP8 x FP8 product on
+ * hi plus one on lo, accumulated together, multiplies by the bf16 row.
  *
  *   x       [rows, cols] bf16, device, 16-byte aligned
- *   codes   [rows, 2, cols] uint8 out: row r's hi codes, then its lo codes
- *           (rows 2r and 2r+1 of a [2*rows, cols] matrix), 16-byte aligned
+ *   codes   [2, rows, cols] uint8 out: every row's hi codes, then every
+ *           row's lo codes (row r's lo codes are row rows + r of a
+ *           [2*rows, cols] matrix), 16-byte aligned
  *   scales  [rows] fp32 out (powers of two)
  * rows >= 0 (0: nothing is enqueued); cols > 0 and cols % 8 == 0, else
  * MOE_ERR_UNSUPPORTED.  Null pointers with rows > 0: MOE_ERR_INVALID_ARG.

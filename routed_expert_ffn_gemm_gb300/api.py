@@ -260,8 +260,8 @@ def moe_quantize_rows_e4m3(x, codes, scales, stream=None):
 
 def moe_split_rows_e4m3x2(x, codes, scales, stream=None):
     """bf16 rows x [rows, cols] as two E4M3 rows each: codes uint8
-    [rows, 2, cols] (hi, then lo) and power-of-two fp32 scales [rows], with
-    x = s * (hi + lo / 16)."""
+    [2, rows, cols] (every row's hi codes, then every row's lo codes) and
+    power-of-two fp32 scales [rows], with x = s * (hi + lo)."""
     rows, cols = (int(v) for v in x.shape)
     _check(x, "x", rows * cols, 2)
     _check(codes, "codes", 2 * rows * cols, 1)

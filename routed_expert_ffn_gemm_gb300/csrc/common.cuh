@@ -215,9 +215,10 @@ moe_status bf16_to_f16_launch(const void* src, void* dst, size_t n, cudaStream_t
 moe_status quantize_rows_e4m3_launch(const void* x, int rows, int d, void* codes, float* scales,
                                      int num_sms, cudaStream_t s, bool f16_in = false);
 // Two-term E4M3 encoding of 16-bit rows (bf16, or f16 with f16_in): codes
-// [rows, 2, d] (hi row, then lo row) and power-of-two scales [rows] with
-// x = s * (hi + lo / 16), exact for elements within 2^13 of the row's
-// largest magnitude: the operands of FP8-weight GEMMs on bf16 activations.
+// [2, rows, d] (every row's hi codes, then every row's lo codes) and
+// power-of-two scales [rows] with x = s * (hi + lo), exact for elements
+// within 2^9 of the row's largest magnitude: the operands of FP8-weight
+// GEMMs on bf16 activations.
 moe_status split_rows_e4m3x2_launch(const void* x, int rows, int d, void* codes, float* scales, int num_sms,
                                     cudaStream_t s, bool f16_in = false);
 

@@ -45,13 +45,14 @@
 // FP8 weights with bf16 activations ("MoE 推理部署", section 专家量化:
 // per-expert scales): every bf16 row (token rows, rows of h) arrives as two
 // E4M3 rows, hi and lo, with one power-of-two scale s per row and
-// x = s * (hi + lo / 16) -- an exact re-encoding of the bf16 values (see
-// the row split in quantize.cu).  Both operands then go straight from the
-// TMA ring to tcgen05.mma kind::f8f6f4; a tile of n rows is an MMA of 2n
-// columns (hi and lo of row j in columns 2j and 2j+1), and the epilogue
-// forms s * (acc[2j] + acc[2j+1] / 16) times the output channel's scale.
-// The products of E4M3 weights and E4M3 terms are exact, so this computes
-// what a 16-bit MMA on the bf16 rows would, with no weight conversion.
+// x = s * (hi + lo) -- the bf16 values themselves for every element within
+// 2^9 of its row's largest magnitude (see the row split in quantize.cu).
+// Both operands go straight from the TMA ring to tcgen05.mma kind::f8f6f4:
+// each K step issues the MMA on the hi rows, then on the lo rows into the
+// same accumulator, so one accumulator column per row holds W (hi + lo),
+// and the epilogue multiplies it by s and the output channel's scale.  The
+// products of E4M3 weights and E4M3 terms are exact, so this computes what
+// a 16-bit MMA on the bf16 rows would, with no weight conversion.
 // (The E4M3 -> f16 converter path below remains for MXFP4 weights, and for
 // FP8 weights when MOE_FP8_CONVERT=1 selects it.)
 //
@@ -122,6 +123,9 @@ struct TcParams {
   int lsu_gather;
   const void* x_src;
   int d_src;  // row length of x_src (elements)
+  // two-term rows: rows between a row's hi codes and its lo codes in the B
+  // matrix (the planes [2, rows, K] of the row split)
+  int b_plane;
   // FP8 activations (gate/up): per-row quantisation scales of the B rows,
   // indexed by token (gather_rows) or by row
   const float* row_scale;
@@ -151,7 +155,7 @@ struct Cfg {
   // E4M3 weights times E4M3 rows (kind::f8f6f4): FP8 activations, or the
   // two-term rows
   static constexpr bool A8 = WF == kWFp8Act8 || X2;
-  static constexpr int RM = X2 ? 2 : 1;         // B rows (accumulator columns) per row of the tile
+  static constexpr int NB = X2 ? 2 : 1;         // B tiles per stage: the hi rows, then the lo rows
   static constexpr bool H16 = FP8 && !X2;       // h stored in f16 (else bf16)
   static constexpr bool MX4 = WF == kWMx4;      // MXFP4 weights (block scales applied by the converters)
   static constexpr bool CHS = FP8 && !MX4;      // per-output-channel weight scales in the epilogue
@@ -181,8 +185,8 @@ struct Cfg {
   static constexpr int NSUB = A8 ? 1 : KB / kBK;               // 128-byte B sub-tiles per stage
   static constexpr int KSTEP = A8 ? 32 : 16;                   // K per MMA instruction
   static constexpr int A_BYTES = kBM * kBK * 2;                // 16 KB bf16 tile (MMA operand)
-  static constexpr int BSUB_BYTES = RM * (PAIR ? BN / 2 : BN) * kBK * 2;
-  static constexpr int B_BYTES = NSUB * BSUB_BYTES;
+  static constexpr int BSUB_BYTES = (PAIR ? BN / 2 : BN) * kBK * 2;
+  static constexpr int B_BYTES = NB * NSUB * BSUB_BYTES;
   // staged weight codes: E4M3 (8 or 16 KB), or packed E2M1 (half that)
   // followed by the UE8M0 block scales, KB/32 runs of 128 bytes
   static constexpr int STG_BYTES = FP8 ? (MX4 ? kBM * KB / 2 : kBM * KB) : 0;
@@ -200,7 +204,7 @@ struct Cfg {
   static constexpr int AVAIL_ = kSmemLimit - 1024 - (8 * 40 + 16 + 4 * 2 * (kMaxGroups + 8));
   // TMEM: one accumulator buffer = NA accumulators of max(BN,128) columns;
   // two buffers when they fit beside the operand slots of the TA path
-  static constexpr int UP_OFF = RM * BN > 128 ? RM * BN : 128;
+  static constexpr int UP_OFF = BN > 128 ? BN : 128;
   static constexpr int ACC_COLS = NA * UP_OFF;
   static constexpr bool TA_DECODE = TA && BN == 32;
   static constexpr int NBUF = TA && !TA_DECODE ? (2 * ACC_COLS + 2 * 64 * NA <= 512 ? 2 : 1)
@@ -241,7 +245,7 @@ struct Cfg {
   // their 1 KB reservations overflow the SM's 228 KB.
   static_assert(2 * (SMEM_BYTES + 1024) > kSmemLimit + 1024, "one TMEM-holding CTA per SM");
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
-  static_assert(BN % 16 == 0 && RM * BN <= 256 && ACC_COLS <= 512, "tile rows");
+  static_assert(BN % 16 == 0 && BN <= 256 && ACC_COLS <= 512, "tile rows");
   static_assert(!PAIR || BN >= 32, "pair tiles split B rows in halves");
   static_assert(!TA || (OSTAGES >= 2 && (TA_DECODE ? UP_OFF == 128 && ACC_COLS * NBUF <= 512 && OSTAGES * NA <= 4
                                                   : NBUF * ACC_COLS + OSTAGES * NA * 64 <= 512)),
@@ -505,11 +509,12 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
         // the tile's MMA width rounded to 32
         const int bhalf = PAIR ? ((x.n_valid + 31) / 32) * 16 : x.n_valid;
         const int brow0 = x.row0 + (int)rank * bhalf;
-        // (B rows of the operand: RM per row of the tile, the row's RM
-        // consecutive rows RM * row .. RM * row + RM - 1 of the B matrix)
-        const int nbox = (C::RM * bhalf + p.boxn - 1) / p.boxn;
-        const int nops = (C::RM * x.n_valid + 3) / 4;  // gather4 copies of this tile
-        // this lane's gather rows: ops lane and lane + 32 (RM * BN <= 256);
+        const int nbox = (bhalf + p.boxn - 1) / p.boxn;
+        // gather4 copies of this tile: nops per B term (the hi rows, then,
+        // two-term rows, the lo rows: rows of the lo plane, p.b_plane rows
+        // further down the B matrix)
+        const int nops = (x.n_valid + 3) / 4;
+        // this lane's gather rows: ops lane and lane + 32 (NB * BN <= 256);
         // rows past the group's end repeat its first row (their columns are
         // unused)
         int gr[2][4];
@@ -517,24 +522,22 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
         for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const int i = 4 * (lane + 32 * h) + q, li = i / C::RM;
-            gr[h][q] = (gather && lane + 32 * h < nops)
-                           ? C::RM * p.gather_rows[x.row0 + (li < x.n_valid ? li : 0)] + i % C::RM
+            const int op = lane + 32 * h, term = op >= nops ? 1 : 0, i = 4 * (op - term * nops) + q;
+            gr[h][q] = (gather && op < C::NB * nops)
+                           ? p.gather_rows[x.row0 + (i < x.n_valid ? i : 0)] + term * p.b_plane
                            : 0;
           }
-        // gathered rows (lsu): this lane's B rows lane + 32 i of the CTA,
-        // their source rows in x_src (-1: past the group's end, not copied)
-        constexpr int CROWS = C::RM * (PAIR ? BN / 2 : BN);
-        constexpr int RPL = CROWS / 32 > 0 ? CROWS / 32 : 1;
+        // gathered rows (lsu): this lane's rows lane + 32 i of the CTA's
+        // B rows, their token ids (-1: past the group's end, not copied)
+        constexpr int RPL = (PAIR ? BN / 2 : BN) / 32 > 0 ? (PAIR ? BN / 2 : BN) / 32 : 1;
         int tok[RPL];
 #pragma unroll
         for (int i = 0; i < RPL; ++i) {
-          const int rr = lane + 32 * i, r = brow0 + rr / C::RM;
-          tok[i] = (lsu && rr < C::RM * bhalf && r < x.row0 + x.n_valid) ? C::RM * p.gather_rows[r] + rr % C::RM
-                                                                           : -1;
+          const int r = brow0 + lane + 32 * i;
+          tok[i] = (lsu && lane + 32 * i < bhalf && r < x.row0 + x.n_valid) ? p.gather_rows[r] : -1;
         }
         const uint32_t bbytes =
-            lsu ? 0u : C::NSUB * (gather ? (uint32_t)nops * 4 * kBK * 2 : (uint32_t)nbox * p.boxn * kBK * 2);
+            lsu ? 0u : C::NB * C::NSUB * (gather ? (uint32_t)nops * 4 * kBK * 2 : (uint32_t)nbox * p.boxn * kBK * 2);
         const uint32_t bytes = C::NA * C::W_BYTES + bbytes;
         const int arow = x.g * p.M + x.mt * C::CH + (int)rank * kBM;
         for (int kb = kb0; kb < kb1; ++kb) {
@@ -556,7 +559,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
               const uint32_t fb = lead(full_bar(stage));
               ptx::mbar_arrive_expect_tx_cluster(fb, bytes);
               ptx::tma_load_3d_pair(sa, &tmA0, fb, arow, kb * 2, pol_w);
-              ptx::tma_load_3d_pair(sb, &tmB, fb, C::RM * brow0, kb * 2, pol_x);
+              ptx::tma_load_3d_pair(sb, &tmB, fb, brow0, kb * 2, pol_x);
             } else if (PAIR && !CONV) {
               // both CTAs' copies complete the even CTA's barrier
               const uint32_t fb = lead(full_bar(stage));
@@ -564,9 +567,11 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
               ptx::tma_load_2d_pair(sa, &tmA0, fb, kb * C::KB, arow, pol_w);
               if (MODE == kGateUp) ptx::tma_load_2d_pair(sa + C::W_BYTES, &tmA1, fb, kb * C::KB, arow, pol_w);
               if (!lsu)
-                for (int i = 0; i < nbox; ++i)
-                  ptx::tma_load_2d_pair(sb + i * p.boxn * kBK * 2, &tmB, fb, kb * C::KB,
-                                        C::RM * brow0 + i * p.boxn, pol_x);
+#pragma unroll
+                for (int term = 0; term < C::NB; ++term)
+                  for (int i = 0; i < nbox; ++i)
+                    ptx::tma_load_2d_pair(sb + term * C::BSUB_BYTES + i * p.boxn * kBK * 2, &tmB, fb, kb * C::KB,
+                                          brow0 + term * p.b_plane + i * p.boxn, pol_x);
             } else {
               ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
               // weight codes (MXFP4: two per byte), then (MXFP4) the
@@ -583,32 +588,35 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
               }
               if (!gather && !lsu)
 #pragma unroll
-                for (int sub = 0; sub < C::NSUB; ++sub)
-                  for (int i = 0; i < nbox; ++i)
-                    ptx::tma_load_2d(sb + sub * C::BSUB_BYTES + i * p.boxn * kBK * 2, &tmB, full_bar(stage),
-                                     kb * C::KB + sub * kBK, C::RM * brow0 + i * p.boxn, pol_x);
+                for (int term = 0; term < C::NB; ++term)
+#pragma unroll
+                  for (int sub = 0; sub < C::NSUB; ++sub)
+                    for (int i = 0; i < nbox; ++i)
+                      ptx::tma_load_2d(sb + (term * C::NSUB + sub) * C::BSUB_BYTES + i * p.boxn * kBK * 2, &tmB,
+                                       full_bar(stage), kb * C::KB + sub * kBK,
+                                       brow0 + term * p.b_plane + i * p.boxn, pol_x);
             }
           }
           if (lsu) {
-            // eight lanes per row, one 16-byte chunk each: a warp-wide copy
-            // moves four rows' whole 128-byte K slices (per 64-element
-            // sub-tile), so every 32-byte sector is fetched once; chunk c of
-            // row r lands at chunk c ^ (r % 8).  Row 32 i + j's source is
-            // lane j's tok[i].  Then one arrival per lane once its copies
-            // have landed.
-            const int q = lane >> 3, c = lane & 7;
+            // one lane per row: its rows' 128-byte K slices (per 64-element
+            // sub-tile), chunk c of row r at chunk c ^ (r % 8); then one
+            // arrival per lane once its copies have landed.  (Eight lanes per
+            // row, one 16-byte chunk each, so that a warp-wide copy moves
+            // four whole row slices, measured five times slower.)
 #pragma unroll
             for (int i = 0; i < RPL; ++i) {
+              if (tok[i] < 0) continue;
+              const int r = lane + 32 * i;
 #pragma unroll
-              for (int g = 0; g < 8; ++g) {
-                const int t = __shfl_sync(0xffffffffu, tok[i], 4 * g + q);
-                if (t < 0) continue;
-                const int r = 32 * i + 4 * g + q;
+              for (int term = 0; term < C::NB; ++term)
 #pragma unroll
-                for (int sub = 0; sub < C::NSUB; ++sub)
-                  ptx::cp_async16(sb + sub * C::BSUB_BYTES + r * 128 + ((c ^ (r & 7)) << 4),
-                                  xs + ((size_t)t * p.d_src + (size_t)kb * C::KB + sub * kBK) * kEsz + 16 * c);
-              }
+                for (int sub = 0; sub < C::NSUB; ++sub) {
+                  const uint8_t* src = xs + ((size_t)(tok[i] + term * p.b_plane) * p.d_src + (size_t)kb * C::KB +
+                                             sub * kBK) * kEsz;
+                  const uint32_t dst = sb + (term * C::NSUB + sub) * C::BSUB_BYTES + r * 128;
+#pragma unroll
+                  for (int c = 0; c < 8; ++c) ptx::cp_async16(dst + ((c ^ (r & 7)) << 4), src + 16 * c);
+                }
             }
             ptx::cp_async_arrive_noinc(relay ? bfull_bar(stage) : full_bar(stage));
           }
@@ -617,11 +625,13 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const int op = lane + 32 * h;
-              if (op < nops)
+              const int term = op >= nops ? 1 : 0;
+              if (op < C::NB * nops)
 #pragma unroll
                 for (int sub = 0; sub < C::NSUB; ++sub)
-                  ptx::tma_gather4_2d(sb + sub * C::BSUB_BYTES + op * 4 * kBK * 2, &tmB, full_bar(stage),
-                                      kb * C::KB + sub * kBK, gr[h][0], gr[h][1], gr[h][2], gr[h][3], pol_x);
+                  ptx::tma_gather4_2d(sb + (term * C::NSUB + sub) * C::BSUB_BYTES + (op - term * nops) * 4 * kBK * 2,
+                                      &tmB, full_bar(stage), kb * C::KB + sub * kBK, gr[h][0], gr[h][1], gr[h][2],
+                                      gr[h][3], pol_x);
             }
           }
           if (++stage == STAGES) {
@@ -681,7 +691,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
             break;
           }
           ptx::tc_fence_after();
-          const int n_mma = C::RM * (PAIR ? ((x.n_valid + 31) / 32) * 32 : ((x.n_valid + 15) / 16) * 16);
+          const int n_mma = PAIR ? ((x.n_valid + 31) / 32) * 32 : ((x.n_valid + 15) / 16) * 16;
           // (kind::f8f6f4 takes the same descriptor bits: E4M3 is format 0)
           const uint32_t idesc = FP8 ? ptx::idesc_f16_f32(C::CH, n_mma) : ptx::idesc_bf16_f32(C::CH, n_mma);
           const uint32_t d0 = tmem_base + (uint32_t)(C::ACC_COLS * buf);
@@ -718,13 +728,20 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
                   if (MODE == kGateUp) ptx::mma_f16_ta(d1, at + C::ta_col(ostage, 1), db, idesc, acc);
                 }
               } else if (A8) {
-                // E4M3 x E4M3: K = 32 per instruction, 32 bytes per step
-                if (PAIR) {
-                  ptx::mma_f8_pair(d0, da0 + ka, db, idesc, acc);
-                  if (MODE == kGateUp) ptx::mma_f8_pair(d1, da1 + ka, db, idesc, acc);
-                } else {
-                  ptx::mma_f8(d0, da0 + ka, db, idesc, acc);
-                  if (MODE == kGateUp) ptx::mma_f8(d1, da1 + ka, db, idesc, acc);
+                // E4M3 x E4M3: K = 32 per instruction, 32 bytes per step;
+                // two-term rows: the hi tile, then the lo tile into the same
+                // accumulator
+#pragma unroll
+                for (int term = 0; term < C::NB; ++term) {
+                  const uint64_t dbt = db + (uint64_t)(term * (C::BSUB_BYTES >> 4));
+                  const uint32_t at = term > 0 ? 1u : acc;
+                  if (PAIR) {
+                    ptx::mma_f8_pair(d0, da0 + ka, dbt, idesc, at);
+                    if (MODE == kGateUp) ptx::mma_f8_pair(d1, da1 + ka, dbt, idesc, at);
+                  } else {
+                    ptx::mma_f8(d0, da0 + ka, dbt, idesc, at);
+                    if (MODE == kGateUp) ptx::mma_f8(d1, da1 + ka, dbt, idesc, at);
+                  }
                 }
               } else if (PAIR) {
                 ptx::mma_f16_pair(d0, da0 + ka, db, idesc, acc);
@@ -811,8 +828,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(C::ACC_COLS * buf);
       const int ch = x.mt * C::CH + (int)rank * kBM + ch_local;
       const bool empty_k = x.ks * kb_per_split >= kblocks;
-      // accumulator columns holding the tile's rows (RM per row)
-      const int n_mma = C::RM * (((x.n_valid + 15) / 16) * 16);
+      const int n_mma = ((x.n_valid + 15) / 16) * 16;
       const float sc0 = C::CHS ? p.scale0[(size_t)x.g * p.M + ch] : 1.f;
       const float sc1 = C::CHS && MODE == kGateUp ? p.scale1[(size_t)x.g * p.M + ch] : 1.f;
       // CW accumulator columns per TMEM wait: 32 for the projection (its
@@ -842,18 +858,12 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
 #pragma unroll
         for (int hlf = 0; hlf < CW / 16; ++hlf) {
           // 16 accumulator columns: rows rb .. rb + NJ - 1 of the tile
-          constexpr int NJ = 16 / C::RM;
-          const int rb = (c0 + 16 * hlf) / C::RM;
+          constexpr int NJ = 16;
+          const int rb = c0 + 16 * hlf;
           const int nj = min(NJ, x.n_valid - rb);
           const uint32_t* a = ra + 16 * hlf;
           const uint32_t* b = rb_ + 16 * hlf;
-          // a row's value: its column, or (two-term rows) hi + lo / 16
-          auto val = [&](const uint32_t* acc, int j) {
-            if constexpr (C::RM == 2)
-              return fmaf(__uint_as_float(acc[2 * j + 1]), 0.0625f, __uint_as_float(acc[2 * j]));
-            else
-              return __uint_as_float(acc[j]);
-          };
+          auto val = [&](const uint32_t* acc, int j) { return __uint_as_float(acc[j]); };
           if (nj > 0) {
             // E4M3 rows: each column (token row, or row of h) carries its
             // row's scale (rows gathered by token: the token's)
@@ -1186,6 +1196,7 @@ moe_status launch_mode(int bn, int wf, bool pair, const TcParams& p, const CUten
     MOE_LAUNCH(256, kWFp8Act8, true);
     MOE_LAUNCH(32, kWFp8X2, true);
     MOE_LAUNCH(128, kWFp8X2, true);
+    MOE_LAUNCH(256, kWFp8X2, true);
     return MOE_ERR_UNSUPPORTED;
   }
   MOE_LAUNCH(32, kWFp8, false);
@@ -1202,6 +1213,7 @@ moe_status launch_mode(int bn, int wf, bool pair, const TcParams& p, const CUten
   MOE_LAUNCH(256, kWFp8Act8, false);
   MOE_LAUNCH(32, kWFp8X2, false);
   MOE_LAUNCH(128, kWFp8X2, false);
+  MOE_LAUNCH(256, kWFp8X2, false);
 #undef MOE_LAUNCH
   return MOE_ERR_UNSUPPORTED;
 }
@@ -1292,16 +1304,16 @@ TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype) {
   const double mean = R / E;
   const double est_max = mean + 3.0 * __builtin_sqrt(mean) + 1.0;
   const int bn = est_max <= 32.0 ? 32 : 128;
-  // Two-term rows (FP8 weights, bf16 activations) take two accumulator
-  // columns per row, so their tiles stop at 128 rows (256 columns).
-  // Converted FP8 weights keep 128-row gate/up tiles: on CTA pairs their
-  // accumulators leave room in TMEM for the f16 weight operand (the TA path)
+  // Converted FP8 weights (and MXFP4) keep 128-row gate/up tiles: on CTA
+  // pairs their accumulators leave room in TMEM for the f16 weight operand
+  // (the TA path).  Two-term rows (FP8 weights, bf16 activations) share one
+  // accumulator column per row and tile like bf16.
   const bool x2 = fp8_two_term(w_dtype);
-  const int bn_gu = (bn == 128 && mean >= 128.0 && w_dtype != MOE_FP8_E4M3 && w_dtype != MOE_MXFP4) ? 256 : bn;
-  const int bn_dn = (bn == 128 && mean >= 128.0 && !x2) ? 256 : bn;
-  auto bn_env = [&](const char* name) { return x2 && env_int(name) == 256 ? 0 : bn_ok(env_int(name)); };
-  pl.bn_gateup = bn_env("MOE_BN_GATEUP") ? env_int("MOE_BN_GATEUP") : bn_gu;
-  pl.bn_down = bn_env("MOE_BN_DOWN") ? env_int("MOE_BN_DOWN") : bn_dn;
+  const bool conv = (w_dtype == MOE_FP8_E4M3 && !x2) || w_dtype == MOE_MXFP4;
+  const int bn_gu = (bn == 128 && mean >= 128.0 && !conv) ? 256 : bn;
+  const int bn_dn = (bn == 128 && mean >= 128.0) ? 256 : bn;
+  pl.bn_gateup = bn_ok(env_int("MOE_BN_GATEUP")) ? env_int("MOE_BN_GATEUP") : bn_gu;
+  pl.bn_down = bn_ok(env_int("MOE_BN_DOWN")) ? env_int("MOE_BN_DOWN") : bn_dn;
   const double touched = E < R ? E : R;
   auto tiles_of = [&](int bn_) {
     const double a = R / bn_;
@@ -1351,7 +1363,7 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
                              cudaEvent_t mid) {
   if (a.R == 0) return MOE_OK;
   const bool x2 = fp8_two_term(a.w_dtype);                     // bf16 rows as two E4M3 rows
-  const int rm = x2 ? 2 : 1;                                   // B rows per row
+  const int nb = x2 ? 2 : 1;                                   // planes of E4M3 rows (hi, lo)
   const bool fa8 = a.w_dtype == MOE_FP8_E4M3_ACT8;             // FP8 activations
   const bool act8 = fa8 || x2;                                 // E4M3 rows, kind::f8f6f4
   const bool mx4 = a.w_dtype == MOE_MXFP4;
@@ -1360,7 +1372,6 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   if (!fp8 && a.w_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   if (fp8 && (a.s_gate == nullptr || a.s_up == nullptr || a.s_down == nullptr)) return MOE_ERR_INVALID_ARG;
   if (act8 && (a.row_scale == nullptr || a.h_q == nullptr || a.h_scale == nullptr)) return MOE_ERR_INVALID_ARG;
-  if (x2 && (plan.bn_gateup > 128 || plan.bn_down > 128)) return MOE_ERR_UNSUPPORTED;
   const int wf_gu = x2 ? kWFp8X2 : fa8 ? kWFp8Act8 : mx4 ? kWMx4 : fp8 ? kWFp8 : kWBf16;
   const int wf_dn = wf_gu;
   if (a.d % kBM != 0 || a.ffn % kBM != 0 || a.G > kMaxGroups) return MOE_ERR_UNSUPPORTED;
@@ -1393,20 +1404,19 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   } else {
     sg = su = sd = wg;
   }
-  // (B rows per box: rm per row of the tile)
-  const int box_gu = rm * boxn_of(plan.bn_gateup, plan.pair_gateup != 0);
-  const int box_dn = rm * boxn_of(plan.bn_down, plan.pair_down != 0);
+  const int box_gu = boxn_of(plan.bn_gateup, plan.pair_gateup != 0);
+  const int box_dn = boxn_of(plan.bn_down, plan.pair_down != 0);
   // gathered token rows: TMA gather4 for decode tiles, cp.async by the
   // producer warp for prefill tiles (gather4 costs a copy per 4 rows)
   const bool lsu = a.gather_rows != nullptr && (plan.bn_gateup >= 128 || plan.pair_gateup);
   if (plan.pair_gateup && a.gather_rows != nullptr && !lsu) return MOE_ERR_UNSUPPORTED;
   // row operand: 128-byte rows, 64 16-bit elements or 128 E4M3 codes
-  // (two-term rows: rm = 2 code rows per row)
+  // (two-term rows: two planes of code rows, hi then lo, one matrix)
   const int xe = act8 ? 1 : 2, xk = act8 ? 2 * kBK : kBK;
   if (a.gather_rows != nullptr)  // token rows by index: one-row boxes for gather4
-    MOE_TRY(make_tmap_2d(&xb, a.x_src, (uint64_t)rm * a.T_src, a.d, xe, 1, xk, 128));
+    MOE_TRY(make_tmap_2d(&xb, a.x_src, (uint64_t)nb * a.T_src, a.d, xe, 1, xk, 128));
   else
-    MOE_TRY(make_tmap_2d(&xb, a.x_perm, (uint64_t)rm * a.R, a.d, xe, box_gu, xk, 128));
+    MOE_TRY(make_tmap_2d(&xb, a.x_perm, (uint64_t)nb * a.R, a.d, xe, box_gu, xk, 128));
   // bf16 down GEMM on pairs: 3-D maps, one copy per operand and stage (its
   // B rows in one box: all BN/2 rows of the CTA)
   const bool k2_dn = !fp8 && plan.pair_down;
@@ -1415,9 +1425,9 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
     MOE_TRY(make_tmap_kpair(&hb, a.h, a.R, a.ffn, 2, plan.bn_down / 2));
   } else {
     MOE_TRY(make_tmap_2d(&wd, a.w_down, (uint64_t)a.G * a.d, wcols_dn, wb, kBM, wk_dn, wsw_dn));
-    // h rows: 16-bit, or their E4M3 codes (rm code rows per row), 128-byte rows
+    // h rows: 16-bit, or their E4M3 codes (two planes for two-term rows), 128-byte rows
     if (act8)
-      MOE_TRY(make_tmap_2d(&hb, a.h_q, (uint64_t)rm * a.R, a.ffn, 1, box_dn, 2 * kBK, 128));
+      MOE_TRY(make_tmap_2d(&hb, a.h_q, (uint64_t)nb * a.R, a.ffn, 1, box_dn, 2 * kBK, 128));
     else
       MOE_TRY(make_tmap_2d(&hb, a.h, a.R, a.ffn, 2, box_dn, kBK, 128));
   }
@@ -1447,6 +1457,7 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   p.lsu_gather = lsu ? 1 : 0;
   p.x_src = a.x_src;
   p.d_src = a.d;
+  p.b_plane = a.gather_rows != nullptr ? a.T_src : a.R;
   p.row_scale = act8 ? a.row_scale : nullptr;
   MOE_TRY(launch_mode<kGateUp>(plan.bn_gateup, wf_gu, plan.pair_gateup != 0, p, wg, wu, xb, sg, su, plan.grid, s));
   p.gather_rows = nullptr;
@@ -1473,6 +1484,7 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
 
   p.M = a.d;
   p.K = a.ffn;
+  p.b_plane = a.R;  // (two-term rows of h: planes [2, R, ffn])
   p.splits = plan.splits_down;
   p.out = a.y;
   p.out_f32 = plan.splits_down > 1 ? 1 : 0;

@@ -77,19 +77,22 @@ __global__ void __launch_bounds__(kQThreads) quantize_rows_e4m3_kernel(const uin
   }
 }
 
-// Two-term E4M3 encoding of bf16 rows, exact for every element within 2^13
-// of its row's largest magnitude (and within s * 2^-14 below that):
+// Two-term E4M3 encoding of bf16 rows: the bf16 values themselves for
+// every element within 2^9 of its row's largest magnitude, and within
+// s * 2^-10 below that:
 //   s_t      = 2^p, p the integer with max_i |x[t,i]| / 2^p in (224, 448]
 //              (1 for an all-zero row)
 //   hi[t,i]  = E4M3(x[t,i] / s_t)                        round to nearest even
-//   lo[t,i]  = E4M3(16 * (x[t,i] / s_t - hi[t,i]))       round to nearest even
-//   x[t,i]   = s_t * (hi[t,i] + lo[t,i] / 16)
-// A bf16 value has 8 significant bits: hi keeps the top four (rounded) and
-// the remainder, at most half an E4M3 step, is a signed 4-bit multiple of
-// x's own last bit, which lo holds exactly while hi is a normal E4M3 value.
-// Dividing by a power of two is exact, and so are the subtraction and the
-// scaling by 16 in fp32.  Codes [rows, 2, d]: row t's hi codes then its lo
-// codes, so the pair is rows 2t and 2t+1 of a [2*rows, d] byte matrix.
+//   lo[t,i]  = E4M3(x[t,i] / s_t - hi[t,i])              round to nearest even
+//   x[t,i]   = s_t * (hi[t,i] + lo[t,i])
+// A bf16 value a = x / s has 8 significant bits: hi keeps the top four
+// (rounded) and the remainder a - hi, at most half of hi's step, is a
+// signed 3-bit multiple of a's own last bit, 2^(e-7) for a in [2^e,
+// 2^(e+1)); E4M3 holds that exactly while 2^(e-7) >= 2^-9, its smallest
+// step, i.e. for a >= 2^-2 (|x| >= s / 4 >= max |x| / 896).  Dividing by a
+// power of two is exact, and so is the subtraction in fp32.  Codes
+// [2, rows, d]: the hi codes of every row, then the lo codes (plane p, row
+// t at row p * rows + t of a [2 * rows, d] byte matrix).
 __device__ __forceinline__ float e4m3_value(uint32_t code) {
   const __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)code, __NV_E4M3);
   return __half2float(__half(h));
@@ -125,8 +128,8 @@ __global__ void __launch_bounds__(kQThreads) split_rows_e4m3x2_kernel(const uint
     // x / 2^p as two exact power-of-two factors (each within fp32's range)
     const float inv_a = ldexpf(1.f, -(p / 2)), inv_b = ldexpf(1.f, -(p - p / 2));
     if (threadIdx.x == 0) scales[r] = ldexpf(1.f, p);
-    uint2* hr = codes + (size_t)(2 * r) * vpr;
-    uint2* lr = hr + vpr;
+    uint2* hr = codes + (size_t)r * vpr;
+    uint2* lr = codes + (size_t)(rows + r) * vpr;
     for (int v = threadIdx.x; v < vpr; v += kQThreads) {
       const uint4 q = xr[v];
       const uint32_t w[4] = {q.x, q.y, q.z, q.w};
@@ -135,7 +138,7 @@ __global__ void __launch_bounds__(kQThreads) split_rows_e4m3x2_kernel(const uint
       for (int i = 0; i < 4; ++i) {
         const float a = lo16<F16>(w[i]) * inv_a * inv_b, b = hi16<F16>(w[i]) * inv_a * inv_b;
         ch[i] = e4m3x2(a, b);
-        const float ra = 16.f * (a - e4m3_value(ch[i] & 0xffu)), rb = 16.f * (b - e4m3_value(ch[i] >> 8));
+        const float ra = a - e4m3_value(ch[i] & 0xffu), rb = b - e4m3_value(ch[i] >> 8);
         cl[i] = e4m3x2(ra, rb);
       }
       hr[v] = make_uint2(ch[0] | (ch[1] << 16), ch[2] | (ch[3] << 16));

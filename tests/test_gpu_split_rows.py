@@ -3,10 +3,10 @@ mode hands bf16 rows to the FP8 x FP8 tensor-core instructions
 ("MoE 推理部署", section 专家量化: FP8 expert weights, activations kept at
 higher precision).  Checked through the C ABI against the encoding's
 definition: s is the power of two that puts the row maximum in (224, 448];
-hi is the nearest E4M3 value of x / s (torch's float8 cast, a library
-rounding, as the pin); lo the nearest E4M3 value of 16 (x / s - hi); and
-s (hi + lo / 16) returns x exactly for every element within 2^13 of its row
-maximum, within s * 2^-14 below that.  Rows span magnitudes from bf16
+hi is the nearest E4M3 value of x / s and lo the nearest E4M3 value of
+x / s - hi (torch's float8 cast, a library rounding, is the pin for both);
+s (hi + lo) returns x exactly for every element within 2^9 of its row
+maximum, and within s * 2^-10 below that.  Rows span magnitudes from bf16
 subnormals to 1e30, with outliers, zeros and signed zeros."""
 
 import numpy as np
@@ -50,11 +50,17 @@ def _rows(rows, cols, seed):
 
 def _split(x):
     rows, cols = x.shape
-    codes = torch.full((rows, 2, cols), 0x7F, dtype=torch.uint8, device=DEV)  # NaN codes until written
+    codes = torch.full((2, rows, cols), 0x7F, dtype=torch.uint8, device=DEV)  # NaN codes until written
     scales = torch.full((rows,), float("nan"), dtype=torch.float32, device=DEV)
     api.moe_split_rows_e4m3x2(x.to(DEV), codes, scales)
     torch.cuda.synchronize()
     return codes.cpu().numpy(), scales.cpu().numpy()
+
+
+def _e4m3(v):
+    """Nearest E4M3 codes of float64 values exact in float32 (torch's cast)."""
+    return torch.from_numpy(np.asarray(v, np.float64).astype(np.float32)).to(torch.float8_e4m3fn) \
+        .view(torch.uint8).numpy()
 
 
 @pytest.mark.parametrize("rows,cols", [(64, 7168), (257, 2048), (3, 8), (1, 128)])
@@ -64,43 +70,36 @@ def test_split_rows_is_the_definition(rows, cols):
     xf = oracle.decode_bf16(inputs.to_numpy_stored(x))
     amax = np.abs(xf).max(axis=1)
     # s: a power of two putting the row maximum in (224, 448]; 1 for zero rows
-    m, e = np.frexp(s.astype(np.float64))
+    m, _ = np.frexp(s.astype(np.float64))
     assert np.all(m == 0.5), "scales are powers of two"
     nz = amax > 0
     assert np.all(s[~nz] == 1.0)
     assert np.all((amax[nz] / s[nz] > 224.0) & (amax[nz] / s[nz] <= 448.0))
-    hi, lo = codes[:, 0, :], codes[:, 1, :]
-    # hi: the nearest E4M3 value of x / s (torch's round-to-nearest-even cast)
-    q = torch.from_numpy((xf / s[:, None].astype(np.float64)).astype(np.float32))
-    want_hi = q.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
-    assert np.array_equal(hi, want_hi)
-    # lo: the nearest E4M3 value of 16 (x / s - hi)
+    hi, lo = codes[0], codes[1]
+    a = xf / s[:, None].astype(np.float64)  # exact: a power-of-two division
+    assert np.array_equal(hi, _e4m3(a))
     hv = oracle.decode_e4m3(hi)
-    r = torch.from_numpy((16.0 * (xf / s[:, None] - hv)).astype(np.float32))
-    assert np.array_equal(lo, r.to(torch.float8_e4m3fn).view(torch.uint8).numpy())
-    # reconstruction: exact within 2^13 of the row maximum, else within s 2^-14
-    back = s[:, None].astype(np.float64) * (hv + oracle.decode_e4m3(lo) / 16.0)
-    big = np.abs(xf) >= amax[:, None] * 2.0 ** -13
+    assert np.array_equal(lo, _e4m3(a - hv))
+    # reconstruction: exact within 2^9 of the row maximum, else within s 2^-10
+    back = s[:, None].astype(np.float64) * (hv + oracle.decode_e4m3(lo))
+    big = np.abs(xf) >= amax[:, None] * 2.0 ** -9
     assert np.array_equal(back[big], xf[big])
-    assert np.all(np.abs(back - xf) <= s[:, None] * 2.0 ** -14)
-    # signed zeros and zeros stay zero (no NaN codes left)
+    assert np.all(np.abs(back - xf) <= s[:, None] * 2.0 ** -10)
     assert not np.any(np.isnan(back))
 
 
 def test_split_rows_of_outlier_tokens():
-    # token rows with a 1e5 outlier beside N(0,1) values (a dynamic range
-    # past 2^13): the outlier and every element within 2^13 of it come back
-    # bit for bit; the N(0,1) elements within s * 2^-14, here 2^8 * 2^-14 =
-    # 1/64, fourteen binades below the outlier's own bf16 step of 2^9
+    # token rows with a 1e5 outlier beside N(0,1) values: the outlier and
+    # every element within 2^9 of it come back bit for bit; the N(0,1)
+    # elements, seventeen binades below it, within s * 2^-10 = 2^8 * 2^-10
     x = torch.randn((16, 4096), generator=torch.Generator().manual_seed(3))
     x[:, 17] = 1e5
     x = x.to(torch.bfloat16)
     codes, s = _split(x)
-    assert np.all(s == 2.0 ** 8)  # 1e5 / 2^8 = 390.6 in (224, 448]
+    assert np.all(s == 2.0 ** 8)  # 99840 / 2^8 = 390 in (224, 448]
     xf = oracle.decode_bf16(inputs.to_numpy_stored(x))
-    back = s[:, None].astype(np.float64) * (oracle.decode_e4m3(codes[:, 0, :]) +
-                                             oracle.decode_e4m3(codes[:, 1, :]) / 16.0)
-    big = np.abs(xf) >= np.abs(xf).max(axis=1, keepdims=True) * 2.0 ** -13
+    back = s[:, None].astype(np.float64) * (oracle.decode_e4m3(codes[0]) + oracle.decode_e4m3(codes[1]))
+    big = np.abs(xf) >= np.abs(xf).max(axis=1, keepdims=True) * 2.0 ** -9
     assert big[:, 17].all()
     assert np.array_equal(back[big], xf[big])
-    assert np.abs(back - xf).max() <= 2.0 ** 8 * 2.0 ** -14
+    assert np.abs(back - xf).max() <= 2.0 ** 8 * 2.0 ** -10

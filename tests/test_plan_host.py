@@ -75,11 +75,10 @@ def test_tile_rows_follow_the_rows_per_expert(name, T, wfmt):
         assert pl["pair_gateup"] == 0
         assert pl["pair_down"] == (1 if wfmt == "bf16" and s.d % 256 == 0 else 0)
     if mean >= 128:  # prefill: whole 256-row tiles, K unsplit, CTA pairs
-        # FP8 weights on two-term rows take two accumulator columns per row:
-        # 128-row tiles (256 columns) in both GEMMs
-        assert pl["bn_down"] == (128 if wfmt == "fp8" else 256)
-        # weights converted to f16 in tensor memory keep 128-row gate/up tiles
-        assert pl["bn_gateup"] == (128 if wfmt in ("fp8", "mxfp4") else 256)
+        assert pl["bn_down"] == 256
+        # weights converted to f16 in tensor memory (MXFP4) keep 128-row
+        # gate/up tiles; FP8 weights on two-term rows tile like bf16
+        assert pl["bn_gateup"] == (128 if wfmt == "mxfp4" else 256)
         assert pl["splits_gateup"] == pl["splits_down"] == 1
         assert pl["pair_gateup"] == pl["pair_down"] == 1
 
