@@ -63,6 +63,7 @@ struct Layout {
   TcPlan plan, sh_plan;
   int router_splits;  // 0: CUDA-core router; else tensor-core logits with this many K splits
   bool gather;        // gate/up gathers token rows (decode tiling) instead of x_perm
+  bool x2_scattered;  // two-term rows written in permuted order (gate/up loads tiles)
 };
 
 // Workspace of moe_layer_forward (a superset of what the other entry points
@@ -96,16 +97,20 @@ Layout layout(const moe_problem& p, Path path, int num_sms, bool allow_splits) {
   // The permuted rows, except on the tensor path: there the gate/up GEMM
   // gathers the token rows itself (TMA gather4 for 32-row tiles, cp.async
   // for larger ones) and this region holds only x's two-term E4M3 rows
-  // (FP8 weights), the f16 copy of x (MXFP4 weights, or FP8 weights on the
-  // converters), or x's E4M3 codes with FP8 activations; x_scale holds the
-  // row scales of the E4M3 rows.
+  // (FP8 weights: per token, or at prefill tiles scattered into the
+  // permuted order, which the GEMM then loads by TMA tiles), the f16 copy
+  // of x (MXFP4 weights, or FP8 weights on the converters), or x's E4M3
+  // codes with FP8 activations; x_scale holds the row scales of the E4M3
+  // rows.
   const bool gather = path == Path::kTensor;
   const bool act8 = p.w_dtype == MOE_FP8_E4M3_ACT8;
   const bool x2 = fp8_two_term(p.w_dtype);
   L.gather = gather;
+  L.x2_scattered = gather && fp8_two_term_scattered(p.w_dtype, L.plan);
+  const size_t x2_rows = L.x2_scattered ? R : T;
   const bool f16x = (p.w_dtype == MOE_FP8_E4M3 && !x2) || p.w_dtype == MOE_MXFP4;
-  L.x_perm = take(gather ? (f16x ? T * d * 2 : act8 ? T * d : x2 ? 2 * T * d : 0) : R * d * ab);
-  L.x_scale = take(act8 || x2 ? T * 4 : 0);
+  L.x_perm = take(gather ? (f16x ? T * d * 2 : act8 ? T * d : x2 ? 2 * x2_rows * d : 0) : R * d * ab);
+  L.x_scale = take(act8 ? T * 4 : x2 ? x2_rows * 4 : 0);
   L.h = take(R * f * ab);
   // E4M3 rows of h (one per row with FP8 activations, two with two-term
   // rows) and their row scales, for the down GEMM
@@ -452,6 +457,12 @@ moe_status layer_forward_impl(const moe_problem* p, const void* x, const void* w
     x_scale = at<float>(workspace, L.x_scale);
     MOE_TRY(quantize_rows_e4m3_launch(x, p->T, p->d, x_perm, x_scale, ctx.num_sms, s));
     x_src = x_perm;
+  } else if (gather && x2 && L.x2_scattered) {
+    // prefill tiles: each token's two rows written to its k permuted rows
+    // (tile loads in the GEMM instead of a two-row gather per row)
+    x_scale = at<float>(workspace, L.x_scale);
+    MOE_TRY(split_rows_e4m3x2_scatter_launch(x, p->T, p->d, p->k, inv_row, R, x_perm, x_scale, ctx.status,
+                                             ctx.num_sms, s));
   } else if (gather && x2) {
     x_scale = at<float>(workspace, L.x_scale);
     MOE_TRY(split_rows_e4m3x2_launch(x, p->T, p->d, x_perm, x_scale, ctx.num_sms, s));
@@ -460,9 +471,10 @@ moe_status layer_forward_impl(const moe_problem* p, const void* x, const void* w
     MOE_TRY(bf16_to_f16_launch(x, x_perm, (size_t)p->T * p->d, s));
     x_src = x_perm;
   }
+  const bool gathered = gather && !L.x2_scattered;
   MOE_TRY(run_grouped(path, R, p->d, p->ffn, p->E, p->w_dtype, x_perm, offsets, w_gate, w_up,
                       w_down, s_gate, s_up, s_down, h, y, L.plan, ctx.status, s,
-                      timer ? timer->ev[3] : nullptr, gather ? perm_token : nullptr, x_src, p->T,
+                      timer ? timer->ev[3] : nullptr, gathered ? perm_token : nullptr, x_src, p->T,
                       at<float>(workspace, L.gu_part), L.cnt_routed ? at<int>(workspace, L.gu_cnt) : nullptr,
                       x_scale, act8 || x2 ? at<uint8_t>(workspace, L.h_q) : nullptr,
                       act8 || x2 ? at<float>(workspace, L.h_scale) : nullptr));

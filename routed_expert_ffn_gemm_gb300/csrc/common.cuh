@@ -221,6 +221,13 @@ moe_status quantize_rows_e4m3_launch(const void* x, int rows, int d, void* codes
 // GEMMs on bf16 activations.
 moe_status split_rows_e4m3x2_launch(const void* x, int rows, int d, void* codes, float* scales, int num_sms,
                                     cudaStream_t s, bool f16_in = false);
+// The same split of bf16 token rows x [T, d], each written to its k rows of
+// the permuted order (dst_rows [T*k]: inv_row) of codes [2, R, d] and
+// scales [R]: the B operand of a gate/up GEMM that loads rows by TMA tiles
+// instead of gathering them.
+moe_status split_rows_e4m3x2_scatter_launch(const void* x, int T, int d, int k, const int32_t* dst_rows, int R,
+                                            void* codes, float* scales, int* status, int num_sms,
+                                            cudaStream_t s);
 
 struct CombineArgs {
   int T, k, d, act_dtype;
@@ -258,6 +265,8 @@ struct TcPlan {
   int grid;            // persistent CTAs
   int pair_gateup;     // 1: the gate/up GEMM runs on CTA pairs (cta_group::2, M = 256)
   int pair_down;       // 1: the down GEMM runs on CTA pairs
+  int boxn_gateup;     // rows per TMA box of the B rows (tile loads), gate/up and down
+  int boxn_down;
 };
 struct TcGroupedArgs {
   int R, d, ffn, G;    // rows, hidden, intermediate, groups (experts)
@@ -294,6 +303,11 @@ struct TcGroupedArgs {
 // FP8 weights with bf16 activations run on two-term E4M3 rows (the default;
 // MOE_FP8_CONVERT=1 selects the E4M3 -> f16 weight converters instead).
 bool fp8_two_term(int w_dtype);
+// Whether the layer hands the gate/up GEMM of this plan two-term rows in
+// permuted order (tile loads) rather than per token (gathered rows): at
+// prefill tiles, where gathering two rows per row costs the producer more
+// than the one scatter pass.
+bool fp8_two_term_scattered(int w_dtype, const TcPlan& plan);
 // Arrival counters the fused gate/up finalize needs for R rows in G groups.
 size_t gu_counters_size(int R, int G, int ffn, const TcPlan& plan);
 TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype);

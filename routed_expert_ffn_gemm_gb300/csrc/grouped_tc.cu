@@ -1233,6 +1233,11 @@ bool fp8_two_term(int w_dtype) {
   return w_dtype == MOE_FP8_E4M3 && env_int("MOE_FP8_CONVERT") != 1;
 }
 
+bool fp8_two_term_scattered(int w_dtype, const TcPlan& plan) {
+  // (MOE_X2_GATHER=1 keeps gathering the rows at prefill tiles: tuning)
+  return fp8_two_term(w_dtype) && (plan.bn_gateup >= 128 || plan.pair_gateup) && env_int("MOE_X2_GATHER") != 1;
+}
+
 namespace {
 
 // K splits (<= 8, each >= 4 k-blocks) so that `units` work units fill whole
@@ -1279,13 +1284,17 @@ __global__ void __launch_bounds__(256) swiglu_finalize_kernel(int R, int M, int 
 }
 // Rows per B box: 16 for decode tiles; else one box for all of a CTA's B
 // rows (BN, or BN/2 on a CTA pair): every TMA copy costs a fixed overhead
-// on top of its bytes, measured to matter at prefill.  MOE_BOXN = 64/128/256
-// overrides (tuning) where it fits.
-int boxn_of(int bn, bool pair) {
+// on top of its bytes, measured to matter at prefill (two 64-row boxes in
+// place of one 128-row box measured 10 % slower on the DeepSeek-shaped down
+// GEMM, whose groups hold about 128 rows, though the larger box fetches
+// rows of the next group).  MOE_BOXN, MOE_BOXN_GATEUP, MOE_BOXN_DOWN =
+// 32/64/128/256 override (tuning) where they divide the CTA's rows, so the
+// last box of a tile never writes past its shared-memory tile.
+int boxn_of(int bn, bool pair, const char* env_name) {
   if (bn < 128) return kBoxSmall;
   const int cap = pair ? bn / 2 : bn;
-  const int e = env_int("MOE_BOXN");
-  if ((e == 64 || e == 128 || e == 256) && e <= cap) return e;
+  const int e = env_int(env_name) ? env_int(env_name) : env_int("MOE_BOXN");
+  if ((e == 32 || e == 64 || e == 128 || e == 256) && e <= cap) return e;
   return cap;
 }
 
@@ -1310,7 +1319,10 @@ TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype) {
   // accumulator column per row and tile like bf16.
   const bool x2 = fp8_two_term(w_dtype);
   const bool conv = (w_dtype == MOE_FP8_E4M3 && !x2) || w_dtype == MOE_MXFP4;
-  const int bn_gu = (bn == 128 && mean >= 128.0 && !conv) ? 256 : bn;
+  // A single dense group (the shared expert) at prefill takes 128-row
+  // gate/up tiles: they are all full, and two TMEM accumulator buffers let
+  // the epilogue overlap the next tile's MMAs.
+  const int bn_gu = (bn == 128 && mean >= 128.0 && !conv && E > 1) ? 256 : bn;
   const int bn_dn = (bn == 128 && mean >= 128.0) ? 256 : bn;
   pl.bn_gateup = bn_ok(env_int("MOE_BN_GATEUP")) ? env_int("MOE_BN_GATEUP") : bn_gu;
   pl.bn_down = bn_ok(env_int("MOE_BN_DOWN")) ? env_int("MOE_BN_DOWN") : bn_dn;
@@ -1348,6 +1360,9 @@ TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype) {
                          ? choose_splits(tiles_of(pl.bn_gateup) * (ffn / (2 * kBM)), (d + 2 * kBK - 1) / (2 * kBK),
                                          num_sms / 2)
                          : choose_splits(tiles_of(pl.bn_gateup) * (ffn / kBM), (d + kw_gu - 1) / kw_gu, num_sms);
+  // (no gate/up split for groups of prefill size: their tiles fill the SMs,
+  // and a split adds a pass over fp32 partials of every row)
+  if (mean >= 128.0) pl.splits_gateup = 1;
   if (env_int("MOE_SPLITS_GATEUP") >= 1 && env_int("MOE_SPLITS_GATEUP") <= 8)
     pl.splits_gateup = env_int("MOE_SPLITS_GATEUP");
   pl.grid = num_sms;
@@ -1356,6 +1371,8 @@ TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype) {
   pl.pair_gateup =
       dec_pair_gu || (pairs_ok && pl.bn_gateup >= 128 && ffn % (2 * kBM) == 0 && pl.splits_gateup == 1) ? 1 : 0;
   pl.pair_down = dec_pair_dn || (pairs_ok && pl.bn_down >= 128 && d % (2 * kBM) == 0) ? 1 : 0;
+  pl.boxn_gateup = boxn_of(pl.bn_gateup, pl.pair_gateup != 0, "MOE_BOXN_GATEUP");
+  pl.boxn_down = boxn_of(pl.bn_down, pl.pair_down != 0, "MOE_BOXN_DOWN");
   return pl;
 }
 
@@ -1404,8 +1421,8 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   } else {
     sg = su = sd = wg;
   }
-  const int box_gu = boxn_of(plan.bn_gateup, plan.pair_gateup != 0);
-  const int box_dn = boxn_of(plan.bn_down, plan.pair_down != 0);
+  const int box_gu = plan.boxn_gateup > 0 ? plan.boxn_gateup : kBoxSmall;
+  const int box_dn = plan.boxn_down > 0 ? plan.boxn_down : kBoxSmall;
   // gathered token rows: TMA gather4 for decode tiles, cp.async by the
   // producer warp for prefill tiles (gather4 costs a copy per 4 rows)
   const bool lsu = a.gather_rows != nullptr && (plan.bn_gateup >= 128 || plan.pair_gateup);

@@ -98,10 +98,16 @@ __device__ __forceinline__ float e4m3_value(uint32_t code) {
   return __half2float(__half(h));
 }
 
+// With dst_rows (scatter form): row t's codes and scale go to rows
+// dst_rows[t*k + j], j < k, of planes of R rows (an out-of-range row is
+// recorded as MOE_ERR_DEVICE_BOUNDS and skipped); else to row t of planes
+// of `rows` rows.
 template <bool F16>
 __global__ void __launch_bounds__(kQThreads) split_rows_e4m3x2_kernel(const uint4* __restrict__ x, int rows,
                                                                       int vpr, uint2* __restrict__ codes,
-                                                                      float* __restrict__ scales) {
+                                                                      float* __restrict__ scales,
+                                                                      const int32_t* __restrict__ dst_rows, int k,
+                                                                      int R, int* status) {
   griddep_begin();
   __shared__ float red[kQThreads / 32];
   for (int r = blockIdx.x; r < rows; r += gridDim.x) {
@@ -127,9 +133,16 @@ __global__ void __launch_bounds__(kQThreads) split_rows_e4m3x2_kernel(const uint
     const int p = amax > 0.f ? (f <= 0.875f ? e - 9 : e - 8) : 0;
     // x / 2^p as two exact power-of-two factors (each within fp32's range)
     const float inv_a = ldexpf(1.f, -(p / 2)), inv_b = ldexpf(1.f, -(p - p / 2));
-    if (threadIdx.x == 0) scales[r] = ldexpf(1.f, p);
-    uint2* hr = codes + (size_t)r * vpr;
-    uint2* lr = codes + (size_t)(rows + r) * vpr;
+    // destination rows of this row's codes (one, or its k permuted rows)
+    const int nd = dst_rows != nullptr ? k : 1;
+    const int plane = dst_rows != nullptr ? R : rows;
+    if (threadIdx.x < nd) {
+      const int dr = dst_rows != nullptr ? dst_rows[(size_t)r * k + threadIdx.x] : r;
+      if (dr >= 0 && dr < plane)
+        scales[dr] = ldexpf(1.f, p);
+      else
+        set_device_status(status, MOE_ERR_DEVICE_BOUNDS);
+    }
     for (int v = threadIdx.x; v < vpr; v += kQThreads) {
       const uint4 q = xr[v];
       const uint32_t w[4] = {q.x, q.y, q.z, q.w};
@@ -141,8 +154,14 @@ __global__ void __launch_bounds__(kQThreads) split_rows_e4m3x2_kernel(const uint
         const float ra = a - e4m3_value(ch[i] & 0xffu), rb = b - e4m3_value(ch[i] >> 8);
         cl[i] = e4m3x2(ra, rb);
       }
-      hr[v] = make_uint2(ch[0] | (ch[1] << 16), ch[2] | (ch[3] << 16));
-      lr[v] = make_uint2(cl[0] | (cl[1] << 16), cl[2] | (cl[3] << 16));
+      const uint2 hv = make_uint2(ch[0] | (ch[1] << 16), ch[2] | (ch[3] << 16));
+      const uint2 lv = make_uint2(cl[0] | (cl[1] << 16), cl[2] | (cl[3] << 16));
+      for (int j = 0; j < nd; ++j) {
+        const int dr = dst_rows != nullptr ? __ldg(dst_rows + (size_t)r * k + j) : r;
+        if (dr < 0 || dr >= plane) continue;
+        codes[(size_t)dr * vpr + v] = hv;
+        codes[(size_t)(plane + dr) * vpr + v] = lv;
+      }
     }
     __syncthreads();  // red[] is rewritten by the next row
   }
@@ -157,10 +176,25 @@ moe_status split_rows_e4m3x2_launch(const void* x, int rows, int d, void* codes,
   const int blocks = rows < 16 * num_sms ? rows : 16 * num_sms;
   if (f16_in)
     MOE_TRY_CUDA(launch_k(split_rows_e4m3x2_kernel<true>, dim3(blocks), dim3(kQThreads), 0, s,
-                          static_cast<const uint4*>(x), rows, d / 8, static_cast<uint2*>(codes), scales));
+                          static_cast<const uint4*>(x), rows, d / 8, static_cast<uint2*>(codes), scales,
+                          (const int32_t*)nullptr, 1, rows, (int*)nullptr));
   else
     MOE_TRY_CUDA(launch_k(split_rows_e4m3x2_kernel<false>, dim3(blocks), dim3(kQThreads), 0, s,
-                          static_cast<const uint4*>(x), rows, d / 8, static_cast<uint2*>(codes), scales));
+                          static_cast<const uint4*>(x), rows, d / 8, static_cast<uint2*>(codes), scales,
+                          (const int32_t*)nullptr, 1, rows, (int*)nullptr));
+  MOE_TRY_CUDA(cudaGetLastError());
+  return MOE_OK;
+}
+
+moe_status split_rows_e4m3x2_scatter_launch(const void* x, int T, int d, int k, const int32_t* dst_rows, int R,
+                                            void* codes, float* scales, int* status, int num_sms,
+                                            cudaStream_t s) {
+  if (T == 0) return MOE_OK;
+  if (T < 0 || d <= 0 || d % 8 != 0 || k < 1 || k > kQThreads || dst_rows == nullptr) return MOE_ERR_UNSUPPORTED;
+  const int blocks = T < 16 * num_sms ? T : 16 * num_sms;
+  MOE_TRY_CUDA(launch_k(split_rows_e4m3x2_kernel<false>, dim3(blocks), dim3(kQThreads), 0, s,
+                        static_cast<const uint4*>(x), T, d / 8, static_cast<uint2*>(codes), scales, dst_rows, k, R,
+                        status));
   MOE_TRY_CUDA(cudaGetLastError());
   return MOE_OK;
 }

@@ -580,11 +580,16 @@ def test_layer_gateup_split_k(splits, bn, d, pair, wfmt, monkeypatch):
 
 
 @pytest.mark.parametrize("bn,pair", [(128, 0), (128, 1), (256, 0), (256, 1)])
-@pytest.mark.parametrize("wfmt", ["bf16", "fp8", "fp8conv", "fp8a8"])
+@pytest.mark.parametrize("wfmt", ["bf16", "fp8", "fp8gather", "fp8conv", "fp8a8"])
 def test_layer_gathered_rows_every_tile(bn, pair, wfmt, monkeypatch):
     # the gate/up GEMM gathers its token rows (cp.async by the producer warp
     # for tiles of >= 128 rows), on single CTAs and on CTA pairs, with groups
-    # spanning several tiles and ragged tails
+    # spanning several tiles and ragged tails.  FP8 weights: the two-term
+    # rows scattered into permuted order (tile loads), or gathered per token
+    # (fp8gather), or the weight converters (fp8conv)
+    if wfmt == "fp8gather":
+        monkeypatch.setenv("MOE_X2_GATHER", "1")
+        wfmt = "fp8"
     monkeypatch.setenv("MOE_BN_GATEUP", str(bn))
     monkeypatch.setenv("MOE_BN_DOWN", str(bn))
     monkeypatch.setenv("MOE_PAIR", str(pair))
