@@ -529,7 +529,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
           }
         // gathered rows (lsu): this lane's rows lane + 32 i of the CTA's
         // B rows, their token ids (-1: past the group's end, not copied)
-        constexpr int RPL = (PAIR ? BN / 2 : BN) / 32 > 0 ? (PAIR ? BN / 2 : BN) / 32 : 1;
+        constexpr int RPL = ((PAIR ? BN / 2 : BN) + 31) / 32;  // (80 rows on a 160-row pair tile: 3)
         int tok[RPL];
 #pragma unroll
         for (int i = 0; i < RPL; ++i) {
@@ -1196,6 +1196,7 @@ moe_status launch_mode(int bn, int wf, bool pair, const TcParams& p, const CUten
     MOE_LAUNCH(256, kWFp8Act8, true);
     MOE_LAUNCH(32, kWFp8X2, true);
     MOE_LAUNCH(128, kWFp8X2, true);
+    MOE_LAUNCH(160, kWFp8X2, true);
     MOE_LAUNCH(256, kWFp8X2, true);
     return MOE_ERR_UNSUPPORTED;
   }
@@ -1213,6 +1214,7 @@ moe_status launch_mode(int bn, int wf, bool pair, const TcParams& p, const CUten
   MOE_LAUNCH(256, kWFp8Act8, false);
   MOE_LAUNCH(32, kWFp8X2, false);
   MOE_LAUNCH(128, kWFp8X2, false);
+  MOE_LAUNCH(160, kWFp8X2, false);
   MOE_LAUNCH(256, kWFp8X2, false);
 #undef MOE_LAUNCH
   return MOE_ERR_UNSUPPORTED;
@@ -1223,7 +1225,8 @@ int env_int(const char* name) {
   return v ? atoi(v) : 0;
 }
 
-int bn_ok(int bn) { return bn == 32 || bn == 128 || bn == 256 ? bn : 0; }
+// (160-row tiles exist for two-term rows only)
+int bn_ok(int bn, bool x2) { return bn == 32 || bn == 128 || bn == 256 || (bn == 160 && x2) ? bn : 0; }
 
 }  // namespace
 
@@ -1319,13 +1322,16 @@ TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype) {
   // accumulator column per row and tile like bf16.
   const bool x2 = fp8_two_term(w_dtype);
   const bool conv = (w_dtype == MOE_FP8_E4M3 && !x2) || w_dtype == MOE_MXFP4;
-  // A single dense group (the shared expert) at prefill takes 128-row
-  // gate/up tiles: they are all full, and two TMEM accumulator buffers let
-  // the epilogue overlap the next tile's MMAs.
-  const int bn_gu = (bn == 128 && mean >= 128.0 && !conv && E > 1) ? 256 : bn;
-  const int bn_dn = (bn == 128 && mean >= 128.0) ? 256 : bn;
-  pl.bn_gateup = bn_ok(env_int("MOE_BN_GATEUP")) ? env_int("MOE_BN_GATEUP") : bn_gu;
-  pl.bn_down = bn_ok(env_int("MOE_BN_DOWN")) ? env_int("MOE_BN_DOWN") : bn_dn;
+  int bn_gu = (bn == 128 && mean >= 128.0 && !conv) ? 256 : bn;
+  int bn_dn = (bn == 128 && mean >= 128.0) ? 256 : bn;
+  // Two-term rows with groups of about 100 to 160 rows (the DeepSeek-V3
+  // shape at 4096 tokens: 128 on average) take 160-row tiles on CTA pairs:
+  // 80 rows per CTA hold nearly every group in one tile, and their smaller
+  // shared-memory tiles leave room for more pipeline stages (4 instead of 3
+  // in gate/up, 6 instead of 4 in down) of bytes the GEMM actually uses.
+  if (x2 && bn == 128 && E > 1 && mean >= 96.0 && est_max <= 192.0) bn_gu = bn_dn = 160;
+  pl.bn_gateup = bn_ok(env_int("MOE_BN_GATEUP"), x2) ? env_int("MOE_BN_GATEUP") : bn_gu;
+  pl.bn_down = bn_ok(env_int("MOE_BN_DOWN"), x2) ? env_int("MOE_BN_DOWN") : bn_dn;
   const double touched = E < R ? E : R;
   auto tiles_of = [&](int bn_) {
     const double a = R / bn_;

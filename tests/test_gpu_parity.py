@@ -277,7 +277,8 @@ def _fp8_stack(E, rows, cols, gen, all_codes_expert=None):
 TILES = [(32, 0), (128, 0), (256, 0), (32, 1), (128, 1), (256, 1)]
 
 
-@pytest.mark.parametrize("bn,pair,fmt", [(bn, pr, f) for bn, pr in TILES for f in ("bf16", "fp8", "fp8conv")])
+@pytest.mark.parametrize("bn,pair,fmt", [(bn, pr, f) for bn, pr in TILES for f in ("bf16", "fp8", "fp8conv")] +
+                         [(160, 0, "fp8"), (160, 1, "fp8")])
 def test_grouped_swiglu_every_tile_size(bn, pair, fmt, monkeypatch):
     # the same ragged groups through each tile-row count of both GEMMs, on
     # single CTAs and on CTA pairs (256 output channels per tile; 32-row
@@ -579,8 +580,9 @@ def test_layer_gateup_split_k(splits, bn, d, pair, wfmt, monkeypatch):
     _layer_check(shape, 4, FP8_TOL if wfmt != "bf16" else BF16_TOL)
 
 
-@pytest.mark.parametrize("bn,pair", [(128, 0), (128, 1), (256, 0), (256, 1)])
-@pytest.mark.parametrize("wfmt", ["bf16", "fp8", "fp8gather", "fp8conv", "fp8a8"])
+@pytest.mark.parametrize("bn,pair,wfmt", [(bn, pr, w) for bn, pr in ((128, 0), (128, 1), (256, 0), (256, 1))
+                                           for w in ("bf16", "fp8", "fp8gather", "fp8conv", "fp8a8")] +
+                         [(160, pr, w) for pr in (0, 1) for w in ("fp8", "fp8gather")])
 def test_layer_gathered_rows_every_tile(bn, pair, wfmt, monkeypatch):
     # the gate/up GEMM gathers its token rows (cp.async by the producer warp
     # for tiles of >= 128 rows), on single CTAs and on CTA pairs, with groups

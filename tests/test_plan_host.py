@@ -51,7 +51,9 @@ def test_plan_bounds(name, T, wfmt, sms):
     s = _shape(name, T, wfmt)
     pl = _plan(s, sms)
     assert pl["grid"] == sms
-    assert pl["bn_gateup"] in (32, 128, 256) and pl["bn_down"] in (32, 128, 256)
+    assert pl["bn_gateup"] in (32, 128, 160, 256) and pl["bn_down"] in (32, 128, 160, 256)
+    if wfmt != "fp8":
+        assert 160 not in (pl["bn_gateup"], pl["bn_down"])
     assert 1 <= pl["splits_gateup"] <= 8 and 1 <= pl["splits_down"] <= 8
     # each K split keeps at least 4 stages of at most 128 elements
     for K, S in ((s.d, pl["splits_gateup"]), (s.ffn, pl["splits_down"])):
@@ -75,10 +77,13 @@ def test_tile_rows_follow_the_rows_per_expert(name, T, wfmt):
         assert pl["pair_gateup"] == 0
         assert pl["pair_down"] == (1 if wfmt == "bf16" and s.d % 256 == 0 else 0)
     if mean >= 128:  # prefill: whole 256-row tiles, K unsplit, CTA pairs
-        assert pl["bn_down"] == 256
+        # FP8 weights on two-term rows with about 128 rows per group take
+        # 160-row tiles (80 rows per CTA of a pair)
+        two_term_160 = wfmt == "fp8" and mean + 3 * mean ** 0.5 + 1 <= 192
+        assert pl["bn_down"] == (160 if two_term_160 else 256)
         # weights converted to f16 in tensor memory (MXFP4) keep 128-row
-        # gate/up tiles; FP8 weights on two-term rows tile like bf16
-        assert pl["bn_gateup"] == (128 if wfmt == "mxfp4" else 256)
+        # gate/up tiles
+        assert pl["bn_gateup"] == (128 if wfmt == "mxfp4" else 160 if two_term_160 else 256)
         assert pl["splits_gateup"] == pl["splits_down"] == 1
         assert pl["pair_gateup"] == pl["pair_down"] == 1
 
