@@ -146,12 +146,16 @@ __host__ __device__ constexpr bool ta_config(int mode, int bn, bool fp8, bool pa
 // kind::f16 MMA.
 // FP8 weights times bf16 rows carried as two E4M3 terms (kind::f8f6f4,
 // two B rows per row: the default for FP8 weights with bf16 activations).
-enum { kWBf16 = 0, kWFp8 = 1, kWFp8Act8 = 2, kWMx4 = 3, kWFp8X2 = 4 };
+// kWFp8X2W: the same with 256 elements of K per stage (two 128-byte K
+// sub-tiles per operand), so that a stage carries twice the MMAs for its
+// fixed costs (barrier waits, fences, commits).
+enum { kWBf16 = 0, kWFp8 = 1, kWFp8Act8 = 2, kWMx4 = 3, kWFp8X2 = 4, kWFp8X2W = 5 };
 
 template <int MODE, int BN, int WF, bool PAIR>
 struct Cfg {
   static constexpr bool FP8 = WF != kWBf16;     // quantised weights: staged, f16 h (or E4M3 rows)
-  static constexpr bool X2 = WF == kWFp8X2;     // bf16 rows as two E4M3 rows each
+  static constexpr bool X2 = WF == kWFp8X2 || WF == kWFp8X2W;  // bf16 rows as two E4M3 rows
+  static constexpr bool WIDE = WF == kWFp8X2W;  // 256 elements of K per stage each
   // E4M3 weights times E4M3 rows (kind::f8f6f4): FP8 activations, or the
   // two-term rows
   static constexpr bool A8 = WF == kWFp8Act8 || X2;
@@ -181,8 +185,9 @@ struct Cfg {
   // FP8 activations: 128 elements of K per stage too, in single 128-byte
   // rows for both operands (one sub-tile); kind::f8f6f4 takes K = 32 per
   // instruction
-  static constexpr int KB = TA || K2 || A8 ? 2 * kBK : kBK;     // K elements per stage
-  static constexpr int NSUB = A8 ? 1 : KB / kBK;               // 128-byte B sub-tiles per stage
+  static constexpr int KB = WIDE ? 4 * kBK : TA || K2 || A8 ? 2 * kBK : kBK;  // K elements per stage
+  static constexpr int SUBK = A8 ? 2 * kBK : kBK;              // K elements per 128-byte sub-tile
+  static constexpr int NSUB = KB / SUBK;                       // 128-byte sub-tiles per operand and stage
   static constexpr int KSTEP = A8 ? 32 : 16;                   // K per MMA instruction
   static constexpr int A_BYTES = kBM * kBK * 2;                // 16 KB bf16 tile (MMA operand)
   static constexpr int BSUB_BYTES = (PAIR ? BN / 2 : BN) * kBK * 2;
@@ -564,22 +569,35 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
               // both CTAs' copies complete the even CTA's barrier
               const uint32_t fb = lead(full_bar(stage));
               ptx::mbar_arrive_expect_tx_cluster(fb, bytes);
-              ptx::tma_load_2d_pair(sa, &tmA0, fb, kb * C::KB, arow, pol_w);
-              if (MODE == kGateUp) ptx::tma_load_2d_pair(sa + C::W_BYTES, &tmA1, fb, kb * C::KB, arow, pol_w);
+#pragma unroll
+              for (int sub = 0; sub < (C::A8 ? C::NSUB : 1); ++sub) {
+                // (E4M3 weights: one 128-byte sub-tile of K per copy)
+                const uint32_t so = sub * (kBM * 128);
+                ptx::tma_load_2d_pair(sa + so, &tmA0, fb, kb * C::KB + sub * C::SUBK, arow, pol_w);
+                if (MODE == kGateUp)
+                  ptx::tma_load_2d_pair(sa + C::W_BYTES + so, &tmA1, fb, kb * C::KB + sub * C::SUBK, arow, pol_w);
+              }
               if (!lsu)
 #pragma unroll
                 for (int term = 0; term < C::NB; ++term)
                   for (int i = 0; i < nbox; ++i)
-                    ptx::tma_load_2d_pair(sb + term * C::BSUB_BYTES + i * p.boxn * kBK * 2, &tmB, fb, kb * C::KB,
-                                          brow0 + term * p.b_plane + i * p.boxn, pol_x);
+#pragma unroll
+                    for (int sub = 0; sub < C::NSUB; ++sub)
+                      ptx::tma_load_2d_pair(sb + (term * C::NSUB + sub) * C::BSUB_BYTES + i * p.boxn * kBK * 2, &tmB,
+                                            fb, kb * C::KB + sub * C::SUBK, brow0 + term * p.b_plane + i * p.boxn,
+                                            pol_x);
             } else {
               ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
               // weight codes (MXFP4: two per byte), then (MXFP4) the
               // k-block's scales of the tile's 128 rows
               const int wx = C::MX4 ? kb * (C::KB / 2) : kb * C::KB;
-              ptx::tma_load_2d(sa, &tmA0, full_bar(stage), wx, arow, pol_w);
-              if (MODE == kGateUp)
-                ptx::tma_load_2d(sa + C::W_BYTES, &tmA1, full_bar(stage), wx, arow, pol_w);
+#pragma unroll
+              for (int sub = 0; sub < (C::A8 ? C::NSUB : 1); ++sub) {
+                const uint32_t so = sub * (kBM * 128);
+                ptx::tma_load_2d(sa + so, &tmA0, full_bar(stage), wx + sub * C::SUBK, arow, pol_w);
+                if (MODE == kGateUp)
+                  ptx::tma_load_2d(sa + C::W_BYTES + so, &tmA1, full_bar(stage), wx + sub * C::SUBK, arow, pol_w);
+              }
               if constexpr (C::MX4) {
                 const int sx = x.mt * C::CH + (int)rank * kBM, sy = x.g * (p.K / 32) + kb * (C::KB / 32);
                 ptx::tma_load_2d(sa + C::STG_BYTES, &tmS0, full_bar(stage), sx, sy, pol_w);
@@ -593,7 +611,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
                   for (int sub = 0; sub < C::NSUB; ++sub)
                     for (int i = 0; i < nbox; ++i)
                       ptx::tma_load_2d(sb + (term * C::NSUB + sub) * C::BSUB_BYTES + i * p.boxn * kBK * 2, &tmB,
-                                       full_bar(stage), kb * C::KB + sub * kBK,
+                                       full_bar(stage), kb * C::KB + sub * C::SUBK,
                                        brow0 + term * p.b_plane + i * p.boxn, pol_x);
             }
           }
@@ -612,7 +630,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
 #pragma unroll
                 for (int sub = 0; sub < C::NSUB; ++sub) {
                   const uint8_t* src = xs + ((size_t)(tok[i] + term * p.b_plane) * p.d_src + (size_t)kb * C::KB +
-                                             sub * kBK) * kEsz;
+                                             sub * C::SUBK) * kEsz;
                   const uint32_t dst = sb + (term * C::NSUB + sub) * C::BSUB_BYTES + r * 128;
 #pragma unroll
                   for (int c = 0; c < 8; ++c) ptx::cp_async16(dst + ((c ^ (r & 7)) << 4), src + 16 * c);
@@ -630,7 +648,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
 #pragma unroll
                 for (int sub = 0; sub < C::NSUB; ++sub)
                   ptx::tma_gather4_2d(sb + (term * C::NSUB + sub) * C::BSUB_BYTES + (op - term * nops) * 4 * kBK * 2,
-                                      &tmB, full_bar(stage), kb * C::KB + sub * kBK, gr[h][0], gr[h][1], gr[h][2],
+                                      &tmB, full_bar(stage), kb * C::KB + sub * C::SUBK, gr[h][0], gr[h][1], gr[h][2],
                                       gr[h][3], pol_x);
             }
           }
@@ -733,7 +751,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
                 // accumulator
 #pragma unroll
                 for (int term = 0; term < C::NB; ++term) {
-                  const uint64_t dbt = db + (uint64_t)(term * (C::BSUB_BYTES >> 4));
+                  const uint64_t dbt = db + (uint64_t)(term * ((C::NSUB * C::BSUB_BYTES) >> 4));
                   const uint32_t at = term > 0 ? 1u : acc;
                   if (PAIR) {
                     ptx::mma_f8_pair(d0, da0 + ka, dbt, idesc, at);
@@ -811,9 +829,21 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
     const int eg = (warp - 2) >> 2;  // which of the quadrant's two warps: alternate column chunks
     int it = 0;
     bool ok = true;
+    constexpr int CW = MODE == kGateUp ? 16 : 32;
     for (int u = u_first; u < total_units; u += u_step, ++it) {
       const int buf = it % C::NBUF;
       const uint32_t acc_phase = (uint32_t)(it / C::NBUF) & 1u;
+      const Unit x = decode_unit(u, offs, prefix, G, MT, S, BN);
+      // E4M3 rows: lane l holds the row scale of the chunk's column l (its
+      // row's scale; rows gathered by token: the token's), loaded one chunk
+      // ahead, the first before the accumulator is ready
+      auto row_scale_of = [&](int cbase) -> float {
+        const int c = cbase + lane;
+        if (!A8 || lane >= CW || c >= x.n_valid) return 1.f;
+        const int r = x.row0 + c;
+        return __ldg(p.row_scale + (p.gather_rows != nullptr ? __ldg(p.gather_rows + r) : r));
+      };
+      float rs_next = row_scale_of(eg * CW);
       // one lane waits, the warp follows its verdict (tcgen05.ld below is
       // warp-collective, so the warp must agree)
       int got = 0;
@@ -824,7 +854,6 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
         break;
       }
       ptx::tc_fence_after();
-      const Unit x = decode_unit(u, offs, prefix, G, MT, S, BN);
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(C::ACC_COLS * buf);
       const int ch = x.mt * C::CH + (int)rank * kBM + ch_local;
       const bool empty_k = x.ks * kb_per_split >= kblocks;
@@ -835,9 +864,10 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
       // epilogue is the longer one per MMA cycle), 16 for gate/up (measured
       // faster there).  BN is a multiple of 32, so columns past n_mma stay
       // inside this accumulator; they are not stored.
-      constexpr int CW = MODE == kGateUp ? 16 : 32;
 #pragma unroll 1
       for (int c0 = eg * CW; c0 < n_mma; c0 += 2 * CW) {
+        const float rs_cur = rs_next;
+        rs_next = row_scale_of(c0 + 2 * CW);
         uint32_t ra[CW], rb_[CW];
 #pragma unroll
         for (int hlf = 0; hlf < CW / 16; ++hlf) {
@@ -866,16 +896,10 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
           auto val = [&](const uint32_t* acc, int j) { return __uint_as_float(acc[j]); };
           if (nj > 0) {
             // E4M3 rows: each column (token row, or row of h) carries its
-            // row's scale (rows gathered by token: the token's)
+            // row's scale, from the lane that loaded it
             float rsc[NJ];
 #pragma unroll
-            for (int j = 0; j < NJ; ++j) {
-              rsc[j] = 1.f;
-              if (A8 && j < nj) {
-                const int r = x.row0 + rb + j;
-                rsc[j] = p.row_scale[p.gather_rows != nullptr ? p.gather_rows[r] : r];
-              }
-            }
+            for (int j = 0; j < NJ; ++j) rsc[j] = A8 ? __shfl_sync(0xffffffffu, rs_cur, 16 * hlf + j) : 1.f;
             if (MODE == kGateUp) {
               if (p.out_f32) {
                 // K-split: scaled fp32 partials, SiLU*mul after the in-order sum
@@ -1180,6 +1204,11 @@ moe_status launch_mode(int bn, int wf, bool pair, const TcParams& p, const CUten
                        const CUtensorMap& s1, int grid, cudaStream_t s) {
 #define MOE_LAUNCH(BN_, WF_, PAIR_) \
   if (bn == BN_ && wf == WF_) return launch_one<MODE, BN_, WF_, PAIR_>(p, a0, a1, b, s0, s1, grid, s)
+  // (256 elements of K per stage: CTA pairs, and gate/up tiles up to 160
+  // rows, so that at least two stages fit in shared memory)
+#define MOE_LAUNCH_WIDE(BN_)                                                                             \
+  if constexpr (MODE == kDown || BN_ <= 160)                                                             \
+    if (bn == BN_ && wf == kWFp8X2W) return launch_one<MODE, BN_, kWFp8X2W, true>(p, a0, a1, b, s0, s1, grid, s)
   if (pair) {
     if (p.M % (2 * kBM) != 0 || grid < 2) return MOE_ERR_UNSUPPORTED;
     MOE_LAUNCH(32, kWFp8, true);
@@ -1198,6 +1227,9 @@ moe_status launch_mode(int bn, int wf, bool pair, const TcParams& p, const CUten
     MOE_LAUNCH(128, kWFp8X2, true);
     MOE_LAUNCH(160, kWFp8X2, true);
     MOE_LAUNCH(256, kWFp8X2, true);
+    MOE_LAUNCH_WIDE(128);
+    MOE_LAUNCH_WIDE(160);
+    MOE_LAUNCH_WIDE(256);
     return MOE_ERR_UNSUPPORTED;
   }
   MOE_LAUNCH(32, kWFp8, false);
@@ -1216,6 +1248,7 @@ moe_status launch_mode(int bn, int wf, bool pair, const TcParams& p, const CUten
   MOE_LAUNCH(128, kWFp8X2, false);
   MOE_LAUNCH(160, kWFp8X2, false);
   MOE_LAUNCH(256, kWFp8X2, false);
+#undef MOE_LAUNCH_WIDE
 #undef MOE_LAUNCH
   return MOE_ERR_UNSUPPORTED;
 }
@@ -1395,8 +1428,14 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   if (!fp8 && a.w_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   if (fp8 && (a.s_gate == nullptr || a.s_up == nullptr || a.s_down == nullptr)) return MOE_ERR_INVALID_ARG;
   if (act8 && (a.row_scale == nullptr || a.h_q == nullptr || a.h_scale == nullptr)) return MOE_ERR_INVALID_ARG;
-  const int wf_gu = x2 ? kWFp8X2 : fa8 ? kWFp8Act8 : mx4 ? kWMx4 : fp8 ? kWFp8 : kWBf16;
-  const int wf_dn = wf_gu;
+  const int wf_base = x2 ? kWFp8X2 : fa8 ? kWFp8Act8 : mx4 ? kWMx4 : fp8 ? kWFp8 : kWBf16;
+  // two-term rows on CTA pairs at prefill tiles: 256 elements of K per
+  // stage (MOE_X2_WIDE: bit 0 down, bit 1 gate/up)
+  const int xw = getenv("MOE_X2_WIDE") != nullptr ? env_int("MOE_X2_WIDE") : 1;
+  const bool wide_gu = x2 && plan.pair_gateup && plan.bn_gateup >= 128 && plan.bn_gateup <= 160 && (xw & 2);
+  const bool wide_dn = x2 && plan.pair_down && plan.bn_down >= 128 && (xw & 1);
+  const int wf_gu = wide_gu ? kWFp8X2W : wf_base;
+  const int wf_dn = wide_dn ? kWFp8X2W : wf_base;
   if (a.d % kBM != 0 || a.ffn % kBM != 0 || a.G > kMaxGroups) return MOE_ERR_UNSUPPORTED;
   // weights: bf16 tiles [128 x 64] with 128-byte swizzle, or E4M3 tiles
   // [128 x 64 bytes] staged unswizzled for the converters
