@@ -834,16 +834,23 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
       const int buf = it % C::NBUF;
       const uint32_t acc_phase = (uint32_t)(it / C::NBUF) & 1u;
       const Unit x = decode_unit(u, offs, prefix, G, MT, S, BN);
-      // E4M3 rows: lane l holds the row scale of the chunk's column l (its
-      // row's scale; rows gathered by token: the token's), loaded one chunk
-      // ahead, the first before the accumulator is ready
+      // Every scale the unit's epilogue needs is requested before the
+      // accumulator wait, so its memory latency hides behind the unit's MMAs.
+      // E4M3 rows: for this warp's chunk i, lane l holds the row scale of the
+      // chunk's column l (its row's scale; rows gathered by token: the token's).
       auto row_scale_of = [&](int cbase) -> float {
         const int c = cbase + lane;
         if (!A8 || lane >= CW || c >= x.n_valid) return 1.f;
         const int r = x.row0 + c;
         return __ldg(p.row_scale + (p.gather_rows != nullptr ? __ldg(p.gather_rows + r) : r));
       };
-      float rs_next = row_scale_of(eg * CW);
+      constexpr int NCH = (BN + 2 * CW - 1) / (2 * CW);  // chunks per warp
+      float rsv[NCH];
+#pragma unroll
+      for (int i = 0; i < NCH; ++i) rsv[i] = row_scale_of(eg * CW + 2 * CW * i);
+      const int ch = x.mt * C::CH + (int)rank * kBM + ch_local;
+      const float sc0 = C::CHS ? __ldg(p.scale0 + (size_t)x.g * p.M + ch) : 1.f;
+      const float sc1 = C::CHS && MODE == kGateUp ? __ldg(p.scale1 + (size_t)x.g * p.M + ch) : 1.f;
       // one lane waits, the warp follows its verdict (tcgen05.ld below is
       // warp-collective, so the warp must agree)
       int got = 0;
@@ -855,19 +862,17 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
       }
       ptx::tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(C::ACC_COLS * buf);
-      const int ch = x.mt * C::CH + (int)rank * kBM + ch_local;
       const bool empty_k = x.ks * kb_per_split >= kblocks;
       const int n_mma = ((x.n_valid + 15) / 16) * 16;
-      const float sc0 = C::CHS ? p.scale0[(size_t)x.g * p.M + ch] : 1.f;
-      const float sc1 = C::CHS && MODE == kGateUp ? p.scale1[(size_t)x.g * p.M + ch] : 1.f;
       // CW accumulator columns per TMEM wait: 32 for the projection (its
       // epilogue is the longer one per MMA cycle), 16 for gate/up (measured
       // faster there).  BN is a multiple of 32, so columns past n_mma stay
       // inside this accumulator; they are not stored.
 #pragma unroll 1
       for (int c0 = eg * CW; c0 < n_mma; c0 += 2 * CW) {
-        const float rs_cur = rs_next;
-        rs_next = row_scale_of(c0 + 2 * CW);
+        const float rs_cur = rsv[0];
+#pragma unroll
+        for (int i = 0; i + 1 < NCH; ++i) rsv[i] = rsv[i + 1];
         uint32_t ra[CW], rb_[CW];
 #pragma unroll
         for (int hlf = 0; hlf < CW / 16; ++hlf) {
