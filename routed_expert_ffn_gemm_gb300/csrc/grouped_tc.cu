@@ -864,6 +864,62 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(C::ACC_COLS * buf);
       const bool empty_k = x.ks * kb_per_split >= kblocks;
       const int n_mma = ((x.n_valid + 15) / 16) * 16;
+      // (not for 256-row tiles with converter warps, whose register cap is lower)
+      if constexpr (MODE == kGateUp && !(C::CONV && BN > 160)) {
+        if (!p.out_f32) {
+          // h of every chunk is computed and packed into registers first, the
+          // accumulator goes back to the MMA warp, and only then are the rows
+          // stored: with one accumulator buffer the next unit's MMAs wait for
+          // the release, not for the stores
+          uint32_t hp[NCH][8];
+#pragma unroll
+          for (int i = 0; i < NCH; ++i) {
+            const int c0 = eg * CW + 2 * CW * i;
+            if (c0 < n_mma) {
+              uint32_t ra[16], rb_[16];
+              ptx::tmem_ld16(taddr + c0, ra);
+              ptx::tmem_ld16(taddr + (uint32_t)C::UP_OFF + c0, rb_);
+              ptx::tmem_ld_wait();
+              if (empty_k) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) ra[j] = rb_[j] = 0u;
+              }
+#pragma unroll
+              for (int j = 0; j < 16; j += 2) {
+                const float r0 = A8 ? __shfl_sync(0xffffffffu, rsv[i], j) : 1.f;
+                const float r1 = A8 ? __shfl_sync(0xffffffffu, rsv[i], j + 1) : 1.f;
+                const float h0 = silu_mul(__uint_as_float(ra[j]) * sc0 * r0, __uint_as_float(rb_[j]) * sc1 * r0);
+                const float h1 = silu_mul(__uint_as_float(ra[j + 1]) * sc0 * r1, __uint_as_float(rb_[j + 1]) * sc1 * r1);
+                if (C::H16) {
+                  const __half2 v = __floats2half2_rn(h0, h1);
+                  hp[i][j / 2] = *reinterpret_cast<const uint32_t*>(&v);
+                } else {
+                  const __nv_bfloat162 v = __floats2bfloat162_rn(h0, h1);
+                  hp[i][j / 2] = *reinterpret_cast<const uint32_t*>(&v);
+                }
+              }
+            }
+          }
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if (PAIR)
+              ptx::mbar_arrive_cluster(lead(acce_bar(buf)));
+            else
+              ptx::mbar_arrive(acce_bar(buf));
+          }
+          // h is 16-bit either way (bf16, or f16 when it feeds an f16 MMA)
+          uint16_t* o = static_cast<uint16_t*>(p.out) + (size_t)x.row0 * p.M + ch;
+#pragma unroll
+          for (int i = 0; i < NCH; ++i) {
+            const int c0 = eg * CW + 2 * CW * i;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (c0 + j < x.n_valid) o[(size_t)(c0 + j) * p.M] = (uint16_t)(hp[i][j / 2] >> (16 * (j & 1)));
+          }
+          continue;
+        }
+      }
       // CW accumulator columns per TMEM wait: 32 for the projection (its
       // epilogue is the longer one per MMA cycle), 16 for gate/up (measured
       // faster there).  BN is a multiple of 32, so columns past n_mma stay
