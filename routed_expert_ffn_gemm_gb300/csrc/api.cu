@@ -170,7 +170,8 @@ moe_status run_grouped(Path path, int R, int d, int ffn, int G, int w_dtype, con
                        const TcPlan& plan, int* status, cudaStream_t s, cudaEvent_t mid,
                        const int32_t* gather_rows = nullptr, const void* x_src = nullptr,
                        int T_src = 0, float* gu_partials = nullptr, int* gu_cnt = nullptr,
-                       const float* row_scale = nullptr, void* h_q = nullptr, float* h_scale = nullptr) {
+                       const float* row_scale = nullptr, void* h_q = nullptr, float* h_scale = nullptr,
+                       int early_down = 0) {
   if (path == Path::kSimt) {
     SimtGroupedArgs a{R, d, ffn, G, static_cast<const float*>(x_rows), offsets,
                       static_cast<const float*>(wg), static_cast<const float*>(wu),
@@ -179,7 +180,8 @@ moe_status run_grouped(Path path, int R, int d, int ffn, int G, int w_dtype, con
     return simt_grouped_launch(a, s, mid);
   }
   TcGroupedArgs a{R, d, ffn, G, w_dtype, x_rows, offsets, wg, wu, wd, sg, su, sd, h, y, status,
-                  wait_limit_ns(), gather_rows, x_src, T_src, gu_partials, gu_cnt, row_scale, h_q, h_scale};
+                  wait_limit_ns(), gather_rows, x_src, T_src, gu_partials, gu_cnt, row_scale, h_q, h_scale,
+                  early_down};
   return tc_grouped_launch(a, plan, s, mid);
 }
 
@@ -477,7 +479,8 @@ moe_status layer_forward_impl(const moe_problem* p, const void* x, const void* w
                       timer ? timer->ev[3] : nullptr, gathered ? perm_token : nullptr, x_src, p->T,
                       at<float>(workspace, L.gu_part), L.cnt_routed ? at<int>(workspace, L.gu_cnt) : nullptr,
                       x_scale, act8 || x2 ? at<uint8_t>(workspace, L.h_q) : nullptr,
-                      act8 || x2 ? at<float>(workspace, L.h_scale) : nullptr));
+                      act8 || x2 ? at<float>(workspace, L.h_scale) : nullptr,
+                      /* early_down: the permutation above wrote the offsets */ 1));
   MOE_TRY(mark(4));
   // 4. shared expert (CUDA-core path: here, one group {0, T}); on the
   // tensor path, join the side stream

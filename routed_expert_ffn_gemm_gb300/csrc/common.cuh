@@ -299,6 +299,11 @@ struct TcGroupedArgs {
   const float* row_scale;
   void* h_q;
   float* h_scale;
+  // 1: the offsets and the weights are complete before gate/up's grid
+  // passes its griddepcontrol.wait (the layer: the permutation wrote the
+  // offsets), so the down GEMM requests its first weight tiles before its
+  // own wait (TcParams::early_w)
+  int early_down;
 };
 // FP8 weights with bf16 activations run on two-term E4M3 rows (the default;
 // MOE_FP8_CONVERT=1 selects the E4M3 -> f16 weight converters instead).

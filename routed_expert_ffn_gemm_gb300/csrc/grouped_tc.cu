@@ -129,6 +129,12 @@ struct TcParams {
   // FP8 activations (gate/up): per-row quantisation scales of the B rows,
   // indexed by token (gather_rows) or by row
   const float* row_scale;
+  // down GEMM, 1: the offsets and the weights were complete before the
+  // predecessor grid passed its own griddepcontrol.wait (every grid between
+  // their producer and this one lets dependants launch only after its
+  // wait), so the unit walk and the first ring slots' weight copies start
+  // before this grid's wait; only the B rows wait for the predecessor
+  int early_w;
 };
 
 // Whether FP8 tiles take the tensor-memory operand path (see Cfg::TA): the
@@ -395,7 +401,8 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
   // units: the pair walks one sequence together
   const int u_first = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int u_step = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
-  griddep_launch_dependents();
+  // weights and offsets ahead of the wait (down GEMM, no converter warps)
+  const bool early = MODE == kDown && !CONV && p.early_w != 0 && !p.selftest && !p.dense;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -435,15 +442,20 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
   }
 
   // The prologue above touches no global memory; from here on the previous
-  // kernel's results (offsets, operands) must be complete.
-  griddep_wait();
-  const uint64_t deadline = ptx::globaltimer_ns() + (uint64_t)p.timeout_ns;
+  // kernel's results (offsets, operands) must be complete.  Dependants may
+  // launch once every CTA is past this wait, so a dependant that launches
+  // knows every grid before this one has completed.
+  if (!early) {
+    griddep_wait();
+    griddep_launch_dependents();
+  }
 
   // Group row ranges (clamped into [0, R]) and the exclusive prefix of
-  // per-group tile counts ceil(rows / BN).
+  // per-group tile counts ceil(rows / BN).  (Early: read past L1, which
+  // may hold lines of an earlier grid.)
   const int G = p.selftest ? 1 : p.G;
   for (int g = threadIdx.x; g <= G; g += C::THREADS) {
-    int o = p.selftest ? 0 : (p.dense ? (g == 0 ? 0 : p.R) : p.offsets[g]);
+    int o = p.selftest ? 0 : (p.dense ? (g == 0 ? 0 : p.R) : early ? __ldcg(p.offsets + g) : p.offsets[g]);
     if (o < 0 || o > p.R) {
       set_device_status(p.status, MOE_ERR_DEVICE_BOUNDS);
       o = o < 0 ? 0 : p.R;
@@ -489,6 +501,53 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
   const int kblocks = (p.K + C::KB - 1) / C::KB;
   const int kb_per_split = (kblocks + S - 1) / S;
 
+  // Bytes one ring slot of unit x receives: the weight tiles and the B rows
+  // (this CTA's half of them on a pair) of nbox boxes, or of nops gather4
+  // copies; cp.async rows (lsu) arrive on their own.
+  auto slot_bytes = [&](int nbox, int nops, bool gather_b) -> uint32_t {
+    const uint32_t bbytes =
+        lsu ? 0u : C::NB * C::NSUB * (gather_b ? (uint32_t)nops * 4 * kBK * 2 : (uint32_t)nbox * p.boxn * kBK * 2);
+    return C::NA * C::W_BYTES + bbytes;
+  };
+  // Early weights: the first unit's first n_pre slots are armed with their
+  // whole byte count and get their weight copies now; the producer adds
+  // their B rows after the wait.  (The ring is empty: no slot to wait for.)
+  int n_pre = 0;
+  if (early) {
+    if (warp == 0 && lane == 0 && u_first < total_units) {
+      const uint64_t pol_w = ptx::policy_evict_first();
+      const Unit x = decode_unit(u_first, offs, prefix, G, MT, S, BN);
+      const int kb0 = x.ks * kb_per_split, kb1 = min(kblocks, kb0 + kb_per_split);
+      const int bhalf = PAIR ? ((x.n_valid + 31) / 32) * 16 : x.n_valid;
+      const uint32_t bytes = slot_bytes((bhalf + p.boxn - 1) / p.boxn, 0, false);
+      const int arow = x.g * p.M + x.mt * C::CH + (int)rank * kBM;
+      n_pre = max(0, min(STAGES, kb1 - kb0));
+      for (int i = 0; i < n_pre; ++i) {
+        const int kb = kb0 + i;
+        const uint32_t sa = sbase + C::RING_OFF + i * C::STAGE_BYTES;
+        if (C::K2) {
+          const uint32_t fb = lead(full_bar(i));
+          ptx::mbar_arrive_expect_tx_cluster(fb, bytes);
+          ptx::tma_load_3d_pair(sa, &tmA0, fb, arow, kb * 2, pol_w);
+        } else if (PAIR) {
+          const uint32_t fb = lead(full_bar(i));
+          ptx::mbar_arrive_expect_tx_cluster(fb, bytes);
+#pragma unroll
+          for (int sub = 0; sub < (C::A8 ? C::NSUB : 1); ++sub)
+            ptx::tma_load_2d_pair(sa + sub * (kBM * 128), &tmA0, fb, kb * C::KB + sub * C::SUBK, arow, pol_w);
+        } else {
+          ptx::mbar_arrive_expect_tx(full_bar(i), bytes);
+#pragma unroll
+          for (int sub = 0; sub < (C::A8 ? C::NSUB : 1); ++sub)
+            ptx::tma_load_2d(sa + sub * (kBM * 128), &tmA0, full_bar(i), kb * C::KB + sub * C::SUBK, arow, pol_w);
+        }
+      }
+    }
+    griddep_wait();
+    griddep_launch_dependents();
+  }
+  const uint64_t deadline = ptx::globaltimer_ns() + (uint64_t)p.timeout_ns;
+
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // Lane 0 waits for free slots and issues the weight copies and row
@@ -507,6 +566,38 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
       uint32_t phase = 0;
       long long issued = 0;  // slots armed so far (the abort path derives their phases)
       bool ok = true;
+      if (n_pre > 0) {
+        // early slots (armed, their weights requested, before the wait):
+        // the B rows of the first unit's first n_pre k-blocks
+        const Unit x = decode_unit(u_first, offs, prefix, G, MT, S, BN);
+        const int kb0 = x.ks * kb_per_split;
+        const int bhalf = PAIR ? ((x.n_valid + 31) / 32) * 16 : x.n_valid;
+        const int brow0 = x.row0 + (int)rank * bhalf;
+        const int nbox = (bhalf + p.boxn - 1) / p.boxn;
+        for (int i = 0; i < n_pre; ++i) {
+          const int kb = kb0 + i;
+          const uint32_t sb = sbase + C::RING_OFF + i * C::STAGE_BYTES + C::B_OFF;
+          if (C::K2) {
+            ptx::tma_load_3d_pair(sb, &tmB, lead(full_bar(i)), brow0, kb * 2, pol_x);
+          } else {
+#pragma unroll
+            for (int term = 0; term < C::NB; ++term)
+#pragma unroll
+              for (int sub = 0; sub < C::NSUB; ++sub)
+                for (int j = 0; j < nbox; ++j) {
+                  const uint32_t dst = sb + (term * C::NSUB + sub) * C::BSUB_BYTES + j * p.boxn * kBK * 2;
+                  const int kx = kb * C::KB + sub * C::SUBK, ry = brow0 + term * p.b_plane + j * p.boxn;
+                  if (PAIR)
+                    ptx::tma_load_2d_pair(dst, &tmB, lead(full_bar(i)), kx, ry, pol_x);
+                  else
+                    ptx::tma_load_2d(dst, &tmB, full_bar(i), kx, ry, pol_x);
+                }
+          }
+        }
+        stage = n_pre == STAGES ? 0 : n_pre;
+        phase = n_pre == STAGES ? 1u : 0u;
+        issued = n_pre;
+      }
       for (int u = u_first; u < total_units && ok; u += u_step) {
         const Unit x = decode_unit(u, offs, prefix, G, MT, S, BN);
         const int kb0 = x.ks * kb_per_split, kb1 = min(kblocks, kb0 + kb_per_split);
@@ -541,11 +632,10 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
           const int r = brow0 + lane + 32 * i;
           tok[i] = (lsu && lane + 32 * i < bhalf && r < x.row0 + x.n_valid) ? p.gather_rows[r] : -1;
         }
-        const uint32_t bbytes =
-            lsu ? 0u : C::NB * C::NSUB * (gather ? (uint32_t)nops * 4 * kBK * 2 : (uint32_t)nbox * p.boxn * kBK * 2);
-        const uint32_t bytes = C::NA * C::W_BYTES + bbytes;
+        const uint32_t bytes = slot_bytes(nbox, nops, gather);
         const int arow = x.g * p.M + x.mt * C::CH + (int)rank * kBM;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        // (the first unit's early slots are already complete but for their B rows)
+        for (int kb = u == u_first ? kb0 + n_pre : kb0; kb < kb1; ++kb) {
           int got = 1;
           if (lane == 0)
             got = ptx::mbar_wait_bounded(empty_bar(stage), phase ^ 1u, deadline, abort_flag) ? 1 : 0;
@@ -1615,6 +1705,7 @@ moe_status tc_grouped_launch(const TcGroupedArgs& a, const TcPlan& plan, cudaStr
   p.scale1 = nullptr;
   p.row_scale = act8 ? a.h_scale : nullptr;
   p.boxn = k2_dn ? plan.bn_down / 2 : box_dn;
+  p.early_w = a.early_down;
   MOE_TRY(launch_mode<kDown>(plan.bn_down, wf_dn, plan.pair_down != 0, p, wd, wd, hb, sd, sd, plan.grid, s));
   return MOE_OK;
 }
