@@ -15,48 +15,23 @@
 
 namespace moe {
 
-// (v1, e1) ranks before (v2, e2): larger logit, ties to the lower index.
-__device__ __forceinline__ bool ranks_before(float v1, int e1, float v2, int e2) {
-  return v1 > v2 || (v1 == v2 && e1 < e2);
+// The selection order as one unsigned key per (logit, expert): a larger key
+// ranks first.  High word: the logit's bits mapped monotonically (numbers
+// above every NaN, -0 folded into +0, which the order ties); low word: the
+// complemented index, so that equal logits go to the lower index.  Every
+// key is nonzero.
+__device__ __forceinline__ unsigned long long selection_key(float v, int e) {
+  const float c = __fadd_rn(v, 0.0f);  // -0 -> +0
+  const uint32_t b = __float_as_uint(c);
+  const uint32_t hi = c != c ? 0u : ((b & 0x80000000u) ? ~b : (b | 0x80000000u));
+  return ((unsigned long long)hi << 32) | (uint32_t)~(uint32_t)e;
 }
 
-// One warp: top-k of one token's logits row (shared or global memory).
-__device__ inline void topk_row(const float* row, int E, int k, int32_t* idx_out, float* w_out) {
+// One warp, lane j < k holding the logit and expert of slot j (slots in
+// selection order): weights exp(l_j - l_0) / sum over the slots, written
+// with the indices.
+__device__ __forceinline__ void topk_weights(float my_v, int my_e, int k, int32_t* idx_out, float* w_out) {
   const int lane = threadIdx.x & 31;
-  const int per_lane = (E + 31) / 32;  // <= 32
-  uint32_t taken = 0;                  // bit i: expert lane + 32*i already chosen
-  float my_v = 0.f;
-  int my_e = 0;
-  for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int be = E;  // E = no candidate
-    for (int i = 0; i < per_lane; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u)) {
-        const float v = row[e];
-        if (ranks_before(v, e, bv, be)) { bv = v; be = e; }
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (ranks_before(ov, oe, bv, be)) { bv = ov; be = oe; }
-    }
-    if (be >= E) {  // only NaN logits remain: take the lowest unchosen expert
-      int le = E;
-      for (int i = 0; i < per_lane; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && !((taken >> i) & 1u)) { le = e; break; }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) le = min(le, __shfl_xor_sync(0xffffffffu, le, o));
-      be = le;
-      bv = row[be];
-    }
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
-    if (lane == j) { my_v = bv; my_e = be; }
-  }
   const float vmax = __shfl_sync(0xffffffffu, my_v, 0);
   const float ex = lane < k ? expf(my_v - vmax) : 0.f;
   float s = ex;
@@ -66,6 +41,39 @@ __device__ inline void topk_row(const float* row, int E, int k, int32_t* idx_out
     idx_out[lane] = my_e;
     w_out[lane] = ex / s;
   }
+}
+
+// One warp: top-k of one token's logits row (shared or global memory).
+// Round j: each lane's best untaken key, then a warp max of the keys (one
+// 64-bit shuffle and compare per level); the winner's lane marks it taken.
+__device__ inline void topk_row(const float* row, int E, int k, int32_t* idx_out, float* w_out) {
+  const int lane = threadIdx.x & 31;
+  const int per_lane = (E + 31) / 32;  // <= 32
+  uint32_t taken = 0;                  // bit i: expert lane + 32*i already chosen
+  float my_v = 0.f;
+  int my_e = 0;
+  for (int j = 0; j < k; ++j) {
+    unsigned long long best = 0ull;  // below every key
+    for (int i = 0; i < per_lane; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u)) {
+        const unsigned long long key = selection_key(row[e], e);
+        best = key > best ? key : best;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
+      best = other > best ? other : best;
+    }
+    const int be = (int)~(uint32_t)best;  // E >= k: an untaken expert always remains
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    if (lane == j) {
+      my_e = be;
+      my_v = row[be];
+    }
+  }
+  topk_weights(my_v, my_e, k, idx_out, w_out);
 }
 
 }  // namespace moe

@@ -76,6 +76,22 @@ def test_router_exact_ties_go_to_lower_index():
     np.testing.assert_allclose(w.cpu().numpy(), w_ref, rtol=2e-6)
 
 
+def test_router_selection_order_with_signed_zeros_infinities_and_nan():
+    # the kernels' documented order beyond the oracle's finite logits:
+    # larger first, -0 and +0 tied (lower index first), -inf after every
+    # other number, NaN logits last (lower index first)
+    rows = [([0.0, -0.0, 1.0, np.nan, -2.0, 3.0, -0.0, np.nan], [5, 2, 0, 1, 6, 4, 3, 7]),
+            ([-np.inf, 0.5, np.inf, -1.0, np.nan, 2.0, -np.inf, 1.0], [2, 5, 7, 1, 3, 0, 6, 4])]
+    for vals, order in rows:
+        lg = np.array([vals] * 9, dtype=np.float32)
+        p = api.problem(9, 128, 128, 8, 8)
+        idx = torch.empty((9, 8), dtype=torch.int32, device=DEV)
+        w = torch.empty((9, 8), dtype=torch.float32, device=DEV)
+        api.moe_router_topk(p, None, None, None, torch.from_numpy(lg).to(DEV), None, idx, w)
+        torch.cuda.synchronize()
+        assert idx.cpu().numpy().tolist() == [order] * 9
+
+
 @pytest.mark.parametrize("act,T,d,E,k", [("bf16", 40, 512, 16, 4), ("bf16", 3, 2048, 128, 8), ("f32", 64, 128, 8, 2),
                                          ("bf16", 200, 7168, 256, 8), ("bf16", 64, 4096, 8, 2),
                                          # tensor-core logits (bf16, E % 128 == 0, T >= 256), ragged T
