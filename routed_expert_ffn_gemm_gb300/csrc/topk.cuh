@@ -15,16 +15,15 @@
 
 namespace moe {
 
-// The selection order as one unsigned key per (logit, expert): a larger key
-// ranks first.  High word: the logit's bits mapped monotonically (numbers
-// above every NaN, -0 folded into +0, which the order ties); low word: the
-// complemented index, so that equal logits go to the lower index.  Every
-// key is nonzero.
-__device__ __forceinline__ unsigned long long selection_key(float v, int e) {
+// The selection order of logits as one unsigned key: a larger key ranks
+// first.  The logit's bits mapped monotonically, -0 folded into +0 (which
+// the order ties) and every NaN at 1, below every number (whose keys are
+// at least 0x007fffff, that of -inf).  0 stands for "no candidate".  Equal
+// keys go to the lower expert index.
+__device__ __forceinline__ uint32_t selection_key(float v) {
   const float c = __fadd_rn(v, 0.0f);  // -0 -> +0
   const uint32_t b = __float_as_uint(c);
-  const uint32_t hi = c != c ? 0u : ((b & 0x80000000u) ? ~b : (b | 0x80000000u));
-  return ((unsigned long long)hi << 32) | (uint32_t)~(uint32_t)e;
+  return c != c ? 1u : ((b & 0x80000000u) ? ~b : (b | 0x80000000u));
 }
 
 // One warp, lane j < k holding the logit and expert of slot j (slots in
@@ -44,8 +43,9 @@ __device__ __forceinline__ void topk_weights(float my_v, int my_e, int k, int32_
 }
 
 // One warp: top-k of one token's logits row (shared or global memory).
-// Round j: each lane's best untaken key, then a warp max of the keys (one
-// 64-bit shuffle and compare per level); the winner's lane marks it taken.
+// Round j: each lane's best untaken (key, index), then one warp max of the
+// keys and one warp min of the indices holding it (redux.sync each); the
+// winner's lane marks it taken.
 __device__ inline void topk_row(const float* row, int E, int k, int32_t* idx_out, float* w_out) {
   const int lane = threadIdx.x & 31;
   const int per_lane = (E + 31) / 32;  // <= 32
@@ -53,20 +53,19 @@ __device__ inline void topk_row(const float* row, int E, int k, int32_t* idx_out
   float my_v = 0.f;
   int my_e = 0;
   for (int j = 0; j < k; ++j) {
-    unsigned long long best = 0ull;  // below every key
-    for (int i = 0; i < per_lane; ++i) {
+    uint32_t key = 0u, e_best = 0xffffffffu;
+    for (int i = 0; i < per_lane; ++i) {  // ascending index: the strict > keeps the lower one
       const int e = lane + 32 * i;
       if (e < E && !((taken >> i) & 1u)) {
-        const unsigned long long key = selection_key(row[e], e);
-        best = key > best ? key : best;
+        const uint32_t ke = selection_key(row[e]);
+        if (ke > key) {
+          key = ke;
+          e_best = (uint32_t)e;
+        }
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
-      best = other > best ? other : best;
-    }
-    const int be = (int)~(uint32_t)best;  // E >= k: an untaken expert always remains
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);  // E >= k: an untaken expert remains
+    const int be = (int)__reduce_min_sync(0xffffffffu, key == kmax ? e_best : 0xffffffffu);
     if ((be & 31) == lane) taken |= 1u << (be >> 5);
     if (lane == j) {
       my_e = be;
