@@ -220,32 +220,49 @@ __global__ void __launch_bounds__(256) permute_count_kernel(int R, int E,
 }
 
 // chunk_cnt[c][e] -> offsets[e] + sum_{c'<c} chunk_cnt[c'][e] (in place).
-// One block of 1024 threads: 32 experts at a time along the lanes (loads
-// coalesced over experts), the chunks split into 32 slices over the warps;
-// per-slice sums combine through shared memory.  A first pass finds the
-// per-expert totals (-> counts, offsets), a second writes the running sums.
+// One block of 1024 threads: experts along the lanes (loads coalesced over
+// experts), the chunks split into 32 slices over the warps; per-slice sums
+// combine through shared memory.  kScanGroups groups of 32 experts share a
+// round (their loads in flight together, two barriers per round).  A first
+// pass finds the per-expert totals (-> counts, offsets), a second writes
+// the running sums.
+constexpr int kScanGroups = 4;
 __global__ void __launch_bounds__(1024) permute_scan_kernel(int n_chunks, int E,
                                                             int32_t* __restrict__ chunk_cnt,
                                                             int32_t* __restrict__ counts,
                                                             int32_t* __restrict__ offsets) {
   griddep_begin();
-  __shared__ int part[32][33];
+  __shared__ int part[kScanGroups][32][33];
   __shared__ int base_e[1024];
   __shared__ int warp_tot[32];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int per = (n_chunks + 31) / 32;
   const int c0 = min(n_chunks, w * per), c1 = min(n_chunks, c0 + per);
-  for (int g = 0; g < E; g += 32) {
-    const int e = g + lane;
-    int sum = 0;
-    if (e < E)
-      for (int c = c0; c < c1; ++c) sum += chunk_cnt[(size_t)c * E + e];
-    part[w][lane] = sum;
+  // this warp's slice sum of expert g0 + 32 gi + lane, for every group gi of
+  // the round, into part[gi][w][lane]
+  auto slice_sums = [&](int g0) {
+    int sum[kScanGroups];
+#pragma unroll
+    for (int gi = 0; gi < kScanGroups; ++gi) sum[gi] = 0;
+    for (int c = c0; c < c1; ++c)
+#pragma unroll
+      for (int gi = 0; gi < kScanGroups; ++gi) {
+        const int e = g0 + 32 * gi + lane;
+        if (e < E) sum[gi] += chunk_cnt[(size_t)c * E + e];
+      }
+#pragma unroll
+    for (int gi = 0; gi < kScanGroups; ++gi) part[gi][w][lane] = sum[gi];
+  };
+  for (int g0 = 0; g0 < E; g0 += 32 * kScanGroups) {
+    slice_sums(g0);
     __syncthreads();
-    if (w == 0 && e < E) {
-      int t = 0;
-      for (int i = 0; i < 32; ++i) t += part[i][lane];
-      base_e[e] = t;
+    if (w < kScanGroups) {
+      const int e = g0 + 32 * w + lane;
+      if (e < E) {
+        int t = 0;
+        for (int i = 0; i < 32; ++i) t += part[w][i][lane];
+        base_e[e] = t;
+      }
     }
     __syncthreads();
   }
@@ -259,20 +276,20 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int n_chunks, int E,
     base_e[e] = incl - tot;
   }
   __syncthreads();
-  for (int g = 0; g < E; g += 32) {
-    const int e2 = g + lane;
-    int sum = 0;
-    if (e2 < E)
-      for (int c = c0; c < c1; ++c) sum += chunk_cnt[(size_t)c * E + e2];
-    part[w][lane] = sum;
+  for (int g0 = 0; g0 < E; g0 += 32 * kScanGroups) {
+    slice_sums(g0);
     __syncthreads();
-    if (e2 < E) {
-      int run = base_e[e2];
-      for (int i = 0; i < w; ++i) run += part[i][lane];
-      for (int c = c0; c < c1; ++c) {
-        const int v = chunk_cnt[(size_t)c * E + e2];
-        chunk_cnt[(size_t)c * E + e2] = run;
-        run += v;
+#pragma unroll
+    for (int gi = 0; gi < kScanGroups; ++gi) {
+      const int e2 = g0 + 32 * gi + lane;
+      if (e2 < E) {
+        int run = base_e[e2];
+        for (int i = 0; i < w; ++i) run += part[gi][i][lane];
+        for (int c = c0; c < c1; ++c) {
+          const int v = chunk_cnt[(size_t)c * E + e2];
+          chunk_cnt[(size_t)c * E + e2] = run;
+          run += v;
+        }
       }
     }
     __syncthreads();

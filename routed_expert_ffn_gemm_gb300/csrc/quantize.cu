@@ -167,6 +167,110 @@ __global__ void __launch_bounds__(kQThreads) split_rows_e4m3x2_kernel(const uint
   }
 }
 
+// The same split with the row held in registers (NV 16-byte vectors per
+// thread, rows of up to NV * 128 * 8 elements): no second read of the row,
+// and each CTA loads its next row while it reduces and writes the current
+// one, so twice the rows are in flight per SM.  Same arithmetic, same codes.
+template <bool F16, int NV>
+__global__ void __launch_bounds__(kQThreads) split_rows_e4m3x2_regs_kernel(const uint4* __restrict__ x, int rows,
+                                                                           int vpr, uint2* __restrict__ codes,
+                                                                           float* __restrict__ scales,
+                                                                           const int32_t* __restrict__ dst_rows,
+                                                                           int k, int R, int* status) {
+  griddep_begin();
+  __shared__ float red[2][kQThreads / 32];  // by row parity: no barrier needed after a row
+  auto load_row = [&](int r, uint4 (&buf)[NV]) {
+    const uint4* xr = x + (size_t)r * vpr;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int v = threadIdx.x + i * kQThreads;
+      buf[i] = v < vpr ? xr[v] : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  uint4 cur[NV], nxt[NV];
+  int r = blockIdx.x;
+  if (r < rows) load_row(r, cur);
+  for (int it = 0; r < rows; r += gridDim.x, ++it) {
+    if (r + (int)gridDim.x < rows) load_row(r + gridDim.x, nxt);
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const uint32_t w[4] = {cur[i].x, cur[i].y, cur[i].z, cur[i].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(lo16<F16>(w[j])), fabsf(hi16<F16>(w[j]))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float* rd = red[it & 1];
+    if ((threadIdx.x & 31) == 0) rd[threadIdx.x >> 5] = m;
+    __syncthreads();
+    float amax = rd[0];
+#pragma unroll
+    for (int i = 1; i < kQThreads / 32; ++i) amax = fmaxf(amax, rd[i]);
+    int e = 0;
+    const float f = frexpf(amax, &e);
+    const int p = amax > 0.f ? (f <= 0.875f ? e - 9 : e - 8) : 0;
+    const float inv_a = ldexpf(1.f, -(p / 2)), inv_b = ldexpf(1.f, -(p - p / 2));
+    const int nd = dst_rows != nullptr ? k : 1;
+    const int plane = dst_rows != nullptr ? R : rows;
+    if (threadIdx.x < nd) {
+      const int dr = dst_rows != nullptr ? dst_rows[(size_t)r * k + threadIdx.x] : r;
+      if (dr >= 0 && dr < plane)
+        scales[dr] = ldexpf(1.f, p);
+      else
+        set_device_status(status, MOE_ERR_DEVICE_BOUNDS);
+    }
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int v = threadIdx.x + i * kQThreads;
+      if (v >= vpr) break;
+      const uint32_t w[4] = {cur[i].x, cur[i].y, cur[i].z, cur[i].w};
+      uint32_t ch[4], cl[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float a = lo16<F16>(w[j]) * inv_a * inv_b, b = hi16<F16>(w[j]) * inv_a * inv_b;
+        ch[j] = e4m3x2(a, b);
+        const float ra = a - e4m3_value(ch[j] & 0xffu), rb = b - e4m3_value(ch[j] >> 8);
+        cl[j] = e4m3x2(ra, rb);
+      }
+      const uint2 hv = make_uint2(ch[0] | (ch[1] << 16), ch[2] | (ch[3] << 16));
+      const uint2 lv = make_uint2(cl[0] | (cl[1] << 16), cl[2] | (cl[3] << 16));
+      for (int j = 0; j < nd; ++j) {
+        const int dr = dst_rows != nullptr ? __ldg(dst_rows + (size_t)r * k + j) : r;
+        if (dr < 0 || dr >= plane) continue;
+        codes[(size_t)dr * vpr + v] = hv;
+        codes[(size_t)(plane + dr) * vpr + v] = lv;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < NV; ++i) cur[i] = nxt[i];
+  }
+}
+
+// One of the split kernels for rows of vpr 16-byte vectors: the register
+// form when the row fits 4 vectors per thread, else the two-pass form (with
+// 8 vectors per thread the register form holds 121 registers, 4 CTAs per
+// SM, and fewer rows in flight than the two-pass form's 16 CTAs).
+template <bool F16>
+moe_status launch_split(int blocks, cudaStream_t s, const uint4* x, int rows, int vpr, uint2* codes,
+                        float* scales, const int32_t* dst_rows, int k, int R, int* status) {
+  const int nv = (vpr + kQThreads - 1) / kQThreads;
+  if (nv <= 1)
+    MOE_TRY_CUDA(launch_k(split_rows_e4m3x2_regs_kernel<F16, 1>, dim3(blocks), dim3(kQThreads), 0, s, x, rows, vpr,
+                          codes, scales, dst_rows, k, R, status));
+  else if (nv <= 2)
+    MOE_TRY_CUDA(launch_k(split_rows_e4m3x2_regs_kernel<F16, 2>, dim3(blocks), dim3(kQThreads), 0, s, x, rows, vpr,
+                          codes, scales, dst_rows, k, R, status));
+  else if (nv <= 4)
+    MOE_TRY_CUDA(launch_k(split_rows_e4m3x2_regs_kernel<F16, 4>, dim3(blocks), dim3(kQThreads), 0, s, x, rows, vpr,
+                          codes, scales, dst_rows, k, R, status));
+  else
+    MOE_TRY_CUDA(launch_k(split_rows_e4m3x2_kernel<F16>, dim3(blocks), dim3(kQThreads), 0, s, x, rows, vpr, codes,
+                          scales, dst_rows, k, R, status));
+  MOE_TRY_CUDA(cudaGetLastError());
+  return MOE_OK;
+}
+
 }  // namespace
 
 moe_status split_rows_e4m3x2_launch(const void* x, int rows, int d, void* codes, float* scales, int num_sms,
@@ -174,16 +278,10 @@ moe_status split_rows_e4m3x2_launch(const void* x, int rows, int d, void* codes,
   if (rows == 0) return MOE_OK;
   if (rows < 0 || d <= 0 || d % 8 != 0) return MOE_ERR_UNSUPPORTED;
   const int blocks = rows < 16 * num_sms ? rows : 16 * num_sms;
-  if (f16_in)
-    MOE_TRY_CUDA(launch_k(split_rows_e4m3x2_kernel<true>, dim3(blocks), dim3(kQThreads), 0, s,
-                          static_cast<const uint4*>(x), rows, d / 8, static_cast<uint2*>(codes), scales,
-                          (const int32_t*)nullptr, 1, rows, (int*)nullptr));
-  else
-    MOE_TRY_CUDA(launch_k(split_rows_e4m3x2_kernel<false>, dim3(blocks), dim3(kQThreads), 0, s,
-                          static_cast<const uint4*>(x), rows, d / 8, static_cast<uint2*>(codes), scales,
-                          (const int32_t*)nullptr, 1, rows, (int*)nullptr));
-  MOE_TRY_CUDA(cudaGetLastError());
-  return MOE_OK;
+  const uint4* xv = static_cast<const uint4*>(x);
+  uint2* cv = static_cast<uint2*>(codes);
+  return f16_in ? launch_split<true>(blocks, s, xv, rows, d / 8, cv, scales, nullptr, 1, rows, nullptr)
+                : launch_split<false>(blocks, s, xv, rows, d / 8, cv, scales, nullptr, 1, rows, nullptr);
 }
 
 moe_status split_rows_e4m3x2_scatter_launch(const void* x, int T, int d, int k, const int32_t* dst_rows, int R,
@@ -192,11 +290,8 @@ moe_status split_rows_e4m3x2_scatter_launch(const void* x, int T, int d, int k, 
   if (T == 0) return MOE_OK;
   if (T < 0 || d <= 0 || d % 8 != 0 || k < 1 || k > kQThreads || dst_rows == nullptr) return MOE_ERR_UNSUPPORTED;
   const int blocks = T < 16 * num_sms ? T : 16 * num_sms;
-  MOE_TRY_CUDA(launch_k(split_rows_e4m3x2_kernel<false>, dim3(blocks), dim3(kQThreads), 0, s,
-                        static_cast<const uint4*>(x), T, d / 8, static_cast<uint2*>(codes), scales, dst_rows, k, R,
-                        status));
-  MOE_TRY_CUDA(cudaGetLastError());
-  return MOE_OK;
+  return launch_split<false>(blocks, s, static_cast<const uint4*>(x), T, d / 8, static_cast<uint2*>(codes), scales,
+                             dst_rows, k, R, status);
 }
 
 moe_status quantize_rows_e4m3_launch(const void* x, int rows, int d, void* codes, float* scales,

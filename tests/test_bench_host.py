@@ -157,3 +157,11 @@ def test_layer_roofline_names_the_binding_bound():
     assert r["frac_binding"] == pytest.approx(0.5)
     r = bench.layer_roofline(1e9, 4e12, 4e-3, 5000.0, 2000.0, 8, 1.0)
     assert r["bound"] == "tensor" and r["frac_binding"] == pytest.approx(0.5)
+
+
+def test_tensor_peak_follows_the_length_of_the_timed_region():
+    # burst figure for a short timed region, sustained for one of a second or more
+    assert bench.tensor_peak_for(57.0, 1910.7, 1710.9) == (1910.7, "burst")
+    assert bench.tensor_peak_for(999.9, 1910.7, 1710.9) == (1910.7, "burst")
+    assert bench.tensor_peak_for(1000.0, 1910.7, 1710.9) == (1710.9, "sustained")
+    assert bench.tensor_peak_for(3006.0, 1910.7, 1710.9) == (1710.9, "sustained")

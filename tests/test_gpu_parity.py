@@ -166,6 +166,8 @@ def _random_idx(T, E, k, rng, skew=False):
 @pytest.mark.parametrize("T,E,k,skew", [(1, 8, 2, False), (64, 8, 2, False), (128, 128, 8, False),
                                         (256, 8, 8, False), (257, 8, 8, False), (1000, 64, 6, True),
                                         (8192, 128, 8, True), (4096, 256, 8, False), (3, 1024, 32, False),
+                                        # chunked path, experts not a multiple of the scan's 128 per round
+                                        (3000, 300, 4, True), (600, 1000, 8, False),
                                         # half a million rows through the chunked path
                                         (65536, 128, 8, False)])
 def test_permute_bit_exact(T, E, k, skew):

@@ -63,7 +63,7 @@ def _e4m3(v):
         .view(torch.uint8).numpy()
 
 
-@pytest.mark.parametrize("rows,cols", [(64, 7168), (257, 2048), (3, 8), (1, 128)])
+@pytest.mark.parametrize("rows,cols", [(64, 7168), (257, 2048), (3, 8), (1, 128), (129, 3072), (5, 4096), (300, 1000)])
 def test_split_rows_is_the_definition(rows, cols):
     x = _rows(rows, cols, rows + cols)
     codes, s = _split(x)
