@@ -556,7 +556,9 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
     // leave at once: no warp-wide step per slot).
     const bool gather = p.gather_rows != nullptr && !lsu;
     if (!p.selftest && (gather || lsu || lane == 0)) {
-      const uint64_t pol_w = ptx::policy_evict_first();
+      // weights: evict-first when one row tile of the expert reads them,
+      // evict-normal when several do (they are read again while in L2)
+      const uint64_t pol_w1 = ptx::policy_evict_first(), pol_wn = ptx::policy_evict_normal();
       const uint64_t pol_x = ptx::policy_evict_last();
       const uint32_t wmask = gather || lsu ? 0xffffffffu : 1u;
       // gathered rows: 16-bit elements (bf16 / f16), or E4M3 bytes (FP8 activations)
@@ -601,6 +603,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
       for (int u = u_first; u < total_units && ok; u += u_step) {
         const Unit x = decode_unit(u, offs, prefix, G, MT, S, BN);
         const int kb0 = x.ks * kb_per_split, kb1 = min(kblocks, kb0 + kb_per_split);
+        const uint64_t pol_w = prefix[x.g + 1] - prefix[x.g] > 1 ? pol_wn : pol_w1;
         // B rows this CTA stages: all of the tile, or (pair) its half of
         // the tile's MMA width rounded to 32
         const int bhalf = PAIR ? ((x.n_valid + 31) / 32) * 16 : x.n_valid;
