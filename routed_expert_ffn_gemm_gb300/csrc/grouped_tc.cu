@@ -626,14 +626,16 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
                            ? p.gather_rows[x.row0 + (i < x.n_valid ? i : 0)] + term * p.b_plane
                            : 0;
           }
-        // gathered rows (lsu): this lane's rows lane + 32 i of the CTA's
-        // B rows, their token ids (-1: past the group's end, not copied)
-        constexpr int RPL = ((PAIR ? BN / 2 : BN) + 31) / 32;  // (80 rows on a 160-row pair tile: 3)
+        // gathered rows (lsu): lanes 2j and 2j + 1 share rows j + 16 i of
+        // the CTA's B rows; their token ids (-1: past the group's end, not
+        // copied)
+        constexpr int RPL = ((PAIR ? BN / 2 : BN) + 15) / 16;  // (80 rows on a 160-row pair tile: 5)
         int tok[RPL];
 #pragma unroll
         for (int i = 0; i < RPL; ++i) {
-          const int r = brow0 + lane + 32 * i;
-          tok[i] = (lsu && lane + 32 * i < bhalf && r < x.row0 + x.n_valid) ? p.gather_rows[r] : -1;
+          const int rr = (lane >> 1) + 16 * i;
+          const int r = brow0 + rr;
+          tok[i] = (lsu && rr < bhalf && r < x.row0 + x.n_valid) ? p.gather_rows[r] : -1;
         }
         const uint32_t bytes = slot_bytes(nbox, nops, gather);
         const int arow = x.g * p.M + x.mt * C::CH + (int)rank * kBM;
@@ -709,15 +711,17 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
             }
           }
           if (lsu) {
-            // one lane per row: its rows' 128-byte K slices (per 64-element
-            // sub-tile), chunk c of row r at chunk c ^ (r % 8); then one
-            // arrival per lane once its copies have landed.  (Eight lanes per
-            // row, one 16-byte chunk each, so that a warp-wide copy moves
-            // four whole row slices, measured five times slower.)
+            // two lanes per row: of each 32-byte sector of the row's
+            // 128-byte K slice (per 64-element sub-tile) the even lane copies
+            // the first 16 bytes and the odd lane the second, so that one
+            // warp instruction asks for 16 whole sectors (one lane per row,
+            // each 16-byte copy asking for half a sector, fetched every
+            // sector twice); chunk c of row r goes to chunk c ^ (r % 8); then
+            // one arrival per lane once its copies have landed
 #pragma unroll
             for (int i = 0; i < RPL; ++i) {
               if (tok[i] < 0) continue;
-              const int r = lane + 32 * i;
+              const int r = (lane >> 1) + 16 * i;
 #pragma unroll
               for (int term = 0; term < C::NB; ++term)
 #pragma unroll
@@ -726,7 +730,10 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
                                              sub * C::SUBK) * kEsz;
                   const uint32_t dst = sb + (term * C::NSUB + sub) * C::BSUB_BYTES + r * 128;
 #pragma unroll
-                  for (int c = 0; c < 8; ++c) ptx::cp_async16(dst + ((c ^ (r & 7)) << 4), src + 16 * c);
+                  for (int j = 0; j < 4; ++j) {
+                    const int c = 2 * j + (lane & 1);
+                    ptx::cp_async16(dst + ((c ^ (r & 7)) << 4), src + 16 * c);
+                  }
                 }
             }
             ptx::cp_async_arrive_noinc(relay ? bfull_bar(stage) : full_bar(stage));
