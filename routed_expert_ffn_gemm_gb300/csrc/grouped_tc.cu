@@ -1534,9 +1534,11 @@ TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype) {
   // CTA pairs.  MOE_PAIR=0 keeps single CTAs; MOE_PAIR=2 also runs every
   // decode tile on pairs.  By default the decode (32-row) tiles of the bf16
   // down GEMM take pairs when that needs no more K splits: measured 5-11 %
-  // faster on the down GEMM (fewer, larger units).  The FP8 and
-  // FP8-activation decode tiles and the gate/up GEMM's decode tiles
-  // measured no faster on pairs (within 1-2 %).
+  // faster on the down GEMM (fewer, larger units); so do the gate/up decode
+  // tiles on two-term rows when their pair units need no K split (2.6 %
+  // faster at 64 tokens of the DeepSeek-V3 shape; with K splits, at one
+  // token, slower).  The other FP8 and FP8-activation decode tiles and the
+  // bf16 gate/up decode tiles measured no faster on pairs (within 1-2 %).
   const char* pe = getenv("MOE_PAIR");
   const bool pairs_ok = !(pe != nullptr && pe[0] == '0') && num_sms >= 2;
   const bool act8 = w_dtype == MOE_FP8_E4M3_ACT8 || x2;  // (E4M3 rows: kind::f8f6f4)
@@ -1554,11 +1556,13 @@ TcPlan tc_plan(int T, int k, int E, int d, int ffn, int num_sms, int w_dtype) {
   const int s_dn_pair = choose_splits(tiles_of(pl.bn_down) * (d / (2 * kBM)), kb_dn_pair, num_sms / 2);
   const bool dn_pair_fits = pl.bn_down == 32 && d % (2 * kBM) == 0;
   const bool dec_pair_dn = dn_pair_fits && (dec_pairs || (pairs_ok && w_dtype == MOE_BF16 && s_dn_pair <= s_dn));
-  const bool dec_pair_gu = dec_pairs && pl.bn_gateup == 32 && ffn % (2 * kBM) == 0;
+  const int s_gu_pair = choose_splits(tiles_of(pl.bn_gateup) * (ffn / (2 * kBM)), (d + 2 * kBK - 1) / (2 * kBK),
+                                      num_sms / 2);
+  const bool dec_pair_gu = pl.bn_gateup == 32 && ffn % (2 * kBM) == 0 &&
+                           (dec_pairs || (pairs_ok && x2 && s_gu_pair == 1 && mean < 128.0));
   pl.splits_down = dec_pair_dn ? s_dn_pair : s_dn;
   pl.splits_gateup = dec_pair_gu
-                         ? choose_splits(tiles_of(pl.bn_gateup) * (ffn / (2 * kBM)), (d + 2 * kBK - 1) / (2 * kBK),
-                                         num_sms / 2)
+                         ? s_gu_pair
                          : choose_splits(tiles_of(pl.bn_gateup) * (ffn / kBM), (d + kw_gu - 1) / kw_gu, num_sms);
   // (no gate/up split for groups of prefill size: their tiles fill the SMs,
   // and a split adds a pass over fp32 partials of every row)
