@@ -1431,8 +1431,15 @@ bool fp8_two_term(int w_dtype) {
 }
 
 bool fp8_two_term_scattered(int w_dtype, const TcPlan& plan) {
-  // (MOE_X2_GATHER=1 keeps gathering the rows at prefill tiles: tuning)
-  return fp8_two_term(w_dtype) && (plan.bn_gateup >= 128 || plan.pair_gateup) && env_int("MOE_X2_GATHER") != 1;
+  if (!fp8_two_term(w_dtype)) return false;
+  // decode tiles on CTA pairs: the rows scattered to their permuted order
+  // and loaded by tiles (the gather4 row copies serve single CTAs here)
+  if (plan.bn_gateup < 128) return plan.pair_gateup != 0;
+  // prefill tiles: gathered per token by the producer warp's row copies
+  // (two lanes per row), which measured faster than writing each token's
+  // two rows to its k permuted rows and loading tiles (DeepSeek-V3-shaped
+  // T=4096: 2.671 -> 2.640 ms); MOE_X2_SCATTER=1 scatters them (tuning)
+  return env_int("MOE_X2_SCATTER") == 1;
 }
 
 namespace {

@@ -599,17 +599,17 @@ def test_layer_gateup_split_k(splits, bn, d, pair, wfmt, monkeypatch):
 
 
 @pytest.mark.parametrize("bn,pair,wfmt", [(bn, pr, w) for bn, pr in ((128, 0), (128, 1), (256, 0), (256, 1))
-                                           for w in ("bf16", "fp8", "fp8gather", "fp8conv", "fp8a8")] +
-                         [(160, pr, w) for pr in (0, 1) for w in ("fp8", "fp8gather")] +
+                                           for w in ("bf16", "fp8", "fp8scatter", "fp8conv", "fp8a8")] +
+                         [(160, pr, w) for pr in (0, 1) for w in ("fp8", "fp8scatter")] +
                          [(bn, 1, "fp8wide") for bn in (128, 160, 256)] + [(128, 1, "fp8narrow")])
 def test_layer_gathered_rows_every_tile(bn, pair, wfmt, monkeypatch):
     # the gate/up GEMM gathers its token rows (cp.async by the producer warp
     # for tiles of >= 128 rows), on single CTAs and on CTA pairs, with groups
     # spanning several tiles and ragged tails.  FP8 weights: the two-term
-    # rows scattered into permuted order (tile loads), or gathered per token
-    # (fp8gather), or the weight converters (fp8conv)
-    if wfmt == "fp8gather":
-        monkeypatch.setenv("MOE_X2_GATHER", "1")
+    # rows gathered per token, or scattered into permuted order (tile loads;
+    # fp8scatter), or the weight converters (fp8conv)
+    if wfmt == "fp8scatter":
+        monkeypatch.setenv("MOE_X2_SCATTER", "1")
         wfmt = "fp8"
     if wfmt in ("fp8wide", "fp8narrow"):  # 256 elements of K per stage in both GEMMs, or in neither
         monkeypatch.setenv("MOE_X2_WIDE", "3" if wfmt == "fp8wide" else "0")
