@@ -149,7 +149,9 @@ typedef struct moe_problem {
  *   p        = softmax(l[t,:]) over all E experts
  *   S_t      = the k experts with the largest l (ties: lower expert index)
  *   w[t,j]   = p[S_t,j] / sum_{e in S_t} p[e]   (== softmax over S_t only)
- * Slots j are in descending weight.
+ * Slots j are in descending weight.  Non-finite logits: infinities order as
+ * numbers, -0 ties +0, and NaN logits rank after every number (among
+ * themselves by expert index).
  *
  *   x            [T, d] act_dtype
  *   w_router     [E, d] act_dtype
