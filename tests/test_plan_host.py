@@ -169,3 +169,18 @@ def test_the_fp32_path_has_no_tiling():
     p = api.problem(64, 128, 256, 8, 2, act="f32", wfmt="f32")
     assert set(api.moe_plan_info_for(p, SMS).values()) == {0}
     assert api.moe_layer_launch_count_for(p, SMS) > 0
+
+
+def test_two_term_token_rows_are_gathered_per_token_at_prefill(monkeypatch):
+    # FP8 weights on bf16 rows at prefill tiles: the token rows are split
+    # once per token (two planes of T rows) and gathered by the gate/up
+    # GEMM; MOE_X2_SCATTER=1 writes them to their T*k permuted rows instead,
+    # which the workspace shows exactly (two planes of codes and one fp32
+    # scale per row)
+    s = _shape("deepseek_v3", 4096, "fp8")
+    p = api.problem_of(s)
+    gathered = api.moe_workspace_size_for(p, SMS)
+    monkeypatch.setenv("MOE_X2_SCATTER", "1")
+    scattered = api.moe_workspace_size_for(p, SMS)
+    R, T = s.T * s.k, s.T
+    assert scattered - gathered == 2 * (R - T) * s.d + 4 * (R - T)
