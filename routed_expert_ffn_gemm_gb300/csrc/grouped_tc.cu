@@ -515,8 +515,11 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
   int n_pre = 0;
   if (early) {
     if (warp == 0 && lane == 0 && u_first < total_units) {
-      const uint64_t pol_w = ptx::policy_evict_first();
       const Unit x = decode_unit(u_first, offs, prefix, G, MT, S, BN);
+      // (the producer's weight policy below: evict-normal when several row
+      // tiles of the expert read the weights)
+      const uint64_t pol_w =
+          prefix[x.g + 1] - prefix[x.g] > 1 ? ptx::policy_evict_normal() : ptx::policy_evict_first();
       const int kb0 = x.ks * kb_per_split, kb1 = min(kblocks, kb0 + kb_per_split);
       const int bhalf = PAIR ? ((x.n_valid + 31) / 32) * 16 : x.n_valid;
       const uint32_t bytes = slot_bytes((bhalf + p.boxn - 1) / p.boxn, 0, false);
@@ -712,7 +715,7 @@ __global__ void __launch_bounds__(Cfg<MODE, BN, WF, PAIR>::THREADS, 1)
           }
           if (lsu) {
             // two lanes per row: of each 32-byte sector of the row's
-            // 128-byte K slice (per 64-element sub-tile) the even lane copies
+            // 128-byte K slice (per 128-byte sub-tile) the even lane copies
             // the first 16 bytes and the odd lane the second, so that one
             // warp instruction asks for 16 whole sectors (one lane per row,
             // each 16-byte copy asking for half a sector, fetched every
